@@ -1,0 +1,502 @@
+// C ABI of libdec.so: validation, workspace plan, handle state, decode graph.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+#include <string>
+#include <vector>
+
+#include "runtime.h"
+
+using namespace dec;
+
+struct dec_handle {
+  Model m;
+  std::vector<LayerPtrs> layers;
+  cudaStream_t stream;
+  int32_t len;          // positions held (host bookkeeping)
+  std::string err;
+  // decode graph, captured for one (logits, d_argmax) pair
+  cudaGraphExec_t graph = nullptr;
+  float* graph_logits = nullptr;
+  int32_t* graph_argmax = nullptr;
+  int graph_timed_pairs = 0;
+  int64_t graph_kernels = 0;
+  int64_t launches = 0;
+  Timing timing;
+  std::vector<cudaEvent_t> events;
+};
+
+static void timing_start(dec_handle* h) { h->timing.n = 0; }
+static void timing_finish(dec_handle* h) { h->timing.n_done = h->timing.n; }
+
+static thread_local std::string g_create_error;
+
+static dec_status fail(dec_handle* h, dec_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (h) h->err = buf;
+  else g_create_error = buf;
+  return st;
+}
+
+static size_t dsize(int32_t dt) { return dt == DEC_BF16 ? 2 : 4; }
+
+static bool validate(const dec_config* c, std::string& why) {
+  char b[256];
+  auto bad = [&](const char* m) { why = m; return false; };
+  if (!c) return bad("config is NULL");
+  if (c->n_layers <= 0 || c->hidden <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 ||
+      c->head_dim <= 0 || c->ffn <= 0 || c->vocab <= 0 || c->max_seq <= 0)
+    return bad("every size must be positive");
+  if (c->n_heads % c->n_kv_heads != 0) return bad("n_heads must be a multiple of n_kv_heads");
+  if (c->head_dim % 2 != 0) return bad("head_dim must be even (RoPE rotates pairs)");
+  if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return bad("rms_eps and rope_theta must be positive");
+  if (c->weight_dtype != DEC_F32 && c->weight_dtype != DEC_BF16) return bad("weight_dtype must be DEC_F32 or DEC_BF16");
+  if (c->kv_dtype != DEC_F32 && c->kv_dtype != DEC_BF16) return bad("kv_dtype must be DEC_F32 or DEC_BF16");
+  if (c->n_experts < 0 || c->n_experts_used < 0) return bad("expert counts must be >= 0");
+  if (c->n_experts == 0 && c->n_experts_used != 0) return bad("n_experts_used must be 0 for a dense FFN");
+  if (c->n_experts > 0 && (c->n_experts_used < 1 || c->n_experts_used > c->n_experts))
+    return bad("experts used must lie in [1, n_experts]");
+  if (c->sliding_window < 0 || c->max_tokens < 0) return bad("sliding_window and max_tokens must be >= 0");
+  if (c->sliding_window > 0 && c->max_seq > c->sliding_window)
+    return bad("under a sliding window max_seq = min(sliding_window, n_ctx) cannot exceed the window");
+  if (c->rope_llama3 && !(c->rope_factor > 0.f && c->rope_low_freq_factor > 0.f &&
+                          c->rope_high_freq_factor > c->rope_low_freq_factor && c->rope_orig_ctx > 0))
+    return bad("llama3 RoPE scaling needs factor > 0, 0 < low < high, orig_ctx > 0");
+  // Limits of this implementation.
+  if (c->head_dim != 16 && c->head_dim != 64 && c->head_dim != 128) return bad("head_dim must be 16, 64 or 128");
+  if (c->n_heads / c->n_kv_heads > MAX_GROUP) return bad("at most 16 query heads per kv head");
+  if (c->n_kv_heads > MAX_KV_HEADS) return bad("at most 192 kv heads");
+  if (c->n_experts > MAX_EXPERTS) return bad("at most 256 experts");
+  if (c->n_experts_used > MAX_EXPERTS_USED) return bad("at most 8 experts per token");
+  const size_t ws = dsize(c->weight_dtype), ks = dsize(c->kv_dtype);
+  if ((c->hidden * ws) % 16 || (c->ffn * ws) % 16 || ((size_t)c->n_heads * c->head_dim * ws) % 16)
+    return bad("hidden, ffn and n_heads*head_dim rows must be whole 16-byte chunks");
+  if ((c->head_dim * ks) % 16) return bad("head_dim rows of the KV cache must be whole 16-byte chunks");
+  const size_t k_slots = c->n_experts ? (size_t)c->n_experts_used : 1;
+  const size_t smem_floats_max = (200 * 1024) / 4 - 64 - MAX_EXPERTS;
+  if ((size_t)c->hidden > smem_floats_max || (size_t)c->n_heads * c->head_dim > smem_floats_max ||
+      k_slots * c->ffn > smem_floats_max) {
+    snprintf(b, sizeof b, "vectors held in shared memory exceed %zu floats", smem_floats_max);
+    return bad(b);
+  }
+  return true;
+}
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+WsPlan dec::plan_workspace(const dec_config& c) {
+  WsPlan p{};
+  const int T = c.max_tokens > 0 ? c.max_tokens : c.max_seq;
+  p.max_tokens = T;
+  const int hd = c.head_dim, qd = c.n_heads * hd, kd = c.n_kv_heads * hd;
+  const int k = c.n_experts ? c.n_experts_used : 1;
+  int nsplit = (c.max_seq + 127) / 128;
+  const int cap = (2 * 152) / c.n_kv_heads;
+  if (nsplit > cap) nsplit = cap;
+  if (nsplit > 64) nsplit = 64;
+  if (nsplit < 1) nsplit = 1;
+  p.nsplit = nsplit;
+  const size_t ws = dsize(c.weight_dtype), ks = dsize(c.kv_dtype);
+  const size_t a_elem = c.weight_dtype == DEC_BF16 ? 2 : 4;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + (bytes ? bytes : 1), 256); return o; };
+  p.st = take(sizeof(DeviceState));
+  p.inv_freq = take(sizeof(double) * (hd / 2));
+  p.rope_tab = take(sizeof(float2) * (size_t)T * (hd / 2));
+  p.x = take(4 * (size_t)c.hidden);
+  p.q = take(4 * (size_t)qd);
+  p.attn = take(4 * (size_t)qd);
+  p.act = take(4 * (size_t)k * c.ffn);
+  p.nbuf = take(4 * (size_t)c.hidden);
+  p.ids = take(4 * (size_t)MAX_EXPERTS_USED);
+  p.wts = take(4 * (size_t)MAX_EXPERTS_USED);
+  p.part = take(4 * (size_t)c.n_heads * nsplit * (hd + 2));
+  p.amax_val = take(4 * (size_t)LM_GRID_MAX);
+  p.amax_idx = take(4 * (size_t)LM_GRID_MAX);
+  p.tokens = take(4 * (size_t)T);
+  size_t amax = c.hidden;
+  if ((size_t)qd > amax) amax = qd;
+  if ((size_t)c.ffn > amax) amax = c.ffn;
+  p.X = take(4 * (size_t)T * c.hidden);
+  p.A = take(a_elem * (size_t)T * amax);
+  p.Q = take(4 * (size_t)T * qd);
+  p.KVlin_k = take(ks * (size_t)(c.max_seq + T) * kd);
+  p.KVlin_v = take(ks * (size_t)(c.max_seq + T) * kd);
+  p.pf_ids = take(4 * (size_t)T * k);
+  p.pf_wts = take(4 * (size_t)T * k);
+  p.pf_count = take(4 * (size_t)(c.n_experts + 1));
+  p.pf_offset = take(4 * (size_t)(c.n_experts + 2));
+  p.pf_rows = take(4 * (size_t)T * k);
+  p.Y = take(c.n_experts ? 4 * (size_t)T * k * c.hidden : 0);
+  p.ACT = take(a_elem * (size_t)T * k * c.ffn);
+  (void)ws;
+  p.kv = off;
+  p.kv_layer_bytes = align_up(ks * (size_t)c.max_seq * kd, 256);
+  off += 2 * p.kv_layer_bytes * c.n_layers;
+  p.total = off;
+  return p;
+}
+
+extern "C" {
+
+dec_status dec_config_validate(const dec_config* cfg, char* msg, size_t msg_len) {
+  std::string why;
+  const bool ok = validate(cfg, why);
+  if (msg && msg_len) {
+    snprintf(msg, msg_len, "%s", ok ? "ok" : why.c_str());
+  }
+  return ok ? DEC_OK : DEC_EINVAL;
+}
+
+size_t dec_workspace_bytes(const dec_config* cfg) {
+  std::string why;
+  if (!validate(cfg, why)) return 0;
+  return plan_workspace(*cfg).total;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspace,
+                      size_t workspace_bytes, void* cuda_stream, dec_handle** out) {
+  std::string why;
+  if (!out) return fail(nullptr, DEC_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (!validate(cfg, why)) return fail(nullptr, DEC_EINVAL, "invalid config: %s", why.c_str());
+  if (!w || !w->tok_embd || !w->out_norm || !w->layers) return fail(nullptr, DEC_EINVAL, "weights missing");
+  if (!cfg->tied_embedding && !w->lm_head) return fail(nullptr, DEC_EINVAL, "untied config needs lm_head");
+  if (!workspace) return fail(nullptr, DEC_EINVAL, "workspace is NULL");
+  if (((uintptr_t)workspace & 255u) != 0) return fail(nullptr, DEC_EINVAL, "workspace must be 256-byte aligned");
+  const WsPlan p = plan_workspace(*cfg);
+  if (workspace_bytes < p.total)
+    return fail(nullptr, DEC_ENOMEM, "workspace has %zu bytes, needs %zu", workspace_bytes, p.total);
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    const dec_layer_weights& L = w->layers[l];
+    if (!L.attn_norm || !L.wqkv || !L.wo || !L.ffn_norm || !L.w_gateup || !L.w_down)
+      return fail(nullptr, DEC_EINVAL, "layer %d: a required weight is NULL", l);
+    if (cfg->qkv_bias && !L.bqkv) return fail(nullptr, DEC_EINVAL, "layer %d: qkv_bias set but bqkv is NULL", l);
+    if (cfg->n_experts > 0 && !L.router) return fail(nullptr, DEC_EINVAL, "layer %d: MoE layer needs router", l);
+    if (!aligned16(L.wqkv) || !aligned16(L.wo) || !aligned16(L.w_gateup) || !aligned16(L.w_down) ||
+        (L.router && !aligned16(L.router)))
+      return fail(nullptr, DEC_EINVAL, "layer %d: weight matrices must be 16-byte aligned", l);
+  }
+  if (!aligned16(w->tok_embd) || (w->lm_head && !aligned16(w->lm_head)))
+    return fail(nullptr, DEC_EINVAL, "embedding / head must be 16-byte aligned");
+
+  dec_handle* h = new (std::nothrow) dec_handle();
+  if (!h) return fail(nullptr, DEC_EINVAL, "out of host memory");
+  h->stream = (cudaStream_t)cuda_stream;
+  h->len = 0;
+  Model& m = h->m;
+  m.cfg = *cfg;
+  if (m.cfg.max_tokens == 0) m.cfg.max_tokens = p.max_tokens;
+  m.ws = workspace;
+  m.ws_bytes = workspace_bytes;
+  m.nsplit = p.nsplit;
+  int lg = (cfg->vocab / 2 + 7) / 8;
+  m.lm_grid = lg < 1 ? 1 : (lg > LM_GRID_MAX ? LM_GRID_MAX : lg);
+  m.tok_embd = w->tok_embd;
+  m.out_norm = (const float*)w->out_norm;
+  m.head = cfg->tied_embedding ? w->tok_embd : w->lm_head;
+  m.trace_ids = nullptr;
+  m.trace_logits = nullptr;
+  m.trace_cap = 1;
+  m.timing = &h->timing;
+  m.launches = &h->launches;
+  char* base = (char*)workspace;
+  Scratch& S = m.s;
+  S.st = (DeviceState*)(base + p.st);
+  S.inv_freq = (double*)(base + p.inv_freq);
+  S.rope_tab = (float2*)(base + p.rope_tab);
+  S.x = (float*)(base + p.x);
+  S.q = (float*)(base + p.q);
+  S.attn = (float*)(base + p.attn);
+  S.act = (float*)(base + p.act);
+  S.nbuf = (float*)(base + p.nbuf);
+  S.ids = (int32_t*)(base + p.ids);
+  S.wts = (float*)(base + p.wts);
+  S.part = (float*)(base + p.part);
+  S.amax_val = (float*)(base + p.amax_val);
+  S.amax_idx = (int32_t*)(base + p.amax_idx);
+  S.tokens = (int32_t*)(base + p.tokens);
+  S.X = (float*)(base + p.X);
+  S.A = base + p.A;
+  S.Q = (float*)(base + p.Q);
+  S.KVlin_k = base + p.KVlin_k;
+  S.KVlin_v = base + p.KVlin_v;
+  S.pf_ids = (int32_t*)(base + p.pf_ids);
+  S.pf_wts = (float*)(base + p.pf_wts);
+  S.pf_count = (int32_t*)(base + p.pf_count);
+  S.pf_offset = (int32_t*)(base + p.pf_offset);
+  S.pf_rows = (int32_t*)(base + p.pf_rows);
+  S.Y = (float*)(base + p.Y);
+  S.ACT = base + p.ACT;
+  h->layers.resize(cfg->n_layers);
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    const dec_layer_weights& L = w->layers[l];
+    LayerPtrs& d = h->layers[l];
+    d.attn_norm = (const float*)L.attn_norm;
+    d.wqkv = L.wqkv;
+    d.bqkv = cfg->qkv_bias ? (const float*)L.bqkv : nullptr;
+    d.wo = L.wo;
+    d.ffn_norm = (const float*)L.ffn_norm;
+    d.w_gateup = L.w_gateup;
+    d.w_down = L.w_down;
+    d.router = cfg->n_experts > 0 ? L.router : nullptr;
+    d.kc = base + p.kv + (size_t)(2 * l) * p.kv_layer_bytes;
+    d.vc = base + p.kv + (size_t)(2 * l + 1) * p.kv_layer_bytes;
+  }
+  m.layers = h->layers.data();
+
+  // RoPE frequencies inv_i = theta^(-2i/hd), llama3-scaled when enabled
+  // (rml "The decoder", Rotary embeddings), computed once in double.
+  std::vector<double> inv(cfg->head_dim / 2);
+  for (int i = 0; i < cfg->head_dim / 2; ++i) {
+    double f = pow((double)cfg->rope_theta, -2.0 * i / cfg->head_dim);
+    if (cfg->rope_llama3) {
+      const double wl = 2.0 * M_PI / f, orig = cfg->rope_orig_ctx;
+      const double lo = cfg->rope_low_freq_factor, hi = cfg->rope_high_freq_factor, fac = cfg->rope_factor;
+      if (wl < orig / hi) {
+      } else if (wl > orig / lo) {
+        f = f / fac;
+      } else {
+        const double sm = (orig / wl - lo) / (hi - lo);
+        f = (1.0 - sm) * f / fac + sm * f;
+      }
+    }
+    inv[i] = f;
+  }
+  cudaError_t e = cudaMemcpy(S.inv_freq, inv.data(), inv.size() * sizeof(double), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(S.st, 0, sizeof(DeviceState));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    delete h;
+    return fail(nullptr, DEC_ECUDA, "CUDA error at create: %s", cudaGetErrorString(e));
+  }
+  *out = h;
+  return DEC_OK;
+}
+
+static dec_status cuda_check(dec_handle* h, const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(h, DEC_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+  return DEC_OK;
+}
+
+// Position rules shared by prefill and decode (rml "The decoder", One forward
+// pass, step 1; Pantheon Sliding Window).
+static dec_status check_positions(dec_handle* h, int32_t n, int32_t start_pos) {
+  const dec_config& c = h->m.cfg;
+  if (n <= 0) return fail(h, DEC_EINVAL, "empty input");
+  if (start_pos < 0 || start_pos > h->len)
+    return fail(h, DEC_EINVAL, "start_pos %d outside [0, %d]", start_pos, h->len);
+  if (c.sliding_window > 0 && c.max_seq == c.sliding_window) {
+    if (h->len > c.max_seq && start_pos < h->len)
+      return fail(h, DEC_EINVAL, "cannot rewind to %d: the ring has overwritten positions below %d",
+                  start_pos, h->len - c.max_seq);
+  } else if ((int64_t)start_pos + n > c.max_seq) {
+    return fail(h, DEC_ERANGE, "cache full: start_pos %d + n %d > max_seq %d", start_pos, n, c.max_seq);
+  }
+  return DEC_OK;
+}
+
+dec_status dec_prefill(dec_handle* h, const int32_t* tokens, int32_t n, int32_t start_pos, float* logits,
+                       int32_t* d_argmax) {
+  if (!h) return DEC_EINVAL;
+  if (!tokens && n > 0) return fail(h, DEC_EINVAL, "tokens is NULL");
+  dec_status st = check_positions(h, n, start_pos);
+  if (st != DEC_OK) return st;
+  for (int32_t i = 0; i < n; ++i)
+    if (tokens[i] < 0 || tokens[i] >= h->m.cfg.vocab)
+      return fail(h, DEC_EINVAL, "token %d at index %d outside [0, %d)", tokens[i], i, h->m.cfg.vocab);
+  const int T = h->m.cfg.max_tokens;
+  timing_start(h);
+  for (int32_t done = 0; done < n; done += T) {
+    const int chunk = (n - done) < T ? (n - done) : T;
+    cudaError_t e = cudaMemcpyAsync(h->m.s.tokens, tokens + done, sizeof(int32_t) * chunk,
+                                    cudaMemcpyHostToDevice, h->stream);
+    if (e != cudaSuccess) return fail(h, DEC_ECUDA, "token copy: %s", cudaGetErrorString(e));
+    const bool last = done + chunk == n;
+    launch_prefill_chunk(h->m, h->stream, chunk, start_pos + done, last ? logits : nullptr,
+                         last ? d_argmax : nullptr);
+    st = cuda_check(h, "prefill launch");
+    if (st != DEC_OK) return st;
+  }
+  timing_finish(h);
+  h->len = start_pos + n;
+  return DEC_OK;
+}
+
+static dec_status run_decode_body(dec_handle* h, float* logits, int32_t* d_argmax) {
+  if (h->stream == nullptr) {
+    timing_start(h);
+    launch_decode_body(h->m, h->stream, logits, d_argmax);
+    timing_finish(h);
+    return cuda_check(h, "decode launch");
+  }
+  if (!h->graph || h->graph_logits != logits || h->graph_argmax != d_argmax) {
+    if (h->graph) {
+      cudaGraphExecDestroy(h->graph);
+      h->graph = nullptr;
+    }
+    cudaGraph_t g;
+    cudaError_t e = cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeRelaxed);
+    if (e != cudaSuccess) return fail(h, DEC_ECUDA, "begin capture: %s", cudaGetErrorString(e));
+    timing_start(h);
+    const int64_t before = h->launches;
+    launch_decode_body(h->m, h->stream, logits, d_argmax);
+    h->graph_kernels = h->launches - before;
+    h->launches = before;
+    h->graph_timed_pairs = h->timing.n;
+    e = cudaStreamEndCapture(h->stream, &g);
+    if (e != cudaSuccess) return fail(h, DEC_ECUDA, "end capture: %s", cudaGetErrorString(e));
+    e = cudaGraphInstantiate(&h->graph, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return fail(h, DEC_ECUDA, "graph instantiate: %s", cudaGetErrorString(e));
+    h->graph_logits = logits;
+    h->graph_argmax = d_argmax;
+  }
+  cudaError_t e = cudaGraphLaunch(h->graph, h->stream);
+  if (e != cudaSuccess) return fail(h, DEC_ECUDA, "graph launch: %s", cudaGetErrorString(e));
+  h->timing.n = h->graph_timed_pairs;
+  h->launches += h->graph_kernels;
+  timing_finish(h);
+  return DEC_OK;
+}
+
+dec_status dec_decode(dec_handle* h, int32_t token, int32_t pos, float* logits) {
+  if (!h) return DEC_EINVAL;
+  dec_status st = check_positions(h, 1, pos);
+  if (st != DEC_OK) return st;
+  if (token < 0 || token >= h->m.cfg.vocab)
+    return fail(h, DEC_EINVAL, "token %d outside [0, %d)", token, h->m.cfg.vocab);
+  launch_set_step(h->m, h->stream, nullptr, token, pos);
+  st = cuda_check(h, "decode launch");
+  if (st != DEC_OK) return st;
+  st = run_decode_body(h, logits, nullptr);
+  if (st != DEC_OK) return st;
+  h->len = pos + 1;
+  return DEC_OK;
+}
+
+dec_status dec_decode_dev(dec_handle* h, const int32_t* d_token, int32_t pos, float* logits,
+                          int32_t* d_argmax) {
+  if (!h) return DEC_EINVAL;
+  if (!d_token) return fail(h, DEC_EINVAL, "d_token is NULL");
+  dec_status st = check_positions(h, 1, pos);
+  if (st != DEC_OK) return st;
+  launch_set_step(h->m, h->stream, d_token, 0, pos);
+  st = cuda_check(h, "decode launch");
+  if (st != DEC_OK) return st;
+  st = run_decode_body(h, logits, d_argmax);
+  if (st != DEC_OK) return st;
+  h->len = pos + 1;
+  return DEC_OK;
+}
+
+dec_status dec_kv_reset(dec_handle* h) {
+  if (!h) return DEC_EINVAL;
+  h->len = 0;
+  return DEC_OK;
+}
+
+int32_t dec_length(const dec_handle* h) { return h ? h->len : -1; }
+
+int64_t dec_launch_count(const dec_handle* h) { return h ? h->launches : -1; }
+
+dec_status dec_kv_layer(const dec_handle* h, int32_t layer, void** k, void** v) {
+  if (!h || !k || !v || layer < 0 || layer >= h->m.cfg.n_layers) return DEC_EINVAL;
+  *k = h->m.layers[layer].kc;
+  *v = h->m.layers[layer].vc;
+  return DEC_OK;
+}
+
+dec_status dec_set_trace(dec_handle* h, int32_t* d_ids, float* d_logits, int32_t capacity) {
+  if (!h) return DEC_EINVAL;
+  if ((d_ids == nullptr) != (d_logits == nullptr)) return fail(h, DEC_EINVAL, "pass both trace buffers or neither");
+  if (d_ids && capacity <= 0) return fail(h, DEC_EINVAL, "trace capacity must be positive");
+  h->m.trace_ids = d_ids;
+  h->m.trace_logits = d_logits;
+  h->m.trace_cap = d_ids ? capacity : 1;
+  if (h->graph) {  // the captured graph holds the old trace pointers
+    cudaGraphExecDestroy(h->graph);
+    h->graph = nullptr;
+  }
+  return DEC_OK;
+}
+
+dec_status dec_check(dec_handle* h) {
+  if (!h) return DEC_EINVAL;
+  cudaError_t e = cudaStreamSynchronize(h->stream);
+  if (e != cudaSuccess) return fail(h, DEC_ECUDA, "stream: %s", cudaGetErrorString(e));
+  unsigned words[2];
+  e = cudaMemcpy(words, &h->m.s.st->err, sizeof words, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(h, DEC_ECUDA, "state read: %s", cudaGetErrorString(e));
+  if (words[0]) {
+    cudaMemset(&h->m.s.st->err, 0, sizeof words);
+    if (words[0] & ERR_TIMEOUT)
+      return fail(h, DEC_ETIMEOUT, "a bounded device wait timed out (site %u)", words[1]);
+    return fail(h, DEC_EINVAL, "a device-side token was outside [0, vocab)");
+  }
+  return DEC_OK;
+}
+
+dec_status dec_timing_enable(dec_handle* h, int32_t kernel_class, int32_t max_launches) {
+  if (!h) return DEC_EINVAL;
+  if (kernel_class < 0 || max_launches < 0) return fail(h, DEC_EINVAL, "bad timing arguments");
+  cudaError_t e = cudaStreamSynchronize(h->stream);
+  if (e != cudaSuccess) return fail(h, DEC_ECUDA, "stream: %s", cudaGetErrorString(e));
+  for (cudaEvent_t ev : h->events) cudaEventDestroy(ev);
+  h->events.clear();
+  h->timing = Timing();
+  if (kernel_class > 0 && max_launches > 0) {
+    h->events.resize(2 * (size_t)max_launches);
+    for (auto& ev : h->events) {
+      e = cudaEventCreate(&ev);
+      if (e != cudaSuccess) return fail(h, DEC_ECUDA, "event create: %s", cudaGetErrorString(e));
+    }
+    h->timing.cls = kernel_class;
+    h->timing.max = max_launches;
+    h->timing.ev = h->events.data();
+  }
+  if (h->graph) {
+    cudaGraphExecDestroy(h->graph);
+    h->graph = nullptr;
+  }
+  return DEC_OK;
+}
+
+dec_status dec_timing_read(dec_handle* h, float* total_ms, int32_t* launches) {
+  if (!h || !total_ms || !launches) return DEC_EINVAL;
+  float tot = 0.f;
+  const int n = h->timing.n_done;
+  for (int i = 0; i < n; ++i) {
+    cudaError_t e = cudaEventSynchronize(h->timing.ev[2 * i + 1]);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, h->timing.ev[2 * i], h->timing.ev[2 * i + 1]);
+    if (e != cudaSuccess) return fail(h, DEC_ECUDA, "event read: %s", cudaGetErrorString(e));
+    tot += ms;
+  }
+  *total_ms = tot;
+  *launches = n;
+  return DEC_OK;
+}
+
+void dec_destroy(dec_handle* h) {
+  if (!h) return;
+  if (h->graph) cudaGraphExecDestroy(h->graph);
+  for (cudaEvent_t ev : h->events) cudaEventDestroy(ev);
+  delete h;
+}
+
+const char* dec_last_error(const dec_handle* h) {
+  return h ? h->err.c_str() : g_create_error.c_str();
+}
+
+}  // extern "C"

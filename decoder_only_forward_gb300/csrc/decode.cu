@@ -1,0 +1,640 @@
+// Decode (one position) kernels: bandwidth-bound fused GEMVs, split-K
+// flash-decode GQA attention, MoE router/top-k and expert GEMVs, LM head with
+// device argmax.  Weights stream once per step with 16-byte loads; every dot
+// product is one warp over the K dimension with fp32 accumulation.
+#include <math.h>
+
+#include "runtime.h"
+
+namespace dec {
+
+constexpr int GEMV_THREADS = 256;
+constexpr int GEMV_WARPS = GEMV_THREADS / 32;
+
+// ---------------------------------------------------------------------------
+// Block-level helpers
+
+// xs[k] = x[k] / sqrt(mean(x^2) + eps) * w[k]   (Pantheon RMSNorm)
+__device__ void block_rmsnorm_to_smem(const float* __restrict__ x, const float* __restrict__ w,
+                                      int K, float eps, float* xs, float* red) {
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    float v = x[k];
+    xs[k] = v;
+    ss = fmaf(v, v, ss);
+  }
+  ss = warp_sum(ss);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  if (warp == 0) {
+    float v = lane < nwarps ? red[lane] : 0.f;
+    v = warp_sum(v);
+    if (lane == 0) red[32] = v;
+  }
+  __syncthreads();
+  const float inv = 1.0f / sqrtf(red[32] / (float)K + eps);
+  for (int k = threadIdx.x; k < K; k += blockDim.x) xs[k] = xs[k] * inv * w[k];
+  __syncthreads();
+}
+
+__device__ void block_copy_to_smem(const float* __restrict__ x, int K, float* xs) {
+  for (int k = threadIdx.x; k < K; k += blockDim.x) xs[k] = x[k];
+  __syncthreads();
+}
+
+// Dot products of two weight rows with the smem vector xs, one warp; the
+// sums end up in every lane.  K * sizeof(W) is a multiple of 16 bytes.
+template <typename W>
+__device__ __forceinline__ void warp_dot2(const W* __restrict__ r0, const W* __restrict__ r1,
+                                          const float* __restrict__ xs, int K, float& s0, float& s1) {
+  constexpr int V = Chunk<W>::N;
+  const int nch = K / V;
+  const int lane = threadIdx.x & 31;
+  float a0 = 0.f, a1 = 0.f;
+  int c = lane;
+  for (; c + 96 < nch; c += 128) {
+    uint4 u0[4], u1[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      u0[i] = ld_stream16(r0 + (size_t)(c + 32 * i) * V);
+      u1[i] = ld_stream16(r1 + (size_t)(c + 32 * i) * V);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float w0[V], w1[V];
+      Chunk<W>::widen(u0[i], w0);
+      Chunk<W>::widen(u1[i], w1);
+      const float* xv = xs + (c + 32 * i) * V;
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        a0 = fmaf(w0[e], xv[e], a0);
+        a1 = fmaf(w1[e], xv[e], a1);
+      }
+    }
+  }
+  for (; c < nch; c += 32) {
+    uint4 u0 = ld_stream16(r0 + (size_t)c * V);
+    uint4 u1 = ld_stream16(r1 + (size_t)c * V);
+    float w0[V], w1[V];
+    Chunk<W>::widen(u0, w0);
+    Chunk<W>::widen(u1, w1);
+    const float* xv = xs + c * V;
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      a0 = fmaf(w0[e], xv[e], a0);
+      a1 = fmaf(w1[e], xv[e], a1);
+    }
+  }
+  s0 = warp_sum(a0);
+  s1 = warp_sum(a1);
+}
+
+// ---------------------------------------------------------------------------
+// Step setup: position, token, RoPE (cos, sin) of this position.
+
+__global__ void k_set_step(DeviceState* st, const int32_t* d_token, int32_t token, int32_t pos,
+                           int32_t vocab, const double* __restrict__ inv_freq, int half,
+                           float2* __restrict__ rope_tab) {
+  if (threadIdx.x == 0) {
+    int t = d_token ? *d_token : token;
+    if (t < 0 || t >= vocab) {
+      raise_error(st, ERR_TOKEN, 0);
+      t = 0;
+    }
+    st->token = t;
+    st->pos = pos;
+  }
+  for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    double sn, cs;
+    sincos((double)pos * inv_freq[i], &sn, &cs);
+    rope_tab[i] = make_float2((float)cs, (float)sn);
+  }
+}
+
+template <typename W>
+__global__ void k_embed_step(const W* __restrict__ E, int h, const DeviceState* __restrict__ st,
+                             float* __restrict__ x) {
+  const W* row = E + (size_t)st->token * h;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < h; i += gridDim.x * blockDim.x)
+    x[i] = to_f32(row[i]);
+}
+
+// ---------------------------------------------------------------------------
+// Fused RMSNorm -> [q;k;v] = Wqkv n (+b) -> RoPE on q,k -> K/V written at the
+// slot of pos.  A warp owns rows (2i, 2i+1), so the rotation of the pair is
+// done in the epilogue (sipllm adjacent-pair RoPE).
+
+template <typename W, typename KV>
+__global__ void __launch_bounds__(GEMV_THREADS) k_norm_qkv(
+    const float* __restrict__ x, const float* __restrict__ nw, float eps,
+    const W* __restrict__ wqkv, const float* __restrict__ bqkv, int K, int qd, int kd, int hd,
+    const float2* __restrict__ rope_tab, const DeviceState* __restrict__ st, int max_seq,
+    int sliding, float* __restrict__ q_out, KV* __restrict__ kc, KV* __restrict__ vc) {
+  extern __shared__ float sm[];
+  float* red = sm;
+  float* xs = sm + 64;
+  block_rmsnorm_to_smem(x, nw, K, eps, xs, red);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int npairs = (qd + 2 * kd) / 2;
+  const int pos = st->pos;
+  const int slot = sliding > 0 ? pos % max_seq : pos;
+  for (int p = blockIdx.x * GEMV_WARPS + warp; p < npairs; p += gridDim.x * GEMV_WARPS) {
+    const int r = 2 * p;
+    float a0, a1;
+    warp_dot2(wqkv + (size_t)r * K, wqkv + (size_t)(r + 1) * K, xs, K, a0, a1);
+    if (lane == 0) {
+      if (bqkv) {
+        a0 += bqkv[r];
+        a1 += bqkv[r + 1];
+      }
+      if (r < qd + kd) {
+        const int d = (r < qd ? r : r - qd) % hd;
+        const float2 cs = rope_tab[d >> 1];
+        const float b0 = a0 * cs.x - a1 * cs.y;
+        const float b1 = a0 * cs.y + a1 * cs.x;
+        a0 = b0;
+        a1 = b1;
+      }
+      if (r < qd) {
+        q_out[r] = a0;
+        q_out[r + 1] = a1;
+      } else if (r < qd + kd) {
+        const size_t o = (size_t)slot * kd + (r - qd);
+        kc[o] = from_f32<KV>(a0);
+        kc[o + 1] = from_f32<KV>(a1);
+      } else {
+        const size_t o = (size_t)slot * kd + (r - qd - kd);
+        vc[o] = from_f32<KV>(a0);
+        vc[o + 1] = from_f32<KV>(a1);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Fused RMSNorm (or a given normalised vector) -> act = silu(Wg n) * (Wu n).
+// Dense: one matrix [2f, K] with gate row r at 2r and up row r at 2r+1.
+// MoE: slot s uses expert ids[s] of the merged [E, 2f, K] tensor; act is [k][f].
+
+template <typename W>
+__global__ void __launch_bounds__(GEMV_THREADS) k_gateup(
+    const float* __restrict__ x, const float* __restrict__ nw, float eps,
+    const float* __restrict__ nvec, const W* __restrict__ wgu, int K, int f,
+    const int32_t* __restrict__ ids, int nslots, float* __restrict__ act) {
+  extern __shared__ float sm[];
+  float* red = sm;
+  float* xs = sm + 64;
+  if (nvec) block_copy_to_smem(nvec, K, xs);
+  else block_rmsnorm_to_smem(x, nw, K, eps, xs, red);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ntask = nslots * f;
+  for (int p = blockIdx.x * GEMV_WARPS + warp; p < ntask; p += gridDim.x * GEMV_WARPS) {
+    const int slot = p / f, j = p - slot * f;
+    const size_t e = ids ? (size_t)ids[slot] : 0;
+    const W* base = wgu + e * (size_t)2 * f * K + (size_t)2 * j * K;
+    float g, u;
+    warp_dot2(base, base + K, xs, K, g, u);
+    if (lane == 0) act[(size_t)slot * f + j] = silu_f(g) * u;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// x[r] += sum_s wt_s * (W_s[r] . v_s)  -- output projection (one slot, weight 1)
+// and dense / MoE down projection.  Slots are summed in selection order.
+
+template <typename W>
+__global__ void __launch_bounds__(GEMV_THREADS) k_gemv_accum(
+    const float* __restrict__ v, const W* __restrict__ w, int N, int K,
+    const int32_t* __restrict__ ids, const float* __restrict__ wts, int nslots,
+    float* __restrict__ x) {
+  extern __shared__ float sm[];
+  float* xs = sm + 64;
+  block_copy_to_smem(v, K * nslots, xs);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int npairs = (N + 1) / 2;
+  for (int p = blockIdx.x * GEMV_WARPS + warp; p < npairs; p += gridDim.x * GEMV_WARPS) {
+    const int r0 = 2 * p;
+    const int r1 = min(r0 + 1, N - 1);
+    float o0 = 0.f, o1 = 0.f;
+    for (int s = 0; s < nslots; ++s) {
+      const size_t e = ids ? (size_t)ids[s] : 0;
+      const W* base = w + e * (size_t)N * K;
+      float a0, a1;
+      warp_dot2(base + (size_t)r0 * K, base + (size_t)r1 * K, xs + (size_t)s * K, K, a0, a1);
+      const float ws = wts ? wts[s] : 1.0f;
+      o0 = fmaf(ws, a0, o0);
+      o1 = fmaf(ws, a1, o1);
+    }
+    if (lane == 0) {
+      x[r0] += o0;
+      if (r1 != r0) x[r1] += o1;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// MoE router: RMSNorm -> logits = Wr n -> top-k by repeated selection (ties to
+// the lower id) -> weights renormalised over the selection (Pantheon Mixture
+// of Experts; rml Mixture of experts).  The softmax denominator over all
+// experts cancels in the renormalisation, so weights are
+// exp(l_e - M) / sum_sel exp(l_s - M).  One CTA.
+
+template <typename W>
+__global__ void __launch_bounds__(GEMV_THREADS) k_moe_router(
+    const float* __restrict__ x, const float* __restrict__ nw, float eps,
+    const W* __restrict__ router, int K, int E, int k, float* __restrict__ nvec,
+    int32_t* __restrict__ ids, float* __restrict__ wts, const DeviceState* __restrict__ st,
+    int32_t* __restrict__ trace_ids, float* __restrict__ trace_logits, int trace_cap, int layer) {
+  extern __shared__ float sm[];
+  float* red = sm;
+  float* logits = sm + 64;               // [E] (E <= 256 -> fits in the 64+256 header)
+  float* xs = sm + 64 + MAX_EXPERTS;
+  block_rmsnorm_to_smem(x, nw, K, eps, xs, red);
+  for (int i = threadIdx.x; i < K; i += blockDim.x) nvec[i] = xs[i];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = warp; e < E; e += GEMV_WARPS) {
+    float a, b;
+    const W* row = router + (size_t)e * K;
+    warp_dot2(row, row, xs, K, a, b);
+    if (lane == 0) logits[e] = a;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int sel[MAX_EXPERTS_USED];
+    float mx = -INFINITY;
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e) {
+        bool taken = false;
+        for (int t = 0; t < j; ++t) taken |= (sel[t] == e);
+        if (taken) continue;
+        if (best < 0 || logits[e] > logits[best]) best = e;
+      }
+      sel[j] = best;
+      mx = fmaxf(mx, logits[best]);
+    }
+    float p[MAX_EXPERTS_USED], tot = 0.f;
+    for (int j = 0; j < k; ++j) {
+      p[j] = expf(logits[sel[j]] - mx);
+      tot += p[j];
+    }
+    for (int j = 0; j < k; ++j) {
+      ids[j] = sel[j];
+      wts[j] = p[j] / tot;
+    }
+    if (trace_ids) {
+      const size_t row = (size_t)layer * trace_cap + (st->pos % trace_cap);
+      for (int j = 0; j < k; ++j) trace_ids[row * k + j] = sel[j];
+      for (int e = 0; e < E; ++e) trace_logits[row * E + e] = logits[e];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Split-K flash-decode: CTA (g, split) handles the G query heads of kv head g
+// over a contiguous share of the readable slots, with a one-pass online
+// softmax (rml Attend).  The last CTA of a kv head merges the partial
+// (max, sum, output) triples in split order.  Key order does not change the
+// softmax, so slots are visited in slot order; the readable count is
+// min(pos+1, max_seq) under a window (Pantheon Sliding Window), else pos+1.
+
+constexpr int FD_THREADS = 128;
+constexpr int FD_TILE = 32;
+
+template <typename KV, int HD>
+__global__ void __launch_bounds__(FD_THREADS) k_flash_decode(
+    const float* __restrict__ q, const KV* __restrict__ kc, const KV* __restrict__ vc, int nq,
+    int nkv, int max_seq, int sliding, DeviceState* __restrict__ st, float* __restrict__ part,
+    float* __restrict__ out) {
+  constexpr int OUTS = (MAX_GROUP * HD + FD_THREADS - 1) / FD_THREADS;
+  __shared__ float qs[MAX_GROUP][HD];
+  __shared__ float ks[FD_TILE][HD + 1];
+  __shared__ __align__(16) float vs[FD_TILE][HD];
+  __shared__ float ps[MAX_GROUP][FD_TILE];
+  __shared__ float mrow[MAX_GROUP], lrow[MAX_GROUP], alpha[MAX_GROUP];
+  __shared__ int is_last;
+
+  const int g = blockIdx.x, split = blockIdx.y, nsplit = gridDim.y;
+  const int G = nq / nkv;
+  const int kd = nkv * HD;
+  const int pos = st->pos;
+  const int m = sliding > 0 ? min(pos + 1, max_seq) : pos + 1;
+  const int per = (m + nsplit - 1) / nsplit;
+  const int j0 = split * per, j1 = min(m, j0 + per);
+  const float scale = 1.0f / sqrtf((float)HD);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  for (int i = tid; i < G * HD; i += FD_THREADS) qs[i / HD][i % HD] = q[(size_t)g * G * HD + i] * scale;
+  if (tid < MAX_GROUP) {
+    mrow[tid] = -INFINITY;
+    lrow[tid] = 0.f;
+  }
+  float acc[OUTS];
+#pragma unroll
+  for (int r = 0; r < OUTS; ++r) acc[r] = 0.f;
+
+  constexpr int CV = 16 / sizeof(KV);  // elements per 16-byte chunk
+  for (int t0 = j0; t0 < j1; t0 += FD_TILE) {
+    const int nt = min(FD_TILE, j1 - t0);
+    __syncthreads();
+    for (int i = tid; i < nt * (HD / CV); i += FD_THREADS) {
+      const int row = i / (HD / CV), c = i % (HD / CV);
+      const size_t off = (size_t)(t0 + row) * kd + (size_t)g * HD + c * CV;
+      float kf[CV], vf[CV];
+      Chunk<KV>::widen(*reinterpret_cast<const uint4*>(kc + off), kf);
+      Chunk<KV>::widen(*reinterpret_cast<const uint4*>(vc + off), vf);
+#pragma unroll
+      for (int e = 0; e < CV; ++e) {
+        ks[row][c * CV + e] = kf[e];
+        vs[row][c * CV + e] = vf[e];
+      }
+    }
+    __syncthreads();
+    for (int hh = warp; hh < G; hh += FD_THREADS / 32) {
+      float s = -INFINITY;
+      if (lane < nt) {
+        s = 0.f;
+#pragma unroll 8
+        for (int d = 0; d < HD; ++d) s = fmaf(qs[hh][d], ks[lane][d], s);
+      }
+      const float mnew = fmaxf(mrow[hh], warp_max(s));
+      const float p = lane < nt ? __expf(s - mnew) : 0.f;
+      const float psum = warp_sum(p);
+      ps[hh][lane] = p;
+      __syncwarp();
+      if (lane == 0) {
+        const float a = __expf(mrow[hh] - mnew);
+        alpha[hh] = a;
+        lrow[hh] = lrow[hh] * a + psum;
+        mrow[hh] = mnew;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < OUTS; ++r) {
+      const int idx = tid + r * FD_THREADS;
+      if (idx < G * HD) {
+        const int hh = idx / HD, d = idx % HD;
+        float o = acc[r] * alpha[hh];
+        for (int j = 0; j < nt; ++j) o = fmaf(ps[hh][j], vs[j][d], o);
+        acc[r] = o;
+      }
+    }
+  }
+  __syncthreads();
+
+  if (nsplit == 1) {
+#pragma unroll
+    for (int r = 0; r < OUTS; ++r) {
+      const int idx = tid + r * FD_THREADS;
+      if (idx < G * HD) out[(size_t)g * G * HD + idx] = acc[r] / lrow[idx / HD];
+    }
+    return;
+  }
+  // Partials: part[(h * nsplit + split) * (HD + 2) + {0..HD-1: o, HD: max, HD+1: sum}]
+#pragma unroll
+  for (int r = 0; r < OUTS; ++r) {
+    const int idx = tid + r * FD_THREADS;
+    if (idx < G * HD) {
+      const int hh = idx / HD, d = idx % HD;
+      part[((size_t)(g * G + hh) * nsplit + split) * (HD + 2) + d] = acc[r];
+    }
+  }
+  if (tid < G) {
+    float* pp = part + ((size_t)(g * G + tid) * nsplit + split) * (HD + 2);
+    pp[HD] = mrow[tid];
+    pp[HD + 1] = lrow[tid];
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned prev = atomicAdd(&st->counters[CNT_ATTN + g], 1u);
+    is_last = (prev == (unsigned)nsplit - 1);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  for (int idx = tid; idx < G * HD; idx += FD_THREADS) {
+    const int hh = idx / HD, d = idx % HD;
+    const float* base = part + (size_t)(g * G + hh) * nsplit * (HD + 2);
+    float M = -INFINITY;
+    for (int s2 = 0; s2 < nsplit; ++s2) M = fmaxf(M, __ldcg(base + s2 * (HD + 2) + HD));
+    float L = 0.f, o = 0.f;
+    for (int s2 = 0; s2 < nsplit; ++s2) {
+      const float* pp = base + s2 * (HD + 2);
+      const float ms = __ldcg(pp + HD);
+      if (ms == -INFINITY) continue;
+      const float sc = __expf(ms - M);
+      L = fmaf(__ldcg(pp + HD + 1), sc, L);
+      o = fmaf(__ldcg(pp + d), sc, o);
+    }
+    out[(size_t)(g * G + hh) * HD + d] = o / L;
+  }
+  if (tid == 0) st->counters[CNT_ATTN + g] = 0u;
+}
+
+// ---------------------------------------------------------------------------
+// Final RMSNorm -> logits = W_out n (fp32), with an optional device argmax:
+// per-CTA (value, index) partials, merged by the last CTA (ties -> lower id).
+
+template <typename W>
+__global__ void __launch_bounds__(GEMV_THREADS) k_norm_lmhead(
+    const float* __restrict__ x, const float* __restrict__ nw, float eps,
+    const W* __restrict__ head, int K, int V, float* __restrict__ logits,
+    int32_t* __restrict__ d_argmax, float* __restrict__ pval, int32_t* __restrict__ pidx,
+    DeviceState* __restrict__ st) {
+  extern __shared__ float sm[];
+  float* red = sm;
+  float* xs = sm + 64;
+  __shared__ float wbest[GEMV_WARPS];
+  __shared__ int wbidx[GEMV_WARPS];
+  __shared__ int is_last;
+  block_rmsnorm_to_smem(x, nw, K, eps, xs, red);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int npairs = (V + 1) / 2;
+  float best = -INFINITY;
+  int bidx = 0x7fffffff;
+  for (int p = blockIdx.x * GEMV_WARPS + warp; p < npairs; p += gridDim.x * GEMV_WARPS) {
+    const int r0 = 2 * p, r1 = min(r0 + 1, V - 1);
+    float a0, a1;
+    warp_dot2(head + (size_t)r0 * K, head + (size_t)r1 * K, xs, K, a0, a1);
+    if (lane == 0) {
+      if (logits) {
+        logits[r0] = a0;
+        if (r1 != r0) logits[r1] = a1;
+      }
+      if (a0 > best || (a0 == best && r0 < bidx)) { best = a0; bidx = r0; }
+      if (a1 > best || (a1 == best && r1 < bidx)) { best = a1; bidx = r1; }
+    }
+  }
+  if (!d_argmax) return;
+  if (lane == 0) {
+    wbest[warp] = best;
+    wbidx[warp] = bidx;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = wbest[0];
+    int bi = wbidx[0];
+    for (int w = 1; w < GEMV_WARPS; ++w)
+      if (wbest[w] > b || (wbest[w] == b && wbidx[w] < bi)) { b = wbest[w]; bi = wbidx[w]; }
+    pval[blockIdx.x] = b;
+    pidx[blockIdx.x] = bi;
+    __threadfence();
+    const unsigned prev = atomicAdd(&st->counters[CNT_ARGMAX], 1u);
+    is_last = (prev == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (is_last && threadIdx.x == 0) {
+    __threadfence();
+    float b = __ldcg(pval);
+    int bi = __ldcg(pidx);
+    for (int i = 1; i < (int)gridDim.x; ++i) {
+      const float v = __ldcg(pval + i);
+      const int vi = __ldcg(pidx + i);
+      if (v > b || (v == b && vi < bi)) { b = v; bi = vi; }
+    }
+    *d_argmax = bi;
+    st->counters[CNT_ARGMAX] = 0u;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers
+
+static inline int gemv_grid(int tasks) {
+  int g = (tasks + GEMV_WARPS - 1) / GEMV_WARPS;
+  return g < 1 ? 1 : (g > 152 * 8 ? 152 * 8 : g);
+}
+
+template <typename F>
+static void set_smem(F* kern, size_t bytes) {
+  if (bytes > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+void launch_set_step(const Model& m, cudaStream_t s, const int32_t* d_token, int32_t token, int32_t pos) {
+  k_set_step<<<1, 128, 0, s>>>(m.s.st, d_token, token, pos, m.cfg.vocab, m.s.inv_freq,
+                               m.cfg.head_dim / 2, m.s.rope_tab);
+  count_launch(m);
+}
+
+template <typename W, typename KV>
+static void decode_body(const Model& m, cudaStream_t s, float* logits, int32_t* d_argmax) {
+  const dec_config& c = m.cfg;
+  const int h = c.hidden, hd = c.head_dim, qd = c.n_heads * hd, kd = c.n_kv_heads * hd;
+  const Scratch& S = m.s;
+  k_embed_step<W><<<(h + 255) / 256, 256, 0, s>>>((const W*)m.tok_embd, h, S.st, S.x);
+  count_launch(m);
+  const size_t sm_h = (64 + MAX_EXPERTS + (size_t)h) * sizeof(float);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerPtrs& L = m.layers[l];
+    {
+      auto kern = k_norm_qkv<W, KV>;
+      set_smem(kern, sm_h);
+      timer_begin(m, DEC_K_QKV, s);
+      kern<<<gemv_grid((qd + 2 * kd) / 2), GEMV_THREADS, sm_h, s>>>(
+          S.x, L.attn_norm, c.rms_eps, (const W*)L.wqkv, L.bqkv, h, qd, kd, hd, S.rope_tab, S.st,
+          c.max_seq, c.sliding_window, S.q, (KV*)L.kc, (KV*)L.vc);
+      timer_end(m, DEC_K_QKV, s);
+      count_launch(m);
+    }
+    {
+      dim3 grid(c.n_kv_heads, m.nsplit);
+      timer_begin(m, DEC_K_ATTN, s);
+      if (hd == 64)
+        k_flash_decode<KV, 64><<<grid, FD_THREADS, 0, s>>>(S.q, (const KV*)L.kc, (const KV*)L.vc,
+            c.n_heads, c.n_kv_heads, c.max_seq, c.sliding_window, S.st, S.part, S.attn);
+      else if (hd == 128)
+        k_flash_decode<KV, 128><<<grid, FD_THREADS, 0, s>>>(S.q, (const KV*)L.kc, (const KV*)L.vc,
+            c.n_heads, c.n_kv_heads, c.max_seq, c.sliding_window, S.st, S.part, S.attn);
+      else
+        k_flash_decode<KV, 16><<<grid, FD_THREADS, 0, s>>>(S.q, (const KV*)L.kc, (const KV*)L.vc,
+            c.n_heads, c.n_kv_heads, c.max_seq, c.sliding_window, S.st, S.part, S.attn);
+      timer_end(m, DEC_K_ATTN, s);
+      count_launch(m);
+    }
+    {
+      const size_t smb = (64 + (size_t)qd) * sizeof(float);
+      auto kern = k_gemv_accum<W>;
+      set_smem(kern, smb);
+      timer_begin(m, DEC_K_OPROJ, s);
+      kern<<<gemv_grid((h + 1) / 2), GEMV_THREADS, smb, s>>>(S.attn, (const W*)L.wo, h, qd, nullptr,
+                                                            nullptr, 1, S.x);
+      timer_end(m, DEC_K_OPROJ, s);
+      count_launch(m);
+    }
+    const int f = c.ffn;
+    if (c.n_experts > 0) {
+      const int k = c.n_experts_used;
+      {
+        auto kern = k_moe_router<W>;
+        set_smem(kern, sm_h);
+        timer_begin(m, DEC_K_ROUTER, s);
+        kern<<<1, GEMV_THREADS, sm_h, s>>>(S.x, L.ffn_norm, c.rms_eps, (const W*)L.router, h,
+                                           c.n_experts, k, S.nbuf, S.ids, S.wts, S.st, m.trace_ids,
+                                           m.trace_logits, m.trace_cap, l);
+        timer_end(m, DEC_K_ROUTER, s);
+        count_launch(m);
+      }
+      {
+        auto kern = k_gateup<W>;
+        set_smem(kern, sm_h);
+        timer_begin(m, DEC_K_GATEUP, s);
+        kern<<<gemv_grid(k * f), GEMV_THREADS, sm_h, s>>>(nullptr, nullptr, 0.f, S.nbuf,
+            (const W*)L.w_gateup, h, f, S.ids, k, S.act);
+        timer_end(m, DEC_K_GATEUP, s);
+        count_launch(m);
+      }
+      {
+        const size_t smb = (64 + (size_t)k * f) * sizeof(float);
+        auto kern = k_gemv_accum<W>;
+        set_smem(kern, smb);
+        timer_begin(m, DEC_K_DOWN, s);
+        kern<<<gemv_grid((h + 1) / 2), GEMV_THREADS, smb, s>>>(S.act, (const W*)L.w_down, h, f,
+                                                              S.ids, S.wts, k, S.x);
+        timer_end(m, DEC_K_DOWN, s);
+        count_launch(m);
+      }
+    } else {
+      {
+        auto kern = k_gateup<W>;
+        set_smem(kern, sm_h);
+        timer_begin(m, DEC_K_GATEUP, s);
+        kern<<<gemv_grid(f), GEMV_THREADS, sm_h, s>>>(S.x, L.ffn_norm, c.rms_eps, nullptr,
+            (const W*)L.w_gateup, h, f, nullptr, 1, S.act);
+        timer_end(m, DEC_K_GATEUP, s);
+        count_launch(m);
+      }
+      {
+        const size_t smb = (64 + (size_t)f) * sizeof(float);
+        auto kern = k_gemv_accum<W>;
+        set_smem(kern, smb);
+        timer_begin(m, DEC_K_DOWN, s);
+        kern<<<gemv_grid((h + 1) / 2), GEMV_THREADS, smb, s>>>(S.act, (const W*)L.w_down, h, f,
+                                                              nullptr, nullptr, 1, S.x);
+        timer_end(m, DEC_K_DOWN, s);
+        count_launch(m);
+      }
+    }
+  }
+  if (logits || d_argmax) {
+    auto kern = k_norm_lmhead<W>;
+    set_smem(kern, sm_h);
+    timer_begin(m, DEC_K_LMHEAD, s);
+    kern<<<m.lm_grid, GEMV_THREADS, sm_h, s>>>(S.x, m.out_norm, c.rms_eps, (const W*)m.head, h,
+                                              c.vocab, logits, d_argmax, S.amax_val, S.amax_idx, S.st);
+    timer_end(m, DEC_K_LMHEAD, s);
+    count_launch(m);
+  }
+}
+
+void launch_decode_body(const Model& m, cudaStream_t s, float* logits, int32_t* d_argmax) {
+  const bool wb = m.cfg.weight_dtype == DEC_BF16, kb = m.cfg.kv_dtype == DEC_BF16;
+  if (wb && kb) decode_body<__nv_bfloat16, __nv_bfloat16>(m, s, logits, d_argmax);
+  else if (wb) decode_body<__nv_bfloat16, float>(m, s, logits, d_argmax);
+  else if (kb) decode_body<float, __nv_bfloat16>(m, s, logits, d_argmax);
+  else decode_body<float, float>(m, s, logits, d_argmax);
+}
+
+}  // namespace dec

@@ -1,0 +1,130 @@
+// Internal interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/dec.h"
+#include "common.cuh"
+
+namespace dec {
+
+struct LayerPtrs {
+  const float* attn_norm;
+  const void* wqkv;
+  const float* bqkv;   // nullable
+  const void* wo;
+  const float* ffn_norm;
+  const void* w_gateup;
+  const void* w_down;
+  const void* router;  // nullable (dense)
+  void* kc;            // this layer's K ring [max_seq][n_kv*hd]
+  void* vc;            // this layer's V ring
+};
+
+// Device scratch carved out of the caller's workspace (see plan_workspace).
+struct Scratch {
+  DeviceState* st;
+  double* inv_freq;     // [hd/2] RoPE frequencies (llama3-scaled if enabled)
+  float2* rope_tab;     // [max(1,max_tokens)][hd/2] (cos, sin) per position of the current call
+  float* x;             // [h] decode residual
+  float* q;             // [nq*hd]
+  float* attn;          // [nq*hd]
+  float* act;           // [k_slots*ffn]
+  float* nbuf;          // [h] normalised FFN input (MoE)
+  int32_t* ids;         // [k] selected experts (decode)
+  float* wts;           // [k]
+  float* part;          // [nq][nsplit][hd+2] split-K partials
+  float* amax_val;      // [LM_GRID_MAX]
+  int32_t* amax_idx;    // [LM_GRID_MAX]
+  int32_t* tokens;      // [max_tokens] prefill token ids on the device
+  // prefill buffers (rows = max_tokens)
+  float* X;             // [T][h] residual rows
+  void* A;              // [T][max(h, nq*hd, ffn)] GEMM A operand (bf16, or f32 for f32 weights)
+  float* Q;             // [T][nq*hd] rotated queries
+  void* KVlin_k;        // [max_seq + T][n_kv*hd] linear K for a wrapping append (kv dtype)
+  void* KVlin_v;
+  int32_t* pf_ids;      // [T][k] routing per row
+  float* pf_wts;        // [T][k]
+  int32_t* pf_count;    // [E] rows per expert
+  int32_t* pf_offset;   // [E+1]
+  int32_t* pf_rows;     // [T*k] (row*k + slot) grouped by expert
+  float* Y;             // [T*k][h] per-(row, slot) expert outputs (MoE)
+  void* ACT;            // [T*k][ffn] gate/up output rows (A operand of down)
+};
+
+constexpr int LM_GRID_MAX = 1024;
+constexpr int MAX_EXPERTS = 256;
+constexpr int MAX_EXPERTS_USED = 8;
+constexpr int MAX_KV_HEADS = 192;
+constexpr int MAX_GROUP = 16;     // query heads per kv head
+constexpr int NUM_COUNTERS = 256;
+
+// Optional CUDA-event pairs recorded around every launch of one kernel class
+// (dec_timing_enable); also captured into the decode graph.
+struct Timing {
+  int cls = 0;
+  int max = 0;
+  int n = 0;              // pairs recorded by the current call
+  int n_done = 0;         // pairs recorded by the last completed call
+  cudaEvent_t* ev = nullptr;
+};
+
+struct Model {
+  dec_config cfg;
+  Timing* timing;       // nullable
+  int64_t* launches;    // host counter of kernel launches
+  LayerPtrs* layers;    // host array [n_layers]
+  const void* tok_embd;
+  const float* out_norm;
+  const void* head;     // tok_embd when tied
+  Scratch s;
+  int nsplit;           // split-K CTAs per kv head in decode attention
+  int lm_grid;          // CTAs of the LM head kernel
+  int32_t* trace_ids;   // nullable
+  float* trace_logits;  // nullable
+  int trace_cap;
+  void* ws;             // workspace base
+  size_t ws_bytes;
+};
+
+// Workspace plan: byte offsets of every region; total size.
+struct WsPlan {
+  size_t st, inv_freq, rope_tab, x, q, attn, act, nbuf, ids, wts, part, amax_val, amax_idx, tokens;
+  size_t X, A, Q, KVlin_k, KVlin_v, pf_ids, pf_wts, pf_count, pf_offset, pf_rows, Y, ACT;
+  size_t kv;            // start of the KV rings
+  size_t kv_layer_bytes;
+  size_t total;
+  int nsplit;
+  int max_tokens;
+};
+
+WsPlan plan_workspace(const dec_config& c);
+
+inline void timer_begin(const Model& m, int cls, cudaStream_t s) {
+  Timing* t = m.timing;
+  if (t && t->cls == cls && t->n < t->max) cudaEventRecord(t->ev[2 * t->n], s);
+}
+inline void timer_end(const Model& m, int cls, cudaStream_t s) {
+  Timing* t = m.timing;
+  if (t && t->cls == cls && t->n < t->max) {
+    cudaEventRecord(t->ev[2 * t->n + 1], s);
+    ++t->n;
+  }
+}
+
+// decode.cu
+void launch_set_step(const Model& m, cudaStream_t s, const int32_t* d_token, int32_t token, int32_t pos);
+void launch_decode_body(const Model& m, cudaStream_t s, float* logits, int32_t* d_argmax);
+
+// prefill.cu
+// Runs tokens (already in m.s.tokens[0..n)) at positions start..start+n-1; writes
+// the last row's logits when logits != nullptr.  wrap_mode: K/V go through the
+// linear scratch and are committed afterwards (needed once the ring may wrap).
+void launch_prefill_chunk(const Model& m, cudaStream_t s, int n, int start, float* logits,
+                          int32_t* d_argmax);
+
+inline void count_launch(const Model& m, int n = 1) { *m.launches += n; }
+
+}  // namespace dec

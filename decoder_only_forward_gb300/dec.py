@@ -1,0 +1,287 @@
+"""ctypes binding of libdec.so (declared in include/dec.h): argument marshalling only.
+
+Every step of the forward pass runs in the library's CUDA kernels; this module
+moves pointers and sizes across the C ABI and owns the torch tensors (device
+memory, streams) the library is given.  Importing it raises if the library has
+not been built: there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import synthetic
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdec.so")
+
+DEC_OK, DEC_EINVAL, DEC_ERANGE, DEC_ECUDA, DEC_ETIMEOUT, DEC_ENOMEM = range(6)
+DEC_F32, DEC_BF16 = 0, 1
+STATUS_NAMES = {0: "DEC_OK", 1: "DEC_EINVAL", 2: "DEC_ERANGE", 3: "DEC_ECUDA", 4: "DEC_ETIMEOUT", 5: "DEC_ENOMEM"}
+
+EXPORTED = ["dec_config_validate", "dec_workspace_bytes", "dec_create", "dec_prefill", "dec_decode",
+            "dec_decode_dev", "dec_kv_reset", "dec_length", "dec_kv_layer", "dec_set_trace",
+            "dec_check", "dec_timing_enable", "dec_timing_read", "dec_launch_count", "dec_destroy",
+            "dec_last_error"]
+
+KERNEL_CLASSES = {"qkv": 1, "attn": 2, "oproj": 3, "gateup": 4, "down": 5, "lmhead": 6, "router": 7,
+                  "pf_gemm": 8, "pf_attn": 9}
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "n_layers", "hidden", "n_heads", "n_kv_heads", "head_dim", "ffn", "vocab", "n_experts",
+        "n_experts_used", "max_seq", "sliding_window", "max_tokens", "tied_embedding", "qkv_bias",
+        "weight_dtype", "kv_dtype")] + [
+        ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("rope_llama3", ctypes.c_int32),
+        ("rope_factor", ctypes.c_float), ("rope_low_freq_factor", ctypes.c_float),
+        ("rope_high_freq_factor", ctypes.c_float), ("rope_orig_ctx", ctypes.c_int32)]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("attn_norm", "wqkv", "bqkv", "wo", "ffn_norm", "w_gateup", "w_down", "router")]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("tok_embd", ctypes.c_void_p), ("out_norm", ctypes.c_void_p),
+                ("lm_head", ctypes.c_void_p), ("layers", ctypes.POINTER(LayerWeights))]
+
+
+def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with decoder_only_forward_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    sig = {
+        "dec_config_validate": (I32, [ctypes.POINTER(Config), ctypes.c_char_p, SZ]),
+        "dec_workspace_bytes": (SZ, [ctypes.POINTER(Config)]),
+        "dec_create": (I32, [ctypes.POINTER(Config), ctypes.POINTER(Weights), P, SZ, P, ctypes.POINTER(P)]),
+        "dec_prefill": (I32, [P, ctypes.POINTER(I32), I32, I32, P, P]),
+        "dec_launch_count": (ctypes.c_int64, [P]),
+        "dec_decode": (I32, [P, I32, I32, P]),
+        "dec_decode_dev": (I32, [P, P, I32, P, P]),
+        "dec_kv_reset": (I32, [P]),
+        "dec_length": (I32, [P]),
+        "dec_kv_layer": (I32, [P, I32, ctypes.POINTER(P), ctypes.POINTER(P)]),
+        "dec_set_trace": (I32, [P, P, P, I32]),
+        "dec_check": (I32, [P]),
+        "dec_timing_enable": (I32, [P, I32, I32]),
+        "dec_timing_read": (I32, [P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(I32)]),
+        "dec_destroy": (None, [P]),
+        "dec_last_error": (ctypes.c_char_p, [P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = load_library()
+
+
+class DecError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+def make_config(w: dict, kv_dtype: str = "f32", max_tokens: int = 0) -> Config:
+    c = Config()
+    for k in ("n_layers", "hidden", "n_heads", "n_kv_heads", "head_dim", "ffn", "vocab",
+              "n_experts", "n_experts_used", "max_seq", "sliding_window"):
+        setattr(c, k, int(w[k]))
+    c.max_tokens = int(max_tokens)
+    c.tied_embedding = int(bool(w["tied"]))
+    c.qkv_bias = int(bool(w["qkv_bias"]))
+    c.weight_dtype = DEC_F32 if w["dtype"] == "f32" else DEC_BF16
+    c.kv_dtype = DEC_F32 if kv_dtype == "f32" else DEC_BF16
+    c.rms_eps = float(w["rms_eps"])
+    c.rope_theta = float(w["rope_theta"])
+    l3 = w.get("rope_llama3")
+    if l3:
+        c.rope_llama3 = 1
+        c.rope_factor = l3["factor"]
+        c.rope_low_freq_factor = l3["low_freq_factor"]
+        c.rope_high_freq_factor = l3["high_freq_factor"]
+        c.rope_orig_ctx = int(l3["orig_ctx"])
+    return c
+
+
+def validate(c: Config) -> tuple:
+    buf = ctypes.create_string_buffer(256)
+    st = lib.dec_config_validate(ctypes.byref(c), buf, 256)
+    return st, buf.value.decode()
+
+
+def workspace_bytes(c: Config) -> int:
+    return int(lib.dec_workspace_bytes(ctypes.byref(c)))
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+class DeviceWeights:
+    """Synthetic weights drawn straight into the library's device layouts.
+
+    Layout only (no arithmetic): [Wq;Wk;Wv] rows concatenated, gate/up rows
+    interleaved per output, experts stacked.
+    """
+
+    def __init__(self, w: dict, device="cuda", seed: int = 1234):
+        self.w = w
+        dt = synthetic.storage_dtype(w)
+        h, f = w["hidden"], w["ffn"]
+        qd, kd = w["n_heads"] * w["head_dim"], w["n_kv_heads"] * w["head_dim"]
+        E = w["n_experts"]
+        d = lambda role, l=-1, e=-1, out=None: synthetic.draw(w, role, l, e, seed, device, out)
+        self.tok_embd = d("tok_embd")
+        self.out_norm = d("out_norm")
+        self.lm_head = None if w["tied"] else d("lm_head")
+        self.layers = []
+        for l in range(w["n_layers"]):
+            L = {"attn_norm": d("attn_norm", l), "ffn_norm": d("ffn_norm", l), "wo": d("wo", l)}
+            wqkv = torch.empty((qd + 2 * kd, h), dtype=dt, device=device)
+            d("wq", l, out=wqkv[:qd])
+            d("wk", l, out=wqkv[qd:qd + kd])
+            d("wv", l, out=wqkv[qd + kd:])
+            L["wqkv"] = wqkv
+            L["bqkv"] = torch.cat([d("bq", l), d("bk", l), d("bv", l)]) if w["qkv_bias"] else None
+            if E:
+                L["router"] = d("router", l)
+                gu = torch.empty((E, 2 * f, h), dtype=dt, device=device)
+                dn = torch.empty((E, h, f), dtype=dt, device=device)
+                for e in range(E):
+                    v = gu[e].view(f, 2, h)
+                    d("w_gate", l, e, out=v[:, 0, :])
+                    d("w_up", l, e, out=v[:, 1, :])
+                    d("w_down", l, e, out=dn[e])
+                L["w_gateup"], L["w_down"] = gu, dn
+            else:
+                L["router"] = None
+                gu = torch.empty((2 * f, h), dtype=dt, device=device)
+                v = gu.view(f, 2, h)
+                d("w_gate", l, out=v[:, 0, :])
+                d("w_up", l, out=v[:, 1, :])
+                L["w_gateup"], L["w_down"] = gu, d("w_down", l)
+            self.layers.append(L)
+        self._c_layers = (LayerWeights * w["n_layers"])()
+        for i, L in enumerate(self.layers):
+            for k in ("attn_norm", "wqkv", "bqkv", "wo", "ffn_norm", "w_gateup", "w_down", "router"):
+                setattr(self._c_layers[i], k, _ptr(L[k]))
+        self.c = Weights(self.tok_embd.data_ptr(), self.out_norm.data_ptr(), _ptr(self.lm_head),
+                         ctypes.cast(self._c_layers, ctypes.POINTER(LayerWeights)))
+
+    def nbytes(self) -> int:
+        t = [self.tok_embd, self.out_norm, self.lm_head]
+        for L in self.layers:
+            t += list(L.values())
+        return sum(x.numel() * x.element_size() for x in t if x is not None)
+
+
+class Decoder:
+    """A handle of the library: weights, workspace (KV cache + scratch) and a stream."""
+
+    def __init__(self, w: dict, weights: Optional[DeviceWeights] = None, device="cuda", seed: int = 1234,
+                 kv_dtype: str = "f32", max_tokens: int = 0, stream: Optional[torch.cuda.Stream] = None):
+        self.w = w
+        self.device = torch.device(device)
+        self.weights = weights if weights is not None else DeviceWeights(w, device, seed)
+        self.cfg = make_config(w, kv_dtype, max_tokens)
+        st, msg = validate(self.cfg)
+        if st != DEC_OK:
+            raise DecError(st, msg)
+        self.ws_bytes = workspace_bytes(self.cfg)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        self.stream = stream if stream is not None else torch.cuda.Stream(device=self.device)
+        self.kv_torch_dtype = torch.float32 if kv_dtype == "f32" else torch.bfloat16
+        h = ctypes.c_void_p()
+        st = lib.dec_create(ctypes.byref(self.cfg), ctypes.byref(self.weights.c), self.workspace.data_ptr(),
+                            self.ws_bytes, ctypes.c_void_p(self.stream.cuda_stream), ctypes.byref(h))
+        if st != DEC_OK:
+            raise DecError(st, lib.dec_last_error(None).decode())
+        self.h = h
+
+    # -- calls -------------------------------------------------------------------
+    def _raise(self, st: int):
+        if st != DEC_OK:
+            raise DecError(st, lib.dec_last_error(self.h).decode())
+
+    def prefill(self, tokens, start_pos: int, logits: Optional[torch.Tensor],
+                d_argmax: Optional[torch.Tensor] = None) -> None:
+        """``tokens``: a host sequence of ids, or a pinned host int32 tensor (copied as is)."""
+        if isinstance(tokens, torch.Tensor):
+            assert tokens.device.type == "cpu" and tokens.dtype == torch.int32 and tokens.is_contiguous()
+            p, n = ctypes.cast(tokens.data_ptr(), ctypes.POINTER(ctypes.c_int32)), tokens.numel()
+        else:
+            a = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+            p, n = a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), a.size
+        self._raise(lib.dec_prefill(self.h, p, int(n), int(start_pos), _ptr(logits), _ptr(d_argmax)))
+
+    @property
+    def launch_count(self) -> int:
+        return int(lib.dec_launch_count(self.h))
+
+    def decode(self, token: int, pos: int, logits: Optional[torch.Tensor]) -> None:
+        self._raise(lib.dec_decode(self.h, int(token), int(pos), _ptr(logits)))
+
+    def decode_dev(self, d_token: torch.Tensor, pos: int, logits: Optional[torch.Tensor],
+                   d_argmax: Optional[torch.Tensor] = None) -> None:
+        self._raise(lib.dec_decode_dev(self.h, d_token.data_ptr(), int(pos), _ptr(logits), _ptr(d_argmax)))
+
+    def kv_reset(self) -> None:
+        self._raise(lib.dec_kv_reset(self.h))
+
+    @property
+    def length(self) -> int:
+        return int(lib.dec_length(self.h))
+
+    def kv_layer(self, layer: int):
+        """(K, V) rings of a layer as [max_seq, n_kv_heads, head_dim] views of the workspace."""
+        k, v = ctypes.c_void_p(), ctypes.c_void_p()
+        self._raise(lib.dec_kv_layer(self.h, int(layer), ctypes.byref(k), ctypes.byref(v)))
+        base = self.workspace.data_ptr()
+        es = 4 if self.kv_torch_dtype == torch.float32 else 2
+        n = self.w["max_seq"] * self.w["n_kv_heads"] * self.w["head_dim"]
+        views = []
+        for p in (k.value, v.value):
+            off = p - base
+            views.append(self.workspace[off:off + n * es].view(self.kv_torch_dtype)
+                         .view(self.w["max_seq"], self.w["n_kv_heads"], self.w["head_dim"]))
+        return views[0], views[1]
+
+    def set_trace(self, ids: Optional[torch.Tensor], logits: Optional[torch.Tensor], capacity: int) -> None:
+        self._raise(lib.dec_set_trace(self.h, _ptr(ids), _ptr(logits), int(capacity)))
+
+    def check(self) -> None:
+        self._raise(lib.dec_check(self.h))
+
+    def timing_enable(self, kernel_class: str, max_launches: int) -> None:
+        cls = KERNEL_CLASSES.get(kernel_class, 0) if isinstance(kernel_class, str) else int(kernel_class)
+        self._raise(lib.dec_timing_enable(self.h, cls, int(max_launches)))
+
+    def timing_read(self) -> tuple:
+        """(summed milliseconds, launches) of the timed kernel class in the most recent call."""
+        ms, n = ctypes.c_float(), ctypes.c_int32()
+        self._raise(lib.dec_timing_read(self.h, ctypes.byref(ms), ctypes.byref(n)))
+        return float(ms.value), int(n.value)
+
+    def synchronize(self) -> None:
+        self.stream.synchronize()
+
+    def close(self) -> None:
+        if getattr(self, "h", None):
+            lib.dec_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

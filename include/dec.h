@@ -1,0 +1,211 @@
+/*
+ * dec.h -- C ABI of libdec.so: the decoder-only transformer forward pass over a
+ * KV cache (single-pass prefill and one-token decode) on one NVIDIA GB300.
+ *
+ * What is computed, per layer, pre-norm (Pantheon "Llama Forward Pass",
+ * Forward Pass Flow; rml "The decoder", One forward pass):
+ *   RMSNorm -> Q/K/V projection (+ optional q/k/v bias) -> adjacent-pair RoPE
+ *   (sipllm "Transformer forward pass", RoPE is adjacent-pair; optional llama3
+ *   frequency scaling, rml Rotary embeddings) -> K/V written at pos (a circular
+ *   buffer under a sliding window, Pantheon Sliding Window) -> causal GQA
+ *   attention, query head h reading kv head h*n_kv/n_head (Pantheon Grouped
+ *   Query Attention; rml Attend) -> output projection + residual -> RMSNorm ->
+ *   SwiGLU FFN or router softmax / top-k / renormalise / weighted expert sum
+ *   (Pantheon Mixture of Experts) + residual; then final RMSNorm and LM head.
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" are CUDA device addresses on the handle's device;
+ *     "host" are ordinary host addresses.  Nothing here takes torch types.
+ *   - Ownership: the caller owns the weights, the workspace and every output
+ *     buffer; the library never allocates device memory and never frees caller
+ *     memory.  Weights and workspace must outlive the handle.
+ *   - Work is enqueued on the handle's stream and the call returns; outputs are
+ *     valid once that stream has been synchronised.
+ *   - Argument errors are detected on the host before anything is enqueued or
+ *     any state changes (rml "The decoder", One forward pass, step 1: "in every
+ *     case nothing has changed yet").
+ *   - Matrices are row-major [out, in] (each output's weights contiguous).
+ */
+#ifndef DEC_H
+#define DEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dec_status {
+  DEC_OK = 0,
+  DEC_EINVAL = 1,   /* bad argument: empty input, token outside [0,vocab), NULL, bad config, bad position */
+  DEC_ERANGE = 2,   /* the cache is full (no sliding window and start_pos + n > max_seq) */
+  DEC_ECUDA = 3,    /* a CUDA call failed; dec_last_error() has the CUDA message */
+  DEC_ETIMEOUT = 4, /* a bounded device wait gave up; the kernel returned without finishing */
+  DEC_ENOMEM = 5    /* the workspace is smaller than dec_workspace_bytes() */
+} dec_status;
+
+typedef enum dec_dtype { DEC_F32 = 0, DEC_BF16 = 1 } dec_dtype;
+
+/*
+ * Model configuration: sizes plus switches (rml "The decoder", The model
+ * config).  Fixed layout with no build-dependent fields (Pantheon ABI note).
+ */
+typedef struct dec_config {
+  int32_t n_layers;
+  int32_t hidden;         /* h */
+  int32_t n_heads;        /* query heads */
+  int32_t n_kv_heads;     /* n_heads % n_kv_heads == 0 */
+  int32_t head_dim;       /* even (RoPE rotates pairs) */
+  int32_t ffn;            /* SwiGLU inner size (per expert for MoE) */
+  int32_t vocab;
+  int32_t n_experts;      /* 0 = dense FFN */
+  int32_t n_experts_used; /* top-k, 1 <= k <= n_experts (0 when dense) */
+  int32_t max_seq;        /* KV slots per layer; = min(sliding_window, n_ctx) under a window */
+  int32_t sliding_window; /* 0 = full causal; else window W (W positions including the query) */
+  int32_t max_tokens;     /* largest n of one dec_prefill call the workspace holds (0 = max_seq);
+                             longer calls are processed in chunks of max_tokens */
+  int32_t tied_embedding; /* 1: LM head = token embedding matrix */
+  int32_t qkv_bias;       /* 1: bqkv present */
+  int32_t weight_dtype;   /* DEC_F32 or DEC_BF16: projection, embedding, router, head matrices */
+  int32_t kv_dtype;       /* DEC_F32 or DEC_BF16: KV cache storage */
+  float rms_eps;
+  float rope_theta;
+  int32_t rope_llama3;    /* 1: llama3 frequency scaling with the four fields below */
+  float rope_factor;
+  float rope_low_freq_factor;
+  float rope_high_freq_factor;
+  int32_t rope_orig_ctx;
+} dec_config;
+
+/*
+ * Per-layer weight views (device).  Norm weights and biases are f32; the
+ * matrices are weight_dtype.  Layouts:
+ *   attn_norm, ffn_norm [hidden]
+ *   wqkv      [(n_heads + 2*n_kv_heads)*head_dim, hidden]: rows Wq, then Wk, then Wv
+ *   bqkv      [(n_heads + 2*n_kv_heads)*head_dim] or NULL (no bias)
+ *   wo        [hidden, n_heads*head_dim]
+ *   w_gateup  dense: [2*ffn, hidden] with gate row r at 2r and up row r at 2r+1;
+ *             MoE:   [n_experts, 2*ffn, hidden], each expert interleaved the same way
+ *   w_down    dense: [hidden, ffn];  MoE: [n_experts, hidden, ffn]
+ *   router    MoE only: [n_experts, hidden]; NULL when dense
+ */
+typedef struct dec_layer_weights {
+  const void *attn_norm, *wqkv, *bqkv, *wo, *ffn_norm, *w_gateup, *w_down, *router;
+} dec_layer_weights;
+
+typedef struct dec_weights {
+  const void *tok_embd;             /* [vocab, hidden] weight_dtype, device */
+  const void *out_norm;             /* [hidden] f32, device */
+  const void *lm_head;              /* [vocab, hidden] weight_dtype, device; NULL when tied */
+  const dec_layer_weights *layers;  /* host array of n_layers entries (copied by dec_create) */
+} dec_weights;
+
+typedef struct dec_handle dec_handle;
+
+/* Checks a configuration (rml "The decoder", ValidateConfig: positive sizes,
+ * heads split evenly into kv groups, even head_dim, positive eps/theta/scales,
+ * 1 <= experts used <= experts) plus this library's limits.  Host only, needs
+ * no GPU.  Writes a message into msg (may be NULL).  Returns DEC_OK or DEC_EINVAL. */
+dec_status dec_config_validate(const dec_config *cfg, char *msg, size_t msg_len);
+
+/* Bytes of device workspace dec_create needs for cfg (KV cache plus all
+ * scratch).  0 if cfg is invalid.  Host only. */
+size_t dec_workspace_bytes(const dec_config *cfg);
+
+/* Creates a handle.  workspace: device, >= dec_workspace_bytes(cfg) bytes,
+ * 256-byte aligned, owned by the caller.  cuda_stream: a cudaStream_t (NULL =
+ * legacy default stream).  Weights are validated for presence and 16-byte
+ * alignment.  Errors: DEC_EINVAL (config, NULL or misaligned pointers),
+ * DEC_ENOMEM (workspace too small), DEC_ECUDA. */
+dec_status dec_create(const dec_config *cfg, const dec_weights *weights, void *workspace,
+                      size_t workspace_bytes, void *cuda_stream, dec_handle **out);
+
+/* Single-pass prefill (sipllm "Transformer forward pass", Single-pass prefill;
+ * rml Forward with n tokens): runs tokens[0..n) at positions start_pos.. through
+ * every layer, each layer once for all positions, writes their K/V, and writes
+ * the LAST position's logits.
+ *   tokens: host, n ids in [0, vocab).  logits: device, [vocab] f32 (may be NULL
+ *   to skip the head).  d_argmax: device int32 or NULL; when given, receives
+ *   argmax(logits) (ties -> lower id), the first greedy token.
+ *   start_pos <= current length; start_pos < length drops the later history.
+ *   Under a sliding window, once positions have wrapped the ring, start_pos must
+ *   equal the length (a rewind would need overwritten slots).
+ * Errors: DEC_EINVAL (n <= 0, bad token, bad start_pos), DEC_ERANGE (no window
+ * and start_pos + n > max_seq), DEC_ECUDA. */
+dec_status dec_prefill(dec_handle *h, const int32_t *tokens, int32_t n, int32_t start_pos,
+                       float *logits, int32_t *d_argmax);
+
+/* One-token decode (sipllm Transformer::forward(token, pos)): identical in
+ * meaning to dec_prefill(&token, 1, pos, logits), run with the decode kernels.
+ * logits: device [vocab] f32. */
+dec_status dec_decode(dec_handle *h, int32_t token, int32_t pos, float *logits);
+
+/* Decode step whose token is read from device memory (greedy loops without a
+ * host round trip).  d_token: device int32.  d_argmax: device int32 or NULL;
+ * when given, receives argmax(logits) (ties -> lower id).  A token outside
+ * [0, vocab) read from d_token is replaced by 0 and reported as DEC_EINVAL by
+ * dec_check(). */
+dec_status dec_decode_dev(dec_handle *h, const int32_t *d_token, int32_t pos, float *logits,
+                          int32_t *d_argmax);
+
+/* Empties the cache (length 0).  Slots are not cleared: the readable length
+ * gates every read. */
+dec_status dec_kv_reset(dec_handle *h);
+
+/* Number of positions currently in the cache (host-side bookkeeping). */
+int32_t dec_length(const dec_handle *h);
+
+/* Device pointers to layer's K and V rings, each [max_seq][n_kv_heads][head_dim]
+ * of kv_dtype; position p lives in slot p % max_seq under a window, else slot p. */
+dec_status dec_kv_layer(const dec_handle *h, int32_t layer, void **k, void **v);
+
+/* Optional MoE trace for testing: when d_ids/d_logits are non-NULL, every
+ * later MoE layer records, for position p, its selected expert ids
+ * (d_ids[(layer*capacity + p % capacity)*n_experts_used + j]) and router logits
+ * (d_logits[(layer*capacity + p % capacity)*n_experts + e]).  Pass NULLs to stop.
+ * Buffers are device memory owned by the caller. */
+dec_status dec_set_trace(dec_handle *h, int32_t *d_ids, float *d_logits, int32_t capacity);
+
+/* Number of kernels this handle has launched so far (graph launches count
+ * every kernel node), for measurement. */
+int64_t dec_launch_count(const dec_handle *h);
+
+/* Synchronises the handle's stream and reports device-side errors raised since
+ * the last check: DEC_ETIMEOUT (a bounded wait gave up), DEC_EINVAL (a device
+ * token out of range), DEC_ECUDA. */
+dec_status dec_check(dec_handle *h);
+
+/* Kernel classes for dec_timing_enable. */
+typedef enum dec_kernel_class {
+  DEC_K_NONE = 0,
+  DEC_K_QKV = 1,      /* decode: RMSNorm -> QKV GEMV -> RoPE -> KV write */
+  DEC_K_ATTN = 2,     /* decode: split-K flash-decode attention */
+  DEC_K_OPROJ = 3,    /* decode: output projection + residual */
+  DEC_K_GATEUP = 4,   /* decode: RMSNorm -> gate/up GEMV -> silu(g)*u (dense or experts) */
+  DEC_K_DOWN = 5,     /* decode: down projection (+ expert combine) + residual */
+  DEC_K_LMHEAD = 6,   /* decode/prefill: final RMSNorm -> LM head (+ argmax) */
+  DEC_K_ROUTER = 7,   /* decode: MoE router + top-k */
+  DEC_K_PF_GEMM = 8,  /* prefill: projection GEMMs */
+  DEC_K_PF_ATTN = 9   /* prefill: causal attention */
+} dec_kernel_class;
+
+/* Measurement hook: from the next call on, a CUDA event pair is recorded on
+ * the handle's stream around each launch of kernel_class (at most
+ * max_launches per call; the decode graph is re-captured to include them).
+ * kernel_class 0 turns it off.  The library creates and owns the events. */
+dec_status dec_timing_enable(dec_handle *h, int32_t kernel_class, int32_t max_launches);
+
+/* Waits for the most recent call's events and returns the summed duration in
+ * milliseconds and the number of timed launches of that call. */
+dec_status dec_timing_read(dec_handle *h, float *total_ms, int32_t *launches);
+
+void dec_destroy(dec_handle *h);
+
+/* Message of the last error on h (or of the last failed dec_create when h is NULL). */
+const char *dec_last_error(const dec_handle *h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DEC_H */

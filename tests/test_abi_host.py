@@ -1,0 +1,113 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared
+symbol, its structs match the header, and configuration validation behaves.
+No GPU is touched (no compute call is made)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from decoder_only_forward_gb300 import build as dec_build
+from decoder_only_forward_gb300 import synthetic
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dec.h")
+
+
+@pytest.fixture(scope="module")
+def dec():
+    dec_build.build()
+    from decoder_only_forward_gb300 import dec as d
+    return d
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dec_[a-z_]+)\s*\(", text)))
+
+
+def test_header_functions_all_exported(dec):
+    declared = _declared_functions()
+    assert len(declared) >= 15
+    lib = ctypes.CDLL(dec._LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in dec.h but not exported"
+    assert sorted(dec.EXPORTED) == declared
+
+
+def test_config_struct_matches_header(dec):
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct dec_config \{(.*?)\} dec_config;", text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"\b(int32_t|float)\s+([a-z_0-9]+)\s*;", body)
+    assert [n for _, n in fields] == [n for n, _ in dec.Config._fields_]
+    for (ty, n), (cn, ct) in zip(fields, dec.Config._fields_):
+        assert (ct is ctypes.c_float) == (ty == "float"), n
+    assert ctypes.sizeof(dec.Config) == 4 * len(fields)
+
+
+@pytest.mark.parametrize("name", sorted(synthetic.WORKLOADS))
+def test_workloads_validate(dec, name):
+    w = synthetic.workload(name)
+    for kv in ("f32", "bf16"):
+        c = dec.make_config(w, kv)
+        st, msg = dec.validate(c)
+        assert st == dec.DEC_OK, msg
+        assert dec.workspace_bytes(c) > 0
+
+
+def test_workspace_covers_kv_cache(dec):
+    w = synthetic.workload("mistral-7b")
+    c32, c16 = dec.make_config(w, "f32"), dec.make_config(w, "bf16")
+    kv32 = 2 * w["n_layers"] * w["max_seq"] * w["n_kv_heads"] * w["head_dim"] * 4
+    assert dec.workspace_bytes(c32) >= kv32
+    assert dec.workspace_bytes(c32) - dec.workspace_bytes(c16) >= kv32 // 2
+
+
+@pytest.mark.parametrize("field,value,needle", [
+    ("n_layers", 0, "positive"),
+    ("n_kv_heads", 3, "multiple"),
+    ("head_dim", 15, "even"),
+    ("rms_eps", 0.0, "positive"),
+    ("rope_theta", -1.0, "positive"),
+    ("n_experts_used", 1, "dense"),
+    ("weight_dtype", 7, "weight_dtype"),
+    ("sliding_window", 16, "window"),
+])
+def test_invalid_configs_rejected(dec, field, value, needle):
+    c = dec.make_config(synthetic.workload("toy"))
+    setattr(c, field, value)
+    st, msg = dec.validate(c)
+    assert st == dec.DEC_EINVAL
+    assert needle in msg
+    assert dec.workspace_bytes(c) == 0
+
+
+def test_expert_count_rules(dec):
+    w = synthetic.workload("mixtral-8x7b")
+    c = dec.make_config(w)
+    c.n_experts_used = 9
+    assert dec.validate(c)[0] == dec.DEC_EINVAL
+    c.n_experts_used = 0
+    assert dec.validate(c)[0] == dec.DEC_EINVAL
+    c.n_experts_used = 2
+    assert dec.validate(c)[0] == dec.DEC_OK
+
+
+def test_llama3_fields_checked(dec):
+    c = dec.make_config(synthetic.workload("toy"))
+    c.rope_llama3 = 1
+    assert dec.validate(c)[0] == dec.DEC_EINVAL
+    c.rope_factor, c.rope_low_freq_factor, c.rope_high_freq_factor, c.rope_orig_ctx = 8.0, 1.0, 4.0, 8192
+    assert dec.validate(c)[0] == dec.DEC_OK
+
+
+def test_create_rejects_bad_arguments_without_gpu(dec):
+    # Argument errors are detected before any CUDA call: NULL weights / workspace.
+    c = dec.make_config(synthetic.workload("toy"))
+    h = ctypes.c_void_p()
+    st = dec.lib.dec_create(ctypes.byref(c), None, None, 0, None, ctypes.byref(h))
+    assert st == dec.DEC_EINVAL and not h.value
+    assert b"weights" in dec.lib.dec_last_error(None)
