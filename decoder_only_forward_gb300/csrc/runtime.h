@@ -102,14 +102,22 @@ struct WsPlan {
 
 WsPlan plan_workspace(const dec_config& c);
 
+// Inside stream capture an event record must be an external node to be
+// timeable after the graph runs; outside capture a plain record is used.
+inline void record_event(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(s, &cs);
+  if (cs == cudaStreamCaptureStatusActive) cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  else cudaEventRecord(ev, s);
+}
 inline void timer_begin(const Model& m, int cls, cudaStream_t s) {
   Timing* t = m.timing;
-  if (t && t->cls == cls && t->n < t->max) cudaEventRecord(t->ev[2 * t->n], s);
+  if (t && t->cls == cls && t->n < t->max) record_event(t->ev[2 * t->n], s);
 }
 inline void timer_end(const Model& m, int cls, cudaStream_t s) {
   Timing* t = m.timing;
   if (t && t->cls == cls && t->n < t->max) {
-    cudaEventRecord(t->ev[2 * t->n + 1], s);
+    record_event(t->ev[2 * t->n + 1], s);
     ++t->n;
   }
 }
