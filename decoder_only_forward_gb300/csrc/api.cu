@@ -34,6 +34,8 @@ static void timing_finish(dec_handle* h) { h->timing.n_done = h->timing.n; }
 
 static thread_local std::string g_create_error;
 
+void dec::set_global_error(const char* msg) { g_create_error = msg; }
+
 static dec_status fail(dec_handle* h, dec_status st, const char* fmt, ...) {
   char buf[512];
   va_list ap;

@@ -501,6 +501,38 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_norm_lmhead(
 }
 
 // ---------------------------------------------------------------------------
+// Standalone attention (dec_attend): position and counters live in a caller
+// scratch area instead of the handle's step state.
+
+__global__ void k_attend_setup(DeviceState* st, int32_t pos, int nkv) {
+  if (threadIdx.x == 0) {
+    st->pos = pos;
+    st->err = 0u;
+  }
+  for (int g = threadIdx.x; g < nkv; g += blockDim.x) st->counters[CNT_ATTN + g] = 0u;
+}
+
+void launch_attend(const float* q, const void* kc, const void* vc, int nq, int nkv, int hd, int max_seq,
+                   int sliding, int kv_dtype, int pos, int nsplit, DeviceState* st, float* part, float* out,
+                   cudaStream_t s) {
+  k_attend_setup<<<1, 128, 0, s>>>(st, pos, nkv);
+  const dim3 grid(nkv, nsplit);
+#define DEC_ATTEND_LAUNCH(KV, HD)                                                                    \
+  k_flash_decode<KV, HD><<<grid, FD_THREADS, 0, s>>>(q, (const KV*)kc, (const KV*)vc, nq, nkv, max_seq, \
+                                                     sliding, st, part, out)
+  if (kv_dtype == DEC_BF16) {
+    if (hd == 64) DEC_ATTEND_LAUNCH(__nv_bfloat16, 64);
+    else if (hd == 128) DEC_ATTEND_LAUNCH(__nv_bfloat16, 128);
+    else DEC_ATTEND_LAUNCH(__nv_bfloat16, 16);
+  } else {
+    if (hd == 64) DEC_ATTEND_LAUNCH(float, 64);
+    else if (hd == 128) DEC_ATTEND_LAUNCH(float, 128);
+    else DEC_ATTEND_LAUNCH(float, 16);
+  }
+#undef DEC_ATTEND_LAUNCH
+}
+
+// ---------------------------------------------------------------------------
 // Host launchers
 
 static inline int gemv_grid(int tasks) {

@@ -135,4 +135,22 @@ void launch_prefill_chunk(const Model& m, cudaStream_t s, int n, int start, floa
 
 inline void count_launch(const Model& m, int n = 1) { *m.launches += n; }
 
+// Standalone attention over a KV ring (decode.cu).  st/part: scratch of
+// attend_scratch_layout().
+void launch_attend(const float* q, const void* kc, const void* vc, int nq, int nkv, int hd, int max_seq,
+                   int sliding, int kv_dtype, int pos, int nsplit, DeviceState* st, float* part, float* out,
+                   cudaStream_t s);
+
+struct AttendLayout {
+  int nsplit;
+  size_t part_offset;   // bytes from the scratch base to the partials
+  size_t total;         // bytes of scratch needed
+};
+// Checks the arguments of a standalone attention call; on success fills lay.
+bool attend_check(const void* q, const void* k, const void* v, const void* out, int nq, int nkv, int hd,
+                  int max_seq, int sliding, int kv_dtype, int pos, AttendLayout& lay, const char** why);
+
+// Message returned by dec_last_error(NULL) (api.cu).
+void set_global_error(const char* msg);
+
 }  // namespace dec

@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "DEC_OK", 1: "DEC_EINVAL", 2: "DEC_ERANGE", 3: "DEC_ECUDA", 4
 EXPORTED = ["dec_config_validate", "dec_workspace_bytes", "dec_create", "dec_prefill", "dec_decode",
             "dec_decode_dev", "dec_kv_reset", "dec_length", "dec_kv_layer", "dec_set_trace",
             "dec_check", "dec_timing_enable", "dec_timing_read", "dec_launch_count", "dec_destroy",
-            "dec_last_error"]
+            "dec_last_error", "dec_attend_scratch_bytes", "dec_attend"]
 
 KERNEL_CLASSES = {"qkv": 1, "attn": 2, "oproj": 3, "gateup": 4, "down": 5, "lmhead": 6, "router": 7,
                   "pf_gemm": 8, "pf_attn": 9}
@@ -73,6 +73,8 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "dec_timing_enable": (I32, [P, I32, I32]),
         "dec_timing_read": (I32, [P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(I32)]),
         "dec_destroy": (None, [P]),
+        "dec_attend_scratch_bytes": (SZ, [I32, I32, I32, I32]),
+        "dec_attend": (I32, [P, P, P, I32, I32, I32, I32, I32, I32, I32, P, P, SZ, P]),
         "dec_last_error": (ctypes.c_char_p, [P]),
     }
     for name, (res, args) in sig.items():
@@ -125,6 +127,24 @@ def workspace_bytes(c: Config) -> int:
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
+
+
+def attend(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, pos: int, sliding_window: int,
+           out: torch.Tensor, scratch: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """dec_attend on torch device tensors: q [nq, hd] f32, k/v rings [max_seq, nkv, hd]."""
+    max_seq, nkv, hd = k.shape
+    nq = q.shape[0]
+    kvd = DEC_F32 if k.dtype == torch.float32 else DEC_BF16
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = lib.dec_attend(q.data_ptr(), k.data_ptr(), v.data_ptr(), nq, nkv, hd, max_seq, int(sliding_window), kvd,
+                        int(pos), out.data_ptr(), scratch.data_ptr(), scratch.numel() * scratch.element_size(),
+                        ctypes.c_void_p(s.cuda_stream))
+    if st != DEC_OK:
+        raise DecError(st, lib.dec_last_error(None).decode())
+
+
+def attend_scratch_bytes(nq: int, nkv: int, hd: int, max_seq: int) -> int:
+    return int(lib.dec_attend_scratch_bytes(nq, nkv, hd, max_seq))
 
 
 class DeviceWeights:

@@ -200,6 +200,23 @@ dec_status dec_timing_enable(dec_handle *h, int32_t kernel_class, int32_t max_la
  * milliseconds and the number of timed launches of that call. */
 dec_status dec_timing_read(dec_handle *h, float *total_ms, int32_t *launches);
 
+/* Standalone attention of one query position over a KV ring: the split-K
+ * flash-decode kernel of the decode step (rml "The decoder", Attend: one-pass
+ * online softmax; Pantheon "Llama Forward Pass", Grouped Query Attention and
+ * Sliding Window).  Query head h reads kv head h*n_kv_heads/n_heads over the
+ * readable slots: min(pos+1, max_seq) under a window, else pos+1 (pos < max_seq).
+ *   q:   device [n_heads][head_dim] f32, already rotated.
+ *   k,v: device rings [max_seq][n_kv_heads][head_dim] of kv_dtype.
+ *   out: device [n_heads][head_dim] f32.
+ *   scratch: device, >= dec_attend_scratch_bytes(...) bytes, 256-byte aligned,
+ *   caller-owned; overwritten by the call.
+ * Enqueued on cuda_stream.  Errors (host-side, before any launch): DEC_EINVAL,
+ * DEC_ENOMEM (scratch too small), DEC_ECUDA.  Messages via dec_last_error(NULL). */
+size_t dec_attend_scratch_bytes(int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t max_seq);
+dec_status dec_attend(const float *q, const void *k, const void *v, int32_t n_heads, int32_t n_kv_heads,
+                      int32_t head_dim, int32_t max_seq, int32_t sliding_window, int32_t kv_dtype,
+                      int32_t pos, float *out, void *scratch, size_t scratch_bytes, void *cuda_stream);
+
 void dec_destroy(dec_handle *h);
 
 /* Message of the last error on h (or of the last failed dec_create when h is NULL). */
