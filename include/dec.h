@@ -217,6 +217,26 @@ dec_status dec_attend(const float *q, const void *k, const void *v, int32_t n_he
                       int32_t head_dim, int32_t max_seq, int32_t sliding_window, int32_t kv_dtype,
                       int32_t pos, float *out, void *scratch, size_t scratch_bytes, void *cuda_stream);
 
+/* dec_attend for callers that cannot allocate device memory (a plug-in whose
+ * host framework's pooled allocator already owns the GPU's memory, or a
+ * latency-critical path where cudaMalloc may not be called).  The pages have
+ * no counterpart: this is an addition of this library.  Arguments and result
+ * are those of dec_attend, without scratch: the scratch is a fixed 1 MiB array
+ * in device memory inside libdec.so, held by every GPU that loads the library
+ * until the process exits.  The call allocates nothing.
+ *   - Sizes whose scratch exceeds 1 MiB (dec_attend_scratch_bytes() > 1 MiB)
+ *     are rejected with DEC_EINVAL and a message.
+ *   - The first call on a device looks up the array's device address on the
+ *     current device (once per device); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (other
+ *     streams, other threads) race and give undefined results.  The call
+ *     resets what must start at zero itself. */
+dec_status dec_attend_noalloc(const float *q, const void *k, const void *v, int32_t n_heads,
+                              int32_t n_kv_heads, int32_t head_dim, int32_t max_seq,
+                              int32_t sliding_window, int32_t kv_dtype, int32_t pos, float *out,
+                              void *cuda_stream);
+
 void dec_destroy(dec_handle *h);
 
 /* Message of the last error on h (or of the last failed dec_create when h is NULL). */
