@@ -106,7 +106,7 @@ WsPlan dec::plan_workspace(const dec_config& c) {
   if (nsplit < 1) nsplit = 1;
   p.nsplit = nsplit;
   const size_t ws = dsize(c.weight_dtype), ks = dsize(c.kv_dtype);
-  const size_t a_elem = c.weight_dtype == DEC_BF16 ? 2 : 4;
+  const size_t a_elem = 4;  // prefill activation rows: f32 (or a bf16 hi/lo pair of the same size)
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + (bytes ? bytes : 1), 256); return o; };
   p.st = take(sizeof(DeviceState));
@@ -136,6 +136,8 @@ WsPlan dec::plan_workspace(const dec_config& c) {
   p.pf_count = take(4 * (size_t)(c.n_experts + 1));
   p.pf_offset = take(4 * (size_t)(c.n_experts + 2));
   p.pf_rows = take(4 * (size_t)T * k);
+  p.pf_inv = take(4 * (size_t)T * k);
+  p.Asort = take(c.n_experts ? a_elem * (size_t)T * k * c.hidden : 0);
   p.Y = take(c.n_experts ? 4 * (size_t)T * k * c.hidden : 0);
   p.ACT = take(a_elem * (size_t)T * k * c.ffn);
   (void)ws;
@@ -237,6 +239,8 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
   S.pf_count = (int32_t*)(base + p.pf_count);
   S.pf_offset = (int32_t*)(base + p.pf_offset);
   S.pf_rows = (int32_t*)(base + p.pf_rows);
+  S.pf_inv = (int32_t*)(base + p.pf_inv);
+  S.Asort = base + p.Asort;
   S.Y = (float*)(base + p.Y);
   S.ACT = base + p.ACT;
   h->layers.resize(cfg->n_layers);

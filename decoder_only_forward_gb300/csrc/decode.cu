@@ -551,6 +551,25 @@ void launch_set_step(const Model& m, cudaStream_t s, const int32_t* d_token, int
   count_launch(m);
 }
 
+template <typename W>
+static void lmhead(const Model& m, cudaStream_t s, const float* x, float* logits, int32_t* d_argmax) {
+  const dec_config& c = m.cfg;
+  const Scratch& S = m.s;
+  const size_t sm_h = (64 + MAX_EXPERTS + (size_t)c.hidden) * sizeof(float);
+  auto kern = k_norm_lmhead<W>;
+  set_smem(kern, sm_h);
+  timer_begin(m, DEC_K_LMHEAD, s);
+  kern<<<m.lm_grid, GEMV_THREADS, sm_h, s>>>(x, m.out_norm, c.rms_eps, (const W*)m.head, c.hidden, c.vocab,
+                                            logits, d_argmax, S.amax_val, S.amax_idx, S.st);
+  timer_end(m, DEC_K_LMHEAD, s);
+  count_launch(m);
+}
+
+void launch_lmhead(const Model& m, cudaStream_t s, const float* x, float* logits, int32_t* d_argmax) {
+  if (m.cfg.weight_dtype == DEC_BF16) lmhead<__nv_bfloat16>(m, s, x, logits, d_argmax);
+  else lmhead<float>(m, s, x, logits, d_argmax);
+}
+
 template <typename W, typename KV>
 static void decode_body(const Model& m, cudaStream_t s, float* logits, int32_t* d_argmax) {
   const dec_config& c = m.cfg;
@@ -650,15 +669,7 @@ static void decode_body(const Model& m, cudaStream_t s, float* logits, int32_t* 
       }
     }
   }
-  if (logits || d_argmax) {
-    auto kern = k_norm_lmhead<W>;
-    set_smem(kern, sm_h);
-    timer_begin(m, DEC_K_LMHEAD, s);
-    kern<<<m.lm_grid, GEMV_THREADS, sm_h, s>>>(S.x, m.out_norm, c.rms_eps, (const W*)m.head, h,
-                                              c.vocab, logits, d_argmax, S.amax_val, S.amax_idx, S.st);
-    timer_end(m, DEC_K_LMHEAD, s);
-    count_launch(m);
-  }
+  if (logits || d_argmax) lmhead<W>(m, s, S.x, logits, d_argmax);
 }
 
 void launch_decode_body(const Model& m, cudaStream_t s, float* logits, int32_t* d_argmax) {

@@ -1,18 +1,524 @@
-// Prefill driver.
-#include "runtime.h"
+// Single-pass prefill (sipllm "Transformer forward pass", Single-pass prefill;
+// rml "The decoder", Forward with n tokens): each layer runs once over all n
+// rows of the chunk, positions ascending, so position t's K/V exists before any
+// later query reads it.  Per layer: RMSNorm rows -> QKV GEMM (+bias, RoPE, K/V
+// rows) -> causal GQA attention -> O GEMM (+residual) -> RMSNorm rows -> SwiGLU
+// GEMMs (+residual) or MoE routing + grouped expert GEMMs + combine.  Only the
+// last row gets the final norm and LM head.
+#include <math.h>
+
+#include "prefill_common.cuh"
 
 namespace dec {
 
-// Positions are swept ascending, so each position's K/V is written before any
-// later position reads it (sipllm "Transformer forward pass", Single-pass
-// prefill).  This first driver runs the decode kernels once per position.
-void launch_prefill_chunk(const Model& m, cudaStream_t s, int n, int start, float* logits,
-                          int32_t* d_argmax) {
-  for (int t = 0; t < n; ++t) {
-    launch_set_step(m, s, m.s.tokens + t, 0, start + t);
-    const bool last = t == n - 1;
-    launch_decode_body(m, s, last ? logits : nullptr, last ? d_argmax : nullptr);
+// ---------------------------------------------------------------------------
+// Row kernels
+
+template <typename W>
+__global__ void k_embed_rows(const W* __restrict__ E, const int32_t* __restrict__ tokens, int h,
+                             float* __restrict__ X) {
+  const int t = blockIdx.x;
+  const W* row = E + (size_t)tokens[t] * h;
+  for (int i = threadIdx.x; i < h; i += blockDim.x) X[(size_t)t * h + i] = to_f32(row[i]);
+}
+
+// (cos, sin) of every rotary pair for positions start..start+n-1, in fp64 then
+// rounded (rml "The decoder", One forward pass, step 3: once per position).
+__global__ void k_rope_rows(const double* __restrict__ inv_freq, int half, int start, int n,
+                            float2* __restrict__ tab) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n * half) return;
+  const int t = i / half, p = i % half;
+  double sn, cs;
+  sincos((double)(start + t) * inv_freq[p], &sn, &cs);
+  tab[i] = make_float2((float)cs, (float)sn);
+}
+
+// A[t] = X[t] / sqrt(mean(X[t]^2) + eps) * w, one CTA per row.
+template <typename TA>
+__global__ void __launch_bounds__(256) k_rmsnorm_rows(const float* __restrict__ X, const float* __restrict__ w,
+                                                      float eps, int h, TA* __restrict__ A) {
+  __shared__ float red[33];
+  const int t = blockIdx.x;
+  const float* x = X + (size_t)t * h;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < h; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
+  ss = warp_sum(ss);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  if (warp == 0) {
+    float v = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.f;
+    v = warp_sum(v);
+    if (lane == 0) red[32] = v;
   }
+  __syncthreads();
+  const float inv = 1.0f / sqrtf(red[32] / (float)h + eps);
+  for (int i = threadIdx.x; i < h; i += blockDim.x) A[(size_t)t * h + i] = from_f32<TA>(x[i] * inv * w[i]);
+}
+
+// ---------------------------------------------------------------------------
+// SIMT GEMM: C[M,N] = A[M,K] . B[N,K]^T with fp32 accumulation, 64x64 tiles.
+// Serves f32 weights (and any shape); the tcgen05 kernel serves bf16.
+// Grouped: blockIdx.z = group g, rows [off[g], off[g+1]), B advanced by g*N*K.
+
+template <typename TA, typename TB>
+__global__ void __launch_bounds__(256) k_gemm_simt(const TA* __restrict__ A, const TB* __restrict__ B, int M,
+                                                   int N, int K, GemmEpi e) {
+  constexpr int BM = 64, BN = 64, BK = 32;
+  __shared__ float As[BK][BM + 4];
+  __shared__ float Bs[BK][BN + 4];
+  int row0 = 0, rows = M;
+  const TB* Bg = B;
+  if (e.group_offset) {
+    const int g = blockIdx.z;
+    row0 = e.group_offset[g];
+    rows = e.group_offset[g + 1] - row0;
+    Bg = B + (size_t)g * N * K;
+  }
+  const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+  if (m0 >= rows) return;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += BK) {
+    for (int i = tid; i < BM * BK; i += 256) {
+      const int r = i / BK, c = i % BK;
+      const int gr = m0 + r, gc = k0 + c;
+      As[c][r] = (gr < rows && gc < K) ? to_f32(A[(size_t)(row0 + gr) * K + gc]) : 0.f;
+    }
+    for (int i = tid; i < BN * BK; i += 256) {
+      const int r = i / BK, c = i % BK;
+      const int gr = n0 + r, gc = k0 + c;
+      Bs[c][r] = (gr < N && gc < K) ? to_f32(Bg[(size_t)gr * K + gc]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < BK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = m0 + ty * 4 + i;
+    if (r >= rows) continue;
+    epi_pair(e, row0 + r, n0 + tx * 4, acc[i][0], acc[i][1]);
+    epi_pair(e, row0 + r, n0 + tx * 4 + 2, acc[i][2], acc[i][3]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Causal GQA attention over the chunk (SIMT): a warp per query row, 32 keys
+// at a time (lane j scores key j, then the warp folds the tile into its online
+// softmax state; rml Attend).  Keys of query position p are [lo, p] with lo = 0
+// or p - W + 1; key position j is read from row (j - base_pos) of K/V.
+
+template <typename KV, typename TO, int HD>
+__global__ void __launch_bounds__(256) k_attn_prefill_simt(
+    const float* __restrict__ Q, const KV* __restrict__ Ks, const KV* __restrict__ Vs, int base_pos, int nq,
+    int nkv, int start, int n, int sliding, TO* __restrict__ O) {
+  constexpr int WARPS = 8, TILE = 32, DPL = (HD + 31) / 32;
+  __shared__ float ks[TILE][HD + 1];
+  __shared__ float vs[TILE][HD];
+  __shared__ float qs[WARPS][HD];
+  const int h = blockIdx.y, g = (h * nkv) / nq;
+  const int kd = nkv * HD, qd = nq * HD;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t0 = blockIdx.x * WARPS;
+  const int t = t0 + warp;
+  const bool active = t < n;
+  const int pos = start + t;
+  const int lo = sliding > 0 ? max(0, pos - sliding + 1) : 0;
+  const float scale = 1.0f / sqrtf((float)HD);
+  if (active)
+    for (int d = lane; d < HD; d += 32) qs[warp][d] = Q[(size_t)t * qd + h * HD + d] * scale;
+  // Key range of the whole CTA.
+  const int tl = min(t0 + WARPS, n) - 1;
+  const int kmin = sliding > 0 ? max(0, start + t0 - sliding + 1) : 0;
+  const int kmax = start + tl;
+  float m = -INFINITY, l = 0.f, o[DPL];
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) o[i] = 0.f;
+  for (int j0 = kmin; j0 <= kmax; j0 += TILE) {
+    const int nt = min(TILE, kmax - j0 + 1);
+    __syncthreads();
+    for (int i = threadIdx.x; i < nt * HD; i += blockDim.x) {
+      const int r = i / HD, d = i % HD;
+      const size_t off = (size_t)(j0 + r - base_pos) * kd + (size_t)g * HD + d;
+      ks[r][d] = to_f32(Ks[off]);
+      vs[r][d] = to_f32(Vs[off]);
+    }
+    __syncthreads();
+    if (!active) continue;
+    const int j = j0 + lane;
+    const bool valid = lane < nt && j >= lo && j <= pos;
+    float s = -INFINITY;
+    if (valid) {
+      s = 0.f;
+#pragma unroll 8
+      for (int d = 0; d < HD; ++d) s = fmaf(qs[warp][d], ks[lane][d], s);
+    }
+    const float tmax = warp_max(s);
+    if (tmax == -INFINITY) continue;
+    const float mnew = fmaxf(m, tmax);
+    const float corr = __expf(m - mnew);
+    const float p = valid ? __expf(s - mnew) : 0.f;
+    l = l * corr + warp_sum(p);
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) o[i] *= corr;
+    for (int jj = 0; jj < nt; ++jj) {
+      const float pj = __shfl_sync(0xffffffffu, p, jj);
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) {
+        const int d = lane + 32 * i;
+        if (d < HD) o[i] = fmaf(pj, vs[jj][d], o[i]);
+      }
+    }
+    m = mnew;
+  }
+  if (!active) return;
+  const float inv = 1.0f / l;
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) {
+    const int d = lane + 32 * i;
+    if (d < HD) O[(size_t)t * qd + h * HD + d] = from_f32<TO>(o[i] * inv);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// K/V ring <-> linear rows, for chunks whose positions wrap the ring.
+
+template <typename KV>
+__global__ void k_kv_gather(const KV* __restrict__ ring_k, const KV* __restrict__ ring_v, int max_seq, int kd,
+                            int h0, int count, KV* __restrict__ lin_k, KV* __restrict__ lin_v) {
+  const size_t total = (size_t)count * kd;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int r = (int)(i / kd), c = (int)(i % kd);
+    const size_t src = (size_t)((h0 + r) % max_seq) * kd + c;
+    lin_k[i] = ring_k[src];
+    lin_v[i] = ring_v[src];
+  }
+}
+
+template <typename KV>
+__global__ void k_kv_commit(const KV* __restrict__ lin_k, const KV* __restrict__ lin_v, int lin_row0, int start,
+                            int t_first, int n, int max_seq, int kd, KV* __restrict__ ring_k, KV* __restrict__ ring_v) {
+  const size_t total = (size_t)(n - t_first) * kd;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int t = t_first + (int)(i / kd), c = (int)(i % kd);
+    const size_t dst = (size_t)((start + t) % max_seq) * kd + c;
+    const size_t src = (size_t)(lin_row0 + t) * kd + c;
+    ring_k[dst] = lin_k[src];
+    ring_v[dst] = lin_v[src];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// MoE for n rows: routing per row (fp32 RMSNorm, router logits, top-k by
+// repeated selection with ties to the lower id, weights renormalised over the
+// selection), a stable counting sort of (row, slot) by expert, grouped expert
+// GEMMs, then a combine in slot order (Pantheon Mixture of Experts; rml
+// Mixture of experts; zLLM moe/prefill grouping).
+
+template <typename W>
+__global__ void __launch_bounds__(256) k_router_rows(const float* __restrict__ X, const float* __restrict__ nw,
+                                                     float eps, const W* __restrict__ router, int h, int E, int k,
+                                                     int32_t* __restrict__ ids, float* __restrict__ wts, int start,
+                                                     int32_t* __restrict__ trace_ids, float* __restrict__ trace_logits,
+                                                     int trace_cap, int layer) {
+  extern __shared__ float sm[];
+  float* red = sm;
+  float* logits = sm + 64;
+  float* xs = sm + 64 + MAX_EXPERTS;
+  const int t = blockIdx.x;
+  const float* x = X + (size_t)t * h;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < h; i += blockDim.x) {
+    const float v = x[i];
+    xs[i] = v;
+    ss = fmaf(v, v, ss);
+  }
+  ss = warp_sum(ss);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  if (warp == 0) {
+    float v = lane < 8 ? red[lane] : 0.f;
+    v = warp_sum(v);
+    if (lane == 0) red[32] = v;
+  }
+  __syncthreads();
+  const float inv = 1.0f / sqrtf(red[32] / (float)h + eps);
+  for (int i = threadIdx.x; i < h; i += blockDim.x) xs[i] = xs[i] * inv * nw[i];
+  __syncthreads();
+  constexpr int V = Chunk<W>::N;
+  for (int e = warp; e < E; e += 8) {
+    const W* row = router + (size_t)e * h;
+    float a = 0.f;
+    for (int c = lane; c < h / V; c += 32) {
+      float wv[V];
+      Chunk<W>::widen(ld_stream16(row + (size_t)c * V), wv);
+#pragma unroll
+      for (int q = 0; q < V; ++q) a = fmaf(wv[q], xs[c * V + q], a);
+    }
+    a = warp_sum(a);
+    if (lane == 0) logits[e] = a;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int sel[MAX_EXPERTS_USED];
+    float mx = -INFINITY;
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e) {
+        bool taken = false;
+        for (int q = 0; q < j; ++q) taken |= (sel[q] == e);
+        if (taken) continue;
+        if (best < 0 || logits[e] > logits[best]) best = e;
+      }
+      sel[j] = best;
+      mx = fmaxf(mx, logits[best]);
+    }
+    float p[MAX_EXPERTS_USED], tot = 0.f;
+    for (int j = 0; j < k; ++j) {
+      p[j] = expf(logits[sel[j]] - mx);
+      tot += p[j];
+    }
+    for (int j = 0; j < k; ++j) {
+      ids[(size_t)t * k + j] = sel[j];
+      wts[(size_t)t * k + j] = p[j] / tot;
+    }
+    if (trace_ids) {
+      const size_t row = (size_t)layer * trace_cap + ((start + t) % trace_cap);
+      for (int j = 0; j < k; ++j) trace_ids[row * k + j] = sel[j];
+      for (int e = 0; e < E; ++e) trace_logits[row * E + e] = logits[e];
+    }
+  }
+}
+
+// Stable counting sort of the n*k (row, slot) entries by expert: offsets[E+1],
+// rows_sorted[pos] = entry, inv[entry] = pos.  One CTA; entries in row order.
+__global__ void __launch_bounds__(256) k_moe_plan(const int32_t* __restrict__ ids, int entries, int E,
+                                                  int32_t* __restrict__ offsets, int32_t* __restrict__ rows_sorted,
+                                                  int32_t* __restrict__ inv) {
+  __shared__ int cnt[MAX_EXPERTS + 1];
+  __shared__ int base[MAX_EXPERTS + 1];
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < entries; i += blockDim.x) atomicAdd(&cnt[ids[i]], 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int e = 0; e < E; ++e) {
+      base[e] = acc;
+      offsets[e] = acc;
+      acc += cnt[e];
+    }
+    offsets[E] = acc;
+  }
+  __syncthreads();
+  // Stable placement: each expert's entries keep row order.  A warp per expert
+  // scans the entries with a ballot so the order is the entry order.
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = warp; e < E; e += blockDim.x >> 5) {
+    int pos = base[e];
+    for (int i0 = 0; i0 < entries; i0 += 32) {
+      const int i = i0 + lane;
+      const bool mine = i < entries && ids[i] == e;
+      const unsigned mask = __ballot_sync(0xffffffffu, mine);
+      if (mine) {
+        const int p = pos + __popc(mask & ((1u << lane) - 1u));
+        rows_sorted[p] = i;
+        inv[i] = p;
+      }
+      pos += __popc(mask);
+    }
+  }
+}
+
+template <typename TA>
+__global__ void k_gather_rows(const TA* __restrict__ A, const int32_t* __restrict__ rows_sorted, int k, int total,
+                              int h, TA* __restrict__ out) {
+  const int p = blockIdx.x;
+  if (p >= total) return;
+  const int t = rows_sorted[p] / k;
+  for (int i = threadIdx.x; i < h; i += blockDim.x) out[(size_t)p * h + i] = A[(size_t)t * h + i];
+}
+
+// X[t] += sum_{j in selection order} w[t,j] * Y[inv[t*k+j]]
+__global__ void k_moe_combine(const float* __restrict__ Y, const int32_t* __restrict__ inv,
+                              const float* __restrict__ wts, int k, int h, float* __restrict__ X) {
+  const int t = blockIdx.x;
+  for (int c = threadIdx.x; c < h; c += blockDim.x) {
+    float acc = 0.f;
+    for (int j = 0; j < k; ++j) acc = fmaf(wts[(size_t)t * k + j], Y[(size_t)inv[(size_t)t * k + j] * h + c], acc);
+    X[(size_t)t * h + c] += acc;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Driver
+
+template <typename TA, typename TW>
+static void gemm(const TA* A, const TW* B, int M, int N, int K, const GemmEpi& e, int groups, int max_rows,
+                 cudaStream_t s, const Model& m) {
+  dim3 grid((max_rows + 63) / 64, (N + 63) / 64, groups);
+  k_gemm_simt<TA, TW><<<grid, 256, 0, s>>>(A, B, M, N, K, e);
+  count_launch(m);
+}
+
+template <typename KV, typename TO>
+static void attention(const Model& m, cudaStream_t s, const KV* Ks, const KV* Vs, int base_pos, int start, int n,
+                      TO* O) {
+  const dec_config& c = m.cfg;
+  dim3 grid((n + 7) / 8, c.n_heads);
+  const float* Q = m.s.Q;
+  if (c.head_dim == 64)
+    k_attn_prefill_simt<KV, TO, 64><<<grid, 256, 0, s>>>(Q, Ks, Vs, base_pos, c.n_heads, c.n_kv_heads, start, n,
+                                                        c.sliding_window, O);
+  else if (c.head_dim == 128)
+    k_attn_prefill_simt<KV, TO, 128><<<grid, 256, 0, s>>>(Q, Ks, Vs, base_pos, c.n_heads, c.n_kv_heads, start, n,
+                                                         c.sliding_window, O);
+  else
+    k_attn_prefill_simt<KV, TO, 16><<<grid, 256, 0, s>>>(Q, Ks, Vs, base_pos, c.n_heads, c.n_kv_heads, start, n,
+                                                        c.sliding_window, O);
+  count_launch(m);
+}
+
+template <typename TW, typename KV>
+static void prefill_chunk(const Model& m, cudaStream_t s, int n, int start, float* logits, int32_t* d_argmax) {
+  // Activations stay fp32 between kernels: rounding them to bf16 for the
+  // GEMMs costs ~3x in end-to-end logit error on the larger-vocabulary models.
+  using TA = float;
+  const dec_config& c = m.cfg;
+  const Scratch& S = m.s;
+  const int h = c.hidden, hd = c.head_dim, qd = c.n_heads * hd, kd = c.n_kv_heads * hd, f = c.ffn;
+  const int half = hd / 2;
+  TA* A = (TA*)S.A;
+  TA* ACT = (TA*)S.ACT;
+  k_embed_rows<TW><<<n, 128, 0, s>>>((const TW*)m.tok_embd, S.tokens, h, S.X);
+  k_rope_rows<<<(n * half + 255) / 256, 256, 0, s>>>(S.inv_freq, half, start, n, S.rope_tab);
+  count_launch(m, 2);
+
+  // Ring slots equal positions unless this chunk can overwrite history it reads.
+  const bool direct = c.sliding_window == 0 || start + n <= c.max_seq;
+  const int h0 = direct ? 0 : (start - c.sliding_window + 1 > 0 ? start - c.sliding_window + 1 : 0);
+  const int hist = start - h0;
+
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerPtrs& L = m.layers[l];
+    k_rmsnorm_rows<TA><<<n, 256, 0, s>>>(S.X, L.attn_norm, c.rms_eps, h, A);
+    count_launch(m);
+    KV* kdst = direct ? (KV*)L.kc : (KV*)S.KVlin_k;
+    KV* vdst = direct ? (KV*)L.vc : (KV*)S.KVlin_v;
+    if (!direct && hist > 0) {
+      k_kv_gather<KV><<<152, 256, 0, s>>>((const KV*)L.kc, (const KV*)L.vc, c.max_seq, kd, h0, hist, kdst, vdst);
+      count_launch(m);
+    }
+    {
+      GemmEpi e{};
+      e.mode = EPI_QKV;
+      e.n_out = qd + 2 * kd;
+      e.bias = L.bqkv;
+      e.rope = S.rope_tab;
+      e.qd = qd;
+      e.kd = kd;
+      e.hd = hd;
+      e.q_out = S.Q;
+      e.q_bf16 = 0;
+      e.k_dst = kdst;
+      e.v_dst = vdst;
+      e.kv_bf16 = std::is_same<KV, __nv_bfloat16>::value;
+      e.kv_row0 = direct ? start : hist;
+      timer_begin(m, DEC_K_PF_GEMM, s);
+      gemm<TA, TW>(A, (const TW*)L.wqkv, n, qd + 2 * kd, h, e, 1, n, s, m);
+      timer_end(m, DEC_K_PF_GEMM, s);
+    }
+    timer_begin(m, DEC_K_PF_ATTN, s);
+    attention<KV, TA>(m, s, kdst, vdst, direct ? 0 : h0, start, n, A);
+    timer_end(m, DEC_K_PF_ATTN, s);
+    if (!direct) {
+      const int t_first = n > c.max_seq ? n - c.max_seq : 0;
+      k_kv_commit<KV><<<152, 256, 0, s>>>(kdst, vdst, hist, start, t_first, n, c.max_seq, kd, (KV*)L.kc,
+                                          (KV*)L.vc);
+      count_launch(m);
+    }
+    {
+      GemmEpi e{};
+      e.mode = EPI_RESID;
+      e.n_out = h;
+      e.out_f32 = S.X;
+      timer_begin(m, DEC_K_PF_GEMM, s);
+      gemm<TA, TW>(A, (const TW*)L.wo, n, h, qd, e, 1, n, s, m);
+      timer_end(m, DEC_K_PF_GEMM, s);
+    }
+    if (c.n_experts == 0) {
+      k_rmsnorm_rows<TA><<<n, 256, 0, s>>>(S.X, L.ffn_norm, c.rms_eps, h, A);
+      count_launch(m);
+      GemmEpi e1{};
+      e1.mode = EPI_SWIGLU;
+      e1.n_out = 2 * f;
+      e1.act = ACT;
+      e1.act_bf16 = std::is_same<TA, __nv_bfloat16>::value;
+      timer_begin(m, DEC_K_PF_GEMM, s);
+      gemm<TA, TW>(A, (const TW*)L.w_gateup, n, 2 * f, h, e1, 1, n, s, m);
+      timer_end(m, DEC_K_PF_GEMM, s);
+      GemmEpi e2{};
+      e2.mode = EPI_RESID;
+      e2.n_out = h;
+      e2.out_f32 = S.X;
+      timer_begin(m, DEC_K_PF_GEMM, s);
+      gemm<TA, TW>(ACT, (const TW*)L.w_down, n, h, f, e2, 1, n, s, m);
+      timer_end(m, DEC_K_PF_GEMM, s);
+    } else {
+      const int k = c.n_experts_used, E = c.n_experts, entries = n * k;
+      const size_t smr = (64 + MAX_EXPERTS + (size_t)h) * sizeof(float);
+      if (smr > 48 * 1024)
+        cudaFuncSetAttribute(k_router_rows<TW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smr);
+      k_router_rows<TW><<<n, 256, smr, s>>>(S.X, L.ffn_norm, c.rms_eps, (const TW*)L.router, h, E, k, S.pf_ids,
+                                            S.pf_wts, start, m.trace_ids, m.trace_logits, m.trace_cap, l);
+      k_moe_plan<<<1, 256, 0, s>>>(S.pf_ids, entries, E, S.pf_offset, S.pf_rows, S.pf_inv);
+      k_rmsnorm_rows<TA><<<n, 256, 0, s>>>(S.X, L.ffn_norm, c.rms_eps, h, A);
+      k_gather_rows<TA><<<entries, 128, 0, s>>>(A, S.pf_rows, k, entries, h, (TA*)S.Asort);
+      count_launch(m, 4);
+      GemmEpi e1{};
+      e1.mode = EPI_SWIGLU;
+      e1.n_out = 2 * f;
+      e1.act = ACT;
+      e1.act_bf16 = std::is_same<TA, __nv_bfloat16>::value;
+      e1.group_offset = S.pf_offset;
+      timer_begin(m, DEC_K_PF_GEMM, s);
+      gemm<TA, TW>((const TA*)S.Asort, (const TW*)L.w_gateup, entries, 2 * f, h, e1, E, n, s, m);
+      timer_end(m, DEC_K_PF_GEMM, s);
+      GemmEpi e2{};
+      e2.mode = EPI_STORE;
+      e2.n_out = h;
+      e2.out_f32 = S.Y;
+      e2.group_offset = S.pf_offset;
+      timer_begin(m, DEC_K_PF_GEMM, s);
+      gemm<TA, TW>(ACT, (const TW*)L.w_down, entries, h, f, e2, E, n, s, m);
+      timer_end(m, DEC_K_PF_GEMM, s);
+      k_moe_combine<<<n, 256, 0, s>>>(S.Y, S.pf_inv, S.pf_wts, k, h, S.X);
+      count_launch(m);
+    }
+  }
+  if (logits || d_argmax) launch_lmhead(m, s, S.X + (size_t)(n - 1) * h, logits, d_argmax);
+}
+
+void launch_prefill_chunk(const Model& m, cudaStream_t s, int n, int start, float* logits, int32_t* d_argmax) {
+  const bool wb = m.cfg.weight_dtype == DEC_BF16, kb = m.cfg.kv_dtype == DEC_BF16;
+  if (wb && kb) prefill_chunk<__nv_bfloat16, __nv_bfloat16>(m, s, n, start, logits, d_argmax);
+  else if (wb) prefill_chunk<__nv_bfloat16, float>(m, s, n, start, logits, d_argmax);
+  else if (kb) prefill_chunk<float, __nv_bfloat16>(m, s, n, start, logits, d_argmax);
+  else prefill_chunk<float, float>(m, s, n, start, logits, d_argmax);
 }
 
 }  // namespace dec

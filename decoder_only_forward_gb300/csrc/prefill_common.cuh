@@ -1,0 +1,100 @@
+// Epilogues shared by the prefill GEMMs (SIMT and tcgen05): every GEMM hands
+// its accumulators over as pairs of adjacent output columns of one row.
+#pragma once
+
+#include "runtime.h"
+
+namespace dec {
+
+enum EpiMode : int {
+  EPI_QKV = 0,     // +bias, adjacent-pair RoPE, q -> Q rows, k/v -> K/V rows (cache or linear scratch)
+  EPI_RESID = 1,   // out[row][col] += v  (residual stream, f32)
+  EPI_SWIGLU = 2,  // columns (2j, 2j+1) = (gate, up) -> act[row][j] = silu(gate) * up
+  EPI_STORE = 3,   // out[row][col] = v (f32)
+};
+
+struct GemmEpi {
+  int mode;
+  int n_out;            // valid output columns (N)
+  // EPI_RESID / EPI_STORE: f32 rows of n_out columns
+  float* out_f32;
+  // EPI_SWIGLU: rows of n_out/2 activations, bf16 when act_bf16 else f32
+  void* act;
+  int act_bf16;
+  // EPI_QKV
+  const float* bias;      // nullable
+  const float2* rope;     // [row][hd/2] (cos, sin) of the row's position
+  int qd, kd, hd;
+  void* q_out;            // [row][qd], bf16 when q_bf16 else f32
+  int q_bf16;
+  void* k_dst;            // K rows: row r goes to row (r + kv_row0), kd columns
+  void* v_dst;
+  int kv_bf16;
+  int kv_row0;
+  // Grouped (MoE) GEMMs: rows of group g are [offset[g], offset[g] + count[g]).
+  const int32_t* group_offset;   // nullable = one group of all rows
+};
+
+template <typename T>
+__device__ __forceinline__ void store_pair(T* p, float a, float b);
+template <>
+__device__ __forceinline__ void store_pair<float>(float* p, float a, float b) {
+  *reinterpret_cast<float2*>(p) = make_float2(a, b);
+}
+template <>
+__device__ __forceinline__ void store_pair<__nv_bfloat16>(__nv_bfloat16* p, float a, float b) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
+}
+
+// Applies the epilogue to columns (col, col+1) of global row `row`.  col is even.
+__device__ __forceinline__ void epi_pair(const GemmEpi& e, int row, int col, float v0, float v1) {
+  if (col >= e.n_out) return;
+  switch (e.mode) {
+    case EPI_RESID: {
+      float2* p = reinterpret_cast<float2*>(e.out_f32 + (size_t)row * e.n_out + col);
+      float2 x = *p;
+      x.x += v0;
+      x.y += v1;
+      *p = x;
+      break;
+    }
+    case EPI_STORE:
+      store_pair(e.out_f32 + (size_t)row * e.n_out + col, v0, v1);
+      break;
+    case EPI_SWIGLU: {
+      const float a = silu_f(v0) * v1;
+      const size_t o = (size_t)row * (e.n_out / 2) + (col >> 1);
+      if (e.act_bf16) reinterpret_cast<__nv_bfloat16*>(e.act)[o] = __float2bfloat16_rn(a);
+      else reinterpret_cast<float*>(e.act)[o] = a;
+      break;
+    }
+    case EPI_QKV: {
+      if (e.bias) {
+        v0 += e.bias[col];
+        v1 += e.bias[col + 1];
+      }
+      if (col < e.qd + e.kd) {
+        const int d = (col < e.qd ? col : col - e.qd) % e.hd;
+        const float2 cs = e.rope[(size_t)row * (e.hd / 2) + (d >> 1)];
+        const float a = v0 * cs.x - v1 * cs.y;
+        const float b = v0 * cs.y + v1 * cs.x;
+        v0 = a;
+        v1 = b;
+      }
+      if (col < e.qd) {
+        const size_t o = (size_t)row * e.qd + col;
+        if (e.q_bf16) store_pair(reinterpret_cast<__nv_bfloat16*>(e.q_out) + o, v0, v1);
+        else store_pair(reinterpret_cast<float*>(e.q_out) + o, v0, v1);
+      } else {
+        const bool is_k = col < e.qd + e.kd;
+        const size_t o = (size_t)(row + e.kv_row0) * e.kd + (is_k ? col - e.qd : col - e.qd - e.kd);
+        void* dst = is_k ? e.k_dst : e.v_dst;
+        if (e.kv_bf16) store_pair(reinterpret_cast<__nv_bfloat16*>(dst) + o, v0, v1);
+        else store_pair(reinterpret_cast<float*>(dst) + o, v0, v1);
+      }
+      break;
+    }
+  }
+}
+
+}  // namespace dec

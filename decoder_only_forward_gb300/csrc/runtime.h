@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "../../include/dec.h"
 #include "common.cuh"
 
@@ -50,6 +52,8 @@ struct Scratch {
   int32_t* pf_count;    // [E] rows per expert
   int32_t* pf_offset;   // [E+1]
   int32_t* pf_rows;     // [T*k] (row*k + slot) grouped by expert
+  int32_t* pf_inv;      // [T*k] sorted position of entry row*k + slot
+  void* Asort;          // [T*k][h] normalised rows gathered by expert (MoE)
   float* Y;             // [T*k][h] per-(row, slot) expert outputs (MoE)
   void* ACT;            // [T*k][ffn] gate/up output rows (A operand of down)
 };
@@ -92,7 +96,7 @@ struct Model {
 // Workspace plan: byte offsets of every region; total size.
 struct WsPlan {
   size_t st, inv_freq, rope_tab, x, q, attn, act, nbuf, ids, wts, part, amax_val, amax_idx, tokens;
-  size_t X, A, Q, KVlin_k, KVlin_v, pf_ids, pf_wts, pf_count, pf_offset, pf_rows, Y, ACT;
+  size_t X, A, Q, KVlin_k, KVlin_v, pf_ids, pf_wts, pf_count, pf_offset, pf_rows, pf_inv, Asort, Y, ACT;
   size_t kv;            // start of the KV rings
   size_t kv_layer_bytes;
   size_t total;
@@ -125,6 +129,8 @@ inline void timer_end(const Model& m, int cls, cudaStream_t s) {
 // decode.cu
 void launch_set_step(const Model& m, cudaStream_t s, const int32_t* d_token, int32_t token, int32_t pos);
 void launch_decode_body(const Model& m, cudaStream_t s, float* logits, int32_t* d_argmax);
+// Final RMSNorm + LM head (+ argmax) of one residual row x.
+void launch_lmhead(const Model& m, cudaStream_t s, const float* x, float* logits, int32_t* d_argmax);
 
 // prefill.cu
 // Runs tokens (already in m.s.tokens[0..n)) at positions start..start+n-1; writes

@@ -224,3 +224,63 @@ def test_mixtral_reduced_expert_ids(dec_mod):
                 assert gap < 4 * err, f"layer {l} pos {p}: ids {list(ids[l, p])} vs {ref_ids}, gap {gap:.2e}"
                 mismatched += 1
     assert mismatched <= 2
+
+
+def test_toy_append_prefill_after_wrap(dec_mod):
+    # Window 8: prefill 12 (wraps), decode 3, then append chunks of 5 and of 10 (> max_seq)
+    # at the current length; each append's last logits match the oracle on the whole sequence.
+    w = synthetic.workload("toy", sliding_window=8, max_seq=8)
+    toks = list(synthetic.prompt_tokens(w, 30, seed=5))
+    d = dec_mod.Decoder(w)
+    lg = torch.empty(w["vocab"], device="cuda")
+    d.prefill(toks[:12], 0, lg)
+    for i in range(12, 15):
+        d.decode(toks[i], i, lg)
+    d.prefill(toks[15:20], 15, lg)
+    d.synchronize()
+    a = lg.cpu().numpy().copy()
+    d.prefill(toks[20:30], 20, lg)
+    d.synchronize()
+    b = lg.cpu().numpy().copy()
+    from tests.gpu_helpers import oracle_session
+    s = oracle_session(w)
+    ref = s.prefill_batched(toks, 0, logits_rows=[19, 29])
+    tol = tolerances(w)[0]
+    compare_logits(np.stack([a, b]), ref, tol, tol)
+    slots = ring_positions(30, 8, 8)
+    kc, _ = d.kv_layer(1)
+    for s_, p in enumerate(slots):
+        np.testing.assert_allclose(kc[s_].cpu().numpy(), s.keys[1][p], atol=1e-5, rtol=1e-5)
+
+
+def _prefill_vs_decode_loop(dec_mod, w, P, extra):
+    """Property at any size (sipllm: single-pass prefill == per-token forward): the prefill
+    path (GEMMs + tiled attention) and the decode path (GEMVs + split-K attention) agree."""
+    toks = synthetic.prompt_tokens(w, P + extra, seed=7)
+    a = dec_mod.Decoder(w)
+    la = torch.empty(w["vocab"], device="cuda")
+    a.prefill(toks, 0, la)                      # one call over P + extra positions
+    b = dec_mod.Decoder(w, weights=a.weights)
+    lb = torch.empty(w["vocab"], device="cuda")
+    b.prefill(toks[:P], 0, lb)
+    for i in range(P, P + extra):               # the tail through the decode kernels
+        b.decode(int(toks[i]), i, lb)
+    a.synchronize()
+    b.synchronize()
+    x, y = la.cpu().numpy(), lb.cpu().numpy()
+    compare_logits(x[None], y[None].astype(np.float64), *tolerances(w))
+    return a, b
+
+
+def test_smollm2_prefill_equals_decode_path_full_size(dec_mod):
+    w = synthetic.workload("smollm2-135m")
+    _prefill_vs_decode_loop(dec_mod, w, w["prompt"], 32)
+
+
+@pytest.mark.slow
+def test_mistral_full_prefill_then_wrapping_decode(dec_mod):
+    # Full Mistral shape: 4096-token prefill fills the 4096-slot window; 48 more
+    # positions wrap the ring.  Single-call prefill of all 4144 vs prefill 4096 + 48 decodes.
+    w = synthetic.workload("mistral-7b")
+    a, b = _prefill_vs_decode_loop(dec_mod, w, 4096, 48)
+    assert a.length == b.length == 4144
