@@ -1,0 +1,243 @@
+// Prefill projection GEMM on the 5th-generation tensor cores:
+//   C[M,N] = A[M,K] . B[N,K]^T, bf16 operands, f32 accumulation in TMEM.
+// A (activations) may be given as a bf16 pair (hi, lo) with A = hi + lo; the
+// kernel then issues two MMAs per K step so the product keeps ~16 bits of the
+// activations' mantissa (bf16 weights with fp32 activations and accumulation).
+//
+// One CTA computes one 128 x BN tile with three warp roles:
+//   warp 0 lane 0: TMA producer, K-blocks of 64 into a ring of smem stages;
+//   warp 1 lane 0: MMA issuer (tcgen05.mma, cta_group::1), frees stages with
+//                  tcgen05.commit; warp 1 also owns the TMEM allocation;
+//   warps 2-5:     epilogue, tcgen05.ld of the accumulator rows (warp w reads
+//                  TMEM lanes 32*(w%4)..+31), then the fused epilogue.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "prefill_common.cuh"
+#include "tc.cuh"
+
+namespace dec {
+
+constexpr int TC_BM = 128, TC_BK = 64, TC_THREADS = 192;
+
+template <int BN, bool SPLIT>
+struct TcCfg {
+  static constexpr int A_BYTES = TC_BM * TC_BK * 2;
+  static constexpr int B_BYTES = BN * TC_BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES * (SPLIT ? 2 : 1) + B_BYTES;
+  static constexpr int STAGES_FIT = (200 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+};
+
+template <int BN, bool SPLIT>
+__global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant__ CUtensorMap tm_ahi,
+                                                           const __grid_constant__ CUtensorMap tm_alo,
+                                                           const __grid_constant__ CUtensorMap tm_b, int M, int N,
+                                                           int K, GemmEpi e, DeviceState* st) {
+  using C = TcCfg<BN, SPLIT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* progress = abort_flag + 1;  // [0] K-blocks issued, [1] K-blocks consumed
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int row0 = 0, rows = M, b_row0 = 0;
+  if (e.group_offset) {
+    const int g = blockIdx.z;
+    row0 = e.group_offset[g];
+    rows = e.group_offset[g + 1] - row0;
+    b_row0 = g * N;
+  }
+  const int m0 = blockIdx.x * TC_BM, n0 = blockIdx.y * BN;
+  if (m0 >= rows) return;  // uniform per CTA, before any barrier or TMEM use
+  const int kblocks = (K + TC_BK - 1) / TC_BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    *abort_flag = 0;
+    progress[0] = 0;
+    progress[1] = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&tm_ahi);
+    if (SPLIT) tma_prefetch_desc(&tm_alo);
+    tma_prefetch_desc(&tm_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, BN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int kb = 0; kb < kblocks; ++kb) {
+        const int s = kb % C::STAGES;
+        const uint32_t ph = (kb / C::STAGES) & 1;
+        if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, st, 101)) break;
+        uint8_t* base = smem + s * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+        tma_load_2d(base, &tm_ahi, &full[s], kb * TC_BK, row0 + m0);
+        if (SPLIT) tma_load_2d(base + C::A_BYTES, &tm_alo, &full[s], kb * TC_BK, row0 + m0);
+        tma_load_2d(base + C::A_BYTES * (SPLIT ? 2 : 1), &tm_b, &full[s], kb * TC_BK, b_row0 + n0);
+        progress[0] = kb + 1;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(TC_BM, BN);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        const int s = kb % C::STAGES;
+        const uint32_t ph = (kb / C::STAGES) & 1;
+        if (!mbar_wait(&full[s], ph, abort_flag, st, 102)) break;
+        tc_fence_after();
+        uint8_t* base = smem + s * C::STAGE_BYTES;
+        const uint64_t da = sw128_kmajor_desc(smem_u32(base));
+        const uint64_t dl = sw128_kmajor_desc(smem_u32(base + C::A_BYTES));
+        const uint64_t db = sw128_kmajor_desc(smem_u32(base + C::A_BYTES * (SPLIT ? 2 : 1)));
+#pragma unroll
+        for (int k = 0; k < TC_BK / 16; ++k) {
+          tc_mma_bf16(tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          if (SPLIT) tc_mma_bf16(tmem, dl + 2 * k, db + 2 * k, idesc, 1u);
+        }
+        tc_commit(&empty[s]);
+        progress[1] = kb + 1;
+      }
+      tc_commit(tfull);
+    }
+  } else {
+    const bool ok = mbar_wait(tfull, 0, abort_flag, st, 103);
+    tc_fence_after();
+    if (ok && !*abort_flag) {
+      const int q = warp & 3;
+      const int r = m0 + q * 32 + lane;
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        if (n0 + c >= N) break;
+        float v[32];
+        tmem_ld32(trow + c, v);
+        if (r < rows) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) epi_pair(e, row0 + r, n0 + c + j, v[j], v[j + 1]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // Never taken when the pipeline is consistent.  Drain what is in flight
+    // (bounded) before the TMEM and shared memory are released.
+    volatile int no_abort = 0;
+    if (threadIdx.x == 0)
+      for (int kb = progress[1]; kb < progress[0]; ++kb)
+        mbar_wait(&full[kb % C::STAGES], (kb / C::STAGES) & 1, &no_abort, nullptr, 0, 100000000ull);
+    if (threadIdx.x == 32) mbar_wait(tfull, 0, &no_abort, nullptr, 0, 100000000ull);
+    __syncthreads();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, BN);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side: tensor maps and launch.
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A [rows, cols] bf16 row-major matrix, tiles of box_rows x 64, 128-byte swizzle.
+static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)TC_BK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool SPLIT>
+static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& al, const CUtensorMap& b, int M, int N, int K,
+                             const GemmEpi& e, int groups, int max_rows, DeviceState* st, cudaStream_t s) {
+  using C = TcCfg<BN, SPLIT>;
+  auto kern = k_gemm_tc<BN, SPLIT>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  dim3 grid((max_rows + TC_BM - 1) / TC_BM, (N + BN - 1) / BN, groups);
+  kern<<<grid, TC_THREADS, C::SMEM, s>>>(a, al, b, M, N, K, e, st);
+  return cudaGetLastError();
+}
+
+// A (hi plane, optional lo plane): [a_rows, K] bf16; B: [groups * N, K] bf16.
+// Grouped when e.group_offset is set (max_rows bounds any one group's rows).
+cudaError_t launch_gemm_tc(const void* a_hi, const void* a_lo, int a_rows, const void* b, int M, int N, int K,
+                           const GemmEpi& e, int groups, int max_rows, DeviceState* st, cudaStream_t s) {
+  if (K % 8 != 0 || a_rows <= 0 || N <= 0) return cudaErrorInvalidValue;
+  const int bn = N >= 1536 ? 256 : 128;
+  CUtensorMap ma, ml, mb;
+  if (!make_map(&ma, a_hi, (uint64_t)a_rows, (uint64_t)K, TC_BM)) return cudaErrorInvalidValue;
+  if (a_lo && !make_map(&ml, a_lo, (uint64_t)a_rows, (uint64_t)K, TC_BM)) return cudaErrorInvalidValue;
+  if (!a_lo) ml = ma;
+  if (!make_map(&mb, b, (uint64_t)N * groups, (uint64_t)K, (uint32_t)bn)) return cudaErrorInvalidValue;
+  if (bn == 256)
+    return a_lo ? launch_tc<256, true>(ma, ml, mb, M, N, K, e, groups, max_rows, st, s)
+                : launch_tc<256, false>(ma, ml, mb, M, N, K, e, groups, max_rows, st, s);
+  return a_lo ? launch_tc<128, true>(ma, ml, mb, M, N, K, e, groups, max_rows, st, s)
+              : launch_tc<128, false>(ma, ml, mb, M, N, K, e, groups, max_rows, st, s);
+}
+
+}  // namespace dec
+
+using namespace dec;
+
+// C = (A_hi + A_lo) . B^T through the tensor-core kernel (C f32, row-major).
+extern "C" dec_status dec_gemm_bf16(const void* a_hi, const void* a_lo, const void* b, float* c, int32_t m,
+                                    int32_t n, int32_t k, void* cuda_stream) {
+  if (!a_hi || !b || !c || m <= 0 || n <= 0 || k <= 0) {
+    set_global_error("dec_gemm_bf16: NULL pointer or non-positive size");
+    return DEC_EINVAL;
+  }
+  if (k % 8 != 0 || n % 2 != 0 || (((uintptr_t)a_hi | (uintptr_t)b | (uintptr_t)(a_lo ? a_lo : a_hi)) & 15u)) {
+    set_global_error("dec_gemm_bf16: k must be a multiple of 8, n even, operands 16-byte aligned");
+    return DEC_EINVAL;
+  }
+  GemmEpi e{};
+  e.mode = EPI_STORE;
+  e.n_out = n;
+  e.out_f32 = c;
+  const cudaError_t err = launch_gemm_tc(a_hi, a_lo, m, b, m, n, k, e, 1, m, nullptr, (cudaStream_t)cuda_stream);
+  if (err != cudaSuccess) {
+    set_global_error(cudaGetErrorString(err));
+    return DEC_ECUDA;
+  }
+  return DEC_OK;
+}

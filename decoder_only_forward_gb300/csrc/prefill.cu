@@ -35,9 +35,8 @@ __global__ void k_rope_rows(const double* __restrict__ inv_freq, int half, int s
 }
 
 // A[t] = X[t] / sqrt(mean(X[t]^2) + eps) * w, one CTA per row.
-template <typename TA>
 __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float* __restrict__ X, const float* __restrict__ w,
-                                                      float eps, int h, TA* __restrict__ A) {
+                                                      float eps, int h, RowOut out) {
   __shared__ float red[33];
   const int t = blockIdx.x;
   const float* x = X + (size_t)t * h;
@@ -54,7 +53,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float* __restrict__ 
   }
   __syncthreads();
   const float inv = 1.0f / sqrtf(red[32] / (float)h + eps);
-  for (int i = threadIdx.x; i < h; i += blockDim.x) A[(size_t)t * h + i] = from_f32<TA>(x[i] * inv * w[i]);
+  for (int i = threadIdx.x; i < h; i += blockDim.x) row_store(out, (size_t)t * h + i, x[i] * inv * w[i]);
 }
 
 // ---------------------------------------------------------------------------
@@ -121,10 +120,10 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const TA* __restrict__ A, con
 // softmax state; rml Attend).  Keys of query position p are [lo, p] with lo = 0
 // or p - W + 1; key position j is read from row (j - base_pos) of K/V.
 
-template <typename KV, typename TO, int HD>
+template <typename KV, int HD>
 __global__ void __launch_bounds__(256) k_attn_prefill_simt(
     const float* __restrict__ Q, const KV* __restrict__ Ks, const KV* __restrict__ Vs, int base_pos, int nq,
-    int nkv, int start, int n, int sliding, TO* __restrict__ O) {
+    int nkv, int start, int n, int sliding, RowOut O) {
   constexpr int WARPS = 8, TILE = 32, DPL = (HD + 31) / 32;
   __shared__ float ks[TILE][HD + 1];
   __shared__ float vs[TILE][HD];
@@ -189,7 +188,7 @@ __global__ void __launch_bounds__(256) k_attn_prefill_simt(
 #pragma unroll
   for (int i = 0; i < DPL; ++i) {
     const int d = lane + 32 * i;
-    if (d < HD) O[(size_t)t * qd + h * HD + d] = from_f32<TO>(o[i] * inv);
+    if (d < HD) row_store(O, (size_t)t * qd + h * HD + d, o[i] * inv);
   }
 }
 
@@ -344,13 +343,14 @@ __global__ void __launch_bounds__(256) k_moe_plan(const int32_t* __restrict__ id
   }
 }
 
-template <typename TA>
-__global__ void k_gather_rows(const TA* __restrict__ A, const int32_t* __restrict__ rows_sorted, int k, int total,
-                              int h, TA* __restrict__ out) {
+// out[p] = A[row of entry p] for every sorted position p (rows of `words`
+// 32-bit words; one call per plane).
+__global__ void k_gather_rows(const uint32_t* __restrict__ A, const int32_t* __restrict__ rows_sorted, int k,
+                              int total, int words, uint32_t* __restrict__ out) {
   const int p = blockIdx.x;
   if (p >= total) return;
   const int t = rows_sorted[p] / k;
-  for (int i = threadIdx.x; i < h; i += blockDim.x) out[(size_t)p * h + i] = A[(size_t)t * h + i];
+  for (int i = threadIdx.x; i < words; i += blockDim.x) out[(size_t)p * words + i] = A[(size_t)t * words + i];
 }
 
 // X[t] += sum_{j in selection order} w[t,j] * Y[inv[t*k+j]]
@@ -367,43 +367,65 @@ __global__ void k_moe_combine(const float* __restrict__ Y, const int32_t* __rest
 // ---------------------------------------------------------------------------
 // Driver
 
-template <typename TA, typename TW>
-static void gemm(const TA* A, const TW* B, int M, int N, int K, const GemmEpi& e, int groups, int max_rows,
-                 cudaStream_t s, const Model& m) {
-  dim3 grid((max_rows + 63) / 64, (N + 63) / 64, groups);
-  k_gemm_simt<TA, TW><<<grid, 256, 0, s>>>(A, B, M, N, K, e);
+// An activation row buffer: f32 rows (f32 weights) or bf16 hi/lo planes of
+// `rows` x `cols` (bf16 weights, for the tensor-core GEMMs).
+struct Act {
+  void* base;
+  bool split;
+  int rows, cols;
+  RowOut out() const {
+    RowOut o;
+    o.hi = base;
+    o.lo = split ? reinterpret_cast<__nv_bfloat16*>(base) + (size_t)rows * cols : nullptr;
+    o.f32 = split ? 0 : 1;
+    return o;
+  }
+  const void* lo() const { return split ? reinterpret_cast<const __nv_bfloat16*>(base) + (size_t)rows * cols : nullptr; }
+};
+
+template <typename TW>
+static void gemm(const Model& m, cudaStream_t s, const Act& a, const TW* B, int M, int N, int K, const GemmEpi& e,
+                 int groups, int max_rows) {
+  timer_begin(m, DEC_K_PF_GEMM, s);
+  if (std::is_same<TW, __nv_bfloat16>::value) {
+    launch_gemm_tc(a.base, a.lo(), a.rows, B, M, N, K, e, groups, max_rows, m.s.st, s);
+  } else {
+    dim3 grid((max_rows + 63) / 64, (N + 63) / 64, groups);
+    k_gemm_simt<float, TW><<<grid, 256, 0, s>>>((const float*)a.base, B, M, N, K, e);
+  }
+  timer_end(m, DEC_K_PF_GEMM, s);
   count_launch(m);
 }
 
-template <typename KV, typename TO>
+template <typename KV>
 static void attention(const Model& m, cudaStream_t s, const KV* Ks, const KV* Vs, int base_pos, int start, int n,
-                      TO* O) {
+                      RowOut O) {
   const dec_config& c = m.cfg;
   dim3 grid((n + 7) / 8, c.n_heads);
   const float* Q = m.s.Q;
+  timer_begin(m, DEC_K_PF_ATTN, s);
   if (c.head_dim == 64)
-    k_attn_prefill_simt<KV, TO, 64><<<grid, 256, 0, s>>>(Q, Ks, Vs, base_pos, c.n_heads, c.n_kv_heads, start, n,
-                                                        c.sliding_window, O);
+    k_attn_prefill_simt<KV, 64><<<grid, 256, 0, s>>>(Q, Ks, Vs, base_pos, c.n_heads, c.n_kv_heads, start, n,
+                                                    c.sliding_window, O);
   else if (c.head_dim == 128)
-    k_attn_prefill_simt<KV, TO, 128><<<grid, 256, 0, s>>>(Q, Ks, Vs, base_pos, c.n_heads, c.n_kv_heads, start, n,
-                                                         c.sliding_window, O);
+    k_attn_prefill_simt<KV, 128><<<grid, 256, 0, s>>>(Q, Ks, Vs, base_pos, c.n_heads, c.n_kv_heads, start, n,
+                                                     c.sliding_window, O);
   else
-    k_attn_prefill_simt<KV, TO, 16><<<grid, 256, 0, s>>>(Q, Ks, Vs, base_pos, c.n_heads, c.n_kv_heads, start, n,
-                                                        c.sliding_window, O);
+    k_attn_prefill_simt<KV, 16><<<grid, 256, 0, s>>>(Q, Ks, Vs, base_pos, c.n_heads, c.n_kv_heads, start, n,
+                                                    c.sliding_window, O);
+  timer_end(m, DEC_K_PF_ATTN, s);
   count_launch(m);
 }
 
 template <typename TW, typename KV>
 static void prefill_chunk(const Model& m, cudaStream_t s, int n, int start, float* logits, int32_t* d_argmax) {
-  // Activations stay fp32 between kernels: rounding them to bf16 for the
-  // GEMMs costs ~3x in end-to-end logit error on the larger-vocabulary models.
-  using TA = float;
   const dec_config& c = m.cfg;
   const Scratch& S = m.s;
   const int h = c.hidden, hd = c.head_dim, qd = c.n_heads * hd, kd = c.n_kv_heads * hd, f = c.ffn;
   const int half = hd / 2;
-  TA* A = (TA*)S.A;
-  TA* ACT = (TA*)S.ACT;
+  // bf16 weights: activations reach the tensor cores as bf16 (hi, lo) pairs;
+  // f32 weights: f32 rows for the SIMT GEMM.  Both keep ~fp32 activations.
+  const bool split = std::is_same<TW, __nv_bfloat16>::value;
   k_embed_rows<TW><<<n, 128, 0, s>>>((const TW*)m.tok_embd, S.tokens, h, S.X);
   k_rope_rows<<<(n * half + 255) / 256, 256, 0, s>>>(S.inv_freq, half, start, n, S.rope_tab);
   count_launch(m, 2);
@@ -413,9 +435,13 @@ static void prefill_chunk(const Model& m, cudaStream_t s, int n, int start, floa
   const int h0 = direct ? 0 : (start - c.sliding_window + 1 > 0 ? start - c.sliding_window + 1 : 0);
   const int hist = start - h0;
 
+  const Act a_h{S.A, split, n, h};      // normalised rows
+  const Act a_q{S.A, split, n, qd};     // attention output rows
+  const Act act{S.ACT, split, n, f};    // dense SwiGLU activations
+
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerPtrs& L = m.layers[l];
-    k_rmsnorm_rows<TA><<<n, 256, 0, s>>>(S.X, L.attn_norm, c.rms_eps, h, A);
+    k_rmsnorm_rows<<<n, 256, 0, s>>>(S.X, L.attn_norm, c.rms_eps, h, a_h.out());
     count_launch(m);
     KV* kdst = direct ? (KV*)L.kc : (KV*)S.KVlin_k;
     KV* vdst = direct ? (KV*)L.vc : (KV*)S.KVlin_v;
@@ -438,13 +464,9 @@ static void prefill_chunk(const Model& m, cudaStream_t s, int n, int start, floa
       e.v_dst = vdst;
       e.kv_bf16 = std::is_same<KV, __nv_bfloat16>::value;
       e.kv_row0 = direct ? start : hist;
-      timer_begin(m, DEC_K_PF_GEMM, s);
-      gemm<TA, TW>(A, (const TW*)L.wqkv, n, qd + 2 * kd, h, e, 1, n, s, m);
-      timer_end(m, DEC_K_PF_GEMM, s);
+      gemm<TW>(m, s, a_h, (const TW*)L.wqkv, n, qd + 2 * kd, h, e, 1, n);
     }
-    timer_begin(m, DEC_K_PF_ATTN, s);
-    attention<KV, TA>(m, s, kdst, vdst, direct ? 0 : h0, start, n, A);
-    timer_end(m, DEC_K_PF_ATTN, s);
+    attention<KV>(m, s, kdst, vdst, direct ? 0 : h0, start, n, a_q.out());
     if (!direct) {
       const int t_first = n > c.max_seq ? n - c.max_seq : 0;
       k_kv_commit<KV><<<152, 256, 0, s>>>(kdst, vdst, hist, start, t_first, n, c.max_seq, kd, (KV*)L.kc,
@@ -456,56 +478,61 @@ static void prefill_chunk(const Model& m, cudaStream_t s, int n, int start, floa
       e.mode = EPI_RESID;
       e.n_out = h;
       e.out_f32 = S.X;
-      timer_begin(m, DEC_K_PF_GEMM, s);
-      gemm<TA, TW>(A, (const TW*)L.wo, n, h, qd, e, 1, n, s, m);
-      timer_end(m, DEC_K_PF_GEMM, s);
+      gemm<TW>(m, s, a_q, (const TW*)L.wo, n, h, qd, e, 1, n);
     }
     if (c.n_experts == 0) {
-      k_rmsnorm_rows<TA><<<n, 256, 0, s>>>(S.X, L.ffn_norm, c.rms_eps, h, A);
+      k_rmsnorm_rows<<<n, 256, 0, s>>>(S.X, L.ffn_norm, c.rms_eps, h, a_h.out());
       count_launch(m);
       GemmEpi e1{};
       e1.mode = EPI_SWIGLU;
       e1.n_out = 2 * f;
-      e1.act = ACT;
-      e1.act_bf16 = std::is_same<TA, __nv_bfloat16>::value;
-      timer_begin(m, DEC_K_PF_GEMM, s);
-      gemm<TA, TW>(A, (const TW*)L.w_gateup, n, 2 * f, h, e1, 1, n, s, m);
-      timer_end(m, DEC_K_PF_GEMM, s);
+      e1.act = act.base;
+      e1.act_bf16 = split;
+      e1.act_lo = act.out().lo;
+      gemm<TW>(m, s, a_h, (const TW*)L.w_gateup, n, 2 * f, h, e1, 1, n);
       GemmEpi e2{};
       e2.mode = EPI_RESID;
       e2.n_out = h;
       e2.out_f32 = S.X;
-      timer_begin(m, DEC_K_PF_GEMM, s);
-      gemm<TA, TW>(ACT, (const TW*)L.w_down, n, h, f, e2, 1, n, s, m);
-      timer_end(m, DEC_K_PF_GEMM, s);
+      gemm<TW>(m, s, act, (const TW*)L.w_down, n, h, f, e2, 1, n);
     } else {
       const int k = c.n_experts_used, E = c.n_experts, entries = n * k;
+      const Act a_sort{S.Asort, split, entries, h};
+      const Act act_sort{S.ACT, split, entries, f};
       const size_t smr = (64 + MAX_EXPERTS + (size_t)h) * sizeof(float);
       if (smr > 48 * 1024)
         cudaFuncSetAttribute(k_router_rows<TW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smr);
       k_router_rows<TW><<<n, 256, smr, s>>>(S.X, L.ffn_norm, c.rms_eps, (const TW*)L.router, h, E, k, S.pf_ids,
                                             S.pf_wts, start, m.trace_ids, m.trace_logits, m.trace_cap, l);
       k_moe_plan<<<1, 256, 0, s>>>(S.pf_ids, entries, E, S.pf_offset, S.pf_rows, S.pf_inv);
-      k_rmsnorm_rows<TA><<<n, 256, 0, s>>>(S.X, L.ffn_norm, c.rms_eps, h, A);
-      k_gather_rows<TA><<<entries, 128, 0, s>>>(A, S.pf_rows, k, entries, h, (TA*)S.Asort);
-      count_launch(m, 4);
+      k_rmsnorm_rows<<<n, 256, 0, s>>>(S.X, L.ffn_norm, c.rms_eps, h, a_h.out());
+      count_launch(m, 3);
+      if (split) {
+        const int words = h / 2;  // bf16 row of h elements
+        k_gather_rows<<<entries, 128, 0, s>>>((const uint32_t*)a_h.base, S.pf_rows, k, entries, words,
+                                              (uint32_t*)a_sort.base);
+        k_gather_rows<<<entries, 128, 0, s>>>((const uint32_t*)a_h.lo(), S.pf_rows, k, entries, words,
+                                              (uint32_t*)a_sort.lo());
+        count_launch(m, 2);
+      } else {
+        k_gather_rows<<<entries, 128, 0, s>>>((const uint32_t*)a_h.base, S.pf_rows, k, entries, h,
+                                              (uint32_t*)a_sort.base);
+        count_launch(m);
+      }
       GemmEpi e1{};
       e1.mode = EPI_SWIGLU;
       e1.n_out = 2 * f;
-      e1.act = ACT;
-      e1.act_bf16 = std::is_same<TA, __nv_bfloat16>::value;
+      e1.act = act_sort.base;
+      e1.act_bf16 = split;
+      e1.act_lo = act_sort.out().lo;
       e1.group_offset = S.pf_offset;
-      timer_begin(m, DEC_K_PF_GEMM, s);
-      gemm<TA, TW>((const TA*)S.Asort, (const TW*)L.w_gateup, entries, 2 * f, h, e1, E, n, s, m);
-      timer_end(m, DEC_K_PF_GEMM, s);
+      gemm<TW>(m, s, a_sort, (const TW*)L.w_gateup, entries, 2 * f, h, e1, E, n);
       GemmEpi e2{};
       e2.mode = EPI_STORE;
       e2.n_out = h;
       e2.out_f32 = S.Y;
       e2.group_offset = S.pf_offset;
-      timer_begin(m, DEC_K_PF_GEMM, s);
-      gemm<TA, TW>(ACT, (const TW*)L.w_down, entries, h, f, e2, E, n, s, m);
-      timer_end(m, DEC_K_PF_GEMM, s);
+      gemm<TW>(m, s, act_sort, (const TW*)L.w_down, entries, h, f, e2, E, n);
       k_moe_combine<<<n, 256, 0, s>>>(S.Y, S.pf_inv, S.pf_wts, k, h, S.X);
       count_launch(m);
     }

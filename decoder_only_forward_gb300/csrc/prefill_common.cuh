@@ -18,9 +18,11 @@ struct GemmEpi {
   int n_out;            // valid output columns (N)
   // EPI_RESID / EPI_STORE: f32 rows of n_out columns
   float* out_f32;
-  // EPI_SWIGLU: rows of n_out/2 activations, bf16 when act_bf16 else f32
+  // EPI_SWIGLU: rows of n_out/2 activations, bf16 when act_bf16 else f32;
+  // with act_lo set, act holds bf16 hi and act_lo the bf16 remainder (a = hi + lo)
   void* act;
   int act_bf16;
+  __nv_bfloat16* act_lo;
   // EPI_QKV
   const float* bias;      // nullable
   const float2* rope;     // [row][hd/2] (cos, sin) of the row's position
@@ -34,6 +36,23 @@ struct GemmEpi {
   // Grouped (MoE) GEMMs: rows of group g are [offset[g], offset[g] + count[g]).
   const int32_t* group_offset;   // nullable = one group of all rows
 };
+
+// Destination of an activation row buffer: f32, or a bf16 (hi, lo) pair of
+// planes with value = hi + lo (the A operand of the tensor-core GEMMs).
+struct RowOut {
+  void* hi;
+  __nv_bfloat16* lo;
+  int f32;
+};
+__device__ __forceinline__ void row_store(const RowOut& o, size_t i, float v) {
+  if (o.f32) {
+    reinterpret_cast<float*>(o.hi)[i] = v;
+  } else {
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    reinterpret_cast<__nv_bfloat16*>(o.hi)[i] = h;
+    if (o.lo) o.lo[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+  }
+}
 
 template <typename T>
 __device__ __forceinline__ void store_pair(T* p, float a, float b);
@@ -64,8 +83,13 @@ __device__ __forceinline__ void epi_pair(const GemmEpi& e, int row, int col, flo
     case EPI_SWIGLU: {
       const float a = silu_f(v0) * v1;
       const size_t o = (size_t)row * (e.n_out / 2) + (col >> 1);
-      if (e.act_bf16) reinterpret_cast<__nv_bfloat16*>(e.act)[o] = __float2bfloat16_rn(a);
-      else reinterpret_cast<float*>(e.act)[o] = a;
+      if (e.act_bf16) {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(a);
+        reinterpret_cast<__nv_bfloat16*>(e.act)[o] = hi;
+        if (e.act_lo) e.act_lo[o] = __float2bfloat16_rn(a - __bfloat162float(hi));
+      } else {
+        reinterpret_cast<float*>(e.act)[o] = a;
+      }
       break;
     }
     case EPI_QKV: {

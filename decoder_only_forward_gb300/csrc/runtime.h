@@ -156,6 +156,11 @@ struct AttendLayout {
 bool attend_check(const void* q, const void* k, const void* v, const void* out, int nq, int nkv, int hd,
                   int max_seq, int sliding, int kv_dtype, int pos, AttendLayout& lay, const char** why);
 
+// Tensor-core GEMM (gemm_tc.cu); see prefill_common.cuh for GemmEpi.
+struct GemmEpi;
+cudaError_t launch_gemm_tc(const void* a_hi, const void* a_lo, int a_rows, const void* b, int M, int N, int K,
+                           const GemmEpi& e, int groups, int max_rows, DeviceState* st, cudaStream_t s);
+
 // Message returned by dec_last_error(NULL) (api.cu).
 void set_global_error(const char* msg);
 

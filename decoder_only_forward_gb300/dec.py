@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "DEC_OK", 1: "DEC_EINVAL", 2: "DEC_ERANGE", 3: "DEC_ECUDA", 4
 EXPORTED = ["dec_config_validate", "dec_workspace_bytes", "dec_create", "dec_prefill", "dec_decode",
             "dec_decode_dev", "dec_kv_reset", "dec_length", "dec_kv_layer", "dec_set_trace",
             "dec_check", "dec_timing_enable", "dec_timing_read", "dec_launch_count", "dec_destroy",
-            "dec_last_error", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc"]
+            "dec_last_error", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc", "dec_gemm_bf16"]
 
 KERNEL_CLASSES = {"qkv": 1, "attn": 2, "oproj": 3, "gateup": 4, "down": 5, "lmhead": 6, "router": 7,
                   "pf_gemm": 8, "pf_attn": 9}
@@ -76,6 +76,7 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "dec_attend_scratch_bytes": (SZ, [I32, I32, I32, I32]),
         "dec_attend": (I32, [P, P, P, I32, I32, I32, I32, I32, I32, I32, P, P, SZ, P]),
         "dec_attend_noalloc": (I32, [P, P, P, I32, I32, I32, I32, I32, I32, I32, P, P]),
+        "dec_gemm_bf16": (I32, [P, P, P, P, I32, I32, I32, P]),
         "dec_last_error": (ctypes.c_char_p, [P]),
     }
     for name, (res, args) in sig.items():
@@ -140,6 +141,18 @@ def attend(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, pos: int, sliding_
     st = lib.dec_attend(q.data_ptr(), k.data_ptr(), v.data_ptr(), nq, nkv, hd, max_seq, int(sliding_window), kvd,
                         int(pos), out.data_ptr(), scratch.data_ptr(), scratch.numel() * scratch.element_size(),
                         ctypes.c_void_p(s.cuda_stream))
+    if st != DEC_OK:
+        raise DecError(st, lib.dec_last_error(None).decode())
+
+
+def gemm_bf16(a_hi: torch.Tensor, a_lo: Optional[torch.Tensor], b: torch.Tensor, c: torch.Tensor,
+              stream: Optional[torch.cuda.Stream] = None) -> None:
+    """c[m, n] = (a_hi + a_lo) @ b.T on the tensor-core kernel (bf16 in, f32 out)."""
+    m, k = a_hi.shape
+    n = b.shape[0]
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = lib.dec_gemm_bf16(a_hi.data_ptr(), _ptr(a_lo), b.data_ptr(), c.data_ptr(), m, n, k,
+                           ctypes.c_void_p(s.cuda_stream))
     if st != DEC_OK:
         raise DecError(st, lib.dec_last_error(None).decode())
 

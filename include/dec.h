@@ -217,6 +217,16 @@ dec_status dec_attend(const float *q, const void *k, const void *v, int32_t n_he
                       int32_t head_dim, int32_t max_seq, int32_t sliding_window, int32_t kv_dtype,
                       int32_t pos, float *out, void *scratch, size_t scratch_bytes, void *cuda_stream);
 
+/* C = (A_hi + A_lo) . B^T on the tensor cores: the projection GEMM of the
+ * prefill path (tcgen05, TMA, f32 accumulation in TMEM), callable alone.
+ *   a_hi, a_lo: device [m][k] bf16 (a_lo may be NULL: A = A_hi); the pair
+ *   carries an f32 activation as hi + lo.  b: device [n][k] bf16 (weights,
+ *   row-major [out, in]).  c: device [m][n] f32.  k a multiple of 8, n even,
+ *   operands 16-byte aligned.  Enqueued on cuda_stream.
+ * Errors: DEC_EINVAL, DEC_ECUDA (messages via dec_last_error(NULL)). */
+dec_status dec_gemm_bf16(const void *a_hi, const void *a_lo, const void *b, float *c, int32_t m, int32_t n,
+                         int32_t k, void *cuda_stream);
+
 /* dec_attend for callers that cannot allocate device memory (a plug-in whose
  * host framework's pooled allocator already owns the GPU's memory, or a
  * latency-critical path where cudaMalloc may not be called).  The pages have

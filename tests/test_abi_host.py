@@ -25,7 +25,7 @@ def dec():
 def _declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(dec_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(dec_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_functions_all_exported(dec):
