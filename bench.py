@@ -329,6 +329,28 @@ def run_ours(args, rank, world, local_rank):
     return out
 
 
+def run_profile(args):
+    """A small fixed sequence for per-kernel profilers: prefill P + D decode steps."""
+    from decoder_only_forward_gb300 import build as dec_build
+    dec_build.build()
+    from decoder_only_forward_gb300 import dec
+    w = synthetic.workload(args.workload)
+    if args.prompt:
+        w["prompt"] = args.prompt
+    d = dec.Decoder(w, kv_dtype=args.kv)
+    d.set_graph(False)
+    P = w["prompt"]
+    logits = torch.empty(w["vocab"], dtype=torch.float32, device="cuda")
+    tok = torch.empty(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    d.prefill(synthetic.prompt_tokens(w, P, seed=0), 0, logits, tok)
+    for i in range(args.profile):
+        d.decode_dev(tok, P + i, logits, tok)
+    d.check()
+    print(f"profile run: {args.workload} prefill {P} + decode {args.profile}, {d.launch_count} kernel launches")
+    d.close()
+
+
 # ---------------------------------------------------------------- reference arm (oracle)
 def run_reference(args):
     w = synthetic.workload(args.workload)
@@ -363,13 +385,20 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="smollm2-135m", choices=sorted(synthetic.WORKLOADS))
     ap.add_argument("--kv", default="f32", choices=["f32", "bf16"])
+    ap.add_argument("--prompt", type=int, default=0, help="override the prompt length (profiling only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", type=int, default=0, metavar="D",
+                    help="profiling driver: one prefill + D decode steps, kernels launched one by one "
+                         "(no graph, no timing passes, no JSON); for per-kernel profilers")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.profile:
+        run_profile(args)
+        return
     if args.impl == "reference":
         if rank != 0:
             return

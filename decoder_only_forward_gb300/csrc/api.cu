@@ -27,6 +27,7 @@ struct dec_handle {
   int64_t launches = 0;
   Timing timing;
   std::vector<cudaEvent_t> events;
+  bool use_graph = true;
 };
 
 static void timing_start(dec_handle* h) { h->timing.n = 0; }
@@ -340,7 +341,7 @@ dec_status dec_prefill(dec_handle* h, const int32_t* tokens, int32_t n, int32_t 
 }
 
 static dec_status run_decode_body(dec_handle* h, float* logits, int32_t* d_argmax) {
-  if (h->stream == nullptr) {
+  if (h->stream == nullptr || !h->use_graph) {
     timing_start(h);
     launch_decode_body(h->m, h->stream, logits, d_argmax);
     timing_finish(h);
@@ -415,6 +416,16 @@ dec_status dec_kv_reset(dec_handle* h) {
 int32_t dec_length(const dec_handle* h) { return h ? h->len : -1; }
 
 int64_t dec_launch_count(const dec_handle* h) { return h ? h->launches : -1; }
+
+dec_status dec_set_graph(dec_handle* h, int32_t enable) {
+  if (!h) return DEC_EINVAL;
+  h->use_graph = enable != 0;
+  if (h->graph) {
+    cudaGraphExecDestroy(h->graph);
+    h->graph = nullptr;
+  }
+  return DEC_OK;
+}
 
 dec_status dec_kv_layer(const dec_handle* h, int32_t layer, void** k, void** v) {
   if (!h || !k || !v || layer < 0 || layer >= h->m.cfg.n_layers) return DEC_EINVAL;

@@ -167,6 +167,11 @@ dec_status dec_kv_layer(const dec_handle *h, int32_t layer, void **k, void **v);
  * Buffers are device memory owned by the caller. */
 dec_status dec_set_trace(dec_handle *h, int32_t *d_ids, float *d_logits, int32_t capacity);
 
+/* Decode steps run as one captured CUDA graph by default (when the handle's
+ * stream is not the legacy default stream).  enable = 0 launches the kernels
+ * one by one instead (e.g. under a per-kernel profiler). */
+dec_status dec_set_graph(dec_handle *h, int32_t enable);
+
 /* Number of kernels this handle has launched so far (graph launches count
  * every kernel node), for measurement. */
 int64_t dec_launch_count(const dec_handle *h);
