@@ -20,6 +20,8 @@ struct dec_handle {
   std::string err;
   // decode graph, captured for one (logits, d_argmax) pair
   cudaGraphExec_t graph = nullptr;
+  cudaGraph_t graph_src = nullptr;        // kept for the setup node's parameter updates
+  cudaGraphNode_t graph_step_node = nullptr;
   float* graph_logits = nullptr;
   int32_t* graph_argmax = nullptr;
   int graph_timed_pairs = 0;
@@ -29,6 +31,14 @@ struct dec_handle {
   std::vector<cudaEvent_t> events;
   bool use_graph = true;
 };
+
+static void drop_graph(dec_handle* h) {
+  if (h->graph) cudaGraphExecDestroy(h->graph);
+  if (h->graph_src) cudaGraphDestroy(h->graph_src);
+  h->graph = nullptr;
+  h->graph_src = nullptr;
+  h->graph_step_node = nullptr;
+}
 
 static void timing_start(dec_handle* h) { h->timing.n = 0; }
 static void timing_finish(dec_handle* h) { h->timing.n_done = h->timing.n; }
@@ -100,11 +110,12 @@ WsPlan dec::plan_workspace(const dec_config& c) {
   p.max_tokens = T;
   const int hd = c.head_dim, qd = c.n_heads * hd, kd = c.n_kv_heads * hd;
   const int k = c.n_experts ? c.n_experts_used : 1;
-  int nsplit = (c.max_seq + 127) / 128;
-  const int cap = (2 * 152) / c.n_kv_heads;
-  if (nsplit > cap) nsplit = cap;
-  if (nsplit > 64) nsplit = 64;
-  if (nsplit < 1) nsplit = 1;
+  // Decode attention: split s owns slots [s*sps, (s+1)*sps), sps a multiple
+  // of 64 keys, at most 64 splits per kv head.
+  const int chunks = (c.max_seq + 63) / 64;
+  const int per = (chunks + 63) / 64;
+  p.attn_sps = 64 * per;
+  const int nsplit = (c.max_seq + p.attn_sps - 1) / p.attn_sps;
   p.nsplit = nsplit;
   const size_t ws = dsize(c.weight_dtype), ks = dsize(c.kv_dtype);
   const size_t a_elem = 4;  // prefill activation rows: f32 (or a bf16 hi/lo pair of the same size)
@@ -204,6 +215,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
   m.ws = workspace;
   m.ws_bytes = workspace_bytes;
   m.nsplit = p.nsplit;
+  m.attn_sps = p.attn_sps;
   int lg = (cfg->vocab / 2 + 7) / 8;
   m.lm_grid = lg < 1 ? 1 : (lg > LM_GRID_MAX ? LM_GRID_MAX : lg);
   m.tok_embd = w->tok_embd;
@@ -340,36 +352,68 @@ dec_status dec_prefill(dec_handle* h, const int32_t* tokens, int32_t n, int32_t 
   return DEC_OK;
 }
 
-static dec_status run_decode_body(dec_handle* h, float* logits, int32_t* d_argmax) {
+// Points the captured step-setup node at this step's token and position.
+static cudaError_t set_step_node(dec_handle* h, const int32_t* d_token, int32_t token, int32_t pos) {
+  DeviceState* st = h->m.s.st;
+  int32_t vocab = h->m.cfg.vocab;
+  const double* inv = h->m.s.inv_freq;
+  int half = h->m.cfg.head_dim / 2;
+  float2* tab = h->m.s.rope_tab;
+  void* args[] = {&st, &d_token, &token, &pos, &vocab, &inv, &half, &tab};
+  cudaKernelNodeParams p = {};
+  p.func = const_cast<void*>(set_step_kernel());
+  p.gridDim = dim3(1);
+  p.blockDim = dim3(128);
+  p.sharedMemBytes = 0;
+  p.kernelParams = args;
+  p.extra = nullptr;
+  return cudaGraphExecKernelNodeSetParams(h->graph, h->graph_step_node, &p);
+}
+
+// One decode step.  On a non-default stream the whole step (setup, every layer,
+// head) is one CUDA graph, captured once per (logits, argmax) pair; per step
+// only the setup node's token/position change.
+static dec_status run_decode_step(dec_handle* h, const int32_t* d_token, int32_t token, int32_t pos,
+                                  float* logits, int32_t* d_argmax) {
   if (h->stream == nullptr || !h->use_graph) {
     timing_start(h);
-    launch_decode_body(h->m, h->stream, logits, d_argmax);
+    launch_decode_body(h->m, h->stream, d_token, token, pos, logits, d_argmax);
     timing_finish(h);
     return cuda_check(h, "decode launch");
   }
   if (!h->graph || h->graph_logits != logits || h->graph_argmax != d_argmax) {
-    if (h->graph) {
-      cudaGraphExecDestroy(h->graph);
-      h->graph = nullptr;
-    }
-    cudaGraph_t g;
+    drop_graph(h);
     cudaError_t e = cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeRelaxed);
     if (e != cudaSuccess) return fail(h, DEC_ECUDA, "begin capture: %s", cudaGetErrorString(e));
     timing_start(h);
     const int64_t before = h->launches;
-    launch_decode_body(h->m, h->stream, logits, d_argmax);
+    launch_decode_body(h->m, h->stream, d_token, token, pos, logits, d_argmax);
     h->graph_kernels = h->launches - before;
     h->launches = before;
     h->graph_timed_pairs = h->timing.n;
+    cudaGraph_t g = nullptr;
     e = cudaStreamEndCapture(h->stream, &g);
     if (e != cudaSuccess) return fail(h, DEC_ECUDA, "end capture: %s", cudaGetErrorString(e));
+    h->graph_src = g;
+    cudaGraphNode_t roots[4];
+    size_t nroots = 4;
+    e = cudaGraphGetRootNodes(g, roots, &nroots);
+    if (e != cudaSuccess || nroots != 1) {
+      drop_graph(h);
+      return fail(h, DEC_ECUDA, "decode graph: expected one root node (%s)", cudaGetErrorString(e));
+    }
+    h->graph_step_node = roots[0];
     e = cudaGraphInstantiate(&h->graph, g, 0);
-    cudaGraphDestroy(g);
-    if (e != cudaSuccess) return fail(h, DEC_ECUDA, "graph instantiate: %s", cudaGetErrorString(e));
+    if (e != cudaSuccess) {
+      drop_graph(h);
+      return fail(h, DEC_ECUDA, "graph instantiate: %s", cudaGetErrorString(e));
+    }
     h->graph_logits = logits;
     h->graph_argmax = d_argmax;
   }
-  cudaError_t e = cudaGraphLaunch(h->graph, h->stream);
+  cudaError_t e = set_step_node(h, d_token, token, pos);
+  if (e != cudaSuccess) return fail(h, DEC_ECUDA, "graph step update: %s", cudaGetErrorString(e));
+  e = cudaGraphLaunch(h->graph, h->stream);
   if (e != cudaSuccess) return fail(h, DEC_ECUDA, "graph launch: %s", cudaGetErrorString(e));
   h->timing.n = h->graph_timed_pairs;
   h->launches += h->graph_kernels;
@@ -383,10 +427,7 @@ dec_status dec_decode(dec_handle* h, int32_t token, int32_t pos, float* logits) 
   if (st != DEC_OK) return st;
   if (token < 0 || token >= h->m.cfg.vocab)
     return fail(h, DEC_EINVAL, "token %d outside [0, %d)", token, h->m.cfg.vocab);
-  launch_set_step(h->m, h->stream, nullptr, token, pos);
-  st = cuda_check(h, "decode launch");
-  if (st != DEC_OK) return st;
-  st = run_decode_body(h, logits, nullptr);
+  st = run_decode_step(h, nullptr, token, pos, logits, nullptr);
   if (st != DEC_OK) return st;
   h->len = pos + 1;
   return DEC_OK;
@@ -398,10 +439,7 @@ dec_status dec_decode_dev(dec_handle* h, const int32_t* d_token, int32_t pos, fl
   if (!d_token) return fail(h, DEC_EINVAL, "d_token is NULL");
   dec_status st = check_positions(h, 1, pos);
   if (st != DEC_OK) return st;
-  launch_set_step(h->m, h->stream, d_token, 0, pos);
-  st = cuda_check(h, "decode launch");
-  if (st != DEC_OK) return st;
-  st = run_decode_body(h, logits, d_argmax);
+  st = run_decode_step(h, d_token, 0, pos, logits, d_argmax);
   if (st != DEC_OK) return st;
   h->len = pos + 1;
   return DEC_OK;
@@ -420,10 +458,7 @@ int64_t dec_launch_count(const dec_handle* h) { return h ? h->launches : -1; }
 dec_status dec_set_graph(dec_handle* h, int32_t enable) {
   if (!h) return DEC_EINVAL;
   h->use_graph = enable != 0;
-  if (h->graph) {
-    cudaGraphExecDestroy(h->graph);
-    h->graph = nullptr;
-  }
+  drop_graph(h);
   return DEC_OK;
 }
 
@@ -441,10 +476,7 @@ dec_status dec_set_trace(dec_handle* h, int32_t* d_ids, float* d_logits, int32_t
   h->m.trace_ids = d_ids;
   h->m.trace_logits = d_logits;
   h->m.trace_cap = d_ids ? capacity : 1;
-  if (h->graph) {  // the captured graph holds the old trace pointers
-    cudaGraphExecDestroy(h->graph);
-    h->graph = nullptr;
-  }
+  drop_graph(h);  // the captured graph holds the old trace pointers
   return DEC_OK;
 }
 
@@ -482,10 +514,7 @@ dec_status dec_timing_enable(dec_handle* h, int32_t kernel_class, int32_t max_la
     h->timing.max = max_launches;
     h->timing.ev = h->events.data();
   }
-  if (h->graph) {
-    cudaGraphExecDestroy(h->graph);
-    h->graph = nullptr;
-  }
+  drop_graph(h);
   return DEC_OK;
 }
 
@@ -507,7 +536,7 @@ dec_status dec_timing_read(dec_handle* h, float* total_ms, int32_t* launches) {
 
 void dec_destroy(dec_handle* h) {
   if (!h) return;
-  if (h->graph) cudaGraphExecDestroy(h->graph);
+  drop_graph(h);
   for (cudaEvent_t ev : h->events) cudaEventDestroy(ev);
   delete h;
 }

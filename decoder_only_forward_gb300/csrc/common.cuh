@@ -84,6 +84,23 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Spin budget of every bounded device wait: about two seconds.
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while its predecessor still runs.  Everything
+// before pdl_wait() must touch only data no in-flight kernel writes (weights,
+// KV of earlier steps); pdl_wait() returns once the predecessor grid has
+// completed and its writes are visible.  Without the launch attribute both
+// are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// 16-byte asynchronous global -> shared copies (L2 only).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ void raise_error(DeviceState* st, unsigned bits, unsigned where) {
   if (atomicOr(&st->err, bits) == 0u) st->where = where;
 }

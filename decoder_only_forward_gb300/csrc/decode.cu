@@ -43,16 +43,14 @@ __device__ void block_copy_to_smem(const float* __restrict__ x, int K, float* xs
   __syncthreads();
 }
 
-// Dot products of two weight rows with the smem vector xs, one warp; the
-// sums end up in every lane.  K * sizeof(W) is a multiple of 16 bytes.
+// Partial dot products of two weight rows with the smem vector xs over the
+// chunks c = c0, c0+32, ... (c0 = lane + 32*i0); K * sizeof(W) is a multiple
+// of 16 bytes.  Accumulates into a0, a1 (no reduction).
 template <typename W>
-__device__ __forceinline__ void warp_dot2(const W* __restrict__ r0, const W* __restrict__ r1,
-                                          const float* __restrict__ xs, int K, float& s0, float& s1) {
+__device__ __forceinline__ void warp_dot2_acc(const W* __restrict__ r0, const W* __restrict__ r1,
+                                              const float* __restrict__ xs, int K, int c, float& a0, float& a1) {
   constexpr int V = Chunk<W>::N;
   const int nch = K / V;
-  const int lane = threadIdx.x & 31;
-  float a0 = 0.f, a1 = 0.f;
-  int c = lane;
   for (; c + 96 < nch; c += 128) {
     uint4 u0[4], u1[4];
 #pragma unroll
@@ -86,6 +84,64 @@ __device__ __forceinline__ void warp_dot2(const W* __restrict__ r0, const W* __r
       a1 = fmaf(w1[e], xv[e], a1);
     }
   }
+}
+
+// Dot products of two weight rows with xs, one warp; sums in every lane.
+template <typename W>
+__device__ __forceinline__ void warp_dot2(const W* __restrict__ r0, const W* __restrict__ r1,
+                                          const float* __restrict__ xs, int K, float& s0, float& s1) {
+  float a0 = 0.f, a1 = 0.f;
+  warp_dot2_acc(r0, r1, xs, K, threadIdx.x & 31, a0, a1);
+  s0 = warp_sum(a0);
+  s1 = warp_sum(a1);
+}
+
+// The first PF chunks per lane of a warp's first row pair, loaded before the
+// kernel waits on its predecessor (weights are never written, so this overlaps
+// the previous kernel).
+constexpr int PF = 4;
+struct RowPf {
+  uint4 a[PF], b[PF];
+};
+
+template <typename W>
+__device__ __forceinline__ void prefetch_pair(const W* __restrict__ r0, const W* __restrict__ r1, int K, RowPf& pf) {
+  constexpr int V = Chunk<W>::N;
+  const int nch = K / V, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < PF; ++i) {
+    const int c = lane + 32 * i;
+    if (c < nch) {
+      pf.a[i] = ld_stream16(r0 + (size_t)c * V);
+      pf.b[i] = ld_stream16(r1 + (size_t)c * V);
+    }
+  }
+}
+
+// warp_dot2 whose first PF chunks per lane come from a prefetch.
+template <typename W>
+__device__ __forceinline__ void warp_dot2_pf(const W* __restrict__ r0, const W* __restrict__ r1,
+                                             const float* __restrict__ xs, int K, const RowPf& pf, float& s0,
+                                             float& s1) {
+  constexpr int V = Chunk<W>::N;
+  const int nch = K / V, lane = threadIdx.x & 31;
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < PF; ++i) {
+    const int c = lane + 32 * i;
+    if (c < nch) {
+      float w0[V], w1[V];
+      Chunk<W>::widen(pf.a[i], w0);
+      Chunk<W>::widen(pf.b[i], w1);
+      const float* xv = xs + c * V;
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        a0 = fmaf(w0[e], xv[e], a0);
+        a1 = fmaf(w1[e], xv[e], a1);
+      }
+    }
+  }
+  warp_dot2_acc(r0, r1, xs, K, lane + 32 * PF, a0, a1);
   s0 = warp_sum(a0);
   s1 = warp_sum(a1);
 }
@@ -96,6 +152,7 @@ __device__ __forceinline__ void warp_dot2(const W* __restrict__ r0, const W* __r
 __global__ void k_set_step(DeviceState* st, const int32_t* d_token, int32_t token, int32_t pos,
                            int32_t vocab, const double* __restrict__ inv_freq, int half,
                            float2* __restrict__ rope_tab) {
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     int t = d_token ? *d_token : token;
     if (t < 0 || t >= vocab) {
@@ -112,14 +169,6 @@ __global__ void k_set_step(DeviceState* st, const int32_t* d_token, int32_t toke
   }
 }
 
-template <typename W>
-__global__ void k_embed_step(const W* __restrict__ E, int h, const DeviceState* __restrict__ st,
-                             float* __restrict__ x) {
-  const W* row = E + (size_t)st->token * h;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < h; i += gridDim.x * blockDim.x)
-    x[i] = to_f32(row[i]);
-}
-
 // ---------------------------------------------------------------------------
 // Fused RMSNorm -> [q;k;v] = Wqkv n (+b) -> RoPE on q,k -> K/V written at the
 // slot of pos.  A warp owns rows (2i, 2i+1), so the rotation of the pair is
@@ -127,22 +176,41 @@ __global__ void k_embed_step(const W* __restrict__ E, int h, const DeviceState* 
 
 template <typename W, typename KV>
 __global__ void __launch_bounds__(GEMV_THREADS) k_norm_qkv(
-    const float* __restrict__ x, const float* __restrict__ nw, float eps,
-    const W* __restrict__ wqkv, const float* __restrict__ bqkv, int K, int qd, int kd, int hd,
-    const float2* __restrict__ rope_tab, const DeviceState* __restrict__ st, int max_seq,
+    const float* __restrict__ x, const W* __restrict__ embed, float* __restrict__ x_out,
+    const float* __restrict__ nw, float eps, const W* __restrict__ wqkv, const float* __restrict__ bqkv, int K,
+    int qd, int kd, int hd, const float2* __restrict__ rope_tab, const DeviceState* __restrict__ st, int max_seq,
     int sliding, float* __restrict__ q_out, KV* __restrict__ kc, KV* __restrict__ vc) {
   extern __shared__ float sm[];
   float* red = sm;
   float* xs = sm + 64;
-  block_rmsnorm_to_smem(x, nw, K, eps, xs, red);
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int npairs = (qd + 2 * kd) / 2;
+  const int p0 = blockIdx.x * GEMV_WARPS + warp;
+  RowPf pf;
+  if (p0 < npairs) prefetch_pair(wqkv + (size_t)2 * p0 * K, wqkv + (size_t)(2 * p0 + 1) * K, K, pf);
+  pdl_wait();
+  if (embed) {
+    // First layer: the residual starts as the token's embedding row (Pantheon
+    // Forward Pass Flow, embed); CTA 0 stores it for the later kernels.
+    const W* row = embed + (size_t)st->token * K;
+    float* xe = xs;  // staged in xs, then normalised in place below
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+      const float v = to_f32(row[k]);
+      xe[k] = v;
+      if (blockIdx.x == 0) x_out[k] = v;
+    }
+    __syncthreads();
+    x = xe;
+  }
+  block_rmsnorm_to_smem(x, nw, K, eps, xs, red);
   const int pos = st->pos;
   const int slot = sliding > 0 ? pos % max_seq : pos;
-  for (int p = blockIdx.x * GEMV_WARPS + warp; p < npairs; p += gridDim.x * GEMV_WARPS) {
+  for (int p = p0; p < npairs; p += gridDim.x * GEMV_WARPS) {
     const int r = 2 * p;
     float a0, a1;
-    warp_dot2(wqkv + (size_t)r * K, wqkv + (size_t)(r + 1) * K, xs, K, a0, a1);
+    if (p == p0) warp_dot2_pf(wqkv + (size_t)r * K, wqkv + (size_t)(r + 1) * K, xs, K, pf, a0, a1);
+    else warp_dot2(wqkv + (size_t)r * K, wqkv + (size_t)(r + 1) * K, xs, K, a0, a1);
     if (lane == 0) {
       if (bqkv) {
         a0 += bqkv[r];
@@ -185,16 +253,23 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gateup(
   extern __shared__ float sm[];
   float* red = sm;
   float* xs = sm + 64;
-  if (nvec) block_copy_to_smem(nvec, K, xs);
-  else block_rmsnorm_to_smem(x, nw, K, eps, xs, red);
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ntask = nslots * f;
-  for (int p = blockIdx.x * GEMV_WARPS + warp; p < ntask; p += gridDim.x * GEMV_WARPS) {
+  const int p0 = blockIdx.x * GEMV_WARPS + warp;
+  RowPf pf;
+  const bool pre = ids == nullptr && p0 < ntask;   // expert rows are known only after the router
+  if (pre) prefetch_pair(wgu + (size_t)2 * p0 * K, wgu + (size_t)(2 * p0 + 1) * K, K, pf);
+  pdl_wait();
+  if (nvec) block_copy_to_smem(nvec, K, xs);
+  else block_rmsnorm_to_smem(x, nw, K, eps, xs, red);
+  for (int p = p0; p < ntask; p += gridDim.x * GEMV_WARPS) {
     const int slot = p / f, j = p - slot * f;
     const size_t e = ids ? (size_t)ids[slot] : 0;
     const W* base = wgu + e * (size_t)2 * f * K + (size_t)2 * j * K;
     float g, u;
-    warp_dot2(base, base + K, xs, K, g, u);
+    if (pre && p == p0) warp_dot2_pf(base, base + K, xs, K, pf, g, u);
+    else warp_dot2(base, base + K, xs, K, g, u);
     if (lane == 0) act[(size_t)slot * f + j] = silu_f(g) * u;
   }
 }
@@ -210,10 +285,16 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv_accum(
     float* __restrict__ x) {
   extern __shared__ float sm[];
   float* xs = sm + 64;
-  block_copy_to_smem(v, K * nslots, xs);
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int npairs = (N + 1) / 2;
-  for (int p = blockIdx.x * GEMV_WARPS + warp; p < npairs; p += gridDim.x * GEMV_WARPS) {
+  const int p0 = blockIdx.x * GEMV_WARPS + warp;
+  RowPf pf;
+  const bool pre = ids == nullptr && nslots == 1 && p0 < npairs;
+  if (pre) prefetch_pair(w + (size_t)2 * p0 * K, w + (size_t)min(2 * p0 + 1, N - 1) * K, K, pf);
+  pdl_wait();
+  block_copy_to_smem(v, K * nslots, xs);
+  for (int p = p0; p < npairs; p += gridDim.x * GEMV_WARPS) {
     const int r0 = 2 * p;
     const int r1 = min(r0 + 1, N - 1);
     float o0 = 0.f, o1 = 0.f;
@@ -221,7 +302,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv_accum(
       const size_t e = ids ? (size_t)ids[s] : 0;
       const W* base = w + e * (size_t)N * K;
       float a0, a1;
-      warp_dot2(base + (size_t)r0 * K, base + (size_t)r1 * K, xs + (size_t)s * K, K, a0, a1);
+      if (pre && p == p0) warp_dot2_pf(base + (size_t)r0 * K, base + (size_t)r1 * K, xs, K, pf, a0, a1);
+      else warp_dot2(base + (size_t)r0 * K, base + (size_t)r1 * K, xs + (size_t)s * K, K, a0, a1);
       const float ws = wts ? wts[s] : 1.0f;
       o0 = fmaf(ws, a0, o0);
       o1 = fmaf(ws, a1, o1);
@@ -250,6 +332,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_moe_router(
   float* red = sm;
   float* logits = sm + 64;               // [E] (E <= 256 -> fits in the 64+256 header)
   float* xs = sm + 64 + MAX_EXPERTS;
+  pdl_launch_dependents();
+  pdl_wait();
   block_rmsnorm_to_smem(x, nw, K, eps, xs, red);
   for (int i = threadIdx.x; i < K; i += blockDim.x) nvec[i] = xs[i];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -435,6 +519,193 @@ __global__ void __launch_bounds__(FD_THREADS) k_flash_decode(
 }
 
 // ---------------------------------------------------------------------------
+// Decode attention with the KV history prefetched before the dependency wait.
+// CTA (g, split) owns the fixed slot range [split*sps, split*sps + sps) of kv
+// head g, processed in chunks of AD_KS keys.  Before pdl_wait() it starts
+// cp.async copies of the first chunk's slots that earlier steps wrote (bounded
+// by the position recorded so far, a hint that can only be one step stale);
+// after the wait it copies what is missing plus the current position's slot
+// (written by the preceding QKV kernel), then scores, online softmax and the
+// weighted sum of V (rml Attend).  The last CTA of a kv head merges the
+// per-split (max, sum, output) triples in split order.
+
+constexpr int AD_THREADS = 128;
+constexpr int AD_KS = 64;
+
+template <typename KV, int HD>
+struct AdLayout {
+  static constexpr int CE = 16 / sizeof(KV);   // elements per 16-byte chunk
+  static constexpr int KROW = HD + CE;         // padded K row (keeps 16-byte alignment)
+  static constexpr int CPR = HD / CE;          // chunks per row
+  static size_t bytes(int G) {
+    return sizeof(KV) * (size_t)AD_KS * (KROW + HD) + sizeof(float) * ((size_t)G * HD + (size_t)G * AD_KS) + 16;
+  }
+};
+
+template <typename KV, int HD>
+__global__ void __launch_bounds__(AD_THREADS) k_attn_decode(
+    const float* __restrict__ q, const KV* __restrict__ kc, const KV* __restrict__ vc, int nq, int nkv,
+    int max_seq, int sliding, int sps, DeviceState* __restrict__ st, float* __restrict__ part,
+    float* __restrict__ out) {
+  using L = AdLayout<KV, HD>;
+  constexpr int OUTS = (MAX_GROUP * HD + AD_THREADS - 1) / AD_THREADS;
+  extern __shared__ __align__(16) uint8_t ad_smem[];
+  const int G = nq / nkv;
+  KV* ks = reinterpret_cast<KV*>(ad_smem);
+  KV* vs = ks + AD_KS * L::KROW;
+  float* qs = reinterpret_cast<float*>(vs + AD_KS * HD);
+  float* ps = qs + G * HD;
+  __shared__ float mrow[MAX_GROUP], lrow[MAX_GROUP], alpha[MAX_GROUP];
+  __shared__ int is_last;
+
+  pdl_launch_dependents();
+  const int g = blockIdx.x, split = blockIdx.y, nsplit = gridDim.y;
+  const int kd = nkv * HD, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int s0 = split * sps, s1 = min(s0 + sps, max_seq);
+
+  // Prefetch (before the wait): slots below the readable count of the last
+  // recorded position.  Only ever-written slots of earlier steps are read.
+  const int hint = *reinterpret_cast<volatile const int*>(&st->pos);
+  const int m_hint = hint < 0 ? 0 : (sliding > 0 ? min(hint + 1, max_seq) : min(hint + 1, max_seq));
+  const int pre_end = max(s0, min(min(s0 + AD_KS, s1), m_hint));
+  for (int i = tid; i < (pre_end - s0) * L::CPR; i += AD_THREADS) {
+    const int r = i / L::CPR, c = i % L::CPR;
+    const size_t go = (size_t)(s0 + r) * kd + (size_t)g * HD + c * L::CE;
+    cp_async16(ks + r * L::KROW + c * L::CE, kc + go);
+    cp_async16(vs + r * HD + c * L::CE, vc + go);
+  }
+  cp_async_commit();
+  pdl_wait();
+  cp_async_wait_all();
+
+  const int pos = st->pos;
+  const int m = sliding > 0 ? min(pos + 1, max_seq) : pos + 1;
+  const int cur = sliding > 0 ? pos % max_seq : pos;
+  const int j1 = min(s1, m);
+  const float scale = 1.0f / sqrtf((float)HD);
+  for (int i = tid; i < G * HD; i += AD_THREADS) qs[i] = q[(size_t)g * G * HD + i] * scale;
+  if (tid < MAX_GROUP) {
+    mrow[tid] = -INFINITY;
+    lrow[tid] = 0.f;
+  }
+  float acc[OUTS];
+#pragma unroll
+  for (int r = 0; r < OUTS; ++r) acc[r] = 0.f;
+
+  for (int c0 = s0; c0 < j1; c0 += AD_KS) {
+    const int nt = min(AD_KS, j1 - c0);
+    const int have = c0 == s0 ? min(pre_end - s0, nt) : 0;
+    if (c0 != s0) __syncthreads();   // the previous chunk's readers are done
+    for (int i = tid; i < (nt - have) * L::CPR; i += AD_THREADS) {
+      const int r = have + i / L::CPR, c = i % L::CPR;
+      const size_t go = (size_t)(c0 + r) * kd + (size_t)g * HD + c * L::CE;
+      cp_async16(ks + r * L::KROW + c * L::CE, kc + go);
+      cp_async16(vs + r * HD + c * L::CE, vc + go);
+    }
+    if (cur >= c0 && cur - c0 < have) {   // the current slot was prefetched before it was written
+      const int r = cur - c0;
+      for (int c = tid; c < L::CPR; c += AD_THREADS) {
+        const size_t go = (size_t)cur * kd + (size_t)g * HD + c * L::CE;
+        cp_async16(ks + r * L::KROW + c * L::CE, kc + go);
+        cp_async16(vs + r * HD + c * L::CE, vc + go);
+      }
+    }
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    for (int idx = tid; idx < G * nt; idx += AD_THREADS) {
+      const int hh = idx / nt, j = idx - hh * nt;
+      const float* qv = qs + hh * HD;
+      const KV* kr = ks + j * L::KROW;
+      float sdot = 0.f;
+#pragma unroll 8
+      for (int d = 0; d < HD; ++d) sdot = fmaf(qv[d], to_f32(kr[d]), sdot);
+      ps[hh * AD_KS + j] = sdot;
+    }
+    __syncthreads();
+    for (int hh = warp; hh < G; hh += AD_THREADS / 32) {
+      float* pr = ps + hh * AD_KS;
+      const float sa = lane < nt ? pr[lane] : -INFINITY;
+      const float sb = lane + 32 < nt ? pr[lane + 32] : -INFINITY;
+      const float mnew = fmaxf(mrow[hh], warp_max(fmaxf(sa, sb)));
+      const float pa = lane < nt ? __expf(sa - mnew) : 0.f;
+      const float pb = lane + 32 < nt ? __expf(sb - mnew) : 0.f;
+      const float psum = warp_sum(pa + pb);
+      if (lane < nt) pr[lane] = pa;
+      if (lane + 32 < nt) pr[lane + 32] = pb;
+      __syncwarp();
+      if (lane == 0) {
+        const float a = __expf(mrow[hh] - mnew);
+        alpha[hh] = a;
+        lrow[hh] = lrow[hh] * a + psum;
+        mrow[hh] = mnew;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < OUTS; ++r) {
+      const int idx = tid + r * AD_THREADS;
+      if (idx < G * HD) {
+        const int hh = idx / HD, d = idx - hh * HD;
+        const float* pr = ps + hh * AD_KS;
+        float o = acc[r] * alpha[hh];
+        for (int j = 0; j < nt; ++j) o = fmaf(pr[j], to_f32(vs[j * HD + d]), o);
+        acc[r] = o;
+      }
+    }
+  }
+  __syncthreads();
+
+  if (nsplit == 1) {
+#pragma unroll
+    for (int r = 0; r < OUTS; ++r) {
+      const int idx = tid + r * AD_THREADS;
+      if (idx < G * HD) out[(size_t)g * G * HD + idx] = acc[r] / lrow[idx / HD];
+    }
+    return;
+  }
+#pragma unroll
+  for (int r = 0; r < OUTS; ++r) {
+    const int idx = tid + r * AD_THREADS;
+    if (idx < G * HD) {
+      const int hh = idx / HD, d = idx - hh * HD;
+      part[((size_t)(g * G + hh) * nsplit + split) * (HD + 2) + d] = acc[r];
+    }
+  }
+  if (tid < G) {
+    float* pp = part + ((size_t)(g * G + tid) * nsplit + split) * (HD + 2);
+    pp[HD] = mrow[tid];
+    pp[HD + 1] = lrow[tid];
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned prev = atomicAdd(&st->counters[CNT_ATTN + g], 1u);
+    is_last = (prev == (unsigned)nsplit - 1);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  for (int idx = tid; idx < G * HD; idx += AD_THREADS) {
+    const int hh = idx / HD, d = idx - hh * HD;
+    const float* base = part + (size_t)(g * G + hh) * nsplit * (HD + 2);
+    float M = -INFINITY;
+    for (int s2 = 0; s2 < nsplit; ++s2) M = fmaxf(M, __ldcg(base + s2 * (HD + 2) + HD));
+    float Lsum = 0.f, o = 0.f;
+    for (int s2 = 0; s2 < nsplit; ++s2) {
+      const float* pp = base + s2 * (HD + 2);
+      const float ms = __ldcg(pp + HD);
+      if (ms == -INFINITY) continue;
+      const float sc = __expf(ms - M);
+      Lsum = fmaf(__ldcg(pp + HD + 1), sc, Lsum);
+      o = fmaf(__ldcg(pp + d), sc, o);
+    }
+    out[(size_t)(g * G + hh) * HD + d] = o / Lsum;
+  }
+  if (tid == 0) st->counters[CNT_ATTN + g] = 0u;
+}
+
+// ---------------------------------------------------------------------------
 // Final RMSNorm -> logits = W_out n (fp32), with an optional device argmax:
 // per-CTA (value, index) partials, merged by the last CTA (ties -> lower id).
 
@@ -450,15 +721,21 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_norm_lmhead(
   __shared__ float wbest[GEMV_WARPS];
   __shared__ int wbidx[GEMV_WARPS];
   __shared__ int is_last;
-  block_rmsnorm_to_smem(x, nw, K, eps, xs, red);
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int npairs = (V + 1) / 2;
+  const int p0 = blockIdx.x * GEMV_WARPS + warp;
+  RowPf pf;
+  if (p0 < npairs) prefetch_pair(head + (size_t)2 * p0 * K, head + (size_t)min(2 * p0 + 1, V - 1) * K, K, pf);
+  pdl_wait();
+  block_rmsnorm_to_smem(x, nw, K, eps, xs, red);
   float best = -INFINITY;
   int bidx = 0x7fffffff;
-  for (int p = blockIdx.x * GEMV_WARPS + warp; p < npairs; p += gridDim.x * GEMV_WARPS) {
+  for (int p = p0; p < npairs; p += gridDim.x * GEMV_WARPS) {
     const int r0 = 2 * p, r1 = min(r0 + 1, V - 1);
     float a0, a1;
-    warp_dot2(head + (size_t)r0 * K, head + (size_t)r1 * K, xs, K, a0, a1);
+    if (p == p0) warp_dot2_pf(head + (size_t)r0 * K, head + (size_t)r1 * K, xs, K, pf, a0, a1);
+    else warp_dot2(head + (size_t)r0 * K, head + (size_t)r1 * K, xs, K, a0, a1);
     if (lane == 0) {
       if (logits) {
         logits[r0] = a0;
@@ -545,6 +822,26 @@ static void set_smem(F* kern, size_t bytes) {
   if (bytes > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+// Launch with programmatic stream serialization: the kernel may start while
+// its predecessor on the stream runs and orders itself with pdl_wait().
+template <typename... KArgs, typename... Args>
+static void launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+const void* set_step_kernel() { return reinterpret_cast<const void*>(&k_set_step); }
+
 void launch_set_step(const Model& m, cudaStream_t s, const int32_t* d_token, int32_t token, int32_t pos) {
   k_set_step<<<1, 128, 0, s>>>(m.s.st, d_token, token, pos, m.cfg.vocab, m.s.inv_freq,
                                m.cfg.head_dim / 2, m.s.rope_tab);
@@ -559,8 +856,8 @@ static void lmhead(const Model& m, cudaStream_t s, const float* x, float* logits
   auto kern = k_norm_lmhead<W>;
   set_smem(kern, sm_h);
   timer_begin(m, DEC_K_LMHEAD, s);
-  kern<<<m.lm_grid, GEMV_THREADS, sm_h, s>>>(x, m.out_norm, c.rms_eps, (const W*)m.head, c.hidden, c.vocab,
-                                            logits, d_argmax, S.amax_val, S.amax_idx, S.st);
+  launch_pdl(kern, dim3(m.lm_grid), dim3(GEMV_THREADS), sm_h, s, x, m.out_norm, c.rms_eps, (const W*)m.head,
+             c.hidden, c.vocab, logits, d_argmax, S.amax_val, S.amax_idx, S.st);
   timer_end(m, DEC_K_LMHEAD, s);
   count_launch(m);
 }
@@ -570,13 +867,27 @@ void launch_lmhead(const Model& m, cudaStream_t s, const float* x, float* logits
   else lmhead<float>(m, s, x, logits, d_argmax);
 }
 
+template <typename KV, int HD>
+static void attn_decode(const Model& m, cudaStream_t s, const LayerPtrs& L) {
+  const dec_config& c = m.cfg;
+  const size_t smb = AdLayout<KV, HD>::bytes(c.n_heads / c.n_kv_heads);
+  auto kern = k_attn_decode<KV, HD>;
+  set_smem(kern, smb);
+  launch_pdl(kern, dim3(c.n_kv_heads, m.nsplit), dim3(AD_THREADS), smb, s, (const float*)m.s.q,
+             (const KV*)L.kc, (const KV*)L.vc, c.n_heads, c.n_kv_heads, c.max_seq, c.sliding_window, m.attn_sps,
+             m.s.st, m.s.part, m.s.attn);
+}
+
+// One decode step: step state + RoPE row, then every layer, then the head.
+// The first kernel orders fully after earlier stream work; every later one is
+// a programmatic dependent of its predecessor.
 template <typename W, typename KV>
-static void decode_body(const Model& m, cudaStream_t s, float* logits, int32_t* d_argmax) {
+static void decode_body(const Model& m, cudaStream_t s, const int32_t* d_token, int32_t token, int32_t pos,
+                        float* logits, int32_t* d_argmax) {
   const dec_config& c = m.cfg;
   const int h = c.hidden, hd = c.head_dim, qd = c.n_heads * hd, kd = c.n_kv_heads * hd;
   const Scratch& S = m.s;
-  k_embed_step<W><<<(h + 255) / 256, 256, 0, s>>>((const W*)m.tok_embd, h, S.st, S.x);
-  count_launch(m);
+  launch_set_step(m, s, d_token, token, pos);
   const size_t sm_h = (64 + MAX_EXPERTS + (size_t)h) * sizeof(float);
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerPtrs& L = m.layers[l];
@@ -584,34 +895,26 @@ static void decode_body(const Model& m, cudaStream_t s, float* logits, int32_t* 
       auto kern = k_norm_qkv<W, KV>;
       set_smem(kern, sm_h);
       timer_begin(m, DEC_K_QKV, s);
-      kern<<<gemv_grid((qd + 2 * kd) / 2), GEMV_THREADS, sm_h, s>>>(
-          S.x, L.attn_norm, c.rms_eps, (const W*)L.wqkv, L.bqkv, h, qd, kd, hd, S.rope_tab, S.st,
-          c.max_seq, c.sliding_window, S.q, (KV*)L.kc, (KV*)L.vc);
+      launch_pdl(kern, dim3(gemv_grid((qd + 2 * kd) / 2)), dim3(GEMV_THREADS), sm_h, s, (const float*)S.x,
+                 l == 0 ? (const W*)m.tok_embd : (const W*)nullptr, S.x, L.attn_norm, c.rms_eps,
+                 (const W*)L.wqkv, L.bqkv, h, qd, kd, hd, (const float2*)S.rope_tab, (const DeviceState*)S.st,
+                 c.max_seq, c.sliding_window, S.q, (KV*)L.kc, (KV*)L.vc);
       timer_end(m, DEC_K_QKV, s);
       count_launch(m);
     }
-    {
-      dim3 grid(c.n_kv_heads, m.nsplit);
-      timer_begin(m, DEC_K_ATTN, s);
-      if (hd == 64)
-        k_flash_decode<KV, 64><<<grid, FD_THREADS, 0, s>>>(S.q, (const KV*)L.kc, (const KV*)L.vc,
-            c.n_heads, c.n_kv_heads, c.max_seq, c.sliding_window, S.st, S.part, S.attn);
-      else if (hd == 128)
-        k_flash_decode<KV, 128><<<grid, FD_THREADS, 0, s>>>(S.q, (const KV*)L.kc, (const KV*)L.vc,
-            c.n_heads, c.n_kv_heads, c.max_seq, c.sliding_window, S.st, S.part, S.attn);
-      else
-        k_flash_decode<KV, 16><<<grid, FD_THREADS, 0, s>>>(S.q, (const KV*)L.kc, (const KV*)L.vc,
-            c.n_heads, c.n_kv_heads, c.max_seq, c.sliding_window, S.st, S.part, S.attn);
-      timer_end(m, DEC_K_ATTN, s);
-      count_launch(m);
-    }
+    timer_begin(m, DEC_K_ATTN, s);
+    if (hd == 64) attn_decode<KV, 64>(m, s, L);
+    else if (hd == 128) attn_decode<KV, 128>(m, s, L);
+    else attn_decode<KV, 16>(m, s, L);
+    timer_end(m, DEC_K_ATTN, s);
+    count_launch(m);
     {
       const size_t smb = (64 + (size_t)qd) * sizeof(float);
       auto kern = k_gemv_accum<W>;
       set_smem(kern, smb);
       timer_begin(m, DEC_K_OPROJ, s);
-      kern<<<gemv_grid((h + 1) / 2), GEMV_THREADS, smb, s>>>(S.attn, (const W*)L.wo, h, qd, nullptr,
-                                                            nullptr, 1, S.x);
+      launch_pdl(kern, dim3(gemv_grid((h + 1) / 2)), dim3(GEMV_THREADS), smb, s, (const float*)S.attn,
+                 (const W*)L.wo, h, qd, (const int32_t*)nullptr, (const float*)nullptr, 1, S.x);
       timer_end(m, DEC_K_OPROJ, s);
       count_launch(m);
     }
@@ -622,9 +925,9 @@ static void decode_body(const Model& m, cudaStream_t s, float* logits, int32_t* 
         auto kern = k_moe_router<W>;
         set_smem(kern, sm_h);
         timer_begin(m, DEC_K_ROUTER, s);
-        kern<<<1, GEMV_THREADS, sm_h, s>>>(S.x, L.ffn_norm, c.rms_eps, (const W*)L.router, h,
-                                           c.n_experts, k, S.nbuf, S.ids, S.wts, S.st, m.trace_ids,
-                                           m.trace_logits, m.trace_cap, l);
+        launch_pdl(kern, dim3(1), dim3(GEMV_THREADS), sm_h, s, (const float*)S.x, L.ffn_norm, c.rms_eps,
+                   (const W*)L.router, h, c.n_experts, k, S.nbuf, S.ids, S.wts, (const DeviceState*)S.st,
+                   m.trace_ids, m.trace_logits, m.trace_cap, l);
         timer_end(m, DEC_K_ROUTER, s);
         count_launch(m);
       }
@@ -632,8 +935,9 @@ static void decode_body(const Model& m, cudaStream_t s, float* logits, int32_t* 
         auto kern = k_gateup<W>;
         set_smem(kern, sm_h);
         timer_begin(m, DEC_K_GATEUP, s);
-        kern<<<gemv_grid(k * f), GEMV_THREADS, sm_h, s>>>(nullptr, nullptr, 0.f, S.nbuf,
-            (const W*)L.w_gateup, h, f, S.ids, k, S.act);
+        launch_pdl(kern, dim3(gemv_grid(k * f)), dim3(GEMV_THREADS), sm_h, s, (const float*)nullptr,
+                   (const float*)nullptr, 0.f, (const float*)S.nbuf, (const W*)L.w_gateup, h, f,
+                   (const int32_t*)S.ids, k, S.act);
         timer_end(m, DEC_K_GATEUP, s);
         count_launch(m);
       }
@@ -642,8 +946,8 @@ static void decode_body(const Model& m, cudaStream_t s, float* logits, int32_t* 
         auto kern = k_gemv_accum<W>;
         set_smem(kern, smb);
         timer_begin(m, DEC_K_DOWN, s);
-        kern<<<gemv_grid((h + 1) / 2), GEMV_THREADS, smb, s>>>(S.act, (const W*)L.w_down, h, f,
-                                                              S.ids, S.wts, k, S.x);
+        launch_pdl(kern, dim3(gemv_grid((h + 1) / 2)), dim3(GEMV_THREADS), smb, s, (const float*)S.act,
+                   (const W*)L.w_down, h, f, (const int32_t*)S.ids, (const float*)S.wts, k, S.x);
         timer_end(m, DEC_K_DOWN, s);
         count_launch(m);
       }
@@ -652,8 +956,9 @@ static void decode_body(const Model& m, cudaStream_t s, float* logits, int32_t* 
         auto kern = k_gateup<W>;
         set_smem(kern, sm_h);
         timer_begin(m, DEC_K_GATEUP, s);
-        kern<<<gemv_grid(f), GEMV_THREADS, sm_h, s>>>(S.x, L.ffn_norm, c.rms_eps, nullptr,
-            (const W*)L.w_gateup, h, f, nullptr, 1, S.act);
+        launch_pdl(kern, dim3(gemv_grid(f)), dim3(GEMV_THREADS), sm_h, s, (const float*)S.x, L.ffn_norm,
+                   c.rms_eps, (const float*)nullptr, (const W*)L.w_gateup, h, f, (const int32_t*)nullptr, 1,
+                   S.act);
         timer_end(m, DEC_K_GATEUP, s);
         count_launch(m);
       }
@@ -662,8 +967,8 @@ static void decode_body(const Model& m, cudaStream_t s, float* logits, int32_t* 
         auto kern = k_gemv_accum<W>;
         set_smem(kern, smb);
         timer_begin(m, DEC_K_DOWN, s);
-        kern<<<gemv_grid((h + 1) / 2), GEMV_THREADS, smb, s>>>(S.act, (const W*)L.w_down, h, f,
-                                                              nullptr, nullptr, 1, S.x);
+        launch_pdl(kern, dim3(gemv_grid((h + 1) / 2)), dim3(GEMV_THREADS), smb, s, (const float*)S.act,
+                   (const W*)L.w_down, h, f, (const int32_t*)nullptr, (const float*)nullptr, 1, S.x);
         timer_end(m, DEC_K_DOWN, s);
         count_launch(m);
       }
@@ -672,12 +977,13 @@ static void decode_body(const Model& m, cudaStream_t s, float* logits, int32_t* 
   if (logits || d_argmax) lmhead<W>(m, s, S.x, logits, d_argmax);
 }
 
-void launch_decode_body(const Model& m, cudaStream_t s, float* logits, int32_t* d_argmax) {
+void launch_decode_body(const Model& m, cudaStream_t s, const int32_t* d_token, int32_t token, int32_t pos,
+                        float* logits, int32_t* d_argmax) {
   const bool wb = m.cfg.weight_dtype == DEC_BF16, kb = m.cfg.kv_dtype == DEC_BF16;
-  if (wb && kb) decode_body<__nv_bfloat16, __nv_bfloat16>(m, s, logits, d_argmax);
-  else if (wb) decode_body<__nv_bfloat16, float>(m, s, logits, d_argmax);
-  else if (kb) decode_body<float, __nv_bfloat16>(m, s, logits, d_argmax);
-  else decode_body<float, float>(m, s, logits, d_argmax);
+  if (wb && kb) decode_body<__nv_bfloat16, __nv_bfloat16>(m, s, d_token, token, pos, logits, d_argmax);
+  else if (wb) decode_body<__nv_bfloat16, float>(m, s, d_token, token, pos, logits, d_argmax);
+  else if (kb) decode_body<float, __nv_bfloat16>(m, s, d_token, token, pos, logits, d_argmax);
+  else decode_body<float, float>(m, s, d_token, token, pos, logits, d_argmax);
 }
 
 }  // namespace dec

@@ -85,6 +85,7 @@ struct Model {
   const void* head;     // tok_embd when tied
   Scratch s;
   int nsplit;           // split-K CTAs per kv head in decode attention
+  int attn_sps;         // KV slots owned by one split
   int lm_grid;          // CTAs of the LM head kernel
   int32_t* trace_ids;   // nullable
   float* trace_logits;  // nullable
@@ -101,6 +102,7 @@ struct WsPlan {
   size_t kv_layer_bytes;
   size_t total;
   int nsplit;
+  int attn_sps;
   int max_tokens;
 };
 
@@ -128,7 +130,11 @@ inline void timer_end(const Model& m, int cls, cudaStream_t s) {
 
 // decode.cu
 void launch_set_step(const Model& m, cudaStream_t s, const int32_t* d_token, int32_t token, int32_t pos);
-void launch_decode_body(const Model& m, cudaStream_t s, float* logits, int32_t* d_argmax);
+// One whole decode step: the setup kernel (token, position, RoPE row) first.
+void launch_decode_body(const Model& m, cudaStream_t s, const int32_t* d_token, int32_t token, int32_t pos,
+                        float* logits, int32_t* d_argmax);
+// Host handle of the setup kernel (for updating its node in a captured graph).
+const void* set_step_kernel();
 // Final RMSNorm + LM head (+ argmax) of one residual row x.
 void launch_lmhead(const Model& m, cudaStream_t s, const float* x, float* logits, int32_t* d_argmax);
 
