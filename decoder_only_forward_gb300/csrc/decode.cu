@@ -49,39 +49,35 @@ __device__ void block_copy_to_smem(const float* __restrict__ x, int K, float* xs
 template <typename W>
 __device__ __forceinline__ void warp_dot2_acc(const W* __restrict__ r0, const W* __restrict__ r1,
                                               const float* __restrict__ xs, int K, int c, float& a0, float& a1) {
-  constexpr int V = Chunk<W>::N;
+  // Up to U chunks per lane are in flight at once; the bound checks are
+  // predicates, so short rows (K of a few hundred) still issue every load
+  // before the first use instead of one DRAM round trip per chunk.
+  constexpr int V = Chunk<W>::N, U = 6;
   const int nch = K / V;
-  for (; c + 96 < nch; c += 128) {
-    uint4 u0[4], u1[4];
+  for (; c < nch; c += 32 * U) {
+    uint4 u0[U], u1[U];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      u0[i] = ld_stream16(r0 + (size_t)(c + 32 * i) * V);
-      u1[i] = ld_stream16(r1 + (size_t)(c + 32 * i) * V);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float w0[V], w1[V];
-      Chunk<W>::widen(u0[i], w0);
-      Chunk<W>::widen(u1[i], w1);
-      const float* xv = xs + (c + 32 * i) * V;
-#pragma unroll
-      for (int e = 0; e < V; ++e) {
-        a0 = fmaf(w0[e], xv[e], a0);
-        a1 = fmaf(w1[e], xv[e], a1);
+    for (int i = 0; i < U; ++i) {
+      const int cc = c + 32 * i;
+      if (cc < nch) {
+        u0[i] = ld_stream16(r0 + (size_t)cc * V);
+        u1[i] = ld_stream16(r1 + (size_t)cc * V);
       }
     }
-  }
-  for (; c < nch; c += 32) {
-    uint4 u0 = ld_stream16(r0 + (size_t)c * V);
-    uint4 u1 = ld_stream16(r1 + (size_t)c * V);
-    float w0[V], w1[V];
-    Chunk<W>::widen(u0, w0);
-    Chunk<W>::widen(u1, w1);
-    const float* xv = xs + c * V;
 #pragma unroll
-    for (int e = 0; e < V; ++e) {
-      a0 = fmaf(w0[e], xv[e], a0);
-      a1 = fmaf(w1[e], xv[e], a1);
+    for (int i = 0; i < U; ++i) {
+      const int cc = c + 32 * i;
+      if (cc < nch) {
+        float w0[V], w1[V];
+        Chunk<W>::widen(u0[i], w0);
+        Chunk<W>::widen(u1[i], w1);
+        const float* xv = xs + cc * V;
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+          a0 = fmaf(w0[e], xv[e], a0);
+          a1 = fmaf(w1[e], xv[e], a1);
+        }
+      }
     }
   }
 }
@@ -282,7 +278,7 @@ template <typename W>
 __global__ void __launch_bounds__(GEMV_THREADS) k_gemv_accum(
     const float* __restrict__ v, const W* __restrict__ w, int N, int K,
     const int32_t* __restrict__ ids, const float* __restrict__ wts, int nslots,
-    float* __restrict__ x) {
+    float* __restrict__ x, const float* __restrict__ part, int psplit, int phd) {
   extern __shared__ float sm[];
   float* xs = sm + 64;
   pdl_launch_dependents();
@@ -293,7 +289,43 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv_accum(
   const bool pre = ids == nullptr && nslots == 1 && p0 < npairs;
   if (pre) prefetch_pair(w + (size_t)2 * p0 * K, w + (size_t)min(2 * p0 + 1, N - 1) * K, K, pf);
   pdl_wait();
-  block_copy_to_smem(v, K * nslots, xs);
+  if (part) {
+    // Input = attention output merged from its split-K partials (max, sum,
+    // unnormalised output per split; rml Attend's online-softmax state).
+    // Phase 1: a warp per head turns the splits' (max, sum) into weights
+    // exp(m_s - M) / L in shared memory; phase 2: every output sums its splits.
+    float* scale = sm + 64 + K;   // [heads][psplit]
+    const int heads = K / phd;
+    for (int hh = warp; hh < heads; hh += GEMV_WARPS) {
+      const float* base = part + (size_t)hh * psplit * (phd + 2);
+      float mloc = -INFINITY;
+      for (int s2 = lane; s2 < psplit; s2 += 32) mloc = fmaxf(mloc, base[s2 * (phd + 2) + phd]);
+      const float M = warp_max(mloc);
+      float lsum = 0.f;
+      for (int s2 = lane; s2 < psplit; s2 += 32) {
+        const float ms = base[s2 * (phd + 2) + phd];
+        const float sc = ms == -INFINITY ? 0.f : __expf(ms - M);
+        scale[hh * psplit + s2] = sc;
+        lsum = fmaf(base[s2 * (phd + 2) + phd + 1], sc, lsum);
+      }
+      const float L = warp_sum(lsum);
+      __syncwarp();
+      for (int s2 = lane; s2 < psplit; s2 += 32) scale[hh * psplit + s2] /= L;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < K; idx += blockDim.x) {
+      const int hh = idx / phd, d = idx - hh * phd;
+      const float* base = part + (size_t)hh * psplit * (phd + 2) + d;
+      const float* sc = scale + hh * psplit;
+      float o = 0.f;
+#pragma unroll 8
+      for (int s2 = 0; s2 < psplit; ++s2) o = fmaf(sc[s2], base[(size_t)s2 * (phd + 2)], o);
+      xs[idx] = o;
+    }
+    __syncthreads();
+  } else {
+    block_copy_to_smem(v, K * nslots, xs);
+  }
   for (int p = p0; p < npairs; p += gridDim.x * GEMV_WARPS) {
     const int r0 = 2 * p;
     const int r1 = min(r0 + 1, N - 1);
@@ -556,7 +588,6 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode(
   float* qs = reinterpret_cast<float*>(vs + AD_KS * HD);
   float* ps = qs + G * HD;
   __shared__ float mrow[MAX_GROUP], lrow[MAX_GROUP], alpha[MAX_GROUP];
-  __shared__ int is_last;
 
   pdl_launch_dependents();
   const int g = blockIdx.x, split = blockIdx.y, nsplit = gridDim.y;
@@ -677,32 +708,7 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode(
     pp[HD] = mrow[tid];
     pp[HD + 1] = lrow[tid];
   }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned prev = atomicAdd(&st->counters[CNT_ATTN + g], 1u);
-    is_last = (prev == (unsigned)nsplit - 1);
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  for (int idx = tid; idx < G * HD; idx += AD_THREADS) {
-    const int hh = idx / HD, d = idx - hh * HD;
-    const float* base = part + (size_t)(g * G + hh) * nsplit * (HD + 2);
-    float M = -INFINITY;
-    for (int s2 = 0; s2 < nsplit; ++s2) M = fmaxf(M, __ldcg(base + s2 * (HD + 2) + HD));
-    float Lsum = 0.f, o = 0.f;
-    for (int s2 = 0; s2 < nsplit; ++s2) {
-      const float* pp = base + s2 * (HD + 2);
-      const float ms = __ldcg(pp + HD);
-      if (ms == -INFINITY) continue;
-      const float sc = __expf(ms - M);
-      Lsum = fmaf(__ldcg(pp + HD + 1), sc, Lsum);
-      o = fmaf(__ldcg(pp + d), sc, o);
-    }
-    out[(size_t)(g * G + hh) * HD + d] = o / Lsum;
-  }
-  if (tid == 0) st->counters[CNT_ATTN + g] = 0u;
+  // The output projection merges the splits (k_gemv_accum's partial prologue).
 }
 
 // ---------------------------------------------------------------------------
@@ -763,16 +769,33 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_norm_lmhead(
     is_last = (prev == gridDim.x - 1);
   }
   __syncthreads();
-  if (is_last && threadIdx.x == 0) {
-    __threadfence();
-    float b = __ldcg(pval);
-    int bi = __ldcg(pidx);
-    for (int i = 1; i < (int)gridDim.x; ++i) {
-      const float v = __ldcg(pval + i);
-      const int vi = __ldcg(pidx + i);
-      if (v > b || (v == b && vi < bi)) { b = v; bi = vi; }
-    }
-    *d_argmax = bi;
+  if (!is_last) return;
+  // The last CTA merges the per-CTA (value, index) partials: each thread folds
+  // a strided subset, then a block reduction; ties keep the lower index.
+  __threadfence();
+  float b = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) {
+    const float v = __ldcg(pval + i);
+    const int vi = __ldcg(pidx + i);
+    if (v > b || (v == b && vi < bi)) { b = v; bi = vi; }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, b, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > b || (ov == b && oi < bi)) { b = ov; bi = oi; }
+  }
+  __syncthreads();
+  if (lane == 0) {
+    wbest[warp] = b;
+    wbidx[warp] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < GEMV_WARPS; ++w)
+      if (wbest[w] > wbest[0] || (wbest[w] == wbest[0] && wbidx[w] < wbidx[0])) { wbest[0] = wbest[w]; wbidx[0] = wbidx[w]; }
+    *d_argmax = wbidx[0];
     st->counters[CNT_ARGMAX] = 0u;
   }
 }
@@ -909,12 +932,14 @@ static void decode_body(const Model& m, cudaStream_t s, const int32_t* d_token, 
     timer_end(m, DEC_K_ATTN, s);
     count_launch(m);
     {
-      const size_t smb = (64 + (size_t)qd) * sizeof(float);
+      const size_t smb = (64 + (size_t)qd + (size_t)c.n_heads * m.nsplit) * sizeof(float);
       auto kern = k_gemv_accum<W>;
       set_smem(kern, smb);
       timer_begin(m, DEC_K_OPROJ, s);
+      const bool merge = m.nsplit > 1;
       launch_pdl(kern, dim3(gemv_grid((h + 1) / 2)), dim3(GEMV_THREADS), smb, s, (const float*)S.attn,
-                 (const W*)L.wo, h, qd, (const int32_t*)nullptr, (const float*)nullptr, 1, S.x);
+                 (const W*)L.wo, h, qd, (const int32_t*)nullptr, (const float*)nullptr, 1, S.x,
+                 merge ? (const float*)S.part : (const float*)nullptr, m.nsplit, hd);
       timer_end(m, DEC_K_OPROJ, s);
       count_launch(m);
     }
@@ -947,7 +972,8 @@ static void decode_body(const Model& m, cudaStream_t s, const int32_t* d_token, 
         set_smem(kern, smb);
         timer_begin(m, DEC_K_DOWN, s);
         launch_pdl(kern, dim3(gemv_grid((h + 1) / 2)), dim3(GEMV_THREADS), smb, s, (const float*)S.act,
-                   (const W*)L.w_down, h, f, (const int32_t*)S.ids, (const float*)S.wts, k, S.x);
+                   (const W*)L.w_down, h, f, (const int32_t*)S.ids, (const float*)S.wts, k, S.x,
+                   (const float*)nullptr, 0, 0);
         timer_end(m, DEC_K_DOWN, s);
         count_launch(m);
       }
@@ -968,7 +994,8 @@ static void decode_body(const Model& m, cudaStream_t s, const int32_t* d_token, 
         set_smem(kern, smb);
         timer_begin(m, DEC_K_DOWN, s);
         launch_pdl(kern, dim3(gemv_grid((h + 1) / 2)), dim3(GEMV_THREADS), smb, s, (const float*)S.act,
-                   (const W*)L.w_down, h, f, (const int32_t*)nullptr, (const float*)nullptr, 1, S.x);
+                   (const W*)L.w_down, h, f, (const int32_t*)nullptr, (const float*)nullptr, 1, S.x,
+                   (const float*)nullptr, 0, 0);
         timer_end(m, DEC_K_DOWN, s);
         count_launch(m);
       }
