@@ -184,6 +184,7 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(max(2 * L2_BYTES, 256 * 2**20) // 4, dtype=torch.float32, device=dev)
 
     def step():
+        d.kv_reset()  # each step is a new sequence
         d.prefill(prompt_np, 0, logits, tok)
         for i in range(D):
             d.decode_dev(tok, P + i, logits, tok)
@@ -192,6 +193,7 @@ def run_ours(args, rank, world, local_rank):
         with torch.cuda.stream(s):
             flush.zero_()
         evs[0].record(s)
+        d.kv_reset()  # each step is a new sequence
         d.prefill(prompt_np, 0, logits, tok)
         evs[1].record(s)
         for i in range(D):
@@ -242,6 +244,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
+        d.kv_reset()
         d.prefill(prompt_pinned, 0, logits, tok)
         for i in range(D):
             d.decode_dev(tok, P + i, logits, tok)
@@ -258,6 +261,7 @@ def run_ours(args, rank, world, local_rank):
     per_class = {}
     for c in classes:
         d.timing_enable(c, 20000)
+        d.kv_reset()  # each step is a new sequence
         d.prefill(prompt_np, 0, logits, tok)
         ms_pf, n_pf = d.timing_read()
         ms_dc, n_dc = 0.0, 0

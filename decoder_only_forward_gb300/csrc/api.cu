@@ -216,7 +216,10 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
   m.ws_bytes = workspace_bytes;
   m.nsplit = p.nsplit;
   m.attn_sps = p.attn_sps;
+  // LM head: two CTAs per SM, each warp walking its row pairs with the next
+  // pair's loads in flight.
   int lg = (cfg->vocab / 2 + 7) / 8;
+  if (lg > 2 * 152) lg = 2 * 152;
   m.lm_grid = lg < 1 ? 1 : (lg > LM_GRID_MAX ? LM_GRID_MAX : lg);
   m.tok_embd = w->tok_embd;
   m.out_norm = (const float*)w->out_norm;

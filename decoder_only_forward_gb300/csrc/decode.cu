@@ -202,11 +202,15 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_norm_qkv(
   block_rmsnorm_to_smem(x, nw, K, eps, xs, red);
   const int pos = st->pos;
   const int slot = sliding > 0 ? pos % max_seq : pos;
-  for (int p = p0; p < npairs; p += gridDim.x * GEMV_WARPS) {
+  const int stride = gridDim.x * GEMV_WARPS;
+  for (int p = p0; p < npairs; p += stride) {
     const int r = 2 * p;
+    RowPf nxt;   // next pair's rows are in flight while this pair is reduced
+    if (p + stride < npairs)
+      prefetch_pair(wqkv + (size_t)2 * (p + stride) * K, wqkv + (size_t)(2 * (p + stride) + 1) * K, K, nxt);
     float a0, a1;
-    if (p == p0) warp_dot2_pf(wqkv + (size_t)r * K, wqkv + (size_t)(r + 1) * K, xs, K, pf, a0, a1);
-    else warp_dot2(wqkv + (size_t)r * K, wqkv + (size_t)(r + 1) * K, xs, K, a0, a1);
+    warp_dot2_pf(wqkv + (size_t)r * K, wqkv + (size_t)(r + 1) * K, xs, K, pf, a0, a1);
+    pf = nxt;
     if (lane == 0) {
       if (bqkv) {
         a0 += bqkv[r];
@@ -259,13 +263,20 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gateup(
   pdl_wait();
   if (nvec) block_copy_to_smem(nvec, K, xs);
   else block_rmsnorm_to_smem(x, nw, K, eps, xs, red);
-  for (int p = p0; p < ntask; p += gridDim.x * GEMV_WARPS) {
+  const int stride = gridDim.x * GEMV_WARPS;
+  for (int p = p0; p < ntask; p += stride) {
     const int slot = p / f, j = p - slot * f;
     const size_t e = ids ? (size_t)ids[slot] : 0;
     const W* base = wgu + e * (size_t)2 * f * K + (size_t)2 * j * K;
     float g, u;
-    if (pre && p == p0) warp_dot2_pf(base, base + K, xs, K, pf, g, u);
-    else warp_dot2(base, base + K, xs, K, g, u);
+    if (pre) {
+      RowPf nxt;
+      if (p + stride < ntask) prefetch_pair(wgu + (size_t)2 * (p + stride) * K, wgu + (size_t)(2 * (p + stride) + 1) * K, K, nxt);
+      warp_dot2_pf(base, base + K, xs, K, pf, g, u);
+      pf = nxt;
+    } else {
+      warp_dot2(base, base + K, xs, K, g, u);
+    }
     if (lane == 0) act[(size_t)slot * f + j] = silu_f(g) * u;
   }
 }
@@ -326,15 +337,19 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv_accum(
   } else {
     block_copy_to_smem(v, K * nslots, xs);
   }
-  for (int p = p0; p < npairs; p += gridDim.x * GEMV_WARPS) {
+  const int stride = gridDim.x * GEMV_WARPS;
+  for (int p = p0; p < npairs; p += stride) {
     const int r0 = 2 * p;
     const int r1 = min(r0 + 1, N - 1);
     float o0 = 0.f, o1 = 0.f;
+    RowPf nxt;
+    if (pre && p + stride < npairs)
+      prefetch_pair(w + (size_t)2 * (p + stride) * K, w + (size_t)min(2 * (p + stride) + 1, N - 1) * K, K, nxt);
     for (int s = 0; s < nslots; ++s) {
       const size_t e = ids ? (size_t)ids[s] : 0;
       const W* base = w + e * (size_t)N * K;
       float a0, a1;
-      if (pre && p == p0) warp_dot2_pf(base + (size_t)r0 * K, base + (size_t)r1 * K, xs, K, pf, a0, a1);
+      if (pre) warp_dot2_pf(base + (size_t)r0 * K, base + (size_t)r1 * K, xs, K, pf, a0, a1);
       else warp_dot2(base + (size_t)r0 * K, base + (size_t)r1 * K, xs + (size_t)s * K, K, a0, a1);
       const float ws = wts ? wts[s] : 1.0f;
       o0 = fmaf(ws, a0, o0);
@@ -344,6 +359,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_gemv_accum(
       x[r0] += o0;
       if (r1 != r0) x[r1] += o1;
     }
+    if (pre) pf = nxt;
   }
 }
 
@@ -737,11 +753,15 @@ __global__ void __launch_bounds__(GEMV_THREADS) k_norm_lmhead(
   block_rmsnorm_to_smem(x, nw, K, eps, xs, red);
   float best = -INFINITY;
   int bidx = 0x7fffffff;
-  for (int p = p0; p < npairs; p += gridDim.x * GEMV_WARPS) {
+  const int stride = gridDim.x * GEMV_WARPS;
+  for (int p = p0; p < npairs; p += stride) {
     const int r0 = 2 * p, r1 = min(r0 + 1, V - 1);
+    RowPf nxt;
+    if (p + stride < npairs)
+      prefetch_pair(head + (size_t)2 * (p + stride) * K, head + (size_t)min(2 * (p + stride) + 1, V - 1) * K, K, nxt);
     float a0, a1;
-    if (p == p0) warp_dot2_pf(head + (size_t)r0 * K, head + (size_t)r1 * K, xs, K, pf, a0, a1);
-    else warp_dot2(head + (size_t)r0 * K, head + (size_t)r1 * K, xs, K, a0, a1);
+    warp_dot2_pf(head + (size_t)r0 * K, head + (size_t)r1 * K, xs, K, pf, a0, a1);
+    pf = nxt;
     if (lane == 0) {
       if (logits) {
         logits[r0] = a0;
