@@ -594,7 +594,7 @@ template <typename KV, int HD>
 __global__ void __launch_bounds__(AD_THREADS) k_attn_decode(
     const float* __restrict__ q, const KV* __restrict__ kc, const KV* __restrict__ vc, int nq, int nkv,
     int max_seq, int sliding, int sps, DeviceState* __restrict__ st, float* __restrict__ part,
-    float* __restrict__ out) {
+    float* __restrict__ out, int merge_here) {
   using L = AdLayout<KV, HD>;
   constexpr int OUTS = (MAX_GROUP * HD + AD_THREADS - 1) / AD_THREADS;
   extern __shared__ __align__(16) uint8_t ad_smem[];
@@ -724,7 +724,43 @@ __global__ void __launch_bounds__(AD_THREADS) k_attn_decode(
     pp[HD] = mrow[tid];
     pp[HD + 1] = lrow[tid];
   }
-  // The output projection merges the splits (k_gemv_accum's partial prologue).
+  if (!merge_here) return;  // the output projection merges the splits (k_gemv_accum's prologue)
+  // Large partial sets: the last CTA of kv head g merges its G heads' splits.
+  __shared__ int is_last;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) is_last = atomicAdd(&st->counters[CNT_ATTN + g], 1u) == (unsigned)nsplit - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  float* wsplit = ps;  // [G][nsplit], nsplit <= AD_KS
+  for (int hh = warp; hh < G; hh += AD_THREADS / 32) {
+    const float* base = part + (size_t)(g * G + hh) * nsplit * (HD + 2);
+    float mloc = -INFINITY;
+    for (int s2 = lane; s2 < nsplit; s2 += 32) mloc = fmaxf(mloc, __ldcg(base + s2 * (HD + 2) + HD));
+    const float M = warp_max(mloc);
+    float lsum = 0.f;
+    for (int s2 = lane; s2 < nsplit; s2 += 32) {
+      const float ms = __ldcg(base + s2 * (HD + 2) + HD);
+      const float sc = ms == -INFINITY ? 0.f : __expf(ms - M);
+      wsplit[hh * AD_KS + s2] = sc;
+      lsum = fmaf(__ldcg(base + s2 * (HD + 2) + HD + 1), sc, lsum);
+    }
+    const float Lsum = warp_sum(lsum);
+    __syncwarp();
+    for (int s2 = lane; s2 < nsplit; s2 += 32) wsplit[hh * AD_KS + s2] /= Lsum;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * HD; idx += AD_THREADS) {
+    const int hh = idx / HD, d = idx - hh * HD;
+    const float* base = part + (size_t)(g * G + hh) * nsplit * (HD + 2) + d;
+    const float* sc = wsplit + hh * AD_KS;
+    float o = 0.f;
+#pragma unroll 8
+    for (int s2 = 0; s2 < nsplit; ++s2) o = fmaf(sc[s2], __ldcg(base + (size_t)s2 * (HD + 2)), o);
+    out[(size_t)(g * G + hh) * HD + d] = o;
+  }
+  if (tid == 0) st->counters[CNT_ATTN + g] = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -910,6 +946,13 @@ void launch_lmhead(const Model& m, cudaStream_t s, const float* x, float* logits
   else lmhead<float>(m, s, x, logits, d_argmax);
 }
 
+// Split partials are merged by every output-projection CTA when they are
+// small, else once per kv head by the attention kernel's last CTA.
+static bool merge_in_attention(const Model& m) {
+  const size_t bytes = (size_t)m.cfg.n_heads * m.nsplit * (m.cfg.head_dim + 2) * sizeof(float);
+  return m.nsplit > 1 && bytes > 64 * 1024;
+}
+
 template <typename KV, int HD>
 static void attn_decode(const Model& m, cudaStream_t s, const LayerPtrs& L) {
   const dec_config& c = m.cfg;
@@ -918,7 +961,7 @@ static void attn_decode(const Model& m, cudaStream_t s, const LayerPtrs& L) {
   set_smem(kern, smb);
   launch_pdl(kern, dim3(c.n_kv_heads, m.nsplit), dim3(AD_THREADS), smb, s, (const float*)m.s.q,
              (const KV*)L.kc, (const KV*)L.vc, c.n_heads, c.n_kv_heads, c.max_seq, c.sliding_window, m.attn_sps,
-             m.s.st, m.s.part, m.s.attn);
+             m.s.st, m.s.part, m.s.attn, merge_in_attention(m) ? 1 : 0);
 }
 
 // One decode step: step state + RoPE row, then every layer, then the head.
@@ -956,7 +999,7 @@ static void decode_body(const Model& m, cudaStream_t s, const int32_t* d_token, 
       auto kern = k_gemv_accum<W>;
       set_smem(kern, smb);
       timer_begin(m, DEC_K_OPROJ, s);
-      const bool merge = m.nsplit > 1;
+      const bool merge = m.nsplit > 1 && !merge_in_attention(m);
       launch_pdl(kern, dim3(gemv_grid((h + 1) / 2)), dim3(GEMV_THREADS), smb, s, (const float*)S.attn,
                  (const W*)L.wo, h, qd, (const int32_t*)nullptr, (const float*)nullptr, 1, S.x,
                  merge ? (const float*)S.part : (const float*)nullptr, m.nsplit, hd);
