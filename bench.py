@@ -257,7 +257,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_s = (time.perf_counter() - t0) / e2e_steps
 
     # ---- attribution: which kernel class dominates, and its roofline ----
-    classes = ["gateup", "down", "qkv", "oproj", "attn", "lmhead", "router"]
+    classes = ["step", "gateup", "down", "qkv", "oproj", "attn", "lmhead", "router"]
     per_class = {}
     for c in classes:
         d.timing_enable(c, 20000)
@@ -276,7 +276,10 @@ def run_ours(args, rank, world, local_rank):
     pc = per_class[dom]
     nl = pc["decode_launches"] + pc["prefill_launches"]
     wb = weight_bytes(w)
-    if dom == "attn":
+    if dom == "step":
+        # The whole decode step is one kernel: its bytes are the step's weights + KV.
+        per_launch_bytes = dbytes / D
+    elif dom == "attn":
         per_launch_bytes = sum(2 * w["n_kv_heads"] * w["head_dim"] * kv_es *
                                (min(p + 1, w["max_seq"]) if w["sliding_window"] else p + 1)
                                for p in range(P + D)) / (P + D)

@@ -30,6 +30,7 @@ struct dec_handle {
   Timing timing;
   std::vector<cudaEvent_t> events;
   bool use_graph = true;
+  bool use_fused = true;
 };
 
 static void drop_graph(dec_handle* h) {
@@ -153,6 +154,7 @@ WsPlan dec::plan_workspace(const dec_config& c) {
   p.Y = take(c.n_experts ? 4 * (size_t)T * k * c.hidden : 0);
   p.ACT = take(a_elem * (size_t)T * k * c.ffn);
   (void)ws;
+  p.mk_layers = take(sizeof(MkLayer) * (size_t)c.n_layers);
   p.kv = off;
   p.kv_layer_bytes = align_up(ks * (size_t)c.max_seq * kd, 256);
   off += 2 * p.kv_layer_bytes * c.n_layers;
@@ -227,6 +229,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
   m.trace_ids = nullptr;
   m.trace_logits = nullptr;
   m.trace_cap = 1;
+  m.mk_stamps = nullptr;
   m.timing = &h->timing;
   m.launches = &h->launches;
   char* base = (char*)workspace;
@@ -275,6 +278,34 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
     d.vc = base + p.kv + (size_t)(2 * l + 1) * p.kv_layer_bytes;
   }
   m.layers = h->layers.data();
+  {
+    std::vector<MkLayer> tab(cfg->n_layers);
+    for (int l = 0; l < cfg->n_layers; ++l) {
+      const LayerPtrs& d = h->layers[l];
+      tab[l] = MkLayer{d.attn_norm, d.wqkv, d.bqkv, d.wo, d.ffn_norm, d.w_gateup, d.w_down, d.router, d.kc, d.vc};
+    }
+    m.mk_layers = (const MkLayer*)(base + p.mk_layers);
+    cudaError_t e2 = cudaMemcpy((void*)m.mk_layers, tab.data(), sizeof(MkLayer) * tab.size(), cudaMemcpyHostToDevice);
+    int dev = 0, sms = 0;
+    if (e2 == cudaSuccess) e2 = cudaGetDevice(&dev);
+    if (e2 == cudaSuccess) e2 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e2 != cudaSuccess) {
+      delete h;
+      return fail(nullptr, DEC_ECUDA, "CUDA error at create: %s", cudaGetErrorString(e2));
+    }
+    mk_prepare(m, sms);
+    cudaGetLastError();  // a configuration the persistent kernel cannot take is not an error
+    // Small models are bound by the latency of ~150 dependent phases per token,
+    // where the per-layer kernels overlapped by programmatic dependent launch
+    // are faster; large models are bound by the weight stream, where the
+    // persistent kernel's bulk-copy rings are faster.
+    size_t wbytes = (size_t)cfg->vocab * cfg->hidden * (cfg->tied_embedding ? 1 : 2);
+    const size_t qd = (size_t)cfg->n_heads * cfg->head_dim, kd = (size_t)cfg->n_kv_heads * cfg->head_dim;
+    const size_t kslots = cfg->n_experts ? cfg->n_experts_used : 1;
+    wbytes += (size_t)cfg->n_layers * ((qd + 2 * kd) * cfg->hidden + cfg->hidden * qd + 3 * kslots * cfg->ffn * cfg->hidden);
+    wbytes *= cfg->weight_dtype == DEC_BF16 ? 2 : 4;
+    h->use_fused = wbytes >= (size_t)4 << 30;
+  }
 
   // RoPE frequencies inv_i = theta^(-2i/hd), llama3-scaled when enabled
   // (rml "The decoder", Rotary embeddings), computed once in double.
@@ -378,6 +409,12 @@ static cudaError_t set_step_node(dec_handle* h, const int32_t* d_token, int32_t 
 // only the setup node's token/position change.
 static dec_status run_decode_step(dec_handle* h, const int32_t* d_token, int32_t token, int32_t pos,
                                   float* logits, int32_t* d_argmax) {
+  if (h->use_fused && h->m.mk_ok) {
+    timing_start(h);
+    launch_decode_mk(h->m, h->stream, d_token, token, pos, logits, d_argmax);
+    timing_finish(h);
+    return cuda_check(h, "decode launch");
+  }
   if (h->stream == nullptr || !h->use_graph) {
     timing_start(h);
     launch_decode_body(h->m, h->stream, d_token, token, pos, logits, d_argmax);
@@ -457,6 +494,20 @@ dec_status dec_kv_reset(dec_handle* h) {
 int32_t dec_length(const dec_handle* h) { return h ? h->len : -1; }
 
 int64_t dec_launch_count(const dec_handle* h) { return h ? h->launches : -1; }
+
+dec_status dec_phase_stamps(dec_handle* h, uint64_t* d_stamps, int32_t capacity) {
+  if (!h) return DEC_EINVAL;
+  const int need = h->m.cfg.n_layers * 6 + 2;
+  if (d_stamps && capacity < need) return fail(h, DEC_EINVAL, "phase stamps need %d entries", need);
+  h->m.mk_stamps = reinterpret_cast<unsigned long long*>(d_stamps);
+  return DEC_OK;
+}
+
+dec_status dec_set_fused(dec_handle* h, int32_t enable) {
+  if (!h) return DEC_EINVAL;
+  h->use_fused = enable != 0;
+  return DEC_OK;
+}
 
 dec_status dec_set_graph(dec_handle* h, int32_t enable) {
   if (!h) return DEC_EINVAL;

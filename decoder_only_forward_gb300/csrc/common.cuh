@@ -21,7 +21,8 @@ struct DeviceState {
   unsigned counters[256];  // last-CTA-done counters (split combine, argmax), self-resetting
 };
 
-enum CounterSlot { CNT_ARGMAX = 0, CNT_ATTN = 1 };  // CNT_ATTN + kv head index
+// CNT_ATTN + kv head index (< 193); CNT_MK_*: grid barrier of the persistent decode kernel.
+enum CounterSlot { CNT_ARGMAX = 0, CNT_ATTN = 1, CNT_MK_BAR = 240, CNT_MK_GEN = 241 };
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -1,0 +1,1063 @@
+// Persistent decode step: the whole one-token forward pass (every layer and
+// the LM head) as ONE cooperative kernel with grid-wide barriers between its
+// phases, so a step costs one launch instead of ~5 per layer.
+//
+// Roles inside each CTA (one CTA per SM):
+//   warps 0-7  compute: phase prologues (RMSNorm, split merge), the dot
+//              products of this CTA's weight rows, epilogues, attention tasks;
+//   warps 8-15 producers: warp 8+w (one lane) feeds compute warp w.  Each walks the same
+//              phase schedule and streams the rows its warp will reduce, in
+//              pieces of up to 4 KB, into that warp's 4-stage shared-memory
+//              ring with cp.async.bulk (TMA bulk copies, mbarrier completion).
+//              It runs ahead across phases and grid barriers, so the HBM
+//              weight stream does not wait for a barrier, and the compute
+//              warps never synchronise with each other inside a GEMV phase.
+//
+// Phases per layer (Pantheon "Llama Forward Pass", Forward Pass Flow):
+//   QKV    RMSNorm -> [q;k;v] rows (+bias) -> adjacent-pair RoPE -> K/V at the slot of pos
+//   ATTN   (kv head, slot range) tasks: one-pass online softmax (rml Attend), partials per split
+//  [MERGE] large split sets merged once per query head
+//   OPROJ  split merge (small sets) -> x += Wo o
+//   GATEUP RMSNorm -> silu(gate) * up (dense), or router -> top-k -> renormalise (MoE)
+//   DOWN   x += Wd act (MoE: selected experts in selection order)
+// then LMHEAD: final RMSNorm -> logits + argmax.  Cross-CTA data (x, q,
+// partials, act) is read with ld.global.cg so no stale L1 line is used.
+#include <math.h>
+
+#include "runtime.h"
+
+namespace dec {
+
+constexpr int MK_COMPUTE_WARPS = 8;
+constexpr int MK_COMPUTE = MK_COMPUTE_WARPS * 32;   // 256 compute threads
+constexpr int MK_THREADS = 2 * MK_COMPUTE;          // + one producer warp per compute warp
+constexpr int MK_STAGES = 4;                        // per compute warp
+constexpr int MK_STAGE_BYTES = 4 * 1024;            // one piece of one weight row
+constexpr int MK_RING_BYTES = MK_COMPUTE_WARPS * MK_STAGES * MK_STAGE_BYTES;  // 128 KB
+constexpr int MK_KS = 64;                           // keys per attention chunk
+
+enum MkPhase { PH_QKV = 0, PH_ATTN, PH_MERGE, PH_OPROJ, PH_GATEUP, PH_DOWN, PH_LMHEAD };
+
+struct MkParams {
+  int n_layers, h, nq, nkv, hd, f, V, E, k, max_seq, sliding, nsplit, sps, merge_phase, nb;
+  float eps;
+  const MkLayer* layers;          // device table
+  const void* embed;
+  const float* out_norm;
+  const void* head;
+  DeviceState* st;
+  const double* inv_freq;
+  float* x;
+  float* q;
+  float* attn;
+  float* act;                     // [k][f]
+  float* part;
+  float* amax_val;
+  int32_t* amax_idx;
+  int32_t* ids_out;               // [k] selected experts of the last MoE layer (for inspection)
+  float* logits;
+  int32_t* d_argmax;
+  const int32_t* d_token;
+  int token, pos;
+  int32_t* trace_ids;
+  float* trace_logits;
+  int trace_cap;
+  int u_bytes;                    // bytes of the shared region after the weight ring
+  unsigned long long* stamps;     // nullable: %globaltimer after each phase (CTA 0), [0] = start
+  int kv_bytes;                   // bytes per KV element
+};
+
+// Shared-memory bookkeeping after the weight ring and the union region.
+struct MkMisc {
+  uint64_t full[MK_COMPUTE_WARPS][MK_STAGES];
+  uint64_t empty[MK_COMPUTE_WARPS][MK_STAGES];
+  float2 cs[64];                 // (cos, sin) of this position's rotary pairs
+  float red[40];
+  float logits[MAX_EXPERTS];
+  int ids[MAX_EXPERTS_USED];
+  float wts[MAX_EXPERTS_USED];
+  float acc[256];                // MoE down: per-row sums over the selected experts
+  float wbest[MK_COMPUTE_WARPS];
+  int wbidx[MK_COMPUTE_WARPS];
+  int token;
+  int abort_flag;
+  int moe_ready;                 // layer index + 1 whose expert ids are in ids[]
+  int consumed[MK_COMPUTE_WARPS];  // stages each warp consumed (for the abort drain)
+  int is_last;
+  float mrow[MAX_GROUP], lrow[MAX_GROUP], alpha[MAX_GROUP];
+};
+
+// ------------------------------------------------------------------ sync
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(MK_COMPUTE) : "memory"); }
+
+__device__ __forceinline__ unsigned ld_volatile_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.volatile.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier of the compute groups of all CTAs (bounded wait).  The
+// arrival is an acq_rel atomic after the CTA's bar.sync (so the CTA's writes
+// are released), the last arriver releases the generation, the others acquire
+// it; no full fences.
+__device__ __forceinline__ bool mk_grid_sync(DeviceState* st, unsigned nb, volatile int* abort_flag, unsigned site) {
+  compute_sync();
+  if (threadIdx.x == 0 && !*abort_flag) {
+    unsigned* cnt = &st->counters[CNT_MK_BAR];
+    unsigned* gen = &st->counters[CNT_MK_GEN];
+    const unsigned g0 = ld_acquire_u32(gen);
+    unsigned prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(cnt) : "memory");
+    if (prev == nb - 1) {
+      asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(cnt) : "memory");
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(gen) : "memory");
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_u32(gen) == g0) {
+        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+          raise_error(st, ERR_TIMEOUT, site);
+          *abort_flag = 1;
+          break;
+        }
+      }
+    }
+  }
+  compute_sync();
+  return !*abort_flag;
+}
+
+// ------------------------------------------------------------------ mbarrier / bulk copy
+__device__ __forceinline__ uint32_t mk_smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mk_mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mk_smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mk_mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mk_smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mk_mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mk_smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mk_mbar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(mk_smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait; gives up when another role has given up.
+__device__ __forceinline__ bool mk_mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             DeviceState* st, unsigned site) {
+  if (mk_mbar_try(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mk_mbar_try(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      raise_error(st, ERR_TIMEOUT, site);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+// Asks L2 to fetch `bytes` (multiple of 16) from global memory ahead of use.
+__device__ __forceinline__ void mk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Contiguous global -> shared copy of `bytes` (multiple of 16, 16-byte aligned).
+__device__ __forceinline__ void mk_bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   mk_smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(mk_smem_u32(bar))
+               : "memory");
+}
+
+}  // namespace dec
+
+namespace dec {
+
+// ------------------------------------------------------------------ schedule
+// The weight rows one CTA handles in one phase: up to k contiguous segments
+// (one per selected expert), streamed in stages of `rps` whole rows.  Producer
+// and consumers both derive it, so they agree stage by stage.
+struct MkSeg {
+  const uint8_t* base;   // row 0 of the segment's matrix
+  int row0, rows;        // rows [row0, row0 + rows)
+  int out0;              // output index of the segment's first row (task space)
+  int slot;              // expert slot (MoE), else 0
+};
+struct MkRows {
+  int nseg;
+  MkSeg seg[MAX_EXPERTS_USED];
+  int K;                 // row length (elements)
+  int rowbytes;
+  int rps;               // rows per stage
+  bool paired;
+};
+
+__device__ __forceinline__ bool mk_is_gemv(int ph) { return ph != PH_ATTN && ph != PH_MERGE; }
+
+template <typename W>
+__device__ void mk_phase_rows(const MkParams& P, int ph, int l, const int* ids, MkRows& R) {
+  const int es = (int)sizeof(W);
+  const int b = blockIdx.x, nb = P.nb;
+  const MkLayer& L = P.layers[l < P.n_layers ? l : 0];
+  const int qd = P.nq * P.hd, kd = P.nkv * P.hd;
+  R.nseg = 0;
+  auto single = [&](const void* mat, int N, int K) {
+    const int per = (N + nb - 1) / nb;
+    const int r0 = b * per, r1 = min(N, r0 + per);
+    R.K = K;
+    R.paired = false;
+    if (r1 > r0) R.seg[R.nseg++] = MkSeg{(const uint8_t*)mat, r0, r1 - r0, r0, 0};
+  };
+  auto paired = [&](const void* mat, int N, int K) {
+    const int P2 = N / 2, per = (P2 + nb - 1) / nb;
+    const int p0 = b * per, p1 = min(P2, p0 + per);
+    R.K = K;
+    R.paired = true;
+    if (p1 > p0) R.seg[R.nseg++] = MkSeg{(const uint8_t*)mat, 2 * p0, 2 * (p1 - p0), 2 * p0, 0};
+  };
+  switch (ph) {
+    case PH_QKV: paired(L.wqkv, qd + 2 * kd, P.h); break;
+    case PH_OPROJ: single(L.wo, P.h, qd); break;
+    case PH_LMHEAD: single(P.head, P.V, P.h); break;
+    case PH_GATEUP:
+      if (P.E == 0) {
+        paired(L.w_gateup, 2 * P.f, P.h);
+      } else {
+        // Tasks = (slot, gate/up row pair), slot-major, split evenly over CTAs.
+        const int T = P.k * P.f, per = (T + nb - 1) / nb;
+        const int t0 = b * per, t1 = min(T, t0 + per);
+        R.K = P.h;
+        R.paired = true;
+        for (int j = 0; j < P.k; ++j) {
+          const int a = max(t0, j * P.f), e = min(t1, (j + 1) * P.f);
+          if (e <= a) continue;
+          const uint8_t* base = (const uint8_t*)L.w_gateup + (size_t)ids[j] * 2 * P.f * P.h * es;
+          R.seg[R.nseg++] = MkSeg{base, 2 * (a - j * P.f), 2 * (e - a), a, j};
+        }
+      }
+      break;
+    case PH_DOWN:
+      if (P.E == 0) {
+        single(L.w_down, P.h, P.f);
+      } else {
+        const int per = (P.h + nb - 1) / nb;
+        const int r0 = b * per, r1 = min(P.h, r0 + per);
+        R.K = P.f;
+        R.paired = false;
+        if (r1 > r0)
+          for (int j = 0; j < P.k; ++j) {
+            const uint8_t* base = (const uint8_t*)L.w_down + (size_t)ids[j] * P.h * P.f * es;
+            R.seg[R.nseg++] = MkSeg{base, r0, r1 - r0, r0, j};
+          }
+      }
+      break;
+    default: break;
+  }
+  R.rowbytes = R.K * es;
+  int rps = MK_STAGE_BYTES / R.rowbytes;
+  if (R.paired) rps &= ~1;
+  R.rps = rps < 1 ? 1 : rps;
+}
+
+// The phase sequence of one step: per layer QKV, ATTN, [MERGE], OPROJ, GATEUP,
+// DOWN; then LMHEAD.  Index i -> (phase, layer).
+__device__ __forceinline__ int mk_phases_per_layer(const MkParams& P) { return P.merge_phase ? 6 : 5; }
+__device__ __forceinline__ void mk_phase_at(const MkParams& P, int i, int& ph, int& l) {
+  const int ppl = mk_phases_per_layer(P);
+  l = i / ppl;
+  if (l >= P.n_layers) {
+    ph = PH_LMHEAD;
+    return;
+  }
+  int j = i - l * ppl;
+  if (!P.merge_phase && j >= PH_MERGE) ++j;
+  ph = j;
+}
+
+// ------------------------------------------------------------------ dot products
+// This warp's share of one row's dot product: chunks c = 32*(warp + 8i) + lane
+// of the 16-byte chunks, so the 8 compute warps split every row's K.
+template <typename W>
+__device__ __forceinline__ float mk_dot_slice(const uint8_t* row, const float* xs, int K) {
+  constexpr int V = Chunk<W>::N;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float a = 0.f;
+  for (int c = 32 * warp + lane; c < K / V; c += MK_COMPUTE) {
+    float w[V];
+    Chunk<W>::widen(*reinterpret_cast<const uint4*>(row + (size_t)c * 16), w);
+    const float* xv = xs + c * V;
+#pragma unroll
+    for (int e = 0; e < V; ++e) a = fmaf(w[e], xv[e], a);
+  }
+  return warp_sum(a);
+}
+
+// Dot of one weight row in shared memory with the f32 vector xs (also in
+// shared memory), one warp; K * sizeof(W) is a multiple of 16 bytes.
+template <typename W>
+__device__ __forceinline__ float mk_dot_row(const uint8_t* row, const float* xs, int K) {
+  constexpr int V = Chunk<W>::N;
+  const int lane = threadIdx.x & 31;
+  float a = 0.f;
+  for (int c = lane; c < K / V; c += 32) {
+    float w[V];
+    Chunk<W>::widen(*reinterpret_cast<const uint4*>(row + (size_t)c * 16), w);
+    const float* xv = xs + c * V;
+#pragma unroll
+    for (int e = 0; e < V; ++e) a = fmaf(w[e], xv[e], a);
+  }
+  return warp_sum(a);
+}
+
+}  // namespace dec
+
+namespace dec {
+
+// ------------------------------------------------------------------ compute prologues
+// xs = v / sqrt(mean(v^2) + eps) * wn over the 256 compute threads, with v the
+// embedding row (erow) or the residual x (read from L2).
+template <typename W>
+__device__ void mk_norm_to_xs(const float* x, const W* erow, const float* __restrict__ wn, int K, float eps,
+                              float* xs, MkMisc* M) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float ss = 0.f;
+  for (int k = tid; k < K; k += MK_COMPUTE) {
+    const float v = erow ? to_f32(erow[k]) : __ldcg(x + k);
+    xs[k] = v;
+    ss = fmaf(v, v, ss);
+  }
+  ss = warp_sum(ss);
+  if (lane == 0) M->red[warp] = ss;
+  compute_sync();
+  if (warp == 0) {
+    float v = lane < MK_COMPUTE_WARPS ? M->red[lane] : 0.f;
+    v = warp_sum(v);
+    if (lane == 0) M->red[32] = v;
+  }
+  compute_sync();
+  const float inv = 1.0f / sqrtf(M->red[32] / (float)K + eps);
+  for (int k = tid; k < K; k += MK_COMPUTE) xs[k] = xs[k] * inv * wn[k];
+  compute_sync();
+}
+
+__device__ void mk_copy_to_xs(const float* src, int K, float* xs) {
+  for (int k = threadIdx.x; k < K; k += MK_COMPUTE) xs[k] = __ldcg(src + k);
+  compute_sync();
+}
+
+// Merges split partials of `heads` query heads [h0, h0+heads) into dst
+// (dst[(h - h0) * HD + d]); scale is [heads][nsplit] scratch.  Weight of split
+// s: exp(m_s - M) / sum_s l_s exp(m_s - M) (one-pass softmax state, rml Attend).
+__device__ void mk_merge_heads(const float* part, int nsplit, int HD, int h0, int heads, float* scale, float* dst,
+                               bool dst_global) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int hh = warp; hh < heads; hh += MK_COMPUTE_WARPS) {
+    const float* base = part + (size_t)(h0 + hh) * nsplit * (HD + 2);
+    float mloc = -INFINITY;
+    for (int s2 = lane; s2 < nsplit; s2 += 32) mloc = fmaxf(mloc, __ldcg(base + s2 * (HD + 2) + HD));
+    const float Mx = warp_max(mloc);
+    float lsum = 0.f;
+    for (int s2 = lane; s2 < nsplit; s2 += 32) {
+      const float ms = __ldcg(base + s2 * (HD + 2) + HD);
+      const float sc = ms == -INFINITY ? 0.f : __expf(ms - Mx);
+      scale[hh * nsplit + s2] = sc;
+      lsum = fmaf(__ldcg(base + s2 * (HD + 2) + HD + 1), sc, lsum);
+    }
+    const float Ls = warp_sum(lsum);
+    __syncwarp();
+    for (int s2 = lane; s2 < nsplit; s2 += 32) scale[hh * nsplit + s2] /= Ls;
+  }
+  compute_sync();
+  for (int idx = tid; idx < heads * HD; idx += MK_COMPUTE) {
+    const int hh = idx / HD, d = idx - hh * HD;
+    const float* base = part + (size_t)(h0 + hh) * nsplit * (HD + 2) + d;
+    const float* sc = scale + hh * nsplit;
+    float o = 0.f;
+#pragma unroll 8
+    for (int s2 = 0; s2 < nsplit; ++s2) o = fmaf(sc[s2], __ldcg(base + (size_t)s2 * (HD + 2)), o);
+    if (dst_global) dst[(size_t)(h0 + hh) * HD + d] = o;
+    else dst[idx] = o;
+  }
+  compute_sync();
+}
+
+// Router of one MoE layer, computed identically by every CTA: logits = Wr xs,
+// top-k by repeated selection (ties -> lower id), weights renormalised over the
+// selection (Pantheon Mixture of Experts; rml Mixture of experts).
+template <typename W>
+__device__ void mk_router(const MkParams& P, int l, const float* xs, MkMisc* M) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const W* router = (const W*)P.layers[l].router;
+  constexpr int V = Chunk<W>::N;
+  for (int e = warp; e < P.E; e += MK_COMPUTE_WARPS) {
+    const W* row = router + (size_t)e * P.h;
+    float a = 0.f;
+    for (int c = lane; c < P.h / V; c += 32) {
+      float wv[V];
+      Chunk<W>::widen(ld_stream16(row + (size_t)c * V), wv);
+#pragma unroll
+      for (int q = 0; q < V; ++q) a = fmaf(wv[q], xs[c * V + q], a);
+    }
+    a = warp_sum(a);
+    if (lane == 0) M->logits[e] = a;
+  }
+  compute_sync();
+  if (tid == 0) {
+    int sel[MAX_EXPERTS_USED];
+    float mx = -INFINITY;
+    for (int j = 0; j < P.k; ++j) {
+      int best = -1;
+      for (int e = 0; e < P.E; ++e) {
+        bool taken = false;
+        for (int t = 0; t < j; ++t) taken |= (sel[t] == e);
+        if (taken) continue;
+        if (best < 0 || M->logits[e] > M->logits[best]) best = e;
+      }
+      sel[j] = best;
+      mx = fmaxf(mx, M->logits[best]);
+    }
+    float pj[MAX_EXPERTS_USED], tot = 0.f;
+    for (int j = 0; j < P.k; ++j) {
+      pj[j] = expf(M->logits[sel[j]] - mx);
+      tot += pj[j];
+    }
+    for (int j = 0; j < P.k; ++j) {
+      M->ids[j] = sel[j];
+      M->wts[j] = pj[j] / tot;
+    }
+    if (blockIdx.x == 0) {
+      for (int j = 0; j < P.k; ++j) P.ids_out[j] = sel[j];
+      if (P.trace_ids) {
+        const size_t row = (size_t)l * P.trace_cap + (P.pos % P.trace_cap);
+        for (int j = 0; j < P.k; ++j) P.trace_ids[row * P.k + j] = sel[j];
+        for (int e = 0; e < P.E; ++e) P.trace_logits[row * P.E + e] = M->logits[e];
+      }
+    }
+    __threadfence_block();
+    *(volatile int*)&M->moe_ready = l + 1;   // releases the producer for this layer's experts
+  }
+  compute_sync();
+}
+
+}  // namespace dec
+
+namespace dec {
+
+// ------------------------------------------------------------------ GEMV phase (consumer side)
+// Warp w reduces units u = w, w+8, ... of every segment (a unit is a row, or a
+// row pair for the paired epilogues), reading each row in <= 4 KB pieces from
+// its own ring in the order its producer lane streams them.
+template <typename W, typename KV>
+__device__ bool mk_gemv_phase(const MkParams& P, int ph, int l, const MkRows& R, uint8_t* ring, MkMisc* M,
+                              float* xs, uint32_t& sc, float& best, int& bidx) {
+  constexpr int V = Chunk<W>::N;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const MkLayer& L = P.layers[l < P.n_layers ? l : 0];
+  const int qd = P.nq * P.hd, kd = P.nkv * P.hd;
+  volatile int* abort_flag = &M->abort_flag;
+  uint8_t* wring = ring + (size_t)warp * MK_STAGES * MK_STAGE_BYTES;
+  bool ok = true;
+  for (int si = 0; si < R.nseg; ++si) {
+    const MkSeg& S = R.seg[si];
+    if (ph == PH_DOWN && P.E > 0) {
+      // Expert slot S.slot multiplies its own activation vector.
+      compute_sync();
+      mk_copy_to_xs(P.act + (size_t)S.slot * P.f, P.f, xs);
+    }
+    const int units = R.paired ? S.rows / 2 : S.rows;
+    for (int u = warp; u < units && ok; u += MK_COMPUTE_WARPS) {
+      const int nrow = R.paired ? 2 : 1;
+      float sums[2] = {0.f, 0.f};
+      for (int q = 0; q < nrow && ok; ++q) {
+        float acc = 0.f;
+        for (int off = 0; off < R.rowbytes; off += MK_STAGE_BYTES) {
+          const int len = min(MK_STAGE_BYTES, R.rowbytes - off);
+          const int st = sc % MK_STAGES;
+          const uint32_t par = (sc / MK_STAGES) & 1u;
+          if (!mk_mbar_wait(&M->full[warp][st], par, abort_flag, P.st, 201)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* piece = wring + (size_t)st * MK_STAGE_BYTES;
+          const int c0 = off / 16;
+          for (int c = lane; c < len / 16; c += 32) {
+            float wv[V];
+            Chunk<W>::widen(*reinterpret_cast<const uint4*>(piece + (size_t)c * 16), wv);
+            const float* xv = xs + (c0 + c) * V;
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc = fmaf(wv[e], xv[e], acc);
+          }
+          __syncwarp();
+          if (lane == 0) mk_mbar_arrive(&M->empty[warp][st]);
+          ++sc;
+          if (lane == 0) M->consumed[warp] = (int)sc;
+        }
+        sums[q] = warp_sum(acc);
+      }
+      if (!ok || lane != 0) continue;
+      if (R.paired) {
+        const int rl = 2 * u;
+        const float a0 = sums[0], a1 = sums[1];
+        if (ph == PH_QKV) {
+          const int row = S.row0 + rl;
+          float v0 = a0, v1 = a1;
+          if (L.bqkv) {
+            v0 += L.bqkv[row];
+            v1 += L.bqkv[row + 1];
+          }
+          if (row < qd + kd) {
+            const int d = (row < qd ? row : row - qd) % P.hd;
+            const float2 cs = M->cs[d >> 1];
+            const float b0 = v0 * cs.x - v1 * cs.y, b1 = v0 * cs.y + v1 * cs.x;
+            v0 = b0;
+            v1 = b1;
+          }
+          const int slot = P.sliding > 0 ? P.pos % P.max_seq : P.pos;
+          if (row < qd) {
+            P.q[row] = v0;
+            P.q[row + 1] = v1;
+          } else {
+            const bool is_k = row < qd + kd;
+            KV* dst = (KV*)(is_k ? L.kc : L.vc);
+            const size_t o = (size_t)slot * kd + (is_k ? row - qd : row - qd - kd);
+            dst[o] = from_f32<KV>(v0);
+            dst[o + 1] = from_f32<KV>(v1);
+          }
+        } else {  // PH_GATEUP: act[task] = silu(gate) * up
+          const int task = P.E > 0 ? S.out0 + (rl >> 1) : (S.row0 + rl) >> 1;
+          P.act[task] = silu_f(a0) * a1;
+        }
+      } else {
+        const int rl = u;
+        const float a = sums[0];
+        const int row = S.row0 + rl;
+        if (ph == PH_LMHEAD) {
+          if (P.logits) P.logits[row] = a;
+          if (a > best || (a == best && row < bidx)) {
+            best = a;
+            bidx = row;
+          }
+        } else if (ph == PH_DOWN && P.E > 0) {
+          float& acc = M->acc[rl];
+          acc = S.slot == 0 ? M->wts[0] * a : fmaf(M->wts[S.slot], a, acc);
+        } else {  // PH_OPROJ, dense PH_DOWN: the residual row this CTA owns
+          P.x[row] = __ldcg(P.x + row) + a;
+        }
+      }
+    }
+  }
+  if (ph == PH_DOWN && P.E > 0) {
+    compute_sync();
+    if (R.nseg > 0)
+      for (int i = threadIdx.x; i < R.seg[0].rows; i += MK_COMPUTE) {
+        const int row = R.seg[0].row0 + i;
+        P.x[row] = __ldcg(P.x + row) + M->acc[i];
+      }
+  }
+  return ok;
+}
+
+}  // namespace dec
+
+namespace dec {
+
+// ------------------------------------------------------------------ attention phase
+// Task (g, split): the G query heads of kv head g over slots
+// [split*sps, split*sps + sps) intersected with the readable slots
+// (min(pos+1, max_seq) under a window, else pos+1; Pantheon Sliding Window),
+// one-pass online softmax in chunks of MK_KS keys (rml Attend).
+template <typename KV, int HD>
+__device__ void mk_attention(const MkParams& P, int l, uint8_t* ureg, MkMisc* M) {
+  constexpr int CE = 16 / sizeof(KV), KROW = HD + CE, CPR = HD / CE;
+  constexpr int OUTS = (MAX_GROUP * HD + MK_COMPUTE - 1) / MK_COMPUTE;
+  const MkLayer& L = P.layers[l];
+  const KV* kc = (const KV*)L.kc;
+  const KV* vc = (const KV*)L.vc;
+  const int G = P.nq / P.nkv, kd = P.nkv * HD;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  KV* ks = reinterpret_cast<KV*>(ureg);
+  KV* vs = ks + MK_KS * KROW;
+  float* qs = reinterpret_cast<float*>(vs + MK_KS * HD);
+  float* ps = qs + G * HD;
+  const int m = P.sliding > 0 ? min(P.pos + 1, P.max_seq) : P.pos + 1;
+  const float scale = 1.0f / sqrtf((float)HD);
+  const int tasks = P.nkv * P.nsplit;
+  for (int t = blockIdx.x; t < tasks; t += P.nb) {
+    const int g = t / P.nsplit, split = t - g * P.nsplit;
+    const int s0 = split * P.sps, j1 = min(min(s0 + P.sps, P.max_seq), m);
+    for (int i = tid; i < G * HD; i += MK_COMPUTE) qs[i] = __ldcg(P.q + (size_t)g * G * HD + i) * scale;
+    if (tid < MAX_GROUP) {
+      M->mrow[tid] = -INFINITY;
+      M->lrow[tid] = 0.f;
+    }
+    float acc[OUTS];
+#pragma unroll
+    for (int r = 0; r < OUTS; ++r) acc[r] = 0.f;
+    for (int c0 = s0; c0 < j1; c0 += MK_KS) {
+      const int nt = min(MK_KS, j1 - c0);
+      compute_sync();   // previous chunk's readers are done
+      for (int i = tid; i < nt * CPR; i += MK_COMPUTE) {
+        const int r = i / CPR, c = i - r * CPR;
+        const size_t go = (size_t)(c0 + r) * kd + (size_t)g * HD + c * CE;
+        cp_async16(ks + r * KROW + c * CE, kc + go);
+        cp_async16(vs + r * HD + c * CE, vc + go);
+      }
+      cp_async_commit();
+      cp_async_wait_all();
+      compute_sync();
+      for (int idx = tid; idx < G * nt; idx += MK_COMPUTE) {
+        const int hh = idx / nt, j = idx - hh * nt;
+        const float* qv = qs + hh * HD;
+        const KV* kr = ks + j * KROW;
+        float sdot = 0.f;
+#pragma unroll 8
+        for (int d = 0; d < HD; ++d) sdot = fmaf(qv[d], to_f32(kr[d]), sdot);
+        ps[hh * MK_KS + j] = sdot;
+      }
+      compute_sync();
+      for (int hh = warp; hh < G; hh += MK_COMPUTE_WARPS) {
+        float* pr = ps + hh * MK_KS;
+        const float sa = lane < nt ? pr[lane] : -INFINITY;
+        const float sb = lane + 32 < nt ? pr[lane + 32] : -INFINITY;
+        const float mnew = fmaxf(M->mrow[hh], warp_max(fmaxf(sa, sb)));
+        const float pa = lane < nt ? __expf(sa - mnew) : 0.f;
+        const float pb = lane + 32 < nt ? __expf(sb - mnew) : 0.f;
+        const float psum = warp_sum(pa + pb);
+        if (lane < nt) pr[lane] = pa;
+        if (lane + 32 < nt) pr[lane + 32] = pb;
+        __syncwarp();
+        if (lane == 0) {
+          const float a = __expf(M->mrow[hh] - mnew);
+          M->alpha[hh] = a;
+          M->lrow[hh] = M->lrow[hh] * a + psum;
+          M->mrow[hh] = mnew;
+        }
+      }
+      compute_sync();
+#pragma unroll
+      for (int r = 0; r < OUTS; ++r) {
+        const int idx = tid + r * MK_COMPUTE;
+        if (idx < G * HD) {
+          const int hh = idx / HD, d = idx - hh * HD;
+          const float* pr = ps + hh * MK_KS;
+          float o = acc[r] * M->alpha[hh];
+          for (int j = 0; j < nt; ++j) o = fmaf(pr[j], to_f32(vs[j * HD + d]), o);
+          acc[r] = o;
+        }
+      }
+    }
+    compute_sync();
+    if (P.nsplit == 1) {
+#pragma unroll
+      for (int r = 0; r < OUTS; ++r) {
+        const int idx = tid + r * MK_COMPUTE;
+        if (idx < G * HD) P.attn[(size_t)g * G * HD + idx] = acc[r] / M->lrow[idx / HD];
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < OUTS; ++r) {
+        const int idx = tid + r * MK_COMPUTE;
+        if (idx < G * HD) {
+          const int hh = idx / HD, d = idx - hh * HD;
+          P.part[((size_t)(g * G + hh) * P.nsplit + split) * (HD + 2) + d] = acc[r];
+        }
+      }
+      if (tid < G) {
+        float* pp = P.part + ((size_t)(g * G + tid) * P.nsplit + split) * (HD + 2);
+        pp[HD] = M->mrow[tid];
+        pp[HD + 1] = M->lrow[tid];
+      }
+    }
+    compute_sync();   // the task's smem is reused by the next task
+  }
+}
+
+}  // namespace dec
+
+namespace dec {
+
+// L2 prefetch of the K/V rows this CTA's attention tasks of layer l will read
+// (issued one phase early; the current position's row is rewritten in L2 by
+// the QKV phase before the attention phase reads it).
+__device__ void mk_prefetch_attention_kv(const MkParams& P, int l, int HD) {
+  const MkLayer& L = P.layers[l];
+  const int kvb = P.kv_bytes;
+  const int kd = P.nkv * HD;
+  const int m = P.sliding > 0 ? min(P.pos + 1, P.max_seq) : P.pos + 1;
+  const int tasks = P.nkv * P.nsplit;
+  int idx = threadIdx.x;
+  for (int t = blockIdx.x; t < tasks; t += P.nb) {
+    const int g = t / P.nsplit, split = t - g * P.nsplit;
+    const int s0 = split * P.sps, j1 = min(min(s0 + P.sps, P.max_seq), m);
+    const int n = j1 > s0 ? j1 - s0 : 0;
+    for (; idx < 2 * n; idx += MK_COMPUTE) {
+      const int r = idx >> 1;
+      const uint8_t* base = (const uint8_t*)((idx & 1) ? L.vc : L.kc);
+      mk_prefetch_l2(base + ((size_t)(s0 + r) * kd + (size_t)g * HD) * kvb, (uint32_t)(HD * kvb));
+    }
+    idx -= 2 * n;
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <typename W, typename KV, int HD>
+__global__ void __launch_bounds__(MK_THREADS, 1) k_decode_step(const MkParams P) {
+  extern __shared__ __align__(1024) uint8_t mk_smem[];
+  uint8_t* ring = mk_smem;
+  uint8_t* ureg = mk_smem + MK_RING_BYTES;
+  MkMisc* M = reinterpret_cast<MkMisc*>(ureg + P.u_bytes);
+  float* xs = reinterpret_cast<float*>(ureg);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int nphase = P.n_layers * mk_phases_per_layer(P) + 1;
+
+  if (tid == 0) {
+    for (int w = 0; w < MK_COMPUTE_WARPS; ++w)
+      for (int s = 0; s < MK_STAGES; ++s) {
+        mk_mbar_init(&M->full[w][s], 1);
+        mk_mbar_init(&M->empty[w][s], 1);
+      }
+    M->abort_flag = 0;
+    M->moe_ready = 0;
+    for (int w = 0; w < MK_COMPUTE_WARPS; ++w) M->consumed[w] = 0;
+    int t = P.d_token ? *P.d_token : P.token;
+    if (t < 0 || t >= P.V) {
+      raise_error(P.st, ERR_TOKEN, 0);
+      t = 0;
+    }
+    M->token = t;
+    if (blockIdx.x == 0) {
+      P.st->token = t;
+      P.st->pos = P.pos;
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  for (int i = tid; i < P.hd / 2; i += MK_THREADS) {
+    double sn, cn;
+    sincos((double)P.pos * P.inv_freq[i], &sn, &cn);
+    M->cs[i] = make_float2((float)cn, (float)sn);
+  }
+  __syncthreads();
+  volatile int* abort_flag = &M->abort_flag;
+
+  if (warp >= MK_COMPUTE_WARPS) {
+    // ---------------- producer: warp 8+w streams compute warp w's rows of every phase, in order
+    const int w = warp - MK_COMPUTE_WARPS;
+    if ((tid & 31) == 0) {
+      uint8_t* wring = ring + (size_t)w * MK_STAGES * MK_STAGE_BYTES;
+      uint32_t sc = 0;
+      bool ok = true;
+      for (int i = 0; i < nphase && ok && !*abort_flag; ++i) {
+        int ph, l;
+        mk_phase_at(P, i, ph, l);
+        if (!mk_is_gemv(ph)) continue;
+        if (P.E > 0 && (ph == PH_GATEUP || ph == PH_DOWN)) {
+          // Expert rows are known once this layer's router has run.
+          const uint64_t t0 = globaltimer_ns();
+          while (*(volatile int*)&M->moe_ready < l + 1 && !*abort_flag) {
+            if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+              raise_error(P.st, ERR_TIMEOUT, 301);
+              *abort_flag = 1;
+            }
+          }
+          if (*abort_flag) break;
+        }
+        MkRows R;
+        mk_phase_rows<W>(P, ph, l, M->ids, R);
+        for (int si = 0; si < R.nseg && ok; ++si) {
+          const MkSeg& S = R.seg[si];
+          const int units = R.paired ? S.rows / 2 : S.rows;
+          const int nrow = R.paired ? 2 : 1;
+          for (int u = w; u < units && ok; u += MK_COMPUTE_WARPS) {
+            for (int q = 0; q < nrow && ok; ++q) {
+              const int rl = R.paired ? 2 * u + q : u;
+              const uint8_t* src = S.base + (size_t)(S.row0 + rl) * R.rowbytes;
+              for (int off = 0; off < R.rowbytes; off += MK_STAGE_BYTES) {
+                const int len = min(MK_STAGE_BYTES, R.rowbytes - off);
+                const int st = sc % MK_STAGES;
+                const uint32_t par = (sc / MK_STAGES) & 1u;
+                if (!mk_mbar_wait(&M->empty[w][st], par ^ 1u, abort_flag, P.st, 302)) {
+                  ok = false;
+                  break;
+                }
+                mk_mbar_expect_tx(&M->full[w][st], (uint32_t)len);
+                mk_bulk_load(wring + (size_t)st * MK_STAGE_BYTES, src + off, (uint32_t)len, &M->full[w][st]);
+                ++sc;
+              }
+            }
+          }
+        }
+      }
+      if (*abort_flag) {
+        // Copies issued but never consumed must land before the CTA exits.
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t k = (uint32_t)*(volatile int*)&M->consumed[w]; k < sc; ++k)
+          while (!mk_mbar_try(&M->full[w][k % MK_STAGES], (k / MK_STAGES) & 1u) &&
+                 globaltimer_ns() - t0 < 100000000ull) {
+          }
+      }
+    }
+    return;
+  }
+
+  // ---------------- compute warps
+  if (P.stamps && blockIdx.x == 0 && tid == 0) P.stamps[0] = globaltimer_ns();
+  const int token = M->token;
+  const int qd = P.nq * P.hd;
+  // The residual starts as the token's embedding row (every CTA writes a share).
+  for (int i = blockIdx.x * MK_COMPUTE + tid; i < P.h; i += P.nb * MK_COMPUTE)
+    P.x[i] = to_f32(((const W*)P.embed)[(size_t)token * P.h + i]);
+  uint32_t sc = 0;
+  float best = -INFINITY;
+  int bidx = 0x7fffffff;
+  for (int i = 0; i < nphase; ++i) {
+    int ph, l;
+    mk_phase_at(P, i, ph, l);
+    const MkLayer& L = P.layers[l < P.n_layers ? l : 0];
+    bool ok = true;
+    switch (ph) {
+      case PH_QKV:
+        mk_prefetch_attention_kv(P, l, P.hd);
+        mk_norm_to_xs<W>(P.x, l == 0 ? (const W*)P.embed + (size_t)token * P.h : nullptr, L.attn_norm, P.h, P.eps,
+                         xs, M);
+        break;
+      case PH_ATTN:
+        mk_attention<KV, HD>(P, l, ureg, M);
+        break;
+      case PH_MERGE:
+        for (int h0 = blockIdx.x; h0 < P.nq; h0 += P.nb)
+          mk_merge_heads(P.part, P.nsplit, HD, h0, 1, xs, P.attn, true);
+        break;
+      case PH_OPROJ:
+        if (P.nsplit > 1 && !P.merge_phase) mk_merge_heads(P.part, P.nsplit, HD, 0, P.nq, xs + qd, xs, false);
+        else mk_copy_to_xs(P.attn, qd, xs);
+        break;
+      case PH_GATEUP:
+        mk_norm_to_xs<W>(P.x, nullptr, L.ffn_norm, P.h, P.eps, xs, M);
+        if (P.E > 0) mk_router<W>(P, l, xs, M);
+        break;
+      case PH_DOWN:
+        if (P.E == 0) mk_copy_to_xs(P.act, P.f, xs);
+        break;
+      case PH_LMHEAD:
+        mk_norm_to_xs<W>(P.x, nullptr, P.out_norm, P.h, P.eps, xs, M);
+        break;
+    }
+    if (mk_is_gemv(ph)) {
+      MkRows R;
+      mk_phase_rows<W>(P, ph, l, M->ids, R);
+      ok = mk_gemv_phase<W, KV>(P, ph, l, R, ring, M, xs, sc, best, bidx);
+    }
+    if (!ok || *abort_flag) break;
+    if (ph != PH_LMHEAD && !mk_grid_sync(P.st, (unsigned)P.nb, abort_flag, 400 + ph)) break;
+    if (P.stamps && blockIdx.x == 0 && tid == 0) P.stamps[i + 1] = globaltimer_ns();
+  }
+  if (*abort_flag || !P.d_argmax) return;
+
+  // ---------------- argmax: CTA best -> per-CTA partial -> last CTA merges
+  const int lane = tid & 31;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+    if (ov > best || (ov == best && oi < bidx)) {
+      best = ov;
+      bidx = oi;
+    }
+  }
+  if (lane == 0) {
+    M->wbest[warp] = best;
+    M->wbidx[warp] = bidx;
+  }
+  compute_sync();
+  if (tid == 0) {
+    float b = M->wbest[0];
+    int bi = M->wbidx[0];
+    for (int w = 1; w < MK_COMPUTE_WARPS; ++w)
+      if (M->wbest[w] > b || (M->wbest[w] == b && M->wbidx[w] < bi)) {
+        b = M->wbest[w];
+        bi = M->wbidx[w];
+      }
+    P.amax_val[blockIdx.x] = b;
+    P.amax_idx[blockIdx.x] = bi;
+    __threadfence();
+    M->is_last = atomicAdd(&P.st->counters[CNT_ARGMAX], 1u) == (unsigned)P.nb - 1;
+  }
+  compute_sync();
+  if (!M->is_last) return;
+  __threadfence();
+  float b = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int i = tid; i < P.nb; i += MK_COMPUTE) {
+    const float v = __ldcg(P.amax_val + i);
+    const int vi = __ldcg(P.amax_idx + i);
+    if (v > b || (v == b && vi < bi)) {
+      b = v;
+      bi = vi;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, b, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > b || (ov == b && oi < bi)) {
+      b = ov;
+      bi = oi;
+    }
+  }
+  compute_sync();
+  if (lane == 0) {
+    M->wbest[warp] = b;
+    M->wbidx[warp] = bi;
+  }
+  compute_sync();
+  if (tid == 0) {
+    for (int w = 1; w < MK_COMPUTE_WARPS; ++w)
+      if (M->wbest[w] > M->wbest[0] || (M->wbest[w] == M->wbest[0] && M->wbidx[w] < M->wbidx[0])) {
+        M->wbest[0] = M->wbest[w];
+        M->wbidx[0] = M->wbidx[w];
+      }
+    *P.d_argmax = M->wbidx[0];
+    P.st->counters[CNT_ARGMAX] = 0u;
+  }
+}
+
+}  // namespace dec
+
+namespace dec {
+
+// ------------------------------------------------------------------ host side
+static size_t mk_u_bytes(const dec_config& c, int nsplit) {
+  const size_t kvs = c.kv_dtype == DEC_BF16 ? 2 : 4;
+  const size_t ce = 16 / kvs, hd = c.head_dim, G = c.n_heads / c.n_kv_heads;
+  size_t xs = (size_t)c.hidden;
+  if ((size_t)c.n_heads * hd > xs) xs = (size_t)c.n_heads * hd;
+  if ((size_t)c.ffn > xs) xs = c.ffn;
+  xs = (xs + (size_t)c.n_heads * nsplit) * sizeof(float);
+  const size_t attn = MK_KS * (hd + ce) * kvs + MK_KS * hd * kvs + G * hd * 4 + G * MK_KS * 4;
+  const size_t u = xs > attn ? xs : attn;
+  return (u + 127) / 128 * 128;
+}
+
+size_t mk_smem_bytes(const dec_config& c, int nsplit) {
+  return (size_t)MK_RING_BYTES + mk_u_bytes(c, nsplit) + sizeof(MkMisc);
+}
+
+template <typename W, typename KV>
+static void* mk_pick(int hd) {
+  if (hd == 64) return (void*)k_decode_step<W, KV, 64>;
+  if (hd == 128) return (void*)k_decode_step<W, KV, 128>;
+  return (void*)k_decode_step<W, KV, 16>;
+}
+
+static void* mk_func(const dec_config& c) {
+  const bool wb = c.weight_dtype == DEC_BF16, kb = c.kv_dtype == DEC_BF16;
+  if (wb && kb) return mk_pick<__nv_bfloat16, __nv_bfloat16>(c.head_dim);
+  if (wb) return mk_pick<__nv_bfloat16, float>(c.head_dim);
+  if (kb) return mk_pick<float, __nv_bfloat16>(c.head_dim);
+  return mk_pick<float, float>(c.head_dim);
+}
+
+// Whether the persistent step fits this configuration on this GPU; sets the
+// kernel's shared-memory limit and the grid (one CTA per SM).
+bool mk_prepare(Model& m, int num_sms) {
+  const dec_config& c = m.cfg;
+  const int es = c.weight_dtype == DEC_BF16 ? 2 : 4;
+  m.mk_ok = false;
+  (void)es;
+  // MoE down keeps one row sum per owned row; RoPE table of up to 64 pairs.
+  if ((c.hidden + num_sms - 1) / num_sms > 256 || c.head_dim / 2 > 64) return false;
+  if (m.nsplit > 1 && m.attn_sps % MK_KS != 0) return false;
+  const size_t smem = mk_smem_bytes(c, m.nsplit);
+  if (smem > 227 * 1024) return false;
+  void* fn = mk_func(c);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return false;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, MK_THREADS, smem) != cudaSuccess || per_sm < 1)
+    return false;
+  m.mk_smem = smem;
+  m.mk_nb = num_sms;
+  m.mk_ok = true;
+  return true;
+}
+
+void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, int32_t token, int32_t pos,
+                      float* logits, int32_t* d_argmax) {
+  const dec_config& c = m.cfg;
+  const Scratch& S = m.s;
+  MkParams P;
+  P.n_layers = c.n_layers;
+  P.h = c.hidden;
+  P.nq = c.n_heads;
+  P.nkv = c.n_kv_heads;
+  P.hd = c.head_dim;
+  P.f = c.ffn;
+  P.V = c.vocab;
+  P.E = c.n_experts;
+  P.k = c.n_experts ? c.n_experts_used : 1;
+  P.max_seq = c.max_seq;
+  P.sliding = c.sliding_window;
+  P.nsplit = m.nsplit;
+  P.sps = m.attn_sps;
+  P.merge_phase = (m.nsplit > 1 && (size_t)c.n_heads * m.nsplit * (c.head_dim + 2) * 4 > 64 * 1024) ? 1 : 0;
+  P.nb = m.mk_nb;
+  P.eps = c.rms_eps;
+  P.layers = m.mk_layers;
+  P.embed = m.tok_embd;
+  P.out_norm = m.out_norm;
+  P.head = m.head;
+  P.st = S.st;
+  P.inv_freq = S.inv_freq;
+  P.x = S.x;
+  P.q = S.q;
+  P.attn = S.attn;
+  P.act = S.act;
+  P.part = S.part;
+  P.amax_val = S.amax_val;
+  P.amax_idx = S.amax_idx;
+  P.ids_out = S.ids;
+  P.logits = logits;
+  P.d_argmax = d_argmax;
+  P.d_token = d_token;
+  P.token = token;
+  P.pos = pos;
+  P.trace_ids = m.trace_ids;
+  P.trace_logits = m.trace_logits;
+  P.trace_cap = m.trace_cap;
+  P.u_bytes = (int)mk_u_bytes(c, m.nsplit);
+  P.stamps = m.mk_stamps;
+  P.kv_bytes = c.kv_dtype == DEC_BF16 ? 2 : 4;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(m.mk_nb);
+  cfg.blockDim = dim3(MK_THREADS);
+  cfg.dynamicSmemBytes = m.mk_smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&P};
+  timer_begin(m, DEC_K_STEP, s);
+  cudaLaunchKernelExC(&cfg, mk_func(c), args);
+  timer_end(m, DEC_K_STEP, s);
+  count_launch(m);
+}
+
+}  // namespace dec

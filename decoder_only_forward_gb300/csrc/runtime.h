@@ -12,6 +12,20 @@
 
 namespace dec {
 
+// Per-layer pointers as the persistent decode kernel reads them (device table).
+struct MkLayer {
+  const float* attn_norm;
+  const void* wqkv;
+  const float* bqkv;
+  const void* wo;
+  const float* ffn_norm;
+  const void* w_gateup;
+  const void* w_down;
+  const void* router;
+  void* kc;
+  void* vc;
+};
+
 struct LayerPtrs {
   const float* attn_norm;
   const void* wqkv;
@@ -86,6 +100,11 @@ struct Model {
   Scratch s;
   int nsplit;           // split-K CTAs per kv head in decode attention
   int attn_sps;         // KV slots owned by one split
+  const MkLayer* mk_layers;  // device copy of the layer table (persistent decode kernel)
+  size_t mk_smem;       // its dynamic shared memory
+  int mk_nb;            // its grid (one CTA per SM)
+  bool mk_ok;           // the persistent kernel fits this configuration
+  unsigned long long* mk_stamps;  // nullable phase timestamps (dec_phase_stamps)
   int lm_grid;          // CTAs of the LM head kernel
   int32_t* trace_ids;   // nullable
   float* trace_logits;  // nullable
@@ -98,6 +117,7 @@ struct Model {
 struct WsPlan {
   size_t st, inv_freq, rope_tab, x, q, attn, act, nbuf, ids, wts, part, amax_val, amax_idx, tokens;
   size_t X, A, Q, KVlin_k, KVlin_v, pf_ids, pf_wts, pf_count, pf_offset, pf_rows, pf_inv, Asort, Y, ACT;
+  size_t mk_layers;     // layer table of the persistent decode kernel
   size_t kv;            // start of the KV rings
   size_t kv_layer_bytes;
   size_t total;
@@ -135,6 +155,12 @@ void launch_decode_body(const Model& m, cudaStream_t s, const int32_t* d_token, 
                         float* logits, int32_t* d_argmax);
 // Host handle of the setup kernel (for updating its node in a captured graph).
 const void* set_step_kernel();
+
+// Persistent single-kernel decode step (decode_mk.cu).
+size_t mk_smem_bytes(const dec_config& c, int nsplit);
+bool mk_prepare(Model& m, int num_sms);
+void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, int32_t token, int32_t pos,
+                      float* logits, int32_t* d_argmax);
 // Final RMSNorm + LM head (+ argmax) of one residual row x.
 void launch_lmhead(const Model& m, cudaStream_t s, const float* x, float* logits, int32_t* d_argmax);
 

@@ -26,10 +26,10 @@ STATUS_NAMES = {0: "DEC_OK", 1: "DEC_EINVAL", 2: "DEC_ERANGE", 3: "DEC_ECUDA", 4
 EXPORTED = ["dec_config_validate", "dec_workspace_bytes", "dec_create", "dec_prefill", "dec_decode",
             "dec_decode_dev", "dec_kv_reset", "dec_length", "dec_kv_layer", "dec_set_trace",
             "dec_check", "dec_timing_enable", "dec_timing_read", "dec_launch_count", "dec_destroy",
-            "dec_last_error", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc", "dec_gemm_bf16", "dec_set_graph"]
+            "dec_last_error", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc", "dec_gemm_bf16", "dec_set_graph", "dec_set_fused", "dec_phase_stamps"]
 
 KERNEL_CLASSES = {"qkv": 1, "attn": 2, "oproj": 3, "gateup": 4, "down": 5, "lmhead": 6, "router": 7,
-                  "pf_gemm": 8, "pf_attn": 9}
+                  "pf_gemm": 8, "pf_attn": 9, "step": 10}
 
 
 class Config(ctypes.Structure):
@@ -78,6 +78,8 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "dec_attend_noalloc": (I32, [P, P, P, I32, I32, I32, I32, I32, I32, I32, P, P]),
         "dec_gemm_bf16": (I32, [P, P, P, P, I32, I32, I32, P]),
         "dec_set_graph": (I32, [P, I32]),
+        "dec_set_fused": (I32, [P, I32]),
+        "dec_phase_stamps": (I32, [P, P, I32]),
         "dec_last_error": (ctypes.c_char_p, [P]),
     }
     for name, (res, args) in sig.items():
@@ -269,6 +271,14 @@ class Decoder:
     def decode_dev(self, d_token: torch.Tensor, pos: int, logits: Optional[torch.Tensor],
                    d_argmax: Optional[torch.Tensor] = None) -> None:
         self._raise(lib.dec_decode_dev(self.h, d_token.data_ptr(), int(pos), _ptr(logits), _ptr(d_argmax)))
+
+    def set_fused(self, enable: bool) -> None:
+        """Persistent one-kernel decode step (default) or per-layer kernels."""
+        self._raise(lib.dec_set_fused(self.h, int(bool(enable))))
+
+    def phase_stamps(self, stamps: Optional[torch.Tensor]) -> None:
+        """Device int64 tensor receiving per-phase GPU timestamps of each fused decode step (None stops)."""
+        self._raise(lib.dec_phase_stamps(self.h, _ptr(stamps), 0 if stamps is None else stamps.numel()))
 
     def set_graph(self, enable: bool) -> None:
         self._raise(lib.dec_set_graph(self.h, int(bool(enable))))

@@ -167,6 +167,22 @@ dec_status dec_kv_layer(const dec_handle *h, int32_t layer, void **k, void **v);
  * Buffers are device memory owned by the caller. */
 dec_status dec_set_trace(dec_handle *h, int32_t *d_ids, float *d_logits, int32_t capacity);
 
+/* Decode step schedule.  enable = 1: ONE persistent cooperative kernel per
+ * step (every layer and the head, grid-wide barriers between phases, weights
+ * streamed by bulk copies), used when the configuration fits its shared-memory
+ * plan.  enable = 0: per-layer kernels chained by programmatic dependent launch
+ * in a CUDA graph.  dec_create picks the persistent kernel when the weights
+ * read per token exceed 4 GB (bandwidth-bound), else the per-layer kernels
+ * (latency-bound).  Results agree to rounding. */
+dec_status dec_set_fused(dec_handle *h, int32_t enable);
+
+/* Measurement hook of the persistent decode step: when d_stamps (device,
+ * >= 6*n_layers + 2 entries) is set, every later fused decode step writes the
+ * GPU's nanosecond timer at its start ([0]) and after each of its phases
+ * (QKV, attention, [merge], output projection, gate/up, down per layer; then
+ * the head).  NULL stops it. */
+dec_status dec_phase_stamps(dec_handle *h, uint64_t *d_stamps, int32_t capacity);
+
 /* Decode steps run as one captured CUDA graph by default (when the handle's
  * stream is not the legacy default stream).  enable = 0 launches the kernels
  * one by one instead (e.g. under a per-kernel profiler). */
@@ -192,7 +208,8 @@ typedef enum dec_kernel_class {
   DEC_K_LMHEAD = 6,   /* decode/prefill: final RMSNorm -> LM head (+ argmax) */
   DEC_K_ROUTER = 7,   /* decode: MoE router + top-k */
   DEC_K_PF_GEMM = 8,  /* prefill: projection GEMMs */
-  DEC_K_PF_ATTN = 9   /* prefill: causal attention */
+  DEC_K_PF_ATTN = 9,  /* prefill: causal attention */
+  DEC_K_STEP = 10     /* decode: the whole step as one persistent kernel */
 } dec_kernel_class;
 
 /* Measurement hook: from the next call on, a CUDA event pair is recorded on

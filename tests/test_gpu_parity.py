@@ -284,3 +284,25 @@ def test_mistral_full_prefill_then_wrapping_decode(dec_mod):
     w = synthetic.workload("mistral-7b")
     a, b = _prefill_vs_decode_loop(dec_mod, w, 4096, 48)
     assert a.length == b.length == 4144
+
+
+@pytest.mark.parametrize("name,kw", [("toy", {}), ("toy", dict(n_experts=4, n_experts_used=2)),
+                                     ("toy", dict(sliding_window=8, max_seq=8)), ("smollm2-135m", {}),
+                                     ("mixtral-8x7b", dict(n_layers=2))])
+def test_fused_step_matches_per_layer_kernels(dec_mod, name, kw):
+    # The persistent one-kernel decode step and the per-layer kernels are two
+    # schedules of the same arithmetic: same greedy stream, logits to rounding.
+    w = synthetic.workload(name, **kw)
+    P = 12 if name == "toy" else 40
+    prompt = synthetic.prompt_tokens(w, P, seed=9)
+    runs = []
+    weights = None
+    for fused in (True, False):
+        d = dec_mod.Decoder(w, weights=weights)
+        weights = d.weights
+        d.set_fused(fused)
+        runs.append(gpu_greedy(d, prompt, 10))
+        d.close()
+    (ra, ta), (rb, tb) = runs
+    assert ta == tb
+    np.testing.assert_allclose(ra, rb, atol=2e-4 if w["dtype"] == "f32" else 2e-3, rtol=1e-4)
