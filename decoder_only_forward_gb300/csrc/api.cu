@@ -154,6 +154,13 @@ WsPlan dec::plan_workspace(const dec_config& c) {
   p.Y = take(c.n_experts ? 4 * (size_t)T * k * c.hidden : 0);
   p.ACT = take(a_elem * (size_t)T * k * c.ffn);
   (void)ws;
+  // Tensor-core prefill attention: K planes and V^T planes (bf16 hi, lo) of up
+  // to max_seq + T key columns; the Q planes reuse the f32 Q rows.
+  const bool at = attn_tc_supported(c);
+  p.at_kcap = at ? c.max_seq + T : 0;
+  p.at_vt_ld = at ? (int)align_up((size_t)(c.max_seq + T), 8) : 0;
+  p.at_Kb = take(2 * 2 * (size_t)p.at_kcap * kd);
+  p.at_Vt = take(2 * 2 * (size_t)kd * p.at_vt_ld);
   p.mk_layers = take(sizeof(MkLayer) * (size_t)c.n_layers);
   p.kv = off;
   p.kv_layer_bytes = align_up(ks * (size_t)c.max_seq * kd, 256);
@@ -262,6 +269,12 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
   S.Asort = base + p.Asort;
   S.Y = (float*)(base + p.Y);
   S.ACT = base + p.ACT;
+  S.at.Qb = (__nv_bfloat16*)S.Q;
+  S.at.qcap = p.max_tokens;
+  S.at.Kb = p.at_kcap ? (__nv_bfloat16*)(base + p.at_Kb) : nullptr;
+  S.at.kcap = p.at_kcap;
+  S.at.Vt = p.at_kcap ? (__nv_bfloat16*)(base + p.at_Vt) : nullptr;
+  S.at.vt_ld = p.at_vt_ld;
   h->layers.resize(cfg->n_layers);
   for (int l = 0; l < cfg->n_layers; ++l) {
     const dec_layer_weights& L = w->layers[l];
@@ -376,8 +389,12 @@ dec_status dec_prefill(dec_handle* h, const int32_t* tokens, int32_t n, int32_t 
                                     cudaMemcpyHostToDevice, h->stream);
     if (e != cudaSuccess) return fail(h, DEC_ECUDA, "token copy: %s", cudaGetErrorString(e));
     const bool last = done + chunk == n;
-    launch_prefill_chunk(h->m, h->stream, chunk, start_pos + done, last ? logits : nullptr,
-                         last ? d_argmax : nullptr);
+    e = launch_prefill_chunk(h->m, h->stream, chunk, start_pos + done, last ? logits : nullptr,
+                             last ? d_argmax : nullptr);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(h, DEC_ECUDA, "prefill launch setup: %s", cudaGetErrorString(e));
+    }
     st = cuda_check(h, "prefill launch");
     if (st != DEC_OK) return st;
   }

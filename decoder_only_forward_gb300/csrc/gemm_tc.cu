@@ -118,9 +118,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
       tc_commit(tfull);
     }
   } else {
-    const bool ok = mbar_wait(tfull, 0, abort_flag, st, 103);
+    // tcgen05.ld is warp-collective: the whole warp takes the same branch.
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull, 0, abort_flag, st, 103) && !*abort_flag);
     tc_fence_after();
-    if (ok && !*abort_flag) {
+    if (ok) {
       const int q = warp & 3;
       const int r = m0 + q * 32 + lane;
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);

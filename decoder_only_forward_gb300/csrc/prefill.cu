@@ -384,25 +384,42 @@ struct Act {
 };
 
 template <typename TW>
-static void gemm(const Model& m, cudaStream_t s, const Act& a, const TW* B, int M, int N, int K, const GemmEpi& e,
-                 int groups, int max_rows) {
+static cudaError_t gemm(const Model& m, cudaStream_t s, const Act& a, const TW* B, int M, int N, int K,
+                        const GemmEpi& e, int groups, int max_rows) {
+  cudaError_t err = cudaSuccess;
   timer_begin(m, DEC_K_PF_GEMM, s);
   if (std::is_same<TW, __nv_bfloat16>::value) {
-    launch_gemm_tc(a.base, a.lo(), a.rows, B, M, N, K, e, groups, max_rows, m.s.st, s);
+    err = launch_gemm_tc(a.base, a.lo(), a.rows, B, M, N, K, e, groups, max_rows, m.s.st, s);
   } else {
     dim3 grid((max_rows + 63) / 64, (N + 63) / 64, groups);
     k_gemm_simt<float, TW><<<grid, 256, 0, s>>>((const float*)a.base, B, M, N, K, e);
   }
   timer_end(m, DEC_K_PF_GEMM, s);
   count_launch(m);
+  return err;
 }
 
 template <typename KV>
-static void attention(const Model& m, cudaStream_t s, const KV* Ks, const KV* Vs, int base_pos, int start, int n,
+static cudaError_t attention(const Model& m, cudaStream_t s, const KV* Ks, const KV* Vs, int base_pos, int start, int n,
                       RowOut O) {
   const dec_config& c = m.cfg;
   dim3 grid((n + 7) / 8, c.n_heads);
   const float* Q = m.s.Q;
+  if (std::is_same<KV, float>::value && m.s.at.Kb) {
+    // Tensor cores: K and V^T planes of the key columns some query can see,
+    // then the flash-attention kernel over 128-row query tiles.
+    const int kd = c.n_kv_heads * c.head_dim;
+    int c0 = c.sliding_window > 0 ? start - c.sliding_window + 1 : 0;
+    c0 = c0 > base_pos ? c0 - base_pos : 0;
+    cudaError_t err = launch_kv_split(reinterpret_cast<const float*>(Ks), reinterpret_cast<const float*>(Vs), kd,
+                                      c0 & ~63, start + n - base_pos, m.s.at, s);
+    timer_begin(m, DEC_K_PF_ATTN, s);
+    const cudaError_t e2 = launch_attn_prefill_tc(m.s.at, n, start, base_pos, c.n_heads, c.n_kv_heads, c.head_dim,
+                                                  c.sliding_window, O, m.s.st, s);
+    timer_end(m, DEC_K_PF_ATTN, s);
+    count_launch(m, 2);
+    return err != cudaSuccess ? err : e2;
+  }
   timer_begin(m, DEC_K_PF_ATTN, s);
   if (c.head_dim == 64)
     k_attn_prefill_simt<KV, 64><<<grid, 256, 0, s>>>(Q, Ks, Vs, base_pos, c.n_heads, c.n_kv_heads, start, n,
@@ -415,11 +432,17 @@ static void attention(const Model& m, cudaStream_t s, const KV* Ks, const KV* Vs
                                                     c.sliding_window, O);
   timer_end(m, DEC_K_PF_ATTN, s);
   count_launch(m);
+  return cudaSuccess;
 }
 
 template <typename TW, typename KV>
-static void prefill_chunk(const Model& m, cudaStream_t s, int n, int start, float* logits, int32_t* d_argmax) {
+static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int n, int start, float* logits,
+                                 int32_t* d_argmax) {
   const dec_config& c = m.cfg;
+  cudaError_t err = cudaSuccess;
+  auto chk = [&err](cudaError_t e) {
+    if (err == cudaSuccess) err = e;
+  };
   const Scratch& S = m.s;
   const int h = c.hidden, hd = c.head_dim, qd = c.n_heads * hd, kd = c.n_kv_heads * hd, f = c.ffn;
   const int half = hd / 2;
@@ -458,15 +481,19 @@ static void prefill_chunk(const Model& m, cudaStream_t s, int n, int start, floa
       e.qd = qd;
       e.kd = kd;
       e.hd = hd;
-      e.q_out = S.Q;
-      e.q_bf16 = 0;
+      // Rotated queries: bf16 (hi, lo) planes for the tensor-core attention,
+      // else f32 rows.
+      const bool q_planes = std::is_same<KV, float>::value && S.at.Kb;
+      e.q_out = q_planes ? (void*)S.at.Qb : (void*)S.Q;
+      e.q_bf16 = q_planes;
+      e.q_lo = q_planes ? S.at.Qb + (size_t)S.at.qcap * qd : nullptr;
       e.k_dst = kdst;
       e.v_dst = vdst;
       e.kv_bf16 = std::is_same<KV, __nv_bfloat16>::value;
       e.kv_row0 = direct ? start : hist;
-      gemm<TW>(m, s, a_h, (const TW*)L.wqkv, n, qd + 2 * kd, h, e, 1, n);
+      chk(gemm<TW>(m, s, a_h, (const TW*)L.wqkv, n, qd + 2 * kd, h, e, 1, n));
     }
-    attention<KV>(m, s, kdst, vdst, direct ? 0 : h0, start, n, a_q.out());
+    chk(attention<KV>(m, s, kdst, vdst, direct ? 0 : h0, start, n, a_q.out()));
     if (!direct) {
       const int t_first = n > c.max_seq ? n - c.max_seq : 0;
       k_kv_commit<KV><<<152, 256, 0, s>>>(kdst, vdst, hist, start, t_first, n, c.max_seq, kd, (KV*)L.kc,
@@ -478,7 +505,7 @@ static void prefill_chunk(const Model& m, cudaStream_t s, int n, int start, floa
       e.mode = EPI_RESID;
       e.n_out = h;
       e.out_f32 = S.X;
-      gemm<TW>(m, s, a_q, (const TW*)L.wo, n, h, qd, e, 1, n);
+      chk(gemm<TW>(m, s, a_q, (const TW*)L.wo, n, h, qd, e, 1, n));
     }
     if (c.n_experts == 0) {
       k_rmsnorm_rows<<<n, 256, 0, s>>>(S.X, L.ffn_norm, c.rms_eps, h, a_h.out());
@@ -489,12 +516,12 @@ static void prefill_chunk(const Model& m, cudaStream_t s, int n, int start, floa
       e1.act = act.base;
       e1.act_bf16 = split;
       e1.act_lo = act.out().lo;
-      gemm<TW>(m, s, a_h, (const TW*)L.w_gateup, n, 2 * f, h, e1, 1, n);
+      chk(gemm<TW>(m, s, a_h, (const TW*)L.w_gateup, n, 2 * f, h, e1, 1, n));
       GemmEpi e2{};
       e2.mode = EPI_RESID;
       e2.n_out = h;
       e2.out_f32 = S.X;
-      gemm<TW>(m, s, act, (const TW*)L.w_down, n, h, f, e2, 1, n);
+      chk(gemm<TW>(m, s, act, (const TW*)L.w_down, n, h, f, e2, 1, n));
     } else {
       const int k = c.n_experts_used, E = c.n_experts, entries = n * k;
       const Act a_sort{S.Asort, split, entries, h};
@@ -526,26 +553,28 @@ static void prefill_chunk(const Model& m, cudaStream_t s, int n, int start, floa
       e1.act_bf16 = split;
       e1.act_lo = act_sort.out().lo;
       e1.group_offset = S.pf_offset;
-      gemm<TW>(m, s, a_sort, (const TW*)L.w_gateup, entries, 2 * f, h, e1, E, n);
+      chk(gemm<TW>(m, s, a_sort, (const TW*)L.w_gateup, entries, 2 * f, h, e1, E, n));
       GemmEpi e2{};
       e2.mode = EPI_STORE;
       e2.n_out = h;
       e2.out_f32 = S.Y;
       e2.group_offset = S.pf_offset;
-      gemm<TW>(m, s, act_sort, (const TW*)L.w_down, entries, h, f, e2, E, n);
+      chk(gemm<TW>(m, s, act_sort, (const TW*)L.w_down, entries, h, f, e2, E, n));
       k_moe_combine<<<n, 256, 0, s>>>(S.Y, S.pf_inv, S.pf_wts, k, h, S.X);
       count_launch(m);
     }
   }
   if (logits || d_argmax) launch_lmhead(m, s, S.X + (size_t)(n - 1) * h, logits, d_argmax);
+  return err;
 }
 
-void launch_prefill_chunk(const Model& m, cudaStream_t s, int n, int start, float* logits, int32_t* d_argmax) {
+cudaError_t launch_prefill_chunk(const Model& m, cudaStream_t s, int n, int start, float* logits,
+                                 int32_t* d_argmax) {
   const bool wb = m.cfg.weight_dtype == DEC_BF16, kb = m.cfg.kv_dtype == DEC_BF16;
-  if (wb && kb) prefill_chunk<__nv_bfloat16, __nv_bfloat16>(m, s, n, start, logits, d_argmax);
-  else if (wb) prefill_chunk<__nv_bfloat16, float>(m, s, n, start, logits, d_argmax);
-  else if (kb) prefill_chunk<float, __nv_bfloat16>(m, s, n, start, logits, d_argmax);
-  else prefill_chunk<float, float>(m, s, n, start, logits, d_argmax);
+  if (wb && kb) return prefill_chunk<__nv_bfloat16, __nv_bfloat16>(m, s, n, start, logits, d_argmax);
+  if (wb) return prefill_chunk<__nv_bfloat16, float>(m, s, n, start, logits, d_argmax);
+  if (kb) return prefill_chunk<float, __nv_bfloat16>(m, s, n, start, logits, d_argmax);
+  return prefill_chunk<float, float>(m, s, n, start, logits, d_argmax);
 }
 
 }  // namespace dec

@@ -29,6 +29,7 @@ struct GemmEpi {
   int qd, kd, hd;
   void* q_out;            // [row][qd], bf16 when q_bf16 else f32
   int q_bf16;
+  __nv_bfloat16* q_lo;    // with q_bf16: the bf16 remainder plane (q = hi + lo); nullable
   void* k_dst;            // K rows: row r goes to row (r + kv_row0), kd columns
   void* v_dst;
   int kv_bf16;
@@ -107,8 +108,15 @@ __device__ __forceinline__ void epi_pair(const GemmEpi& e, int row, int col, flo
       }
       if (col < e.qd) {
         const size_t o = (size_t)row * e.qd + col;
-        if (e.q_bf16) store_pair(reinterpret_cast<__nv_bfloat16*>(e.q_out) + o, v0, v1);
-        else store_pair(reinterpret_cast<float*>(e.q_out) + o, v0, v1);
+        if (e.q_bf16) {
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(v0, v1);
+          *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(e.q_out) + o) = hi;
+          if (e.q_lo)
+            *reinterpret_cast<__nv_bfloat162*>(e.q_lo + o) =
+                __floats2bfloat162_rn(v0 - __low2float(hi), v1 - __high2float(hi));
+        } else {
+          store_pair(reinterpret_cast<float*>(e.q_out) + o, v0, v1);
+        }
       } else {
         const bool is_k = col < e.qd + e.kd;
         const size_t o = (size_t)(row + e.kv_row0) * e.kd + (is_k ? col - e.qd : col - e.qd - e.kd);

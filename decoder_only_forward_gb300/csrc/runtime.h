@@ -39,6 +39,17 @@ struct LayerPtrs {
   void* vc;            // this layer's V ring
 };
 
+// bf16 (hi, lo) operand planes of the tensor-core prefill attention; plane
+// 1 (lo) follows plane 0 (hi) at the stated capacity.
+struct AttnTcPlanes {
+  __nv_bfloat16* Qb;    // [2][qcap][nq*hd] rotated queries (aliases Scratch::Q)
+  int qcap;
+  __nv_bfloat16* Kb;    // [2][kcap][n_kv*hd] keys as rows, column = position - base
+  int kcap;
+  __nv_bfloat16* Vt;    // [2][n_kv*hd][vt_ld] values transposed
+  int vt_ld;
+};
+
 // Device scratch carved out of the caller's workspace (see plan_workspace).
 struct Scratch {
   DeviceState* st;
@@ -70,6 +81,7 @@ struct Scratch {
   void* Asort;          // [T*k][h] normalised rows gathered by expert (MoE)
   float* Y;             // [T*k][h] per-(row, slot) expert outputs (MoE)
   void* ACT;            // [T*k][ffn] gate/up output rows (A operand of down)
+  AttnTcPlanes at;      // at.Kb == nullptr: this configuration takes the SIMT attention
 };
 
 constexpr int LM_GRID_MAX = 1024;
@@ -117,6 +129,8 @@ struct Model {
 struct WsPlan {
   size_t st, inv_freq, rope_tab, x, q, attn, act, nbuf, ids, wts, part, amax_val, amax_idx, tokens;
   size_t X, A, Q, KVlin_k, KVlin_v, pf_ids, pf_wts, pf_count, pf_offset, pf_rows, pf_inv, Asort, Y, ACT;
+  size_t at_Kb, at_Vt;
+  int at_kcap, at_vt_ld;  // 0: no tensor-core prefill attention for this configuration
   size_t mk_layers;     // layer table of the persistent decode kernel
   size_t kv;            // start of the KV rings
   size_t kv_layer_bytes;
@@ -168,8 +182,9 @@ void launch_lmhead(const Model& m, cudaStream_t s, const float* x, float* logits
 // Runs tokens (already in m.s.tokens[0..n)) at positions start..start+n-1; writes
 // the last row's logits when logits != nullptr.  wrap_mode: K/V go through the
 // linear scratch and are committed afterwards (needed once the ring may wrap).
-void launch_prefill_chunk(const Model& m, cudaStream_t s, int n, int start, float* logits,
-                          int32_t* d_argmax);
+// Returns the first launch-setup error (a tensor map the driver rejects, ...).
+cudaError_t launch_prefill_chunk(const Model& m, cudaStream_t s, int n, int start, float* logits,
+                                 int32_t* d_argmax);
 
 inline void count_launch(const Model& m, int n = 1) { *m.launches += n; }
 
@@ -192,6 +207,18 @@ bool attend_check(const void* q, const void* k, const void* v, const void* out, 
 struct GemmEpi;
 cudaError_t launch_gemm_tc(const void* a_hi, const void* a_lo, int a_rows, const void* b, int M, int N, int K,
                            const GemmEpi& e, int groups, int max_rows, DeviceState* st, cudaStream_t s);
+
+struct RowOut;
+// Tensor-core causal prefill attention (attn_tc.cu) over key columns
+// [0, start + n - base_pos); head_dim 64 or 128.  launch_kv_split fills the K
+// and V^T planes of rows [r0, r1) from f32 K/V row buffers.
+cudaError_t launch_attn_prefill_tc(const AttnTcPlanes& pl, int n, int start, int base_pos, int nq, int nkv, int hd,
+                                   int sliding, RowOut out, DeviceState* st, cudaStream_t s);
+cudaError_t launch_kv_split(const float* K, const float* V, int kd, int r0, int r1, const AttnTcPlanes& pl,
+                            cudaStream_t s);
+inline bool attn_tc_supported(const dec_config& c) {
+  return c.kv_dtype == DEC_F32 && (c.head_dim == 64 || c.head_dim == 128);
+}
 
 // Message returned by dec_last_error(NULL) (api.cu).
 void set_global_error(const char* msg);
