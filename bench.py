@@ -344,6 +344,8 @@ def run_profile(args):
     w = synthetic.workload(args.workload)
     if args.prompt:
         w["prompt"] = args.prompt
+    if args.layers:
+        w["n_layers"] = args.layers
     d = dec.Decoder(w, kv_dtype=args.kv)
     d.set_graph(False)
     P = w["prompt"]
@@ -393,6 +395,8 @@ def main():
     ap.add_argument("--workload", default="smollm2-135m", choices=sorted(synthetic.WORKLOADS))
     ap.add_argument("--kv", default="f32", choices=["f32", "bf16"])
     ap.add_argument("--prompt", type=int, default=0, help="override the prompt length (profiling only)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the layer count (with --profile only: small cases for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", type=int, default=0, metavar="D",
                     help="profiling driver: one prefill + D decode steps, kernels launched one by one "
@@ -406,6 +410,8 @@ def main():
     if args.profile:
         run_profile(args)
         return
+    if args.layers:
+        ap.error("--layers changes the workload: it is for --profile runs only")
     if args.impl == "reference":
         if rank != 0:
             return

@@ -562,6 +562,9 @@ dec_status dec_check(dec_handle* h) {
     cudaMemset(&h->m.s.st->err, 0, sizeof words);
     if (words[0] & ERR_TIMEOUT)
       return fail(h, DEC_ETIMEOUT, "a bounded device wait timed out (site %u)", words[1]);
+    if (words[0] & ERR_LAYOUT)
+      return fail(h, DEC_ECUDA, "a kernel's shared-memory window was not aligned for its tiles (site %u)",
+                  words[1]);
     return fail(h, DEC_EINVAL, "a device-side token was outside [0, vocab)");
   }
   return DEC_OK;

@@ -27,8 +27,11 @@
 
 namespace dec {
 
-constexpr int AT_BM = 128, AT_BN = 64, AT_THREADS = 192;
+constexpr int AT_BM = 128, AT_BN = 64;
+constexpr int AT_SOFT = 256;                 // softmax threads: two per query row
+constexpr int AT_THREADS = 64 + AT_SOFT;     // + TMA producer warp + MMA warp
 
+// Shared-memory layout (offsets from a 1024-byte aligned base).
 template <int HD>
 struct AtCfg {
   static constexpr int QS = HD / 64;                     // 64 bf16 = 128 B per slab row
@@ -36,11 +39,21 @@ struct AtCfg {
   static constexpr int K_PLANE = QS * AT_BN * 128;
   static constexpr int V_PLANE = HD * 128;               // V^T: HD rows x 64 keys
   static constexpr int P_PLANE = AT_BM * 128;            // 128 rows x 64 keys
-  static constexpr int STAGE_BYTES = 2 * K_PLANE + 2 * V_PLANE;
-  static constexpr int SMEM = 2 * Q_PLANE + 2 * STAGE_BYTES + 2 * P_PLANE + 1024 + 256;
-  static constexpr int TMEM_COLS = (AT_BN + HD) <= 128 ? 128 : 256;
+  static constexpr int K_STAGE = 2 * K_PLANE, V_STAGE = 2 * V_PLANE;
+  static constexpr int OFF_K = 2 * Q_PLANE;              // K ring: 2 stages
+  static constexpr int OFF_V = OFF_K + 2 * K_STAGE;      // V^T ring: 2 stages
+  static constexpr int OFF_P = OFF_V + 2 * V_STAGE;
+  static constexpr int OFF_X = OFF_P + 2 * P_PLANE;      // row max exchange [2 buffers][2 halves][128] f32
+  static constexpr int OFF_BAR = OFF_X + 2 * 2 * AT_BM * 4;
+  static constexpr int LAYOUT = OFF_BAR + 128;
+  static constexpr int SLACK = 896;                      // room to align a 128-byte aligned window base
+  static constexpr int SMEM = LAYOUT + SLACK;
+  static constexpr int O_LD = HD + 4;                    // staged output rows (f32), in the K/V rings
+  static constexpr int TMEM_COLS = 256;                  // S double buffer [0, 128), O [128, 128 + HD)
 };
 static_assert(AtCfg<128>::SMEM <= 232448, "shared memory of the HD=128 attention tile");
+static_assert(AT_BM * AtCfg<128>::O_LD * 4 <= AtCfg<128>::OFF_P - AtCfg<128>::OFF_K, "output staging");
+static_assert(AT_BM * AtCfg<64>::O_LD * 4 <= AtCfg<64>::OFF_P - AtCfg<64>::OFF_K, "output staging");
 
 struct AtArgs {
   int n, start, base_pos, nq, nkv, sliding;
@@ -56,6 +69,32 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// 2^x on the special-function unit (flushes subnormal results to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Barrier 1 over the softmax threads; returns whether any of them passed `pred`.
+__device__ __forceinline__ bool soft_sync_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "n"(AT_SOFT)
+      : "memory");
+  return r != 0;
+}
+
+// Rows whose running max grows by less than this (log2 units) keep the stale
+// max: P then reaches up to 2^8, which the (hi, lo) planes carry exactly as
+// well, and O needs no rescale.  The final O / l is the same either way.
+constexpr float AT_RESCALE_LOG2 = 8.f;
+
 template <int HD>
 __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_prefill_tc(const __grid_constant__ CUtensorMap tm_q,
                                                                   const __grid_constant__ CUtensorMap tm_k,
@@ -63,18 +102,28 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_prefill_tc(const __grid_
                                                                   AtArgs a) {
   using C = AtCfg<HD>;
   extern __shared__ uint8_t at_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;                                      // hi plane, then lo plane
-  uint8_t* sKV = sQ + 2 * C::Q_PLANE;                      // 2 stages of (K hi, K lo, V^T hi, V^T lo)
-  uint8_t* sP = sKV + 2 * C::STAGE_BYTES;                  // hi plane, then lo plane
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * C::P_PLANE);
+  const uint32_t pad = (1024u - (smem_u32(at_raw) & 1023u)) & 1023u;
+  if (pad > (uint32_t)C::SLACK) {  // same window for every thread: a uniform exit
+    if (threadIdx.x == 0) raise_error(a.st, ERR_LAYOUT, 120);
+    return;
+  }
+  uint8_t* smem = at_raw + pad;
+  uint8_t* sQ = smem;                  // hi plane, then lo plane
+  uint8_t* sK = smem + C::OFF_K;       // stage s: hi plane, lo plane
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sP = smem + C::OFF_P;       // hi plane, then lo plane
+  float* xmax = reinterpret_cast<float*>(smem + C::OFF_X);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;    // [2]
-  uint64_t* kv_empty = bars + 3;   // [2]
-  uint64_t* s_full = bars + 5;
-  uint64_t* p_ready = bars + 6;
-  uint64_t* o_done = bars + 7;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+  uint64_t* k_full = bars + 1;     // [2]
+  uint64_t* k_empty = bars + 3;    // [2]
+  uint64_t* v_full = bars + 5;     // [2]
+  uint64_t* v_empty = bars + 7;    // [2]
+  uint64_t* s_full = bars + 9;     // [2] one per S buffer
+  uint64_t* p_ready = bars + 11;
+  uint64_t* o_done = bars + 12;
+  uint64_t* drained = bars + 13;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -91,12 +140,15 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_prefill_tc(const __grid_
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+      mbar_init(&s_full[s], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_ready, 128);
+    mbar_init(p_ready, AT_SOFT);
     mbar_init(o_done, 1);
+    mbar_init(drained, 1);
     *abort_flag = 0;
     mbar_fence_init();
     tma_prefetch_desc(&tm_q);
@@ -111,72 +163,105 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_prefill_tc(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + AT_BN;
+  const uint32_t tO = tmem + 2 * AT_BN;
 
   if (warp == 0) {
     if (lane == 0) {
+      // K of tile j waits only for S(j-2); V^T of tile j for P.V(j-2).
       mbar_arrive_expect_tx(q_full, 2 * C::Q_PLANE);
       for (int p = 0; p < 2; ++p)
         for (int s = 0; s < C::QS; ++s)
           tma_load_3d(sQ + p * C::Q_PLANE + s * AT_BM * 128, &tm_q, q_full, h * HD + 64 * s, t0, p);
+      int nk = 0, nv = 0;
       for (int j = 0; j < ntiles; ++j) {
         const int st = j & 1;
-        if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1, abort_flag, a.st, 121)) break;
+        const uint32_t ph = ((j >> 1) & 1) ^ 1;
         const int r0 = (kt0 + j) * AT_BN;
-        uint8_t* sK = sKV + st * C::STAGE_BYTES;
-        uint8_t* sV = sK + 2 * C::K_PLANE;
-        mbar_arrive_expect_tx(&kv_full[st], C::STAGE_BYTES);
-        for (int p = 0; p < 2; ++p) {
+        if (!mbar_wait(&k_empty[st], ph, abort_flag, a.st, 121)) break;
+        mbar_arrive_expect_tx(&k_full[st], C::K_STAGE);
+        for (int p = 0; p < 2; ++p)
           for (int s = 0; s < C::QS; ++s)
-            tma_load_3d(sK + p * C::K_PLANE + s * AT_BN * 128, &tm_k, &kv_full[st], g * HD + 64 * s, r0, p);
-          tma_load_3d(sV + p * C::V_PLANE, &tm_vt, &kv_full[st], r0, g * HD, p);
-        }
+            tma_load_3d(sK + st * C::K_STAGE + p * C::K_PLANE + s * AT_BN * 128, &tm_k, &k_full[st],
+                        g * HD + 64 * s, r0, p);
+        ++nk;
+        if (!mbar_wait(&v_empty[st], ph, abort_flag, a.st, 128)) break;
+        mbar_arrive_expect_tx(&v_full[st], C::V_STAGE);
+        for (int p = 0; p < 2; ++p)
+          tma_load_3d(sV + st * C::V_STAGE + p * C::V_PLANE, &tm_vt, &v_full[st], r0, g * HD, p);
+        ++nv;
+      }
+      if (*abort_flag) {
+        // Let this CTA's copies land before its shared memory is given back.
+        volatile int no_abort = 0;
+        mbar_wait(q_full, 0, &no_abort, nullptr, 0, 100000000ull);
+        for (int j = max(0, nk - 2); j < nk; ++j)
+          mbar_wait(&k_full[j & 1], (j >> 1) & 1, &no_abort, nullptr, 0, 100000000ull);
+        for (int j = max(0, nv - 2); j < nv; ++j)
+          mbar_wait(&v_full[j & 1], (j >> 1) & 1, &no_abort, nullptr, 0, 100000000ull);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(AT_BM, AT_BN);
       constexpr uint32_t id_o = idesc_bf16_f32(AT_BM, HD);
-      bool ok = mbar_wait(q_full, 0, abort_flag, a.st, 122);
-      for (int j = 0; j < ntiles && ok; ++j) {
+      // S(j) = Qh.Kh + Qh.Kl + Ql.Kh into S buffer j & 1, 16 head-dim elements per step.
+      auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
-        if (!mbar_wait(&kv_full[st], (j >> 1) & 1, abort_flag, a.st, 123)) break;
+        if (!mbar_wait(&k_full[st], (j >> 1) & 1, abort_flag, a.st, 123)) return false;
         tc_fence_after();
-        const uint8_t* sK = sKV + st * C::STAGE_BYTES;
-        const uint8_t* sV = sK + 2 * C::K_PLANE;
-        // S = Qh.Kh + Qh.Kl + Ql.Kh, 16 head-dim elements (32 bytes) per step.
+        const uint8_t* kbase = sK + st * C::K_STAGE;
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks) {
           const uint32_t off = (ks & 3) * 32;
           const uint32_t qa = smem_u32(sQ + (ks >> 2) * AT_BM * 128 + off);
-          const uint32_t kb = smem_u32(sK + (ks >> 2) * AT_BN * 128 + off);
+          const uint32_t kb = smem_u32(kbase + (ks >> 2) * AT_BN * 128 + off);
           const uint64_t qh = sw128_kmajor_desc(qa), ql = sw128_kmajor_desc(qa + C::Q_PLANE);
           const uint64_t kh = sw128_kmajor_desc(kb), kl = sw128_kmajor_desc(kb + C::K_PLANE);
-          tc_mma_bf16(tS, qh, kh, id_s, ks > 0 ? 1u : 0u);
-          tc_mma_bf16(tS, qh, kl, id_s, 1u);
-          tc_mma_bf16(tS, ql, kh, id_s, 1u);
+          const uint32_t d = tmem + st * AT_BN;
+          tc_mma_bf16(d, qh, kh, id_s, ks > 0 ? 1u : 0u);
+          tc_mma_bf16(d, qh, kl, id_s, 1u);
+          tc_mma_bf16(d, ql, kh, id_s, 1u);
         }
-        tc_commit(s_full);
+        tc_commit(&s_full[st]);
+        tc_commit(&k_empty[st]);
+        return true;
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag, a.st, 122) && issue_s(0);
+      for (int j = 0; j < ntiles && ok; ++j) {
+        // S of the next tile runs while the softmax threads work on this one.
+        if (j + 1 < ntiles && !issue_s(j + 1)) break;
         if (!mbar_wait(p_ready, j & 1, abort_flag, a.st, 124)) break;
+        if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, abort_flag, a.st, 129)) break;
         tc_fence_after();
         // O += Ph.Vh + Ph.Vl + Pl.Vh over the tile's 64 keys.
+        const uint8_t* vbase = sV + (j & 1) * C::V_STAGE;
 #pragma unroll
         for (int ks = 0; ks < AT_BN / 16; ++ks) {
-          const uint32_t off = ks * 32;
-          const uint32_t pa = smem_u32(sP + off);
-          const uint32_t vb = smem_u32(sV + off);
+          const uint32_t pa = smem_u32(sP + ks * 32);
+          const uint32_t vb = smem_u32(vbase + ks * 32);
           const uint64_t ph = sw128_kmajor_desc(pa), pl = sw128_kmajor_desc(pa + C::P_PLANE);
           const uint64_t vh = sw128_kmajor_desc(vb), vl = sw128_kmajor_desc(vb + C::V_PLANE);
           tc_mma_bf16(tO, ph, vh, id_o, (j > 0 || ks > 0) ? 1u : 0u);
           tc_mma_bf16(tO, ph, vl, id_o, 1u);
           tc_mma_bf16(tO, pl, vh, id_o, 1u);
         }
-        tc_commit(&kv_empty[st]);
+        tc_commit(&v_empty[j & 1]);
         tc_commit(o_done);
       }
+      // Every MMA issued here completes before the TMEM goes back.
+      tc_commit(drained);
+      volatile int no_abort = 0;
+      mbar_wait(drained, 0, &no_abort, nullptr, 0, 100000000ull);
     }
   } else {
-    // Softmax warps: thread -> query row r (TMEM lane r).
+    // Softmax: warps 2-5 take keys 0-31 of each tile and O columns [0, HD/2),
+    // warps 6-9 keys 32-63 and O columns [HD/2, HD); thread -> query row r
+    // (TMEM lane r: warp w reaches lanes 32 (w % 4) .. 32 (w % 4) + 31).
+    // The two threads of a row share the tile max through shared memory and
+    // agree on every decision, so they keep identical running maxima.
+    // Branches around tcgen05.ld / st are warp-uniform and every exit from
+    // the tile loop is agreed by all softmax threads at barrier 1.
+    const int hf = (warp - 2) >> 2;
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const int t = t0 + r;
@@ -184,62 +269,88 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_prefill_tc(const __grid_
     const int qpos = a.start + t;
     const int lo = a.sliding > 0 ? max(0, qpos - a.sliding + 1) : 0;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    // tcgen05.ld / st are warp-collective: every branch around them is taken
-    // by the whole warp (__all_sync / __any_sync), also when a wait gives up.
-    for (int j = 0; j < ntiles && ok; ++j) {
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort_flag, a.st, 125))) {
-        ok = false;
+    const float scale = a.scale_log2;
+    float m = -INFINITY, l = 0.f;   // running max (log2 units) and this half's sum
+    bool bad = false;
+    for (int j = 0; j < ntiles; ++j) {
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag, a.st, 125));
+      float sv[32];
+      float mt = -INFINITY;
+      if (got) {
+        tc_fence_after();
+        tmem_ld32(tmem + (j & 1) * AT_BN + hf * 32 + lane_off, sv);
+        const int kabs0 = (kt0 + j) * AT_BN + a.base_pos + hf * 32;
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+        for (int jj = 0; jj < 32; jj += 4) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int kp = kabs0 + jj + u;
+            if (!(row_ok && kp <= qpos && kp >= lo)) sv[jj + u] = -INFINITY;
+          }
+          mx0 = fmaxf(mx0, sv[jj]);
+          mx1 = fmaxf(mx1, sv[jj + 1]);
+          mx2 = fmaxf(mx2, sv[jj + 2]);
+          mx3 = fmaxf(mx3, sv[jj + 3]);
+        }
+        mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      }
+      float* xb = xmax + (j & 1) * 2 * AT_BM;
+      xb[hf * AT_BM + r] = mt;
+      if (soft_sync_or(!got || bad)) {
+        bad = true;
         break;
       }
-      tc_fence_after();
-      float sv[AT_BN];
-      tmem_ld32(tS + lane_off, sv);
-      tmem_ld32(tS + lane_off + 32, sv + 32);
-      const int kabs0 = (kt0 + j) * AT_BN + a.base_pos;
-      float mt = -INFINITY;
-#pragma unroll
-      for (int jj = 0; jj < AT_BN; ++jj) {
-        const int kp = kabs0 + jj;
-        const bool valid = row_ok && kp <= qpos && kp >= lo;
-        sv[jj] = valid ? sv[jj] * a.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, sv[jj]);
+      const float ms = fmaxf(mt, xb[(hf ^ 1) * AT_BM + r]) * scale;   // -inf stays -inf
+      float alpha = 1.f;
+      if (ms > m + AT_RESCALE_LOG2) {
+        alpha = m == -INFINITY ? 0.f : ex2_approx(m - ms);
+        m = ms;
       }
-      const float mnew = fmaxf(m, mt);
-      const float alpha = m == -INFINITY ? 0.f : exp2f(m - mnew);
-      float psum = 0.f;
+      float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
+      if (m == -INFINITY) {
 #pragma unroll
-      for (int jj = 0; jj < AT_BN; ++jj) {
-        const float pv = mnew == -INFINITY ? 0.f : exp2f(sv[jj] - mnew);
-        sv[jj] = pv;
-        psum += pv;
+        for (int jj = 0; jj < 32; ++jj) sv[jj] = 0.f;
+      } else {
+        const float negm = -m;
+#pragma unroll
+        for (int jj = 0; jj < 32; jj += 4) {
+          sv[jj] = ex2_approx(fmaf(sv[jj], scale, negm));
+          sv[jj + 1] = ex2_approx(fmaf(sv[jj + 1], scale, negm));
+          sv[jj + 2] = ex2_approx(fmaf(sv[jj + 2], scale, negm));
+          sv[jj + 3] = ex2_approx(fmaf(sv[jj + 3], scale, negm));
+          ps0 += sv[jj];
+          ps1 += sv[jj + 1];
+          ps2 += sv[jj + 2];
+          ps3 += sv[jj + 3];
+        }
       }
-      l = l * alpha + psum;
-      m = mnew;
+      l = l * alpha + ((ps0 + ps1) + (ps2 + ps3));
       // P and O are still in use by the previous tile's P.V until it completes.
       if (j > 0) {
         if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag, a.st, 126))) {
-          ok = false;
-          break;
+          bad = true;   // the next barrier takes everyone out
+          continue;
         }
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          for (int c = 0; c < HD; c += 32) {
+#pragma unroll
+          for (int c = 0; c < HD / 2; c += 32) {
             float ov[32];
-            tmem_ld32(tO + lane_off + c, ov);
+            const uint32_t ta = tO + lane_off + hf * (HD / 2) + c;
+            tmem_ld32(ta, ov);
 #pragma unroll
             for (int e = 0; e < 32; ++e) ov[e] *= alpha;
-            tmem_st32(tO + lane_off + c, ov);
+            tmem_st32(ta, ov);
           }
         }
       }
-      // P row r into the swizzled K-major planes: 16-byte chunk c (keys
-      // 8c..8c+7) of row r sits at chunk c ^ (r % 8).
+      // This half of P row r into the swizzled K-major planes: 16-byte chunk
+      // cg (keys 8cg..8cg+7) of row r sits at chunk cg ^ (r % 8).
       uint8_t* rowh = sP + r * 128;
       uint8_t* rowl = rowh + C::P_PLANE;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t hw[4], lw[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -247,7 +358,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_prefill_tc(const __grid_
           hw[i] = pack_bf16(x0, x1);
           lw[i] = pack_bf16(x0 - bf16_lo(hw[i]), x1 - bf16_hi(hw[i]));
         }
-        const int cc = (c ^ (r & 7)) * 16;
+        const int cc = ((hf * 4 + c) ^ (r & 7)) * 16;
         *reinterpret_cast<uint4*>(rowh + cc) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         *reinterpret_cast<uint4*>(rowl + cc) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
       }
@@ -255,26 +366,39 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_prefill_tc(const __grid_
       tc_fence_before();
       mbar_arrive(p_ready);
     }
-    if (ok && __all_sync(0xffffffffu, mbar_wait(o_done, (ntiles - 1) & 1, abort_flag, a.st, 127))) {
+    // Epilogue: row sums of both halves, O / l staged in the (now idle) K/V
+    // rings, then stored row by row with consecutive threads on consecutive
+    // columns.
+    float* xb = xmax + (ntiles & 1) * 2 * AT_BM;
+    xb[hf * AT_BM + r] = l;
+    const bool got =
+        !bad && __all_sync(0xffffffffu, mbar_wait(o_done, (ntiles - 1) & 1, abort_flag, a.st, 127));
+    if (!soft_sync_or(!got)) {
       tc_fence_after();
-      const float inv = l > 0.f ? 1.0f / l : 0.f;
-      for (int c = 0; c < HD; c += 32) {
-        float ov[32];
-        tmem_ld32(tO + lane_off + c, ov);
-        if (row_ok)
+      const float lt = l + xb[(hf ^ 1) * AT_BM + r];
+      const float inv = lt > 0.f ? 1.0f / lt : 0.f;
+      float* sO = reinterpret_cast<float*>(sK);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) row_store(a.out, (size_t)t * a.qd + h * HD + c + e, ov[e] * inv);
+      for (int c = 0; c < HD / 2; c += 32) {
+        float ov[32];
+        tmem_ld32(tO + lane_off + hf * (HD / 2) + c, ov);
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(sO + r * C::O_LD + hf * (HD / 2) + c + e) =
+              make_float4(ov[e] * inv, ov[e + 1] * inv, ov[e + 2] * inv, ov[e + 3] * inv);
+      }
+      soft_sync_or(false);
+      const int sid = threadIdx.x - 64;
+      for (int idx = sid; idx < AT_BM * (HD / 4); idx += AT_SOFT) {
+        const int row = idx / (HD / 4), c4 = idx % (HD / 4);
+        if (t0 + row < a.n)
+          row_store4(a.out, (size_t)(t0 + row) * a.qd + h * HD + 4 * c4,
+                     *reinterpret_cast<const float4*>(sO + row * C::O_LD + 4 * c4));
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (*abort_flag) {
-    // A role gave up: let issued MMAs finish before the TMEM goes back.
-    volatile int no_abort = 0;
-    if (threadIdx.x == 32) mbar_wait(o_done, (ntiles - 1) & 1, &no_abort, nullptr, 0, 100000000ull);
-    __syncthreads();
-  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();

@@ -10,6 +10,7 @@ namespace dec {
 // Device error word bits (DeviceState::err).
 constexpr unsigned ERR_TIMEOUT = 1u;   // a bounded wait gave up
 constexpr unsigned ERR_TOKEN = 2u;     // a device-side token outside [0, vocab)
+constexpr unsigned ERR_LAYOUT = 4u;    // a kernel's shared-memory window could not hold its tile layout
 
 // Per-handle device-resident step state.  Kernels of a decode step read the
 // position and token from here, so one captured CUDA graph serves every step.

@@ -55,6 +55,27 @@ __device__ __forceinline__ void row_store(const RowOut& o, size_t i, float v) {
   }
 }
 
+// Four consecutive values (i a multiple of 4).
+__device__ __forceinline__ void row_store4(const RowOut& o, size_t i, float4 v) {
+  if (o.f32) {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(o.hi) + i) = v;
+  } else {
+    const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y), h23 = __floats2bfloat162_rn(v.z, v.w);
+    uint2 hh;
+    hh.x = *reinterpret_cast<const uint32_t*>(&h01);
+    hh.y = *reinterpret_cast<const uint32_t*>(&h23);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(o.hi) + i) = hh;
+    if (o.lo) {
+      const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - __low2float(h01), v.y - __high2float(h01));
+      const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - __low2float(h23), v.w - __high2float(h23));
+      uint2 ll;
+      ll.x = *reinterpret_cast<const uint32_t*>(&l01);
+      ll.y = *reinterpret_cast<const uint32_t*>(&l23);
+      *reinterpret_cast<uint2*>(o.lo + i) = ll;
+    }
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ void store_pair(T* p, float a, float b);
 template <>

@@ -194,7 +194,8 @@ int64_t dec_launch_count(const dec_handle *h);
 
 /* Synchronises the handle's stream and reports device-side errors raised since
  * the last check: DEC_ETIMEOUT (a bounded wait gave up), DEC_EINVAL (a device
- * token out of range), DEC_ECUDA. */
+ * token out of range), DEC_ECUDA (a CUDA error, or a kernel whose shared-memory
+ * window was not aligned for its tile layout and did no work). */
 dec_status dec_check(dec_handle *h);
 
 /* Kernel classes for dec_timing_enable. */
