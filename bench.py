@@ -348,6 +348,8 @@ def run_profile(args):
         w["n_layers"] = args.layers
     d = dec.Decoder(w, kv_dtype=args.kv)
     d.set_graph(False)
+    if args.fused != "auto":
+        d.set_fused(args.fused == "on")
     P = w["prompt"]
     logits = torch.empty(w["vocab"], dtype=torch.float32, device="cuda")
     tok = torch.empty(1, dtype=torch.int32, device="cuda")
@@ -397,6 +399,8 @@ def main():
     ap.add_argument("--prompt", type=int, default=0, help="override the prompt length (profiling only)")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (with --profile only: small cases for profiler captures)")
+    ap.add_argument("--fused", default="auto", choices=["auto", "on", "off"],
+                    help="decode schedule of a --profile run: the persistent one-kernel step or per-layer kernels")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", type=int, default=0, metavar="D",
                     help="profiling driver: one prefill + D decode steps, kernels launched one by one "

@@ -4,12 +4,18 @@
 // kernel then issues two MMAs per K step so the product keeps ~16 bits of the
 // activations' mantissa (bf16 weights with fp32 activations and accumulation).
 //
-// One CTA computes one 128 x BN tile with three warp roles:
+// Persistent: one CTA per SM walks 128 x BN output tiles (tile t, t + grid,
+// ...), ordered so that CTAs running at the same time share weight columns
+// (B) in L2.  Three warp roles:
 //   warp 0 lane 0: TMA producer, K-blocks of 64 into a ring of smem stages;
 //   warp 1 lane 0: MMA issuer (tcgen05.mma, cta_group::1), frees stages with
-//                  tcgen05.commit; warp 1 also owns the TMEM allocation;
-//   warps 2-5:     epilogue, tcgen05.ld of the accumulator rows (warp w reads
-//                  TMEM lanes 32*(w%4)..+31), then the fused epilogue.
+//                  tcgen05.commit, alternates between two TMEM accumulators;
+//                  warp 1 also owns the TMEM allocation;
+//   warps 2-5:     epilogue of the previous tile while the next one
+//                  accumulates: tcgen05.ld of 32 rows x 32 columns per warp,
+//                  a transpose through the warp's own smem slice, then the
+//                  fused epilogue with consecutive lanes on consecutive
+//                  column pairs (coalesced stores).
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -26,44 +32,68 @@ struct TcCfg {
   static constexpr int A_BYTES = TC_BM * TC_BK * 2;
   static constexpr int B_BYTES = BN * TC_BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES * (SPLIT ? 2 : 1) + B_BYTES;
-  static constexpr int STAGES_FIT = (200 * 1024) / STAGE_BYTES;
+  static constexpr int EPI_LD = 33;                          // floats per staged row
+  static constexpr int EPI_BYTES = 4 * 32 * EPI_LD * 4;      // one 32 x 32 slice per epilogue warp
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int STAGES_FIT = (232448 - 1024 - EPI_BYTES - BAR_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;
+  static constexpr int TMEM_COLS = 2 * BN;                   // two accumulators
 };
 
 template <int BN, bool SPLIT>
 __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant__ CUtensorMap tm_ahi,
                                                            const __grid_constant__ CUtensorMap tm_alo,
                                                            const __grid_constant__ CUtensorMap tm_b, int M, int N,
-                                                           int K, GemmEpi e, DeviceState* st) {
+                                                           int K, GemmEpi e, int groups, int m_tiles,
+                                                           DeviceState* st) {
   using C = TcCfg<BN, SPLIT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  float* epi_smem = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES + C::EPI_BYTES);
   uint64_t* empty = full + C::STAGES;
-  uint64_t* tfull = empty + C::STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
+  uint64_t* acc_full = empty + C::STAGES;   // [2]
+  uint64_t* acc_empty = acc_full + 2;       // [2]
+  uint64_t* drained = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drained + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* progress = abort_flag + 1;  // [0] K-blocks issued, [1] K-blocks consumed
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int row0 = 0, rows = M, b_row0 = 0;
-  if (e.group_offset) {
-    const int g = blockIdx.z;
-    row0 = e.group_offset[g];
-    rows = e.group_offset[g + 1] - row0;
-    b_row0 = g * N;
-  }
-  const int m0 = blockIdx.x * TC_BM, n0 = blockIdx.y * BN;
-  if (m0 >= rows) return;  // uniform per CTA, before any barrier or TMEM use
+  const int n_tiles = (N + BN - 1) / BN;
+  const int per_n = groups * m_tiles;            // tiles sharing one BN block of weight rows
+  const int total = n_tiles * per_n;
   const int kblocks = (K + TC_BK - 1) / TC_BK;
+  // Tile t -> (group, 128-row block, BN-column block); rows of group g are
+  // [offset[g], offset[g+1]) when grouped.  A tile past its group's rows has
+  // no work (the same answer for every role).
+  auto decode_tile = [&](int t, int& row0, int& rows, int& b_row0, int& m0, int& n0) -> bool {
+    const int nb = t / per_n, rem = t % per_n;
+    const int g = rem / m_tiles, mb = rem % m_tiles;
+    row0 = 0;
+    rows = M;
+    b_row0 = 0;
+    if (e.group_offset) {
+      row0 = e.group_offset[g];
+      rows = e.group_offset[g + 1] - row0;
+      b_row0 = g * N;
+    }
+    m0 = mb * TC_BM;
+    n0 = nb * BN;
+    return m0 < rows;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(tfull, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);   // one arrival per epilogue warp
+    }
+    mbar_init(drained, 1);
     *abort_flag = 0;
     progress[0] = 0;
     progress[1] = 0;
@@ -73,7 +103,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
     tma_prefetch_desc(&tm_b);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, BN);
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -83,77 +113,123 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int kb = 0; kb < kblocks; ++kb) {
-        const int s = kb % C::STAGES;
-        const uint32_t ph = (kb / C::STAGES) & 1;
-        if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, st, 101)) break;
-        uint8_t* base = smem + s * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-        tma_load_2d(base, &tm_ahi, &full[s], kb * TC_BK, row0 + m0);
-        if (SPLIT) tma_load_2d(base + C::A_BYTES, &tm_alo, &full[s], kb * TC_BK, row0 + m0);
-        tma_load_2d(base + C::A_BYTES * (SPLIT ? 2 : 1), &tm_b, &full[s], kb * TC_BK, b_row0 + n0);
-        progress[0] = kb + 1;
+      int kb_all = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int row0, rows, b_row0, m0, n0;
+        if (!decode_tile(t, row0, rows, b_row0, m0, n0)) continue;
+        for (int kb = 0; kb < kblocks; ++kb, ++kb_all) {
+          const int s = kb_all % C::STAGES;
+          const uint32_t ph = (kb_all / C::STAGES) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, st, 101)) {
+            ok = false;
+            break;
+          }
+          uint8_t* base = smem + s * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          tma_load_2d(base, &tm_ahi, &full[s], kb * TC_BK, row0 + m0);
+          if (SPLIT) tma_load_2d(base + C::A_BYTES, &tm_alo, &full[s], kb * TC_BK, row0 + m0);
+          tma_load_2d(base + C::A_BYTES * (SPLIT ? 2 : 1), &tm_b, &full[s], kb * TC_BK, b_row0 + n0);
+          progress[0] = kb_all + 1;
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(TC_BM, BN);
-      for (int kb = 0; kb < kblocks; ++kb) {
-        const int s = kb % C::STAGES;
-        const uint32_t ph = (kb / C::STAGES) & 1;
-        if (!mbar_wait(&full[s], ph, abort_flag, st, 102)) break;
+      int kb_all = 0, it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int row0, rows, b_row0, m0, n0;
+        if (!decode_tile(t, row0, rows, b_row0, m0, n0)) continue;
+        const int b = it & 1;
+        // The epilogue must have drained this accumulator (tile it - 2).
+        if (!mbar_wait(&acc_empty[b], ((it >> 1) & 1) ^ 1, abort_flag, st, 104)) break;
         tc_fence_after();
-        uint8_t* base = smem + s * C::STAGE_BYTES;
-        const uint64_t da = sw128_kmajor_desc(smem_u32(base));
-        const uint64_t dl = sw128_kmajor_desc(smem_u32(base + C::A_BYTES));
-        const uint64_t db = sw128_kmajor_desc(smem_u32(base + C::A_BYTES * (SPLIT ? 2 : 1)));
+        const uint32_t acc = tmem + b * BN;
+        for (int kb = 0; kb < kblocks; ++kb, ++kb_all) {
+          const int s = kb_all % C::STAGES;
+          const uint32_t ph = (kb_all / C::STAGES) & 1;
+          if (!mbar_wait(&full[s], ph, abort_flag, st, 102)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint8_t* base = smem + s * C::STAGE_BYTES;
+          const uint64_t da = sw128_kmajor_desc(smem_u32(base));
+          const uint64_t dl = sw128_kmajor_desc(smem_u32(base + C::A_BYTES));
+          const uint64_t db = sw128_kmajor_desc(smem_u32(base + C::A_BYTES * (SPLIT ? 2 : 1)));
 #pragma unroll
-        for (int k = 0; k < TC_BK / 16; ++k) {
-          tc_mma_bf16(tmem, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
-          if (SPLIT) tc_mma_bf16(tmem, dl + 2 * k, db + 2 * k, idesc, 1u);
+          for (int k = 0; k < TC_BK / 16; ++k) {
+            tc_mma_bf16(acc, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            if (SPLIT) tc_mma_bf16(acc, dl + 2 * k, db + 2 * k, idesc, 1u);
+          }
+          tc_commit(&empty[s]);
+          progress[1] = kb_all + 1;
         }
-        tc_commit(&empty[s]);
-        progress[1] = kb + 1;
+        if (!ok) break;
+        tc_commit(&acc_full[b]);
+        ++it;
       }
-      tc_commit(tfull);
+      // Every MMA issued here completes before the TMEM goes back.
+      tc_commit(drained);
+      volatile int no_abort = 0;
+      mbar_wait(drained, 0, &no_abort, nullptr, 0, 100000000ull);
     }
   } else {
-    // tcgen05.ld is warp-collective: the whole warp takes the same branch.
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(tfull, 0, abort_flag, st, 103) && !*abort_flag);
-    tc_fence_after();
-    if (ok) {
-      const int q = warp & 3;
-      const int r = m0 + q * 32 + lane;
-      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+    // tcgen05.ld is warp-collective: every branch around it is warp-uniform.
+    const int q = warp & 3;
+    float* slice = epi_smem + q * 32 * C::EPI_LD;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      int row0, rows, b_row0, m0, n0;
+      if (!decode_tile(t, row0, rows, b_row0, m0, n0)) continue;
+      const int b = it & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[b], (it >> 1) & 1, abort_flag, st, 103))) break;
+      tc_fence_after();
+      const uint32_t acc = tmem + b * BN + lane_base;
+      const int r_base = m0 + q * 32;          // this warp's first row within the group
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         if (n0 + c >= N) break;
         float v[32];
-        tmem_ld32(trow + c, v);
-        if (r < rows) {
+        tmem_ld32(acc + c, v);
+        // Row `lane` of the slice <- this lane's accumulator row.
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) epi_pair(e, row0 + r, n0 + c + j, v[j], v[j + 1]);
+        for (int j = 0; j < 32; ++j) slice[lane * C::EPI_LD + j] = v[j];
+        __syncwarp();
+        // Lanes 0-15: row rr, lanes 16-31: row rr + 1; column pair (lane & 15).
+        const int pc = 2 * (lane & 15);
+#pragma unroll 4
+        for (int rr = 0; rr < 32; rr += 2) {
+          const int lr = rr + (lane >> 4);
+          if (r_base + lr < rows)
+            epi_pair(e, row0 + r_base + lr, n0 + c + pc, slice[lr * C::EPI_LD + pc], slice[lr * C::EPI_LD + pc + 1]);
         }
+        __syncwarp();
       }
+      tc_fence_before();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
+      ++it;
     }
   }
 
   tc_fence_before();
   __syncthreads();
   if (*abort_flag) {
-    // Never taken when the pipeline is consistent.  Drain what is in flight
-    // (bounded) before the TMEM and shared memory are released.
+    // Never taken when the pipeline is consistent.  Let the copies in flight
+    // land (bounded) before the shared memory is released.
     volatile int no_abort = 0;
     if (threadIdx.x == 0)
       for (int kb = progress[1]; kb < progress[0]; ++kb)
         mbar_wait(&full[kb % C::STAGES], (kb / C::STAGES) & 1, &no_abort, nullptr, 0, 100000000ull);
-    if (threadIdx.x == 32) mbar_wait(tfull, 0, &no_abort, nullptr, 0, 100000000ull);
     __syncthreads();
   }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, BN);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
@@ -187,14 +263,29 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+static int num_sms() {
+  static int n = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+      n = 0;
+  });
+  return n > 0 ? n : 1;
+}
+
 template <int BN, bool SPLIT>
 static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& al, const CUtensorMap& b, int M, int N, int K,
                              const GemmEpi& e, int groups, int max_rows, DeviceState* st, cudaStream_t s) {
   using C = TcCfg<BN, SPLIT>;
   auto kern = k_gemm_tc<BN, SPLIT>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  dim3 grid((max_rows + TC_BM - 1) / TC_BM, (N + BN - 1) / BN, groups);
-  kern<<<grid, TC_THREADS, C::SMEM, s>>>(a, al, b, M, N, K, e, st);
+  const int m_tiles = (max_rows + TC_BM - 1) / TC_BM;
+  const long long total = (long long)m_tiles * groups * ((N + BN - 1) / BN);
+  const int sms = num_sms();
+  const int grid = (int)(total < sms ? total : sms);
+  kern<<<grid, TC_THREADS, C::SMEM, s>>>(a, al, b, M, N, K, e, groups, m_tiles, st);
   return cudaGetLastError();
 }
 
