@@ -175,6 +175,8 @@ def run_ours(args, rank, world, local_rank):
     P, D = w["prompt"], w["decode"]
     kv_es = 4 if args.kv == "f32" else 2
     d = dec.Decoder(w, device=dev, kv_dtype=args.kv)
+    if args.fused != "auto":
+        d.set_fused(args.fused)
     s = d.stream
     prompt_np = synthetic.prompt_tokens(w, P, seed=0)
     prompt_pinned = torch.from_numpy(prompt_np).pin_memory()
@@ -311,6 +313,7 @@ def run_ours(args, rank, world, local_rank):
             "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"] if w["dtype"] != "f32" else "f32",
             "data": "synthetic (random-init weights N(0,0.02), norms 1+N(0,0.1), uniform random prompt)",
             "config": {"workload": args.workload, "prompt_tokens": P, "decode_tokens": D, "batch": 1,
+                       "decode_schedule": d.fused_mode(),
                        "kv_dtype": args.kv, "weights_gb": round(d.weights.nbytes() / 1e9, 3),
                        "l2": "flushed before each step (write of a 258 MB buffer); weights also exceed L2",
                        "parallelism": f"replicas x{n}" if n > 1 else "single GPU"},
@@ -349,7 +352,7 @@ def run_profile(args):
     d = dec.Decoder(w, kv_dtype=args.kv)
     d.set_graph(False)
     if args.fused != "auto":
-        d.set_fused(args.fused == "on")
+        d.set_fused(args.fused)
     P = w["prompt"]
     logits = torch.empty(w["vocab"], dtype=torch.float32, device="cuda")
     tok = torch.empty(1, dtype=torch.int32, device="cuda")
@@ -399,8 +402,9 @@ def main():
     ap.add_argument("--prompt", type=int, default=0, help="override the prompt length (profiling only)")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (with --profile only: small cases for profiler captures)")
-    ap.add_argument("--fused", default="auto", choices=["auto", "on", "off"],
-                    help="decode schedule of a --profile run: the persistent one-kernel step or per-layer kernels")
+    ap.add_argument("--fused", default="auto", choices=["auto", "off", "grid", "cluster"],
+                    help="decode schedule: per-layer kernels, or the persistent one-kernel step over every SM "
+                         "or on one thread-block cluster (default: the handle's own choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", type=int, default=0, metavar="D",
                     help="profiling driver: one prefill + D decode steps, kernels launched one by one "

@@ -30,7 +30,7 @@ struct dec_handle {
   Timing timing;
   std::vector<cudaEvent_t> events;
   bool use_graph = true;
-  bool use_fused = true;
+  int fused_mode = 1;   // DEC_FUSED_*
 };
 
 static void drop_graph(dec_handle* h) {
@@ -317,7 +317,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
     const size_t kslots = cfg->n_experts ? cfg->n_experts_used : 1;
     wbytes += (size_t)cfg->n_layers * ((qd + 2 * kd) * cfg->hidden + cfg->hidden * qd + 3 * kslots * cfg->ffn * cfg->hidden);
     wbytes *= cfg->weight_dtype == DEC_BF16 ? 2 : 4;
-    h->use_fused = wbytes >= (size_t)4 << 30;
+    h->fused_mode = wbytes >= (size_t)4 << 30 ? DEC_FUSED_GRID : DEC_FUSED_OFF;
   }
 
   // RoPE frequencies inv_i = theta^(-2i/hd), llama3-scaled when enabled
@@ -426,9 +426,10 @@ static cudaError_t set_step_node(dec_handle* h, const int32_t* d_token, int32_t 
 // only the setup node's token/position change.
 static dec_status run_decode_step(dec_handle* h, const int32_t* d_token, int32_t token, int32_t pos,
                                   float* logits, int32_t* d_argmax) {
-  if (h->use_fused && h->m.mk_ok) {
+  const bool cluster = h->fused_mode == DEC_FUSED_CLUSTER && h->m.mk_cluster > 0;
+  if (h->m.mk_ok && (cluster || h->fused_mode == DEC_FUSED_GRID)) {
     timing_start(h);
-    launch_decode_mk(h->m, h->stream, d_token, token, pos, logits, d_argmax);
+    launch_decode_mk(h->m, h->stream, d_token, token, pos, logits, d_argmax, cluster);
     timing_finish(h);
     return cuda_check(h, "decode launch");
   }
@@ -520,10 +521,26 @@ dec_status dec_phase_stamps(dec_handle* h, uint64_t* d_stamps, int32_t capacity)
   return DEC_OK;
 }
 
-dec_status dec_set_fused(dec_handle* h, int32_t enable) {
+dec_status dec_set_fused(dec_handle* h, int32_t mode) {
   if (!h) return DEC_EINVAL;
-  h->use_fused = enable != 0;
+  if (mode < DEC_FUSED_OFF || mode > DEC_FUSED_CLUSTER) return fail(h, DEC_EINVAL, "unknown schedule %d", mode);
+  h->fused_mode = mode;
   return DEC_OK;
+}
+
+int32_t dec_fused_mode(const dec_handle* h) {
+  if (!h) return -1;
+  if (h->fused_mode == DEC_FUSED_CLUSTER && h->m.mk_ok && h->m.mk_cluster > 0) return DEC_FUSED_CLUSTER;
+  if (h->fused_mode == DEC_FUSED_GRID && h->m.mk_ok) return DEC_FUSED_GRID;
+  return DEC_FUSED_OFF;
+}
+
+int32_t dec_fused_available(const dec_handle* h, int32_t mode) {
+  if (!h) return 0;
+  if (mode == DEC_FUSED_OFF) return 1;
+  if (mode == DEC_FUSED_GRID) return h->m.mk_ok ? 1 : 0;
+  if (mode == DEC_FUSED_CLUSTER) return h->m.mk_ok && h->m.mk_cluster > 0 ? h->m.mk_cluster : 0;
+  return 0;
 }
 
 dec_status dec_set_graph(dec_handle* h, int32_t enable) {

@@ -65,6 +65,7 @@ struct MkParams {
   int u_bytes;                    // bytes of the shared region after the weight ring
   unsigned long long* stamps;     // nullable: %globaltimer after each phase (CTA 0), [0] = start
   int kv_bytes;                   // bytes per KV element
+  int cluster;                    // > 0: the grid is ONE thread-block cluster of this many CTAs
 };
 
 // Shared-memory bookkeeping after the weight ring and the union region.
@@ -85,6 +86,8 @@ struct MkMisc {
   int consumed[MK_COMPUTE_WARPS];  // stages each warp consumed (for the abort drain)
   int is_last;
   float mrow[MAX_GROUP], lrow[MAX_GROUP], alpha[MAX_GROUP];
+  uint64_t cbar;                 // cluster mode: phase barrier, one arrival per CTA of the cluster
+  unsigned cgen;                 // cluster mode: barrier instances completed
 };
 
 // ------------------------------------------------------------------ sync
@@ -132,6 +135,44 @@ __device__ __forceinline__ bool mk_grid_sync(DeviceState* st, unsigned nb, volat
   return !*abort_flag;
 }
 
+// Cluster mode: the same phase barrier over the CTAs of one cluster.  Each
+// CTA's thread 0 arrives (release, cluster scope) on the barrier in every
+// CTA's shared memory, then waits (acquire, cluster scope) for the arrivals
+// of all CTAs on its own.  A CTA can be at most one instance ahead of any
+// other, so the parity of the instance count names the phase to wait for.
+__device__ __forceinline__ bool mk_cluster_sync(DeviceState* st, unsigned nb, uint64_t* cbar, unsigned* cgen,
+                                                volatile int* abort_flag, unsigned site) {
+  compute_sync();
+  if (threadIdx.x == 0 && !*abort_flag) {
+    const uint32_t la = static_cast<uint32_t>(__cvta_generic_to_shared(cbar));
+    for (unsigned r = 0; r < nb; ++r) {
+      uint32_t ra;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(r));
+      asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
+    }
+    const uint32_t parity = *cgen & 1u;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+      uint32_t ok;
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(ok)
+          : "r"(la), "r"(parity)
+          : "memory");
+      if (ok) break;
+      if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+        raise_error(st, ERR_TIMEOUT, site);
+        *abort_flag = 1;
+        break;
+      }
+    }
+    ++*cgen;
+  }
+  compute_sync();
+  return !*abort_flag;
+}
+
 // ------------------------------------------------------------------ mbarrier / bulk copy
 __device__ __forceinline__ uint32_t mk_smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -146,12 +187,14 @@ __device__ __forceinline__ void mk_mbar_expect_tx(uint64_t* bar, uint32_t bytes)
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mk_smem_u32(bar)), "r"(bytes)
                : "memory");
 }
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes (or about 20 us pass) instead of spinning.
 __device__ __forceinline__ bool mk_mbar_try(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(mk_smem_u32(bar)), "r"(parity)
+      : "r"(mk_smem_u32(bar)), "r"(parity), "r"(20000u)
       : "memory");
   return ok != 0;
 }
@@ -460,9 +503,34 @@ __device__ void mk_router(const MkParams& P, int l, const float* xs, MkMisc* M) 
 namespace dec {
 
 // ------------------------------------------------------------------ GEMV phase (consumer side)
-// Warp w reduces units u = w, w+8, ... of every segment (a unit is a row, or a
-// row pair for the paired epilogues), reading each row in <= 4 KB pieces from
-// its own ring in the order its producer lane streams them.
+constexpr int MK_RB = 4;   // rows reduced together per pass
+
+// V consecutive floats of the activation vector in shared memory (16-byte aligned).
+template <int V>
+__device__ __forceinline__ void mk_load_xs(const float* p, float* v) {
+#pragma unroll
+  for (int i = 0; i < V; i += 4) {
+    const float4 t = *reinterpret_cast<const float4*>(p + i);
+    v[i] = t.x;
+    v[i + 1] = t.y;
+    v[i + 2] = t.z;
+    v[i + 3] = t.w;
+  }
+}
+
+// Rows [r0, r1) of segment S (relative to S.row0) that warp w reduces: a
+// contiguous block of whole units (a unit is a row, or a row pair for the
+// paired epilogues).  Rows of up to 4 KB are streamed several per stage,
+// longer rows in 4 KB pieces; producer and consumer walk the same plan.
+__device__ __forceinline__ void mk_warp_rows(const MkRows& R, const MkSeg& S, int w, int& r0, int& r1) {
+  const int nrow = R.paired ? 2 : 1;
+  const int units = S.rows / nrow;
+  const int upw = (units + MK_COMPUTE_WARPS - 1) / MK_COMPUTE_WARPS;
+  const int u0 = min(units, w * upw), u1 = min(units, u0 + upw);
+  r0 = u0 * nrow;
+  r1 = u1 * nrow;
+}
+
 template <typename W, typename KV>
 __device__ bool mk_gemv_phase(const MkParams& P, int ph, int l, const MkRows& R, uint8_t* ring, MkMisc* M,
                               float* xs, uint32_t& sc, float& best, int& bidx) {
@@ -472,50 +540,36 @@ __device__ bool mk_gemv_phase(const MkParams& P, int ph, int l, const MkRows& R,
   const int qd = P.nq * P.hd, kd = P.nkv * P.hd;
   volatile int* abort_flag = &M->abort_flag;
   uint8_t* wring = ring + (size_t)warp * MK_STAGES * MK_STAGE_BYTES;
+  const int cpr = R.rowbytes / 16;   // 16-byte chunks per row
+  // Hot-loop state in registers (the by-reference arguments are written back
+  // at the end).
+  uint32_t scl = sc;
+  float bst = best;
+  int bix = bidx;
+  DeviceState* const stp = P.st;
+  float* const logits = P.logits;
   bool ok = true;
   for (int si = 0; si < R.nseg; ++si) {
-    const MkSeg& S = R.seg[si];
+    const MkSeg S = R.seg[si];   // by value: its fields stay in registers
     if (ph == PH_DOWN && P.E > 0) {
       // Expert slot S.slot multiplies its own activation vector.
       compute_sync();
       mk_copy_to_xs(P.act + (size_t)S.slot * P.f, P.f, xs);
     }
-    const int units = R.paired ? S.rows / 2 : S.rows;
-    for (int u = warp; u < units && ok; u += MK_COMPUTE_WARPS) {
-      const int nrow = R.paired ? 2 : 1;
-      float sums[2] = {0.f, 0.f};
-      for (int q = 0; q < nrow && ok; ++q) {
-        float acc = 0.f;
-        for (int off = 0; off < R.rowbytes; off += MK_STAGE_BYTES) {
-          const int len = min(MK_STAGE_BYTES, R.rowbytes - off);
-          const int st = sc % MK_STAGES;
-          const uint32_t par = (sc / MK_STAGES) & 1u;
-          if (!mk_mbar_wait(&M->full[warp][st], par, abort_flag, P.st, 201)) {
-            ok = false;
-            break;
-          }
-          const uint8_t* piece = wring + (size_t)st * MK_STAGE_BYTES;
-          const int c0 = off / 16;
-          for (int c = lane; c < len / 16; c += 32) {
-            float wv[V];
-            Chunk<W>::widen(*reinterpret_cast<const uint4*>(piece + (size_t)c * 16), wv);
-            const float* xv = xs + (c0 + c) * V;
-#pragma unroll
-            for (int e = 0; e < V; ++e) acc = fmaf(wv[e], xv[e], acc);
-          }
-          __syncwarp();
-          if (lane == 0) mk_mbar_arrive(&M->empty[warp][st]);
-          ++sc;
-          if (lane == 0) M->consumed[warp] = (int)sc;
-        }
-        sums[q] = warp_sum(acc);
-      }
-      if (!ok || lane != 0) continue;
+    int r0, r1;
+    mk_warp_rows(R, S, warp, r0, r1);
+    float pend = 0.f;   // sum of the even row of a pair in progress
+    // Epilogue of row rl (relative to S.row0) once its sum is known (lane 0).
+    auto finish = [&](int rl, float sum) {
       if (R.paired) {
-        const int rl = 2 * u;
-        const float a0 = sums[0], a1 = sums[1];
+        if ((rl & 1) == 0) {
+          pend = sum;
+          return;
+        }
+        if (lane != 0) return;
+        const float a0 = pend, a1 = sum;
         if (ph == PH_QKV) {
-          const int row = S.row0 + rl;
+          const int row = S.row0 + rl - 1;
           float v0 = a0, v1 = a1;
           if (L.bqkv) {
             v0 += L.bqkv[row];
@@ -540,29 +594,120 @@ __device__ bool mk_gemv_phase(const MkParams& P, int ph, int l, const MkRows& R,
             dst[o + 1] = from_f32<KV>(v1);
           }
         } else {  // PH_GATEUP: act[task] = silu(gate) * up
-          const int task = P.E > 0 ? S.out0 + (rl >> 1) : (S.row0 + rl) >> 1;
+          const int task = P.E > 0 ? S.out0 + ((rl - 1) >> 1) : (S.row0 + rl - 1) >> 1;
           P.act[task] = silu_f(a0) * a1;
         }
       } else {
-        const int rl = u;
-        const float a = sums[0];
+        if (lane != 0) return;
+        const float a = sum;
         const int row = S.row0 + rl;
         if (ph == PH_LMHEAD) {
-          if (P.logits) P.logits[row] = a;
-          if (a > best || (a == best && row < bidx)) {
-            best = a;
-            bidx = row;
+          if (logits) logits[row] = a;
+          if (a > bst || (a == bst && row < bix)) {
+            bst = a;
+            bix = row;
           }
         } else if (ph == PH_DOWN && P.E > 0) {
           float& acc = M->acc[rl];
           acc = S.slot == 0 ? M->wts[0] * a : fmaf(M->wts[S.slot], a, acc);
-        } else {  // PH_OPROJ, dense PH_DOWN: the residual row this CTA owns
-          P.x[row] = __ldcg(P.x + row) + a;
+        } else {  // PH_OPROJ, dense PH_DOWN: added to the residual row after the phase
+          M->acc[rl] = a;
         }
+      }
+    };
+    auto next_stage = [&]() -> const uint8_t* {
+      const int st = scl % MK_STAGES;
+      const uint32_t par = (scl / MK_STAGES) & 1u;
+      if (!mk_mbar_wait(&M->full[warp][st], par, abort_flag, stp, 201)) return nullptr;
+      return wring + (size_t)st * MK_STAGE_BYTES;
+    };
+    auto release_stage = [&]() {
+      __syncwarp();
+      const int st = scl % MK_STAGES;
+      if (lane == 0) mk_mbar_arrive(&M->empty[warp][st]);
+      ++scl;
+      if (lane == 0) M->consumed[warp] = (int)scl;
+    };
+    if (R.rowbytes <= MK_STAGE_BYTES) {
+      // Up to MK_RB rows of a stage per pass: each xs chunk is read once for
+      // all of them, and their FMA chains and shuffle reductions interleave.
+      const int rps = MK_STAGE_BYTES / R.rowbytes;
+      for (int r = r0; r < r1 && ok; r += rps) {
+        const int n = min(rps, r1 - r);
+        const uint8_t* piece = next_stage();
+        if (!piece) {
+          ok = false;
+          break;
+        }
+        for (int j0 = 0; j0 < n; j0 += MK_RB) {
+          const int nj = min(MK_RB, n - j0);
+          const uint8_t* rows = piece + (size_t)j0 * R.rowbytes;
+          float acc[MK_RB];
+#pragma unroll
+          for (int j = 0; j < MK_RB; ++j) acc[j] = 0.f;
+          for (int c = lane; c < cpr; c += 32) {
+            float xv[V];
+            mk_load_xs<V>(xs + c * V, xv);
+#pragma unroll
+            for (int j = 0; j < MK_RB; ++j) {
+              if (j < nj) {
+                float wv[V];
+                Chunk<W>::widen(*reinterpret_cast<const uint4*>(rows + (size_t)j * R.rowbytes + (size_t)c * 16), wv);
+#pragma unroll
+                for (int e = 0; e < V; ++e) acc[j] = fmaf(wv[e], xv[e], acc[j]);
+              }
+            }
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int j = 0; j < MK_RB; ++j) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
+          for (int j = 0; j < nj; ++j) finish(r + j0 + j, acc[j]);
+        }
+        release_stage();
+      }
+    } else {
+      for (int r = r0; r < r1 && ok; ++r) {
+        float acc0 = 0.f, acc1 = 0.f;
+        for (int off = 0; off < R.rowbytes; off += MK_STAGE_BYTES) {
+          const int len = min(MK_STAGE_BYTES, R.rowbytes - off);
+          const uint8_t* piece = next_stage();
+          if (!piece) {
+            ok = false;
+            break;
+          }
+          const int c0 = off / 16, nc = len / 16;
+          int c = lane;
+          for (; c + 32 < nc; c += 64) {
+            float w0[V], w1[V], x0[V], x1[V];
+            Chunk<W>::widen(*reinterpret_cast<const uint4*>(piece + (size_t)c * 16), w0);
+            Chunk<W>::widen(*reinterpret_cast<const uint4*>(piece + (size_t)(c + 32) * 16), w1);
+            mk_load_xs<V>(xs + (c0 + c) * V, x0);
+            mk_load_xs<V>(xs + (c0 + c + 32) * V, x1);
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+              acc0 = fmaf(w0[e], x0[e], acc0);
+              acc1 = fmaf(w1[e], x1[e], acc1);
+            }
+          }
+          if (c < nc) {
+            float w0[V], x0[V];
+            Chunk<W>::widen(*reinterpret_cast<const uint4*>(piece + (size_t)c * 16), w0);
+            mk_load_xs<V>(xs + (c0 + c) * V, x0);
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc0 = fmaf(w0[e], x0[e], acc0);
+          }
+          release_stage();
+        }
+        if (ok) finish(r, warp_sum(acc0 + acc1));
       }
     }
   }
-  if (ph == PH_DOWN && P.E > 0) {
+  sc = scl;
+  best = bst;
+  bidx = bix;
+  if (ph == PH_OPROJ || ph == PH_DOWN) {
+    // The residual rows this CTA owns (at most 256), one coalesced pass.
     compute_sync();
     if (R.nseg > 0)
       for (int i = threadIdx.x; i < R.seg[0].rows; i += MK_COMPUTE) {
@@ -717,14 +862,17 @@ __device__ void mk_prefetch_attention_kv(const MkParams& P, int l, int HD) {
 
 // ------------------------------------------------------------------ the kernel
 template <typename W, typename KV, int HD>
-__global__ void __launch_bounds__(MK_THREADS, 1) k_decode_step(const MkParams P) {
+__device__ void mk_produce(const MkParams& P, uint8_t* ring, MkMisc* M);
+template <typename W, typename KV, int HD>
+__device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMisc* M);
+
+template <typename W, typename KV, int HD>
+__global__ void __launch_bounds__(MK_THREADS, 1) k_decode_step(const __grid_constant__ MkParams P) {
   extern __shared__ __align__(1024) uint8_t mk_smem[];
   uint8_t* ring = mk_smem;
   uint8_t* ureg = mk_smem + MK_RING_BYTES;
   MkMisc* M = reinterpret_cast<MkMisc*>(ureg + P.u_bytes);
-  float* xs = reinterpret_cast<float*>(ureg);
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int nphase = P.n_layers * mk_phases_per_layer(P) + 1;
+  const int tid = threadIdx.x;
 
   if (tid == 0) {
     for (int w = 0; w < MK_COMPUTE_WARPS; ++w)
@@ -735,6 +883,8 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_step(const MkParams P)
     M->abort_flag = 0;
     M->moe_ready = 0;
     for (int w = 0; w < MK_COMPUTE_WARPS; ++w) M->consumed[w] = 0;
+    if (P.cluster) mk_mbar_init(&M->cbar, (uint32_t)P.cluster);
+    M->cgen = 0;
     int t = P.d_token ? *P.d_token : P.token;
     if (t < 0 || t >= P.V) {
       raise_error(P.st, ERR_TOKEN, 0);
@@ -754,9 +904,21 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_step(const MkParams P)
     M->cs[i] = make_float2((float)cn, (float)sn);
   }
   __syncthreads();
-  volatile int* abort_flag = &M->abort_flag;
+  // Cluster mode: every CTA's barrier is initialised before any remote
+  // arrival, and (at the end) no CTA exits while another may still arrive on
+  // its barrier.  barrier.cluster counts every thread of the cluster.
+  if (P.cluster) asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+  if ((tid >> 5) >= MK_COMPUTE_WARPS) mk_produce<W, KV, HD>(P, ring, M);
+  else mk_compute<W, KV, HD>(P, ring, ureg, M);
+  if (P.cluster) asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
 
-  if (warp >= MK_COMPUTE_WARPS) {
+template <typename W, typename KV, int HD>
+__device__ void mk_produce(const MkParams& P, uint8_t* ring, MkMisc* M) {
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int nphase = P.n_layers * mk_phases_per_layer(P) + 1;
+  volatile int* abort_flag = &M->abort_flag;
+  {
     // ---------------- producer: warp 8+w streams compute warp w's rows of every phase, in order
     const int w = warp - MK_COMPUTE_WARPS;
     if ((tid & 31) == 0) {
@@ -781,26 +943,27 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_step(const MkParams P)
         MkRows R;
         mk_phase_rows<W>(P, ph, l, M->ids, R);
         for (int si = 0; si < R.nseg && ok; ++si) {
-          const MkSeg& S = R.seg[si];
-          const int units = R.paired ? S.rows / 2 : S.rows;
-          const int nrow = R.paired ? 2 : 1;
-          for (int u = w; u < units && ok; u += MK_COMPUTE_WARPS) {
-            for (int q = 0; q < nrow && ok; ++q) {
-              const int rl = R.paired ? 2 * u + q : u;
-              const uint8_t* src = S.base + (size_t)(S.row0 + rl) * R.rowbytes;
-              for (int off = 0; off < R.rowbytes; off += MK_STAGE_BYTES) {
-                const int len = min(MK_STAGE_BYTES, R.rowbytes - off);
-                const int st = sc % MK_STAGES;
-                const uint32_t par = (sc / MK_STAGES) & 1u;
-                if (!mk_mbar_wait(&M->empty[w][st], par ^ 1u, abort_flag, P.st, 302)) {
-                  ok = false;
-                  break;
-                }
-                mk_mbar_expect_tx(&M->full[w][st], (uint32_t)len);
-                mk_bulk_load(wring + (size_t)st * MK_STAGE_BYTES, src + off, (uint32_t)len, &M->full[w][st]);
-                ++sc;
-              }
-            }
+          const MkSeg S = R.seg[si];   // by value: its fields stay in registers
+          int r0, r1;
+          mk_warp_rows(R, S, w, r0, r1);
+          const uint8_t* base = S.base + (size_t)S.row0 * R.rowbytes;
+          auto issue = [&](const uint8_t* src, int len) -> bool {
+            const int st = sc % MK_STAGES;
+            const uint32_t par = (sc / MK_STAGES) & 1u;
+            if (!mk_mbar_wait(&M->empty[w][st], par ^ 1u, abort_flag, P.st, 302)) return false;
+            mk_mbar_expect_tx(&M->full[w][st], (uint32_t)len);
+            mk_bulk_load(wring + (size_t)st * MK_STAGE_BYTES, src, (uint32_t)len, &M->full[w][st]);
+            ++sc;
+            return true;
+          };
+          if (R.rowbytes <= MK_STAGE_BYTES) {
+            const int rps = MK_STAGE_BYTES / R.rowbytes;
+            for (int r = r0; r < r1 && ok; r += rps)
+              ok = issue(base + (size_t)r * R.rowbytes, min(rps, r1 - r) * R.rowbytes);
+          } else {
+            for (int r = r0; r < r1 && ok; ++r)
+              for (int off = 0; off < R.rowbytes && ok; off += MK_STAGE_BYTES)
+                ok = issue(base + (size_t)r * R.rowbytes + off, min(MK_STAGE_BYTES, R.rowbytes - off));
           }
         }
       }
@@ -813,9 +976,15 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_step(const MkParams P)
           }
       }
     }
-    return;
   }
+}
 
+template <typename W, typename KV, int HD>
+__device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMisc* M) {
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int nphase = P.n_layers * mk_phases_per_layer(P) + 1;
+  volatile int* abort_flag = &M->abort_flag;
+  float* xs = reinterpret_cast<float*>(ureg);
   // ---------------- compute warps
   if (P.stamps && blockIdx.x == 0 && tid == 0) P.stamps[0] = globaltimer_ns();
   const int token = M->token;
@@ -865,7 +1034,11 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_step(const MkParams P)
       ok = mk_gemv_phase<W, KV>(P, ph, l, R, ring, M, xs, sc, best, bidx);
     }
     if (!ok || *abort_flag) break;
-    if (ph != PH_LMHEAD && !mk_grid_sync(P.st, (unsigned)P.nb, abort_flag, 400 + ph)) break;
+    if (ph != PH_LMHEAD) {
+      const bool synced = P.cluster ? mk_cluster_sync(P.st, (unsigned)P.nb, &M->cbar, &M->cgen, abort_flag, 400 + ph)
+                                    : mk_grid_sync(P.st, (unsigned)P.nb, abort_flag, 400 + ph);
+      if (!synced) break;
+    }
     if (P.stamps && blockIdx.x == 0 && tid == 0) P.stamps[i + 1] = globaltimer_ns();
   }
   if (*abort_flag || !P.d_argmax) return;
@@ -980,6 +1153,7 @@ bool mk_prepare(Model& m, int num_sms) {
   const dec_config& c = m.cfg;
   const int es = c.weight_dtype == DEC_BF16 ? 2 : 4;
   m.mk_ok = false;
+  m.mk_cluster = 0;
   (void)es;
   // MoE down keeps one row sum per owned row; RoPE table of up to 64 pairs.
   if ((c.hidden + num_sms - 1) / num_sms > 256 || c.head_dim / 2 > 64) return false;
@@ -994,11 +1168,39 @@ bool mk_prepare(Model& m, int num_sms) {
   m.mk_smem = smem;
   m.mk_nb = num_sms;
   m.mk_ok = true;
+  // One-cluster schedule: 16 CTAs (a non-portable size) or 8, if the GPU can
+  // place such a cluster with this kernel's shared memory; the MoE row sums
+  // need at most 256 residual rows per CTA.
+  m.mk_cluster = 0;
+  for (int cs = 16; cs >= 8; cs /= 2) {
+    if ((c.hidden + cs - 1) / cs > 256) break;
+    if (cs > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs);
+    cfg.blockDim = dim3(MK_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = cs;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int nc = 0;
+    if (cudaOccupancyMaxActiveClusters(&nc, fn, &cfg) == cudaSuccess && nc >= 1) {
+      m.mk_cluster = cs;
+      break;
+    }
+    cudaGetLastError();
+  }
   return true;
 }
 
 void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, int32_t token, int32_t pos,
-                      float* logits, int32_t* d_argmax) {
+                      float* logits, int32_t* d_argmax, bool cluster) {
   const dec_config& c = m.cfg;
   const Scratch& S = m.s;
   MkParams P;
@@ -1016,7 +1218,8 @@ void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, in
   P.nsplit = m.nsplit;
   P.sps = m.attn_sps;
   P.merge_phase = (m.nsplit > 1 && (size_t)c.n_heads * m.nsplit * (c.head_dim + 2) * 4 > 64 * 1024) ? 1 : 0;
-  P.nb = m.mk_nb;
+  P.nb = cluster ? m.mk_cluster : m.mk_nb;
+  P.cluster = cluster ? m.mk_cluster : 0;
   P.eps = c.rms_eps;
   P.layers = m.mk_layers;
   P.embed = m.tok_embd;
@@ -1044,13 +1247,20 @@ void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, in
   P.stamps = m.mk_stamps;
   P.kv_bytes = c.kv_dtype == DEC_BF16 ? 2 : 4;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(m.mk_nb);
+  cfg.gridDim = dim3(P.nb);
   cfg.blockDim = dim3(MK_THREADS);
   cfg.dynamicSmemBytes = m.mk_smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  if (cluster) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = P.nb;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void* args[] = {&P};

@@ -116,6 +116,7 @@ struct Model {
   size_t mk_smem;       // its dynamic shared memory
   int mk_nb;            // its grid (one CTA per SM)
   bool mk_ok;           // the persistent kernel fits this configuration
+  int mk_cluster;       // CTAs of its one-cluster schedule (0: the GPU cannot place such a cluster)
   unsigned long long* mk_stamps;  // nullable phase timestamps (dec_phase_stamps)
   int lm_grid;          // CTAs of the LM head kernel
   int32_t* trace_ids;   // nullable
@@ -173,8 +174,9 @@ const void* set_step_kernel();
 // Persistent single-kernel decode step (decode_mk.cu).
 size_t mk_smem_bytes(const dec_config& c, int nsplit);
 bool mk_prepare(Model& m, int num_sms);
+// cluster: run on one thread-block cluster of m.mk_cluster CTAs, else over m.mk_nb CTAs (one per SM).
 void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, int32_t token, int32_t pos,
-                      float* logits, int32_t* d_argmax);
+                      float* logits, int32_t* d_argmax, bool cluster);
 // Final RMSNorm + LM head (+ argmax) of one residual row x.
 void launch_lmhead(const Model& m, cudaStream_t s, const float* x, float* logits, int32_t* d_argmax);
 

@@ -21,12 +21,14 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdec.so"
 
 DEC_OK, DEC_EINVAL, DEC_ERANGE, DEC_ECUDA, DEC_ETIMEOUT, DEC_ENOMEM = range(6)
 DEC_F32, DEC_BF16 = 0, 1
+DEC_FUSED_OFF, DEC_FUSED_GRID, DEC_FUSED_CLUSTER = 0, 1, 2
+FUSED_MODES = {"off": DEC_FUSED_OFF, "grid": DEC_FUSED_GRID, "cluster": DEC_FUSED_CLUSTER}
 STATUS_NAMES = {0: "DEC_OK", 1: "DEC_EINVAL", 2: "DEC_ERANGE", 3: "DEC_ECUDA", 4: "DEC_ETIMEOUT", 5: "DEC_ENOMEM"}
 
 EXPORTED = ["dec_config_validate", "dec_workspace_bytes", "dec_create", "dec_prefill", "dec_decode",
             "dec_decode_dev", "dec_kv_reset", "dec_length", "dec_kv_layer", "dec_set_trace",
             "dec_check", "dec_timing_enable", "dec_timing_read", "dec_launch_count", "dec_destroy",
-            "dec_last_error", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc", "dec_gemm_bf16", "dec_set_graph", "dec_set_fused", "dec_phase_stamps"]
+            "dec_last_error", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc", "dec_gemm_bf16", "dec_set_graph", "dec_set_fused", "dec_fused_available", "dec_fused_mode", "dec_phase_stamps"]
 
 KERNEL_CLASSES = {"qkv": 1, "attn": 2, "oproj": 3, "gateup": 4, "down": 5, "lmhead": 6, "router": 7,
                   "pf_gemm": 8, "pf_attn": 9, "step": 10}
@@ -79,6 +81,8 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "dec_gemm_bf16": (I32, [P, P, P, P, I32, I32, I32, P]),
         "dec_set_graph": (I32, [P, I32]),
         "dec_set_fused": (I32, [P, I32]),
+        "dec_fused_available": (I32, [P, I32]),
+        "dec_fused_mode": (I32, [P]),
         "dec_phase_stamps": (I32, [P, P, I32]),
         "dec_last_error": (ctypes.c_char_p, [P]),
     }
@@ -272,9 +276,25 @@ class Decoder:
                    d_argmax: Optional[torch.Tensor] = None) -> None:
         self._raise(lib.dec_decode_dev(self.h, d_token.data_ptr(), int(pos), _ptr(logits), _ptr(d_argmax)))
 
-    def set_fused(self, enable: bool) -> None:
-        """Persistent one-kernel decode step (default) or per-layer kernels."""
-        self._raise(lib.dec_set_fused(self.h, int(bool(enable))))
+    def set_fused(self, mode) -> None:
+        """Decode schedule: "off" (per-layer kernels), "grid" (one persistent kernel over every SM) or
+        "cluster" (one persistent kernel on one thread-block cluster); True means "grid", False "off"."""
+        if isinstance(mode, bool):
+            mode = DEC_FUSED_GRID if mode else DEC_FUSED_OFF
+        elif isinstance(mode, str):
+            mode = FUSED_MODES[mode]
+        self._raise(lib.dec_set_fused(self.h, int(mode)))
+
+    def fused_mode(self) -> str:
+        """The schedule the next decode step takes: "off", "grid" or "cluster"."""
+        m = int(lib.dec_fused_mode(self.h))
+        return {v: k for k, v in FUSED_MODES.items()}[m]
+
+    def fused_available(self, mode) -> int:
+        """1 (or the cluster's CTA count) when the schedule can run on this handle, else 0."""
+        if isinstance(mode, str):
+            mode = FUSED_MODES[mode]
+        return int(lib.dec_fused_available(self.h, int(mode)))
 
     def phase_stamps(self, stamps: Optional[torch.Tensor]) -> None:
         """Device int64 tensor receiving per-phase GPU timestamps of each fused decode step (None stops)."""

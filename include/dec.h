@@ -167,14 +167,28 @@ dec_status dec_kv_layer(const dec_handle *h, int32_t layer, void **k, void **v);
  * Buffers are device memory owned by the caller. */
 dec_status dec_set_trace(dec_handle *h, int32_t *d_ids, float *d_logits, int32_t capacity);
 
-/* Decode step schedule.  enable = 1: ONE persistent cooperative kernel per
- * step (every layer and the head, grid-wide barriers between phases, weights
- * streamed by bulk copies), used when the configuration fits its shared-memory
- * plan.  enable = 0: per-layer kernels chained by programmatic dependent launch
- * in a CUDA graph.  dec_create picks the persistent kernel when the weights
- * read per token exceed 4 GB (bandwidth-bound), else the per-layer kernels
- * (latency-bound).  Results agree to rounding. */
-dec_status dec_set_fused(dec_handle *h, int32_t enable);
+/* Decode step schedules (dec_set_fused). */
+typedef enum dec_schedule {
+  DEC_FUSED_OFF = 0,      /* per-layer kernels chained by programmatic dependent launch in a CUDA graph */
+  DEC_FUSED_GRID = 1,     /* ONE persistent cooperative kernel per step over every SM: every layer and the
+                             head, grid-wide barriers between phases, weights streamed by bulk copies */
+  DEC_FUSED_CLUSTER = 2   /* the same persistent step on ONE thread-block cluster (up to 16 SMs), whose
+                             phase barriers are shared-memory mbarriers across the cluster */
+} dec_schedule;
+
+/* Selects the decode step schedule.  A schedule the configuration or GPU cannot
+ * take (see dec_fused_available) falls back to DEC_FUSED_OFF at each step.
+ * dec_create picks DEC_FUSED_GRID when the weights read per token exceed 4 GB
+ * (bandwidth-bound), else DEC_FUSED_OFF (latency-bound).  Results agree to
+ * rounding.  DEC_EINVAL for an unknown mode. */
+dec_status dec_set_fused(dec_handle *h, int32_t mode);
+
+/* Whether a schedule can run on this handle: 1 (DEC_FUSED_OFF, DEC_FUSED_GRID),
+ * the cluster's CTA count (DEC_FUSED_CLUSTER), or 0. */
+int32_t dec_fused_available(const dec_handle *h, int32_t mode);
+
+/* The schedule the next decode step takes (after any fallback); -1 for NULL. */
+int32_t dec_fused_mode(const dec_handle *h);
 
 /* Measurement hook of the persistent decode step: when d_stamps (device,
  * >= 6*n_layers + 2 entries) is set, every later fused decode step writes the

@@ -290,19 +290,25 @@ def test_mistral_full_prefill_then_wrapping_decode(dec_mod):
                                      ("toy", dict(sliding_window=8, max_seq=8)), ("smollm2-135m", {}),
                                      ("mixtral-8x7b", dict(n_layers=2))])
 def test_fused_step_matches_per_layer_kernels(dec_mod, name, kw):
-    # The persistent one-kernel decode step and the per-layer kernels are two
-    # schedules of the same arithmetic: same greedy stream, logits to rounding.
+    # The per-layer kernels and the persistent one-kernel decode step (over
+    # every SM, or on one thread-block cluster) are schedules of the same
+    # arithmetic: same greedy stream, logits to rounding.
     w = synthetic.workload(name, **kw)
     P = 12 if name == "toy" else 40
     prompt = synthetic.prompt_tokens(w, P, seed=9)
     runs = []
     weights = None
-    for fused in (True, False):
+    for mode in ("off", "grid", "cluster"):
         d = dec_mod.Decoder(w, weights=weights)
         weights = d.weights
-        d.set_fused(fused)
-        runs.append(gpu_greedy(d, prompt, 10))
+        if not d.fused_available(mode):
+            assert mode == "cluster", f"schedule {mode} unavailable"
+            d.close()
+            continue
+        d.set_fused(mode)
+        runs.append((mode, gpu_greedy(d, prompt, 10)))
         d.close()
-    (ra, ta), (rb, tb) = runs
-    assert ta == tb
-    np.testing.assert_allclose(ra, rb, atol=2e-4 if w["dtype"] == "f32" else 2e-3, rtol=1e-4)
+    (_, (ra, ta)) = runs[0]
+    for mode, (rb, tb) in runs[1:]:
+        assert ta == tb, mode
+        np.testing.assert_allclose(ra, rb, atol=2e-4 if w["dtype"] == "f32" else 2e-3, rtol=1e-4, err_msg=mode)
