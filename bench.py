@@ -11,6 +11,7 @@ oracle on the host cores instead (the baseline arm).  Prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -58,6 +59,32 @@ def weight_bytes(w: dict) -> dict:
         "lmhead": w["vocab"] * h * es,
         "embed_row": h * es,
     }
+
+
+# DRAM bytes per launch of a roofline kernel, from one ncu capture each (the
+# summaries under profiles/ give the commands).  A figure holds only for the
+# kernel source it measured: the source file's SHA-256 at capture time must
+# match the current file, else the bench reports traffic as null.
+TRAFFIC = {
+    ("smollm2-135m", "down"): {
+        "bytes": 1814336, "source": "decoder_only_forward_gb300/csrc/decode.cu",
+        "sha256": "3d7213fecd5001252701110382d8e9dfd57676011ecc1ded9bf6666198c7ae34",
+        "profile": "profiles/gemv_down_smollm2-135m_traffic.md"},
+}
+
+
+def measured_traffic(workload: str, kernel: str):
+    t = TRAFFIC.get((workload, kernel))
+    if t is None:
+        return None
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), t["source"])
+    try:
+        with open(path, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != t["sha256"]:
+                return None
+    except OSError:
+        return None
+    return t["bytes"]
 
 
 def decode_bytes(w: dict, pos: int, kv_es: int) -> float:
@@ -290,7 +317,8 @@ def run_ours(args, rank, world, local_rank):
     avg_launch_s = (pc["prefill_ms"] + pc["decode_ms"]) / max(nl, 1) / 1e3
     achieved = per_launch_bytes / avg_launch_s / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": None, "peak_kind": peak_kind,
+                "frac": round(achieved / hbm, 4), "traffic": measured_traffic(args.workload, dom),
+                "peak_kind": peak_kind,
                 "bytes_per_launch": int(per_launch_bytes), "avg_launch_us": round(avg_launch_s * 1e6, 3),
                 "launches_per_step": nl}
 

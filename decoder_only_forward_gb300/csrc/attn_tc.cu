@@ -3,8 +3,8 @@
 // kv head with a one-pass online softmax (rml "The decoder", Attend; the
 // ZLLM page's softmax(QK^T/sqrt(d) + mask)V).
 //
-//   S  = Q . K^T   M=128, N=64,  K=HD   (TMEM columns [0, 64))
-//   O += P . V     M=128, N=HD,  K=64   (TMEM columns [64, 64+HD))
+//   S(j) = Q . K(j)^T   M=128, N=64, K=HD   (TMEM columns [64 (j%2), 64 (j%2) + 64))
+//   O   += P(j) . V(j)  M=128, N=HD, K=64   (TMEM columns [128, 128 + HD))
 //
 // Every operand x is carried as a pair of bf16 planes, hi = bf16(x) and
 // lo = bf16(x - hi), and each product as hi.hi + hi.lo + lo.hi: the dropped
@@ -15,9 +15,10 @@
 // Operands sit in shared memory K-major with 128-byte swizzling: the Q planes
 // come from the QKV epilogue, the K planes and a transposed V (V^T rows of
 // keys) from k_kv_split, P from the softmax threads.  Roles: warp 0 TMA
-// producer, warp 1 MMA issuer (and TMEM owner), warps 2-5 softmax: thread i
-// of those owns query row i (TMEM lane i), keeps its running max and sum in
-// registers, and rescales its O row in TMEM when the max grows.
+// producer (separate K and V^T rings, so K runs two tiles ahead), warp 1 MMA
+// issuer and TMEM owner (S of the next tile is issued before P.V of this one,
+// into the other S buffer), warps 2-9 softmax: two threads per query row, each
+// owning half of a tile's keys and half of O's columns.
 #include <cudaTypedefs.h>
 
 #include <mutex>
