@@ -162,6 +162,7 @@ WsPlan dec::plan_workspace(const dec_config& c) {
   p.at_Kb = take(2 * 2 * (size_t)p.at_kcap * kd);
   p.at_Vt = take(2 * 2 * (size_t)kd * p.at_vt_ld);
   p.mk_layers = take(sizeof(MkLayer) * (size_t)c.n_layers);
+  p.mk_maps = take(mk_maps_bytes(c));
   p.kv = off;
   p.kv_layer_bytes = align_up(ks * (size_t)c.max_seq * kd, 256);
   off += 2 * p.kv_layer_bytes * c.n_layers;
@@ -298,6 +299,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
       tab[l] = MkLayer{d.attn_norm, d.wqkv, d.bqkv, d.wo, d.ffn_norm, d.w_gateup, d.w_down, d.router, d.kc, d.vc};
     }
     m.mk_layers = (const MkLayer*)(base + p.mk_layers);
+    m.mk_maps = mk_maps_bytes(*cfg) ? (void*)(base + p.mk_maps) : nullptr;
     cudaError_t e2 = cudaMemcpy((void*)m.mk_layers, tab.data(), sizeof(MkLayer) * tab.size(), cudaMemcpyHostToDevice);
     int dev = 0, sms = 0;
     if (e2 == cudaSuccess) e2 = cudaGetDevice(&dev);
@@ -310,14 +312,15 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
     cudaGetLastError();  // a configuration the persistent kernel cannot take is not an error
     // Small models are bound by the latency of ~150 dependent phases per token,
     // where the per-layer kernels overlapped by programmatic dependent launch
-    // are faster; large models are bound by the weight stream, where the
-    // persistent kernel's bulk-copy rings are faster.
+    // are faster (SmolLM2-135M, 0.27 GB per token); from about half a GB per
+    // token the persistent kernel's weight rings win (Qwen2.5-0.5B, ~1 GB:
+    // 1030 vs 715 tok/s decode on GB300).
     size_t wbytes = (size_t)cfg->vocab * cfg->hidden * (cfg->tied_embedding ? 1 : 2);
     const size_t qd = (size_t)cfg->n_heads * cfg->head_dim, kd = (size_t)cfg->n_kv_heads * cfg->head_dim;
     const size_t kslots = cfg->n_experts ? cfg->n_experts_used : 1;
     wbytes += (size_t)cfg->n_layers * ((qd + 2 * kd) * cfg->hidden + cfg->hidden * qd + 3 * kslots * cfg->ffn * cfg->hidden);
     wbytes *= cfg->weight_dtype == DEC_BF16 ? 2 : 4;
-    h->fused_mode = wbytes >= (size_t)4 << 30 ? DEC_FUSED_GRID : DEC_FUSED_OFF;
+    h->fused_mode = wbytes >= (size_t)512 << 20 ? DEC_FUSED_GRID : DEC_FUSED_OFF;
   }
 
   // RoPE frequencies inv_i = theta^(-2i/hd), llama3-scaled when enabled

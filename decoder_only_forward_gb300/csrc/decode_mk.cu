@@ -22,19 +22,48 @@
 //   DOWN   x += Wd act (MoE: selected experts in selection order)
 // then LMHEAD: final RMSNorm -> logits + argmax.  Cross-CTA data (x, q,
 // partials, act) is read with ld.global.cg so no stale L1 line is used.
+#include <cudaTypedefs.h>
 #include <math.h>
 
+#include <mutex>
+#include <vector>
+
 #include "runtime.h"
+#include "tc.cuh"
 
 namespace dec {
 
 constexpr int MK_COMPUTE_WARPS = 8;
 constexpr int MK_COMPUTE = MK_COMPUTE_WARPS * 32;   // 256 compute threads
 constexpr int MK_THREADS = 2 * MK_COMPUTE;          // + one producer warp per compute warp
-constexpr int MK_STAGES = 4;                        // per compute warp
-constexpr int MK_STAGE_BYTES = 4 * 1024;            // one piece of one weight row
-constexpr int MK_RING_BYTES = MK_COMPUTE_WARPS * MK_STAGES * MK_STAGE_BYTES;  // 128 KB
+constexpr int MK_WARP_RING = 16 * 1024;            // weight ring of one compute warp
+constexpr int MK_RING_BYTES = MK_COMPUTE_WARPS * MK_WARP_RING;  // 128 KB
+constexpr int MK_MAX_STAGES = 8;
 constexpr int MK_KS = 64;                           // keys per attention chunk
+
+// Weight-ring stages by weight type.  bf16 weights: tensor-core GEMV, a stage
+// is 16 rows x MK_KG columns as MK_BPS TMA boxes of 64 columns side by side
+// (128-byte swizzled), so each weight row is fetched in runs of MK_KG * 2
+// bytes (DRAM page locality).  f32
+// weights: CUDA-core GEMV, a stage is up to 4 KB of whole rows or one piece
+// of a longer row.
+template <typename W> struct MkRing;
+template <> struct MkRing<float> {
+  static constexpr int STAGES = 4, BYTES = 4096;
+  static constexpr bool MMA = false;
+};
+#ifndef MK_BPS
+#define MK_BPS 2   // 64-column boxes per stage of the tensor-core GEMV
+#endif
+constexpr int MK_TM = 16, MK_TK = 64;               // one TMA box: rows x columns (2 KB bf16)
+constexpr int MK_KG = MK_TK * MK_BPS;               // columns per stage: each row read in runs of 2^7 * MK_BPS B
+template <> struct MkRing<__nv_bfloat16> {
+  static constexpr int STAGES = 8 / MK_BPS, BYTES = 2048 * MK_BPS;
+  static constexpr bool MMA = true;
+};
+constexpr int MK_CHUNK = 8;                         // row blocks reduced together (partials in smem)
+// Tensor maps per layer (bf16 weights): QKV, O, gate/up, down; then the head.
+enum MkMap { MAP_QKV = 0, MAP_O, MAP_GATEUP, MAP_DOWN, MAPS_PER_LAYER };
 
 enum MkPhase { PH_QKV = 0, PH_ATTN, PH_MERGE, PH_OPROJ, PH_GATEUP, PH_DOWN, PH_LMHEAD };
 
@@ -66,12 +95,16 @@ struct MkParams {
   unsigned long long* stamps;     // nullable: %globaltimer after each phase (CTA 0), [0] = start
   int kv_bytes;                   // bytes per KV element
   int cluster;                    // > 0: the grid is ONE thread-block cluster of this many CTAs
+  const CUtensorMap* maps;        // bf16 weights: [n_layers * MAPS_PER_LAYER + 1] (global memory)
+  int xb_plane;                   // bf16 weights: elements per plane of the (hi, lo) activation copy
+  int xs_floats;                  // floats of the f32 activation vector region
 };
 
 // Shared-memory bookkeeping after the weight ring and the union region.
 struct MkMisc {
-  uint64_t full[MK_COMPUTE_WARPS][MK_STAGES];
-  uint64_t empty[MK_COMPUTE_WARPS][MK_STAGES];
+  uint64_t full[MK_COMPUTE_WARPS][MK_MAX_STAGES];
+  uint64_t empty[MK_COMPUTE_WARPS][MK_MAX_STAGES];
+  float part[MK_CHUNK][MK_COMPUTE_WARPS][MK_TM];  // tensor-core GEMV: per-warp row partials
   float2 cs[64];                 // (cos, sin) of this position's rotary pairs
   float red[40];
   float logits[MAX_EXPERTS];
@@ -234,24 +267,30 @@ namespace dec {
 
 // ------------------------------------------------------------------ schedule
 // The weight rows one CTA handles in one phase: up to k contiguous segments
-// (one per selected expert), streamed in stages of `rps` whole rows.  Producer
-// and consumers both derive it, so they agree stage by stage.
+// (one per selected expert).  Producer and consumers both derive it, so they
+// agree stage by stage.  On the tensor-core path every CTA's share is a
+// multiple of 16 rows (the MMA's M), so no CTA reads rows another one owns.
 struct MkSeg {
   const uint8_t* base;   // row 0 of the segment's matrix
   int row0, rows;        // rows [row0, row0 + rows)
   int out0;              // output index of the segment's first row (task space)
   int slot;              // expert slot (MoE), else 0
+  int map;               // tensor map of the matrix (bf16 weights)
+  int maprow;            // row of the map holding the segment's row row0
 };
 struct MkRows {
   int nseg;
   MkSeg seg[MAX_EXPERTS_USED];
   int K;                 // row length (elements)
   int rowbytes;
-  int rps;               // rows per stage
+  int rps;               // rows per stage (CUDA-core path)
   bool paired;
 };
 
 __device__ __forceinline__ bool mk_is_gemv(int ph) { return ph != PH_ATTN && ph != PH_MERGE; }
+
+// ceil(n / nb) rounded up to a multiple of g.
+__device__ __forceinline__ int mk_share(int n, int nb, int g) { return ((n + nb - 1) / nb + g - 1) / g * g; }
 
 template <typename W>
 __device__ void mk_phase_rows(const MkParams& P, int ph, int l, const int* ids, MkRows& R) {
@@ -259,61 +298,64 @@ __device__ void mk_phase_rows(const MkParams& P, int ph, int l, const int* ids, 
   const int b = blockIdx.x, nb = P.nb;
   const MkLayer& L = P.layers[l < P.n_layers ? l : 0];
   const int qd = P.nq * P.hd, kd = P.nkv * P.hd;
+  const int g = MkRing<W>::MMA ? MK_TM : 1;     // row granularity of a CTA's share
+  const int mbase = (l < P.n_layers ? l : 0) * MAPS_PER_LAYER;
   R.nseg = 0;
-  auto single = [&](const void* mat, int N, int K) {
-    const int per = (N + nb - 1) / nb;
-    const int r0 = b * per, r1 = min(N, r0 + per);
+  auto single = [&](const void* mat, int N, int K, int map) {
+    const int per = mk_share(N, nb, g);
+    const int r0 = min(N, b * per), r1 = min(N, r0 + per);
     R.K = K;
     R.paired = false;
-    if (r1 > r0) R.seg[R.nseg++] = MkSeg{(const uint8_t*)mat, r0, r1 - r0, r0, 0};
+    if (r1 > r0) R.seg[R.nseg++] = MkSeg{(const uint8_t*)mat, r0, r1 - r0, r0, 0, map, r0};
   };
-  auto paired = [&](const void* mat, int N, int K) {
-    const int P2 = N / 2, per = (P2 + nb - 1) / nb;
-    const int p0 = b * per, p1 = min(P2, p0 + per);
+  auto paired = [&](const void* mat, int N, int K, int map) {
+    const int P2 = N / 2, per = mk_share(P2, nb, (g + 1) / 2);
+    const int p0 = min(P2, b * per), p1 = min(P2, p0 + per);
     R.K = K;
     R.paired = true;
-    if (p1 > p0) R.seg[R.nseg++] = MkSeg{(const uint8_t*)mat, 2 * p0, 2 * (p1 - p0), 2 * p0, 0};
+    if (p1 > p0) R.seg[R.nseg++] = MkSeg{(const uint8_t*)mat, 2 * p0, 2 * (p1 - p0), 2 * p0, 0, map, 2 * p0};
   };
   switch (ph) {
-    case PH_QKV: paired(L.wqkv, qd + 2 * kd, P.h); break;
-    case PH_OPROJ: single(L.wo, P.h, qd); break;
-    case PH_LMHEAD: single(P.head, P.V, P.h); break;
+    case PH_QKV: paired(L.wqkv, qd + 2 * kd, P.h, mbase + MAP_QKV); break;
+    case PH_OPROJ: single(L.wo, P.h, qd, mbase + MAP_O); break;
+    case PH_LMHEAD: single(P.head, P.V, P.h, P.n_layers * MAPS_PER_LAYER); break;
     case PH_GATEUP:
       if (P.E == 0) {
-        paired(L.w_gateup, 2 * P.f, P.h);
+        paired(L.w_gateup, 2 * P.f, P.h, mbase + MAP_GATEUP);
       } else {
         // Tasks = (slot, gate/up row pair), slot-major, split evenly over CTAs.
-        const int T = P.k * P.f, per = (T + nb - 1) / nb;
-        const int t0 = b * per, t1 = min(T, t0 + per);
+        const int T = P.k * P.f, per = mk_share(T, nb, (g + 1) / 2);
+        const int t0 = min(T, b * per), t1 = min(T, t0 + per);
         R.K = P.h;
         R.paired = true;
         for (int j = 0; j < P.k; ++j) {
           const int a = max(t0, j * P.f), e = min(t1, (j + 1) * P.f);
           if (e <= a) continue;
           const uint8_t* base = (const uint8_t*)L.w_gateup + (size_t)ids[j] * 2 * P.f * P.h * es;
-          R.seg[R.nseg++] = MkSeg{base, 2 * (a - j * P.f), 2 * (e - a), a, j};
+          const int r0 = 2 * (a - j * P.f);
+          R.seg[R.nseg++] = MkSeg{base, r0, 2 * (e - a), a, j, mbase + MAP_GATEUP, ids[j] * 2 * P.f + r0};
         }
       }
       break;
     case PH_DOWN:
       if (P.E == 0) {
-        single(L.w_down, P.h, P.f);
+        single(L.w_down, P.h, P.f, mbase + MAP_DOWN);
       } else {
-        const int per = (P.h + nb - 1) / nb;
-        const int r0 = b * per, r1 = min(P.h, r0 + per);
+        const int per = mk_share(P.h, nb, g);
+        const int r0 = min(P.h, b * per), r1 = min(P.h, r0 + per);
         R.K = P.f;
         R.paired = false;
         if (r1 > r0)
           for (int j = 0; j < P.k; ++j) {
             const uint8_t* base = (const uint8_t*)L.w_down + (size_t)ids[j] * P.h * P.f * es;
-            R.seg[R.nseg++] = MkSeg{base, r0, r1 - r0, r0, j};
+            R.seg[R.nseg++] = MkSeg{base, r0, r1 - r0, r0, j, mbase + MAP_DOWN, ids[j] * P.h + r0};
           }
       }
       break;
     default: break;
   }
   R.rowbytes = R.K * es;
-  int rps = MK_STAGE_BYTES / R.rowbytes;
+  int rps = MkRing<W>::BYTES / R.rowbytes;
   if (R.paired) rps &= ~1;
   R.rps = rps < 1 ? 1 : rps;
 }
@@ -373,18 +415,41 @@ __device__ __forceinline__ float mk_dot_row(const uint8_t* row, const float* xs,
 namespace dec {
 
 // ------------------------------------------------------------------ compute prologues
+// dst[0..K) = src[0..K): global f32 written by other CTAs, fetched with 16-byte
+// asynchronous copies through L2, all in flight at once (src, dst 16-byte
+// aligned).
+__device__ void mk_fetch(const float* src, int K, float* dst) {
+  const int nv = K >> 2;
+  for (int i = threadIdx.x; i < nv; i += MK_COMPUTE) cp_async16(dst + 4 * i, src + 4 * i);
+  cp_async_commit();
+  for (int k = 4 * nv + threadIdx.x; k < K; k += MK_COMPUTE) dst[k] = __ldcg(src + k);
+  cp_async_wait_all();
+  compute_sync();
+}
+
+// Element k of the activation as a bf16 (hi, lo) pair: the B operand of the
+// tensor-core GEMV (x = hi + lo to ~16 bits).
+__device__ __forceinline__ void mk_put_xb(__nv_bfloat16* xb, int plane, int k, float v) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+  xb[k] = hi;
+  xb[plane + k] = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
 // xs = v / sqrt(mean(v^2) + eps) * wn over the 256 compute threads, with v the
-// embedding row (erow) or the residual x (read from L2).
+// embedding row (erow) or the residual x (fetched from L2).  With xb, the
+// result also goes to the bf16 (hi, lo) planes, zero-padded to kpad columns.
 template <typename W>
 __device__ void mk_norm_to_xs(const float* x, const W* erow, const float* __restrict__ wn, int K, float eps,
-                              float* xs, MkMisc* M) {
+                              float* xs, MkMisc* M, __nv_bfloat16* xb = nullptr, int plane = 0, int kpad = 0) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float ss = 0.f;
-  for (int k = tid; k < K; k += MK_COMPUTE) {
-    const float v = erow ? to_f32(erow[k]) : __ldcg(x + k);
-    xs[k] = v;
-    ss = fmaf(v, v, ss);
+  if (erow) {
+    for (int k = tid; k < K; k += MK_COMPUTE) xs[k] = to_f32(erow[k]);
+    compute_sync();
+  } else {
+    mk_fetch(x, K, xs);
   }
+  float ss = 0.f;
+  for (int k = tid; k < K; k += MK_COMPUTE) ss = fmaf(xs[k], xs[k], ss);
   ss = warp_sum(ss);
   if (lane == 0) M->red[warp] = ss;
   compute_sync();
@@ -395,14 +460,28 @@ __device__ void mk_norm_to_xs(const float* x, const W* erow, const float* __rest
   }
   compute_sync();
   const float inv = 1.0f / sqrtf(M->red[32] / (float)K + eps);
-  for (int k = tid; k < K; k += MK_COMPUTE) xs[k] = xs[k] * inv * wn[k];
+  const int kend = xb && kpad > K ? kpad : K;
+  // Norm weights four at a time, their loads issued before any use.
+  for (int k0 = tid; k0 < kend; k0 += 4 * MK_COMPUTE) {
+    float wv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = k0 + u * MK_COMPUTE;
+      wv[u] = k < K ? wn[k] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = k0 + u * MK_COMPUTE;
+      if (k >= kend) break;
+      const float v = k < K ? xs[k] * inv * wv[u] : 0.f;
+      if (k < K) xs[k] = v;
+      if (xb) mk_put_xb(xb, plane, k, v);
+    }
+  }
   compute_sync();
 }
 
-__device__ void mk_copy_to_xs(const float* src, int K, float* xs) {
-  for (int k = threadIdx.x; k < K; k += MK_COMPUTE) xs[k] = __ldcg(src + k);
-  compute_sync();
-}
+__device__ void mk_copy_to_xs(const float* src, int K, float* xs) { mk_fetch(src, K, xs); }
 
 // Merges split partials of `heads` query heads [h0, h0+heads) into dst
 // (dst[(h - h0) * HD + d]); scale is [heads][nsplit] scratch.  Weight of split
@@ -503,7 +582,7 @@ __device__ void mk_router(const MkParams& P, int l, const float* xs, MkMisc* M) 
 namespace dec {
 
 // ------------------------------------------------------------------ GEMV phase (consumer side)
-constexpr int MK_RB = 4;   // rows reduced together per pass
+constexpr int MK_RB = 4;   // rows reduced together per pass (CUDA-core path)
 
 // V consecutive floats of the activation vector in shared memory (16-byte aligned).
 template <int V>
@@ -518,10 +597,11 @@ __device__ __forceinline__ void mk_load_xs(const float* p, float* v) {
   }
 }
 
-// Rows [r0, r1) of segment S (relative to S.row0) that warp w reduces: a
-// contiguous block of whole units (a unit is a row, or a row pair for the
-// paired epilogues).  Rows of up to 4 KB are streamed several per stage,
-// longer rows in 4 KB pieces; producer and consumer walk the same plan.
+// Rows [r0, r1) of segment S (relative to S.row0) that warp w reduces on the
+// CUDA-core path: a contiguous block of whole units (a unit is a row, or a
+// row pair for the paired epilogues).  Rows of up to one stage are streamed
+// several per stage, longer rows in stage-sized pieces; producer and consumer
+// walk the same plan.
 __device__ __forceinline__ void mk_warp_rows(const MkRows& R, const MkSeg& S, int w, int& r0, int& r1) {
   const int nrow = R.paired ? 2 : 1;
   const int units = S.rows / nrow;
@@ -531,175 +611,344 @@ __device__ __forceinline__ void mk_warp_rows(const MkRows& R, const MkSeg& S, in
   r1 = u1 * nrow;
 }
 
+// Tensor-core path: segment S is cut into 16-row blocks, taken MK_CHUNK at a
+// time; inside a chunk, tile (b, kb) (local block b, MK_KG-column group kb) is
+// number t = b * KB + kb and belongs to warp t % 8.  The first kb of local
+// block b that warp w owns:
+__device__ __forceinline__ int mk_first_kb(int b, int KB, int w) {
+  return ((w - (b * KB) % MK_COMPUTE_WARPS) % MK_COMPUTE_WARPS + MK_COMPUTE_WARPS) % MK_COMPUTE_WARPS;
+}
+
+// Epilogue of a row pair (rl = even row relative to S.row0): QKV bias, RoPE and
+// the q / K / V stores, or SwiGLU for gate/up.
+template <typename KV>
+__device__ __forceinline__ void mk_epi_pair(const MkParams& P, int ph, const MkLayer& L, const MkSeg& S,
+                                            const MkMisc* M, int rl, float a0, float a1) {
+  const int qd = P.nq * P.hd, kd = P.nkv * P.hd;
+  if (ph == PH_QKV) {
+    const int row = S.row0 + rl;
+    float v0 = a0, v1 = a1;
+    if (L.bqkv) {
+      v0 += L.bqkv[row];
+      v1 += L.bqkv[row + 1];
+    }
+    if (row < qd + kd) {
+      const int d = (row < qd ? row : row - qd) % P.hd;
+      const float2 cs = M->cs[d >> 1];
+      const float b0 = v0 * cs.x - v1 * cs.y, b1 = v0 * cs.y + v1 * cs.x;
+      v0 = b0;
+      v1 = b1;
+    }
+    const int slot = P.sliding > 0 ? P.pos % P.max_seq : P.pos;
+    if (row < qd) {
+      P.q[row] = v0;
+      P.q[row + 1] = v1;
+    } else {
+      const bool is_k = row < qd + kd;
+      KV* dst = (KV*)(is_k ? L.kc : L.vc);
+      const size_t o = (size_t)slot * kd + (is_k ? row - qd : row - qd - kd);
+      dst[o] = from_f32<KV>(v0);
+      dst[o + 1] = from_f32<KV>(v1);
+    }
+  } else {  // PH_GATEUP: act[task] = silu(gate) * up
+    const int task = P.E > 0 ? S.out0 + (rl >> 1) : (S.row0 + rl) >> 1;
+    P.act[task] = silu_f(a0) * a1;
+  }
+}
+
+// Epilogue of a single row: logits (+ running argmax), the MoE down row sum
+// over the selected experts, or the residual increment of O / down.
+__device__ __forceinline__ void mk_epi_row(const MkParams& P, int ph, const MkSeg& S, MkMisc* M, int rl, float a,
+                                           float& bst, int& bix) {
+  const int row = S.row0 + rl;
+  if (ph == PH_LMHEAD) {
+    if (P.logits) P.logits[row] = a;
+    if (a > bst || (a == bst && row < bix)) {
+      bst = a;
+      bix = row;
+    }
+  } else if (ph == PH_DOWN && P.E > 0) {
+    float& acc = M->acc[rl];
+    acc = S.slot == 0 ? M->wts[0] * a : fmaf(M->wts[S.slot], a, acc);
+  } else {  // PH_OPROJ, dense PH_DOWN: added to the residual row after the phase
+    M->acc[rl] = a;
+  }
+}
+
+// Four 8x8 b16 matrices from shared memory (lane l gives row l % 8 of matrix l / 8).
+__device__ __forceinline__ void mk_ldsm4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// d (16x8 f32) += a (16x16 bf16, row) . b (16x8 bf16, col).
+__device__ __forceinline__ void mk_mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                            uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Barrier 1 over the compute threads; returns whether any of them passed
+// `pred`, so that every compute warp takes the same way out of a phase.
+__device__ __forceinline__ bool compute_sync_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "n"(MK_COMPUTE)
+      : "memory");
+  return r != 0;
+}
+
+// The activation vector as bf16 (hi, lo) planes, zero-padded to whole column
+// groups.  A global source (the FFN activation, K a multiple of 4) is read
+// as float4, four loads in flight per thread.
+__device__ void mk_to_xb(const float* src, bool src_global, int K, __nv_bfloat16* xb, int plane) {
+  const int KP = (K + MK_KG - 1) / MK_KG * MK_KG;
+  if (src_global) {
+    const int nv = K >> 2, np = KP >> 2;
+    for (int i0 = threadIdx.x; i0 < np; i0 += 4 * MK_COMPUTE) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * MK_COMPUTE;
+        v[u] = i < nv ? __ldcg(reinterpret_cast<const float4*>(src) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * MK_COMPUTE;
+        if (i < np) {
+          mk_put_xb(xb, plane, 4 * i, v[u].x);
+          mk_put_xb(xb, plane, 4 * i + 1, v[u].y);
+          mk_put_xb(xb, plane, 4 * i + 2, v[u].z);
+          mk_put_xb(xb, plane, 4 * i + 3, v[u].w);
+        }
+      }
+    }
+  } else {
+    for (int k = threadIdx.x; k < KP; k += MK_COMPUTE) mk_put_xb(xb, plane, k, k < K ? src[k] : 0.f);
+  }
+  compute_sync();
+}
+
+// One GEMV phase on the compute side.  Every compute warp runs the same loop
+// structure whatever happens to its waits (a warp whose wait gave up skips
+// work, not loops), so all of them meet at every compute_sync.
 template <typename W, typename KV>
 __device__ bool mk_gemv_phase(const MkParams& P, int ph, int l, const MkRows& R, uint8_t* ring, MkMisc* M,
                               float* xs, uint32_t& sc, float& best, int& bidx) {
-  constexpr int V = Chunk<W>::N;
+  constexpr int NS = MkRing<W>::STAGES, SB = MkRing<W>::BYTES;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const MkLayer& L = P.layers[l < P.n_layers ? l : 0];
-  const int qd = P.nq * P.hd, kd = P.nkv * P.hd;
   volatile int* abort_flag = &M->abort_flag;
-  uint8_t* wring = ring + (size_t)warp * MK_STAGES * MK_STAGE_BYTES;
-  const int cpr = R.rowbytes / 16;   // 16-byte chunks per row
+  uint8_t* wring = ring + (size_t)warp * MK_WARP_RING;
   // Hot-loop state in registers (the by-reference arguments are written back
   // at the end).
   uint32_t scl = sc;
   float bst = best;
   int bix = bidx;
   DeviceState* const stp = P.st;
-  float* const logits = P.logits;
   bool ok = true;
-  for (int si = 0; si < R.nseg; ++si) {
-    const MkSeg S = R.seg[si];   // by value: its fields stay in registers
-    if (ph == PH_DOWN && P.E > 0) {
-      // Expert slot S.slot multiplies its own activation vector.
-      compute_sync();
-      mk_copy_to_xs(P.act + (size_t)S.slot * P.f, P.f, xs);
-    }
-    int r0, r1;
-    mk_warp_rows(R, S, warp, r0, r1);
-    float pend = 0.f;   // sum of the even row of a pair in progress
-    // Epilogue of row rl (relative to S.row0) once its sum is known (lane 0).
-    auto finish = [&](int rl, float sum) {
-      if (R.paired) {
-        if ((rl & 1) == 0) {
-          pend = sum;
-          return;
-        }
-        if (lane != 0) return;
-        const float a0 = pend, a1 = sum;
-        if (ph == PH_QKV) {
-          const int row = S.row0 + rl - 1;
-          float v0 = a0, v1 = a1;
-          if (L.bqkv) {
-            v0 += L.bqkv[row];
-            v1 += L.bqkv[row + 1];
-          }
-          if (row < qd + kd) {
-            const int d = (row < qd ? row : row - qd) % P.hd;
-            const float2 cs = M->cs[d >> 1];
-            const float b0 = v0 * cs.x - v1 * cs.y, b1 = v0 * cs.y + v1 * cs.x;
-            v0 = b0;
-            v1 = b1;
-          }
-          const int slot = P.sliding > 0 ? P.pos % P.max_seq : P.pos;
-          if (row < qd) {
-            P.q[row] = v0;
-            P.q[row + 1] = v1;
-          } else {
-            const bool is_k = row < qd + kd;
-            KV* dst = (KV*)(is_k ? L.kc : L.vc);
-            const size_t o = (size_t)slot * kd + (is_k ? row - qd : row - qd - kd);
-            dst[o] = from_f32<KV>(v0);
-            dst[o + 1] = from_f32<KV>(v1);
-          }
-        } else {  // PH_GATEUP: act[task] = silu(gate) * up
-          const int task = P.E > 0 ? S.out0 + ((rl - 1) >> 1) : (S.row0 + rl - 1) >> 1;
-          P.act[task] = silu_f(a0) * a1;
-        }
-      } else {
-        if (lane != 0) return;
-        const float a = sum;
-        const int row = S.row0 + rl;
-        if (ph == PH_LMHEAD) {
-          if (logits) logits[row] = a;
-          if (a > bst || (a == bst && row < bix)) {
-            bst = a;
-            bix = row;
-          }
-        } else if (ph == PH_DOWN && P.E > 0) {
-          float& acc = M->acc[rl];
-          acc = S.slot == 0 ? M->wts[0] * a : fmaf(M->wts[S.slot], a, acc);
-        } else {  // PH_OPROJ, dense PH_DOWN: added to the residual row after the phase
-          M->acc[rl] = a;
-        }
+  auto next_stage = [&]() -> const uint8_t* {
+    const int st = scl % NS;
+    const uint32_t par = (scl / NS) & 1u;
+    if (!mk_mbar_wait(&M->full[warp][st], par, abort_flag, stp, 201)) return nullptr;
+    return wring + (size_t)st * SB;
+  };
+  auto release_stage = [&]() {
+    __syncwarp();
+    const int st = scl % NS;
+    if (lane == 0) mk_mbar_arrive(&M->empty[warp][st]);
+    ++scl;
+    if (lane == 0) M->consumed[warp] = (int)scl;
+  };
+  if constexpr (!MkRing<W>::MMA) {
+    // ---------------- CUDA-core path (f32 weights)
+    constexpr int V = Chunk<W>::N;
+    const int cpr = R.rowbytes / 16;   // 16-byte chunks per row
+    for (int si = 0; si < R.nseg; ++si) {
+      const MkSeg S = R.seg[si];   // by value: its fields stay in registers
+      if (ph == PH_DOWN && P.E > 0) {
+        // Expert slot S.slot multiplies its own activation vector.
+        compute_sync();
+        mk_copy_to_xs(P.act + (size_t)S.slot * P.f, P.f, xs);
       }
-    };
-    auto next_stage = [&]() -> const uint8_t* {
-      const int st = scl % MK_STAGES;
-      const uint32_t par = (scl / MK_STAGES) & 1u;
-      if (!mk_mbar_wait(&M->full[warp][st], par, abort_flag, stp, 201)) return nullptr;
-      return wring + (size_t)st * MK_STAGE_BYTES;
-    };
-    auto release_stage = [&]() {
-      __syncwarp();
-      const int st = scl % MK_STAGES;
-      if (lane == 0) mk_mbar_arrive(&M->empty[warp][st]);
-      ++scl;
-      if (lane == 0) M->consumed[warp] = (int)scl;
-    };
-    if (R.rowbytes <= MK_STAGE_BYTES) {
-      // Up to MK_RB rows of a stage per pass: each xs chunk is read once for
-      // all of them, and their FMA chains and shuffle reductions interleave.
-      const int rps = MK_STAGE_BYTES / R.rowbytes;
-      for (int r = r0; r < r1 && ok; r += rps) {
-        const int n = min(rps, r1 - r);
-        const uint8_t* piece = next_stage();
-        if (!piece) {
-          ok = false;
-          break;
-        }
-        for (int j0 = 0; j0 < n; j0 += MK_RB) {
-          const int nj = min(MK_RB, n - j0);
-          const uint8_t* rows = piece + (size_t)j0 * R.rowbytes;
-          float acc[MK_RB];
-#pragma unroll
-          for (int j = 0; j < MK_RB; ++j) acc[j] = 0.f;
-          for (int c = lane; c < cpr; c += 32) {
-            float xv[V];
-            mk_load_xs<V>(xs + c * V, xv);
-#pragma unroll
-            for (int j = 0; j < MK_RB; ++j) {
-              if (j < nj) {
-                float wv[V];
-                Chunk<W>::widen(*reinterpret_cast<const uint4*>(rows + (size_t)j * R.rowbytes + (size_t)c * 16), wv);
-#pragma unroll
-                for (int e = 0; e < V; ++e) acc[j] = fmaf(wv[e], xv[e], acc[j]);
-              }
-            }
+      int r0, r1;
+      mk_warp_rows(R, S, warp, r0, r1);
+      float pend = 0.f;   // sum of the even row of a pair in progress
+      auto finish = [&](int rl, float sum) {
+        if (R.paired) {
+          if ((rl & 1) == 0) {
+            pend = sum;
+            return;
           }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int j = 0; j < MK_RB; ++j) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
-          for (int j = 0; j < nj; ++j) finish(r + j0 + j, acc[j]);
+          if (lane == 0) mk_epi_pair<KV>(P, ph, L, S, M, rl - 1, pend, sum);
+        } else if (lane == 0) {
+          mk_epi_row(P, ph, S, M, rl, sum, bst, bix);
         }
-        release_stage();
-      }
-    } else {
-      for (int r = r0; r < r1 && ok; ++r) {
-        float acc0 = 0.f, acc1 = 0.f;
-        for (int off = 0; off < R.rowbytes; off += MK_STAGE_BYTES) {
-          const int len = min(MK_STAGE_BYTES, R.rowbytes - off);
+      };
+      if (R.rowbytes <= SB) {
+        // Up to MK_RB rows of a stage per pass: each xs chunk is read once for
+        // all of them, and their FMA chains and shuffle reductions interleave.
+        const int rps = SB / R.rowbytes;
+        for (int r = r0; r < r1 && ok; r += rps) {
+          const int n = min(rps, r1 - r);
           const uint8_t* piece = next_stage();
           if (!piece) {
             ok = false;
             break;
           }
-          const int c0 = off / 16, nc = len / 16;
-          int c = lane;
-          for (; c + 32 < nc; c += 64) {
-            float w0[V], w1[V], x0[V], x1[V];
-            Chunk<W>::widen(*reinterpret_cast<const uint4*>(piece + (size_t)c * 16), w0);
-            Chunk<W>::widen(*reinterpret_cast<const uint4*>(piece + (size_t)(c + 32) * 16), w1);
-            mk_load_xs<V>(xs + (c0 + c) * V, x0);
-            mk_load_xs<V>(xs + (c0 + c + 32) * V, x1);
+          for (int j0 = 0; j0 < n; j0 += MK_RB) {
+            const int nj = min(MK_RB, n - j0);
+            const uint8_t* rows = piece + (size_t)j0 * R.rowbytes;
+            float acc[MK_RB];
 #pragma unroll
-            for (int e = 0; e < V; ++e) {
-              acc0 = fmaf(w0[e], x0[e], acc0);
-              acc1 = fmaf(w1[e], x1[e], acc1);
+            for (int j = 0; j < MK_RB; ++j) acc[j] = 0.f;
+            for (int c = lane; c < cpr; c += 32) {
+              float xv[V];
+              mk_load_xs<V>(xs + c * V, xv);
+#pragma unroll
+              for (int j = 0; j < MK_RB; ++j) {
+                if (j < nj) {
+                  float wv[V];
+                  Chunk<W>::widen(*reinterpret_cast<const uint4*>(rows + (size_t)j * R.rowbytes + (size_t)c * 16), wv);
+#pragma unroll
+                  for (int e = 0; e < V; ++e) acc[j] = fmaf(wv[e], xv[e], acc[j]);
+                }
+              }
             }
-          }
-          if (c < nc) {
-            float w0[V], x0[V];
-            Chunk<W>::widen(*reinterpret_cast<const uint4*>(piece + (size_t)c * 16), w0);
-            mk_load_xs<V>(xs + (c0 + c) * V, x0);
 #pragma unroll
-            for (int e = 0; e < V; ++e) acc0 = fmaf(w0[e], x0[e], acc0);
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+              for (int j = 0; j < MK_RB; ++j) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
+            for (int j = 0; j < nj; ++j) finish(r + j0 + j, acc[j]);
           }
           release_stage();
         }
-        if (ok) finish(r, warp_sum(acc0 + acc1));
+      } else {
+        for (int r = r0; r < r1 && ok; ++r) {
+          float acc0 = 0.f, acc1 = 0.f;
+          for (int off = 0; off < R.rowbytes; off += SB) {
+            const int len = min(SB, R.rowbytes - off);
+            const uint8_t* piece = next_stage();
+            if (!piece) {
+              ok = false;
+              break;
+            }
+            const int c0 = off / 16, nc = len / 16;
+            int c = lane;
+            for (; c + 32 < nc; c += 64) {
+              float w0[V], w1[V], x0[V], x1[V];
+              Chunk<W>::widen(*reinterpret_cast<const uint4*>(piece + (size_t)c * 16), w0);
+              Chunk<W>::widen(*reinterpret_cast<const uint4*>(piece + (size_t)(c + 32) * 16), w1);
+              mk_load_xs<V>(xs + (c0 + c) * V, x0);
+              mk_load_xs<V>(xs + (c0 + c + 32) * V, x1);
+#pragma unroll
+              for (int e = 0; e < V; ++e) {
+                acc0 = fmaf(w0[e], x0[e], acc0);
+                acc1 = fmaf(w1[e], x1[e], acc1);
+              }
+            }
+            if (c < nc) {
+              float w0[V], x0[V];
+              Chunk<W>::widen(*reinterpret_cast<const uint4*>(piece + (size_t)c * 16), w0);
+              mk_load_xs<V>(xs + (c0 + c) * V, x0);
+#pragma unroll
+              for (int e = 0; e < V; ++e) acc0 = fmaf(w0[e], x0[e], acc0);
+            }
+            release_stage();
+          }
+          if (ok) finish(r, warp_sum(acc0 + acc1));
+        }
+      }
+    }
+  } else {
+    // ---------------- tensor-core path (bf16 weights)
+    // A = a 16 x 64 weight tile from the ring (128-byte swizzled by TMA), via
+    // ldmatrix; B = the activation's (hi, lo) bf16 planes as columns 0 and 1
+    // of the 16 x 8 operand (lanes of groups 0 and 1 carry them, the others
+    // zeros); row r's dot product is D[r][0] + D[r][1], f32-accumulated.
+    const int KB = (R.K + MK_KG - 1) / MK_KG;   // column groups (stages) per row block
+    const int grp = lane >> 2, t4 = lane & 3;
+    __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(xs + P.xs_floats);
+    const __nv_bfloat16* xbl = xb + (grp & 1) * P.xb_plane;   // plane of lane groups 0 / 1
+    const bool bl = grp < 2;
+    // ldmatrix.x4 lane roles: matrix q = lane / 8 covers rows (q & 1) * 8 + lane % 8
+    // and 16-byte column chunk (q >> 1) of each 16-column step.
+    const int lrow = ((lane >> 3) & 1) * 8 + (lane & 7), lch = lane >> 4;
+    for (int si = 0; si < R.nseg; ++si) {
+      const MkSeg S = R.seg[si];   // by value: its fields stay in registers
+      if (ph == PH_DOWN) {
+        // The activation this segment multiplies (MoE: its expert slot's).
+        compute_sync();
+        mk_to_xb(P.act + (size_t)(P.E > 0 ? S.slot : 0) * P.f, true, P.f, xb, P.xb_plane);
+      }
+      const int nblk = (S.rows + MK_TM - 1) / MK_TM;
+      for (int c0 = 0; c0 < nblk; c0 += MK_CHUNK) {
+        const int nbc = min(MK_CHUNK, nblk - c0);
+        for (int b = 0; b < nbc; ++b) {
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int kb = mk_first_kb(b, KB, warp); kb < KB && ok; kb += MK_COMPUTE_WARPS) {
+            const uint8_t* tile = next_stage();
+            if (!tile) {
+              ok = false;
+              break;
+            }
+#pragma unroll
+            for (int j = 0; j < MK_BPS; ++j) {
+              const uint32_t base = mk_smem_u32(tile) + 2048u * j;
+              const uint32_t rsw = ((base >> 7) + (uint32_t)lrow) & 7u;   // swizzle phase of this lane's row
+#pragma unroll
+              for (int ks = 0; ks < MK_TK / 16; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                mk_ldsm4(base + (uint32_t)lrow * 128u + (((uint32_t)(2 * ks + lch) ^ rsw) << 4), a0, a1, a2, a3);
+                const int k0 = (kb * MK_BPS + j) * MK_TK + ks * 16 + 2 * t4;
+                const uint32_t b0 = bl ? *reinterpret_cast<const uint32_t*>(xbl + k0) : 0u;
+                const uint32_t b1 = bl ? *reinterpret_cast<const uint32_t*>(xbl + k0 + 8) : 0u;
+                mk_mma_bf16(d, a0, a1, a2, a3, b0, b1);
+              }
+            }
+            release_stage();
+          }
+          if (t4 == 0) {
+            M->part[b][warp][grp] = d[0] + d[1];
+            M->part[b][warp][grp + 8] = d[2] + d[3];
+          }
+        }
+        compute_sync();
+        // Rows of the chunk: the 8 warps' partials summed in warp order.
+        if (R.paired) {
+          for (int i = threadIdx.x; i < nbc * (MK_TM / 2); i += MK_COMPUTE) {
+            const int b = i / (MK_TM / 2), pr = 2 * (i % (MK_TM / 2));
+            const int rl = (c0 + b) * MK_TM + pr;
+            if (rl >= S.rows) continue;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int w = 0; w < MK_COMPUTE_WARPS; ++w) {
+              a0 += M->part[b][w][pr];
+              a1 += M->part[b][w][pr + 1];
+            }
+            mk_epi_pair<KV>(P, ph, L, S, M, rl, a0, a1);
+          }
+        } else {
+          for (int i = threadIdx.x; i < nbc * MK_TM; i += MK_COMPUTE) {
+            const int b = i / MK_TM, r = i % MK_TM;
+            const int rl = (c0 + b) * MK_TM + r;
+            if (rl >= S.rows) continue;
+            float a = 0.f;
+#pragma unroll
+            for (int w = 0; w < MK_COMPUTE_WARPS; ++w) a += M->part[b][w][r];
+            mk_epi_row(P, ph, S, M, rl, a, bst, bix);
+          }
+        }
+        compute_sync();
       }
     }
   }
@@ -837,21 +1086,23 @@ __device__ void mk_attention(const MkParams& P, int l, uint8_t* ureg, MkMisc* M)
 
 namespace dec {
 
-// L2 prefetch of the K/V rows this CTA's attention tasks of layer l will read
-// (issued one phase early; the current position's row is rewritten in L2 by
-// the QKV phase before the attention phase reads it).
-__device__ void mk_prefetch_attention_kv(const MkParams& P, int l, int HD) {
+// L2 prefetch of the K/V rows this CTA's attention tasks of layer l will read,
+// shared among the `nparts` producer lanes (part `part`).  The producers reach
+// the attention phase while the QKV weights are still streaming, so the
+// prefetch runs ahead of the attention phase off the compute path (the current
+// position's row, rewritten by the QKV phase, is updated in L2 by that write).
+__device__ void mk_prefetch_attention_kv(const MkParams& P, int l, int HD, int part, int nparts) {
   const MkLayer& L = P.layers[l];
   const int kvb = P.kv_bytes;
   const int kd = P.nkv * HD;
   const int m = P.sliding > 0 ? min(P.pos + 1, P.max_seq) : P.pos + 1;
   const int tasks = P.nkv * P.nsplit;
-  int idx = threadIdx.x;
+  int idx = part;
   for (int t = blockIdx.x; t < tasks; t += P.nb) {
     const int g = t / P.nsplit, split = t - g * P.nsplit;
     const int s0 = split * P.sps, j1 = min(min(s0 + P.sps, P.max_seq), m);
     const int n = j1 > s0 ? j1 - s0 : 0;
-    for (; idx < 2 * n; idx += MK_COMPUTE) {
+    for (; idx < 2 * n; idx += nparts) {
       const int r = idx >> 1;
       const uint8_t* base = (const uint8_t*)((idx & 1) ? L.vc : L.kc);
       mk_prefetch_l2(base + ((size_t)(s0 + r) * kd + (size_t)g * HD) * kvb, (uint32_t)(HD * kvb));
@@ -873,10 +1124,17 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_step(const __grid_cons
   uint8_t* ureg = mk_smem + MK_RING_BYTES;
   MkMisc* M = reinterpret_cast<MkMisc*>(ureg + P.u_bytes);
   const int tid = threadIdx.x;
+  // Swizzled TMA tiles and their ldmatrix addressing assume a 1024-byte
+  // aligned window; every CTA of the launch has the same window, so this exit
+  // is uniform (also across a cluster).
+  if (mk_smem_u32(mk_smem) & 1023u) {
+    if (tid == 0) raise_error(P.st, ERR_LAYOUT, 130);
+    return;
+  }
 
   if (tid == 0) {
     for (int w = 0; w < MK_COMPUTE_WARPS; ++w)
-      for (int s = 0; s < MK_STAGES; ++s) {
+      for (int s = 0; s < MkRing<W>::STAGES; ++s) {
         mk_mbar_init(&M->full[w][s], 1);
         mk_mbar_init(&M->empty[w][s], 1);
       }
@@ -920,14 +1178,24 @@ __device__ void mk_produce(const MkParams& P, uint8_t* ring, MkMisc* M) {
   volatile int* abort_flag = &M->abort_flag;
   {
     // ---------------- producer: warp 8+w streams compute warp w's rows of every phase, in order
+    constexpr int NS = MkRing<W>::STAGES, SB = MkRing<W>::BYTES;
     const int w = warp - MK_COMPUTE_WARPS;
     if ((tid & 31) == 0) {
-      uint8_t* wring = ring + (size_t)w * MK_STAGES * MK_STAGE_BYTES;
+      uint8_t* wring = ring + (size_t)w * MK_WARP_RING;
       uint32_t sc = 0;
       bool ok = true;
+      auto claim = [&](uint32_t len) -> int {   // next stage, armed for len bytes; -1 if gave up
+        const int st = sc % NS;
+        const uint32_t par = (sc / NS) & 1u;
+        if (!mk_mbar_wait(&M->empty[w][st], par ^ 1u, abort_flag, P.st, 302)) return -1;
+        mk_mbar_expect_tx(&M->full[w][st], len);
+        ++sc;
+        return st;
+      };
       for (int i = 0; i < nphase && ok && !*abort_flag; ++i) {
         int ph, l;
         mk_phase_at(P, i, ph, l);
+        if (ph == PH_ATTN) mk_prefetch_attention_kv(P, l, P.hd, w, MK_COMPUTE_WARPS);
         if (!mk_is_gemv(ph)) continue;
         if (P.E > 0 && (ph == PH_GATEUP || ph == PH_DOWN)) {
           // Expert rows are known once this layer's router has run.
@@ -944,26 +1212,42 @@ __device__ void mk_produce(const MkParams& P, uint8_t* ring, MkMisc* M) {
         mk_phase_rows<W>(P, ph, l, M->ids, R);
         for (int si = 0; si < R.nseg && ok; ++si) {
           const MkSeg S = R.seg[si];   // by value: its fields stay in registers
-          int r0, r1;
-          mk_warp_rows(R, S, w, r0, r1);
-          const uint8_t* base = S.base + (size_t)S.row0 * R.rowbytes;
-          auto issue = [&](const uint8_t* src, int len) -> bool {
-            const int st = sc % MK_STAGES;
-            const uint32_t par = (sc / MK_STAGES) & 1u;
-            if (!mk_mbar_wait(&M->empty[w][st], par ^ 1u, abort_flag, P.st, 302)) return false;
-            mk_mbar_expect_tx(&M->full[w][st], (uint32_t)len);
-            mk_bulk_load(wring + (size_t)st * MK_STAGE_BYTES, src, (uint32_t)len, &M->full[w][st]);
-            ++sc;
-            return true;
-          };
-          if (R.rowbytes <= MK_STAGE_BYTES) {
-            const int rps = MK_STAGE_BYTES / R.rowbytes;
-            for (int r = r0; r < r1 && ok; r += rps)
-              ok = issue(base + (size_t)r * R.rowbytes, min(rps, r1 - r) * R.rowbytes);
+          if constexpr (MkRing<W>::MMA) {
+            // 16 x 64 tiles in the consumer's order: block by block, this
+            // warp's column blocks of each (see mk_first_kb).
+            const CUtensorMap* map = P.maps + S.map;
+            const int KB = (R.K + MK_KG - 1) / MK_KG;
+            const int nblk = (S.rows + MK_TM - 1) / MK_TM;
+            for (int blk = 0; blk < nblk && ok; ++blk)
+              for (int kb = mk_first_kb(blk % MK_CHUNK, KB, w); kb < KB && ok; kb += MK_COMPUTE_WARPS) {
+                const int st = claim((uint32_t)SB);
+                if (st < 0) {
+                  ok = false;
+                  break;
+                }
+                for (int j = 0; j < MK_BPS; ++j)
+                  tma_load_2d(wring + (size_t)st * SB + 2048 * j, map, &M->full[w][st], (kb * MK_BPS + j) * MK_TK,
+                              S.maprow + blk * MK_TM);
+              }
           } else {
-            for (int r = r0; r < r1 && ok; ++r)
-              for (int off = 0; off < R.rowbytes && ok; off += MK_STAGE_BYTES)
-                ok = issue(base + (size_t)r * R.rowbytes + off, min(MK_STAGE_BYTES, R.rowbytes - off));
+            int r0, r1;
+            mk_warp_rows(R, S, w, r0, r1);
+            const uint8_t* base = S.base + (size_t)S.row0 * R.rowbytes;
+            auto issue = [&](const uint8_t* src, int len) -> bool {
+              const int st = claim((uint32_t)len);
+              if (st < 0) return false;
+              mk_bulk_load(wring + (size_t)st * SB, src, (uint32_t)len, &M->full[w][st]);
+              return true;
+            };
+            if (R.rowbytes <= SB) {
+              const int rps = SB / R.rowbytes;
+              for (int r = r0; r < r1 && ok; r += rps)
+                ok = issue(base + (size_t)r * R.rowbytes, min(rps, r1 - r) * R.rowbytes);
+            } else {
+              for (int r = r0; r < r1 && ok; ++r)
+                for (int off = 0; off < R.rowbytes && ok; off += SB)
+                  ok = issue(base + (size_t)r * R.rowbytes + off, min(SB, R.rowbytes - off));
+            }
           }
         }
       }
@@ -971,8 +1255,7 @@ __device__ void mk_produce(const MkParams& P, uint8_t* ring, MkMisc* M) {
         // Copies issued but never consumed must land before the CTA exits.
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t k = (uint32_t)*(volatile int*)&M->consumed[w]; k < sc; ++k)
-          while (!mk_mbar_try(&M->full[w][k % MK_STAGES], (k / MK_STAGES) & 1u) &&
-                 globaltimer_ns() - t0 < 100000000ull) {
+          while (!mk_mbar_try(&M->full[w][k % NS], (k / NS) & 1u) && globaltimer_ns() - t0 < 100000000ull) {
           }
       }
     }
@@ -985,6 +1268,10 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
   const int nphase = P.n_layers * mk_phases_per_layer(P) + 1;
   volatile int* abort_flag = &M->abort_flag;
   float* xs = reinterpret_cast<float*>(ureg);
+  // Tensor-core GEMV operand: the activation as bf16 (hi, lo) planes after xs.
+  constexpr bool MMA = MkRing<W>::MMA;
+  __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(xs + P.xs_floats);
+  const int kpad_h = (P.h + MK_KG - 1) / MK_KG * MK_KG;
   // ---------------- compute warps
   if (P.stamps && blockIdx.x == 0 && tid == 0) P.stamps[0] = globaltimer_ns();
   const int token = M->token;
@@ -1002,9 +1289,8 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
     bool ok = true;
     switch (ph) {
       case PH_QKV:
-        mk_prefetch_attention_kv(P, l, P.hd);
         mk_norm_to_xs<W>(P.x, l == 0 ? (const W*)P.embed + (size_t)token * P.h : nullptr, L.attn_norm, P.h, P.eps,
-                         xs, M);
+                         xs, M, MMA ? xb : nullptr, P.xb_plane, kpad_h);
         break;
       case PH_ATTN:
         mk_attention<KV, HD>(P, l, ureg, M);
@@ -1016,16 +1302,18 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
       case PH_OPROJ:
         if (P.nsplit > 1 && !P.merge_phase) mk_merge_heads(P.part, P.nsplit, HD, 0, P.nq, xs + qd, xs, false);
         else mk_copy_to_xs(P.attn, qd, xs);
+        if (MMA) mk_to_xb(xs, false, qd, xb, P.xb_plane);
         break;
       case PH_GATEUP:
-        mk_norm_to_xs<W>(P.x, nullptr, L.ffn_norm, P.h, P.eps, xs, M);
+        mk_norm_to_xs<W>(P.x, nullptr, L.ffn_norm, P.h, P.eps, xs, M, MMA ? xb : nullptr, P.xb_plane, kpad_h);
         if (P.E > 0) mk_router<W>(P, l, xs, M);
         break;
       case PH_DOWN:
-        if (P.E == 0) mk_copy_to_xs(P.act, P.f, xs);
+        // (tensor-core path: the activation is converted per segment)
+        if (!MMA && P.E == 0) mk_copy_to_xs(P.act, P.f, xs);
         break;
       case PH_LMHEAD:
-        mk_norm_to_xs<W>(P.x, nullptr, P.out_norm, P.h, P.eps, xs, M);
+        mk_norm_to_xs<W>(P.x, nullptr, P.out_norm, P.h, P.eps, xs, M, MMA ? xb : nullptr, P.xb_plane, kpad_h);
         break;
     }
     if (mk_is_gemv(ph)) {
@@ -1033,15 +1321,17 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
       mk_phase_rows<W>(P, ph, l, M->ids, R);
       ok = mk_gemv_phase<W, KV>(P, ph, l, R, ring, M, xs, sc, best, bidx);
     }
-    if (!ok || *abort_flag) break;
+    // Every exit below is agreed by all compute threads (a thread that left
+    // alone would leave the others at the next compute barrier).
+    if (compute_sync_or(!ok || *abort_flag)) break;
     if (ph != PH_LMHEAD) {
       const bool synced = P.cluster ? mk_cluster_sync(P.st, (unsigned)P.nb, &M->cbar, &M->cgen, abort_flag, 400 + ph)
                                     : mk_grid_sync(P.st, (unsigned)P.nb, abort_flag, 400 + ph);
-      if (!synced) break;
+      if (compute_sync_or(!synced)) break;
     }
     if (P.stamps && blockIdx.x == 0 && tid == 0) P.stamps[i + 1] = globaltimer_ns();
   }
-  if (*abort_flag || !P.d_argmax) return;
+  if (compute_sync_or(*abort_flag) || !P.d_argmax) return;
 
   // ---------------- argmax: CTA best -> per-CTA partial -> last CTA merges
   const int lane = tid & 31;
@@ -1116,13 +1406,32 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
 namespace dec {
 
 // ------------------------------------------------------------------ host side
+// Floats of the f32 activation region xs: the phase inputs (on the tensor-core
+// path only those of length hidden or n_heads*head_dim; the FFN activation goes
+// straight to the bf16 planes) plus the split-merge scratch of the output
+// projection.
+static int mk_xs_floats(const dec_config& c, int nsplit) {
+  size_t xs = (size_t)c.hidden;
+  if ((size_t)c.n_heads * c.head_dim > xs) xs = (size_t)c.n_heads * c.head_dim;
+  if (c.weight_dtype != DEC_BF16 && (size_t)c.ffn > xs) xs = c.ffn;
+  xs += (size_t)c.n_heads * nsplit;
+  return (int)((xs + 3) / 4 * 4);
+}
+
+// Elements of one bf16 activation plane (tensor-core path): the longest row,
+// in whole 64-column blocks.
+static int mk_xb_plane(const dec_config& c) {
+  size_t k = (size_t)c.hidden;
+  if ((size_t)c.n_heads * c.head_dim > k) k = (size_t)c.n_heads * c.head_dim;
+  if ((size_t)c.ffn > k) k = c.ffn;
+  return (int)((k + MK_KG - 1) / MK_KG * MK_KG);
+}
+
 static size_t mk_u_bytes(const dec_config& c, int nsplit) {
   const size_t kvs = c.kv_dtype == DEC_BF16 ? 2 : 4;
   const size_t ce = 16 / kvs, hd = c.head_dim, G = c.n_heads / c.n_kv_heads;
-  size_t xs = (size_t)c.hidden;
-  if ((size_t)c.n_heads * hd > xs) xs = (size_t)c.n_heads * hd;
-  if ((size_t)c.ffn > xs) xs = c.ffn;
-  xs = (xs + (size_t)c.n_heads * nsplit) * sizeof(float);
+  size_t xs = (size_t)mk_xs_floats(c, nsplit) * sizeof(float);
+  if (c.weight_dtype == DEC_BF16) xs += 2 * sizeof(__nv_bfloat16) * (size_t)mk_xb_plane(c);
   const size_t attn = MK_KS * (hd + ce) * kvs + MK_KS * hd * kvs + G * hd * 4 + G * MK_KS * 4;
   const size_t u = xs > attn ? xs : attn;
   return (u + 127) / 128 * 128;
@@ -1130,6 +1439,57 @@ static size_t mk_u_bytes(const dec_config& c, int nsplit) {
 
 size_t mk_smem_bytes(const dec_config& c, int nsplit) {
   return (size_t)MK_RING_BYTES + mk_u_bytes(c, nsplit) + sizeof(MkMisc);
+}
+
+size_t mk_maps_bytes(const dec_config& c) {
+  return c.weight_dtype == DEC_BF16 ? sizeof(CUtensorMap) * ((size_t)c.n_layers * MAPS_PER_LAYER + 1) : 0;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 mk_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A [rows][K] bf16 weight matrix as 16 x 64 tiles with 128-byte swizzling.
+static bool mk_encode(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K) {
+  auto fn = mk_encode_fn();
+  if (!fn || !base) return false;
+  const cuuint64_t dims[2] = {K, rows};
+  const cuuint64_t strides[1] = {K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)MK_TK, (cuuint32_t)MK_TM};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor maps of every bf16 weight matrix the step streams, copied to m.mk_maps.
+static bool mk_build_maps(Model& m) {
+  const dec_config& c = m.cfg;
+  if (c.weight_dtype != DEC_BF16) return true;
+  if (!m.mk_maps) return false;
+  const uint64_t h = c.hidden, qd = (uint64_t)c.n_heads * c.head_dim, kd = (uint64_t)c.n_kv_heads * c.head_dim;
+  const uint64_t f = c.ffn, E = c.n_experts > 0 ? c.n_experts : 1;
+  std::vector<CUtensorMap> maps((size_t)c.n_layers * MAPS_PER_LAYER + 1);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerPtrs& L = m.layers[l];
+    CUtensorMap* t = &maps[(size_t)l * MAPS_PER_LAYER];
+    if (!mk_encode(t + MAP_QKV, L.wqkv, qd + 2 * kd, h) || !mk_encode(t + MAP_O, L.wo, h, qd) ||
+        !mk_encode(t + MAP_GATEUP, L.w_gateup, E * 2 * f, h) || !mk_encode(t + MAP_DOWN, L.w_down, E * h, f))
+      return false;
+  }
+  if (!mk_encode(&maps.back(), m.head, (uint64_t)c.vocab, h)) return false;
+  return cudaMemcpy(m.mk_maps, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice) ==
+         cudaSuccess;
 }
 
 template <typename W, typename KV>
@@ -1155,8 +1515,11 @@ bool mk_prepare(Model& m, int num_sms) {
   m.mk_ok = false;
   m.mk_cluster = 0;
   (void)es;
-  // MoE down keeps one row sum per owned row; RoPE table of up to 64 pairs.
-  if ((c.hidden + num_sms - 1) / num_sms > 256 || c.head_dim / 2 > 64) return false;
+  // MoE down keeps one row sum per owned row (a CTA owns ceil(hidden / CTAs)
+  // rows, in 16-row blocks on the tensor-core path); RoPE table of up to 64 pairs.
+  auto rows_per_cta = [&](int nb) { return ((c.hidden + nb - 1) / nb + 15) / 16 * 16; };
+  if (rows_per_cta(num_sms) > 256 || c.head_dim / 2 > 64) return false;
+  if (!mk_build_maps(m)) return false;
   if (m.nsplit > 1 && m.attn_sps % MK_KS != 0) return false;
   const size_t smem = mk_smem_bytes(c, m.nsplit);
   if (smem > 227 * 1024) return false;
@@ -1173,7 +1536,7 @@ bool mk_prepare(Model& m, int num_sms) {
   // need at most 256 residual rows per CTA.
   m.mk_cluster = 0;
   for (int cs = 16; cs >= 8; cs /= 2) {
-    if ((c.hidden + cs - 1) / cs > 256) break;
+    if (rows_per_cta(cs) > 256) break;
     if (cs > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
       cudaGetLastError();
       continue;
@@ -1246,6 +1609,9 @@ void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, in
   P.u_bytes = (int)mk_u_bytes(c, m.nsplit);
   P.stamps = m.mk_stamps;
   P.kv_bytes = c.kv_dtype == DEC_BF16 ? 2 : 4;
+  P.maps = reinterpret_cast<const CUtensorMap*>(m.mk_maps);
+  P.xs_floats = mk_xs_floats(c, m.nsplit);
+  P.xb_plane = mk_xb_plane(c);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(P.nb);
   cfg.blockDim = dim3(MK_THREADS);

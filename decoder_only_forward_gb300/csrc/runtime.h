@@ -117,6 +117,7 @@ struct Model {
   int mk_nb;            // its grid (one CTA per SM)
   bool mk_ok;           // the persistent kernel fits this configuration
   int mk_cluster;       // CTAs of its one-cluster schedule (0: the GPU cannot place such a cluster)
+  void* mk_maps;        // its weight tensor maps (bf16 weights; device, in the workspace)
   unsigned long long* mk_stamps;  // nullable phase timestamps (dec_phase_stamps)
   int lm_grid;          // CTAs of the LM head kernel
   int32_t* trace_ids;   // nullable
@@ -133,6 +134,7 @@ struct WsPlan {
   size_t at_Kb, at_Vt;
   int at_kcap, at_vt_ld;  // 0: no tensor-core prefill attention for this configuration
   size_t mk_layers;     // layer table of the persistent decode kernel
+  size_t mk_maps;       // its weight tensor maps
   size_t kv;            // start of the KV rings
   size_t kv_layer_bytes;
   size_t total;
@@ -173,6 +175,7 @@ const void* set_step_kernel();
 
 // Persistent single-kernel decode step (decode_mk.cu).
 size_t mk_smem_bytes(const dec_config& c, int nsplit);
+size_t mk_maps_bytes(const dec_config& c);
 bool mk_prepare(Model& m, int num_sms);
 // cluster: run on one thread-block cluster of m.mk_cluster CTAs, else over m.mk_nb CTAs (one per SM).
 void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, int32_t token, int32_t pos,

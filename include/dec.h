@@ -178,8 +178,8 @@ typedef enum dec_schedule {
 
 /* Selects the decode step schedule.  A schedule the configuration or GPU cannot
  * take (see dec_fused_available) falls back to DEC_FUSED_OFF at each step.
- * dec_create picks DEC_FUSED_GRID when the weights read per token exceed 4 GB
- * (bandwidth-bound), else DEC_FUSED_OFF (latency-bound).  Results agree to
+ * dec_create picks DEC_FUSED_GRID when the weights read per token reach
+ * 512 MB, else DEC_FUSED_OFF (small models: latency-bound).  Results agree to
  * rounding.  DEC_EINVAL for an unknown mode. */
 dec_status dec_set_fused(dec_handle *h, int32_t mode);
 
