@@ -98,6 +98,7 @@ struct MkParams {
   const CUtensorMap* maps;        // bf16 weights: [n_layers * MAPS_PER_LAYER + 1] (global memory)
   int xb_plane;                   // bf16 weights: elements per plane of the (hi, lo) activation copy
   int xs_floats;                  // floats of the f32 activation vector region
+  int attn_warp;                  // attention as per-warp tasks fed by the producer rings
 };
 
 // Shared-memory bookkeeping after the weight ring and the union region.
@@ -971,6 +972,297 @@ __device__ bool mk_gemv_phase(const MkParams& P, int ph, int l, const MkRows& R,
 
 namespace dec {
 
+// ------------------------------------------------------------------ attention phase, warp tasks
+// Task t = (kv head g, split) belongs to warp (t / nb) % 8 of CTA t % nb.  That
+// warp's producer streams the task's K and V rows (one head's row = HD
+// elements) through the warp's weight ring, RPP keys per stage: K piece, then
+// V piece.  The row of the current position is rewritten by this step's QKV
+// phase, possibly after its producer copied it: the consumer reads that row
+// from global memory (through L2).  Used for head_dim 64/128 and at most 8
+// query heads per kv head; partials have the same layout as the CTA tasks'.
+template <typename W, typename KV, int HD>
+struct MkAttnGeom {
+  static constexpr int SB = MkRing<W>::BYTES;
+  static constexpr int RB = HD * (int)sizeof(KV);   // bytes of one head's K or V row
+  static constexpr int RPP = SB / RB;                // keys per piece (stage)
+};
+
+__device__ __forceinline__ void mk_attn_task(const MkParams& P, int t, int m, int& g, int& split, int& s0, int& j1) {
+  g = t / P.nsplit;
+  split = t - g * P.nsplit;
+  s0 = split * P.sps;
+  j1 = min(min(s0 + P.sps, P.max_seq), m);
+}
+
+// A CTA's attention tasks t = blockIdx.x + i * nb (i < per = ceil(tasks / nb),
+// the same for every CTA) are each cut into S slices of their key range, S the
+// largest power of two <= 8 with per * S <= 8 (at least 1): sub-task j = i * S + k
+// runs on warp j % 8 in round j / 8 and takes slice k.  The S softmax states of a
+// task are combined in shared memory at the end of its round.
+__device__ __forceinline__ int mk_attn_ways(const MkParams& P) {
+  const int per = (P.nkv * P.nsplit + P.nb - 1) / P.nb;
+  int S = 1;
+  while (S < 8 && 2 * S * per <= MK_COMPUTE_WARPS) S *= 2;
+  return S;
+}
+__device__ __forceinline__ int mk_attn_subtasks(const MkParams& P, int S) {
+  return (P.nkv * P.nsplit + P.nb - 1) / P.nb * S;
+}
+__device__ __forceinline__ bool mk_attn_sub(const MkParams& P, int j, int S, int m, int& t, int& g, int& split,
+                                            int& a, int& b) {
+  t = blockIdx.x + (j / S) * P.nb;
+  if (t >= P.nkv * P.nsplit) return false;
+  int s0, j1;
+  mk_attn_task(P, t, m, g, split, s0, j1);
+  const int len = max(0, j1 - s0), k = j % S;
+  a = s0 + (len * k) / S;
+  b = s0 + (len * (k + 1)) / S;
+  return true;
+}
+
+// 2^x on the special-function unit (subnormal results flushed to zero).
+__device__ __forceinline__ float ex2f_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 32 partial sums per lane -> lane i holds the warp-wide sum of slot i (31 shuffles).
+__device__ __forceinline__ void mk_reduce_scatter32(float* v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int n = 16; n >= 1; n >>= 1) {
+    const bool upper = (lane & n) != 0;
+#pragma unroll
+    for (int j = 0; j < n; ++j) {
+      const float send = upper ? v[j] : v[j + n];
+      const float keep = upper ? v[j + n] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, n);
+    }
+  }
+}
+
+// DPL consecutive elements of a K/V row (this lane's dims), as f32.
+template <typename KV, int DPL>
+__device__ __forceinline__ void mk_load_dims(const KV* p, float* v, bool global) {
+  if constexpr (sizeof(KV) == 4) {
+    if constexpr (DPL == 4) {
+      const float4 t = global ? __ldcg(reinterpret_cast<const float4*>(p)) : *reinterpret_cast<const float4*>(p);
+      v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else {
+      const float2 t = global ? __ldcg(reinterpret_cast<const float2*>(p)) : *reinterpret_cast<const float2*>(p);
+      v[0] = t.x; v[1] = t.y;
+    }
+  } else {
+#pragma unroll
+    for (int d = 0; d < DPL; d += 2) {
+      const uint32_t u = global ? __ldcg(reinterpret_cast<const unsigned int*>(p + d))
+                                : *reinterpret_cast<const uint32_t*>(p + d);
+      v[d] = bf16_lo(u);
+      v[d + 1] = bf16_hi(u);
+    }
+  }
+}
+
+template <typename W, typename KV, int HD, int GP>
+__device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8_t* ureg, MkMisc* M, uint32_t& sc) {
+  using AG = MkAttnGeom<W, KV, HD>;
+  constexpr int NS = MkRing<W>::STAGES, SB = AG::SB, RB = AG::RB, RPP = AG::RPP;
+  constexpr int DPL = HD / 32;                                  // dims per lane
+  constexpr int KG = (32 / GP) < RPP ? (32 / GP) : RPP;         // keys per reduce group
+  constexpr int NG = RPP / KG;                                  // groups per piece
+  constexpr float LOG2E = 1.4426950408889634f;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const MkLayer& L = P.layers[l];
+  const KV* kc = (const KV*)L.kc;
+  const KV* vc = (const KV*)L.vc;
+  const int G = P.nq / P.nkv, kd = P.nkv * HD, tasks = P.nkv * P.nsplit;
+  const int m = P.sliding > 0 ? min(P.pos + 1, P.max_seq) : P.pos + 1;
+  const int slot_pos = P.sliding > 0 ? P.pos % P.max_seq : P.pos;
+  const float qscale = LOG2E / sqrtf((float)HD);               // scores in log2 units
+  volatile int* abort_flag = &M->abort_flag;
+  uint8_t* wring = ring + (size_t)warp * MK_WARP_RING;
+  DeviceState* const stp = P.st;
+  uint32_t scl = sc;
+  bool ok = true;
+  const int own = lane % GP;                                    // this lane's head in the score slots
+  const int S = mk_attn_ways(P), nsub = mk_attn_subtasks(P, S);
+  float* sst = reinterpret_cast<float*>(ureg);                  // [8 slots][G][HD + 2] softmax states
+  (void)tasks;
+  for (int j0 = 0; j0 < nsub; j0 += MK_COMPUTE_WARPS) {
+   const int j = j0 + warp;
+   int t, g, split, s0, j1;
+   if (j < nsub && mk_attn_sub(P, j, S, m, t, g, split, s0, j1)) {
+    float qv[GP][DPL], acc[GP][DPL];
+#pragma unroll
+    for (int h = 0; h < GP; ++h)
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) {
+        qv[h][d] = h < G ? __ldcg(P.q + (size_t)(g * G + h) * HD + lane * DPL + d) * qscale : 0.f;
+        acc[h][d] = 0.f;
+      }
+    float mown = -INFINITY, lown = 0.f;   // running max / sum of head `own`
+    for (int c0 = s0; c0 < j1; c0 += RPP) {
+      const int nk = min(RPP, j1 - c0);
+      // ---- K piece: scores of (key, head) slots, one per lane after the reduction
+      float scr[NG];
+      const uint8_t* tile = nullptr;
+      if (ok) {
+        const int st = scl % NS;
+        if (mk_mbar_wait(&M->full[warp][st], (scl / NS) & 1u, abort_flag, stp, 203)) tile = wring + (size_t)st * SB;
+        else ok = false;
+      }
+#pragma unroll
+      for (int q = 0; q < NG; ++q) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KG; ++kk) {
+          const int r = q * KG + kk;
+          if (ok && r < nk) {
+            float kv[DPL];
+            const bool cur = c0 + r == slot_pos;
+            mk_load_dims<KV, DPL>(cur ? kc + (size_t)slot_pos * kd + (size_t)g * HD + lane * DPL
+                                      : reinterpret_cast<const KV*>(tile + (size_t)r * RB) + lane * DPL,
+                                  kv, cur);
+#pragma unroll
+            for (int h = 0; h < GP; ++h) {
+              float s = 0.f;
+#pragma unroll
+              for (int d = 0; d < DPL; ++d) s = fmaf(qv[h][d], kv[d], s);
+              v[kk * GP + h] = s;
+            }
+          }
+        }
+        mk_reduce_scatter32(v);
+        const int r = q * KG + lane / GP;
+        scr[q] = (lane < KG * GP && r < nk && own < G) ? v[0] : -INFINITY;
+      }
+      if (tile) {
+        __syncwarp();
+        if (lane == 0) mk_mbar_arrive(&M->empty[warp][scl % NS]);
+        ++scl;
+        if (lane == 0) M->consumed[warp] = (int)scl;
+      }
+      // ---- online softmax over the piece (lanes of one head share its state)
+      float cm = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < NG; ++q) cm = fmaxf(cm, scr[q]);
+#pragma unroll
+      for (int o = GP; o < 32; o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+      const float mn = fmaxf(mown, cm);
+      const float al = mown == -INFINITY ? 0.f : ex2f_approx(mown - mn);
+      float pr[NG], ps = 0.f;
+#pragma unroll
+      for (int q = 0; q < NG; ++q) {
+        pr[q] = scr[q] == -INFINITY ? 0.f : ex2f_approx(scr[q] - mn);
+        ps += pr[q];
+      }
+#pragma unroll
+      for (int o = GP; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+      lown = lown * al + ps;
+      mown = mn;
+#pragma unroll
+      for (int h = 0; h < GP; ++h) {
+        const float a = __shfl_sync(0xffffffffu, al, h);
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) acc[h][d] *= a;
+      }
+      // ---- V piece: acc[h] += p[key, h] * V[key]
+      tile = nullptr;
+      if (ok) {
+        const int st = scl % NS;
+        if (mk_mbar_wait(&M->full[warp][st], (scl / NS) & 1u, abort_flag, stp, 204)) tile = wring + (size_t)st * SB;
+        else ok = false;
+      }
+#pragma unroll
+      for (int r = 0; r < RPP; ++r) {
+        if (ok && r < nk) {
+          float vv[DPL];
+          const bool cur = c0 + r == slot_pos;
+          mk_load_dims<KV, DPL>(cur ? vc + (size_t)slot_pos * kd + (size_t)g * HD + lane * DPL
+                                    : reinterpret_cast<const KV*>(tile + (size_t)r * RB) + lane * DPL,
+                                vv, cur);
+#pragma unroll
+          for (int h = 0; h < GP; ++h) {
+            const float pw = __shfl_sync(0xffffffffu, pr[r / KG], (r % KG) * GP + h);
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) acc[h][d] = fmaf(pw, vv[d], acc[h][d]);
+          }
+        }
+      }
+      if (tile) {
+        __syncwarp();
+        if (lane == 0) mk_mbar_arrive(&M->empty[warp][scl % NS]);
+        ++scl;
+        if (lane == 0) M->consumed[warp] = (int)scl;
+      }
+    }
+    // ---- this slice's state (max in log2 units) into its shared-memory slot
+    float* so = sst + (size_t)(j - j0) * G * (HD + 2);
+#pragma unroll
+    for (int h = 0; h < GP; ++h)
+      if (h < G) {
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) so[h * (HD + 2) + lane * DPL + d] = acc[h][d];
+      }
+    if (lane < G) {
+      so[lane * (HD + 2) + HD] = mown;
+      so[lane * (HD + 2) + HD + 1] = lown;
+    }
+   }
+    // ---- combine the S slices of each task of this round: a split partial
+    // (max in natural-log units, as the merge expects), or with one split the
+    // normalised output.
+    compute_sync();
+    const int tpr = MK_COMPUTE_WARPS / S;
+    for (int e = threadIdx.x; e < tpr * G * HD; e += MK_COMPUTE) {
+      const int ti = e / (G * HD), h = (e / HD) % G, d = e % HD;
+      const int jt = j0 + ti * S;
+      int tt, gg, sp, a, b;
+      if (jt >= nsub || !mk_attn_sub(P, jt, S, m, tt, gg, sp, a, b)) continue;
+      const float* st0 = sst + (size_t)(ti * S) * G * (HD + 2) + h * (HD + 2);
+      float mx = -INFINITY;
+      for (int k = 0; k < S; ++k) mx = fmaxf(mx, st0[(size_t)k * G * (HD + 2) + HD]);
+      float lsum = 0.f, o = 0.f;
+      if (mx != -INFINITY)
+        for (int k = 0; k < S; ++k) {
+          const float* sk = st0 + (size_t)k * G * (HD + 2);
+          const float wk = sk[HD] == -INFINITY ? 0.f : ex2f_approx(sk[HD] - mx);
+          lsum = fmaf(sk[HD + 1], wk, lsum);
+          o = fmaf(sk[d], wk, o);
+        }
+      if (P.nsplit == 1) {
+        P.attn[(size_t)(gg * G + h) * HD + d] = lsum > 0.f ? o / lsum : 0.f;
+      } else {
+        float* pp = P.part + ((size_t)(gg * G + h) * P.nsplit + sp) * (HD + 2);
+        pp[d] = o;
+        if (d == 0) {
+          pp[HD] = mx == -INFINITY ? -INFINITY : mx / LOG2E;
+          pp[HD + 1] = lsum;
+        }
+      }
+    }
+    compute_sync();
+  }
+  sc = scl;
+  return ok;
+}
+
+template <typename W, typename KV, int HD>
+__device__ bool mk_attention_warp_any(const MkParams& P, int l, uint8_t* ring, uint8_t* ureg, MkMisc* M,
+                                      uint32_t& sc) {
+  if constexpr (HD == 64 || HD == 128) {
+    // Groups of 1-3 query heads per kv head run in the 4-head layout (unused
+    // slots stay empty): two instantiations keep the build short.
+    if (P.nq / P.nkv <= 4) return mk_attention_warp<W, KV, HD, 4>(P, l, ring, ureg, M, sc);
+    return mk_attention_warp<W, KV, HD, 8>(P, l, ring, ureg, M, sc);
+  } else {
+    return false;
+  }
+}
+
 // ------------------------------------------------------------------ attention phase
 // Task (g, split): the G query heads of kv head g over slots
 // [split*sps, split*sps + sps) intersected with the readable slots
@@ -1196,6 +1488,36 @@ __device__ void mk_produce(const MkParams& P, uint8_t* ring, MkMisc* M) {
         int ph, l;
         mk_phase_at(P, i, ph, l);
         if (ph == PH_ATTN) mk_prefetch_attention_kv(P, l, P.hd, w, MK_COMPUTE_WARPS);
+        if constexpr (HD == 64 || HD == 128) {
+          if (ph == PH_ATTN && P.attn_warp) {
+            // This warp's attention tasks: per RPP keys a K piece, then a V piece,
+            // one bulk copy per key row of the task's kv head.
+            using AG = MkAttnGeom<W, KV, HD>;
+            const MkLayer& L = P.layers[l];
+            const int m = P.sliding > 0 ? min(P.pos + 1, P.max_seq) : P.pos + 1;
+            const int kd = P.nkv * HD;
+            const int S = mk_attn_ways(P), nsub = mk_attn_subtasks(P, S);
+            for (int j = w; j < nsub && ok; j += MK_COMPUTE_WARPS) {
+              int t, g, split, s0, j1;   // [s0, j1): this sub-task's keys
+              if (!mk_attn_sub(P, j, S, m, t, g, split, s0, j1)) continue;
+              for (int c0 = s0; c0 < j1 && ok; c0 += AG::RPP) {
+                const int nk = min(AG::RPP, j1 - c0);
+                for (int kv = 0; kv < 2 && ok; ++kv) {
+                  const int st = claim((uint32_t)(nk * AG::RB));
+                  if (st < 0) {
+                    ok = false;
+                    break;
+                  }
+                  const KV* base = (const KV*)(kv ? L.vc : L.kc);
+                  for (int r = 0; r < nk; ++r)
+                    mk_bulk_load(wring + (size_t)st * SB + (size_t)r * AG::RB,
+                                 base + (size_t)(c0 + r) * kd + (size_t)g * HD, (uint32_t)AG::RB, &M->full[w][st]);
+                }
+              }
+            }
+            continue;
+          }
+        }
         if (!mk_is_gemv(ph)) continue;
         if (P.E > 0 && (ph == PH_GATEUP || ph == PH_DOWN)) {
           // Expert rows are known once this layer's router has run.
@@ -1293,7 +1615,8 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
                          xs, M, MMA ? xb : nullptr, P.xb_plane, kpad_h);
         break;
       case PH_ATTN:
-        mk_attention<KV, HD>(P, l, ureg, M);
+        if (P.attn_warp) ok = mk_attention_warp_any<W, KV, HD>(P, l, ring, ureg, M, sc);
+        else mk_attention<KV, HD>(P, l, ureg, M);
         break;
       case PH_MERGE:
         for (int h0 = blockIdx.x; h0 < P.nq; h0 += P.nb)
@@ -1432,9 +1755,19 @@ static size_t mk_u_bytes(const dec_config& c, int nsplit) {
   const size_t ce = 16 / kvs, hd = c.head_dim, G = c.n_heads / c.n_kv_heads;
   size_t xs = (size_t)mk_xs_floats(c, nsplit) * sizeof(float);
   if (c.weight_dtype == DEC_BF16) xs += 2 * sizeof(__nv_bfloat16) * (size_t)mk_xb_plane(c);
-  const size_t attn = MK_KS * (hd + ce) * kvs + MK_KS * hd * kvs + G * hd * 4 + G * MK_KS * 4;
+  size_t attn = MK_KS * (hd + ce) * kvs + MK_KS * hd * kvs + G * hd * 4 + G * MK_KS * 4;
+  const size_t slots = (size_t)MK_COMPUTE_WARPS * G * (hd + 2) * 4;   // warp-task softmax states
+  if (slots > attn) attn = slots;
   const size_t u = xs > attn ? xs : attn;
   return (u + 127) / 128 * 128;
+}
+
+// Attention as per-warp tasks: head_dim 64/128 (a lane owns head_dim / 32
+// dims), at most 8 query heads per kv head, and a stage holds at least one
+// head's K or V row.
+static bool mk_attn_warp_ok(const dec_config& c) {
+  const int G = c.n_heads / c.n_kv_heads;
+  return (c.head_dim == 64 || c.head_dim == 128) && G >= 1 && G <= 8;
 }
 
 size_t mk_smem_bytes(const dec_config& c, int nsplit) {
@@ -1499,12 +1832,17 @@ static void* mk_pick(int hd) {
   return (void*)k_decode_step<W, KV, 16>;
 }
 
+// The persistent step's instantiations: bf16 weights at every head_dim, f32
+// weights only at head_dim 16 (the fp32 toy shape; larger f32 models keep the
+// per-layer kernels), which keeps this file's build time in check.
 static void* mk_func(const dec_config& c) {
   const bool wb = c.weight_dtype == DEC_BF16, kb = c.kv_dtype == DEC_BF16;
-  if (wb && kb) return mk_pick<__nv_bfloat16, __nv_bfloat16>(c.head_dim);
-  if (wb) return mk_pick<__nv_bfloat16, float>(c.head_dim);
-  if (kb) return mk_pick<float, __nv_bfloat16>(c.head_dim);
-  return mk_pick<float, float>(c.head_dim);
+  if (!wb) {
+    if (c.head_dim != 16) return nullptr;
+    return kb ? (void*)k_decode_step<float, __nv_bfloat16, 16> : (void*)k_decode_step<float, float, 16>;
+  }
+  if (kb) return mk_pick<__nv_bfloat16, __nv_bfloat16>(c.head_dim);
+  return mk_pick<__nv_bfloat16, float>(c.head_dim);
 }
 
 // Whether the persistent step fits this configuration on this GPU; sets the
@@ -1524,6 +1862,7 @@ bool mk_prepare(Model& m, int num_sms) {
   const size_t smem = mk_smem_bytes(c, m.nsplit);
   if (smem > 227 * 1024) return false;
   void* fn = mk_func(c);
+  if (!fn) return false;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return false;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, MK_THREADS, smem) != cudaSuccess || per_sm < 1)
@@ -1612,6 +1951,7 @@ void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, in
   P.maps = reinterpret_cast<const CUtensorMap*>(m.mk_maps);
   P.xs_floats = mk_xs_floats(c, m.nsplit);
   P.xb_plane = mk_xb_plane(c);
+  P.attn_warp = mk_attn_warp_ok(c) ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(P.nb);
   cfg.blockDim = dim3(MK_THREADS);
