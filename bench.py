@@ -70,6 +70,10 @@ TRAFFIC = {
         "bytes": 1814336, "source": "decoder_only_forward_gb300/csrc/decode.cu",
         "sha256": "3d7213fecd5001252701110382d8e9dfd57676011ecc1ded9bf6666198c7ae34",
         "profile": "profiles/gemv_down_smollm2-135m_traffic.md"},
+    ("mistral-7b", "step"): {
+        "bytes": 15712395008, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
+        "sha256": "4bf7258819f5eaeff409afa95ceaa4deb2af4270224b2c6b5de9309906a0eb17",
+        "profile": "profiles/decode_step_traffic_mistral-7b.md"},
 }
 
 
