@@ -96,6 +96,16 @@ class OracleConfig:
     rope_theta: float = 10000.0
     # llama3 scaling: dict(factor=, low_freq_factor=, high_freq_factor=, orig_ctx=) or None
     rope_llama3: Optional[dict] = None
+    # Which dimensions pair (RML Rotary embeddings, "Which dimensions pair"): False =
+    # adjacent (2i, 2i+1) (kInterleaved), True = (i, i + rope_dim/2) (kHalf, rotate_half).
+    rope_half: bool = False
+    # Rotary width (SIP partial-rotary rope_rot): only the first rope_dim dims of a head
+    # turn, the rest pass through; 0 means head_dim.
+    rope_dim: int = 0
+
+    @property
+    def rotary_dim(self) -> int:
+        return self.rope_dim if self.rope_dim else self.head_dim
 
     @classmethod
     def from_dict(cls, d: dict) -> "OracleConfig":
@@ -144,27 +154,43 @@ def llama3_scale_inv_freq(inv_freq, factor: float, low_freq_factor: float,
     return out
 
 
-def rope_inv_freq(head_dim: int, theta: float, llama3: Optional[dict] = None) -> np.ndarray:
-    """inv_freq[i] = theta^(-2i/head_dim) for pair i in [0, head_dim/2) (RML Rotary embeddings)."""
-    i = np.arange(head_dim // 2, dtype=F64)
-    inv = np.power(F64(theta), -2.0 * i / head_dim)
+def rope_inv_freq(head_dim: int, theta: float, llama3: Optional[dict] = None, rope_dim: int = 0) -> np.ndarray:
+    """inv_freq[i] = theta^(-2i/d) for pair i in [0, d/2), d the rotary width (RML Rotary
+    embeddings; with partial rotary, SIP rope_rot, d = rope_dim)."""
+    d = rope_dim if rope_dim else head_dim
+    i = np.arange(d // 2, dtype=F64)
+    inv = np.power(F64(theta), -2.0 * i / d)
     if llama3:
         inv = llama3_scale_inv_freq(inv, **llama3)
     return inv
 
 
-def rope_rotate(vec, pos: int, inv_freq) -> np.ndarray:
-    """Rotate adjacent pairs (v[2i], v[2i+1]) by angle pos*inv_freq[i] (SIP "RoPE is adjacent-pair").
+def rope_pairs(head_dim: int, half: bool = False, rope_dim: int = 0):
+    """Index arrays (a, b) of the rotated pairs of one head: pair i is (a[i], b[i]).
+
+    Adjacent style (SIP "RoPE is adjacent-pair"; kInterleaved): (2i, 2i+1).  Half
+    style (RML "Which dimensions pair"; kHalf): (i, i + d/2).  d = rope_dim or
+    head_dim; dims >= d are not rotated (SIP partial-rotary).
+    """
+    d = rope_dim if rope_dim else head_dim
+    i = np.arange(d // 2)
+    return (i, i + d // 2) if half else (2 * i, 2 * i + 1)
+
+
+def rope_rotate(vec, pos: int, inv_freq, half: bool = False, rope_dim: int = 0) -> np.ndarray:
+    """Rotate each pair (v[a_i], v[b_i]) by angle pos*inv_freq[i]:
+    (a, b) -> (a cos - b sin, a sin + b cos).
 
     ``vec`` is [..., head_dim]; each head is rotated independently.
     """
     v = np.array(vec, dtype=F64, copy=True)
+    ia, ib = rope_pairs(v.shape[-1], half, rope_dim)
     ang = F64(pos) * np.asarray(inv_freq, F64)
     c, s = np.cos(ang), np.sin(ang)
-    a = v[..., 0::2].copy()
-    b = v[..., 1::2].copy()
-    v[..., 0::2] = a * c - b * s
-    v[..., 1::2] = a * s + b * c
+    a = v[..., ia].copy()
+    b = v[..., ib].copy()
+    v[..., ia] = a * c - b * s
+    v[..., ib] = a * s + b * c
     return v
 
 
@@ -315,7 +341,7 @@ class Session:
     def __init__(self, cfg: OracleConfig, weights, trace: bool = False, trace_hidden: bool = False):
         self.cfg = cfg
         self.w = weights
-        self.inv_freq = rope_inv_freq(cfg.head_dim, cfg.rope_theta, cfg.rope_llama3)
+        self.inv_freq = rope_inv_freq(cfg.head_dim, cfg.rope_theta, cfg.rope_llama3, cfg.rope_dim)
         self.keys = [[] for _ in range(cfg.n_layers)]
         self.values = [[] for _ in range(cfg.n_layers)]
         self.trace = Trace() if trace else None
@@ -351,8 +377,8 @@ class Session:
             q = q + lw["bq"]
             k = k + lw["bk"]
             v = v + lw["bv"]
-        q = rope_rotate(q.reshape(nq, hd), pos, self.inv_freq)
-        k = rope_rotate(k.reshape(nkv, hd), pos, self.inv_freq)
+        q = rope_rotate(q.reshape(nq, hd), pos, self.inv_freq, c.rope_half, c.rope_dim)
+        k = rope_rotate(k.reshape(nkv, hd), pos, self.inv_freq, c.rope_half, c.rope_dim)
         if len(self.keys[l]) != pos:
             raise AssertionError("positions must be appended in ascending order")
         self.keys[l].append(k)
@@ -434,12 +460,14 @@ class Session:
         ang = pos[:, None].astype(F64) * self.inv_freq[None, :]
         cos, sin = np.cos(ang), np.sin(ang)
 
-        def rot(T):  # T [n, heads, hd]
-            a = T[..., 0::2].copy()
-            b = T[..., 1::2].copy()
-            out = np.empty_like(T)
-            out[..., 0::2] = a * cos[:, None, :] - b * sin[:, None, :]
-            out[..., 1::2] = a * sin[:, None, :] + b * cos[:, None, :]
+        ia, ib = rope_pairs(hd, c.rope_half, c.rope_dim)
+
+        def rot(T):  # T [n, heads, hd]; row t at position pos[t]
+            a = T[..., ia].copy()
+            b = T[..., ib].copy()
+            out = T.copy()
+            out[..., ia] = a * cos[:, None, :] - b * sin[:, None, :]
+            out[..., ib] = a * sin[:, None, :] + b * cos[:, None, :]
             return out
 
         scale = 1.0 / math.sqrt(hd)

@@ -15,7 +15,7 @@ import scipy.special
 import torch
 import torch.nn.functional as F
 
-from oracle import (OracleConfig, Session, attend_ref, kv_head_of, llama3_scale_inv_freq,
+from oracle import (DictWeights, OracleConfig, Session, attend_ref, kv_head_of, llama3_scale_inv_freq,
                     moe_ffn, rmsnorm, rope_inv_freq, rope_rotate, route_topk, silu, swiglu,
                     window_start)
 from tests.oracle_helpers import random_weights, toy_cfg, torch_library_forward
@@ -137,6 +137,82 @@ def test_rope_adjacent_equals_rotate_half_on_permuted_dims():
     y = np.empty(hd)
     y[perm] = yh
     np.testing.assert_allclose(rope_rotate(x, pos, inv), y, atol=1e-14)
+
+
+def test_rope_half_style_is_rotate_half():
+    # rml "Which dimensions pair": kHalf pairs dim i with i + head_dim/2, i.e. HF's
+    # x * cos + rotate_half(x) * sin, written here independently.
+    hd, pos = 16, 91
+    inv = rope_inv_freq(hd, 10000.0)
+    x = np.random.default_rng(11).normal(size=(3, hd))
+    ang = np.concatenate([pos * inv, pos * inv])
+    rot_half = np.concatenate([-x[:, hd // 2:], x[:, :hd // 2]], axis=1)
+    np.testing.assert_allclose(rope_rotate(x, pos, inv, half=True), x * np.cos(ang) + rot_half * np.sin(ang),
+                               atol=1e-14)
+
+
+def test_rope_half_style_matches_complex_multiplication():
+    hd, pos = 32, 1311
+    inv = rope_inv_freq(hd, 1e6)
+    v = np.random.default_rng(12).normal(size=hd)
+    z = (v[:hd // 2] + 1j * v[hd // 2:]) * np.exp(1j * pos * inv)
+    np.testing.assert_allclose(rope_rotate(v, pos, inv, half=True), np.concatenate([z.real, z.imag]), atol=1e-13)
+
+
+@pytest.mark.parametrize("half", [False, True])
+def test_partial_rotary_passes_the_tail_through(half):
+    # sipllm partial-rotary (rope_rot): only the first rope_dim dims turn, the rest
+    # pass through; the rotated part is a full rotation of a rope_dim-wide head.
+    hd, rd, pos, theta = 32, 12, 57, 10000.0
+    inv = rope_inv_freq(hd, theta, rope_dim=rd)
+    assert inv.shape == (rd // 2,)
+    v = np.random.default_rng(13).normal(size=(2, hd))
+    out = rope_rotate(v, pos, inv, half=half, rope_dim=rd)
+    np.testing.assert_array_equal(out[:, rd:], v[:, rd:])
+    np.testing.assert_allclose(out[:, :rd], rope_rotate(v[:, :rd], pos, rope_inv_freq(rd, theta), half=half),
+                               atol=1e-14)
+
+
+def test_partial_rotary_frequencies_closed_form():
+    # inv_freq[i] = theta^(-2i/rope_dim): with rope_dim 4 and theta 1e4 the two pairs
+    # turn 1 and 1e-2 radians per position whatever head_dim is.
+    np.testing.assert_allclose(rope_inv_freq(64, 1e4, rope_dim=4), [1.0, 1e-2], rtol=1e-15)
+
+
+@pytest.mark.parametrize("half,rd", [(True, 0), (True, 12), (False, 12)])
+def test_rope_variants_keep_relative_position_invariance(half, rd):
+    hd = 32
+    inv = rope_inv_freq(hd, 10000.0, rope_dim=rd)
+    rng = np.random.default_rng(14)
+    q, k = rng.normal(size=hd), rng.normal(size=hd)
+    a = rope_rotate(q, 250, inv, half, rd) @ rope_rotate(k, 243, inv, half, rd)
+    b = rope_rotate(q, 9, inv, half, rd) @ rope_rotate(k, 2, inv, half, rd)
+    assert abs(a - b) < 1e-12
+
+
+def test_half_style_model_equals_adjacent_model_on_permuted_qk_rows():
+    # The same decoder with kHalf pairing and with adjacent pairing on q/k weight
+    # rows permuted per head ((i, i + d/2) -> (2i, 2i+1)) gives the same logits:
+    # attention sees only q . k, which the consistent permutation leaves unchanged.
+    cfg_h = toy_cfg(rope_dim=8, rope_half=True)
+    cfg_a = toy_cfg(rope_dim=8)
+    w = random_weights(cfg_h, seed=21)
+    hd, rd = cfg_h.head_dim, 8
+    src = np.concatenate([np.stack([np.arange(rd // 2), np.arange(rd // 2) + rd // 2], 1).ravel(),
+                          np.arange(rd, hd)])          # permuted row p <- original row src[p]
+
+    def permute(m, heads):
+        return np.concatenate([m[h * hd + src] for h in range(heads)])
+
+    layers = []
+    for l in range(cfg_h.n_layers):
+        lw = w.layer(l)
+        layers.append(dict(lw, wq=permute(lw["wq"], cfg_h.n_heads), wk=permute(lw["wk"], cfg_h.n_kv_heads)))
+    wp = DictWeights(w.embed_rows(np.arange(cfg_h.vocab)), w.out_norm(), layers, lm_head=w.lm_head())
+    toks = [3, 1, 4, 1, 5, 9, 2, 6]
+    a = Session(cfg_h, w).prefill(toks, 0, all_logits=True)
+    b = Session(cfg_a, wp).prefill(toks, 0, all_logits=True)
+    np.testing.assert_allclose(a, b, atol=1e-12)
 
 
 def test_llama3_worked_example():
