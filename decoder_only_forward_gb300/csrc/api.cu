@@ -61,6 +61,32 @@ static dec_status fail(dec_handle* h, dec_status st, const char* fmt, ...) {
 
 static size_t dsize(int32_t dt) { return dt == DEC_BF16 ? 2 : 4; }
 
+// Row r of wqkv (and entry r of bqkv) <- the row that holds dim src(d) of the
+// same head, for q and k rows: src(2i) = i, src(2i+1) = i + rd/2 for i < rd/2,
+// src(d) = d beyond the rotary width rd; v rows are copied unchanged.
+__global__ void k_permute_qk_rows(const uint4* __restrict__ w, const float* __restrict__ b, int qd, int kd, int hd,
+                                  int rd, int row_chunks, uint4* __restrict__ wdst, float* __restrict__ bdst) {
+  const int r = blockIdx.x;
+  int src = r;
+  if (r < qd + kd) {
+    const int d = (r < qd ? r : r - qd) % hd;
+    const int sd = d < rd ? ((d & 1) ? (d >> 1) + rd / 2 : (d >> 1)) : d;
+    src = r - d + sd;
+  }
+  for (int i = threadIdx.x; i < row_chunks; i += blockDim.x)
+    wdst[(size_t)r * row_chunks + i] = w[(size_t)src * row_chunks + i];
+  if (b && bdst && threadIdx.x == 0) bdst[r] = b[src];
+}
+
+void dec::launch_permute_qk_rows(const dec_config& c, const void* w, const float* b, void* wdst, float* bdst,
+                                 cudaStream_t s) {
+  const int qd = c.n_heads * c.head_dim, kd = c.n_kv_heads * c.head_dim;
+  const int rd = c.rope_dim ? c.rope_dim : c.head_dim;
+  const int chunks = (int)((size_t)c.hidden * dsize(c.weight_dtype) / 16);
+  k_permute_qk_rows<<<qd + 2 * kd, 128, 0, s>>>((const uint4*)w, b, qd, kd, c.head_dim, rd, chunks, (uint4*)wdst,
+                                                bdst);
+}
+
 static bool validate(const dec_config* c, std::string& why) {
   char b[256];
   auto bad = [&](const char* m) { why = m; return false; };
@@ -80,6 +106,9 @@ static bool validate(const dec_config* c, std::string& why) {
   if (c->sliding_window < 0 || c->max_tokens < 0) return bad("sliding_window and max_tokens must be >= 0");
   if (c->sliding_window > 0 && c->max_seq > c->sliding_window)
     return bad("under a sliding window max_seq = min(sliding_window, n_ctx) cannot exceed the window");
+  if (c->rope_half != 0 && c->rope_half != 1) return bad("rope_half must be 0 or 1");
+  if (c->rope_dim < 0 || c->rope_dim > c->head_dim || c->rope_dim % 2 != 0)
+    return bad("rope_dim must be even and in [0, head_dim] (0 = head_dim)");
   if (c->rope_llama3 && !(c->rope_factor > 0.f && c->rope_low_freq_factor > 0.f &&
                           c->rope_high_freq_factor > c->rope_low_freq_factor && c->rope_orig_ctx > 0))
     return bad("llama3 RoPE scaling needs factor > 0, 0 < low < high, orig_ctx > 0");
@@ -153,7 +182,6 @@ WsPlan dec::plan_workspace(const dec_config& c) {
   p.Asort = take(c.n_experts ? a_elem * (size_t)T * k * c.hidden : 0);
   p.Y = take(c.n_experts ? 4 * (size_t)T * k * c.hidden : 0);
   p.ACT = take(a_elem * (size_t)T * k * c.ffn);
-  (void)ws;
   // Tensor-core prefill attention: K planes and V^T planes (bf16 hi, lo) of up
   // to max_seq + T key columns; the Q planes reuse the f32 Q rows.
   const bool at = attn_tc_supported(c);
@@ -161,6 +189,10 @@ WsPlan dec::plan_workspace(const dec_config& c) {
   p.at_vt_ld = at ? (int)align_up((size_t)(c.max_seq + T), 8) : 0;
   p.at_Kb = take(2 * 2 * (size_t)p.at_kcap * kd);
   p.at_Vt = take(2 * 2 * (size_t)kd * p.at_vt_ld);
+  // kHalf RoPE: per-head row-permuted copies of the q/k rows (and biases) of wqkv.
+  const size_t qkv_rows = (size_t)qd + 2 * kd;
+  p.wqkv_perm = take(c.rope_half ? (size_t)c.n_layers * qkv_rows * c.hidden * ws : 0);
+  p.bqkv_perm = take(c.rope_half && c.qkv_bias ? (size_t)c.n_layers * qkv_rows * 4 : 0);
   p.mk_layers = take(sizeof(MkLayer) * (size_t)c.n_layers);
   p.mk_maps = take(mk_maps_bytes(c));
   p.kv = off;
@@ -291,6 +323,21 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
     d.kc = base + p.kv + (size_t)(2 * l) * p.kv_layer_bytes;
     d.vc = base + p.kv + (size_t)(2 * l + 1) * p.kv_layer_bytes;
   }
+  if (cfg->rope_half) {
+    // kHalf pairs (i, i + d/2) become adjacent pairs (2i, 2i+1) on q/k rows
+    // permuted per head: every kernel rotates adjacent pairs, and attention,
+    // which only forms q . k, is unchanged by the common permutation.
+    const size_t qkv_rows = (size_t)cfg->n_heads * cfg->head_dim + 2 * (size_t)cfg->n_kv_heads * cfg->head_dim;
+    const size_t row_bytes = (size_t)cfg->hidden * dsize(cfg->weight_dtype);
+    for (int l = 0; l < cfg->n_layers; ++l) {
+      LayerPtrs& d = h->layers[l];
+      char* wdst = base + p.wqkv_perm + (size_t)l * qkv_rows * row_bytes;
+      float* bdst = d.bqkv ? (float*)(base + p.bqkv_perm) + (size_t)l * qkv_rows : nullptr;
+      launch_permute_qk_rows(*cfg, d.wqkv, d.bqkv, wdst, bdst, h->stream);
+      d.wqkv = wdst;
+      d.bqkv = bdst;
+    }
+  }
   m.layers = h->layers.data();
   {
     std::vector<MkLayer> tab(cfg->n_layers);
@@ -325,9 +372,12 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
 
   // RoPE frequencies inv_i = theta^(-2i/hd), llama3-scaled when enabled
   // (rml "The decoder", Rotary embeddings), computed once in double.
-  std::vector<double> inv(cfg->head_dim / 2);
-  for (int i = 0; i < cfg->head_dim / 2; ++i) {
-    double f = pow((double)cfg->rope_theta, -2.0 * i / cfg->head_dim);
+  // Pairs beyond the rotary width keep frequency 0: a rotation by angle 0 (cos 1,
+  // sin 0) leaves them exactly as they are (partial rotary).
+  const int rdim = cfg->rope_dim ? cfg->rope_dim : cfg->head_dim;
+  std::vector<double> inv(cfg->head_dim / 2, 0.0);
+  for (int i = 0; i < rdim / 2; ++i) {
+    double f = pow((double)cfg->rope_theta, -2.0 * i / rdim);
     if (cfg->rope_llama3) {
       const double wl = 2.0 * M_PI / f, orig = cfg->rope_orig_ctx;
       const double lo = cfg->rope_low_freq_factor, hi = cfg->rope_high_freq_factor, fac = cfg->rope_factor;

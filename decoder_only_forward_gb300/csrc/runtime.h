@@ -133,6 +133,7 @@ struct WsPlan {
   size_t X, A, Q, KVlin_k, KVlin_v, pf_ids, pf_wts, pf_count, pf_offset, pf_rows, pf_inv, Asort, Y, ACT;
   size_t at_Kb, at_Vt;
   int at_kcap, at_vt_ld;  // 0: no tensor-core prefill attention for this configuration
+  size_t wqkv_perm, bqkv_perm;  // kHalf RoPE: q/k rows permuted per head
   size_t mk_layers;     // layer table of the persistent decode kernel
   size_t mk_maps;       // its weight tensor maps
   size_t kv;            // start of the KV rings
@@ -224,6 +225,11 @@ cudaError_t launch_kv_split(const float* K, const float* V, int kd, int r0, int 
 inline bool attn_tc_supported(const dec_config& c) {
   return c.kv_dtype == DEC_F32 && (c.head_dim == 64 || c.head_dim == 128);
 }
+
+// Copies one layer's wqkv (and bqkv) with the q/k rows of every head permuted
+// so that kHalf RoPE pairs (i, i + rope_dim/2) become adjacent (api.cu).
+void launch_permute_qk_rows(const dec_config& c, const void* w, const float* b, void* wdst, float* bdst,
+                            cudaStream_t s);
 
 // Message returned by dec_last_error(NULL) (api.cu).
 void set_global_error(const char* msg);

@@ -41,7 +41,8 @@ class Config(ctypes.Structure):
         "weight_dtype", "kv_dtype")] + [
         ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("rope_llama3", ctypes.c_int32),
         ("rope_factor", ctypes.c_float), ("rope_low_freq_factor", ctypes.c_float),
-        ("rope_high_freq_factor", ctypes.c_float), ("rope_orig_ctx", ctypes.c_int32)]
+        ("rope_high_freq_factor", ctypes.c_float), ("rope_orig_ctx", ctypes.c_int32),
+        ("rope_half", ctypes.c_int32), ("rope_dim", ctypes.c_int32)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -121,6 +122,8 @@ def make_config(w: dict, kv_dtype: str = "f32", max_tokens: int = 0) -> Config:
         c.rope_low_freq_factor = l3["low_freq_factor"]
         c.rope_high_freq_factor = l3["high_freq_factor"]
         c.rope_orig_ctx = int(l3["orig_ctx"])
+    c.rope_half = int(bool(w.get("rope_half", False)))
+    c.rope_dim = int(w.get("rope_dim", 0))
     return c
 
 

@@ -76,6 +76,15 @@ typedef struct dec_config {
   float rope_low_freq_factor;
   float rope_high_freq_factor;
   int32_t rope_orig_ctx;
+  int32_t rope_half;      /* which dimensions pair (rml "The decoder", Rotary embeddings): 0 = adjacent
+                             (2i, 2i+1) (kInterleaved, llama.cpp order); 1 = (i, i + rope_dim/2)
+                             (kHalf, rotate_half).  With 1, the library keeps a per-head row-permuted
+                             copy of each layer's q/k weight rows and biases in the workspace, and
+                             the K cache holds each head's dims in the adjacent order
+                             (0, d/2, 1, d/2+1, ..., then the unrotated tail) */
+  int32_t rope_dim;       /* rotary width: only the first rope_dim dims of a head turn, the rest
+                             pass through (sipllm partial-rotary rope_rot); 0 = head_dim; even,
+                             <= head_dim.  inv_freq_i = theta^(-2i/rope_dim) */
 } dec_config;
 
 /*

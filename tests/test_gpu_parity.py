@@ -103,6 +103,29 @@ def test_toy_llama3_rope(dec_mod):
     compare_logits(rows, ref, *tolerances(w))
 
 
+@pytest.mark.parametrize("kw", [dict(rope_half=True), dict(rope_dim=8), dict(rope_half=True, rope_dim=8)])
+def test_toy_rope_pairing_and_partial_rotary(dec_mod, kw):
+    # kHalf pairing (i, i + d/2) and partial rotary (first rope_dim dims only),
+    # fp32 throughout: the same bound as the default adjacent-pair toy.
+    w = synthetic.workload("toy", **kw)
+    _, _, rows, taus, ref, *_ = _run_case(dec_mod, w, 12, 8)
+    tol, _ = tolerances(w)
+    compare_logits(rows, ref, tol, tol)
+
+
+@pytest.mark.parametrize("mode", ["off", "grid"])
+def test_smollm2_shape_rope_half_partial(dec_mod, mode):
+    # A SmolLM2-shaped bf16 model with kHalf pairing over the first 32 of 64 dims,
+    # on the per-layer and the persistent decode schedules.
+    w = synthetic.workload("smollm2-135m", n_layers=4, rope_half=True, rope_dim=32)
+    d = dec_mod.Decoder(w)
+    d.set_fused(mode)
+    prompt = synthetic.prompt_tokens(w, 40, seed=0)
+    rows, taus = gpu_greedy(d, prompt, 6)
+    ref, _ = oracle_teacher_forced(w, prompt, taus, 6)
+    compare_logits(rows, ref, *tolerances(w))
+
+
 def test_toy_chunked_prefill(dec_mod):
     # max_tokens 5: a 16-token prompt runs as chunks 5+5+5+1.
     w = synthetic.workload("toy")
