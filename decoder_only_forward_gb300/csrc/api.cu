@@ -16,7 +16,8 @@ struct dec_handle {
   Model m;
   std::vector<LayerPtrs> layers;
   cudaStream_t stream;
-  int32_t len;          // positions held (host bookkeeping)
+  std::vector<int32_t> lens;   // positions held per sequence (host bookkeeping)
+  RowsMeta meta;        // rows of the current batched decode step
   std::string err;
   // decode graph, captured for one (logits, d_argmax) pair
   cudaGraphExec_t graph = nullptr;
@@ -109,6 +110,7 @@ static bool validate(const dec_config* c, std::string& why) {
   if (c->rope_half != 0 && c->rope_half != 1) return bad("rope_half must be 0 or 1");
   if (c->rope_dim < 0 || c->rope_dim > c->head_dim || c->rope_dim % 2 != 0)
     return bad("rope_dim must be even and in [0, head_dim] (0 = head_dim)");
+  if (c->n_seqs < 0 || c->n_seqs > 65536) return bad("n_seqs must be in [0, 65536] (0 = 1)");
   if (c->rope_llama3 && !(c->rope_factor > 0.f && c->rope_low_freq_factor > 0.f &&
                           c->rope_high_freq_factor > c->rope_low_freq_factor && c->rope_orig_ctx > 0))
     return bad("llama3 RoPE scaling needs factor > 0, 0 < low < high, orig_ctx > 0");
@@ -195,8 +197,19 @@ WsPlan dec::plan_workspace(const dec_config& c) {
   p.bqkv_perm = take(c.rope_half && c.qkv_bias ? (size_t)c.n_layers * qkv_rows * 4 : 0);
   p.mk_layers = take(sizeof(MkLayer) * (size_t)c.n_layers);
   p.mk_maps = take(mk_maps_bytes(c));
+  // Batched decode: per-row metadata and the attention split partials.
+  const int bmax = T < MAX_BATCH ? T : MAX_BATCH;
+  p.b_seq = take(4 * (size_t)MAX_BATCH);
+  p.b_pos = take(4 * (size_t)MAX_BATCH);
+  p.b_rows = take(4 * (size_t)MAX_BATCH);
+  p.b_part = take(4 * (size_t)bmax * c.n_heads * AR_MAX_SPLIT * (hd + 2));
+  // KV rings: [layer][K, V][seq][ring_rows][n_kv*hd], ring_rows = max_seq
+  // rounded up to 64 rows so every ring starts 256-byte aligned.
+  p.n_seqs = c.n_seqs > 0 ? c.n_seqs : 1;
+  p.ring_rows = (int)align_up((size_t)c.max_seq, 64);
+  p.ring_bytes = ks * (size_t)p.ring_rows * kd;
   p.kv = off;
-  p.kv_layer_bytes = align_up(ks * (size_t)c.max_seq * kd, 256);
+  p.kv_layer_bytes = p.ring_bytes * p.n_seqs;
   off += 2 * p.kv_layer_bytes * c.n_layers;
   p.total = off;
   return p;
@@ -250,7 +263,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
   dec_handle* h = new (std::nothrow) dec_handle();
   if (!h) return fail(nullptr, DEC_EINVAL, "out of host memory");
   h->stream = (cudaStream_t)cuda_stream;
-  h->len = 0;
+  h->lens.assign(p.n_seqs, 0);
   Model& m = h->m;
   m.cfg = *cfg;
   if (m.cfg.max_tokens == 0) m.cfg.max_tokens = p.max_tokens;
@@ -258,6 +271,9 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
   m.ws_bytes = workspace_bytes;
   m.nsplit = p.nsplit;
   m.attn_sps = p.attn_sps;
+  m.n_seqs = p.n_seqs;
+  m.ring_rows = p.ring_rows;
+  m.ring_bytes = p.ring_bytes;
   // LM head: two CTAs per SM, each warp walking its row pairs with the next
   // pair's loads in flight.
   int lg = (cfg->vocab / 2 + 7) / 8;
@@ -308,6 +324,10 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
   S.at.kcap = p.at_kcap;
   S.at.Vt = p.at_kcap ? (__nv_bfloat16*)(base + p.at_Vt) : nullptr;
   S.at.vt_ld = p.at_vt_ld;
+  S.b_seq = (int32_t*)(base + p.b_seq);
+  S.b_pos = (int32_t*)(base + p.b_pos);
+  S.b_rows = (int32_t*)(base + p.b_rows);
+  S.b_part = (float*)(base + p.b_part);
   h->layers.resize(cfg->n_layers);
   for (int l = 0; l < cfg->n_layers; ++l) {
     const dec_layer_weights& L = w->layers[l];
@@ -410,26 +430,28 @@ static dec_status cuda_check(dec_handle* h, const char* what) {
 
 // Position rules shared by prefill and decode (rml "The decoder", One forward
 // pass, step 1; Pantheon Sliding Window).
-static dec_status check_positions(dec_handle* h, int32_t n, int32_t start_pos) {
+static dec_status check_positions(dec_handle* h, int32_t seq, int32_t n, int32_t start_pos) {
   const dec_config& c = h->m.cfg;
   if (n <= 0) return fail(h, DEC_EINVAL, "empty input");
-  if (start_pos < 0 || start_pos > h->len)
-    return fail(h, DEC_EINVAL, "start_pos %d outside [0, %d]", start_pos, h->len);
+  const int32_t len = h->lens[seq];
+  if (start_pos < 0 || start_pos > len)
+    return fail(h, DEC_EINVAL, "start_pos %d outside [0, %d]", start_pos, len);
   if (c.sliding_window > 0 && c.max_seq == c.sliding_window) {
-    if (h->len > c.max_seq && start_pos < h->len)
+    if (len > c.max_seq && start_pos < len)
       return fail(h, DEC_EINVAL, "cannot rewind to %d: the ring has overwritten positions below %d",
-                  start_pos, h->len - c.max_seq);
+                  start_pos, len - c.max_seq);
   } else if ((int64_t)start_pos + n > c.max_seq) {
     return fail(h, DEC_ERANGE, "cache full: start_pos %d + n %d > max_seq %d", start_pos, n, c.max_seq);
   }
   return DEC_OK;
 }
 
-dec_status dec_prefill(dec_handle* h, const int32_t* tokens, int32_t n, int32_t start_pos, float* logits,
-                       int32_t* d_argmax) {
+dec_status dec_prefill_seq(dec_handle* h, int32_t seq, const int32_t* tokens, int32_t n, int32_t start_pos,
+                           float* logits, int32_t* d_argmax) {
   if (!h) return DEC_EINVAL;
+  if (seq < 0 || seq >= h->m.n_seqs) return fail(h, DEC_EINVAL, "sequence %d outside [0, %d)", seq, h->m.n_seqs);
   if (!tokens && n > 0) return fail(h, DEC_EINVAL, "tokens is NULL");
-  dec_status st = check_positions(h, n, start_pos);
+  dec_status st = check_positions(h, seq, n, start_pos);
   if (st != DEC_OK) return st;
   for (int32_t i = 0; i < n; ++i)
     if (tokens[i] < 0 || tokens[i] >= h->m.cfg.vocab)
@@ -442,7 +464,7 @@ dec_status dec_prefill(dec_handle* h, const int32_t* tokens, int32_t n, int32_t 
                                     cudaMemcpyHostToDevice, h->stream);
     if (e != cudaSuccess) return fail(h, DEC_ECUDA, "token copy: %s", cudaGetErrorString(e));
     const bool last = done + chunk == n;
-    e = launch_prefill_chunk(h->m, h->stream, chunk, start_pos + done, last ? logits : nullptr,
+    e = launch_prefill_chunk(h->m, h->stream, seq, chunk, start_pos + done, last ? logits : nullptr,
                              last ? d_argmax : nullptr);
     if (e != cudaSuccess) {
       cudaGetLastError();
@@ -452,8 +474,13 @@ dec_status dec_prefill(dec_handle* h, const int32_t* tokens, int32_t n, int32_t 
     if (st != DEC_OK) return st;
   }
   timing_finish(h);
-  h->len = start_pos + n;
+  h->lens[seq] = start_pos + n;
   return DEC_OK;
+}
+
+dec_status dec_prefill(dec_handle* h, const int32_t* tokens, int32_t n, int32_t start_pos, float* logits,
+                       int32_t* d_argmax) {
+  return dec_prefill_seq(h, 0, tokens, n, start_pos, logits, d_argmax);
 }
 
 // Points the captured step-setup node at this step's token and position.
@@ -534,13 +561,13 @@ static dec_status run_decode_step(dec_handle* h, const int32_t* d_token, int32_t
 
 dec_status dec_decode(dec_handle* h, int32_t token, int32_t pos, float* logits) {
   if (!h) return DEC_EINVAL;
-  dec_status st = check_positions(h, 1, pos);
+  dec_status st = check_positions(h, 0, 1, pos);
   if (st != DEC_OK) return st;
   if (token < 0 || token >= h->m.cfg.vocab)
     return fail(h, DEC_EINVAL, "token %d outside [0, %d)", token, h->m.cfg.vocab);
   st = run_decode_step(h, nullptr, token, pos, logits, nullptr);
   if (st != DEC_OK) return st;
-  h->len = pos + 1;
+  h->lens[0] = pos + 1;
   return DEC_OK;
 }
 
@@ -548,21 +575,71 @@ dec_status dec_decode_dev(dec_handle* h, const int32_t* d_token, int32_t pos, fl
                           int32_t* d_argmax) {
   if (!h) return DEC_EINVAL;
   if (!d_token) return fail(h, DEC_EINVAL, "d_token is NULL");
-  dec_status st = check_positions(h, 1, pos);
+  dec_status st = check_positions(h, 0, 1, pos);
   if (st != DEC_OK) return st;
   st = run_decode_step(h, d_token, 0, pos, logits, d_argmax);
   if (st != DEC_OK) return st;
-  h->len = pos + 1;
+  h->lens[0] = pos + 1;
   return DEC_OK;
 }
 
-dec_status dec_kv_reset(dec_handle* h) {
+dec_status dec_kv_reset(dec_handle* h) { return dec_kv_reset_seq(h, 0); }
+
+dec_status dec_kv_reset_seq(dec_handle* h, int32_t seq) {
   if (!h) return DEC_EINVAL;
-  h->len = 0;
+  if (seq < 0 || seq >= h->m.n_seqs) return fail(h, DEC_EINVAL, "sequence %d outside [0, %d)", seq, h->m.n_seqs);
+  h->lens[seq] = 0;
   return DEC_OK;
 }
 
-int32_t dec_length(const dec_handle* h) { return h ? h->len : -1; }
+int32_t dec_length(const dec_handle* h) { return dec_length_seq(h, 0); }
+
+int32_t dec_length_seq(const dec_handle* h, int32_t seq) {
+  if (!h || seq < 0 || seq >= h->m.n_seqs) return -1;
+  return h->lens[seq];
+}
+
+// One step of `batch` sequences through the row kernels; every argument is
+// checked before anything is enqueued.
+dec_status dec_decode_batch(dec_handle* h, int32_t batch, const int32_t* seqs, const int32_t* positions,
+                            const int32_t* d_tokens, float* logits, int32_t* d_argmax) {
+  if (!h) return DEC_EINVAL;
+  const dec_config& c = h->m.cfg;
+  const int bmax = c.max_tokens < MAX_BATCH ? c.max_tokens : MAX_BATCH;
+  if (batch < 1 || batch > bmax) return fail(h, DEC_EINVAL, "batch %d outside [1, %d]", batch, bmax);
+  if (!seqs || !positions || !d_tokens || !logits)
+    return fail(h, DEC_EINVAL, "seqs, positions, d_tokens and logits must not be NULL");
+  std::vector<char> seen(h->m.n_seqs, 0);
+  for (int32_t i = 0; i < batch; ++i) {
+    const int32_t q = seqs[i];
+    if (q < 0 || q >= h->m.n_seqs)
+      return fail(h, DEC_EINVAL, "row %d: sequence %d outside [0, %d)", i, q, h->m.n_seqs);
+    if (seen[q]) return fail(h, DEC_EINVAL, "row %d: sequence %d appears twice in the batch", i, q);
+    seen[q] = 1;
+    const dec_status st = check_positions(h, q, 1, positions[i]);
+    if (st != DEC_OK) return st;
+  }
+  RowsMeta& meta = h->meta;
+  for (int32_t i = 0; i < batch; ++i) {
+    const int32_t p = positions[i];
+    const int32_t slot = c.sliding_window > 0 ? p % c.max_seq : p;
+    meta.seq[i] = seqs[i];
+    meta.pos[i] = p;
+    meta.rows[i] = seqs[i] * h->m.ring_rows + slot;
+  }
+  timing_start(h);
+  cudaError_t e = launch_rows_setup(h->m, h->stream, meta, d_tokens, batch);
+  if (e == cudaSuccess) e = launch_decode_rows(h->m, h->stream, batch, logits, d_argmax);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(h, DEC_ECUDA, "batched decode launch: %s", cudaGetErrorString(e));
+  }
+  const dec_status st = cuda_check(h, "batched decode launch");
+  if (st != DEC_OK) return st;
+  timing_finish(h);
+  for (int32_t i = 0; i < batch; ++i) h->lens[seqs[i]] = positions[i] + 1;
+  return DEC_OK;
+}
 
 int64_t dec_launch_count(const dec_handle* h) { return h ? h->launches : -1; }
 
@@ -604,9 +681,14 @@ dec_status dec_set_graph(dec_handle* h, int32_t enable) {
 }
 
 dec_status dec_kv_layer(const dec_handle* h, int32_t layer, void** k, void** v) {
-  if (!h || !k || !v || layer < 0 || layer >= h->m.cfg.n_layers) return DEC_EINVAL;
-  *k = h->m.layers[layer].kc;
-  *v = h->m.layers[layer].vc;
+  return dec_kv_layer_seq(h, layer, 0, k, v);
+}
+
+dec_status dec_kv_layer_seq(const dec_handle* h, int32_t layer, int32_t seq, void** k, void** v) {
+  if (!h || !k || !v || layer < 0 || layer >= h->m.cfg.n_layers || seq < 0 || seq >= h->m.n_seqs)
+    return DEC_EINVAL;
+  *k = (char*)h->m.layers[layer].kc + (size_t)seq * h->m.ring_bytes;
+  *v = (char*)h->m.layers[layer].vc + (size_t)seq * h->m.ring_bytes;
   return DEC_OK;
 }
 

@@ -34,6 +34,78 @@ __global__ void k_rope_rows(const double* __restrict__ inv_freq, int half, int s
   tab[i] = make_float2((float)cs, (float)sn);
 }
 
+// Batched decode setup: each row's sequence, position and K/V row (passed by
+// value), its token id (an id outside [0, vocab) becomes 0 and raises
+// ERR_TOKEN) and the (cos, sin) table of the row's own position.
+__global__ void k_rows_setup(const __grid_constant__ RowsMeta meta, int B, const int32_t* __restrict__ d_tokens,
+                             int vocab, const double* __restrict__ inv_freq, int half, int32_t* __restrict__ tokens,
+                             int32_t* __restrict__ b_seq, int32_t* __restrict__ b_pos, int32_t* __restrict__ b_rows,
+                             float2* __restrict__ tab, DeviceState* st) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < B) {
+    int t = d_tokens[i];
+    if (t < 0 || t >= vocab) {
+      raise_error(st, ERR_TOKEN, 0);
+      t = 0;
+    }
+    tokens[i] = t;
+    b_seq[i] = meta.seq[i];
+    b_pos[i] = meta.pos[i];
+    b_rows[i] = meta.rows[i];
+  }
+  if (i < B * half) {
+    const int r = i / half, p = i % half;
+    double sn, cs;
+    sincos((double)meta.pos[r] * inv_freq[p], &sn, &cs);
+    tab[i] = make_float2((float)cs, (float)sn);
+  }
+}
+
+// out[r] = argmax over logits row r (ties -> lower id), one CTA per row.
+__global__ void __launch_bounds__(1024) k_argmax_rows(const float* __restrict__ logits, int V,
+                                                      int32_t* __restrict__ out) {
+  __shared__ float bv[32];
+  __shared__ int bi[32];
+  const float* x = logits + (size_t)blockIdx.x * V;
+  float best = -INFINITY;
+  int idx = 0x7fffffff;
+  for (int i = threadIdx.x; i < V; i += blockDim.x) {
+    const float v = x[i];
+    if (v > best) {   // ascending i per thread: the first maximum is kept
+      best = v;
+      idx = i;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+    if (ov > best || (ov == best && oi < idx)) {
+      best = ov;
+      idx = oi;
+    }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    bv[warp] = best;
+    bi[warp] = idx;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    best = lane < nw ? bv[lane] : -INFINITY;
+    idx = lane < nw ? bi[lane] : 0x7fffffff;
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+      if (ov > best || (ov == best && oi < idx)) {
+        best = ov;
+        idx = oi;
+      }
+    }
+    if (lane == 0) out[blockIdx.x] = idx == 0x7fffffff ? 0 : idx;
+  }
+}
+
 // A[t] = X[t] / sqrt(mean(X[t]^2) + eps) * w, one CTA per row.
 __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float* __restrict__ X, const float* __restrict__ w,
                                                       float eps, int h, RowOut out) {
@@ -435,8 +507,90 @@ static cudaError_t attention(const Model& m, cudaStream_t s, const KV* Ks, const
   return cudaSuccess;
 }
 
+// FFN half of a layer over n rows, residual in m.s.X: RMSNorm -> SwiGLU GEMMs
+// (+residual), or router softmax / top-k -> rows grouped by expert -> grouped
+// expert GEMMs -> weighted combine (+residual).  start: position of row 0 for
+// the router trace; trace = false records nothing.
+template <typename TW>
+static cudaError_t ffn_rows(const Model& m, cudaStream_t s, const LayerPtrs& L, int l, int n, int start, bool trace) {
+  const dec_config& c = m.cfg;
+  const Scratch& S = m.s;
+  cudaError_t err = cudaSuccess;
+  auto chk = [&err](cudaError_t e) {
+    if (err == cudaSuccess) err = e;
+  };
+  const int h = c.hidden, f = c.ffn;
+  const bool split = std::is_same<TW, __nv_bfloat16>::value;
+  const Act a_h{S.A, split, n, h};
+  const Act act{S.ACT, split, n, f};
+  if (c.n_experts == 0) {
+    k_rmsnorm_rows<<<n, 256, 0, s>>>(S.X, L.ffn_norm, c.rms_eps, h, a_h.out());
+    count_launch(m);
+    GemmEpi e1{};
+    e1.mode = EPI_SWIGLU;
+    e1.n_out = 2 * f;
+    e1.act = act.base;
+    e1.act_bf16 = split;
+    e1.act_lo = act.out().lo;
+    chk(gemm<TW>(m, s, a_h, (const TW*)L.w_gateup, n, 2 * f, h, e1, 1, n));
+    GemmEpi e2{};
+    e2.mode = EPI_RESID;
+    e2.n_out = h;
+    e2.out_f32 = S.X;
+    chk(gemm<TW>(m, s, act, (const TW*)L.w_down, n, h, f, e2, 1, n));
+    return err;
+  }
+  const int k = c.n_experts_used, E = c.n_experts, entries = n * k;
+  const Act a_sort{S.Asort, split, entries, h};
+  const Act act_sort{S.ACT, split, entries, f};
+  const size_t smr = (64 + MAX_EXPERTS + (size_t)h) * sizeof(float);
+  if (smr > 48 * 1024)
+    cudaFuncSetAttribute(k_router_rows<TW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smr);
+  k_router_rows<TW><<<n, 256, smr, s>>>(S.X, L.ffn_norm, c.rms_eps, (const TW*)L.router, h, E, k, S.pf_ids,
+                                        S.pf_wts, start, trace ? m.trace_ids : nullptr,
+                                        trace ? m.trace_logits : nullptr, m.trace_cap, l);
+  k_moe_plan<<<1, 256, 0, s>>>(S.pf_ids, entries, E, S.pf_offset, S.pf_rows, S.pf_inv);
+  k_rmsnorm_rows<<<n, 256, 0, s>>>(S.X, L.ffn_norm, c.rms_eps, h, a_h.out());
+  count_launch(m, 3);
+  if (split) {
+    const int words = h / 2;  // bf16 row of h elements
+    k_gather_rows<<<entries, 128, 0, s>>>((const uint32_t*)a_h.base, S.pf_rows, k, entries, words,
+                                          (uint32_t*)a_sort.base);
+    k_gather_rows<<<entries, 128, 0, s>>>((const uint32_t*)a_h.lo(), S.pf_rows, k, entries, words,
+                                          (uint32_t*)a_sort.lo());
+    count_launch(m, 2);
+  } else {
+    k_gather_rows<<<entries, 128, 0, s>>>((const uint32_t*)a_h.base, S.pf_rows, k, entries, h,
+                                          (uint32_t*)a_sort.base);
+    count_launch(m);
+  }
+  GemmEpi e1{};
+  e1.mode = EPI_SWIGLU;
+  e1.n_out = 2 * f;
+  e1.act = act_sort.base;
+  e1.act_bf16 = split;
+  e1.act_lo = act_sort.out().lo;
+  e1.group_offset = S.pf_offset;
+  chk(gemm<TW>(m, s, a_sort, (const TW*)L.w_gateup, entries, 2 * f, h, e1, E, n));
+  GemmEpi e2{};
+  e2.mode = EPI_STORE;
+  e2.n_out = h;
+  e2.out_f32 = S.Y;
+  e2.group_offset = S.pf_offset;
+  chk(gemm<TW>(m, s, act_sort, (const TW*)L.w_down, entries, h, f, e2, E, n));
+  k_moe_combine<<<n, 256, 0, s>>>(S.Y, S.pf_inv, S.pf_wts, k, h, S.X);
+  count_launch(m);
+  return err;
+}
+
+// Sequence seq's ring of one layer (ring sets hold n_seqs rings back to back).
+template <typename KV>
+static KV* seq_ring(const Model& m, void* layer_ring, int seq) {
+  return reinterpret_cast<KV*>(reinterpret_cast<char*>(layer_ring) + (size_t)seq * m.ring_bytes);
+}
+
 template <typename TW, typename KV>
-static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int n, int start, float* logits,
+static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n, int start, float* logits,
                                  int32_t* d_argmax) {
   const dec_config& c = m.cfg;
   cudaError_t err = cudaSuccess;
@@ -444,7 +598,7 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int n, int star
     if (err == cudaSuccess) err = e;
   };
   const Scratch& S = m.s;
-  const int h = c.hidden, hd = c.head_dim, qd = c.n_heads * hd, kd = c.n_kv_heads * hd, f = c.ffn;
+  const int h = c.hidden, hd = c.head_dim, qd = c.n_heads * hd, kd = c.n_kv_heads * hd;
   const int half = hd / 2;
   // bf16 weights: activations reach the tensor cores as bf16 (hi, lo) pairs;
   // f32 weights: f32 rows for the SIMT GEMM.  Both keep ~fp32 activations.
@@ -460,16 +614,17 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int n, int star
 
   const Act a_h{S.A, split, n, h};      // normalised rows
   const Act a_q{S.A, split, n, qd};     // attention output rows
-  const Act act{S.ACT, split, n, f};    // dense SwiGLU activations
 
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerPtrs& L = m.layers[l];
+    KV* kc = seq_ring<KV>(m, L.kc, seq);
+    KV* vc = seq_ring<KV>(m, L.vc, seq);
     k_rmsnorm_rows<<<n, 256, 0, s>>>(S.X, L.attn_norm, c.rms_eps, h, a_h.out());
     count_launch(m);
-    KV* kdst = direct ? (KV*)L.kc : (KV*)S.KVlin_k;
-    KV* vdst = direct ? (KV*)L.vc : (KV*)S.KVlin_v;
+    KV* kdst = direct ? kc : (KV*)S.KVlin_k;
+    KV* vdst = direct ? vc : (KV*)S.KVlin_v;
     if (!direct && hist > 0) {
-      k_kv_gather<KV><<<152, 256, 0, s>>>((const KV*)L.kc, (const KV*)L.vc, c.max_seq, kd, h0, hist, kdst, vdst);
+      k_kv_gather<KV><<<152, 256, 0, s>>>(kc, vc, c.max_seq, kd, h0, hist, kdst, vdst);
       count_launch(m);
     }
     {
@@ -496,8 +651,7 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int n, int star
     chk(attention<KV>(m, s, kdst, vdst, direct ? 0 : h0, start, n, a_q.out()));
     if (!direct) {
       const int t_first = n > c.max_seq ? n - c.max_seq : 0;
-      k_kv_commit<KV><<<152, 256, 0, s>>>(kdst, vdst, hist, start, t_first, n, c.max_seq, kd, (KV*)L.kc,
-                                          (KV*)L.vc);
+      k_kv_commit<KV><<<152, 256, 0, s>>>(kdst, vdst, hist, start, t_first, n, c.max_seq, kd, kc, vc);
       count_launch(m);
     }
     {
@@ -507,74 +661,113 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int n, int star
       e.out_f32 = S.X;
       chk(gemm<TW>(m, s, a_q, (const TW*)L.wo, n, h, qd, e, 1, n));
     }
-    if (c.n_experts == 0) {
-      k_rmsnorm_rows<<<n, 256, 0, s>>>(S.X, L.ffn_norm, c.rms_eps, h, a_h.out());
-      count_launch(m);
-      GemmEpi e1{};
-      e1.mode = EPI_SWIGLU;
-      e1.n_out = 2 * f;
-      e1.act = act.base;
-      e1.act_bf16 = split;
-      e1.act_lo = act.out().lo;
-      chk(gemm<TW>(m, s, a_h, (const TW*)L.w_gateup, n, 2 * f, h, e1, 1, n));
-      GemmEpi e2{};
-      e2.mode = EPI_RESID;
-      e2.n_out = h;
-      e2.out_f32 = S.X;
-      chk(gemm<TW>(m, s, act, (const TW*)L.w_down, n, h, f, e2, 1, n));
-    } else {
-      const int k = c.n_experts_used, E = c.n_experts, entries = n * k;
-      const Act a_sort{S.Asort, split, entries, h};
-      const Act act_sort{S.ACT, split, entries, f};
-      const size_t smr = (64 + MAX_EXPERTS + (size_t)h) * sizeof(float);
-      if (smr > 48 * 1024)
-        cudaFuncSetAttribute(k_router_rows<TW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smr);
-      k_router_rows<TW><<<n, 256, smr, s>>>(S.X, L.ffn_norm, c.rms_eps, (const TW*)L.router, h, E, k, S.pf_ids,
-                                            S.pf_wts, start, m.trace_ids, m.trace_logits, m.trace_cap, l);
-      k_moe_plan<<<1, 256, 0, s>>>(S.pf_ids, entries, E, S.pf_offset, S.pf_rows, S.pf_inv);
-      k_rmsnorm_rows<<<n, 256, 0, s>>>(S.X, L.ffn_norm, c.rms_eps, h, a_h.out());
-      count_launch(m, 3);
-      if (split) {
-        const int words = h / 2;  // bf16 row of h elements
-        k_gather_rows<<<entries, 128, 0, s>>>((const uint32_t*)a_h.base, S.pf_rows, k, entries, words,
-                                              (uint32_t*)a_sort.base);
-        k_gather_rows<<<entries, 128, 0, s>>>((const uint32_t*)a_h.lo(), S.pf_rows, k, entries, words,
-                                              (uint32_t*)a_sort.lo());
-        count_launch(m, 2);
-      } else {
-        k_gather_rows<<<entries, 128, 0, s>>>((const uint32_t*)a_h.base, S.pf_rows, k, entries, h,
-                                              (uint32_t*)a_sort.base);
-        count_launch(m);
-      }
-      GemmEpi e1{};
-      e1.mode = EPI_SWIGLU;
-      e1.n_out = 2 * f;
-      e1.act = act_sort.base;
-      e1.act_bf16 = split;
-      e1.act_lo = act_sort.out().lo;
-      e1.group_offset = S.pf_offset;
-      chk(gemm<TW>(m, s, a_sort, (const TW*)L.w_gateup, entries, 2 * f, h, e1, E, n));
-      GemmEpi e2{};
-      e2.mode = EPI_STORE;
-      e2.n_out = h;
-      e2.out_f32 = S.Y;
-      e2.group_offset = S.pf_offset;
-      chk(gemm<TW>(m, s, act_sort, (const TW*)L.w_down, entries, h, f, e2, E, n));
-      k_moe_combine<<<n, 256, 0, s>>>(S.Y, S.pf_inv, S.pf_wts, k, h, S.X);
-      count_launch(m);
-    }
+    chk(ffn_rows<TW>(m, s, L, l, n, start, seq == 0));
   }
   if (logits || d_argmax) launch_lmhead(m, s, S.X + (size_t)(n - 1) * h, logits, d_argmax);
   return err;
 }
 
-cudaError_t launch_prefill_chunk(const Model& m, cudaStream_t s, int n, int start, float* logits,
+cudaError_t launch_prefill_chunk(const Model& m, cudaStream_t s, int seq, int n, int start, float* logits,
                                  int32_t* d_argmax) {
   const bool wb = m.cfg.weight_dtype == DEC_BF16, kb = m.cfg.kv_dtype == DEC_BF16;
-  if (wb && kb) return prefill_chunk<__nv_bfloat16, __nv_bfloat16>(m, s, n, start, logits, d_argmax);
-  if (wb) return prefill_chunk<__nv_bfloat16, float>(m, s, n, start, logits, d_argmax);
-  if (kb) return prefill_chunk<float, __nv_bfloat16>(m, s, n, start, logits, d_argmax);
-  return prefill_chunk<float, float>(m, s, n, start, logits, d_argmax);
+  if (wb && kb) return prefill_chunk<__nv_bfloat16, __nv_bfloat16>(m, s, seq, n, start, logits, d_argmax);
+  if (wb) return prefill_chunk<__nv_bfloat16, float>(m, s, seq, n, start, logits, d_argmax);
+  if (kb) return prefill_chunk<float, __nv_bfloat16>(m, s, seq, n, start, logits, d_argmax);
+  return prefill_chunk<float, float>(m, s, seq, n, start, logits, d_argmax);
+}
+
+// ---------------------------------------------------------------------------
+// Batched decode (Pantheon "Llama Forward Pass", Batched Multi-Sequence
+// Decode): B rows, row b one token of sequence b_seq[b] at position b_pos[b].
+// The projections, FFN/MoE and LM head are the prefill GEMMs over the B rows
+// (each weight matrix read once per step for every row); RoPE uses each row's
+// own position; the QKV epilogue writes row b's K/V into row b_rows[b] of the
+// layer's ring set (its sequence's ring, slot of its position); attention is
+// per row over its own sequence (attn_rows.cu).  No kernel mixes rows except
+// through per-row-independent arithmetic, so a row's result does not depend
+// on the batch.
+
+template <typename TW, typename KV>
+static cudaError_t decode_rows(const Model& m, cudaStream_t s, int B, float* logits, int32_t* d_argmax) {
+  const dec_config& c = m.cfg;
+  cudaError_t err = cudaSuccess;
+  auto chk = [&err](cudaError_t e) {
+    if (err == cudaSuccess) err = e;
+  };
+  const Scratch& S = m.s;
+  const int h = c.hidden, hd = c.head_dim, qd = c.n_heads * hd, kd = c.n_kv_heads * hd;
+  const bool split = std::is_same<TW, __nv_bfloat16>::value;
+  k_embed_rows<TW><<<B, 128, 0, s>>>((const TW*)m.tok_embd, S.tokens, h, S.X);
+  count_launch(m);
+  const Act a_h{S.A, split, B, h};
+  const Act a_q{S.A, split, B, qd};
+  const int nsplit = attn_rows_splits(c);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerPtrs& L = m.layers[l];
+    k_rmsnorm_rows<<<B, 256, 0, s>>>(S.X, L.attn_norm, c.rms_eps, h, a_h.out());
+    count_launch(m);
+    {
+      GemmEpi e{};
+      e.mode = EPI_QKV;
+      e.n_out = qd + 2 * kd;
+      e.bias = L.bqkv;
+      e.rope = S.rope_tab;
+      e.qd = qd;
+      e.kd = kd;
+      e.hd = hd;
+      e.q_out = S.Q;
+      e.k_dst = L.kc;
+      e.v_dst = L.vc;
+      e.kv_bf16 = std::is_same<KV, __nv_bfloat16>::value;
+      e.kv_rows = S.b_rows;
+      chk(gemm<TW>(m, s, a_h, (const TW*)L.wqkv, B, qd + 2 * kd, h, e, 1, B));
+    }
+    timer_begin(m, DEC_K_ATTN, s);
+    launch_attn_rows(c, S.Q, L.kc, L.vc, m.ring_bytes, S.b_seq, S.b_pos, B, nsplit, S.b_part, a_q.out(), s);
+    timer_end(m, DEC_K_ATTN, s);
+    count_launch(m, 2);
+    {
+      GemmEpi e{};
+      e.mode = EPI_RESID;
+      e.n_out = h;
+      e.out_f32 = S.X;
+      chk(gemm<TW>(m, s, a_q, (const TW*)L.wo, B, h, qd, e, 1, B));
+    }
+    chk(ffn_rows<TW>(m, s, L, l, B, 0, false));
+  }
+  // Final RMSNorm and the LM head over every row.
+  k_rmsnorm_rows<<<B, 256, 0, s>>>(S.X, m.out_norm, c.rms_eps, h, a_h.out());
+  count_launch(m);
+  {
+    GemmEpi e{};
+    e.mode = EPI_STORE;
+    e.n_out = c.vocab;
+    e.out_f32 = logits;
+    chk(gemm<TW>(m, s, a_h, (const TW*)m.head, B, c.vocab, h, e, 1, B));
+  }
+  if (d_argmax) {
+    k_argmax_rows<<<B, 1024, 0, s>>>(logits, c.vocab, d_argmax);
+    count_launch(m);
+  }
+  return err;
+}
+
+cudaError_t launch_decode_rows(const Model& m, cudaStream_t s, int B, float* logits, int32_t* d_argmax) {
+  const bool wb = m.cfg.weight_dtype == DEC_BF16, kb = m.cfg.kv_dtype == DEC_BF16;
+  if (wb && kb) return decode_rows<__nv_bfloat16, __nv_bfloat16>(m, s, B, logits, d_argmax);
+  if (wb) return decode_rows<__nv_bfloat16, float>(m, s, B, logits, d_argmax);
+  if (kb) return decode_rows<float, __nv_bfloat16>(m, s, B, logits, d_argmax);
+  return decode_rows<float, float>(m, s, B, logits, d_argmax);
+}
+
+cudaError_t launch_rows_setup(const Model& m, cudaStream_t s, const RowsMeta& meta, const int32_t* d_tokens, int B) {
+  const int half = m.cfg.head_dim / 2;
+  const int n = B * half > B ? B * half : B;
+  const Scratch& S = m.s;
+  k_rows_setup<<<(n + 255) / 256, 256, 0, s>>>(meta, B, d_tokens, m.cfg.vocab, S.inv_freq, half, S.tokens, S.b_seq,
+                                               S.b_pos, S.b_rows, S.rope_tab, S.st);
+  count_launch(m);
+  return cudaGetLastError();
 }
 
 }  // namespace dec

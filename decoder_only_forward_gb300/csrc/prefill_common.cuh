@@ -34,6 +34,7 @@ struct GemmEpi {
   void* v_dst;
   int kv_bf16;
   int kv_row0;
+  const int32_t* kv_rows;  // nullable: row r's K/V go to row kv_rows[r] instead of r + kv_row0
   // Grouped (MoE) GEMMs: rows of group g are [offset[g], offset[g] + count[g]).
   const int32_t* group_offset;   // nullable = one group of all rows
 };
@@ -140,7 +141,8 @@ __device__ __forceinline__ void epi_pair(const GemmEpi& e, int row, int col, flo
         }
       } else {
         const bool is_k = col < e.qd + e.kd;
-        const size_t o = (size_t)(row + e.kv_row0) * e.kd + (is_k ? col - e.qd : col - e.qd - e.kd);
+        const size_t kr = e.kv_rows ? (size_t)e.kv_rows[row] : (size_t)(row + e.kv_row0);
+        const size_t o = kr * e.kd + (is_k ? col - e.qd : col - e.qd - e.kd);
         void* dst = is_k ? e.k_dst : e.v_dst;
         if (e.kv_bf16) store_pair(reinterpret_cast<__nv_bfloat16*>(dst) + o, v0, v1);
         else store_pair(reinterpret_cast<float*>(dst) + o, v0, v1);

@@ -82,6 +82,11 @@ struct Scratch {
   float* Y;             // [T*k][h] per-(row, slot) expert outputs (MoE)
   void* ACT;            // [T*k][ffn] gate/up output rows (A operand of down)
   AttnTcPlanes at;      // at.Kb == nullptr: this configuration takes the SIMT attention
+  // batched decode (rows = sequences of one step)
+  int32_t* b_seq;       // [MAX_BATCH] sequence of each row
+  int32_t* b_pos;       // [MAX_BATCH] position of each row
+  int32_t* b_rows;      // [MAX_BATCH] K/V row of each row: seq * ring_rows + slot(pos)
+  float* b_part;        // [MAX_BATCH][nq][AR_MAX_SPLIT][hd+2] attention split partials
 };
 
 constexpr int LM_GRID_MAX = 1024;
@@ -90,6 +95,8 @@ constexpr int MAX_EXPERTS_USED = 8;
 constexpr int MAX_KV_HEADS = 192;
 constexpr int MAX_GROUP = 16;     // query heads per kv head
 constexpr int NUM_COUNTERS = 256;
+constexpr int MAX_BATCH = 256;    // rows of one batched decode step (also <= max_tokens)
+constexpr int AR_MAX_SPLIT = 16;  // key splits per kv head in batched decode attention
 
 // Optional CUDA-event pairs recorded around every launch of one kernel class
 // (dec_timing_enable); also captured into the decode graph.
@@ -125,6 +132,10 @@ struct Model {
   int trace_cap;
   void* ws;             // workspace base
   size_t ws_bytes;
+  int n_seqs;           // sequences whose KV rings the workspace holds
+  int ring_rows;        // rows of one sequence's ring (max_seq rounded up to 64)
+  size_t ring_bytes;    // bytes of one sequence's K (or V) ring of one layer
+  int num_sms;
 };
 
 // Workspace plan: byte offsets of every region; total size.
@@ -136,8 +147,12 @@ struct WsPlan {
   size_t wqkv_perm, bqkv_perm;  // kHalf RoPE: q/k rows permuted per head
   size_t mk_layers;     // layer table of the persistent decode kernel
   size_t mk_maps;       // its weight tensor maps
-  size_t kv;            // start of the KV rings
-  size_t kv_layer_bytes;
+  size_t b_seq, b_pos, b_rows, b_part;  // batched decode
+  size_t kv;            // start of the KV rings: [layer][K, V][seq][ring_rows][n_kv*hd]
+  size_t kv_layer_bytes; // one layer's K (or V) rings of every sequence
+  size_t ring_bytes;    // one sequence's ring
+  int ring_rows;
+  int n_seqs;
   size_t total;
   int nsplit;
   int attn_sps;
@@ -189,8 +204,29 @@ void launch_lmhead(const Model& m, cudaStream_t s, const float* x, float* logits
 // the last row's logits when logits != nullptr.  wrap_mode: K/V go through the
 // linear scratch and are committed afterwards (needed once the ring may wrap).
 // Returns the first launch-setup error (a tensor map the driver rejects, ...).
-cudaError_t launch_prefill_chunk(const Model& m, cudaStream_t s, int n, int start, float* logits,
+// seq: the sequence whose rings the chunk reads and writes.
+cudaError_t launch_prefill_chunk(const Model& m, cudaStream_t s, int seq, int n, int start, float* logits,
                                  int32_t* d_argmax);
+// One batched decode step over B rows: token ids in m.s.tokens, sequences,
+// positions and K/V rows in m.s.b_seq / b_pos / b_rows (device).  Writes
+// logits [B][vocab] and, when d_argmax is given, each row's argmax.
+cudaError_t launch_decode_rows(const Model& m, cudaStream_t s, int B, float* logits, int32_t* d_argmax);
+// Its setup: per-row sequence, position and K/V row into m.s.b_*, token ids
+// from d_tokens (checked) and each row's RoPE (cos, sin).
+struct RowsMeta {
+  int32_t seq[MAX_BATCH];
+  int32_t pos[MAX_BATCH];
+  int32_t rows[MAX_BATCH];   // seq * ring_rows + slot(pos)
+};
+cudaError_t launch_rows_setup(const Model& m, cudaStream_t s, const RowsMeta& meta, const int32_t* d_tokens, int B);
+
+struct RowOut;
+// Batched decode attention (attn_rows.cu): rotated queries Q [B][nq*hd] f32,
+// the layer's ring sets kc/vc (sequence s at s * ring_bytes).
+int attn_rows_splits(const dec_config& c);
+void launch_attn_rows(const dec_config& c, const float* Q, const void* kc, const void* vc, size_t ring_bytes,
+                      const int32_t* seq, const int32_t* pos, int B, int nsplit, float* part, RowOut out,
+                      cudaStream_t s);
 
 inline void count_launch(const Model& m, int n = 1) { *m.launches += n; }
 

@@ -28,7 +28,8 @@ STATUS_NAMES = {0: "DEC_OK", 1: "DEC_EINVAL", 2: "DEC_ERANGE", 3: "DEC_ECUDA", 4
 EXPORTED = ["dec_config_validate", "dec_workspace_bytes", "dec_create", "dec_prefill", "dec_decode",
             "dec_decode_dev", "dec_kv_reset", "dec_length", "dec_kv_layer", "dec_set_trace",
             "dec_check", "dec_timing_enable", "dec_timing_read", "dec_launch_count", "dec_destroy",
-            "dec_last_error", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc", "dec_gemm_bf16", "dec_set_graph", "dec_set_fused", "dec_fused_available", "dec_fused_mode", "dec_phase_stamps"]
+            "dec_last_error", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc", "dec_gemm_bf16", "dec_set_graph", "dec_set_fused", "dec_fused_available", "dec_fused_mode", "dec_phase_stamps",
+            "dec_prefill_seq", "dec_kv_reset_seq", "dec_length_seq", "dec_decode_batch", "dec_kv_layer_seq"]
 
 KERNEL_CLASSES = {"qkv": 1, "attn": 2, "oproj": 3, "gateup": 4, "down": 5, "lmhead": 6, "router": 7,
                   "pf_gemm": 8, "pf_attn": 9, "step": 10}
@@ -42,7 +43,7 @@ class Config(ctypes.Structure):
         ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("rope_llama3", ctypes.c_int32),
         ("rope_factor", ctypes.c_float), ("rope_low_freq_factor", ctypes.c_float),
         ("rope_high_freq_factor", ctypes.c_float), ("rope_orig_ctx", ctypes.c_int32),
-        ("rope_half", ctypes.c_int32), ("rope_dim", ctypes.c_int32)]
+        ("rope_half", ctypes.c_int32), ("rope_dim", ctypes.c_int32), ("n_seqs", ctypes.c_int32)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -86,6 +87,11 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "dec_fused_mode": (I32, [P]),
         "dec_phase_stamps": (I32, [P, P, I32]),
         "dec_last_error": (ctypes.c_char_p, [P]),
+        "dec_prefill_seq": (I32, [P, I32, ctypes.POINTER(I32), I32, I32, P, P]),
+        "dec_kv_reset_seq": (I32, [P, I32]),
+        "dec_length_seq": (I32, [P, I32]),
+        "dec_decode_batch": (I32, [P, I32, ctypes.POINTER(I32), ctypes.POINTER(I32), P, P, P]),
+        "dec_kv_layer_seq": (I32, [P, I32, I32, ctypes.POINTER(P), ctypes.POINTER(P)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -103,7 +109,7 @@ class DecError(RuntimeError):
         self.status = status
 
 
-def make_config(w: dict, kv_dtype: str = "f32", max_tokens: int = 0) -> Config:
+def make_config(w: dict, kv_dtype: str = "f32", max_tokens: int = 0, n_seqs: int = 0) -> Config:
     c = Config()
     for k in ("n_layers", "hidden", "n_heads", "n_kv_heads", "head_dim", "ffn", "vocab",
               "n_experts", "n_experts_used", "max_seq", "sliding_window"):
@@ -124,6 +130,7 @@ def make_config(w: dict, kv_dtype: str = "f32", max_tokens: int = 0) -> Config:
         c.rope_orig_ctx = int(l3["orig_ctx"])
     c.rope_half = int(bool(w.get("rope_half", False)))
     c.rope_dim = int(w.get("rope_dim", 0))
+    c.n_seqs = int(n_seqs)
     return c
 
 
@@ -233,11 +240,12 @@ class Decoder:
     """A handle of the library: weights, workspace (KV cache + scratch) and a stream."""
 
     def __init__(self, w: dict, weights: Optional[DeviceWeights] = None, device="cuda", seed: int = 1234,
-                 kv_dtype: str = "f32", max_tokens: int = 0, stream: Optional[torch.cuda.Stream] = None):
+                 kv_dtype: str = "f32", max_tokens: int = 0, stream: Optional[torch.cuda.Stream] = None,
+                 n_seqs: int = 0):
         self.w = w
         self.device = torch.device(device)
         self.weights = weights if weights is not None else DeviceWeights(w, device, seed)
-        self.cfg = make_config(w, kv_dtype, max_tokens)
+        self.cfg = make_config(w, kv_dtype, max_tokens, n_seqs)
         st, msg = validate(self.cfg)
         if st != DEC_OK:
             raise DecError(st, msg)
@@ -258,15 +266,28 @@ class Decoder:
             raise DecError(st, lib.dec_last_error(self.h).decode())
 
     def prefill(self, tokens, start_pos: int, logits: Optional[torch.Tensor],
-                d_argmax: Optional[torch.Tensor] = None) -> None:
-        """``tokens``: a host sequence of ids, or a pinned host int32 tensor (copied as is)."""
+                d_argmax: Optional[torch.Tensor] = None, seq: int = 0) -> None:
+        """``tokens``: a host sequence of ids, or a pinned host int32 tensor (copied as is).
+        ``seq``: the sequence whose KV rings are used (dec_prefill_seq)."""
         if isinstance(tokens, torch.Tensor):
             assert tokens.device.type == "cpu" and tokens.dtype == torch.int32 and tokens.is_contiguous()
             p, n = ctypes.cast(tokens.data_ptr(), ctypes.POINTER(ctypes.c_int32)), tokens.numel()
         else:
             a = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
             p, n = a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), a.size
-        self._raise(lib.dec_prefill(self.h, p, int(n), int(start_pos), _ptr(logits), _ptr(d_argmax)))
+        self._raise(lib.dec_prefill_seq(self.h, int(seq), p, int(n), int(start_pos), _ptr(logits), _ptr(d_argmax)))
+
+    def decode_batch(self, seqs, positions, d_tokens: torch.Tensor, logits: torch.Tensor,
+                     d_argmax: Optional[torch.Tensor] = None) -> None:
+        """One batched decode step (dec_decode_batch): host ``seqs``/``positions`` (B each), device int32
+        ``d_tokens`` [B], device f32 ``logits`` [B, vocab], optional device int32 ``d_argmax`` [B]."""
+        sq = np.ascontiguousarray(np.asarray(seqs, dtype=np.int32))
+        ps = np.ascontiguousarray(np.asarray(positions, dtype=np.int32))
+        if sq.size != ps.size:
+            raise ValueError("seqs and positions must have the same length")
+        I32P = ctypes.POINTER(ctypes.c_int32)
+        self._raise(lib.dec_decode_batch(self.h, int(sq.size), sq.ctypes.data_as(I32P), ps.ctypes.data_as(I32P),
+                                         d_tokens.data_ptr(), logits.data_ptr(), _ptr(d_argmax)))
 
     @property
     def launch_count(self) -> int:
@@ -306,17 +327,21 @@ class Decoder:
     def set_graph(self, enable: bool) -> None:
         self._raise(lib.dec_set_graph(self.h, int(bool(enable))))
 
-    def kv_reset(self) -> None:
-        self._raise(lib.dec_kv_reset(self.h))
+    def kv_reset(self, seq: int = 0) -> None:
+        self._raise(lib.dec_kv_reset_seq(self.h, int(seq)))
 
     @property
     def length(self) -> int:
         return int(lib.dec_length(self.h))
 
-    def kv_layer(self, layer: int):
-        """(K, V) rings of a layer as [max_seq, n_kv_heads, head_dim] views of the workspace."""
+    def length_of(self, seq: int) -> int:
+        return int(lib.dec_length_seq(self.h, int(seq)))
+
+    def kv_layer(self, layer: int, seq: int = 0):
+        """(K, V) rings of a layer (of sequence ``seq``) as [max_seq, n_kv_heads, head_dim] views of the
+        workspace."""
         k, v = ctypes.c_void_p(), ctypes.c_void_p()
-        self._raise(lib.dec_kv_layer(self.h, int(layer), ctypes.byref(k), ctypes.byref(v)))
+        self._raise(lib.dec_kv_layer_seq(self.h, int(layer), int(seq), ctypes.byref(k), ctypes.byref(v)))
         base = self.workspace.data_ptr()
         es = 4 if self.kv_torch_dtype == torch.float32 else 2
         n = self.w["max_seq"] * self.w["n_kv_heads"] * self.w["head_dim"]

@@ -85,6 +85,11 @@ typedef struct dec_config {
   int32_t rope_dim;       /* rotary width: only the first rope_dim dims of a head turn, the rest
                              pass through (sipllm partial-rotary rope_rot); 0 = head_dim; even,
                              <= head_dim.  inv_freq_i = theta^(-2i/rope_dim) */
+  int32_t n_seqs;         /* independent sequences whose KV rings the workspace holds (0 = 1): each
+                             has its own positions and length.  dec_prefill / dec_decode /
+                             dec_kv_reset act on sequence 0; dec_prefill_seq, dec_kv_reset_seq and
+                             dec_decode_batch on any (Pantheon "Llama Forward Pass", Batched
+                             Multi-Sequence Decode: a KV cache and position per sequence) */
 } dec_config;
 
 /*
@@ -165,9 +170,42 @@ dec_status dec_kv_reset(dec_handle *h);
 /* Number of positions currently in the cache (host-side bookkeeping). */
 int32_t dec_length(const dec_handle *h);
 
+/* Sequence-addressed forms of dec_prefill, dec_kv_reset and dec_length:
+ * seq in [0, n_seqs) selects whose KV rings are read and written; the rules of
+ * the plain calls apply per sequence.  DEC_EINVAL for seq out of range
+ * (dec_length_seq returns -1). */
+dec_status dec_prefill_seq(dec_handle *h, int32_t seq, const int32_t *tokens, int32_t n, int32_t start_pos,
+                           float *logits, int32_t *d_argmax);
+dec_status dec_kv_reset_seq(dec_handle *h, int32_t seq);
+int32_t dec_length_seq(const dec_handle *h, int32_t seq);
+
+/* Batched decode: one step of `batch` independent sequences, row i being token
+ * d_tokens[i] of sequence seqs[i] at position positions[i] (Pantheon "Llama
+ * Forward Pass", Batched Multi-Sequence Decode: each sequence keeps its own KV
+ * cache and position and attends only to its own keys; one weight read serves
+ * every row, the throughput lever named under "Future work" of sipllm
+ * "Transformer forward pass").  Projections, FFN/MoE and the LM head run as
+ * tensor-core GEMMs over the rows (the prefill kernels).  A row's result is
+ * bit-identical whatever the other rows, its place in the batch or the batch
+ * size; against dec_decode it agrees to rounding (different kernels).
+ *   batch: 1 <= batch <= min(max_tokens, 256).
+ *   seqs, positions: host, batch entries; sequences distinct, in [0, n_seqs);
+ *     each position obeys the dec_decode rules for its sequence.
+ *   d_tokens: device, batch int32 ids in [0, vocab) (a device id outside is
+ *     replaced by 0 and reported by dec_check as DEC_EINVAL).
+ *   logits: device [batch][vocab] f32, row i for row i.
+ *   d_argmax: device [batch] int32 or NULL: each row's argmax (ties -> lower id).
+ * Errors (host-side, before anything is enqueued or any length changes):
+ * DEC_EINVAL, DEC_ERANGE; DEC_ECUDA from a launch. */
+dec_status dec_decode_batch(dec_handle *h, int32_t batch, const int32_t *seqs, const int32_t *positions,
+                            const int32_t *d_tokens, float *logits, int32_t *d_argmax);
+
 /* Device pointers to layer's K and V rings, each [max_seq][n_kv_heads][head_dim]
  * of kv_dtype; position p lives in slot p % max_seq under a window, else slot p. */
 dec_status dec_kv_layer(const dec_handle *h, int32_t layer, void **k, void **v);
+
+/* The same for sequence seq in [0, n_seqs) (dec_kv_layer is sequence 0). */
+dec_status dec_kv_layer_seq(const dec_handle *h, int32_t layer, int32_t seq, void **k, void **v);
 
 /* Optional MoE trace for testing: when d_ids/d_logits are non-NULL, every
  * later MoE layer records, for position p, its selected expert ids

@@ -111,3 +111,22 @@ def test_create_rejects_bad_arguments_without_gpu(dec):
     st = dec.lib.dec_create(ctypes.byref(c), None, None, 0, None, ctypes.byref(h))
     assert st == dec.DEC_EINVAL and not h.value
     assert b"weights" in dec.lib.dec_last_error(None)
+
+
+def test_workspace_grows_by_one_kv_ring_set_per_sequence(dec):
+    w = synthetic.workload("mistral-7b")
+    base = dec.workspace_bytes(dec.make_config(w, "f32"))
+    rows = (w["max_seq"] + 63) // 64 * 64
+    ring_set = 2 * w["n_layers"] * rows * w["n_kv_heads"] * w["head_dim"] * 4
+    for n in (2, 5):
+        assert dec.workspace_bytes(dec.make_config(w, "f32", n_seqs=n)) - base == (n - 1) * ring_set
+    assert dec.workspace_bytes(dec.make_config(w, "f32", n_seqs=1)) == base
+
+
+def test_n_seqs_checked(dec):
+    c = dec.make_config(synthetic.workload("toy"))
+    c.n_seqs = -1
+    st, msg = dec.validate(c)
+    assert st == dec.DEC_EINVAL and "n_seqs" in msg
+    c.n_seqs = 8
+    assert dec.validate(c)[0] == dec.DEC_OK
