@@ -100,6 +100,21 @@ def decode_bytes(w: dict, pos: int, kv_es: int) -> float:
     return w["n_layers"] * (per_layer + kv) + b["lmhead"] + b["embed_row"] + 4 * w["hidden"]
 
 
+def batched_step_bytes(w: dict, positions, kv_es: int) -> float:
+    """HBM bytes of one batched decode step: every weight matrix once (all experts for a MoE, an
+    upper bound: a batch of rows usually touches every expert), the LM head, one embedding row and
+    each row's readable K/V."""
+    b = weight_bytes(w)
+    E = w["n_experts"]
+    ffn = (b["gateup"] + b["down"]) * (E // w["n_experts_used"] if E else 1)
+    per_layer = b["qkv"] + b["oproj"] + ffn + b["router"] + 2 * 4 * w["hidden"]
+    kv = 0
+    for pos in positions:
+        m = min(pos + 1, w["max_seq"]) if w["sliding_window"] > 0 else pos + 1
+        kv += 2 * w["n_kv_heads"] * w["head_dim"] * m * kv_es
+    return w["n_layers"] * per_layer + w["n_layers"] * kv + b["lmhead"] + len(positions) * b["embed_row"]
+
+
 def prefill_flops(w: dict, P: int) -> float:
     h, f, hd = w["hidden"], w["ffn"], w["head_dim"]
     qd, kd = w["n_heads"] * hd, w["n_kv_heads"] * hd
@@ -367,6 +382,56 @@ def run_ours(args, rank, world, local_rank):
             "cpu_baseline": cpu,
             "wall_s_timed": round(wall, 3),
         }
+    if rank == 0 and args.batch > 0:
+        out["batched_decode"] = run_batched(args, w, d.weights, dev, kv_es)
+    d.close()
+    return out
+
+
+def run_batched(args, w, weights, dev, kv_es):
+    """Batched multi-sequence decode: ``args.batch`` sequences, each prefilled with its own prompt of
+    the workload's length, then greedy steps of all of them at once (dec_decode_batch, tokens fed
+    back from the device argmax).  Inputs exceed L2 (weights and the sequences' K/V), so no flush."""
+    from decoder_only_forward_gb300 import dec
+    B, P, V = args.batch, w["prompt"], w["vocab"]
+    if w["sliding_window"] == 0 and P + 3 + args.batch_steps > w["max_seq"]:
+        return {"skipped": "the cache cannot hold the prompt plus the timed steps"}
+    d = dec.Decoder(w, weights=weights, device=dev, kv_dtype=args.kv, n_seqs=B)
+    lg = torch.empty(V, dtype=torch.float32, device=dev)
+    for sq in range(B):
+        d.prefill(synthetic.prompt_tokens(w, P, seed=100 + sq), 0, lg, seq=sq)
+    seqs = list(range(B))
+    tok = torch.zeros(B, dtype=torch.int32, device=dev)
+    logits = torch.empty((B, V), dtype=torch.float32, device=dev)
+    pos = P
+    for _ in range(3):
+        d.decode_batch(seqs, [pos] * B, tok, logits, tok)
+        pos += 1
+    d.check()
+    K = args.batch_steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    launches0 = d.launch_count
+    e0.record(d.stream)
+    for i in range(K):
+        d.decode_batch(seqs, [pos + i] * B, tok, logits, tok)
+    e1.record(d.stream)
+    torch.cuda.synchronize(dev)
+    launches = d.launch_count - launches0
+    ms = e0.elapsed_time(e1) / K
+    nbytes = sum(batched_step_bytes(w, [pos + i] * B, kv_es) for i in range(K)) / K
+    # Attribution: the attention kernels' share of one step.
+    d.timing_enable("attn", 4 * w["n_layers"])
+    d.decode_batch(seqs, [pos + K] * B, tok, logits, tok)
+    attn_ms, n_attn = d.timing_read()
+    d.timing_enable("attn", 0)
+    d.check()
+    hbm = peaks()[0]
+    out = {"batch": B, "steps": K, "tok_s": round(B * 1e3 / ms, 1), "ms_per_step": round(ms, 4),
+           "bytes_per_step": int(nbytes), "hbm_frac": round(nbytes / (ms / 1e3) / (hbm * 1e9), 4),
+           "attn_ms_per_step": round(attn_ms, 4), "gpu_launches_per_step": int(launches / K),
+           "note": "each sequence prefilled with its own prompt; one CUDA graph per step; bytes count every "
+                   "weight once plus each row's readable K/V"}
     d.close()
     return out
 
@@ -438,6 +503,9 @@ def main():
                     help="decode schedule: per-layer kernels, or the persistent one-kernel step over every SM "
                          "or on one thread-block cluster (default: the handle's own choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=16,
+                    help="also time batched multi-sequence decode at this batch (0: skip)")
+    ap.add_argument("--batch-steps", type=int, default=32)
     ap.add_argument("--profile", type=int, default=0, metavar="D",
                     help="profiling driver: one prefill + D decode steps, kernels launched one by one "
                          "(no graph, no timing passes, no JSON); for per-kernel profilers")

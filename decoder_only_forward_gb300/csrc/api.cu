@@ -30,6 +30,16 @@ struct dec_handle {
   int64_t launches = 0;
   Timing timing;
   std::vector<cudaEvent_t> events;
+  // batched decode graph, captured for one (batch, tokens, logits, argmax)
+  cudaGraphExec_t bgraph = nullptr;
+  cudaGraph_t bgraph_src = nullptr;
+  cudaGraphNode_t bgraph_setup = nullptr;
+  int bgraph_batch = 0;
+  const int32_t* bgraph_tokens = nullptr;
+  float* bgraph_logits = nullptr;
+  int32_t* bgraph_argmax = nullptr;
+  int bgraph_timed_pairs = 0;
+  int64_t bgraph_kernels = 0;
   bool use_graph = true;
   int fused_mode = 1;   // DEC_FUSED_*
 };
@@ -40,6 +50,11 @@ static void drop_graph(dec_handle* h) {
   h->graph = nullptr;
   h->graph_src = nullptr;
   h->graph_step_node = nullptr;
+  if (h->bgraph) cudaGraphExecDestroy(h->bgraph);
+  if (h->bgraph_src) cudaGraphDestroy(h->bgraph_src);
+  h->bgraph = nullptr;
+  h->bgraph_src = nullptr;
+  h->bgraph_setup = nullptr;
 }
 
 static void timing_start(dec_handle* h) { h->timing.n = 0; }
@@ -203,6 +218,16 @@ WsPlan dec::plan_workspace(const dec_config& c) {
   p.b_pos = take(4 * (size_t)MAX_BATCH);
   p.b_rows = take(4 * (size_t)MAX_BATCH);
   p.b_part = take(4 * (size_t)bmax * c.n_heads * AR_MAX_SPLIT * (hd + 2));
+  // Split-K partials of the tensor-core GEMMs (bf16 weights): room for 8 splits
+  // of one 128-row tile of the widest GEMM, at most 128 MB; a GEMM takes only
+  // the splits that fit.
+  size_t nmax = (size_t)qd + 2 * kd;
+  if ((size_t)c.hidden > nmax) nmax = c.hidden;
+  if (2 * (size_t)c.ffn > nmax) nmax = 2 * (size_t)c.ffn;
+  if ((size_t)c.vocab > nmax) nmax = c.vocab;
+  p.kpart_bytes = c.weight_dtype == DEC_BF16 ? 8 * 128 * nmax * 4 : 0;
+  if (p.kpart_bytes > ((size_t)128 << 20)) p.kpart_bytes = (size_t)128 << 20;
+  p.kpart = take(p.kpart_bytes);
   // KV rings: [layer][K, V][seq][ring_rows][n_kv*hd], ring_rows = max_seq
   // rounded up to 64 rows so every ring starts 256-byte aligned.
   p.n_seqs = c.n_seqs > 0 ? c.n_seqs : 1;
@@ -328,6 +353,8 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
   S.b_pos = (int32_t*)(base + p.b_pos);
   S.b_rows = (int32_t*)(base + p.b_rows);
   S.b_part = (float*)(base + p.b_part);
+  S.kpart = p.kpart_bytes ? (float*)(base + p.kpart) : nullptr;
+  S.kpart_bytes = p.kpart_bytes;
   h->layers.resize(cfg->n_layers);
   for (int l = 0; l < cfg->n_layers; ++l) {
     const dec_layer_weights& L = w->layers[l];
@@ -627,16 +654,70 @@ dec_status dec_decode_batch(dec_handle* h, int32_t batch, const int32_t* seqs, c
     meta.pos[i] = p;
     meta.rows[i] = seqs[i] * h->m.ring_rows + slot;
   }
-  timing_start(h);
-  cudaError_t e = launch_rows_setup(h->m, h->stream, meta, d_tokens, batch);
-  if (e == cudaSuccess) e = launch_decode_rows(h->m, h->stream, batch, logits, d_argmax);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return fail(h, DEC_ECUDA, "batched decode launch: %s", cudaGetErrorString(e));
+  if (h->stream == nullptr || !h->use_graph) {
+    timing_start(h);
+    cudaError_t e = launch_rows_setup(h->m, h->stream, meta, d_tokens, batch);
+    if (e == cudaSuccess) e = launch_decode_rows(h->m, h->stream, batch, logits, d_argmax);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(h, DEC_ECUDA, "batched decode launch: %s", cudaGetErrorString(e));
+    }
+    const dec_status st = cuda_check(h, "batched decode launch");
+    if (st != DEC_OK) return st;
+    timing_finish(h);
+  } else {
+    // One CUDA graph per (batch, tokens, logits, argmax); per step only the
+    // setup node's rows change.
+    if (!h->bgraph || h->bgraph_batch != batch || h->bgraph_tokens != d_tokens || h->bgraph_logits != logits ||
+        h->bgraph_argmax != d_argmax) {
+      if (h->bgraph) cudaGraphExecDestroy(h->bgraph);
+      if (h->bgraph_src) cudaGraphDestroy(h->bgraph_src);
+      h->bgraph = nullptr;
+      h->bgraph_src = nullptr;
+      cudaError_t e = cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeRelaxed);
+      if (e != cudaSuccess) return fail(h, DEC_ECUDA, "begin capture: %s", cudaGetErrorString(e));
+      timing_start(h);
+      const int64_t before = h->launches;
+      cudaError_t le = launch_rows_setup(h->m, h->stream, meta, d_tokens, batch);
+      if (le == cudaSuccess) le = launch_decode_rows(h->m, h->stream, batch, logits, d_argmax);
+      h->bgraph_kernels = h->launches - before;
+      h->launches = before;
+      h->bgraph_timed_pairs = h->timing.n;
+      cudaGraph_t g = nullptr;
+      e = cudaStreamEndCapture(h->stream, &g);
+      if (le != cudaSuccess || e != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        cudaGetLastError();
+        return fail(h, DEC_ECUDA, "batched decode capture: %s",
+                    cudaGetErrorString(le != cudaSuccess ? le : e));
+      }
+      h->bgraph_src = g;
+      cudaGraphNode_t roots[4];
+      size_t nroots = 4;
+      e = cudaGraphGetRootNodes(g, roots, &nroots);
+      if (e != cudaSuccess || nroots != 1) {
+        drop_graph(h);
+        return fail(h, DEC_ECUDA, "batched decode graph: expected one root node (%s)", cudaGetErrorString(e));
+      }
+      h->bgraph_setup = roots[0];
+      e = cudaGraphInstantiate(&h->bgraph, g, 0);
+      if (e != cudaSuccess) {
+        drop_graph(h);
+        return fail(h, DEC_ECUDA, "batched graph instantiate: %s", cudaGetErrorString(e));
+      }
+      h->bgraph_batch = batch;
+      h->bgraph_tokens = d_tokens;
+      h->bgraph_logits = logits;
+      h->bgraph_argmax = d_argmax;
+    }
+    cudaError_t e = update_rows_setup_node(h->bgraph, h->bgraph_setup, h->m, meta, d_tokens, batch);
+    if (e != cudaSuccess) return fail(h, DEC_ECUDA, "batched graph update: %s", cudaGetErrorString(e));
+    e = cudaGraphLaunch(h->bgraph, h->stream);
+    if (e != cudaSuccess) return fail(h, DEC_ECUDA, "batched graph launch: %s", cudaGetErrorString(e));
+    h->timing.n = h->bgraph_timed_pairs;
+    h->launches += h->bgraph_kernels;
+    timing_finish(h);
   }
-  const dec_status st = cuda_check(h, "batched decode launch");
-  if (st != DEC_OK) return st;
-  timing_finish(h);
   for (int32_t i = 0; i < batch; ++i) h->lens[seqs[i]] = positions[i] + 1;
   return DEC_OK;
 }

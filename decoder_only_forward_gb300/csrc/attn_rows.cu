@@ -17,17 +17,29 @@ namespace dec {
 constexpr int AR_THREADS = 128;
 constexpr int AR_TILE = 32;   // keys staged per step (one key per lane when scoring)
 
+// Shared-memory K tile: rows of HD floats as float4 chunks, chunk c of row r
+// stored at c ^ (r & 7) so that 8 lanes reading chunk c of 8 consecutive rows
+// hit 8 different 16-byte bank groups.
+template <int HD>
+__device__ __forceinline__ int ar_swz(int row, int c) {
+  constexpr int M = (HD / 4) < 8 ? (HD / 4) - 1 : 7;
+  return c ^ (row & M);
+}
+
 template <typename KV, int HD>
 __global__ void __launch_bounds__(AR_THREADS) k_attn_rows(
     const float* __restrict__ Q, const KV* __restrict__ kc, const KV* __restrict__ vc, size_t ring_elems,
     const int32_t* __restrict__ seq, const int32_t* __restrict__ pos, int nq, int nkv, int max_seq, int sliding,
     float* __restrict__ part) {
-  constexpr int OUTS = (MAX_GROUP * HD + AR_THREADS - 1) / AR_THREADS;
-  constexpr int CE = 16 / sizeof(KV);   // elements per 16-byte chunk
-  __shared__ float qs[MAX_GROUP][HD];
-  __shared__ float ks[AR_TILE][HD + 1];
-  __shared__ __align__(16) float vs[AR_TILE][HD];
-  __shared__ float ps[MAX_GROUP][AR_TILE];
+  constexpr int CE = 16 / sizeof(KV);     // elements per 16-byte global chunk
+  constexpr int CPR = HD / CE;            // global chunks per row
+  constexpr int C4 = HD / 4;              // float4 chunks per row
+  constexpr int LPT = (AR_TILE * CPR + AR_THREADS - 1) / AR_THREADS;
+  constexpr int R = (MAX_GROUP * C4 + AR_THREADS - 1) / AR_THREADS;   // (head, chunk) slots per thread
+  __shared__ __align__(16) float4 qs[MAX_GROUP][C4];
+  __shared__ __align__(16) float4 ks[AR_TILE][C4];
+  __shared__ __align__(16) float4 vs[AR_TILE][C4];
+  __shared__ float ps[MAX_GROUP][AR_TILE + 1];
   __shared__ float mrow[MAX_GROUP], lrow[MAX_GROUP], alpha[MAX_GROUP];
 
   const int g = blockIdx.x, split = blockIdx.y, nsplit = gridDim.y, b = blockIdx.z;
@@ -42,38 +54,72 @@ __global__ void __launch_bounds__(AR_THREADS) k_attn_rows(
   const float scale = 1.0f / sqrtf((float)HD);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  for (int i = tid; i < G * HD; i += AR_THREADS) qs[i / HD][i % HD] = q[i] * scale;
+  for (int i = tid; i < G * C4; i += AR_THREADS) {
+    float4 v = reinterpret_cast<const float4*>(q)[i];
+    v.x *= scale;
+    v.y *= scale;
+    v.z *= scale;
+    v.w *= scale;
+    qs[i / C4][i % C4] = v;
+  }
   if (tid < MAX_GROUP) {
     mrow[tid] = -INFINITY;
     lrow[tid] = 0.f;
   }
-  float acc[OUTS];
+  float4 acc[R];
 #pragma unroll
-  for (int r = 0; r < OUTS; ++r) acc[r] = 0.f;
+  for (int r = 0; r < R; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
 
+  // The next tile's K/V chunks are loaded into registers while the current
+  // tile is scored from shared memory.
+  uint4 kr[LPT], vr[LPT];
+  auto load = [&](int t0) {
+#pragma unroll
+    for (int j = 0; j < LPT; ++j) {
+      const int i = tid + j * AR_THREADS, row = i / CPR, c = i % CPR;
+      if (i < AR_TILE * CPR && t0 + row < j1) {
+        const size_t off = (size_t)(t0 + row) * kd + (size_t)g * HD + c * CE;
+        kr[j] = __ldcs(reinterpret_cast<const uint4*>(K + off));
+        vr[j] = __ldcs(reinterpret_cast<const uint4*>(V + off));
+      }
+    }
+  };
+  if (j0 < j1) load(j0);
   for (int t0 = j0; t0 < j1; t0 += AR_TILE) {
     const int nt = min(AR_TILE, j1 - t0);
     __syncthreads();
-    for (int i = tid; i < nt * (HD / CE); i += AR_THREADS) {
-      const int row = i / (HD / CE), c = i % (HD / CE);
-      const size_t off = (size_t)(t0 + row) * kd + (size_t)g * HD + c * CE;
-      float kf[CE], vf[CE];
-      Chunk<KV>::widen(__ldcs(reinterpret_cast<const uint4*>(K + off)), kf);
-      Chunk<KV>::widen(__ldcs(reinterpret_cast<const uint4*>(V + off)), vf);
 #pragma unroll
-      for (int e = 0; e < CE; ++e) {
-        ks[row][c * CE + e] = kf[e];
-        vs[row][c * CE + e] = vf[e];
+    for (int j = 0; j < LPT; ++j) {
+      const int i = tid + j * AR_THREADS, row = i / CPR, c = i % CPR;
+      if (i < AR_TILE * CPR && row < nt) {
+        float kf[CE], vf[CE];
+        Chunk<KV>::widen(kr[j], kf);
+        Chunk<KV>::widen(vr[j], vf);
+#pragma unroll
+        for (int h4 = 0; h4 < CE / 4; ++h4) {
+          const int c4 = c * (CE / 4) + h4;
+          ks[row][ar_swz<HD>(row, c4)] = make_float4(kf[4 * h4], kf[4 * h4 + 1], kf[4 * h4 + 2], kf[4 * h4 + 3]);
+          vs[row][c4] = make_float4(vf[4 * h4], vf[4 * h4 + 1], vf[4 * h4 + 2], vf[4 * h4 + 3]);
+        }
       }
     }
     __syncthreads();
-    // Scores: warp per head, lane per key.
+    if (t0 + AR_TILE < j1) load(t0 + AR_TILE);
+    // Scores: warp per head, lane per key; float4 reads of the key row and a
+    // broadcast of the query.
     for (int hh = warp; hh < G; hh += AR_THREADS / 32) {
       float s = -INFINITY;
       if (lane < nt) {
-        s = 0.f;
+        float s0 = 0.f, s1 = 0.f;
 #pragma unroll 8
-        for (int d = 0; d < HD; ++d) s = fmaf(qs[hh][d], ks[lane][d], s);
+        for (int c = 0; c < C4; ++c) {
+          const float4 kv = ks[lane][ar_swz<HD>(lane, c)], qv = qs[hh][c];
+          s0 = fmaf(qv.x, kv.x, s0);
+          s1 = fmaf(qv.y, kv.y, s1);
+          s0 = fmaf(qv.z, kv.z, s0);
+          s1 = fmaf(qv.w, kv.w, s1);
+        }
+        s = s0 + s1;
       }
       const float mnew = fmaxf(mrow[hh], warp_max(s));
       const float e = lane < nt ? __expf(s - mnew) : 0.f;
@@ -88,13 +134,26 @@ __global__ void __launch_bounds__(AR_THREADS) k_attn_rows(
       }
     }
     __syncthreads();
+    // Weighted sum of V: slot (head, float4 chunk) per thread.
 #pragma unroll
-    for (int r = 0; r < OUTS; ++r) {
-      const int idx = tid + r * AR_THREADS;
-      if (idx < G * HD) {
-        const int hh = idx / HD, d = idx % HD;
-        float o = acc[r] * alpha[hh];
-        for (int j = 0; j < nt; ++j) o = fmaf(ps[hh][j], vs[j][d], o);
+    for (int r = 0; r < R; ++r) {
+      const int slot = tid + r * AR_THREADS;
+      if (slot < G * C4) {
+        const int hh = slot / C4, c = slot % C4;
+        const float a = alpha[hh];
+        float4 o = acc[r];
+        o.x *= a;
+        o.y *= a;
+        o.z *= a;
+        o.w *= a;
+        for (int j = 0; j < nt; ++j) {
+          const float pj = ps[hh][j];
+          const float4 v = vs[j][c];
+          o.x = fmaf(pj, v.x, o.x);
+          o.y = fmaf(pj, v.y, o.y);
+          o.z = fmaf(pj, v.z, o.z);
+          o.w = fmaf(pj, v.w, o.w);
+        }
         acc[r] = o;
       }
     }
@@ -103,11 +162,15 @@ __global__ void __launch_bounds__(AR_THREADS) k_attn_rows(
   // part[((b*nq + head) * nsplit + split) * (HD+2) + {0..HD-1: output, HD: max, HD+1: sum}];
   // an empty split leaves (-inf, 0, zeros), which the merge skips.
 #pragma unroll
-  for (int r = 0; r < OUTS; ++r) {
-    const int idx = tid + r * AR_THREADS;
-    if (idx < G * HD) {
-      const int hh = idx / HD, d = idx % HD;
-      part[(((size_t)b * nq + g * G + hh) * nsplit + split) * (HD + 2) + d] = acc[r];
+  for (int r = 0; r < R; ++r) {
+    const int slot = tid + r * AR_THREADS;
+    if (slot < G * C4) {
+      const int hh = slot / C4, c = slot % C4;
+      float* pp = part + (((size_t)b * nq + g * G + hh) * nsplit + split) * (HD + 2) + 4 * c;
+      pp[0] = acc[r].x;
+      pp[1] = acc[r].y;
+      pp[2] = acc[r].z;
+      pp[3] = acc[r].w;
     }
   }
   if (tid < G) {

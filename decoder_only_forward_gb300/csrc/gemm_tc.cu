@@ -6,7 +6,11 @@
 //
 // Persistent: one CTA per SM walks 128 x BN output tiles (tile t, t + grid,
 // ...), ordered so that CTAs running at the same time share weight columns
-// (B) in L2.  Three warp roles:
+// (B) in L2.  When there are too few tiles to occupy the SMs (few rows, the
+// batched decode step), K is split into ksplit ranges: unit t is K range
+// t % ksplit of tile t / ksplit, its raw f32 sum goes to a partial buffer, and
+// k_splitk_epi adds the ranges in order and applies the epilogue.  Three warp
+// roles:
 //   warp 0 lane 0: TMA producer, K-blocks of 64 into a ring of smem stages;
 //   warp 1 lane 0: MMA issuer (tcgen05.mma, cta_group::1), frees stages with
 //                  tcgen05.commit, alternates between two TMEM accumulators;
@@ -45,8 +49,8 @@ template <int BN, bool SPLIT>
 __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant__ CUtensorMap tm_ahi,
                                                            const __grid_constant__ CUtensorMap tm_alo,
                                                            const __grid_constant__ CUtensorMap tm_b, int M, int N,
-                                                           int K, GemmEpi e, int groups, int m_tiles,
-                                                           DeviceState* st) {
+                                                           int K, GemmEpi e, int groups, int m_tiles, int ksplit,
+                                                           float* __restrict__ kpart, DeviceState* st) {
   using C = TcCfg<BN, SPLIT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -63,12 +67,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = (N + BN - 1) / BN;
   const int per_n = groups * m_tiles;            // tiles sharing one BN block of weight rows
-  const int total = n_tiles * per_n;
+  const int total = n_tiles * per_n * ksplit;
   const int kblocks = (K + TC_BK - 1) / TC_BK;
+  const int kb_per = (kblocks + ksplit - 1) / ksplit;   // every split non-empty (host's choice)
   // Tile t -> (group, 128-row block, BN-column block); rows of group g are
   // [offset[g], offset[g+1]) when grouped.  A tile past its group's rows has
   // no work (the same answer for every role).
-  auto decode_tile = [&](int t, int& row0, int& rows, int& b_row0, int& m0, int& n0) -> bool {
+  auto decode_tile = [&](int u, int& row0, int& rows, int& b_row0, int& m0, int& n0) -> bool {
+    const int t = u / ksplit;
     const int nb = t / per_n, rem = t % per_n;
     const int g = rem / m_tiles, mb = rem % m_tiles;
     row0 = 0;
@@ -118,7 +124,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         int row0, rows, b_row0, m0, n0;
         if (!decode_tile(t, row0, rows, b_row0, m0, n0)) continue;
-        for (int kb = 0; kb < kblocks; ++kb, ++kb_all) {
+        const int kb0 = (t % ksplit) * kb_per, kb1 = min(kblocks, kb0 + kb_per);
+        for (int kb = kb0; kb < kb1; ++kb, ++kb_all) {
           const int s = kb_all % C::STAGES;
           const uint32_t ph = (kb_all / C::STAGES) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, st, 101)) {
@@ -147,7 +154,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
         if (!mbar_wait(&acc_empty[b], ((it >> 1) & 1) ^ 1, abort_flag, st, 104)) break;
         tc_fence_after();
         const uint32_t acc = tmem + b * BN;
-        for (int kb = 0; kb < kblocks; ++kb, ++kb_all) {
+        const int kb0 = (t % ksplit) * kb_per, kb1 = min(kblocks, kb0 + kb_per);
+        for (int kb = kb0; kb < kb1; ++kb, ++kb_all) {
           const int s = kb_all % C::STAGES;
           const uint32_t ph = (kb_all / C::STAGES) & 1;
           if (!mbar_wait(&full[s], ph, abort_flag, st, 102)) {
@@ -161,7 +169,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
           const uint64_t db = sw128_kmajor_desc(smem_u32(base + C::A_BYTES * (SPLIT ? 2 : 1)));
 #pragma unroll
           for (int k = 0; k < TC_BK / 16; ++k) {
-            tc_mma_bf16(acc, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            tc_mma_bf16(acc, da + 2 * k, db + 2 * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
             if (SPLIT) tc_mma_bf16(acc, dl + 2 * k, db + 2 * k, idesc, 1u);
           }
           tc_commit(&empty[s]);
@@ -190,8 +198,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
       tc_fence_after();
       const uint32_t acc = tmem + b * BN + lane_base;
       const int r_base = m0 + q * 32;          // this warp's first row within the group
+      float* kp = ksplit > 1 ? kpart + (size_t)(t % ksplit) * M * N : nullptr;
+      // A warp whose 32 rows are all past the tile's rows (a batch of few rows)
+      // only keeps the accumulator hand-off in step.
+      const bool idle = r_base >= rows;
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
+      for (int c = 0; c < BN && !idle; c += 32) {
         if (n0 + c >= N) break;
         float v[32];
         tmem_ld32(acc + c, v);
@@ -204,8 +216,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
 #pragma unroll 4
         for (int rr = 0; rr < 32; rr += 2) {
           const int lr = rr + (lane >> 4);
-          if (r_base + lr < rows)
-            epi_pair(e, row0 + r_base + lr, n0 + c + pc, slice[lr * C::EPI_LD + pc], slice[lr * C::EPI_LD + pc + 1]);
+          if (r_base + lr < rows) {
+            const int row = row0 + r_base + lr, col = n0 + c + pc;
+            if (kp) {
+              float* d = kp + (size_t)row * N + col;
+              const float v0 = slice[lr * C::EPI_LD + pc], v1 = slice[lr * C::EPI_LD + pc + 1];
+              if ((N & 1) == 0) {
+                if (col < N) *reinterpret_cast<float2*>(d) = make_float2(v0, v1);
+              } else if (col < N) {
+                d[0] = v0;
+                if (col + 1 < N) d[1] = v1;
+              }
+            } else {
+              epi_pair(e, row, col, slice[lr * C::EPI_LD + pc], slice[lr * C::EPI_LD + pc + 1]);
+            }
+          }
         }
         __syncwarp();
       }
@@ -230,6 +255,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// Sum of the ksplit partial products of every (row, column pair), in split
+// order, then the GEMM's epilogue.
+__global__ void __launch_bounds__(256) k_splitk_epi(const float* __restrict__ part, int ksplit, int M, int N,
+                                                    GemmEpi e) {
+  const int half = (N + 1) >> 1;
+  const size_t pairs = (size_t)M * half, plane = (size_t)M * N;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < pairs; i += (size_t)gridDim.x * blockDim.x) {
+    const int row = (int)(i / half), col = 2 * (int)(i % half);
+    const bool two = col + 1 < N;
+    const float* p = part + (size_t)row * N + col;
+    float a0 = p[0], a1 = two ? p[1] : 0.f;
+    for (int z = 1; z < ksplit; ++z) {
+      a0 += p[z * plane];
+      if (two) a1 += p[z * plane + 1];
+    }
+    epi_pair(e, row, col, a0, a1);
   }
 }
 
@@ -275,24 +319,65 @@ static int num_sms() {
   return n > 0 ? n : 1;
 }
 
+// K splits for a GEMM whose tiles alone would leave SMs idle: the count that
+// minimises (waves of units) x (K-blocks per unit) x (time of one weight
+// K-block at an SM's share of HBM), plus the partial sums' round trip for
+// s > 1, within the partial buffer.  rows: the rows the partial buffer holds
+// per split.  A function of the GEMM's shape and the GPU only: for the same
+// weights and tile rows every call takes the same split (and rounding).
+static int pick_ksplit(long long tiles, int kblocks, int BN, long long rows, int N, size_t cap_bytes, int sms) {
+  const double bw = 6.0e12;                                    // bytes/s, a round HBM copy rate
+  const double t_kb = (double)BN * TC_BK * 2.0 / (bw / sms);    // one weight K-block on one SM
+  double best_t = 0.0;
+  int best = 1;
+  for (int s = 1; s <= 16 && s <= kblocks; ++s) {
+    const int kb_per = (kblocks + s - 1) / s;
+    if ((kblocks + kb_per - 1) / kb_per != s) continue;         // a split would be empty
+    const double part_bytes = (double)s * rows * N * 4.0;
+    if (s > 1 && part_bytes > (double)cap_bytes) break;
+    const long long units = tiles * s;
+    double t = (double)((units + sms - 1) / sms) * kb_per * t_kb;
+    if (s > 1) t += 2.0 * part_bytes / bw + 3e-6;               // partials out and back, one more launch
+    if (s == 1 || t < 0.97 * best_t) {
+      best_t = t;
+      best = s;
+    }
+  }
+  return best;
+}
+
 template <int BN, bool SPLIT>
 static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& al, const CUtensorMap& b, int M, int N, int K,
-                             const GemmEpi& e, int groups, int max_rows, DeviceState* st, cudaStream_t s) {
+                             const GemmEpi& e, int groups, int max_rows, float* kpart, size_t kpart_bytes,
+                             DeviceState* st, cudaStream_t s) {
   using C = TcCfg<BN, SPLIT>;
   auto kern = k_gemm_tc<BN, SPLIT>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   const int m_tiles = (max_rows + TC_BM - 1) / TC_BM;
-  const long long total = (long long)m_tiles * groups * ((N + BN - 1) / BN);
+  const long long tiles = (long long)m_tiles * groups * ((N + BN - 1) / BN);
   const int sms = num_sms();
+  const int kblocks = (K + TC_BK - 1) / TC_BK;
+  // Grouped GEMMs keep all M rows per split; plain ones a whole number of row tiles.
+  const long long rows = groups > 1 ? (long long)M : (long long)m_tiles * TC_BM;
+  const int ksplit = kpart ? pick_ksplit(tiles, kblocks, BN, rows, N, kpart_bytes, sms) : 1;
+  const long long total = tiles * ksplit;
   const int grid = (int)(total < sms ? total : sms);
-  kern<<<grid, TC_THREADS, C::SMEM, s>>>(a, al, b, M, N, K, e, groups, m_tiles, st);
+  kern<<<grid, TC_THREADS, C::SMEM, s>>>(a, al, b, M, N, K, e, groups, m_tiles, ksplit, kpart, st);
+  if (ksplit > 1) {
+    const long long pairs = (long long)M * ((N + 1) / 2);
+    long long blocks = (pairs + 255) / 256;
+    if (blocks > 8LL * sms) blocks = 8LL * sms;
+    k_splitk_epi<<<(int)blocks, 256, 0, s>>>(kpart, ksplit, M, N, e);
+  }
   return cudaGetLastError();
 }
 
 // A (hi plane, optional lo plane): [a_rows, K] bf16; B: [groups * N, K] bf16.
 // Grouped when e.group_offset is set (max_rows bounds any one group's rows).
+// kpart (nullable): f32 scratch of kpart_bytes for split-K partial sums.
 cudaError_t launch_gemm_tc(const void* a_hi, const void* a_lo, int a_rows, const void* b, int M, int N, int K,
-                           const GemmEpi& e, int groups, int max_rows, DeviceState* st, cudaStream_t s) {
+                           const GemmEpi& e, int groups, int max_rows, float* kpart, size_t kpart_bytes,
+                           DeviceState* st, cudaStream_t s) {
   if (K % 8 != 0 || a_rows <= 0 || N <= 0) return cudaErrorInvalidValue;
   const int bn = N >= 1536 ? 256 : 128;
   CUtensorMap ma, ml, mb;
@@ -301,10 +386,10 @@ cudaError_t launch_gemm_tc(const void* a_hi, const void* a_lo, int a_rows, const
   if (!a_lo) ml = ma;
   if (!make_map(&mb, b, (uint64_t)N * groups, (uint64_t)K, (uint32_t)bn)) return cudaErrorInvalidValue;
   if (bn == 256)
-    return a_lo ? launch_tc<256, true>(ma, ml, mb, M, N, K, e, groups, max_rows, st, s)
-                : launch_tc<256, false>(ma, ml, mb, M, N, K, e, groups, max_rows, st, s);
-  return a_lo ? launch_tc<128, true>(ma, ml, mb, M, N, K, e, groups, max_rows, st, s)
-              : launch_tc<128, false>(ma, ml, mb, M, N, K, e, groups, max_rows, st, s);
+    return a_lo ? launch_tc<256, true>(ma, ml, mb, M, N, K, e, groups, max_rows, kpart, kpart_bytes, st, s)
+                : launch_tc<256, false>(ma, ml, mb, M, N, K, e, groups, max_rows, kpart, kpart_bytes, st, s);
+  return a_lo ? launch_tc<128, true>(ma, ml, mb, M, N, K, e, groups, max_rows, kpart, kpart_bytes, st, s)
+              : launch_tc<128, false>(ma, ml, mb, M, N, K, e, groups, max_rows, kpart, kpart_bytes, st, s);
 }
 
 }  // namespace dec
@@ -326,7 +411,8 @@ extern "C" dec_status dec_gemm_bf16(const void* a_hi, const void* a_lo, const vo
   e.mode = EPI_STORE;
   e.n_out = n;
   e.out_f32 = c;
-  const cudaError_t err = launch_gemm_tc(a_hi, a_lo, m, b, m, n, k, e, 1, m, nullptr, (cudaStream_t)cuda_stream);
+  const cudaError_t err =
+      launch_gemm_tc(a_hi, a_lo, m, b, m, n, k, e, 1, m, nullptr, 0, nullptr, (cudaStream_t)cuda_stream);
   if (err != cudaSuccess) {
     set_global_error(cudaGetErrorString(err));
     return DEC_ECUDA;

@@ -461,7 +461,8 @@ static cudaError_t gemm(const Model& m, cudaStream_t s, const Act& a, const TW* 
   cudaError_t err = cudaSuccess;
   timer_begin(m, DEC_K_PF_GEMM, s);
   if (std::is_same<TW, __nv_bfloat16>::value) {
-    err = launch_gemm_tc(a.base, a.lo(), a.rows, B, M, N, K, e, groups, max_rows, m.s.st, s);
+    err = launch_gemm_tc(a.base, a.lo(), a.rows, B, M, N, K, e, groups, max_rows, m.s.kpart, m.s.kpart_bytes, m.s.st,
+                         s);
   } else {
     dim3 grid((max_rows + 63) / 64, (N + 63) / 64, groups);
     k_gemm_simt<float, TW><<<grid, 256, 0, s>>>((const float*)a.base, B, M, N, K, e);
@@ -760,14 +761,38 @@ cudaError_t launch_decode_rows(const Model& m, cudaStream_t s, int B, float* log
   return decode_rows<float, float>(m, s, B, logits, d_argmax);
 }
 
-cudaError_t launch_rows_setup(const Model& m, cudaStream_t s, const RowsMeta& meta, const int32_t* d_tokens, int B) {
+static int rows_setup_blocks(const Model& m, int B) {
   const int half = m.cfg.head_dim / 2;
   const int n = B * half > B ? B * half : B;
+  return (n + 255) / 256;
+}
+
+cudaError_t launch_rows_setup(const Model& m, cudaStream_t s, const RowsMeta& meta, const int32_t* d_tokens, int B) {
   const Scratch& S = m.s;
-  k_rows_setup<<<(n + 255) / 256, 256, 0, s>>>(meta, B, d_tokens, m.cfg.vocab, S.inv_freq, half, S.tokens, S.b_seq,
-                                               S.b_pos, S.b_rows, S.rope_tab, S.st);
+  k_rows_setup<<<rows_setup_blocks(m, B), 256, 0, s>>>(meta, B, d_tokens, m.cfg.vocab, S.inv_freq,
+                                                       m.cfg.head_dim / 2, S.tokens, S.b_seq, S.b_pos, S.b_rows,
+                                                       S.rope_tab, S.st);
   count_launch(m);
   return cudaGetLastError();
+}
+
+cudaError_t update_rows_setup_node(cudaGraphExec_t g, cudaGraphNode_t node, const Model& m, const RowsMeta& meta,
+                                   const int32_t* d_tokens, int B) {
+  const Scratch& S = m.s;
+  int vocab = m.cfg.vocab, half = m.cfg.head_dim / 2;
+  const double* inv = S.inv_freq;
+  int32_t *tokens = S.tokens, *bs = S.b_seq, *bp = S.b_pos, *br = S.b_rows;
+  float2* tab = S.rope_tab;
+  DeviceState* st = S.st;
+  void* args[] = {const_cast<RowsMeta*>(&meta), &B, &d_tokens, &vocab, &inv, &half, &tokens, &bs, &bp, &br, &tab, &st};
+  cudaKernelNodeParams p = {};
+  p.func = reinterpret_cast<void*>(k_rows_setup);
+  p.gridDim = dim3(rows_setup_blocks(m, B));
+  p.blockDim = dim3(256);
+  p.sharedMemBytes = 0;
+  p.kernelParams = args;
+  p.extra = nullptr;
+  return cudaGraphExecKernelNodeSetParams(g, node, &p);
 }
 
 }  // namespace dec

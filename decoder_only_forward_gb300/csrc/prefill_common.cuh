@@ -93,16 +93,28 @@ __device__ __forceinline__ void epi_pair(const GemmEpi& e, int row, int col, flo
   if (col >= e.n_out) return;
   switch (e.mode) {
     case EPI_RESID: {
-      float2* p = reinterpret_cast<float2*>(e.out_f32 + (size_t)row * e.n_out + col);
-      float2 x = *p;
-      x.x += v0;
-      x.y += v1;
-      *p = x;
+      float* p = e.out_f32 + (size_t)row * e.n_out + col;
+      if ((e.n_out & 1) == 0) {
+        float2 x = *reinterpret_cast<float2*>(p);
+        x.x += v0;
+        x.y += v1;
+        *reinterpret_cast<float2*>(p) = x;
+      } else {   // odd rows: no 8-byte alignment, and the last column stands alone
+        p[0] += v0;
+        if (col + 1 < e.n_out) p[1] += v1;
+      }
       break;
     }
-    case EPI_STORE:
-      store_pair(e.out_f32 + (size_t)row * e.n_out + col, v0, v1);
+    case EPI_STORE: {
+      float* p = e.out_f32 + (size_t)row * e.n_out + col;
+      if ((e.n_out & 1) == 0) {
+        store_pair(p, v0, v1);
+      } else {
+        p[0] = v0;
+        if (col + 1 < e.n_out) p[1] = v1;
+      }
       break;
+    }
     case EPI_SWIGLU: {
       const float a = silu_f(v0) * v1;
       const size_t o = (size_t)row * (e.n_out / 2) + (col >> 1);

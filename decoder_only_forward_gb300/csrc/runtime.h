@@ -87,6 +87,8 @@ struct Scratch {
   int32_t* b_pos;       // [MAX_BATCH] position of each row
   int32_t* b_rows;      // [MAX_BATCH] K/V row of each row: seq * ring_rows + slot(pos)
   float* b_part;        // [MAX_BATCH][nq][AR_MAX_SPLIT][hd+2] attention split partials
+  float* kpart;         // split-K partial sums of the tensor-core GEMMs
+  size_t kpart_bytes;
 };
 
 constexpr int LM_GRID_MAX = 1024;
@@ -148,6 +150,7 @@ struct WsPlan {
   size_t mk_layers;     // layer table of the persistent decode kernel
   size_t mk_maps;       // its weight tensor maps
   size_t b_seq, b_pos, b_rows, b_part;  // batched decode
+  size_t kpart, kpart_bytes;            // split-K partials
   size_t kv;            // start of the KV rings: [layer][K, V][seq][ring_rows][n_kv*hd]
   size_t kv_layer_bytes; // one layer's K (or V) rings of every sequence
   size_t ring_bytes;    // one sequence's ring
@@ -219,6 +222,9 @@ struct RowsMeta {
   int32_t rows[MAX_BATCH];   // seq * ring_rows + slot(pos)
 };
 cudaError_t launch_rows_setup(const Model& m, cudaStream_t s, const RowsMeta& meta, const int32_t* d_tokens, int B);
+// Points a captured setup node (of a graph captured for the same B) at new rows.
+cudaError_t update_rows_setup_node(cudaGraphExec_t g, cudaGraphNode_t node, const Model& m, const RowsMeta& meta,
+                                   const int32_t* d_tokens, int B);
 
 struct RowOut;
 // Batched decode attention (attn_rows.cu): rotated queries Q [B][nq*hd] f32,
@@ -247,8 +253,10 @@ bool attend_check(const void* q, const void* k, const void* v, const void* out, 
 
 // Tensor-core GEMM (gemm_tc.cu); see prefill_common.cuh for GemmEpi.
 struct GemmEpi;
+// kpart (nullable): f32 scratch of kpart_bytes for split-K partial sums.
 cudaError_t launch_gemm_tc(const void* a_hi, const void* a_lo, int a_rows, const void* b, int M, int N, int K,
-                           const GemmEpi& e, int groups, int max_rows, DeviceState* st, cudaStream_t s);
+                           const GemmEpi& e, int groups, int max_rows, float* kpart, size_t kpart_bytes,
+                           DeviceState* st, cudaStream_t s);
 
 struct RowOut;
 // Tensor-core causal prefill attention (attn_tc.cu) over key columns
