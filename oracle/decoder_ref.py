@@ -32,6 +32,12 @@ Per position p (absolute), per layer, pre-norm:
                                                               [PAN Mixture of Experts; RML Mixture of experts]
   logits = W_out rmsnorm(x, w_out)                             [PAN Forward Pass Flow]
 
+Optional int8 K/V cache (RML "The decoder", KV cache): every cached key and
+value row is stored as groups of G channels (G the largest power of two that
+divides head_dim, at most 32, so a group never spans two heads), each group as
+round(x / s) with one float32 scale s = max|x| / 127; attention reads the
+stored values back as code * s, the current position's included.
+
 Readings taken where the pages are silent, garbled or disagree (each is listed
 in the design notes as well):
   * RoPE pairs: pair i is dims (2i, 2i+1) with inv_freq_i = theta^(-2i/hd)
@@ -43,6 +49,11 @@ in the design notes as well):
   * Qwen2-style bias on q, k, v only (RML model config), not on the output.
   * Expert weights are always renormalised (every workload here does).
   * Argmax and top-k ties go to the lower index.
+  * int8 K/V: the quantisation decision is taken in float32 (the precision a
+    kernel holds K/V in): x rounded to float32, s = max|x| / 127 and x / s
+    each one float32 operation, "round" = half away from zero (C round),
+    codes clamped to [-127, 127], read back as float32(code * s).  An all-zero
+    group stores s = 0 and codes 0.
 
 Two execution orders are provided: ``Session.prefill`` (row-wise: layer-outer,
 position-inner, one matrix-vector product per row, the single-pass prefill of
@@ -102,6 +113,8 @@ class OracleConfig:
     # Rotary width (SIP partial-rotary rope_rot): only the first rope_dim dims of a head
     # turn, the rest pass through; 0 means head_dim.
     rope_dim: int = 0
+    # int8 K/V cache with per-group float32 scales (RML "The decoder", KV cache).
+    kv_int8: bool = False
 
     @property
     def rotary_dim(self) -> int:
@@ -192,6 +205,57 @@ def rope_rotate(vec, pos: int, inv_freq, half: bool = False, rope_dim: int = 0) 
     v[..., ia] = a * c - b * s
     v[..., ib] = a * s + b * c
     return v
+
+
+# --------------------------------------------------------------------------
+# int8 K/V cache (RML "The decoder", KV cache)
+# --------------------------------------------------------------------------
+
+def kv_group_size(head_dim: int) -> int:
+    """Channels per int8 scale group: the largest power of two dividing head_dim, at most 32."""
+    g = 1
+    while g < 32 and head_dim % (2 * g) == 0:
+        g *= 2
+    return g
+
+
+def round_half_away(x) -> np.ndarray:
+    """C round(): to the nearest integer, halves away from zero."""
+    x = np.asarray(x, F64)
+    return np.sign(x) * np.floor(np.abs(x) + 0.5)
+
+
+def quantize_int8_groups(row, group: int):
+    """One cached row -> (codes int8 [n], scales float32 [n / group]).
+
+    Each group of ``group`` channels becomes round(x / s) with s = max|x| / 127,
+    the arithmetic in float32 (see the module notes); an all-zero group keeps
+    s = 0 and codes 0.
+    """
+    x = np.asarray(row, F64).astype(np.float32).reshape(-1, group)
+    m = np.abs(x).max(axis=1)
+    s = (m / np.float32(127.0)).astype(np.float32)
+    codes = np.zeros(x.shape, np.int8)
+    nz = s > 0
+    if nz.any():
+        qf = (x[nz] / s[nz, None]).astype(np.float32)
+        codes[nz] = np.clip(round_half_away(qf), -127, 127).astype(np.int8)
+    return codes.reshape(-1), s
+
+
+def dequantize_int8_groups(codes, scales, group: int) -> np.ndarray:
+    """Stored row read back: float32(code * s), as float64."""
+    c = np.asarray(codes, np.int8).astype(np.float32).reshape(-1, group)
+    s = np.asarray(scales, np.float32)
+    return (c * s[:, None]).astype(np.float32).astype(F64).reshape(-1)
+
+
+def kv_int8_roundtrip(row, head_dim: int) -> np.ndarray:
+    """The value an int8 cache gives back for a row of K or V (any shape, heads of head_dim)."""
+    a = np.asarray(row, F64)
+    g = kv_group_size(head_dim)
+    codes, scales = quantize_int8_groups(a.reshape(-1), g)
+    return dequantize_int8_groups(codes, scales, g).reshape(a.shape)
 
 
 def kv_head_of(h: int, n_heads: int, n_kv_heads: int) -> int:
@@ -381,8 +445,11 @@ class Session:
         k = rope_rotate(k.reshape(nkv, hd), pos, self.inv_freq, c.rope_half, c.rope_dim)
         if len(self.keys[l]) != pos:
             raise AssertionError("positions must be appended in ascending order")
+        v = v.reshape(nkv, hd)
+        if c.kv_int8:
+            k, v = kv_int8_roundtrip(k, hd), kv_int8_roundtrip(v, hd)
         self.keys[l].append(k)
-        self.values[l].append(v.reshape(nkv, hd))
+        self.values[l].append(v)
         lo = window_start(pos, c.sliding_window)
         o = attend_ref(q, np.stack(self.keys[l][lo:pos + 1]),
                        np.stack(self.values[l][lo:pos + 1]), nq, nkv)
@@ -485,6 +552,8 @@ class Session:
             K = rot(K.reshape(n, nkv, hd))
             V = V.reshape(n, nkv, hd)
             for t in range(n):
+                if c.kv_int8:
+                    K[t], V[t] = kv_int8_roundtrip(K[t], hd), kv_int8_roundtrip(V[t], hd)
                 self.keys[l].append(K[t])
                 self.values[l].append(V[t])
             Kall = np.stack(self.keys[l])
