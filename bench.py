@@ -91,7 +91,16 @@ def measured_traffic(workload: str, kernel: str):
     return t["bytes"]
 
 
-def decode_bytes(w: dict, pos: int, kv_es: int) -> float:
+def kv_bytes_per_element(w: dict, kv: str) -> float:
+    """Stored bytes per K (or V) element: 4, 2, or for int8 rows (codes + per-group f32 scales) the
+    row's bytes over its n_kv_heads * head_dim elements."""
+    if kv != "i8":
+        return 4 if kv == "f32" else 2
+    from decoder_only_forward_gb300.dec import kv_int8_row_layout
+    return kv_int8_row_layout(w["n_kv_heads"], w["head_dim"])[0] / (w["n_kv_heads"] * w["head_dim"])
+
+
+def decode_bytes(w: dict, pos: int, kv_es: float) -> float:
     """Weights + KV read by one decode step at absolute position pos (SURVEY-style roofline bytes)."""
     b = weight_bytes(w)
     per_layer = b["qkv"] + b["oproj"] + b["gateup"] + b["down"] + b["router"] + 2 * 4 * w["hidden"]
@@ -219,7 +228,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     w = synthetic.workload(args.workload)
     P, D = w["prompt"], w["decode"]
-    kv_es = 4 if args.kv == "f32" else 2
+    kv_es = kv_bytes_per_element(w, args.kv)
     d = dec.Decoder(w, device=dev, kv_dtype=args.kv)
     if args.fused != "auto":
         d.set_fused(args.fused)
@@ -495,7 +504,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="smollm2-135m", choices=sorted(synthetic.WORKLOADS))
-    ap.add_argument("--kv", default="f32", choices=["f32", "bf16"])
+    ap.add_argument("--kv", default="f32", choices=["f32", "bf16", "i8"])
     ap.add_argument("--prompt", type=int, default=0, help="override the prompt length (profiling only)")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (with --profile only: small cases for profiler captures)")

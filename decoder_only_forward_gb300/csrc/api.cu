@@ -114,7 +114,8 @@ static bool validate(const dec_config* c, std::string& why) {
   if (c->head_dim % 2 != 0) return bad("head_dim must be even (RoPE rotates pairs)");
   if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return bad("rms_eps and rope_theta must be positive");
   if (c->weight_dtype != DEC_F32 && c->weight_dtype != DEC_BF16) return bad("weight_dtype must be DEC_F32 or DEC_BF16");
-  if (c->kv_dtype != DEC_F32 && c->kv_dtype != DEC_BF16) return bad("kv_dtype must be DEC_F32 or DEC_BF16");
+  if (c->kv_dtype != DEC_F32 && c->kv_dtype != DEC_BF16 && c->kv_dtype != DEC_I8)
+    return bad("kv_dtype must be DEC_F32, DEC_BF16 or DEC_I8");
   if (c->n_experts < 0 || c->n_experts_used < 0) return bad("expert counts must be >= 0");
   if (c->n_experts == 0 && c->n_experts_used != 0) return bad("n_experts_used must be 0 for a dense FFN");
   if (c->n_experts > 0 && (c->n_experts_used < 1 || c->n_experts_used > c->n_experts))
@@ -135,7 +136,7 @@ static bool validate(const dec_config* c, std::string& why) {
   if (c->n_kv_heads > MAX_KV_HEADS) return bad("at most 192 kv heads");
   if (c->n_experts > MAX_EXPERTS) return bad("at most 256 experts");
   if (c->n_experts_used > MAX_EXPERTS_USED) return bad("at most 8 experts per token");
-  const size_t ws = dsize(c->weight_dtype), ks = dsize(c->kv_dtype);
+  const size_t ws = dsize(c->weight_dtype), ks = c->kv_dtype == DEC_I8 ? 1 : dsize(c->kv_dtype);
   if ((c->hidden * ws) % 16 || (c->ffn * ws) % 16 || ((size_t)c->n_heads * c->head_dim * ws) % 16)
     return bad("hidden, ffn and n_heads*head_dim rows must be whole 16-byte chunks");
   if ((c->head_dim * ks) % 16) return bad("head_dim rows of the KV cache must be whole 16-byte chunks");
@@ -232,7 +233,7 @@ WsPlan dec::plan_workspace(const dec_config& c) {
   // rounded up to 64 rows so every ring starts 256-byte aligned.
   p.n_seqs = c.n_seqs > 0 ? c.n_seqs : 1;
   p.ring_rows = (int)align_up((size_t)c.max_seq, 64);
-  p.ring_bytes = ks * (size_t)p.ring_rows * kd;
+  p.ring_bytes = (size_t)kv_row_layout(c).bytes * p.ring_rows;
   p.kv = off;
   p.kv_layer_bytes = p.ring_bytes * p.n_seqs;
   off += 2 * p.kv_layer_bytes * c.n_layers;
@@ -531,8 +532,16 @@ static cudaError_t set_step_node(dec_handle* h, const int32_t* d_token, int32_t 
 // One decode step.  On a non-default stream the whole step (setup, every layer,
 // head) is one CUDA graph, captured once per (logits, argmax) pair; per step
 // only the setup node's token/position change.
+static dec_status run_rows(dec_handle* h, int32_t batch, const int32_t* seqs, const int32_t* positions,
+                           const int32_t* d_tokens, int32_t host_token, float* logits, int32_t* d_argmax);
+
 static dec_status run_decode_step(dec_handle* h, const int32_t* d_token, int32_t token, int32_t pos,
                                   float* logits, int32_t* d_argmax) {
+  if (h->m.cfg.kv_dtype == DEC_I8) {
+    // The int8 cache is written and read by the row kernels: one row, sequence 0.
+    const int32_t seq0 = 0;
+    return run_rows(h, 1, &seq0, &pos, d_token, token, logits, d_argmax);
+  }
   const bool cluster = h->fused_mode == DEC_FUSED_CLUSTER && h->m.mk_cluster > 0;
   if (h->m.mk_ok && (cluster || h->fused_mode == DEC_FUSED_GRID)) {
     timing_start(h);
@@ -626,6 +635,83 @@ int32_t dec_length_seq(const dec_handle* h, int32_t seq) {
   return h->lens[seq];
 }
 
+// Enqueues one step of the row kernels for rows already validated: one CUDA
+// graph per (batch, token source, logits, argmax) on a non-default stream.
+static dec_status run_rows(dec_handle* h, int32_t batch, const int32_t* seqs, const int32_t* positions,
+                           const int32_t* d_tokens, int32_t host_token, float* logits, int32_t* d_argmax) {
+  const dec_config& c = h->m.cfg;
+  RowsMeta& meta = h->meta;
+  for (int32_t i = 0; i < batch; ++i) {
+    const int32_t p = positions[i];
+    const int32_t slot = c.sliding_window > 0 ? p % c.max_seq : p;
+    meta.seq[i] = seqs[i];
+    meta.pos[i] = p;
+    meta.rows[i] = seqs[i] * h->m.ring_rows + slot;
+  }
+  if (h->stream == nullptr || !h->use_graph) {
+    timing_start(h);
+    cudaError_t e = launch_rows_setup(h->m, h->stream, meta, d_tokens, host_token, batch);
+    if (e == cudaSuccess) e = launch_decode_rows(h->m, h->stream, batch, logits, d_argmax);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(h, DEC_ECUDA, "batched decode launch: %s", cudaGetErrorString(e));
+    }
+    const dec_status st = cuda_check(h, "batched decode launch");
+    if (st != DEC_OK) return st;
+    timing_finish(h);
+    return DEC_OK;
+  }
+  if (!h->bgraph || h->bgraph_batch != batch || h->bgraph_tokens != d_tokens || h->bgraph_logits != logits ||
+      h->bgraph_argmax != d_argmax) {
+    if (h->bgraph) cudaGraphExecDestroy(h->bgraph);
+    if (h->bgraph_src) cudaGraphDestroy(h->bgraph_src);
+    h->bgraph = nullptr;
+    h->bgraph_src = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeRelaxed);
+    if (e != cudaSuccess) return fail(h, DEC_ECUDA, "begin capture: %s", cudaGetErrorString(e));
+    timing_start(h);
+    const int64_t before = h->launches;
+    cudaError_t le = launch_rows_setup(h->m, h->stream, meta, d_tokens, host_token, batch);
+    if (le == cudaSuccess) le = launch_decode_rows(h->m, h->stream, batch, logits, d_argmax);
+    h->bgraph_kernels = h->launches - before;
+    h->launches = before;
+    h->bgraph_timed_pairs = h->timing.n;
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(h->stream, &g);
+    if (le != cudaSuccess || e != cudaSuccess) {
+      if (g) cudaGraphDestroy(g);
+      cudaGetLastError();
+      return fail(h, DEC_ECUDA, "batched decode capture: %s", cudaGetErrorString(le != cudaSuccess ? le : e));
+    }
+    h->bgraph_src = g;
+    cudaGraphNode_t roots[4];
+    size_t nroots = 4;
+    e = cudaGraphGetRootNodes(g, roots, &nroots);
+    if (e != cudaSuccess || nroots != 1) {
+      drop_graph(h);
+      return fail(h, DEC_ECUDA, "batched decode graph: expected one root node (%s)", cudaGetErrorString(e));
+    }
+    h->bgraph_setup = roots[0];
+    e = cudaGraphInstantiate(&h->bgraph, g, 0);
+    if (e != cudaSuccess) {
+      drop_graph(h);
+      return fail(h, DEC_ECUDA, "batched graph instantiate: %s", cudaGetErrorString(e));
+    }
+    h->bgraph_batch = batch;
+    h->bgraph_tokens = d_tokens;
+    h->bgraph_logits = logits;
+    h->bgraph_argmax = d_argmax;
+  }
+  cudaError_t e = update_rows_setup_node(h->bgraph, h->bgraph_setup, h->m, meta, d_tokens, host_token, batch);
+  if (e != cudaSuccess) return fail(h, DEC_ECUDA, "batched graph update: %s", cudaGetErrorString(e));
+  e = cudaGraphLaunch(h->bgraph, h->stream);
+  if (e != cudaSuccess) return fail(h, DEC_ECUDA, "batched graph launch: %s", cudaGetErrorString(e));
+  h->timing.n = h->bgraph_timed_pairs;
+  h->launches += h->bgraph_kernels;
+  timing_finish(h);
+  return DEC_OK;
+}
+
 // One step of `batch` sequences through the row kernels; every argument is
 // checked before anything is enqueued.
 dec_status dec_decode_batch(dec_handle* h, int32_t batch, const int32_t* seqs, const int32_t* positions,
@@ -646,78 +732,8 @@ dec_status dec_decode_batch(dec_handle* h, int32_t batch, const int32_t* seqs, c
     const dec_status st = check_positions(h, q, 1, positions[i]);
     if (st != DEC_OK) return st;
   }
-  RowsMeta& meta = h->meta;
-  for (int32_t i = 0; i < batch; ++i) {
-    const int32_t p = positions[i];
-    const int32_t slot = c.sliding_window > 0 ? p % c.max_seq : p;
-    meta.seq[i] = seqs[i];
-    meta.pos[i] = p;
-    meta.rows[i] = seqs[i] * h->m.ring_rows + slot;
-  }
-  if (h->stream == nullptr || !h->use_graph) {
-    timing_start(h);
-    cudaError_t e = launch_rows_setup(h->m, h->stream, meta, d_tokens, batch);
-    if (e == cudaSuccess) e = launch_decode_rows(h->m, h->stream, batch, logits, d_argmax);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      return fail(h, DEC_ECUDA, "batched decode launch: %s", cudaGetErrorString(e));
-    }
-    const dec_status st = cuda_check(h, "batched decode launch");
-    if (st != DEC_OK) return st;
-    timing_finish(h);
-  } else {
-    // One CUDA graph per (batch, tokens, logits, argmax); per step only the
-    // setup node's rows change.
-    if (!h->bgraph || h->bgraph_batch != batch || h->bgraph_tokens != d_tokens || h->bgraph_logits != logits ||
-        h->bgraph_argmax != d_argmax) {
-      if (h->bgraph) cudaGraphExecDestroy(h->bgraph);
-      if (h->bgraph_src) cudaGraphDestroy(h->bgraph_src);
-      h->bgraph = nullptr;
-      h->bgraph_src = nullptr;
-      cudaError_t e = cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeRelaxed);
-      if (e != cudaSuccess) return fail(h, DEC_ECUDA, "begin capture: %s", cudaGetErrorString(e));
-      timing_start(h);
-      const int64_t before = h->launches;
-      cudaError_t le = launch_rows_setup(h->m, h->stream, meta, d_tokens, batch);
-      if (le == cudaSuccess) le = launch_decode_rows(h->m, h->stream, batch, logits, d_argmax);
-      h->bgraph_kernels = h->launches - before;
-      h->launches = before;
-      h->bgraph_timed_pairs = h->timing.n;
-      cudaGraph_t g = nullptr;
-      e = cudaStreamEndCapture(h->stream, &g);
-      if (le != cudaSuccess || e != cudaSuccess) {
-        if (g) cudaGraphDestroy(g);
-        cudaGetLastError();
-        return fail(h, DEC_ECUDA, "batched decode capture: %s",
-                    cudaGetErrorString(le != cudaSuccess ? le : e));
-      }
-      h->bgraph_src = g;
-      cudaGraphNode_t roots[4];
-      size_t nroots = 4;
-      e = cudaGraphGetRootNodes(g, roots, &nroots);
-      if (e != cudaSuccess || nroots != 1) {
-        drop_graph(h);
-        return fail(h, DEC_ECUDA, "batched decode graph: expected one root node (%s)", cudaGetErrorString(e));
-      }
-      h->bgraph_setup = roots[0];
-      e = cudaGraphInstantiate(&h->bgraph, g, 0);
-      if (e != cudaSuccess) {
-        drop_graph(h);
-        return fail(h, DEC_ECUDA, "batched graph instantiate: %s", cudaGetErrorString(e));
-      }
-      h->bgraph_batch = batch;
-      h->bgraph_tokens = d_tokens;
-      h->bgraph_logits = logits;
-      h->bgraph_argmax = d_argmax;
-    }
-    cudaError_t e = update_rows_setup_node(h->bgraph, h->bgraph_setup, h->m, meta, d_tokens, batch);
-    if (e != cudaSuccess) return fail(h, DEC_ECUDA, "batched graph update: %s", cudaGetErrorString(e));
-    e = cudaGraphLaunch(h->bgraph, h->stream);
-    if (e != cudaSuccess) return fail(h, DEC_ECUDA, "batched graph launch: %s", cudaGetErrorString(e));
-    h->timing.n = h->bgraph_timed_pairs;
-    h->launches += h->bgraph_kernels;
-    timing_finish(h);
-  }
+  const dec_status st = run_rows(h, batch, seqs, positions, d_tokens, 0, logits, d_argmax);
+  if (st != DEC_OK) return st;
   for (int32_t i = 0; i < batch; ++i) h->lens[seqs[i]] = positions[i] + 1;
   return DEC_OK;
 }

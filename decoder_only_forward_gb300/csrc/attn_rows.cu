@@ -26,30 +26,77 @@ __device__ __forceinline__ int ar_swz(int row, int c) {
   return c ^ (row & M);
 }
 
-template <typename KV, int HD>
+// 16 int8 codes of one scale group read back as code * s.  A code c becomes a
+// float without a conversion instruction: the byte c ^ 0x80 = c + 128 (0..255)
+// is placed under the exponent of 2^23, giving the float 2^23 + c + 128
+// exactly, and 2^23 + 128 is subtracted (exact for every c).
+__device__ __forceinline__ void widen_i8(const uint4& u, float s, float* f) {
+  const uint32_t w[4] = {u.x ^ 0x80808080u, u.y ^ 0x80808080u, u.z ^ 0x80808080u, u.w ^ 0x80808080u};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    // bytes of the result: (byte i & 3 of the word, 0x00, 0x00, 0x4B)
+    const uint32_t bits = __byte_perm(w[i >> 2], 0x4B000000u, 0x7540u + (i & 3));
+    f[i] = __fmul_rn(__int_as_float(bits) - 8388736.0f, s);
+  }
+}
+
+// Shared-memory layout of one CTA (G query heads per kv head):
+//   qs   [G][C4] float4        scaled queries
+//   kv   [2][AR_TILE][C4]      K (swizzled) and V of the tile; reused at the end
+//                              for the cross-warp sum of the outputs [4][G][C4]
+//   red  [4][G][AR_TILE] f32   per-warp partial scores
+//   ps   [AR_TILE][AR_PSW] f32 softmax weights of the tile, key-major
+//   mrow, lrow, alpha [G]
+constexpr int AR_PSW = 20;   // >= MAX_GROUP, a multiple of 4 (float4 rows)
+
+template <int HD>
+__host__ __device__ constexpr size_t ar_smem_bytes(int G) {
+  return 16 * ((size_t)G * (HD / 4) + 2 * (size_t)AR_TILE * (HD / 4)) +
+         4 * (4 * (size_t)G * AR_TILE + (size_t)AR_TILE * AR_PSW + 3 * (size_t)G);
+}
+
+// KV: float, __nv_bfloat16 or int8_t (rows of the int8 format: scales, then
+// codes at byte code_off; qgroup channels per scale).  Rows are row_bytes apart.
+//
+// Work split inside a 32-key tile: for the scores, warp w takes a quarter of
+// head_dim for all 32 keys (lane = key) and all G heads, so each K chunk read
+// from shared memory serves every head; the partial dot products meet in
+// shared memory.  For P.V, warp w takes a quarter of the keys, each lane one
+// float4 of head_dim for all G heads, so each V chunk serves every head; the
+// warps' sums meet once, after the last tile.
+// NHG: head groups of 4 held in registers (G <= 4 * NHG).
+template <typename KV, int HD, int NHG>
 __global__ void __launch_bounds__(AR_THREADS) k_attn_rows(
-    const float* __restrict__ Q, const KV* __restrict__ kc, const KV* __restrict__ vc, size_t ring_elems,
-    const int32_t* __restrict__ seq, const int32_t* __restrict__ pos, int nq, int nkv, int max_seq, int sliding,
-    float* __restrict__ part) {
-  constexpr int CE = 16 / sizeof(KV);     // elements per 16-byte global chunk
+    const float* __restrict__ Q, const char* __restrict__ kc, const char* __restrict__ vc, size_t ring_bytes,
+    int row_bytes, int code_off, int qgroup, const int32_t* __restrict__ seq, const int32_t* __restrict__ pos, int nq,
+    int nkv, int max_seq, int sliding, float* __restrict__ part) {
+  constexpr bool I8 = std::is_same<KV, int8_t>::value;
+  constexpr int CE = I8 ? 16 : 16 / (int)sizeof(KV);   // elements per 16-byte global chunk
   constexpr int CPR = HD / CE;            // global chunks per row
   constexpr int C4 = HD / 4;              // float4 chunks per row
+  constexpr int CW = C4 / 4;              // score chunks per warp
   constexpr int LPT = (AR_TILE * CPR + AR_THREADS - 1) / AR_THREADS;
-  constexpr int R = (MAX_GROUP * C4 + AR_THREADS - 1) / AR_THREADS;   // (head, chunk) slots per thread
-  __shared__ __align__(16) float4 qs[MAX_GROUP][C4];
-  __shared__ __align__(16) float4 ks[AR_TILE][C4];
-  __shared__ __align__(16) float4 vs[AR_TILE][C4];
-  __shared__ float ps[MAX_GROUP][AR_TILE + 1];
-  __shared__ float mrow[MAX_GROUP], lrow[MAX_GROUP], alpha[MAX_GROUP];
+  constexpr int KPP = 32 / C4;            // keys per P.V pass of a warp (lanes: chunk, key)
+  extern __shared__ __align__(16) uint8_t ar_smem[];
 
   const int g = blockIdx.x, split = blockIdx.y, nsplit = gridDim.y, b = blockIdx.z;
-  const int G = nq / nkv, kd = nkv * HD;
+  const int G = nq / nkv;
+  float4* qs = reinterpret_cast<float4*>(ar_smem);                      // [G][C4]
+  float4* kvb = qs + (size_t)G * C4;                                     // [2][AR_TILE][C4]
+  float4* ks = kvb;
+  float4* vs = kvb + AR_TILE * C4;
+  float* red = reinterpret_cast<float*>(kvb + 2 * AR_TILE * C4);        // [4][G][AR_TILE]
+  float* ps = red + 4 * G * AR_TILE;                                     // [AR_TILE][AR_PSW]
+  float* mrow = ps + AR_TILE * AR_PSW;
+  float* lrow = mrow + G;
+  float* alpha = lrow + G;
+
   const int p = pos[b];
   const int m = sliding > 0 ? min(p + 1, max_seq) : p + 1;
   const int per = ((m + nsplit - 1) / nsplit + AR_TILE - 1) / AR_TILE * AR_TILE;
   const int j0 = split * per, j1 = min(m, j0 + per);
-  const KV* K = kc + (size_t)seq[b] * ring_elems;
-  const KV* V = vc + (size_t)seq[b] * ring_elems;
+  const char* K = kc + (size_t)seq[b] * ring_bytes;
+  const char* V = vc + (size_t)seq[b] * ring_bytes;
   const float* q = Q + (size_t)b * nq * HD + (size_t)g * G * HD;
   const float scale = 1.0f / sqrtf((float)HD);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -60,27 +107,38 @@ __global__ void __launch_bounds__(AR_THREADS) k_attn_rows(
     v.y *= scale;
     v.z *= scale;
     v.w *= scale;
-    qs[i / C4][i % C4] = v;
+    qs[i] = v;
   }
-  if (tid < MAX_GROUP) {
+  if (tid < G) {
     mrow[tid] = -INFINITY;
     lrow[tid] = 0.f;
   }
-  float4 acc[R];
+  // P.V accumulators: head group hg, head u of the group, float4 chunk pc.
+  const int pc = lane % C4, pr = lane / C4;
+  float4 acc[NHG][4];
 #pragma unroll
-  for (int r = 0; r < R; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int hg = 0; hg < NHG; ++hg)
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc[hg][u] = make_float4(0.f, 0.f, 0.f, 0.f);
 
   // The next tile's K/V chunks are loaded into registers while the current
   // tile is scored from shared memory.
   uint4 kr[LPT], vr[LPT];
+  float ksc[LPT], vsc[LPT];   // int8: the chunk's group scale
   auto load = [&](int t0) {
 #pragma unroll
     for (int j = 0; j < LPT; ++j) {
       const int i = tid + j * AR_THREADS, row = i / CPR, c = i % CPR;
       if (i < AR_TILE * CPR && t0 + row < j1) {
-        const size_t off = (size_t)(t0 + row) * kd + (size_t)g * HD + c * CE;
+        const size_t rb = (size_t)(t0 + row) * row_bytes;
+        const int ch = g * HD + c * CE;   // first channel of the chunk
+        const size_t off = I8 ? rb + code_off + ch : rb + (size_t)ch * sizeof(KV);
         kr[j] = __ldcs(reinterpret_cast<const uint4*>(K + off));
         vr[j] = __ldcs(reinterpret_cast<const uint4*>(V + off));
+        if constexpr (I8) {
+          ksc[j] = __ldcs(reinterpret_cast<const float*>(K + rb) + ch / qgroup);
+          vsc[j] = __ldcs(reinterpret_cast<const float*>(V + rb) + ch / qgroup);
+        }
       }
     }
   };
@@ -93,38 +151,59 @@ __global__ void __launch_bounds__(AR_THREADS) k_attn_rows(
       const int i = tid + j * AR_THREADS, row = i / CPR, c = i % CPR;
       if (i < AR_TILE * CPR && row < nt) {
         float kf[CE], vf[CE];
-        Chunk<KV>::widen(kr[j], kf);
-        Chunk<KV>::widen(vr[j], vf);
+        if constexpr (I8) {
+          widen_i8(kr[j], ksc[j], kf);
+          widen_i8(vr[j], vsc[j], vf);
+        } else {
+          Chunk<KV>::widen(kr[j], kf);
+          Chunk<KV>::widen(vr[j], vf);
+        }
 #pragma unroll
         for (int h4 = 0; h4 < CE / 4; ++h4) {
           const int c4 = c * (CE / 4) + h4;
-          ks[row][ar_swz<HD>(row, c4)] = make_float4(kf[4 * h4], kf[4 * h4 + 1], kf[4 * h4 + 2], kf[4 * h4 + 3]);
-          vs[row][c4] = make_float4(vf[4 * h4], vf[4 * h4 + 1], vf[4 * h4 + 2], vf[4 * h4 + 3]);
+          ks[row * C4 + ar_swz<HD>(row, c4)] =
+              make_float4(kf[4 * h4], kf[4 * h4 + 1], kf[4 * h4 + 2], kf[4 * h4 + 3]);
+          vs[row * C4 + c4] = make_float4(vf[4 * h4], vf[4 * h4 + 1], vf[4 * h4 + 2], vf[4 * h4 + 3]);
         }
       }
     }
     __syncthreads();
     if (t0 + AR_TILE < j1) load(t0 + AR_TILE);
-    // Scores: warp per head, lane per key; float4 reads of the key row and a
-    // broadcast of the query.
+    // Partial scores: key = lane, chunks [warp*CW, warp*CW + CW), all heads.
+#pragma unroll
+    for (int hg = 0; hg < NHG; ++hg) {
+      if (hg * 4 < G) {
+        float sp[4] = {0.f, 0.f, 0.f, 0.f};
+        if (lane < nt) {
+#pragma unroll
+          for (int cc = 0; cc < CW; ++cc) {
+            const int c = warp * CW + cc;
+            const float4 kv = ks[lane * C4 + ar_swz<HD>(lane, c)];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (hg * 4 + u < G) {
+                const float4 qv = qs[(hg * 4 + u) * C4 + c];
+                sp[u] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, fmaf(qv.z, kv.z, fmaf(qv.w, kv.w, sp[u]))));
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (hg * 4 + u < G) red[(warp * G + hg * 4 + u) * AR_TILE + lane] = sp[u];
+      }
+    }
+    __syncthreads();
+    // Scores, online softmax: warp per head, lane per key.
     for (int hh = warp; hh < G; hh += AR_THREADS / 32) {
       float s = -INFINITY;
-      if (lane < nt) {
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll 8
-        for (int c = 0; c < C4; ++c) {
-          const float4 kv = ks[lane][ar_swz<HD>(lane, c)], qv = qs[hh][c];
-          s0 = fmaf(qv.x, kv.x, s0);
-          s1 = fmaf(qv.y, kv.y, s1);
-          s0 = fmaf(qv.z, kv.z, s0);
-          s1 = fmaf(qv.w, kv.w, s1);
-        }
-        s = s0 + s1;
-      }
+      if (lane < nt)
+        s = red[(0 * G + hh) * AR_TILE + lane] + red[(1 * G + hh) * AR_TILE + lane] +
+            red[(2 * G + hh) * AR_TILE + lane] + red[(3 * G + hh) * AR_TILE + lane];
       const float mnew = fmaxf(mrow[hh], warp_max(s));
       const float e = lane < nt ? __expf(s - mnew) : 0.f;
       const float esum = warp_sum(e);
-      ps[hh][lane] = e;
+      ps[lane * AR_PSW + hh] = e;
       __syncwarp();
       if (lane == 0) {
         const float a = __expf(mrow[hh] - mnew);
@@ -134,44 +213,85 @@ __global__ void __launch_bounds__(AR_THREADS) k_attn_rows(
       }
     }
     __syncthreads();
-    // Weighted sum of V: slot (head, float4 chunk) per thread.
+    // P.V: this warp's keys of the tile, lane = (chunk pc, key pr of the pass).
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int slot = tid + r * AR_THREADS;
-      if (slot < G * C4) {
-        const int hh = slot / C4, c = slot % C4;
-        const float a = alpha[hh];
-        float4 o = acc[r];
-        o.x *= a;
-        o.y *= a;
-        o.z *= a;
-        o.w *= a;
-        for (int j = 0; j < nt; ++j) {
-          const float pj = ps[hh][j];
-          const float4 v = vs[j][c];
-          o.x = fmaf(pj, v.x, o.x);
-          o.y = fmaf(pj, v.y, o.y);
-          o.z = fmaf(pj, v.z, o.z);
-          o.w = fmaf(pj, v.w, o.w);
+    for (int hg = 0; hg < NHG; ++hg) {
+      if (hg * 4 < G) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (hg * 4 + u < G) {
+            const float a = alpha[hg * 4 + u];
+            acc[hg][u].x *= a;
+            acc[hg][u].y *= a;
+            acc[hg][u].z *= a;
+            acc[hg][u].w *= a;
+          }
         }
-        acc[r] = o;
       }
     }
+    for (int kg = warp; kg * KPP < nt; kg += 4) {
+      const int j = kg * KPP + pr;
+      if (j < nt) {
+        const float4 v = vs[j * C4 + pc];
+#pragma unroll
+        for (int hg = 0; hg < NHG; ++hg) {
+          if (hg * 4 < G) {
+            const float4 pw = *reinterpret_cast<const float4*>(ps + j * AR_PSW + hg * 4);
+            const float pu[4] = {pw.x, pw.y, pw.z, pw.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              acc[hg][u].x = fmaf(pu[u], v.x, acc[hg][u].x);
+              acc[hg][u].y = fmaf(pu[u], v.y, acc[hg][u].y);
+              acc[hg][u].z = fmaf(pu[u], v.z, acc[hg][u].z);
+              acc[hg][u].w = fmaf(pu[u], v.w, acc[hg][u].w);
+            }
+          }
+        }
+      }
+    }
+  }
+  // Lanes holding the same chunk for different keys, then the four warps.
+#pragma unroll
+  for (int o = C4; o < 32; o <<= 1) {
+#pragma unroll
+    for (int hg = 0; hg < NHG; ++hg) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc[hg][u].x += __shfl_xor_sync(0xffffffffu, acc[hg][u].x, o);
+        acc[hg][u].y += __shfl_xor_sync(0xffffffffu, acc[hg][u].y, o);
+        acc[hg][u].z += __shfl_xor_sync(0xffffffffu, acc[hg][u].z, o);
+        acc[hg][u].w += __shfl_xor_sync(0xffffffffu, acc[hg][u].w, o);
+      }
+    }
+  }
+  __syncthreads();   // the tile buffers become the cross-warp sum [4][G][C4]
+  float4* sum4 = kvb;
+  if (pr == 0) {
+#pragma unroll
+    for (int hg = 0; hg < NHG; ++hg)
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (hg * 4 + u < G) sum4[(warp * G + hg * 4 + u) * C4 + pc] = acc[hg][u];
   }
   __syncthreads();
   // part[((b*nq + head) * nsplit + split) * (HD+2) + {0..HD-1: output, HD: max, HD+1: sum}];
   // an empty split leaves (-inf, 0, zeros), which the merge skips.
+  for (int i = tid; i < G * C4; i += AR_THREADS) {
+    const int hh = i / C4, c = i % C4;
+    float4 o = sum4[(0 * G + hh) * C4 + c];
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int slot = tid + r * AR_THREADS;
-    if (slot < G * C4) {
-      const int hh = slot / C4, c = slot % C4;
-      float* pp = part + (((size_t)b * nq + g * G + hh) * nsplit + split) * (HD + 2) + 4 * c;
-      pp[0] = acc[r].x;
-      pp[1] = acc[r].y;
-      pp[2] = acc[r].z;
-      pp[3] = acc[r].w;
+    for (int w2 = 1; w2 < 4; ++w2) {
+      const float4 t = sum4[(w2 * G + hh) * C4 + c];
+      o.x += t.x;
+      o.y += t.y;
+      o.z += t.z;
+      o.w += t.w;
     }
+    float* pp = part + (((size_t)b * nq + g * G + hh) * nsplit + split) * (HD + 2) + 4 * c;
+    pp[0] = o.x;
+    pp[1] = o.y;
+    pp[2] = o.z;
+    pp[3] = o.w;
   }
   if (tid < G) {
     float* pp = part + (((size_t)b * nq + g * G + tid) * nsplit + split) * (HD + 2);
@@ -209,33 +329,48 @@ int attn_rows_splits(const dec_config& c) {
   return ns < 1 ? 1 : (ns > AR_MAX_SPLIT ? AR_MAX_SPLIT : ns);
 }
 
+template <typename KV, int HD, int NHG>
+static void attn_rows_g(const dec_config& c, const float* Q, const void* kc, const void* vc, size_t ring_bytes,
+                        const int32_t* seq, const int32_t* pos, int B, int nsplit, float* part, cudaStream_t s) {
+  const KvRowLayout L = kv_row_layout(c);
+  const dim3 grid(c.n_kv_heads, nsplit, B);
+  const size_t smem = ar_smem_bytes<HD>(c.n_heads / c.n_kv_heads);
+  if (smem > 48 * 1024)
+    cudaFuncSetAttribute(k_attn_rows<KV, HD, NHG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  k_attn_rows<KV, HD, NHG><<<grid, AR_THREADS, smem, s>>>(Q, (const char*)kc, (const char*)vc, ring_bytes, L.bytes, L.code_off,
+                                                  L.group, seq, pos, c.n_heads, c.n_kv_heads, c.max_seq,
+                                                  c.sliding_window, part);
+}
+
 template <typename KV, int HD>
 static void attn_rows(const dec_config& c, const float* Q, const void* kc, const void* vc, size_t ring_bytes,
                       const int32_t* seq, const int32_t* pos, int B, int nsplit, float* part, RowOut out,
                       cudaStream_t s) {
-  const dim3 grid(c.n_kv_heads, nsplit, B);
-  k_attn_rows<KV, HD><<<grid, AR_THREADS, 0, s>>>(Q, (const KV*)kc, (const KV*)vc, ring_bytes / sizeof(KV), seq,
-                                                  pos, c.n_heads, c.n_kv_heads, c.max_seq, c.sliding_window, part);
+  const int G = c.n_heads / c.n_kv_heads;
+  if (G <= 4) attn_rows_g<KV, HD, 1>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, s);
+  else if (G <= 8) attn_rows_g<KV, HD, 2>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, s);
+  else attn_rows_g<KV, HD, 4>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, s);
   k_attn_rows_merge<HD><<<dim3(c.n_heads, B), HD, 0, s>>>(part, c.n_heads, nsplit, out);
+}
+
+template <int HD>
+static void attn_rows_hd(const dec_config& c, const float* Q, const void* kc, const void* vc, size_t ring_bytes,
+                         const int32_t* seq, const int32_t* pos, int B, int nsplit, float* part, RowOut out,
+                         cudaStream_t s) {
+  if (c.kv_dtype == DEC_BF16)
+    attn_rows<__nv_bfloat16, HD>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s);
+  else if (c.kv_dtype == DEC_I8)
+    attn_rows<int8_t, HD>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s);
+  else
+    attn_rows<float, HD>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s);
 }
 
 void launch_attn_rows(const dec_config& c, const float* Q, const void* kc, const void* vc, size_t ring_bytes,
                       const int32_t* seq, const int32_t* pos, int B, int nsplit, float* part, RowOut out,
                       cudaStream_t s) {
-  const bool kb = c.kv_dtype == DEC_BF16;
-  switch (c.head_dim) {
-    case 16:
-      kb ? attn_rows<__nv_bfloat16, 16>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s)
-         : attn_rows<float, 16>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s);
-      break;
-    case 64:
-      kb ? attn_rows<__nv_bfloat16, 64>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s)
-         : attn_rows<float, 64>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s);
-      break;
-    default:
-      kb ? attn_rows<__nv_bfloat16, 128>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s)
-         : attn_rows<float, 128>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s);
-  }
+  if (c.head_dim == 16) attn_rows_hd<16>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s);
+  else if (c.head_dim == 64) attn_rows_hd<64>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s);
+  else attn_rows_hd<128>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s);
 }
 
 }  // namespace dec

@@ -38,12 +38,12 @@ __global__ void k_rope_rows(const double* __restrict__ inv_freq, int half, int s
 // value), its token id (an id outside [0, vocab) becomes 0 and raises
 // ERR_TOKEN) and the (cos, sin) table of the row's own position.
 __global__ void k_rows_setup(const __grid_constant__ RowsMeta meta, int B, const int32_t* __restrict__ d_tokens,
-                             int vocab, const double* __restrict__ inv_freq, int half, int32_t* __restrict__ tokens,
+                             int32_t host_token, int vocab, const double* __restrict__ inv_freq, int half, int32_t* __restrict__ tokens,
                              int32_t* __restrict__ b_seq, int32_t* __restrict__ b_pos, int32_t* __restrict__ b_rows,
                              float2* __restrict__ tab, DeviceState* st) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < B) {
-    int t = d_tokens[i];
+    int t = d_tokens ? d_tokens[i] : host_token;
     if (t < 0 || t >= vocab) {
       raise_error(st, ERR_TOKEN, 0);
       t = 0;
@@ -609,8 +609,12 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n,
   count_launch(m, 2);
 
   // Ring slots equal positions unless this chunk can overwrite history it reads.
-  const bool direct = c.sliding_window == 0 || start + n <= c.max_seq;
-  const int h0 = direct ? 0 : (start - c.sliding_window + 1 > 0 ? start - c.sliding_window + 1 : 0);
+  // An int8 cache always takes the linear f32 rows: history read back from the
+  // ring, the chunk's rows quantised and read back before attention.
+  const bool i8 = c.kv_dtype == DEC_I8;
+  const bool direct = !i8 && (c.sliding_window == 0 || start + n <= c.max_seq);
+  const int h0 = direct || c.sliding_window == 0 ? 0
+                 : (start - c.sliding_window + 1 > 0 ? start - c.sliding_window + 1 : 0);
   const int hist = start - h0;
 
   const Act a_h{S.A, split, n, h};      // normalised rows
@@ -625,7 +629,8 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n,
     KV* kdst = direct ? kc : (KV*)S.KVlin_k;
     KV* vdst = direct ? vc : (KV*)S.KVlin_v;
     if (!direct && hist > 0) {
-      k_kv_gather<KV><<<152, 256, 0, s>>>(kc, vc, c.max_seq, kd, h0, hist, kdst, vdst);
+      if (i8) launch_kv_gather_i8(c, kc, vc, h0, hist, (float*)kdst, (float*)vdst, s);
+      else k_kv_gather<KV><<<152, 256, 0, s>>>(kc, vc, c.max_seq, kd, h0, hist, kdst, vdst);
       count_launch(m);
     }
     {
@@ -649,9 +654,18 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n,
       e.kv_row0 = direct ? start : hist;
       chk(gemm<TW>(m, s, a_h, (const TW*)L.wqkv, n, qd + 2 * kd, h, e, 1, n));
     }
+    const int t_first = n > c.max_seq ? n - c.max_seq : 0;
+    if (i8) {
+      // Codes of the rows whose slot survives the chunk go to the ring; every
+      // row's read-back replaces it in the linear rows, so attention sees what
+      // the cache holds.
+      float* lk = (float*)kdst + (size_t)hist * kd;
+      float* lv = (float*)vdst + (size_t)hist * kd;
+      launch_kv_quant(c, lk, lv, n, nullptr, start, t_first, kc, vc, lk, lv, s);
+      count_launch(m);
+    }
     chk(attention<KV>(m, s, kdst, vdst, direct ? 0 : h0, start, n, a_q.out()));
-    if (!direct) {
-      const int t_first = n > c.max_seq ? n - c.max_seq : 0;
+    if (!direct && !i8) {
       k_kv_commit<KV><<<152, 256, 0, s>>>(kdst, vdst, hist, start, t_first, n, c.max_seq, kd, kc, vc);
       count_launch(m);
     }
@@ -670,6 +684,7 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n,
 
 cudaError_t launch_prefill_chunk(const Model& m, cudaStream_t s, int seq, int n, int start, float* logits,
                                  int32_t* d_argmax) {
+  // An int8 cache runs on f32 linear rows (KV = float here).
   const bool wb = m.cfg.weight_dtype == DEC_BF16, kb = m.cfg.kv_dtype == DEC_BF16;
   if (wb && kb) return prefill_chunk<__nv_bfloat16, __nv_bfloat16>(m, s, seq, n, start, logits, d_argmax);
   if (wb) return prefill_chunk<__nv_bfloat16, float>(m, s, seq, n, start, logits, d_argmax);
@@ -703,6 +718,7 @@ static cudaError_t decode_rows(const Model& m, cudaStream_t s, int B, float* log
   const Act a_h{S.A, split, B, h};
   const Act a_q{S.A, split, B, qd};
   const int nsplit = attn_rows_splits(c);
+  const bool i8 = c.kv_dtype == DEC_I8;
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerPtrs& L = m.layers[l];
     k_rmsnorm_rows<<<B, 256, 0, s>>>(S.X, L.attn_norm, c.rms_eps, h, a_h.out());
@@ -717,11 +733,18 @@ static cudaError_t decode_rows(const Model& m, cudaStream_t s, int B, float* log
       e.kd = kd;
       e.hd = hd;
       e.q_out = S.Q;
-      e.k_dst = L.kc;
-      e.v_dst = L.vc;
+      // int8 cache: f32 K/V rows to the linear scratch, quantised into the
+      // rings below; else straight into each row's ring.
+      e.k_dst = i8 ? S.KVlin_k : L.kc;
+      e.v_dst = i8 ? S.KVlin_v : L.vc;
       e.kv_bf16 = std::is_same<KV, __nv_bfloat16>::value;
-      e.kv_rows = S.b_rows;
+      e.kv_rows = i8 ? nullptr : S.b_rows;
       chk(gemm<TW>(m, s, a_h, (const TW*)L.wqkv, B, qd + 2 * kd, h, e, 1, B));
+    }
+    if (i8) {
+      launch_kv_quant(c, (const float*)S.KVlin_k, (const float*)S.KVlin_v, B, S.b_rows, 0, 0, L.kc, L.vc, nullptr,
+                      nullptr, s);
+      count_launch(m);
     }
     timer_begin(m, DEC_K_ATTN, s);
     launch_attn_rows(c, S.Q, L.kc, L.vc, m.ring_bytes, S.b_seq, S.b_pos, B, nsplit, S.b_part, a_q.out(), s);
@@ -767,9 +790,10 @@ static int rows_setup_blocks(const Model& m, int B) {
   return (n + 255) / 256;
 }
 
-cudaError_t launch_rows_setup(const Model& m, cudaStream_t s, const RowsMeta& meta, const int32_t* d_tokens, int B) {
+cudaError_t launch_rows_setup(const Model& m, cudaStream_t s, const RowsMeta& meta, const int32_t* d_tokens,
+                              int32_t host_token, int B) {
   const Scratch& S = m.s;
-  k_rows_setup<<<rows_setup_blocks(m, B), 256, 0, s>>>(meta, B, d_tokens, m.cfg.vocab, S.inv_freq,
+  k_rows_setup<<<rows_setup_blocks(m, B), 256, 0, s>>>(meta, B, d_tokens, host_token, m.cfg.vocab, S.inv_freq,
                                                        m.cfg.head_dim / 2, S.tokens, S.b_seq, S.b_pos, S.b_rows,
                                                        S.rope_tab, S.st);
   count_launch(m);
@@ -777,14 +801,15 @@ cudaError_t launch_rows_setup(const Model& m, cudaStream_t s, const RowsMeta& me
 }
 
 cudaError_t update_rows_setup_node(cudaGraphExec_t g, cudaGraphNode_t node, const Model& m, const RowsMeta& meta,
-                                   const int32_t* d_tokens, int B) {
+                                   const int32_t* d_tokens, int32_t host_token, int B) {
   const Scratch& S = m.s;
   int vocab = m.cfg.vocab, half = m.cfg.head_dim / 2;
   const double* inv = S.inv_freq;
   int32_t *tokens = S.tokens, *bs = S.b_seq, *bp = S.b_pos, *br = S.b_rows;
   float2* tab = S.rope_tab;
   DeviceState* st = S.st;
-  void* args[] = {const_cast<RowsMeta*>(&meta), &B, &d_tokens, &vocab, &inv, &half, &tokens, &bs, &bp, &br, &tab, &st};
+  void* args[] = {const_cast<RowsMeta*>(&meta), &B, &d_tokens, &host_token, &vocab, &inv, &half, &tokens, &bs, &bp,
+                  &br, &tab, &st};
   cudaKernelNodeParams p = {};
   p.func = reinterpret_cast<void*>(k_rows_setup);
   p.gridDim = dim3(rows_setup_blocks(m, B));

@@ -192,6 +192,35 @@ void launch_decode_body(const Model& m, cudaStream_t s, const int32_t* d_token, 
 // Host handle of the setup kernel (for updating its node in a captured graph).
 const void* set_step_kernel();
 
+// int8 K/V rows (kv_int8.cu): [scales: kd/G f32, padded to 16 B][codes: kd
+// int8, padded to 16 B], G the largest power of two dividing head_dim, <= 32.
+struct KvRowLayout {
+  int bytes;      // one ring row
+  int code_off;   // bytes before the codes (the scales' area)
+  int group;      // channels per scale
+};
+inline int kv_group_size(int hd) {
+  int g = 1;
+  while (g < 32 && hd % (2 * g) == 0) g *= 2;
+  return g;
+}
+inline KvRowLayout kv_row_layout(const dec_config& c) {
+  const int kd = c.n_kv_heads * c.head_dim;
+  if (c.kv_dtype != DEC_I8) return KvRowLayout{kd * (c.kv_dtype == DEC_BF16 ? 2 : 4), 0, 1};
+  const int g = kv_group_size(c.head_dim);
+  const int sb = (kd / g * 4 + 15) / 16 * 16;
+  return KvRowLayout{sb + (kd + 15) / 16 * 16, sb, g};
+}
+// f32 rows -> int8 ring rows (dst_rows[r], or the slot of position pos0 + r);
+// rows below t_first are not stored; rt_k/rt_v (nullable) get the values read
+// back.  planes: 2 = K and V, 1 = K only.
+void launch_kv_quant(const dec_config& c, const float* src_k, const float* src_v, int n, const int32_t* dst_rows,
+                     int pos0, int t_first, void* ring_k, void* ring_v, float* rt_k, float* rt_v, cudaStream_t s,
+                     int planes = 2);
+// int8 ring rows of positions h0 .. h0+count-1 -> f32 rows.
+void launch_kv_gather_i8(const dec_config& c, const void* ring_k, const void* ring_v, int h0, int count,
+                         float* lin_k, float* lin_v, cudaStream_t s);
+
 // Persistent single-kernel decode step (decode_mk.cu).
 size_t mk_smem_bytes(const dec_config& c, int nsplit);
 size_t mk_maps_bytes(const dec_config& c);
@@ -221,10 +250,12 @@ struct RowsMeta {
   int32_t pos[MAX_BATCH];
   int32_t rows[MAX_BATCH];   // seq * ring_rows + slot(pos)
 };
-cudaError_t launch_rows_setup(const Model& m, cudaStream_t s, const RowsMeta& meta, const int32_t* d_tokens, int B);
+// d_tokens == nullptr: one row whose token is host_token.
+cudaError_t launch_rows_setup(const Model& m, cudaStream_t s, const RowsMeta& meta, const int32_t* d_tokens,
+                              int32_t host_token, int B);
 // Points a captured setup node (of a graph captured for the same B) at new rows.
 cudaError_t update_rows_setup_node(cudaGraphExec_t g, cudaGraphNode_t node, const Model& m, const RowsMeta& meta,
-                                   const int32_t* d_tokens, int B);
+                                   const int32_t* d_tokens, int32_t host_token, int B);
 
 struct RowOut;
 // Batched decode attention (attn_rows.cu): rotated queries Q [B][nq*hd] f32,
@@ -266,8 +297,10 @@ cudaError_t launch_attn_prefill_tc(const AttnTcPlanes& pl, int n, int start, int
                                    int sliding, RowOut out, DeviceState* st, cudaStream_t s);
 cudaError_t launch_kv_split(const float* K, const float* V, int kd, int r0, int r1, const AttnTcPlanes& pl,
                             cudaStream_t s);
+// The tensor-core prefill attention reads f32 K/V rows: the f32 cache itself,
+// or the f32 read-back of an int8 cache.
 inline bool attn_tc_supported(const dec_config& c) {
-  return c.kv_dtype == DEC_F32 && (c.head_dim == 64 || c.head_dim == 128);
+  return c.kv_dtype != DEC_BF16 && (c.head_dim == 64 || c.head_dim == 128);
 }
 
 // Copies one layer's wqkv (and bqkv) with the q/k rows of every head permuted

@@ -20,7 +20,8 @@ from . import synthetic
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdec.so")
 
 DEC_OK, DEC_EINVAL, DEC_ERANGE, DEC_ECUDA, DEC_ETIMEOUT, DEC_ENOMEM = range(6)
-DEC_F32, DEC_BF16 = 0, 1
+DEC_F32, DEC_BF16, DEC_I8 = 0, 1, 2
+KV_DTYPES = {"f32": DEC_F32, "bf16": DEC_BF16, "i8": DEC_I8}
 DEC_FUSED_OFF, DEC_FUSED_GRID, DEC_FUSED_CLUSTER = 0, 1, 2
 FUSED_MODES = {"off": DEC_FUSED_OFF, "grid": DEC_FUSED_GRID, "cluster": DEC_FUSED_CLUSTER}
 STATUS_NAMES = {0: "DEC_OK", 1: "DEC_EINVAL", 2: "DEC_ERANGE", 3: "DEC_ECUDA", 4: "DEC_ETIMEOUT", 5: "DEC_ENOMEM"}
@@ -29,7 +30,8 @@ EXPORTED = ["dec_config_validate", "dec_workspace_bytes", "dec_create", "dec_pre
             "dec_decode_dev", "dec_kv_reset", "dec_length", "dec_kv_layer", "dec_set_trace",
             "dec_check", "dec_timing_enable", "dec_timing_read", "dec_launch_count", "dec_destroy",
             "dec_last_error", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc", "dec_gemm_bf16", "dec_set_graph", "dec_set_fused", "dec_fused_available", "dec_fused_mode", "dec_phase_stamps",
-            "dec_prefill_seq", "dec_kv_reset_seq", "dec_length_seq", "dec_decode_batch", "dec_kv_layer_seq"]
+            "dec_prefill_seq", "dec_kv_reset_seq", "dec_length_seq", "dec_decode_batch", "dec_kv_layer_seq",
+            "dec_kv_quantize_int8"]
 
 KERNEL_CLASSES = {"qkv": 1, "attn": 2, "oproj": 3, "gateup": 4, "down": 5, "lmhead": 6, "router": 7,
                   "pf_gemm": 8, "pf_attn": 9, "step": 10}
@@ -92,6 +94,7 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "dec_length_seq": (I32, [P, I32]),
         "dec_decode_batch": (I32, [P, I32, ctypes.POINTER(I32), ctypes.POINTER(I32), P, P, P]),
         "dec_kv_layer_seq": (I32, [P, I32, I32, ctypes.POINTER(P), ctypes.POINTER(P)]),
+        "dec_kv_quantize_int8": (I32, [P, I32, I32, I32, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -118,7 +121,7 @@ def make_config(w: dict, kv_dtype: str = "f32", max_tokens: int = 0, n_seqs: int
     c.tied_embedding = int(bool(w["tied"]))
     c.qkv_bias = int(bool(w["qkv_bias"]))
     c.weight_dtype = DEC_F32 if w["dtype"] == "f32" else DEC_BF16
-    c.kv_dtype = DEC_F32 if kv_dtype == "f32" else DEC_BF16
+    c.kv_dtype = KV_DTYPES[kv_dtype]
     c.rms_eps = float(w["rms_eps"])
     c.rope_theta = float(w["rope_theta"])
     l3 = w.get("rope_llama3")
@@ -172,6 +175,45 @@ def gemm_bf16(a_hi: torch.Tensor, a_lo: Optional[torch.Tensor], b: torch.Tensor,
                            ctypes.c_void_p(s.cuda_stream))
     if st != DEC_OK:
         raise DecError(st, lib.dec_last_error(None).decode())
+
+
+def kv_int8_group(head_dim: int) -> int:
+    """Channels per scale of the int8 cache rows (the library's rule, restated for views)."""
+    g = 1
+    while g < 32 and head_dim % (2 * g) == 0:
+        g *= 2
+    return g
+
+
+def kv_int8_row_layout(n_kv_heads: int, head_dim: int) -> tuple:
+    """(row bytes, code offset, group) of the DEC_I8 row format of dec.h."""
+    kd = n_kv_heads * head_dim
+    g = kv_int8_group(head_dim)
+    sb = (kd // g * 4 + 15) // 16 * 16
+    return sb + (kd + 15) // 16 * 16, sb, g
+
+
+def split_int8_rows(rows: torch.Tensor, n_kv_heads: int, head_dim: int) -> tuple:
+    """uint8 rows of the DEC_I8 format -> (scales f32 [n, kd/g], codes int8 [n, kd]) views."""
+    kd = n_kv_heads * head_dim
+    _, off, g = kv_int8_row_layout(n_kv_heads, head_dim)
+    scales = rows[:, :kd // g * 4].contiguous().view(torch.float32)
+    codes = rows[:, off:off + kd].contiguous().view(torch.int8)
+    return scales, codes
+
+
+def kv_quantize_int8(x: torch.Tensor, n_kv_heads: int, head_dim: int,
+                     stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """dec_kv_quantize_int8: device f32 rows [n, n_kv_heads*head_dim] -> uint8 rows of the DEC_I8 format."""
+    n = x.shape[0]
+    rb, _, _ = kv_int8_row_layout(n_kv_heads, head_dim)
+    out = torch.zeros((n, rb), dtype=torch.uint8, device=x.device)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = lib.dec_kv_quantize_int8(x.data_ptr(), n, n_kv_heads, head_dim, out.data_ptr(),
+                                  ctypes.c_void_p(s.cuda_stream))
+    if st != DEC_OK:
+        raise DecError(st, lib.dec_last_error(None).decode())
+    return out
 
 
 def attend_scratch_bytes(nq: int, nkv: int, hd: int, max_seq: int) -> int:
@@ -252,7 +294,8 @@ class Decoder:
         self.ws_bytes = workspace_bytes(self.cfg)
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
         self.stream = stream if stream is not None else torch.cuda.Stream(device=self.device)
-        self.kv_torch_dtype = torch.float32 if kv_dtype == "f32" else torch.bfloat16
+        self.kv_dtype = kv_dtype
+        self.kv_torch_dtype = {"f32": torch.float32, "bf16": torch.bfloat16, "i8": torch.uint8}[kv_dtype]
         h = ctypes.c_void_p()
         st = lib.dec_create(ctypes.byref(self.cfg), ctypes.byref(self.weights.c), self.workspace.data_ptr(),
                             self.ws_bytes, ctypes.c_void_p(self.stream.cuda_stream), ctypes.byref(h))
@@ -339,17 +382,21 @@ class Decoder:
 
     def kv_layer(self, layer: int, seq: int = 0):
         """(K, V) rings of a layer (of sequence ``seq``) as [max_seq, n_kv_heads, head_dim] views of the
-        workspace."""
+        workspace; for an int8 cache, [max_seq, row_bytes] uint8 rows (see ``split_int8_rows``)."""
         k, v = ctypes.c_void_p(), ctypes.c_void_p()
         self._raise(lib.dec_kv_layer_seq(self.h, int(layer), int(seq), ctypes.byref(k), ctypes.byref(v)))
         base = self.workspace.data_ptr()
-        es = 4 if self.kv_torch_dtype == torch.float32 else 2
-        n = self.w["max_seq"] * self.w["n_kv_heads"] * self.w["head_dim"]
+        ms, nkv, hd = self.w["max_seq"], self.w["n_kv_heads"], self.w["head_dim"]
         views = []
         for p in (k.value, v.value):
             off = p - base
-            views.append(self.workspace[off:off + n * es].view(self.kv_torch_dtype)
-                         .view(self.w["max_seq"], self.w["n_kv_heads"], self.w["head_dim"]))
+            if self.kv_dtype == "i8":
+                rb = kv_int8_row_layout(nkv, hd)[0]
+                views.append(self.workspace[off:off + ms * rb].view(ms, rb))
+            else:
+                es = 4 if self.kv_torch_dtype == torch.float32 else 2
+                views.append(self.workspace[off:off + ms * nkv * hd * es].view(self.kv_torch_dtype)
+                             .view(ms, nkv, hd))
         return views[0], views[1]
 
     def set_trace(self, ids: Optional[torch.Tensor], logits: Optional[torch.Tensor], capacity: int) -> None:

@@ -45,7 +45,15 @@ typedef enum dec_status {
   DEC_ENOMEM = 5    /* the workspace is smaller than dec_workspace_bytes() */
 } dec_status;
 
-typedef enum dec_dtype { DEC_F32 = 0, DEC_BF16 = 1 } dec_dtype;
+typedef enum dec_dtype {
+  DEC_F32 = 0,
+  DEC_BF16 = 1,
+  DEC_I8 = 2   /* K/V cache only: int8 codes with one f32 scale per group of channels (rml "The decoder",
+                  KV cache): the group is the largest power of two dividing head_dim, at most 32; each
+                  group stored as round(x / s), s = max|x| / 127, in f32 with halves rounded away from
+                  zero and codes in [-127, 127]; read back as code * s.  A ring row is the row's scales
+                  (kd/group f32, padded to 16 bytes) then its codes (kd int8, padded to 16 bytes) */
+} dec_dtype;
 
 /*
  * Model configuration: sizes plus switches (rml "The decoder", The model
@@ -68,7 +76,9 @@ typedef struct dec_config {
   int32_t tied_embedding; /* 1: LM head = token embedding matrix */
   int32_t qkv_bias;       /* 1: bqkv present */
   int32_t weight_dtype;   /* DEC_F32 or DEC_BF16: projection, embedding, router, head matrices */
-  int32_t kv_dtype;       /* DEC_F32 or DEC_BF16: KV cache storage */
+  int32_t kv_dtype;       /* DEC_F32, DEC_BF16 or DEC_I8: KV cache storage.  With DEC_I8 every decode
+                             step (dec_decode, dec_decode_dev) runs the batched row kernels with one
+                             row; the fused schedules are not available */
   float rms_eps;
   float rope_theta;
   int32_t rope_llama3;    /* 1: llama3 frequency scaling with the four fields below */
@@ -201,7 +211,8 @@ dec_status dec_decode_batch(dec_handle *h, int32_t batch, const int32_t *seqs, c
                             const int32_t *d_tokens, float *logits, int32_t *d_argmax);
 
 /* Device pointers to layer's K and V rings, each [max_seq][n_kv_heads][head_dim]
- * of kv_dtype; position p lives in slot p % max_seq under a window, else slot p. */
+ * of kv_dtype (DEC_I8: max_seq rows of the int8 row format of dec_dtype);
+ * position p lives in slot p % max_seq under a window, else slot p. */
 dec_status dec_kv_layer(const dec_handle *h, int32_t layer, void **k, void **v);
 
 /* The same for sequence seq in [0, n_seqs) (dec_kv_layer is sequence 0). */
@@ -330,6 +341,14 @@ dec_status dec_attend_noalloc(const float *q, const void *k, const void *v, int3
                               int32_t n_kv_heads, int32_t head_dim, int32_t max_seq,
                               int32_t sliding_window, int32_t kv_dtype, int32_t pos, float *out,
                               void *cuda_stream);
+
+/* The int8 K/V quantiser of the cache, callable alone: rows x (device,
+ * [n_rows][n_kv_heads * head_dim] f32) -> out (device, n_rows rows of the
+ * DEC_I8 row format: scales then codes, see dec_dtype).  head_dim a multiple
+ * of 16, n_rows <= 65535.  Enqueued on cuda_stream.  Errors: DEC_EINVAL,
+ * DEC_ECUDA (messages via dec_last_error(NULL)). */
+dec_status dec_kv_quantize_int8(const float *x, int32_t n_rows, int32_t n_kv_heads, int32_t head_dim, void *out,
+                                void *cuda_stream);
 
 void dec_destroy(dec_handle *h);
 
