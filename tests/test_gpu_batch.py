@@ -254,3 +254,12 @@ def test_batch_device_token_out_of_range_reported(dec_mod):
         d.check()
     assert ei.value.status == dec_mod.DEC_EINVAL
     d.check()  # the flag was cleared by the report
+
+
+def test_smollm2_shape_batch_bf16_kv(dec_mod):
+    # bf16 rings with head_dim 64 take the compact-tile attention; 9 query heads over 3 kv heads.
+    w = synthetic.workload("smollm2-135m", n_layers=4)
+    prompts = [list(synthetic.prompt_tokens(w, n, seed=85 + i)) for i, n in enumerate([20, 77, 5])]
+    d = dec_mod.Decoder(w, n_seqs=3, kv_dtype="bf16")
+    rows, taus = batch_greedy(d, prompts, 6, order=[2, 0, 1])
+    _check_against_oracle(w, prompts, rows, taus, 6, "bf16")
