@@ -32,6 +32,15 @@ Per position p (absolute), per layer, pre-norm:
                                                               [PAN Mixture of Experts; RML Mixture of experts]
   logits = W_out rmsnorm(x, w_out)                             [PAN Forward Pass Flow]
 
+Optional norms (RML "The decoder", One forward pass, steps 4 and 6; SIP
+Tradeoffs, optional weight roles):
+  QK-norm: after the biases and before RoPE, q and k are RMS-normalised per
+    head with a head_dim weight shared by the heads ("head"), or over the whole
+    q / k row with a row-long weight ("row"), with the model's eps.
+  Sandwich norms: each block's output (attention after Wo, FFN after down /
+    the expert sum) is RMS-normalised with its post norm weight before it is
+    added to the residual.
+
 Optional int8 K/V cache (RML "The decoder", KV cache): every cached key and
 value row is stored as groups of G channels (G the largest power of two that
 divides head_dim, at most 32, so a group never spans two heads), each group as
@@ -115,6 +124,12 @@ class OracleConfig:
     rope_dim: int = 0
     # int8 K/V cache with per-group float32 scales (RML "The decoder", KV cache).
     kv_int8: bool = False
+    # QK-norm (RML One forward pass step 4): "" off, "head" per head (weights [hd]),
+    # "row" over the whole q / k row (weights [nq*hd] / [nkv*hd]).
+    qk_norm: str = ""
+    # Sandwich norms (RML One forward pass step 6): post-attention / post-FFN RMSNorm of
+    # each block's output before the residual add (weights post_attn_norm, post_ffn_norm).
+    sandwich_norms: bool = False
 
     @property
     def rotary_dim(self) -> int:
@@ -256,6 +271,17 @@ def kv_int8_roundtrip(row, head_dim: int) -> np.ndarray:
     g = kv_group_size(head_dim)
     codes, scales = quantize_int8_groups(a.reshape(-1), g)
     return dequantize_int8_groups(codes, scales, g).reshape(a.shape)
+
+
+def qk_normalise(vec, weight, heads: int, mode: str, eps: float) -> np.ndarray:
+    """QK-norm of q or k rows (last axis heads * hd): RMSNorm of each head with the
+    shared [hd] weight ("head"), or of the whole row with a row-long weight ("row")."""
+    v = np.asarray(vec, F64)
+    if mode == "head":
+        return rmsnorm(v.reshape(*v.shape[:-1], heads, v.shape[-1] // heads), weight, eps).reshape(v.shape)
+    if mode == "row":
+        return rmsnorm(v, weight, eps)
+    raise ValueError(f"unknown qk_norm mode {mode!r}")
 
 
 def kv_head_of(h: int, n_heads: int, n_kv_heads: int) -> int:
@@ -441,6 +467,9 @@ class Session:
             q = q + lw["bq"]
             k = k + lw["bk"]
             v = v + lw["bv"]
+        if c.qk_norm:
+            q = qk_normalise(q, lw["q_norm"], nq, c.qk_norm, c.rms_eps)
+            k = qk_normalise(k, lw["k_norm"], nkv, c.qk_norm, c.rms_eps)
         q = rope_rotate(q.reshape(nq, hd), pos, self.inv_freq, c.rope_half, c.rope_dim)
         k = rope_rotate(k.reshape(nkv, hd), pos, self.inv_freq, c.rope_half, c.rope_dim)
         if len(self.keys[l]) != pos:
@@ -453,7 +482,10 @@ class Session:
         lo = window_start(pos, c.sliding_window)
         o = attend_ref(q, np.stack(self.keys[l][lo:pos + 1]),
                        np.stack(self.values[l][lo:pos + 1]), nq, nkv)
-        return x + lw["wo"] @ o.reshape(-1)
+        out = lw["wo"] @ o.reshape(-1)
+        if c.sandwich_norms:
+            out = rmsnorm(out, lw["post_attn_norm"], c.rms_eps)
+        return x + out
 
     def _ffn_row(self, l: int, lw: dict, x: np.ndarray, pos: int) -> np.ndarray:
         c = self.cfg
@@ -467,6 +499,8 @@ class Session:
                 self.trace.expert_weights[(l, pos)] = wts
         else:
             out = swiglu(n, lw["w_gate"], lw["w_up"], lw["w_down"])
+        if c.sandwich_norms:
+            out = rmsnorm(out, lw["post_ffn_norm"], c.rms_eps)
         return x + out
 
     def _block_row(self, l: int, lw: dict, x: np.ndarray, pos: int) -> np.ndarray:
@@ -548,6 +582,9 @@ class Session:
                 Q = Q + lw["bq"]
                 K = K + lw["bk"]
                 V = V + lw["bv"]
+            if c.qk_norm:
+                Q = qk_normalise(Q, lw["q_norm"], nq, c.qk_norm, c.rms_eps)
+                K = qk_normalise(K, lw["k_norm"], nkv, c.qk_norm, c.rms_eps)
             Q = rot(Q.reshape(n, nq, hd))
             K = rot(K.reshape(n, nkv, hd))
             V = V.reshape(n, nkv, hd)
@@ -568,7 +605,8 @@ class Session:
                 S[mask] = -np.inf
                 E = np.exp(S - S.max(axis=1, keepdims=True))
                 O[:, h, :] = (E / E.sum(axis=1, keepdims=True)) @ Vall[:, g, :]
-            X = X + O.reshape(n, nq * hd) @ lw["wo"].T
+            A = O.reshape(n, nq * hd) @ lw["wo"].T
+            X = X + (rmsnorm(A, lw["post_attn_norm"], c.rms_eps) if c.sandwich_norms else A)
             N2 = rmsnorm(X, lw["ffn_norm"], c.rms_eps)
             if c.is_moe:
                 R = N2 @ lw["router"].T
@@ -586,7 +624,7 @@ class Session:
                 F = np.zeros((n, c.hidden), F64)
                 for s in range(c.n_experts_used):
                     F += np.array([routes[t][1][s] for t in range(n)])[:, None] * outs[:, s]
-                X = X + F
+                X = X + (rmsnorm(F, lw["post_ffn_norm"], c.rms_eps) if c.sandwich_norms else F)
                 if self.trace is not None:
                     for t in range(n):
                         p = int(pos[t])
@@ -594,7 +632,8 @@ class Session:
                         self.trace.expert_ids[(l, p)] = list(routes[t][0])
                         self.trace.expert_weights[(l, p)] = routes[t][1]
             else:
-                X = X + (silu(N2 @ lw["w_gate"].T) * (N2 @ lw["w_up"].T)) @ lw["w_down"].T
+                F = (silu(N2 @ lw["w_gate"].T) * (N2 @ lw["w_up"].T)) @ lw["w_down"].T
+                X = X + (rmsnorm(F, lw["post_ffn_norm"], c.rms_eps) if c.sandwich_norms else F)
             if self.trace is not None and self.trace_hidden:
                 for t in range(n):
                     self.trace.hidden[(l, int(pos[t]))] = X[t].copy()

@@ -32,6 +32,11 @@ def random_weights(cfg: OracleConfig, seed: int = 0, zero_layers: bool = False) 
                   wq=mat(qd, h), wk=mat(kd, h), wv=mat(kd, h), wo=mat(h, qd))
         if cfg.qkv_bias:
             lw.update(bq=mat(qd), bk=mat(kd), bv=mat(kd))
+        if cfg.qk_norm:
+            nq_w, nk_w = (cfg.head_dim, cfg.head_dim) if cfg.qk_norm == "head" else (qd, kd)
+            lw.update(q_norm=1 + rng.normal(0, 0.1, nq_w), k_norm=1 + rng.normal(0, 0.1, nk_w))
+        if cfg.sandwich_norms:
+            lw.update(post_attn_norm=1 + rng.normal(0, 0.1, h), post_ffn_norm=1 + rng.normal(0, 0.1, h))
         if cfg.n_experts:
             lw["router"] = mat(cfg.n_experts, h, s=0.5)
             experts.append([(mat(f, h), mat(f, h), mat(h, f)) for _ in range(cfg.n_experts)])
@@ -51,7 +56,8 @@ def torch_library_forward(cfg: OracleConfig, w: DictWeights, tokens) -> np.ndarr
     polar(1, pos * freq) (the complex form of the rotation).  Attention:
     F.scaled_dot_product_attention with an explicit boolean causal/window mask
     and enable_gqa (head h uses kv head h // group).  FFN: F.linear + F.silu.
-    MoE: torch.softmax, torch.topk, division by the selected sum.
+    MoE: torch.softmax, torch.topk, division by the selected sum.  QK-norm and
+    sandwich norms: F.rms_norm over each head / the row / the block output.
     """
     d = torch.float64
     T = lambda a: torch.as_tensor(np.asarray(a), dtype=d)
@@ -77,12 +83,21 @@ def torch_library_forward(cfg: OracleConfig, w: DictWeights, tokens) -> np.ndarr
         Q = F.linear(N, lw["wq"], lw.get("bq"))
         K = F.linear(N, lw["wk"], lw.get("bk"))
         V = F.linear(N, lw["wv"], lw.get("bv"))
+        if cfg.qk_norm == "head":
+            Q = F.rms_norm(Q.reshape(n, nq, hd), (hd,), weight=lw["q_norm"], eps=cfg.rms_eps).reshape(n, -1)
+            K = F.rms_norm(K.reshape(n, nkv, hd), (hd,), weight=lw["k_norm"], eps=cfg.rms_eps).reshape(n, -1)
+        elif cfg.qk_norm == "row":
+            Q = F.rms_norm(Q, (nq * hd,), weight=lw["q_norm"], eps=cfg.rms_eps)
+            K = F.rms_norm(K, (nkv * hd,), weight=lw["k_norm"], eps=cfg.rms_eps)
         Q, K = rope(Q, nq), rope(K, nkv)
         V = V.reshape(n, nkv, hd)
         O = F.scaled_dot_product_attention(Q.transpose(0, 1)[None], K.transpose(0, 1)[None],
                                            V.transpose(0, 1)[None], attn_mask=allowed,
                                            enable_gqa=True)
-        X = X + F.linear(O[0].transpose(0, 1).reshape(n, nq * hd), lw["wo"])
+        A = F.linear(O[0].transpose(0, 1).reshape(n, nq * hd), lw["wo"])
+        if cfg.sandwich_norms:
+            A = F.rms_norm(A, (h,), weight=lw["post_attn_norm"], eps=cfg.rms_eps)
+        X = X + A
         N2 = F.rms_norm(X, (h,), weight=lw["ffn_norm"], eps=cfg.rms_eps)
         if cfg.n_experts:
             probs = torch.softmax(F.linear(N2, lw["router"]), dim=-1)
@@ -93,8 +108,10 @@ def torch_library_forward(cfg: OracleConfig, w: DictWeights, tokens) -> np.ndarr
                 for s in range(cfg.n_experts_used):
                     wg, wu, wd = (T(a) for a in w.expert(l, int(top.indices[t, s])))
                     Fo[t] += wts[t, s] * F.linear(F.silu(F.linear(N2[t], wg)) * F.linear(N2[t], wu), wd)
-            X = X + Fo
         else:
-            X = X + F.linear(F.silu(F.linear(N2, lw["w_gate"])) * F.linear(N2, lw["w_up"]), lw["w_down"])
+            Fo = F.linear(F.silu(F.linear(N2, lw["w_gate"])) * F.linear(N2, lw["w_up"]), lw["w_down"])
+        if cfg.sandwich_norms:
+            Fo = F.rms_norm(Fo, (h,), weight=lw["post_ffn_norm"], eps=cfg.rms_eps)
+        X = X + Fo
     Nf = F.rms_norm(X, (h,), weight=T(w.out_norm()), eps=cfg.rms_eps)
     return F.linear(Nf, T(w.lm_head())).numpy()
