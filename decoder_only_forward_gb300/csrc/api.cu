@@ -94,6 +94,21 @@ __global__ void k_permute_qk_rows(const uint4* __restrict__ w, const float* __re
   if (b && bdst && threadIdx.x == 0) bdst[r] = b[src];
 }
 
+// dst[i] = src[i - d + src(d)], d = i % hd: a per-head vector (a QK-norm weight)
+// in the permuted dim order of the kHalf q/k rows.
+__global__ void k_permute_head_vector(const float* __restrict__ src, int n, int hd, int rd, float* __restrict__ dst) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int d = i % hd;
+  const int sd = d < rd ? ((d & 1) ? (d >> 1) + rd / 2 : (d >> 1)) : d;
+  dst[i] = src[i - d + sd];
+}
+
+void dec::launch_permute_head_vector(const dec_config& c, const float* src, int n, float* dst, cudaStream_t s) {
+  const int rd = c.rope_dim ? c.rope_dim : c.head_dim;
+  k_permute_head_vector<<<(n + 255) / 256, 256, 0, s>>>(src, n, c.head_dim, rd, dst);
+}
+
 void dec::launch_permute_qk_rows(const dec_config& c, const void* w, const float* b, void* wdst, float* bdst,
                                  cudaStream_t s) {
   const int qd = c.n_heads * c.head_dim, kd = c.n_kv_heads * c.head_dim;
@@ -127,6 +142,9 @@ static bool validate(const dec_config* c, std::string& why) {
   if (c->rope_dim < 0 || c->rope_dim > c->head_dim || c->rope_dim % 2 != 0)
     return bad("rope_dim must be even and in [0, head_dim] (0 = head_dim)");
   if (c->n_seqs < 0 || c->n_seqs > 65536) return bad("n_seqs must be in [0, 65536] (0 = 1)");
+  if (c->qk_norm < 0 || c->qk_norm > 2) return bad("qk_norm must be 0 (off), 1 (per head) or 2 (whole row)");
+  if (c->qk_norm && c->kv_dtype == DEC_BF16) return bad("qk_norm needs a DEC_F32 or DEC_I8 cache");
+  if (c->sandwich_norms != 0 && c->sandwich_norms != 1) return bad("sandwich_norms must be 0 or 1");
   if (c->rope_llama3 && !(c->rope_factor > 0.f && c->rope_low_freq_factor > 0.f &&
                           c->rope_high_freq_factor > c->rope_low_freq_factor && c->rope_orig_ctx > 0))
     return bad("llama3 RoPE scaling needs factor > 0, 0 < low < high, orig_ctx > 0");
@@ -229,6 +247,10 @@ WsPlan dec::plan_workspace(const dec_config& c) {
   p.kpart_bytes = c.weight_dtype == DEC_BF16 ? 8 * 128 * nmax * 4 : 0;
   if (p.kpart_bytes > ((size_t)128 << 20)) p.kpart_bytes = (size_t)128 << 20;
   p.kpart = take(p.kpart_bytes);
+  p.Z = take(c.sandwich_norms ? 4 * (size_t)T * c.hidden : 0);
+  // kHalf with QK-norm: the norm weights follow the permuted q/k dims.
+  const size_t qn = c.qk_norm == 2 ? (size_t)qd : (size_t)hd, kn = c.qk_norm == 2 ? (size_t)kd : (size_t)hd;
+  p.qk_perm = take(c.qk_norm && c.rope_half ? 4 * (size_t)c.n_layers * (qn + kn) : 0);
   // KV rings: [layer][K, V][seq][ring_rows][n_kv*hd], ring_rows = max_seq
   // rounded up to 64 rows so every ring starts 256-byte aligned.
   p.n_seqs = c.n_seqs > 0 ? c.n_seqs : 1;
@@ -279,6 +301,10 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
       return fail(nullptr, DEC_EINVAL, "layer %d: a required weight is NULL", l);
     if (cfg->qkv_bias && !L.bqkv) return fail(nullptr, DEC_EINVAL, "layer %d: qkv_bias set but bqkv is NULL", l);
     if (cfg->n_experts > 0 && !L.router) return fail(nullptr, DEC_EINVAL, "layer %d: MoE layer needs router", l);
+    if (cfg->qk_norm && (!L.q_norm || !L.k_norm))
+      return fail(nullptr, DEC_EINVAL, "layer %d: qk_norm set but q_norm / k_norm is NULL", l);
+    if (cfg->sandwich_norms && (!L.post_attn_norm || !L.post_ffn_norm))
+      return fail(nullptr, DEC_EINVAL, "layer %d: sandwich_norms set but a post norm is NULL", l);
     if (!aligned16(L.wqkv) || !aligned16(L.wo) || !aligned16(L.w_gateup) || !aligned16(L.w_down) ||
         (L.router && !aligned16(L.router)))
       return fail(nullptr, DEC_EINVAL, "layer %d: weight matrices must be 16-byte aligned", l);
@@ -356,6 +382,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
   S.b_part = (float*)(base + p.b_part);
   S.kpart = p.kpart_bytes ? (float*)(base + p.kpart) : nullptr;
   S.kpart_bytes = p.kpart_bytes;
+  S.Z = cfg->sandwich_norms ? (float*)(base + p.Z) : nullptr;
   h->layers.resize(cfg->n_layers);
   for (int l = 0; l < cfg->n_layers; ++l) {
     const dec_layer_weights& L = w->layers[l];
@@ -370,6 +397,10 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
     d.router = cfg->n_experts > 0 ? L.router : nullptr;
     d.kc = base + p.kv + (size_t)(2 * l) * p.kv_layer_bytes;
     d.vc = base + p.kv + (size_t)(2 * l + 1) * p.kv_layer_bytes;
+    d.q_norm = cfg->qk_norm ? (const float*)L.q_norm : nullptr;
+    d.k_norm = cfg->qk_norm ? (const float*)L.k_norm : nullptr;
+    d.post_attn_norm = cfg->sandwich_norms ? (const float*)L.post_attn_norm : nullptr;
+    d.post_ffn_norm = cfg->sandwich_norms ? (const float*)L.post_ffn_norm : nullptr;
   }
   if (cfg->rope_half) {
     // kHalf pairs (i, i + d/2) become adjacent pairs (2i, 2i+1) on q/k rows
@@ -384,6 +415,15 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
       launch_permute_qk_rows(*cfg, d.wqkv, d.bqkv, wdst, bdst, h->stream);
       d.wqkv = wdst;
       d.bqkv = bdst;
+      if (cfg->qk_norm) {
+        const size_t qn = cfg->qk_norm == 2 ? (size_t)cfg->n_heads * cfg->head_dim : (size_t)cfg->head_dim;
+        const size_t kn = cfg->qk_norm == 2 ? (size_t)cfg->n_kv_heads * cfg->head_dim : (size_t)cfg->head_dim;
+        float* qdst = (float*)(base + p.qk_perm) + (size_t)l * (qn + kn);
+        launch_permute_head_vector(*cfg, d.q_norm, (int)qn, qdst, h->stream);
+        launch_permute_head_vector(*cfg, d.k_norm, (int)kn, qdst + qn, h->stream);
+        d.q_norm = qdst;
+        d.k_norm = qdst + qn;
+      }
     }
   }
   m.layers = h->layers.data();
@@ -537,8 +577,8 @@ static dec_status run_rows(dec_handle* h, int32_t batch, const int32_t* seqs, co
 
 static dec_status run_decode_step(dec_handle* h, const int32_t* d_token, int32_t token, int32_t pos,
                                   float* logits, int32_t* d_argmax) {
-  if (h->m.cfg.kv_dtype == DEC_I8) {
-    // The int8 cache is written and read by the row kernels: one row, sequence 0.
+  if (decode_needs_rows(h->m.cfg)) {
+    // int8 caches, QK-norm and sandwich norms run on the row kernels: one row, sequence 0.
     const int32_t seq0 = 0;
     return run_rows(h, 1, &seq0, &pos, d_token, token, logits, d_argmax);
   }

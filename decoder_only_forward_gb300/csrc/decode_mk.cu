@@ -1853,7 +1853,7 @@ bool mk_prepare(Model& m, int num_sms) {
   m.mk_ok = false;
   m.mk_cluster = 0;
   (void)es;
-  if (c.kv_dtype == DEC_I8) return false;   // the int8 cache is served by the row kernels
+  if (decode_needs_rows(c)) return false;   // served by the row kernels
   // MoE down keeps one row sum per owned row (a CTA owns ceil(hidden / CTAs)
   // rows, in 16-row blocks on the tensor-core path); RoPE table of up to 64 pairs.
   auto rows_per_cta = [&](int nb) { return ((c.hidden + nb - 1) / nb + 15) / 16 * 16; };

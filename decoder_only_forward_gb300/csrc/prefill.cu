@@ -437,6 +437,98 @@ __global__ void k_moe_combine(const float* __restrict__ Y, const int32_t* __rest
 }
 
 // ---------------------------------------------------------------------------
+// QK-norm and sandwich norms (rml "The decoder", One forward pass steps 4, 6)
+
+// QK-norm then RoPE of one row's q (blockIdx.y = 0) or k (1): RMSNorm of each
+// head with the shared [hd] weight (mode 1) or of the whole row (mode 2), then
+// the adjacent-pair rotation of each head with the row's (cos, sin) table.  q
+// is read from q_src and written to q_dst (the same rows or another buffer);
+// k is rewritten in place at row k_rows[t] (or k_row0 + t) of k_base.
+__global__ void __launch_bounds__(128) k_qk_norm_rope(const float* q_src, float* q_dst, float* k_base,
+                                                      const int32_t* __restrict__ k_rows, int k_row0, int nq,
+                                                      int nkv, int hd, int mode, const float* __restrict__ q_w,
+                                                      const float* __restrict__ k_w, float eps,
+                                                      const float2* __restrict__ rope) {
+  __shared__ float red[5];
+  const int t = blockIdx.x, is_k = blockIdx.y;
+  const int heads = is_k ? nkv : nq, len = heads * hd;
+  const float* src = is_k ? k_base + (size_t)(k_rows ? k_rows[t] : k_row0 + t) * len : q_src + (size_t)t * len;
+  float* dst = is_k ? const_cast<float*>(src) : q_dst + (size_t)t * len;
+  const float* w = is_k ? k_w : q_w;
+  const float2* cs = rope + (size_t)t * (hd / 2);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float inv_row = 0.f;
+  if (mode == 2) {
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < len; i += blockDim.x) ss = fmaf(src[i], src[i], ss);
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) red[4] = red[0] + red[1] + red[2] + red[3];
+    __syncthreads();
+    inv_row = 1.0f / sqrtf(red[4] / (float)len + eps);
+  }
+  // A warp per head: lane i takes pairs i, i + 32, ...
+  for (int h = warp; h < heads; h += blockDim.x / 32) {
+    const float* x = src + (size_t)h * hd;
+    float inv = inv_row;
+    if (mode == 1) {
+      float ss = 0.f;
+      for (int d = lane; d < hd; d += 32) ss = fmaf(x[d], x[d], ss);
+      inv = 1.0f / sqrtf(warp_sum(ss) / (float)hd + eps);
+    }
+    const float* wh = mode == 1 ? w : w + (size_t)h * hd;
+    float2 out[2];
+    int np = 0;
+    for (int i = lane; i < hd / 2; i += 32) {
+      const float a = x[2 * i] * inv * wh[2 * i], b = x[2 * i + 1] * inv * wh[2 * i + 1];
+      const float2 c = cs[i];
+      out[np++] = make_float2(a * c.x - b * c.y, a * c.y + b * c.x);
+    }
+    __syncwarp();   // every lane has read the head before any writes it back
+    np = 0;
+    for (int i = lane; i < hd / 2; i += 32) {
+      dst[(size_t)h * hd + 2 * i] = out[np].x;
+      dst[(size_t)h * hd + 2 * i + 1] = out[np].y;
+      ++np;
+    }
+  }
+}
+
+// f32 rows -> bf16 (hi, lo) planes (lo plane at plane_stride elements).
+__global__ void k_rows_to_planes(const float* __restrict__ src, size_t n, __nv_bfloat16* __restrict__ hi,
+                                 size_t plane_stride) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const float v = src[i];
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    hi[i] = h;
+    hi[plane_stride + i] = __float2bfloat16_rn(v - __bfloat162float(h));
+  }
+}
+
+// X[t] += Z[t] / sqrt(mean(Z[t]^2) + eps) * w, one CTA per row.
+__global__ void __launch_bounds__(256) k_rmsnorm_add_rows(float* __restrict__ X, const float* __restrict__ Z,
+                                                          const float* __restrict__ w, float eps, int h) {
+  __shared__ float red[33];
+  const int t = blockIdx.x;
+  const float* z = Z + (size_t)t * h;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < h; i += blockDim.x) ss = fmaf(z[i], z[i], ss);
+  ss = warp_sum(ss);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  if (warp == 0) {
+    float v = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.f;
+    v = warp_sum(v);
+    if (lane == 0) red[32] = v;
+  }
+  __syncthreads();
+  const float inv = 1.0f / sqrtf(red[32] / (float)h + eps);
+  for (int i = threadIdx.x; i < h; i += blockDim.x) X[(size_t)t * h + i] += z[i] * inv * w[i];
+}
+
+// ---------------------------------------------------------------------------
 // Driver
 
 // An activation row buffer: f32 rows (f32 weights) or bf16 hi/lo planes of
@@ -535,10 +627,15 @@ static cudaError_t ffn_rows(const Model& m, cudaStream_t s, const LayerPtrs& L, 
     e1.act_lo = act.out().lo;
     chk(gemm<TW>(m, s, a_h, (const TW*)L.w_gateup, n, 2 * f, h, e1, 1, n));
     GemmEpi e2{};
-    e2.mode = EPI_RESID;
+    // Sandwich norms: the block output goes to Z and is normalised into x.
+    e2.mode = c.sandwich_norms ? EPI_STORE : EPI_RESID;
     e2.n_out = h;
-    e2.out_f32 = S.X;
+    e2.out_f32 = c.sandwich_norms ? S.Z : S.X;
     chk(gemm<TW>(m, s, act, (const TW*)L.w_down, n, h, f, e2, 1, n));
+    if (c.sandwich_norms) {
+      k_rmsnorm_add_rows<<<n, 256, 0, s>>>(S.X, S.Z, L.post_ffn_norm, c.rms_eps, h);
+      count_launch(m);
+    }
     return err;
   }
   const int k = c.n_experts_used, E = c.n_experts, entries = n * k;
@@ -579,9 +676,54 @@ static cudaError_t ffn_rows(const Model& m, cudaStream_t s, const LayerPtrs& L, 
   e2.out_f32 = S.Y;
   e2.group_offset = S.pf_offset;
   chk(gemm<TW>(m, s, act_sort, (const TW*)L.w_down, entries, h, f, e2, E, n));
-  k_moe_combine<<<n, 256, 0, s>>>(S.Y, S.pf_inv, S.pf_wts, k, h, S.X);
-  count_launch(m);
+  if (c.sandwich_norms) {
+    cudaMemsetAsync(S.Z, 0, sizeof(float) * (size_t)n * h, s);
+    k_moe_combine<<<n, 256, 0, s>>>(S.Y, S.pf_inv, S.pf_wts, k, h, S.Z);
+    k_rmsnorm_add_rows<<<n, 256, 0, s>>>(S.X, S.Z, L.post_ffn_norm, c.rms_eps, h);
+    count_launch(m, 2);
+  } else {
+    k_moe_combine<<<n, 256, 0, s>>>(S.Y, S.pf_inv, S.pf_wts, k, h, S.X);
+    count_launch(m);
+  }
   return err;
+}
+
+// Attention output projection over n rows: x += Wo.o, or with sandwich norms
+// x += rmsnorm(Wo.o) * w_post.
+template <typename TW>
+static cudaError_t oproj_rows(const Model& m, cudaStream_t s, const LayerPtrs& L, int n, const Act& a_q) {
+  const dec_config& c = m.cfg;
+  const Scratch& S = m.s;
+  const int h = c.hidden, qd = c.n_heads * c.head_dim;
+  GemmEpi e{};
+  e.mode = c.sandwich_norms ? EPI_STORE : EPI_RESID;
+  e.n_out = h;
+  e.out_f32 = c.sandwich_norms ? S.Z : S.X;
+  const cudaError_t err = gemm<TW>(m, s, a_q, (const TW*)L.wo, n, h, qd, e, 1, n);
+  if (c.sandwich_norms) {
+    k_rmsnorm_add_rows<<<n, 256, 0, s>>>(S.X, S.Z, L.post_attn_norm, c.rms_eps, h);
+    count_launch(m);
+  }
+  return err;
+}
+
+// QK-norm + RoPE after a QKV GEMM that wrote unrotated q (f32 rows in S.Q) and
+// k (f32 rows at k_base).  planes: the rotated q goes to the bf16 (hi, lo)
+// planes of the tensor-core attention (through S.A, free between the GEMM and
+// the attention), else back into S.Q.
+static void qk_norm_rows(const Model& m, cudaStream_t s, const LayerPtrs& L, int n, float* k_base,
+                         const int32_t* k_rows, int k_row0, bool planes) {
+  const dec_config& c = m.cfg;
+  const Scratch& S = m.s;
+  const int qd = c.n_heads * c.head_dim;
+  float* q_dst = planes ? (float*)S.A : S.Q;
+  k_qk_norm_rope<<<dim3(n, 2), 128, 0, s>>>(S.Q, q_dst, k_base, k_rows, k_row0, c.n_heads, c.n_kv_heads,
+                                            c.head_dim, c.qk_norm, L.q_norm, L.k_norm, c.rms_eps, S.rope_tab);
+  count_launch(m);
+  if (planes) {
+    k_rows_to_planes<<<152, 256, 0, s>>>((const float*)S.A, (size_t)n * qd, S.at.Qb, (size_t)S.at.qcap * qd);
+    count_launch(m);
+  }
 }
 
 // Sequence seq's ring of one layer (ring sets hold n_seqs rings back to back).
@@ -619,6 +761,7 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n,
 
   const Act a_h{S.A, split, n, h};      // normalised rows
   const Act a_q{S.A, split, n, qd};     // attention output rows
+  const bool qkn = c.qk_norm != 0;
 
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerPtrs& L = m.layers[l];
@@ -643,16 +786,19 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n,
       e.kd = kd;
       e.hd = hd;
       // Rotated queries: bf16 (hi, lo) planes for the tensor-core attention,
-      // else f32 rows.
+      // else f32 rows.  With QK-norm the epilogue leaves q and k unrotated
+      // (f32) and qk_norm_rows normalises and rotates them.
       const bool q_planes = std::is_same<KV, float>::value && S.at.Kb;
-      e.q_out = q_planes ? (void*)S.at.Qb : (void*)S.Q;
-      e.q_bf16 = q_planes;
-      e.q_lo = q_planes ? S.at.Qb + (size_t)S.at.qcap * qd : nullptr;
+      e.q_out = q_planes && !qkn ? (void*)S.at.Qb : (void*)S.Q;
+      e.q_bf16 = q_planes && !qkn;
+      e.q_lo = q_planes && !qkn ? S.at.Qb + (size_t)S.at.qcap * qd : nullptr;
+      if (qkn) e.rope = nullptr;
       e.k_dst = kdst;
       e.v_dst = vdst;
       e.kv_bf16 = std::is_same<KV, __nv_bfloat16>::value;
       e.kv_row0 = direct ? start : hist;
       chk(gemm<TW>(m, s, a_h, (const TW*)L.wqkv, n, qd + 2 * kd, h, e, 1, n));
+      if (qkn) qk_norm_rows(m, s, L, n, (float*)kdst, nullptr, e.kv_row0, q_planes);
     }
     const int t_first = n > c.max_seq ? n - c.max_seq : 0;
     if (i8) {
@@ -669,13 +815,7 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n,
       k_kv_commit<KV><<<152, 256, 0, s>>>(kdst, vdst, hist, start, t_first, n, c.max_seq, kd, kc, vc);
       count_launch(m);
     }
-    {
-      GemmEpi e{};
-      e.mode = EPI_RESID;
-      e.n_out = h;
-      e.out_f32 = S.X;
-      chk(gemm<TW>(m, s, a_q, (const TW*)L.wo, n, h, qd, e, 1, n));
-    }
+    chk(oproj_rows<TW>(m, s, L, n, a_q));
     chk(ffn_rows<TW>(m, s, L, l, n, start, seq == 0));
   }
   if (logits || d_argmax) launch_lmhead(m, s, S.X + (size_t)(n - 1) * h, logits, d_argmax);
@@ -739,7 +879,9 @@ static cudaError_t decode_rows(const Model& m, cudaStream_t s, int B, float* log
       e.v_dst = i8 ? S.KVlin_v : L.vc;
       e.kv_bf16 = std::is_same<KV, __nv_bfloat16>::value;
       e.kv_rows = i8 ? nullptr : S.b_rows;
+      if (c.qk_norm) e.rope = nullptr;
       chk(gemm<TW>(m, s, a_h, (const TW*)L.wqkv, B, qd + 2 * kd, h, e, 1, B));
+      if (c.qk_norm) qk_norm_rows(m, s, L, B, (float*)e.k_dst, e.kv_rows, 0, false);
     }
     if (i8) {
       launch_kv_quant(c, (const float*)S.KVlin_k, (const float*)S.KVlin_v, B, S.b_rows, 0, 0, L.kc, L.vc, nullptr,
@@ -750,13 +892,7 @@ static cudaError_t decode_rows(const Model& m, cudaStream_t s, int B, float* log
     launch_attn_rows(c, S.Q, L.kc, L.vc, m.ring_bytes, S.b_seq, S.b_pos, B, nsplit, S.b_part, a_q.out(), s);
     timer_end(m, DEC_K_ATTN, s);
     count_launch(m, 2);
-    {
-      GemmEpi e{};
-      e.mode = EPI_RESID;
-      e.n_out = h;
-      e.out_f32 = S.X;
-      chk(gemm<TW>(m, s, a_q, (const TW*)L.wo, B, h, qd, e, 1, B));
-    }
+    chk(oproj_rows<TW>(m, s, L, B, a_q));
     chk(ffn_rows<TW>(m, s, L, l, B, 0, false));
   }
   // Final RMSNorm and the LM head over every row.

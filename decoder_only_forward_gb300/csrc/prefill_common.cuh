@@ -132,7 +132,7 @@ __device__ __forceinline__ void epi_pair(const GemmEpi& e, int row, int col, flo
         v0 += e.bias[col];
         v1 += e.bias[col + 1];
       }
-      if (col < e.qd + e.kd) {
+      if (e.rope && col < e.qd + e.kd) {   // no table: q and k left unrotated (QK-norm comes first)
         const int d = (col < e.qd ? col : col - e.qd) % e.hd;
         const float2 cs = e.rope[(size_t)row * (e.hd / 2) + (d >> 1)];
         const float a = v0 * cs.x - v1 * cs.y;

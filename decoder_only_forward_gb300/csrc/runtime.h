@@ -37,6 +37,10 @@ struct LayerPtrs {
   const void* router;  // nullable (dense)
   void* kc;            // this layer's K ring [max_seq][n_kv*hd]
   void* vc;            // this layer's V ring
+  const float* q_norm;  // QK-norm weights (nullable)
+  const float* k_norm;
+  const float* post_attn_norm;  // sandwich norms (nullable)
+  const float* post_ffn_norm;
 };
 
 // bf16 (hi, lo) operand planes of the tensor-core prefill attention; plane
@@ -89,6 +93,7 @@ struct Scratch {
   float* b_part;        // [MAX_BATCH][nq][AR_MAX_SPLIT][hd+2] attention split partials
   float* kpart;         // split-K partial sums of the tensor-core GEMMs
   size_t kpart_bytes;
+  float* Z;             // [T][h] block output before its post norm (sandwich norms)
 };
 
 constexpr int LM_GRID_MAX = 1024;
@@ -151,6 +156,8 @@ struct WsPlan {
   size_t mk_maps;       // its weight tensor maps
   size_t b_seq, b_pos, b_rows, b_part;  // batched decode
   size_t kpart, kpart_bytes;            // split-K partials
+  size_t Z;                             // sandwich block outputs
+  size_t qk_perm;                       // kHalf + QK-norm: permuted norm weights
   size_t kv;            // start of the KV rings: [layer][K, V][seq][ring_rows][n_kv*hd]
   size_t kv_layer_bytes; // one layer's K (or V) rings of every sequence
   size_t ring_bytes;    // one sequence's ring
@@ -199,6 +206,11 @@ struct KvRowLayout {
   int code_off;   // bytes before the codes (the scales' area)
   int group;      // channels per scale
 };
+// Models whose decode runs the row kernels (one row per step): the persistent
+// step and the per-layer decode kernels implement none of these.
+inline bool decode_needs_rows(const dec_config& c) {
+  return c.kv_dtype == DEC_I8 || c.qk_norm != 0 || c.sandwich_norms != 0;
+}
 inline int kv_group_size(int hd) {
   int g = 1;
   while (g < 32 && hd % (2 * g) == 0) g *= 2;
@@ -307,6 +319,8 @@ inline bool attn_tc_supported(const dec_config& c) {
 // so that kHalf RoPE pairs (i, i + rope_dim/2) become adjacent (api.cu).
 void launch_permute_qk_rows(const dec_config& c, const void* w, const float* b, void* wdst, float* bdst,
                             cudaStream_t s);
+// A per-head vector (n = heads * hd) in the same permuted dim order.
+void launch_permute_head_vector(const dec_config& c, const float* src, int n, float* dst, cudaStream_t s);
 
 // Message returned by dec_last_error(NULL) (api.cu).
 void set_global_error(const char* msg);

@@ -45,12 +45,14 @@ class Config(ctypes.Structure):
         ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("rope_llama3", ctypes.c_int32),
         ("rope_factor", ctypes.c_float), ("rope_low_freq_factor", ctypes.c_float),
         ("rope_high_freq_factor", ctypes.c_float), ("rope_orig_ctx", ctypes.c_int32),
-        ("rope_half", ctypes.c_int32), ("rope_dim", ctypes.c_int32), ("n_seqs", ctypes.c_int32)]
+        ("rope_half", ctypes.c_int32), ("rope_dim", ctypes.c_int32), ("n_seqs", ctypes.c_int32),
+        ("qk_norm", ctypes.c_int32), ("sandwich_norms", ctypes.c_int32)]
 
 
 class LayerWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("attn_norm", "wqkv", "bqkv", "wo", "ffn_norm", "w_gateup", "w_down", "router")]
+                ("attn_norm", "wqkv", "bqkv", "wo", "ffn_norm", "w_gateup", "w_down", "router",
+                 "q_norm", "k_norm", "post_attn_norm", "post_ffn_norm")]
 
 
 class Weights(ctypes.Structure):
@@ -134,6 +136,8 @@ def make_config(w: dict, kv_dtype: str = "f32", max_tokens: int = 0, n_seqs: int
     c.rope_half = int(bool(w.get("rope_half", False)))
     c.rope_dim = int(w.get("rope_dim", 0))
     c.n_seqs = int(n_seqs)
+    c.qk_norm = {None: 0, "": 0, "head": 1, "row": 2}[w.get("qk_norm")]
+    c.sandwich_norms = int(bool(w.get("sandwich_norms", False)))
     return c
 
 
@@ -240,6 +244,11 @@ class DeviceWeights:
         self.layers = []
         for l in range(w["n_layers"]):
             L = {"attn_norm": d("attn_norm", l), "ffn_norm": d("ffn_norm", l), "wo": d("wo", l)}
+            qkn, sw = w.get("qk_norm"), w.get("sandwich_norms")
+            L["q_norm"] = d("q_norm", l) if qkn else None
+            L["k_norm"] = d("k_norm", l) if qkn else None
+            L["post_attn_norm"] = d("post_attn_norm", l) if sw else None
+            L["post_ffn_norm"] = d("post_ffn_norm", l) if sw else None
             wqkv = torch.empty((qd + 2 * kd, h), dtype=dt, device=device)
             d("wq", l, out=wqkv[:qd])
             d("wk", l, out=wqkv[qd:qd + kd])
@@ -266,7 +275,8 @@ class DeviceWeights:
             self.layers.append(L)
         self._c_layers = (LayerWeights * w["n_layers"])()
         for i, L in enumerate(self.layers):
-            for k in ("attn_norm", "wqkv", "bqkv", "wo", "ffn_norm", "w_gateup", "w_down", "router"):
+            for k in ("attn_norm", "wqkv", "bqkv", "wo", "ffn_norm", "w_gateup", "w_down", "router",
+                      "q_norm", "k_norm", "post_attn_norm", "post_ffn_norm"):
                 setattr(self._c_layers[i], k, _ptr(L[k]))
         self.c = Weights(self.tok_embd.data_ptr(), self.out_norm.data_ptr(), _ptr(self.lm_head),
                          ctypes.cast(self._c_layers, ctypes.POINTER(LayerWeights)))

@@ -72,10 +72,14 @@ def role_shape(cfg: dict, role: str) -> tuple:
         "wq": (qd, h), "wk": (kd, h), "wv": (kd, h), "bq": (qd,), "bk": (kd,), "bv": (kd,),
         "wo": (h, qd), "w_gate": (f, h), "w_up": (f, h), "w_down": (h, f),
         "router": (cfg["n_experts"], h),
+        # QK-norm weights: one head_dim vector shared by the heads, or row-long ("row")
+        "q_norm": (qd if cfg.get("qk_norm") == "row" else cfg["head_dim"],),
+        "k_norm": (kd if cfg.get("qk_norm") == "row" else cfg["head_dim"],),
+        "post_attn_norm": (h,), "post_ffn_norm": (h,),
     }[role]
 
 
-_NORMS = {"out_norm", "attn_norm", "ffn_norm"}
+_NORMS = {"out_norm", "attn_norm", "ffn_norm", "q_norm", "k_norm", "post_attn_norm", "post_ffn_norm"}
 _BIASES = {"bq", "bk", "bv"}
 
 
@@ -106,6 +110,10 @@ def layer_roles(cfg: dict) -> list:
     roles = ["attn_norm", "wq", "wk", "wv", "wo", "ffn_norm"]
     if cfg["qkv_bias"]:
         roles += ["bq", "bk", "bv"]
+    if cfg.get("qk_norm"):
+        roles += ["q_norm", "k_norm"]
+    if cfg.get("sandwich_norms"):
+        roles += ["post_attn_norm", "post_ffn_norm"]
     roles += ["router"] if cfg["n_experts"] > 0 else ["w_gate", "w_up", "w_down"]
     return roles
 

@@ -76,9 +76,10 @@ typedef struct dec_config {
   int32_t tied_embedding; /* 1: LM head = token embedding matrix */
   int32_t qkv_bias;       /* 1: bqkv present */
   int32_t weight_dtype;   /* DEC_F32 or DEC_BF16: projection, embedding, router, head matrices */
-  int32_t kv_dtype;       /* DEC_F32, DEC_BF16 or DEC_I8: KV cache storage.  With DEC_I8 every decode
-                             step (dec_decode, dec_decode_dev) runs the batched row kernels with one
-                             row; the fused schedules are not available */
+  int32_t kv_dtype;       /* DEC_F32, DEC_BF16 or DEC_I8: KV cache storage.  With DEC_I8 (and with
+                             qk_norm or sandwich_norms) every decode step (dec_decode, dec_decode_dev)
+                             runs the batched row kernels with one row; the fused schedules are not
+                             available */
   float rms_eps;
   float rope_theta;
   int32_t rope_llama3;    /* 1: llama3 frequency scaling with the four fields below */
@@ -100,6 +101,14 @@ typedef struct dec_config {
                              dec_kv_reset act on sequence 0; dec_prefill_seq, dec_kv_reset_seq and
                              dec_decode_batch on any (Pantheon "Llama Forward Pass", Batched
                              Multi-Sequence Decode: a KV cache and position per sequence) */
+  int32_t qk_norm;        /* QK-norm (rml "The decoder", One forward pass step 4): after the biases and
+                             before RoPE, q and k are RMS-normalised with eps = rms_eps.  0 off; 1 per head
+                             with one [head_dim] weight shared by the heads (q_norm, k_norm); 2 over the whole
+                             q / k row with [n_heads*head_dim] / [n_kv_heads*head_dim] weights.  Not with a
+                             DEC_BF16 cache (DEC_EINVAL) */
+  int32_t sandwich_norms; /* 1: each block's output (attention after wo, FFN after the down projection or
+                             the expert sum) is RMS-normalised with post_attn_norm / post_ffn_norm before
+                             the residual add (rml "The decoder", One forward pass step 6) */
 } dec_config;
 
 /*
@@ -116,6 +125,8 @@ typedef struct dec_config {
  */
 typedef struct dec_layer_weights {
   const void *attn_norm, *wqkv, *bqkv, *wo, *ffn_norm, *w_gateup, *w_down, *router;
+  const void *q_norm, *k_norm;                /* f32, with qk_norm (see dec_config); else NULL */
+  const void *post_attn_norm, *post_ffn_norm; /* f32 [hidden], with sandwich_norms; else NULL */
 } dec_layer_weights;
 
 typedef struct dec_weights {

@@ -130,3 +130,16 @@ def test_n_seqs_checked(dec):
     assert st == dec.DEC_EINVAL and "n_seqs" in msg
     c.n_seqs = 8
     assert dec.validate(c)[0] == dec.DEC_OK
+
+
+def test_norm_variant_fields_checked(dec):
+    c = dec.make_config(synthetic.workload("toy", qk_norm="head", sandwich_norms=True))
+    assert (c.qk_norm, c.sandwich_norms) == (1, 1)
+    assert dec.validate(c)[0] == dec.DEC_OK
+    c.kv_dtype = dec.DEC_BF16
+    st, msg = dec.validate(c)
+    assert st == dec.DEC_EINVAL and "qk_norm" in msg
+    c.kv_dtype, c.qk_norm = dec.DEC_F32, 3
+    assert dec.validate(c)[0] == dec.DEC_EINVAL
+    c.qk_norm, c.sandwich_norms = 2, 2
+    assert dec.validate(c)[0] == dec.DEC_EINVAL
