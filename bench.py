@@ -35,6 +35,16 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
+def workload_of(args) -> dict:
+    """The named workload, with the architecture variant flags applied."""
+    kw = {}
+    if getattr(args, "qk_norm", ""):
+        kw["qk_norm"] = args.qk_norm
+    if getattr(args, "sandwich", False):
+        kw["sandwich_norms"] = True
+    return synthetic.workload(args.workload, **kw)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -226,7 +236,7 @@ def run_ours(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = synthetic.workload(args.workload)
+    w = workload_of(args)
     P, D = w["prompt"], w["decode"]
     kv_es = kv_bytes_per_element(w, args.kv)
     d = dec.Decoder(w, device=dev, kv_dtype=args.kv)
@@ -368,7 +378,8 @@ def run_ours(args, rank, world, local_rank):
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"] if w["dtype"] != "f32" else "f32",
             "data": "synthetic (random-init weights N(0,0.02), norms 1+N(0,0.1), uniform random prompt)",
-            "config": {"workload": args.workload, "prompt_tokens": P, "decode_tokens": D, "batch": 1,
+            "config": {"workload": args.workload + (f"+qk_norm_{args.qk_norm}" if args.qk_norm else "")
+                       + ("+sandwich" if args.sandwich else ""), "prompt_tokens": P, "decode_tokens": D, "batch": 1,
                        "decode_schedule": d.fused_mode(),
                        "kv_dtype": args.kv, "weights_gb": round(d.weights.nbytes() / 1e9, 3),
                        "l2": "flushed before each step (write of a 258 MB buffer); weights also exceed L2",
@@ -450,7 +461,7 @@ def run_profile(args):
     from decoder_only_forward_gb300 import build as dec_build
     dec_build.build()
     from decoder_only_forward_gb300 import dec
-    w = synthetic.workload(args.workload)
+    w = workload_of(args)
     if args.prompt:
         w["prompt"] = args.prompt
     if args.layers:
@@ -473,7 +484,7 @@ def run_profile(args):
 
 # ---------------------------------------------------------------- reference arm (oracle)
 def run_reference(args):
-    w = synthetic.workload(args.workload)
+    w = workload_of(args)
     npf, ndc = oracle_sample_size(w)
     dev = "cpu"
     rates, secs = [], []
@@ -515,6 +526,9 @@ def main():
     ap.add_argument("--batch", type=int, default=16,
                     help="also time batched multi-sequence decode at this batch (0: skip)")
     ap.add_argument("--batch-steps", type=int, default=32)
+    ap.add_argument("--qk-norm", default="", choices=["", "head", "row"],
+                    help="architecture variant: QK-norm (adds q_norm/k_norm weights)")
+    ap.add_argument("--sandwich", action="store_true", help="architecture variant: sandwich norms")
     ap.add_argument("--profile", type=int, default=0, metavar="D",
                     help="profiling driver: one prefill + D decode steps, kernels launched one by one "
                          "(no graph, no timing passes, no JSON); for per-kernel profilers")
