@@ -32,6 +32,12 @@ Per position p (absolute), per layer, pre-norm:
                                                               [PAN Mixture of Experts; RML Mixture of experts]
   logits = W_out rmsnorm(x, w_out)                             [PAN Forward Pass Flow]
 
+Per-layer RoPE base (SIP RoPE, "per-layer base (Gemma 3)"; RML One forward pass
+step 3 computes a global and a local table): with rope_theta_local set, layer l
+rotates with rope_theta when it is one of every rope_global_every layers
+((l + 1) % rope_global_every == 0) and with rope_theta_local otherwise; llama3
+scaling, when on, applies to the global base only.
+
 Optional norms (RML "The decoder", One forward pass, steps 4 and 6; SIP
 Tradeoffs, optional weight roles):
   QK-norm: after the biases and before RoPE, q and k are RMS-normalised per
@@ -130,6 +136,16 @@ class OracleConfig:
     # Sandwich norms (RML One forward pass step 6): post-attention / post-FFN RMSNorm of
     # each block's output before the residual add (weights post_attn_norm, post_ffn_norm).
     sandwich_norms: bool = False
+    # Per-layer RoPE base (SIP RoPE, Gemma 3): 0 = one base for every layer; else local
+    # layers use rope_theta_local and every rope_global_every-th layer the global base.
+    rope_theta_local: float = 0.0
+    rope_global_every: int = 0
+
+    def layer_is_global(self, l: int) -> bool:
+        """Whether layer l rotates with the global base (always, without a local base)."""
+        if not self.rope_theta_local:
+            return True
+        return self.rope_global_every > 0 and (l + 1) % self.rope_global_every == 0
 
     @property
     def rotary_dim(self) -> int:
@@ -432,6 +448,8 @@ class Session:
         self.cfg = cfg
         self.w = weights
         self.inv_freq = rope_inv_freq(cfg.head_dim, cfg.rope_theta, cfg.rope_llama3, cfg.rope_dim)
+        self.inv_freq_local = (rope_inv_freq(cfg.head_dim, cfg.rope_theta_local, None, cfg.rope_dim)
+                               if cfg.rope_theta_local else self.inv_freq)
         self.keys = [[] for _ in range(cfg.n_layers)]
         self.values = [[] for _ in range(cfg.n_layers)]
         self.trace = Trace() if trace else None
@@ -470,8 +488,9 @@ class Session:
         if c.qk_norm:
             q = qk_normalise(q, lw["q_norm"], nq, c.qk_norm, c.rms_eps)
             k = qk_normalise(k, lw["k_norm"], nkv, c.qk_norm, c.rms_eps)
-        q = rope_rotate(q.reshape(nq, hd), pos, self.inv_freq, c.rope_half, c.rope_dim)
-        k = rope_rotate(k.reshape(nkv, hd), pos, self.inv_freq, c.rope_half, c.rope_dim)
+        inv = self.inv_freq if c.layer_is_global(l) else self.inv_freq_local
+        q = rope_rotate(q.reshape(nq, hd), pos, inv, c.rope_half, c.rope_dim)
+        k = rope_rotate(k.reshape(nkv, hd), pos, inv, c.rope_half, c.rope_dim)
         if len(self.keys[l]) != pos:
             raise AssertionError("positions must be appended in ascending order")
         v = v.reshape(nkv, hd)
@@ -558,12 +577,15 @@ class Session:
         nq, nkv, hd = c.n_heads, c.n_kv_heads, c.head_dim
         pos = start_pos + np.arange(n)
         X = self.w.embed_rows(tokens)
-        ang = pos[:, None].astype(F64) * self.inv_freq[None, :]
-        cos, sin = np.cos(ang), np.sin(ang)
+        tables = {}
+        for name, inv in (("global", self.inv_freq), ("local", self.inv_freq_local)):
+            ang = pos[:, None].astype(F64) * inv[None, :]
+            tables[name] = (np.cos(ang), np.sin(ang))
 
         ia, ib = rope_pairs(hd, c.rope_half, c.rope_dim)
 
-        def rot(T):  # T [n, heads, hd]; row t at position pos[t]
+        def rot(T, l):  # T [n, heads, hd]; row t at position pos[t]; layer l's base
+            cos, sin = tables["global" if c.layer_is_global(l) else "local"]
             a = T[..., ia].copy()
             b = T[..., ib].copy()
             out = T.copy()
@@ -585,8 +607,8 @@ class Session:
             if c.qk_norm:
                 Q = qk_normalise(Q, lw["q_norm"], nq, c.qk_norm, c.rms_eps)
                 K = qk_normalise(K, lw["k_norm"], nkv, c.qk_norm, c.rms_eps)
-            Q = rot(Q.reshape(n, nq, hd))
-            K = rot(K.reshape(n, nkv, hd))
+            Q = rot(Q.reshape(n, nq, hd), l)
+            K = rot(K.reshape(n, nkv, hd), l)
             V = V.reshape(n, nkv, hd)
             for t in range(n):
                 if c.kv_int8:

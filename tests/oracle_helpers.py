@@ -65,15 +65,19 @@ def torch_library_forward(cfg: OracleConfig, w: DictWeights, tokens) -> np.ndarr
     h, nq, nkv, hd = cfg.hidden, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
     X = T(w.embed_rows(tokens))
     pos = torch.arange(n, dtype=d)
-    freq = cfg.rope_theta ** (-torch.arange(0, hd, 2, dtype=d) / hd)
-    cis = torch.polar(torch.ones(n, hd // 2, dtype=d), pos[:, None] * freq[None, :])
+    def cis_of(theta):
+        freq = theta ** (-torch.arange(0, hd, 2, dtype=d) / hd)
+        return torch.polar(torch.ones(n, hd // 2, dtype=d), pos[:, None] * freq[None, :])
+
+    cis_global = cis_of(cfg.rope_theta)
+    cis_local = cis_of(cfg.rope_theta_local) if cfg.rope_theta_local else cis_global
     i = torch.arange(n)[:, None]
     j = torch.arange(n)[None, :]
     allowed = j <= i
     if cfg.sliding_window > 0:
         allowed &= j >= i - cfg.sliding_window + 1
 
-    def rope(Y, heads):
+    def rope(Y, heads, cis):
         c = torch.view_as_complex(Y.reshape(n, heads, hd // 2, 2).contiguous())
         return torch.view_as_real(c * cis[:, None, :]).reshape(n, heads, hd)
 
@@ -89,7 +93,10 @@ def torch_library_forward(cfg: OracleConfig, w: DictWeights, tokens) -> np.ndarr
         elif cfg.qk_norm == "row":
             Q = F.rms_norm(Q, (nq * hd,), weight=lw["q_norm"], eps=cfg.rms_eps)
             K = F.rms_norm(K, (nkv * hd,), weight=lw["k_norm"], eps=cfg.rms_eps)
-        Q, K = rope(Q, nq), rope(K, nkv)
+        # Gemma-style base per layer: every rope_global_every-th layer (1-based) is global.
+        is_global = not cfg.rope_theta_local or (cfg.rope_global_every and (l + 1) % cfg.rope_global_every == 0)
+        cis = cis_global if is_global else cis_local
+        Q, K = rope(Q, nq, cis), rope(K, nkv, cis)
         V = V.reshape(n, nkv, hd)
         O = F.scaled_dot_product_attention(Q.transpose(0, 1)[None], K.transpose(0, 1)[None],
                                            V.transpose(0, 1)[None], attn_mask=allowed,

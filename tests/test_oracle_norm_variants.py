@@ -98,3 +98,52 @@ def test_sandwich_with_zero_post_weights_passes_the_embedding_through():
     ms = np.mean(x * x, axis=-1, keepdims=True)
     ref = (x / np.sqrt(ms + cfg.rms_eps) * w.out_norm()) @ w.lm_head().T
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- per-layer RoPE base
+@pytest.mark.parametrize("every", [0, 2, 3])
+def test_per_layer_rope_base_matches_torch_library(every):
+    cfg = toy_cfg(n_layers=3, rope_theta_local=50.0, rope_global_every=every)
+    w = random_weights(cfg, seed=52)
+    toks = _toks(cfg, 9, 53)
+    ref = torch_library_forward(cfg, w, toks)
+    got = Session(cfg, w).prefill(toks, 0, all_logits=True)
+    np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-11)
+    b = Session(cfg, w).prefill_batched(toks, 0, logits_rows=range(9))
+    np.testing.assert_allclose(b, got, rtol=1e-12, atol=1e-12)
+
+
+def test_local_base_equal_to_global_is_the_plain_model():
+    cfg = toy_cfg(n_layers=3)
+    cfg2 = toy_cfg(n_layers=3, rope_theta_local=cfg.rope_theta, rope_global_every=3)
+    w = random_weights(cfg, seed=54)
+    toks = _toks(cfg, 7, 55)
+    assert np.array_equal(Session(cfg, w).prefill(toks, 0, all_logits=True),
+                          Session(cfg2, w).prefill(toks, 0, all_logits=True))
+
+
+def test_global_layer_pattern():
+    cfg = toy_cfg(n_layers=7, rope_theta_local=10.0, rope_global_every=3)
+    assert [cfg.layer_is_global(l) for l in range(7)] == [False, False, True, False, False, True, False]
+    assert not any(toy_cfg(n_layers=4, rope_theta_local=10.0).layer_is_global(l) for l in range(4))
+    assert all(toy_cfg(n_layers=4).layer_is_global(l) for l in range(4))
+
+
+def test_local_base_changes_only_local_layers_keys():
+    # Layer 0's keys do not depend on the cache: with layer 0 global (every=1) they equal the
+    # plain model's; with layer 0 local they are the plain keys rotated by the local base.
+    cfg = toy_cfg(n_layers=2)
+    w = random_weights(cfg, seed=56)
+    toks = _toks(cfg, 5, 57)
+    plain = Session(cfg, w)
+    plain.prefill(toks, 0)
+    glob = Session(toy_cfg(n_layers=2, rope_theta_local=50.0, rope_global_every=1), w)
+    glob.prefill(toks, 0)
+    loc = Session(toy_cfg(n_layers=2, rope_theta_local=50.0, rope_global_every=2), w)
+    loc.prefill(toks, 0)
+    for p in range(5):
+        assert np.array_equal(glob.keys[0][p], plain.keys[0][p])
+        if p > 0:
+            assert not np.allclose(loc.keys[0][p], plain.keys[0][p])
+        np.testing.assert_allclose(np.linalg.norm(loc.keys[0][p], axis=-1),
+                                   np.linalg.norm(plain.keys[0][p], axis=-1), rtol=1e-12)
