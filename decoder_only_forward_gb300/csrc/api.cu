@@ -145,6 +145,8 @@ static bool validate(const dec_config* c, std::string& why) {
   if (c->qk_norm < 0 || c->qk_norm > 2) return bad("qk_norm must be 0 (off), 1 (per head) or 2 (whole row)");
   if (c->qk_norm && c->kv_dtype == DEC_BF16) return bad("qk_norm needs a DEC_F32 or DEC_I8 cache");
   if (c->sandwich_norms != 0 && c->sandwich_norms != 1) return bad("sandwich_norms must be 0 or 1");
+  if (!(c->rope_theta_local >= 0.f) || c->rope_global_every < 0)
+    return bad("rope_theta_local and rope_global_every must be >= 0");
   if (c->rope_llama3 && !(c->rope_factor > 0.f && c->rope_low_freq_factor > 0.f &&
                           c->rope_high_freq_factor > c->rope_low_freq_factor && c->rope_orig_ctx > 0))
     return bad("llama3 RoPE scaling needs factor > 0, 0 < low < high, orig_ctx > 0");
@@ -248,6 +250,9 @@ WsPlan dec::plan_workspace(const dec_config& c) {
   if (p.kpart_bytes > ((size_t)128 << 20)) p.kpart_bytes = (size_t)128 << 20;
   p.kpart = take(p.kpart_bytes);
   p.Z = take(c.sandwich_norms ? 4 * (size_t)T * c.hidden : 0);
+  const bool local = c.rope_theta_local > 0.f;
+  p.inv_freq_local = take(local ? sizeof(double) * (hd / 2) : 0);
+  p.rope_tab_local = take(local ? sizeof(float2) * (size_t)T * (hd / 2) : 0);
   // kHalf with QK-norm: the norm weights follow the permuted q/k dims.
   const size_t qn = c.qk_norm == 2 ? (size_t)qd : (size_t)hd, kn = c.qk_norm == 2 ? (size_t)kd : (size_t)hd;
   p.qk_perm = take(c.qk_norm && c.rope_half ? 4 * (size_t)c.n_layers * (qn + kn) : 0);
@@ -383,6 +388,8 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
   S.kpart = p.kpart_bytes ? (float*)(base + p.kpart) : nullptr;
   S.kpart_bytes = p.kpart_bytes;
   S.Z = cfg->sandwich_norms ? (float*)(base + p.Z) : nullptr;
+  S.inv_freq_local = cfg->rope_theta_local > 0.f ? (double*)(base + p.inv_freq_local) : nullptr;
+  S.rope_tab_local = cfg->rope_theta_local > 0.f ? (float2*)(base + p.rope_tab_local) : nullptr;
   h->layers.resize(cfg->n_layers);
   for (int l = 0; l < cfg->n_layers; ++l) {
     const dec_layer_weights& L = w->layers[l];
@@ -480,6 +487,12 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
     inv[i] = f;
   }
   cudaError_t e = cudaMemcpy(S.inv_freq, inv.data(), inv.size() * sizeof(double), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && S.inv_freq_local) {
+    // Local layers: the same rotary width, their own base, no llama3 scaling.
+    std::vector<double> invl(cfg->head_dim / 2, 0.0);
+    for (int i = 0; i < rdim / 2; ++i) invl[i] = pow((double)cfg->rope_theta_local, -2.0 * i / rdim);
+    e = cudaMemcpy(S.inv_freq_local, invl.data(), invl.size() * sizeof(double), cudaMemcpyHostToDevice);
+  }
   if (e == cudaSuccess) e = cudaMemset(S.st, 0, sizeof(DeviceState));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {

@@ -40,7 +40,8 @@ __global__ void k_rope_rows(const double* __restrict__ inv_freq, int half, int s
 __global__ void k_rows_setup(const __grid_constant__ RowsMeta meta, int B, const int32_t* __restrict__ d_tokens,
                              int32_t host_token, int vocab, const double* __restrict__ inv_freq, int half, int32_t* __restrict__ tokens,
                              int32_t* __restrict__ b_seq, int32_t* __restrict__ b_pos, int32_t* __restrict__ b_rows,
-                             float2* __restrict__ tab, DeviceState* st) {
+                             float2* __restrict__ tab, DeviceState* st, const double* __restrict__ inv_local,
+                             float2* __restrict__ tab_local) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < B) {
     int t = d_tokens ? d_tokens[i] : host_token;
@@ -58,6 +59,10 @@ __global__ void k_rows_setup(const __grid_constant__ RowsMeta meta, int B, const
     double sn, cs;
     sincos((double)meta.pos[r] * inv_freq[p], &sn, &cs);
     tab[i] = make_float2((float)cs, (float)sn);
+    if (tab_local) {   // the local layers' base (per-layer RoPE)
+      sincos((double)meta.pos[r] * inv_local[p], &sn, &cs);
+      tab_local[i] = make_float2((float)cs, (float)sn);
+    }
   }
 }
 
@@ -712,13 +717,13 @@ static cudaError_t oproj_rows(const Model& m, cudaStream_t s, const LayerPtrs& L
 // planes of the tensor-core attention (through S.A, free between the GEMM and
 // the attention), else back into S.Q.
 static void qk_norm_rows(const Model& m, cudaStream_t s, const LayerPtrs& L, int n, float* k_base,
-                         const int32_t* k_rows, int k_row0, bool planes) {
+                         const int32_t* k_rows, int k_row0, bool planes, const float2* rope) {
   const dec_config& c = m.cfg;
   const Scratch& S = m.s;
   const int qd = c.n_heads * c.head_dim;
   float* q_dst = planes ? (float*)S.A : S.Q;
   k_qk_norm_rope<<<dim3(n, 2), 128, 0, s>>>(S.Q, q_dst, k_base, k_rows, k_row0, c.n_heads, c.n_kv_heads,
-                                            c.head_dim, c.qk_norm, L.q_norm, L.k_norm, c.rms_eps, S.rope_tab);
+                                            c.head_dim, c.qk_norm, L.q_norm, L.k_norm, c.rms_eps, rope);
   count_launch(m);
   if (planes) {
     k_rows_to_planes<<<152, 256, 0, s>>>((const float*)S.A, (size_t)n * qd, S.at.Qb, (size_t)S.at.qcap * qd);
@@ -749,6 +754,10 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n,
   k_embed_rows<TW><<<n, 128, 0, s>>>((const TW*)m.tok_embd, S.tokens, h, S.X);
   k_rope_rows<<<(n * half + 255) / 256, 256, 0, s>>>(S.inv_freq, half, start, n, S.rope_tab);
   count_launch(m, 2);
+  if (S.rope_tab_local) {
+    k_rope_rows<<<(n * half + 255) / 256, 256, 0, s>>>(S.inv_freq_local, half, start, n, S.rope_tab_local);
+    count_launch(m);
+  }
 
   // Ring slots equal positions unless this chunk can overwrite history it reads.
   // An int8 cache always takes the linear f32 rows: history read back from the
@@ -781,7 +790,7 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n,
       e.mode = EPI_QKV;
       e.n_out = qd + 2 * kd;
       e.bias = L.bqkv;
-      e.rope = S.rope_tab;
+      e.rope = layer_rope_global(c, l) ? S.rope_tab : S.rope_tab_local;
       e.qd = qd;
       e.kd = kd;
       e.hd = hd;
@@ -792,13 +801,14 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n,
       e.q_out = q_planes && !qkn ? (void*)S.at.Qb : (void*)S.Q;
       e.q_bf16 = q_planes && !qkn;
       e.q_lo = q_planes && !qkn ? S.at.Qb + (size_t)S.at.qcap * qd : nullptr;
+      const float2* rope = e.rope;
       if (qkn) e.rope = nullptr;
       e.k_dst = kdst;
       e.v_dst = vdst;
       e.kv_bf16 = std::is_same<KV, __nv_bfloat16>::value;
       e.kv_row0 = direct ? start : hist;
       chk(gemm<TW>(m, s, a_h, (const TW*)L.wqkv, n, qd + 2 * kd, h, e, 1, n));
-      if (qkn) qk_norm_rows(m, s, L, n, (float*)kdst, nullptr, e.kv_row0, q_planes);
+      if (qkn) qk_norm_rows(m, s, L, n, (float*)kdst, nullptr, e.kv_row0, q_planes, rope);
     }
     const int t_first = n > c.max_seq ? n - c.max_seq : 0;
     if (i8) {
@@ -868,7 +878,7 @@ static cudaError_t decode_rows(const Model& m, cudaStream_t s, int B, float* log
       e.mode = EPI_QKV;
       e.n_out = qd + 2 * kd;
       e.bias = L.bqkv;
-      e.rope = S.rope_tab;
+      e.rope = layer_rope_global(c, l) ? S.rope_tab : S.rope_tab_local;
       e.qd = qd;
       e.kd = kd;
       e.hd = hd;
@@ -879,9 +889,10 @@ static cudaError_t decode_rows(const Model& m, cudaStream_t s, int B, float* log
       e.v_dst = i8 ? S.KVlin_v : L.vc;
       e.kv_bf16 = std::is_same<KV, __nv_bfloat16>::value;
       e.kv_rows = i8 ? nullptr : S.b_rows;
+      const float2* rope = e.rope;
       if (c.qk_norm) e.rope = nullptr;
       chk(gemm<TW>(m, s, a_h, (const TW*)L.wqkv, B, qd + 2 * kd, h, e, 1, B));
-      if (c.qk_norm) qk_norm_rows(m, s, L, B, (float*)e.k_dst, e.kv_rows, 0, false);
+      if (c.qk_norm) qk_norm_rows(m, s, L, B, (float*)e.k_dst, e.kv_rows, 0, false, rope);
     }
     if (i8) {
       launch_kv_quant(c, (const float*)S.KVlin_k, (const float*)S.KVlin_v, B, S.b_rows, 0, 0, L.kc, L.vc, nullptr,
@@ -931,7 +942,7 @@ cudaError_t launch_rows_setup(const Model& m, cudaStream_t s, const RowsMeta& me
   const Scratch& S = m.s;
   k_rows_setup<<<rows_setup_blocks(m, B), 256, 0, s>>>(meta, B, d_tokens, host_token, m.cfg.vocab, S.inv_freq,
                                                        m.cfg.head_dim / 2, S.tokens, S.b_seq, S.b_pos, S.b_rows,
-                                                       S.rope_tab, S.st);
+                                                       S.rope_tab, S.st, S.inv_freq_local, S.rope_tab_local);
   count_launch(m);
   return cudaGetLastError();
 }
@@ -944,8 +955,10 @@ cudaError_t update_rows_setup_node(cudaGraphExec_t g, cudaGraphNode_t node, cons
   int32_t *tokens = S.tokens, *bs = S.b_seq, *bp = S.b_pos, *br = S.b_rows;
   float2* tab = S.rope_tab;
   DeviceState* st = S.st;
+  const double* invl = S.inv_freq_local;
+  float2* tabl = S.rope_tab_local;
   void* args[] = {const_cast<RowsMeta*>(&meta), &B, &d_tokens, &host_token, &vocab, &inv, &half, &tokens, &bs, &bp,
-                  &br, &tab, &st};
+                  &br, &tab, &st, &invl, &tabl};
   cudaKernelNodeParams p = {};
   p.func = reinterpret_cast<void*>(k_rows_setup);
   p.gridDim = dim3(rows_setup_blocks(m, B));

@@ -59,6 +59,8 @@ struct Scratch {
   DeviceState* st;
   double* inv_freq;     // [hd/2] RoPE frequencies (llama3-scaled if enabled)
   float2* rope_tab;     // [max(1,max_tokens)][hd/2] (cos, sin) per position of the current call
+  double* inv_freq_local;  // the local layers' frequencies (per-layer base), else nullptr
+  float2* rope_tab_local;  // their (cos, sin) rows, else nullptr
   float* x;             // [h] decode residual
   float* q;             // [nq*hd]
   float* attn;          // [nq*hd]
@@ -157,6 +159,7 @@ struct WsPlan {
   size_t b_seq, b_pos, b_rows, b_part;  // batched decode
   size_t kpart, kpart_bytes;            // split-K partials
   size_t Z;                             // sandwich block outputs
+  size_t inv_freq_local, rope_tab_local;  // per-layer RoPE base
   size_t qk_perm;                       // kHalf + QK-norm: permuted norm weights
   size_t kv;            // start of the KV rings: [layer][K, V][seq][ring_rows][n_kv*hd]
   size_t kv_layer_bytes; // one layer's K (or V) rings of every sequence
@@ -209,7 +212,12 @@ struct KvRowLayout {
 // Models whose decode runs the row kernels (one row per step): the persistent
 // step and the per-layer decode kernels implement none of these.
 inline bool decode_needs_rows(const dec_config& c) {
-  return c.kv_dtype == DEC_I8 || c.qk_norm != 0 || c.sandwich_norms != 0;
+  return c.kv_dtype == DEC_I8 || c.qk_norm != 0 || c.sandwich_norms != 0 || c.rope_theta_local > 0.f;
+}
+// Whether layer l rotates with the global base (every layer without a local base).
+inline bool layer_rope_global(const dec_config& c, int l) {
+  if (!(c.rope_theta_local > 0.f)) return true;
+  return c.rope_global_every > 0 && (l + 1) % c.rope_global_every == 0;
 }
 inline int kv_group_size(int hd) {
   int g = 1;

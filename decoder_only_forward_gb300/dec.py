@@ -46,7 +46,8 @@ class Config(ctypes.Structure):
         ("rope_factor", ctypes.c_float), ("rope_low_freq_factor", ctypes.c_float),
         ("rope_high_freq_factor", ctypes.c_float), ("rope_orig_ctx", ctypes.c_int32),
         ("rope_half", ctypes.c_int32), ("rope_dim", ctypes.c_int32), ("n_seqs", ctypes.c_int32),
-        ("qk_norm", ctypes.c_int32), ("sandwich_norms", ctypes.c_int32)]
+        ("qk_norm", ctypes.c_int32), ("sandwich_norms", ctypes.c_int32),
+        ("rope_theta_local", ctypes.c_float), ("rope_global_every", ctypes.c_int32)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -138,6 +139,8 @@ def make_config(w: dict, kv_dtype: str = "f32", max_tokens: int = 0, n_seqs: int
     c.n_seqs = int(n_seqs)
     c.qk_norm = {None: 0, "": 0, "head": 1, "row": 2}[w.get("qk_norm")]
     c.sandwich_norms = int(bool(w.get("sandwich_norms", False)))
+    c.rope_theta_local = float(w.get("rope_theta_local", 0.0) or 0.0)
+    c.rope_global_every = int(w.get("rope_global_every", 0) or 0)
     return c
 
 

@@ -109,6 +109,11 @@ typedef struct dec_config {
   int32_t sandwich_norms; /* 1: each block's output (attention after wo, FFN after the down projection or
                              the expert sum) is RMS-normalised with post_attn_norm / post_ffn_norm before
                              the residual add (rml "The decoder", One forward pass step 6) */
+  float rope_theta_local; /* per-layer RoPE base (sipllm "Transformer forward pass", RoPE: Gemma 3): 0 = one
+                             base; else local layers rotate with this base (no llama3 scaling) and every
+                             rope_global_every-th layer, l with (l + 1) % rope_global_every == 0, with
+                             rope_theta (0 = no global layer) */
+  int32_t rope_global_every;
 } dec_config;
 
 /*

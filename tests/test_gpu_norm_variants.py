@@ -93,3 +93,51 @@ def test_smollm2_shape_norm_variants_batched(dec_mod):
     for s_, p in enumerate(prompts):
         ref, _ = oracle_teacher_forced(w, p, taus[s_], 5)
         compare_logits(np.stack(rows[s_]), ref, *tolerances(w))
+
+
+@pytest.mark.parametrize("kw", [dict(rope_theta_local=50.0, rope_global_every=2),
+                                dict(rope_theta_local=50.0, rope_global_every=0),
+                                dict(rope_theta_local=500.0, rope_global_every=2, qk_norm="head",
+                                     sandwich_norms=True)])
+def test_toy_per_layer_rope_base(dec_mod, kw):
+    w = synthetic.workload("toy", **kw)
+    rows, taus, ref = _run(dec_mod, w, 16, 10, seed=5)
+    tol, _ = tolerances(w)
+    compare_logits(rows, ref, tol, tol)
+
+
+def test_gemma_like_combination_chunked_window(dec_mod):
+    # Local base on layer 0, global on layer 1, QK-norm, sandwich norms, a window, chunked prefill.
+    w = synthetic.workload("toy", rope_theta_local=20.0, rope_global_every=2, qk_norm="head",
+                           sandwich_norms=True, sliding_window=8, max_seq=8)
+    rows, taus, ref = _run(dec_mod, w, 13, 9, max_tokens=5, seed=6)
+    tol, _ = tolerances(w)
+    compare_logits(rows, ref, tol, tol)
+
+
+def test_qwen_shape_per_layer_base_batched(dec_mod):
+    w = synthetic.workload("qwen2.5-0.5b", n_layers=3, rope_theta_local=10000.0, rope_global_every=3)
+    prompts = [list(synthetic.prompt_tokens(w, n, seed=97 + i)) for i, n in enumerate([6, 21])]
+    d = dec_mod.Decoder(w, n_seqs=2)
+    V = w["vocab"]
+    lg = torch.empty(V, device="cuda")
+    rows = [[] for _ in prompts]
+    taus = [[] for _ in prompts]
+    for s_, p in enumerate(prompts):
+        d.prefill(p, 0, lg, seq=s_)
+        d.synchronize()
+        rows[s_].append(lg.cpu().numpy().copy())
+        taus[s_].append(int(np.argmax(rows[s_][-1])))
+    tok = torch.tensor([t[0] for t in taus], dtype=torch.int32, device="cuda")
+    out = torch.empty((2, V), device="cuda")
+    for _ in range(4):
+        d.decode_batch([0, 1], [d.length_of(0), d.length_of(1)], tok, out, tok)
+        d.synchronize()
+        h = out.cpu().numpy()
+        for s_ in range(2):
+            rows[s_].append(h[s_].copy())
+            taus[s_].append(int(np.argmax(h[s_])))
+    d.check()
+    for s_, p in enumerate(prompts):
+        ref, _ = oracle_teacher_forced(w, p, taus[s_], 4)
+        compare_logits(np.stack(rows[s_]), ref, *tolerances(w))
