@@ -416,7 +416,10 @@ def run_batched(args, w, weights, dev, kv_es):
     B, P, V = args.batch, w["prompt"], w["vocab"]
     if w["sliding_window"] == 0 and P + 3 + args.batch_steps > w["max_seq"]:
         return {"skipped": "the cache cannot hold the prompt plus the timed steps"}
-    d = dec.Decoder(w, weights=weights, device=dev, kv_dtype=args.kv, n_seqs=B)
+    # A paged cache gets exactly the pages B sequences of max_seq positions need.
+    ps = args.page_size
+    n_pages = B * ((w["max_seq"] + ps - 1) // ps) if ps else 0
+    d = dec.Decoder(w, weights=weights, device=dev, kv_dtype=args.kv, n_seqs=B, page_size=ps, n_pages=n_pages)
     lg = torch.empty(V, dtype=torch.float32, device=dev)
     for sq in range(B):
         d.prefill(synthetic.prompt_tokens(w, P, seed=100 + sq), 0, lg, seq=sq)
@@ -450,6 +453,7 @@ def run_batched(args, w, weights, dev, kv_es):
     out = {"batch": B, "steps": K, "tok_s": round(B * 1e3 / ms, 1), "ms_per_step": round(ms, 4),
            "bytes_per_step": int(nbytes), "hbm_frac": round(nbytes / (ms / 1e3) / (hbm * 1e9), 4),
            "attn_ms_per_step": round(attn_ms, 4), "gpu_launches_per_step": int(launches / K),
+           "kv_layout": f"paged, {ps} positions per page" if ps else "contiguous rings",
            "note": "each sequence prefilled with its own prompt; one CUDA graph per step; bytes count every "
                    "weight once plus each row's readable K/V"}
     d.close()
@@ -529,6 +533,8 @@ def main():
     ap.add_argument("--qk-norm", default="", choices=["", "head", "row"],
                     help="architecture variant: QK-norm (adds q_norm/k_norm weights)")
     ap.add_argument("--sandwich", action="store_true", help="architecture variant: sandwich norms")
+    ap.add_argument("--page-size", type=int, default=0,
+                    help="batched decode on a paged cache of this page size (0: contiguous rings)")
     ap.add_argument("--profile", type=int, default=0, metavar="D",
                     help="profiling driver: one prefill + D decode steps, kernels launched one by one "
                          "(no graph, no timing passes, no JSON); for per-kernel profilers")

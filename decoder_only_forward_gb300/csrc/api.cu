@@ -18,6 +18,10 @@ struct dec_handle {
   cudaStream_t stream;
   std::vector<int32_t> lens;   // positions held per sequence (host bookkeeping)
   RowsMeta meta;        // rows of the current batched decode step
+  // paged cache: host copy of the page table and the free pages
+  std::vector<int32_t> pages;       // [n_seqs][pages_per_seq], -1 = none
+  std::vector<int32_t> free_pages;  // a stack
+  PageSet pset;
   std::string err;
   // decode graph, captured for one (logits, d_argmax) pair
   cudaGraphExec_t graph = nullptr;
@@ -147,6 +151,10 @@ static bool validate(const dec_config* c, std::string& why) {
   if (c->sandwich_norms != 0 && c->sandwich_norms != 1) return bad("sandwich_norms must be 0 or 1");
   if (!(c->rope_theta_local >= 0.f) || c->rope_global_every < 0)
     return bad("rope_theta_local and rope_global_every must be >= 0");
+  if (c->page_size < 0 || (c->page_size > 0 && (c->page_size < 16 || (c->page_size & (c->page_size - 1)))))
+    return bad("page_size must be 0 or a power of two >= 16");
+  if (c->page_size > 0 && c->n_pages < 1) return bad("a paged cache needs n_pages >= 1");
+  if (c->n_pages < 0) return bad("n_pages must be >= 0");
   if (c->rope_llama3 && !(c->rope_factor > 0.f && c->rope_low_freq_factor > 0.f &&
                           c->rope_high_freq_factor > c->rope_low_freq_factor && c->rope_orig_ctx > 0))
     return bad("llama3 RoPE scaling needs factor > 0, 0 < low < high, orig_ctx > 0");
@@ -261,9 +269,18 @@ WsPlan dec::plan_workspace(const dec_config& c) {
   p.n_seqs = c.n_seqs > 0 ? c.n_seqs : 1;
   p.ring_rows = (int)align_up((size_t)c.max_seq, 64);
   p.ring_bytes = (size_t)kv_row_layout(c).bytes * p.ring_rows;
+  p.pages_per_seq = c.page_size > 0 ? (c.max_seq + c.page_size - 1) / c.page_size : 0;
+  p.page_table = take(c.page_size > 0 ? 4 * (size_t)p.n_seqs * p.pages_per_seq : 0);
   p.kv = off;
-  p.kv_layer_bytes = p.ring_bytes * p.n_seqs;
-  off += 2 * p.kv_layer_bytes * c.n_layers;
+  if (c.page_size > 0) {
+    // Arena of pages, each [layer][K, V][page_size rows]; one layer's K base is
+    // kv + layer * 2 * page_size rows, pages 2 * n_layers * page_size rows apart.
+    p.kv_layer_bytes = (size_t)kv_row_layout(c).bytes * c.page_size;   // one K (or V) block of a page
+    off += (size_t)c.n_pages * 2 * c.n_layers * p.kv_layer_bytes;
+  } else {
+    p.kv_layer_bytes = p.ring_bytes * p.n_seqs;
+    off += 2 * p.kv_layer_bytes * c.n_layers;
+  }
   p.total = off;
   return p;
 }
@@ -321,6 +338,11 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
   if (!h) return fail(nullptr, DEC_EINVAL, "out of host memory");
   h->stream = (cudaStream_t)cuda_stream;
   h->lens.assign(p.n_seqs, 0);
+  if (cfg->page_size > 0) {
+    h->pages.assign((size_t)p.n_seqs * p.pages_per_seq, -1);
+    h->free_pages.resize(cfg->n_pages);
+    for (int i = 0; i < cfg->n_pages; ++i) h->free_pages[i] = cfg->n_pages - 1 - i;   // page 0 on top
+  }
   Model& m = h->m;
   m.cfg = *cfg;
   if (m.cfg.max_tokens == 0) m.cfg.max_tokens = p.max_tokens;
@@ -331,6 +353,14 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
   m.n_seqs = p.n_seqs;
   m.ring_rows = p.ring_rows;
   m.ring_bytes = p.ring_bytes;
+  m.paging = KvPaging{};
+  m.paging.ring_rows = p.ring_rows;
+  if (cfg->page_size > 0) {
+    m.paging.table = (const int32_t*)((char*)workspace + p.page_table);
+    m.paging.pages_per_seq = p.pages_per_seq;
+    m.paging.page = cfg->page_size;
+    m.paging.stride_rows = 2LL * cfg->n_layers * cfg->page_size;
+  }
   // LM head: two CTAs per SM, each warp walking its row pairs with the next
   // pair's loads in flight.
   int lg = (cfg->vocab / 2 + 7) / 8;
@@ -402,7 +432,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
     d.w_gateup = L.w_gateup;
     d.w_down = L.w_down;
     d.router = cfg->n_experts > 0 ? L.router : nullptr;
-    d.kc = base + p.kv + (size_t)(2 * l) * p.kv_layer_bytes;
+    d.kc = base + p.kv + (size_t)(2 * l) * p.kv_layer_bytes;       // paged: page 0's blocks of layer l
     d.vc = base + p.kv + (size_t)(2 * l + 1) * p.kv_layer_bytes;
     d.q_norm = cfg->qk_norm ? (const float*)L.q_norm : nullptr;
     d.k_norm = cfg->qk_norm ? (const float*)L.k_norm : nullptr;
@@ -527,6 +557,56 @@ static dec_status check_positions(dec_handle* h, int32_t seq, int32_t n, int32_t
   return DEC_OK;
 }
 
+// Paged cache: the pages that writing positions [p0, p0 + n) of seq needs and
+// does not hold yet, taken from the free stack (all or none: DEC_ENOMEM leaves
+// everything as it was), then written into the device table on the stream.
+static dec_status reserve_pages(dec_handle* h, const int32_t* seqs, const int32_t* p0s, int count, int32_t n) {
+  const dec_config& c = h->m.cfg;
+  if (c.page_size <= 0) return DEC_OK;
+  const int pps = h->m.paging.pages_per_seq, P = c.page_size;
+  std::vector<std::pair<int, int>> taken;   // (table index, page)
+  for (int i = 0; i < count; ++i) {
+    const int32_t span = n < c.max_seq ? n : c.max_seq;   // under a window the slots of n > max_seq repeat
+    for (int32_t t = 0; t < span; ++t) {
+      const int32_t p = p0s[i] + t;
+      const int32_t slot = c.sliding_window > 0 ? p % c.max_seq : p;
+      const int idx = seqs[i] * pps + slot / P;
+      if (h->pages[idx] >= 0) continue;
+      if (h->free_pages.empty()) {
+        for (auto& tp : taken) {
+          h->free_pages.push_back(tp.second);
+          h->pages[tp.first] = -1;
+        }
+        return fail(h, DEC_ENOMEM, "paged cache: all %d pages are in use", c.n_pages);
+      }
+      const int pg = h->free_pages.back();
+      h->free_pages.pop_back();
+      h->pages[idx] = pg;
+      taken.emplace_back(idx, pg);
+    }
+  }
+  PageSet& ps = h->pset;
+  for (size_t i = 0; i < taken.size(); i += 256) {
+    ps.n = (int)std::min<size_t>(256, taken.size() - i);
+    for (int j = 0; j < ps.n; ++j) {
+      ps.idx[j] = taken[i + j].first;
+      ps.val[j] = taken[i + j].second;
+    }
+    launch_set_pages(const_cast<int32_t*>(h->m.paging.table), ps, h->stream);
+  }
+  return cuda_check(h, "page table update");
+}
+
+static void release_pages(dec_handle* h, int32_t seq) {
+  if (h->m.cfg.page_size <= 0) return;
+  const int pps = h->m.paging.pages_per_seq;
+  for (int i = 0; i < pps; ++i) {
+    int32_t& e = h->pages[(size_t)seq * pps + i];
+    if (e >= 0) h->free_pages.push_back(e);
+    e = -1;
+  }
+}
+
 dec_status dec_prefill_seq(dec_handle* h, int32_t seq, const int32_t* tokens, int32_t n, int32_t start_pos,
                            float* logits, int32_t* d_argmax) {
   if (!h) return DEC_EINVAL;
@@ -537,6 +617,8 @@ dec_status dec_prefill_seq(dec_handle* h, int32_t seq, const int32_t* tokens, in
   for (int32_t i = 0; i < n; ++i)
     if (tokens[i] < 0 || tokens[i] >= h->m.cfg.vocab)
       return fail(h, DEC_EINVAL, "token %d at index %d outside [0, %d)", tokens[i], i, h->m.cfg.vocab);
+  st = reserve_pages(h, &seq, &start_pos, 1, n);
+  if (st != DEC_OK) return st;
   const int T = h->m.cfg.max_tokens;
   timing_start(h);
   for (int32_t done = 0; done < n; done += T) {
@@ -678,6 +760,31 @@ dec_status dec_kv_reset_seq(dec_handle* h, int32_t seq) {
   if (!h) return DEC_EINVAL;
   if (seq < 0 || seq >= h->m.n_seqs) return fail(h, DEC_EINVAL, "sequence %d outside [0, %d)", seq, h->m.n_seqs);
   h->lens[seq] = 0;
+  release_pages(h, seq);
+  return DEC_OK;
+}
+
+int32_t dec_pages_free(const dec_handle* h) {
+  if (!h || h->m.cfg.page_size <= 0) return -1;
+  return (int32_t)h->free_pages.size();
+}
+
+dec_status dec_kv_slot(const dec_handle* h, int32_t layer, int32_t seq, int32_t slot, void** k, void** v) {
+  if (!h || !k || !v || layer < 0 || layer >= h->m.cfg.n_layers || seq < 0 || seq >= h->m.n_seqs || slot < 0 ||
+      slot >= h->m.cfg.max_seq)
+    return DEC_EINVAL;
+  const KvPaging& pg = h->m.paging;
+  long long row;
+  if (h->m.cfg.page_size > 0) {
+    const int32_t page = h->pages[(size_t)seq * pg.pages_per_seq + slot / pg.page];
+    if (page < 0) return DEC_EINVAL;
+    row = page * pg.stride_rows + slot % pg.page;
+  } else {
+    row = (long long)seq * pg.ring_rows + slot;
+  }
+  const size_t rb = (size_t)kv_row_layout(h->m.cfg).bytes;
+  *k = (char*)h->m.layers[layer].kc + (size_t)row * rb;
+  *v = (char*)h->m.layers[layer].vc + (size_t)row * rb;
   return DEC_OK;
 }
 
@@ -694,12 +801,20 @@ static dec_status run_rows(dec_handle* h, int32_t batch, const int32_t* seqs, co
                            const int32_t* d_tokens, int32_t host_token, float* logits, int32_t* d_argmax) {
   const dec_config& c = h->m.cfg;
   RowsMeta& meta = h->meta;
+  const dec_status ps = reserve_pages(h, seqs, positions, batch, 1);
+  if (ps != DEC_OK) return ps;
   for (int32_t i = 0; i < batch; ++i) {
     const int32_t p = positions[i];
     const int32_t slot = c.sliding_window > 0 ? p % c.max_seq : p;
     meta.seq[i] = seqs[i];
     meta.pos[i] = p;
-    meta.rows[i] = seqs[i] * h->m.ring_rows + slot;
+    if (c.page_size > 0) {
+      const KvPaging& pg = h->m.paging;
+      meta.rows[i] = (int32_t)(h->pages[(size_t)seqs[i] * pg.pages_per_seq + slot / pg.page] * pg.stride_rows +
+                               slot % pg.page);
+    } else {
+      meta.rows[i] = seqs[i] * h->m.ring_rows + slot;
+    }
   }
   if (h->stream == nullptr || !h->use_graph) {
     timing_start(h);
@@ -835,7 +950,8 @@ dec_status dec_kv_layer(const dec_handle* h, int32_t layer, void** k, void** v) 
 }
 
 dec_status dec_kv_layer_seq(const dec_handle* h, int32_t layer, int32_t seq, void** k, void** v) {
-  if (!h || !k || !v || layer < 0 || layer >= h->m.cfg.n_layers || seq < 0 || seq >= h->m.n_seqs)
+  if (!h || !k || !v || layer < 0 || layer >= h->m.cfg.n_layers || seq < 0 || seq >= h->m.n_seqs ||
+      h->m.cfg.page_size > 0)
     return DEC_EINVAL;
   *k = (char*)h->m.layers[layer].kc + (size_t)seq * h->m.ring_bytes;
   *v = (char*)h->m.layers[layer].vc + (size_t)seq * h->m.ring_bytes;

@@ -67,7 +67,7 @@ __host__ __device__ constexpr size_t ar_smem_bytes(int G) {
 // NHG: head groups of 4 held in registers (G <= 4 * NHG).
 template <typename KV, int HD, int NHG>
 __global__ void __launch_bounds__(AR_THREADS) k_attn_rows(
-    const float* __restrict__ Q, const char* __restrict__ kc, const char* __restrict__ vc, size_t ring_bytes,
+    const float* __restrict__ Q, const char* __restrict__ kc, const char* __restrict__ vc, const KvPaging pg,
     int row_bytes, int code_off, int qgroup, const int32_t* __restrict__ seq, const int32_t* __restrict__ pos, int nq,
     int nkv, int max_seq, int sliding, float* __restrict__ part) {
   constexpr bool I8 = std::is_same<KV, int8_t>::value;
@@ -95,8 +95,9 @@ __global__ void __launch_bounds__(AR_THREADS) k_attn_rows(
   const int m = sliding > 0 ? min(p + 1, max_seq) : p + 1;
   const int per = ((m + nsplit - 1) / nsplit + AR_TILE - 1) / AR_TILE * AR_TILE;
   const int j0 = split * per, j1 = min(m, j0 + per);
-  const char* K = kc + (size_t)seq[b] * ring_bytes;
-  const char* V = vc + (size_t)seq[b] * ring_bytes;
+  const char* K = kc;   // the layer's bases; rows through pg
+  const char* V = vc;
+  const int sq = seq[b];
   const float* q = Q + (size_t)b * nq * HD + (size_t)g * G * HD;
   const float scale = 1.0f / sqrtf((float)HD);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -130,7 +131,7 @@ __global__ void __launch_bounds__(AR_THREADS) k_attn_rows(
     for (int j = 0; j < LPT; ++j) {
       const int i = tid + j * AR_THREADS, row = i / CPR, c = i % CPR;
       if (i < AR_TILE * CPR && t0 + row < j1) {
-        const size_t rb = (size_t)(t0 + row) * row_bytes;
+        const size_t rb = (size_t)kv_phys_row(pg, sq, t0 + row) * row_bytes;
         const int ch = g * HD + c * CE;   // first channel of the chunk
         const size_t off = I8 ? rb + code_off + ch : rb + (size_t)ch * sizeof(KV);
         kr[j] = __ldcs(reinterpret_cast<const uint4*>(K + off));
@@ -330,7 +331,7 @@ struct ArcLayout {
 
 template <typename KV, int HD, int NHG>
 __global__ void __launch_bounds__(AR_THREADS) k_attn_rows_c(
-    const float* __restrict__ Q, const char* __restrict__ kc, const char* __restrict__ vc, size_t ring_bytes,
+    const float* __restrict__ Q, const char* __restrict__ kc, const char* __restrict__ vc, const KvPaging pg,
     int row_bytes, int code_off, const int32_t* __restrict__ seq, const int32_t* __restrict__ pos, int nq, int nkv,
     int max_seq, int sliding, float* __restrict__ part) {
   using LY = ArcLayout<KV, HD>;
@@ -361,8 +362,9 @@ __global__ void __launch_bounds__(AR_THREADS) k_attn_rows_c(
   const int m = sliding > 0 ? min(p + 1, max_seq) : p + 1;
   const int per = ((m + nsplit - 1) / nsplit + AR_TILE - 1) / AR_TILE * AR_TILE;
   const int j0 = split * per, j1 = min(m, j0 + per);
-  const char* K = kc + (size_t)seq[b] * ring_bytes;
-  const char* V = vc + (size_t)seq[b] * ring_bytes;
+  const char* K = kc;   // the layer's bases; rows through pg
+  const char* V = vc;
+  const int sq = seq[b];
   const float* q = Q + (size_t)b * nq * HD + (size_t)g * G * HD;
   const float scale = 1.0f / sqrtf((float)HD);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -394,7 +396,7 @@ __global__ void __launch_bounds__(AR_THREADS) k_attn_rows_c(
     for (int j = 0; j < LPT; ++j) {
       const int i = tid + j * AR_THREADS, row = i / NCH, c = i % NCH;
       if (i < AR_TILE * NCH && t0 + row < j1) {
-        const size_t off = (size_t)(t0 + row) * row_bytes + head_off + c * 16;
+        const size_t off = (size_t)kv_phys_row(pg, sq, t0 + row) * row_bytes + head_off + c * 16;
         kr[j] = __ldcs(reinterpret_cast<const uint4*>(K + off));
         vr[j] = __ldcs(reinterpret_cast<const uint4*>(V + off));
       }
@@ -402,7 +404,7 @@ __global__ void __launch_bounds__(AR_THREADS) k_attn_rows_c(
     if constexpr (I8) {
       const int row = tid / NG, gi = tid % NG;
       if (tid < AR_TILE * NG && t0 + row < j1) {
-        const size_t off = (size_t)(t0 + row) * row_bytes + 4 * ((size_t)g * NG + gi);
+        const size_t off = (size_t)kv_phys_row(pg, sq, t0 + row) * row_bytes + 4 * ((size_t)g * NG + gi);
         ksr = __ldcs(reinterpret_cast<const float*>(K + off));
         vsr = __ldcs(reinterpret_cast<const float*>(V + off));
       }
@@ -615,7 +617,7 @@ int attn_rows_splits(const dec_config& c) {
 }
 
 template <typename KV, int HD, int NHG>
-static void attn_rows_g(const dec_config& c, const float* Q, const void* kc, const void* vc, size_t ring_bytes,
+static void attn_rows_g(const dec_config& c, const float* Q, const void* kc, const void* vc, const KvPaging& pg,
                         const int32_t* seq, const int32_t* pos, int B, int nsplit, float* part, cudaStream_t s) {
   const KvRowLayout L = kv_row_layout(c);
   const dim3 grid(c.n_kv_heads, nsplit, B);
@@ -624,7 +626,7 @@ static void attn_rows_g(const dec_config& c, const float* Q, const void* kc, con
     const size_t smem = ArcLayout<KV, HD>::bytes(c.n_heads / c.n_kv_heads);
     if (smem > 48 * 1024)
       cudaFuncSetAttribute(k_attn_rows_c<KV, HD, NHG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k_attn_rows_c<KV, HD, NHG><<<grid, AR_THREADS, smem, s>>>(Q, (const char*)kc, (const char*)vc, ring_bytes,
+    k_attn_rows_c<KV, HD, NHG><<<grid, AR_THREADS, smem, s>>>(Q, (const char*)kc, (const char*)vc, pg,
                                                               L.bytes, L.code_off, seq, pos, c.n_heads,
                                                               c.n_kv_heads, c.max_seq, c.sliding_window, part);
     return;
@@ -632,40 +634,40 @@ static void attn_rows_g(const dec_config& c, const float* Q, const void* kc, con
   const size_t smem = ar_smem_bytes<HD>(c.n_heads / c.n_kv_heads);
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(k_attn_rows<KV, HD, NHG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  k_attn_rows<KV, HD, NHG><<<grid, AR_THREADS, smem, s>>>(Q, (const char*)kc, (const char*)vc, ring_bytes, L.bytes, L.code_off,
+  k_attn_rows<KV, HD, NHG><<<grid, AR_THREADS, smem, s>>>(Q, (const char*)kc, (const char*)vc, pg, L.bytes, L.code_off,
                                                   L.group, seq, pos, c.n_heads, c.n_kv_heads, c.max_seq,
                                                   c.sliding_window, part);
 }
 
 template <typename KV, int HD>
-static void attn_rows(const dec_config& c, const float* Q, const void* kc, const void* vc, size_t ring_bytes,
+static void attn_rows(const dec_config& c, const float* Q, const void* kc, const void* vc, const KvPaging& pg,
                       const int32_t* seq, const int32_t* pos, int B, int nsplit, float* part, RowOut out,
                       cudaStream_t s) {
   const int G = c.n_heads / c.n_kv_heads;
-  if (G <= 4) attn_rows_g<KV, HD, 1>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, s);
-  else if (G <= 8) attn_rows_g<KV, HD, 2>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, s);
-  else attn_rows_g<KV, HD, 4>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, s);
+  if (G <= 4) attn_rows_g<KV, HD, 1>(c, Q, kc, vc, pg, seq, pos, B, nsplit, part, s);
+  else if (G <= 8) attn_rows_g<KV, HD, 2>(c, Q, kc, vc, pg, seq, pos, B, nsplit, part, s);
+  else attn_rows_g<KV, HD, 4>(c, Q, kc, vc, pg, seq, pos, B, nsplit, part, s);
   k_attn_rows_merge<HD><<<dim3(c.n_heads, B), HD, 0, s>>>(part, c.n_heads, nsplit, out);
 }
 
 template <int HD>
-static void attn_rows_hd(const dec_config& c, const float* Q, const void* kc, const void* vc, size_t ring_bytes,
+static void attn_rows_hd(const dec_config& c, const float* Q, const void* kc, const void* vc, const KvPaging& pg,
                          const int32_t* seq, const int32_t* pos, int B, int nsplit, float* part, RowOut out,
                          cudaStream_t s) {
   if (c.kv_dtype == DEC_BF16)
-    attn_rows<__nv_bfloat16, HD>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s);
+    attn_rows<__nv_bfloat16, HD>(c, Q, kc, vc, pg, seq, pos, B, nsplit, part, out, s);
   else if (c.kv_dtype == DEC_I8)
-    attn_rows<int8_t, HD>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s);
+    attn_rows<int8_t, HD>(c, Q, kc, vc, pg, seq, pos, B, nsplit, part, out, s);
   else
-    attn_rows<float, HD>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s);
+    attn_rows<float, HD>(c, Q, kc, vc, pg, seq, pos, B, nsplit, part, out, s);
 }
 
-void launch_attn_rows(const dec_config& c, const float* Q, const void* kc, const void* vc, size_t ring_bytes,
+void launch_attn_rows(const dec_config& c, const float* Q, const void* kc, const void* vc, const KvPaging& pg,
                       const int32_t* seq, const int32_t* pos, int B, int nsplit, float* part, RowOut out,
                       cudaStream_t s) {
-  if (c.head_dim == 16) attn_rows_hd<16>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s);
-  else if (c.head_dim == 64) attn_rows_hd<64>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s);
-  else attn_rows_hd<128>(c, Q, kc, vc, ring_bytes, seq, pos, B, nsplit, part, out, s);
+  if (c.head_dim == 16) attn_rows_hd<16>(c, Q, kc, vc, pg, seq, pos, B, nsplit, part, out, s);
+  else if (c.head_dim == 64) attn_rows_hd<64>(c, Q, kc, vc, pg, seq, pos, B, nsplit, part, out, s);
+  else attn_rows_hd<128>(c, Q, kc, vc, pg, seq, pos, B, nsplit, part, out, s);
 }
 
 }  // namespace dec

@@ -21,7 +21,8 @@ namespace dec {
 // once, before its own store.
 __global__ void __launch_bounds__(256) k_kv_quant(const float* src_k, const float* src_v,
                                                   int n, int kd, int G, const int32_t* __restrict__ dst_rows,
-                                                  int pos0, int sliding, int max_seq, int t_first,
+                                                  const KvPaging pg, int seq, int pos0, int sliding, int max_seq,
+                                                  int t_first,
                                                   char* __restrict__ ring_k, char* __restrict__ ring_v,
                                                   int row_bytes, int code_off, float* rt_k, float* rt_v) {
   const int lane = threadIdx.x & 31;
@@ -49,7 +50,7 @@ __global__ void __launch_bounds__(256) k_kv_quant(const float* src_k, const floa
     row = dst_rows[r];
   } else {
     const int p = pos0 + r;
-    row = sliding > 0 ? p % max_seq : p;
+    row = kv_phys_row(pg, seq, sliding > 0 ? p % max_seq : p);
   }
   char* dst = (is_v ? ring_v : ring_k) + row * (long long)row_bytes;
   dst[code_off + ch] = (char)(signed char)code;
@@ -58,13 +59,13 @@ __global__ void __launch_bounds__(256) k_kv_quant(const float* src_k, const floa
 
 // Ring rows of positions h0 .. h0 + count - 1 (slot p % max_seq) -> f32 rows,
 // read back as code * s.
-__global__ void k_kv_gather_i8(const char* __restrict__ ring_k, const char* __restrict__ ring_v, int max_seq,
-                               int kd, int G, int row_bytes, int code_off, int h0, int count,
+__global__ void k_kv_gather_i8(const char* __restrict__ ring_k, const char* __restrict__ ring_v, const KvPaging pg,
+                               int seq, int max_seq, int kd, int G, int row_bytes, int code_off, int h0, int count,
                                float* __restrict__ lin_k, float* __restrict__ lin_v) {
   const size_t total = (size_t)count * kd;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
     const int r = (int)(i / kd), c = (int)(i % kd);
-    const size_t row = (size_t)((h0 + r) % max_seq) * row_bytes;
+    const size_t row = (size_t)kv_phys_row(pg, seq, (h0 + r) % max_seq) * row_bytes;
     const float sk = reinterpret_cast<const float*>(ring_k + row)[c / G];
     const float sv = reinterpret_cast<const float*>(ring_v + row)[c / G];
     lin_k[i] = __fmul_rn((float)(signed char)ring_k[row + code_off + c], sk);
@@ -73,22 +74,32 @@ __global__ void k_kv_gather_i8(const char* __restrict__ ring_k, const char* __re
 }
 
 void launch_kv_quant(const dec_config& c, const float* src_k, const float* src_v, int n, const int32_t* dst_rows,
-                     int pos0, int t_first, void* ring_k, void* ring_v, float* rt_k, float* rt_v, cudaStream_t s,
-                     int planes) {
+                     const KvPaging& pg, int seq, int pos0, int t_first, void* ring_k, void* ring_v, float* rt_k,
+                     float* rt_v, cudaStream_t s, int planes) {
   const KvRowLayout L = kv_row_layout(c);
   const int kd = c.n_kv_heads * c.head_dim;
   const int warps = 8;
   const dim3 grid((kd + 32 * warps - 1) / (32 * warps), n, planes);
-  k_kv_quant<<<grid, 32 * warps, 0, s>>>(src_k, src_v, n, kd, L.group, dst_rows, pos0, c.sliding_window, c.max_seq,
-                                         t_first, (char*)ring_k, (char*)ring_v, L.bytes, L.code_off, rt_k, rt_v);
+  k_kv_quant<<<grid, 32 * warps, 0, s>>>(src_k, src_v, n, kd, L.group, dst_rows, pg, seq, pos0, c.sliding_window,
+                                         c.max_seq, t_first, (char*)ring_k, (char*)ring_v, L.bytes, L.code_off, rt_k,
+                                         rt_v);
 }
 
-void launch_kv_gather_i8(const dec_config& c, const void* ring_k, const void* ring_v, int h0, int count,
-                         float* lin_k, float* lin_v, cudaStream_t s) {
+void launch_kv_gather_i8(const dec_config& c, const void* ring_k, const void* ring_v, const KvPaging& pg, int seq,
+                         int h0, int count, float* lin_k, float* lin_v, cudaStream_t s) {
   const KvRowLayout L = kv_row_layout(c);
-  k_kv_gather_i8<<<152, 256, 0, s>>>((const char*)ring_k, (const char*)ring_v, c.max_seq,
+  k_kv_gather_i8<<<152, 256, 0, s>>>((const char*)ring_k, (const char*)ring_v, pg, seq, c.max_seq,
                                      c.n_kv_heads * c.head_dim, L.group, L.bytes, L.code_off, h0, count, lin_k,
                                      lin_v);
+}
+
+__global__ void k_set_pages(int32_t* __restrict__ table, const __grid_constant__ PageSet ps) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < ps.n) table[ps.idx[i]] = ps.val[i];
+}
+
+void launch_set_pages(int32_t* table, const PageSet& ps, cudaStream_t s) {
+  if (ps.n > 0) k_set_pages<<<1, 256, 0, s>>>(table, ps);
 }
 
 }  // namespace dec
@@ -108,8 +119,10 @@ extern "C" dec_status dec_kv_quantize_int8(const float* x, int32_t n_rows, int32
   c.head_dim = head_dim;
   c.kv_dtype = DEC_I8;
   c.max_seq = n_rows;
-  launch_kv_quant(c, x, nullptr, n_rows, nullptr, 0, 0, out, nullptr, nullptr, nullptr, (cudaStream_t)cuda_stream,
-                  1);
+  KvPaging pg{};
+  pg.ring_rows = n_rows;
+  launch_kv_quant(c, x, nullptr, n_rows, nullptr, pg, 0, 0, 0, out, nullptr, nullptr, nullptr,
+                  (cudaStream_t)cuda_stream, 1);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_global_error(cudaGetErrorString(e));

@@ -273,12 +273,12 @@ __global__ void __launch_bounds__(256) k_attn_prefill_simt(
 // K/V ring <-> linear rows, for chunks whose positions wrap the ring.
 
 template <typename KV>
-__global__ void k_kv_gather(const KV* __restrict__ ring_k, const KV* __restrict__ ring_v, int max_seq, int kd,
-                            int h0, int count, KV* __restrict__ lin_k, KV* __restrict__ lin_v) {
+__global__ void k_kv_gather(const KV* __restrict__ ring_k, const KV* __restrict__ ring_v, const KvPaging pg, int seq,
+                            int max_seq, int kd, int h0, int count, KV* __restrict__ lin_k, KV* __restrict__ lin_v) {
   const size_t total = (size_t)count * kd;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
     const int r = (int)(i / kd), c = (int)(i % kd);
-    const size_t src = (size_t)((h0 + r) % max_seq) * kd + c;
+    const size_t src = (size_t)kv_phys_row(pg, seq, (h0 + r) % max_seq) * kd + c;
     lin_k[i] = ring_k[src];
     lin_v[i] = ring_v[src];
   }
@@ -286,11 +286,12 @@ __global__ void k_kv_gather(const KV* __restrict__ ring_k, const KV* __restrict_
 
 template <typename KV>
 __global__ void k_kv_commit(const KV* __restrict__ lin_k, const KV* __restrict__ lin_v, int lin_row0, int start,
-                            int t_first, int n, int max_seq, int kd, KV* __restrict__ ring_k, KV* __restrict__ ring_v) {
+                            int t_first, int n, int max_seq, int kd, KV* __restrict__ ring_k, KV* __restrict__ ring_v,
+                            const KvPaging pg, int seq) {
   const size_t total = (size_t)(n - t_first) * kd;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
     const int t = t_first + (int)(i / kd), c = (int)(i % kd);
-    const size_t dst = (size_t)((start + t) % max_seq) * kd + c;
+    const size_t dst = (size_t)kv_phys_row(pg, seq, (start + t) % max_seq) * kd + c;
     const size_t src = (size_t)(lin_row0 + t) * kd + c;
     ring_k[dst] = lin_k[src];
     ring_v[dst] = lin_v[src];
@@ -763,7 +764,8 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n,
   // An int8 cache always takes the linear f32 rows: history read back from the
   // ring, the chunk's rows quantised and read back before attention.
   const bool i8 = c.kv_dtype == DEC_I8;
-  const bool direct = !i8 && (c.sliding_window == 0 || start + n <= c.max_seq);
+  const bool paged = m.paging.table != nullptr;
+  const bool direct = !i8 && !paged && (c.sliding_window == 0 || start + n <= c.max_seq);
   const int h0 = direct || c.sliding_window == 0 ? 0
                  : (start - c.sliding_window + 1 > 0 ? start - c.sliding_window + 1 : 0);
   const int hist = start - h0;
@@ -781,8 +783,9 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n,
     KV* kdst = direct ? kc : (KV*)S.KVlin_k;
     KV* vdst = direct ? vc : (KV*)S.KVlin_v;
     if (!direct && hist > 0) {
-      if (i8) launch_kv_gather_i8(c, kc, vc, h0, hist, (float*)kdst, (float*)vdst, s);
-      else k_kv_gather<KV><<<152, 256, 0, s>>>(kc, vc, c.max_seq, kd, h0, hist, kdst, vdst);
+      if (i8) launch_kv_gather_i8(c, L.kc, L.vc, m.paging, seq, h0, hist, (float*)kdst, (float*)vdst, s);
+      else k_kv_gather<KV><<<152, 256, 0, s>>>((const KV*)L.kc, (const KV*)L.vc, m.paging, seq, c.max_seq, kd, h0,
+                                               hist, kdst, vdst);
       count_launch(m);
     }
     {
@@ -817,12 +820,13 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n,
       // the cache holds.
       float* lk = (float*)kdst + (size_t)hist * kd;
       float* lv = (float*)vdst + (size_t)hist * kd;
-      launch_kv_quant(c, lk, lv, n, nullptr, start, t_first, kc, vc, lk, lv, s);
+      launch_kv_quant(c, lk, lv, n, nullptr, m.paging, seq, start, t_first, L.kc, L.vc, lk, lv, s);
       count_launch(m);
     }
     chk(attention<KV>(m, s, kdst, vdst, direct ? 0 : h0, start, n, a_q.out()));
     if (!direct && !i8) {
-      k_kv_commit<KV><<<152, 256, 0, s>>>(kdst, vdst, hist, start, t_first, n, c.max_seq, kd, kc, vc);
+      k_kv_commit<KV><<<152, 256, 0, s>>>(kdst, vdst, hist, start, t_first, n, c.max_seq, kd, (KV*)L.kc, (KV*)L.vc,
+                                          m.paging, seq);
       count_launch(m);
     }
     chk(oproj_rows<TW>(m, s, L, n, a_q));
@@ -895,12 +899,12 @@ static cudaError_t decode_rows(const Model& m, cudaStream_t s, int B, float* log
       if (c.qk_norm) qk_norm_rows(m, s, L, B, (float*)e.k_dst, e.kv_rows, 0, false, rope);
     }
     if (i8) {
-      launch_kv_quant(c, (const float*)S.KVlin_k, (const float*)S.KVlin_v, B, S.b_rows, 0, 0, L.kc, L.vc, nullptr,
-                      nullptr, s);
+      launch_kv_quant(c, (const float*)S.KVlin_k, (const float*)S.KVlin_v, B, S.b_rows, m.paging, 0, 0, 0, L.kc,
+                      L.vc, nullptr, nullptr, s);
       count_launch(m);
     }
     timer_begin(m, DEC_K_ATTN, s);
-    launch_attn_rows(c, S.Q, L.kc, L.vc, m.ring_bytes, S.b_seq, S.b_pos, B, nsplit, S.b_part, a_q.out(), s);
+    launch_attn_rows(c, S.Q, L.kc, L.vc, m.paging, S.b_seq, S.b_pos, B, nsplit, S.b_part, a_q.out(), s);
     timer_end(m, DEC_K_ATTN, s);
     count_launch(m, 2);
     chk(oproj_rows<TW>(m, s, L, B, a_q));

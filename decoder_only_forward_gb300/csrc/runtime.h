@@ -12,6 +12,23 @@
 
 namespace dec {
 
+// Where the K (or V) row of (sequence, slot) lives, in rows from a layer's K
+// (or V) base: contiguous rings (table == nullptr) keep each sequence's
+// ring_rows rows together; a paged cache (rml "The decoder", KV cache: pages of
+// `page` positions out of one arena) looks the slot's page up in the
+// sequence's page table, pages being stride_rows rows apart.
+struct KvPaging {
+  const int32_t* table;   // device [n_seqs][pages_per_seq] physical page ids, or nullptr
+  int pages_per_seq;
+  int page;               // slots per page
+  long long stride_rows;  // rows between consecutive pages of one layer's K: 2 * n_layers * page
+  int ring_rows;          // contiguous rings: rows per sequence
+};
+__host__ __device__ inline long long kv_phys_row(const KvPaging& pg, int seq, int slot) {
+  if (!pg.table) return (long long)seq * pg.ring_rows + slot;
+  return (long long)pg.table[seq * pg.pages_per_seq + slot / pg.page] * pg.stride_rows + slot % pg.page;
+}
+
 // Per-layer pointers as the persistent decode kernel reads them (device table).
 struct MkLayer {
   const float* attn_norm;
@@ -141,6 +158,7 @@ struct Model {
   int trace_cap;
   void* ws;             // workspace base
   size_t ws_bytes;
+  KvPaging paging;      // K/V row addressing (device page table when paged)
   int n_seqs;           // sequences whose KV rings the workspace holds
   int ring_rows;        // rows of one sequence's ring (max_seq rounded up to 64)
   size_t ring_bytes;    // bytes of one sequence's K (or V) ring of one layer
@@ -160,6 +178,8 @@ struct WsPlan {
   size_t kpart, kpart_bytes;            // split-K partials
   size_t Z;                             // sandwich block outputs
   size_t inv_freq_local, rope_tab_local;  // per-layer RoPE base
+  size_t page_table;                      // paged cache: [n_seqs][pages_per_seq] int32
+  int pages_per_seq;
   size_t qk_perm;                       // kHalf + QK-norm: permuted norm weights
   size_t kv;            // start of the KV rings: [layer][K, V][seq][ring_rows][n_kv*hd]
   size_t kv_layer_bytes; // one layer's K (or V) rings of every sequence
@@ -212,7 +232,8 @@ struct KvRowLayout {
 // Models whose decode runs the row kernels (one row per step): the persistent
 // step and the per-layer decode kernels implement none of these.
 inline bool decode_needs_rows(const dec_config& c) {
-  return c.kv_dtype == DEC_I8 || c.qk_norm != 0 || c.sandwich_norms != 0 || c.rope_theta_local > 0.f;
+  return c.kv_dtype == DEC_I8 || c.qk_norm != 0 || c.sandwich_norms != 0 || c.rope_theta_local > 0.f ||
+         c.page_size > 0;
 }
 // Whether layer l rotates with the global base (every layer without a local base).
 inline bool layer_rope_global(const dec_config& c, int l) {
@@ -231,15 +252,23 @@ inline KvRowLayout kv_row_layout(const dec_config& c) {
   const int sb = (kd / g * 4 + 15) / 16 * 16;
   return KvRowLayout{sb + (kd + 15) / 16 * 16, sb, g};
 }
-// f32 rows -> int8 ring rows (dst_rows[r], or the slot of position pos0 + r);
-// rows below t_first are not stored; rt_k/rt_v (nullable) get the values read
-// back.  planes: 2 = K and V, 1 = K only.
+// f32 rows -> int8 ring rows: row r to dst_rows[r] (rows from the layer base),
+// or to the row of (seq, slot of position pos0 + r) under pg; rows below t_first
+// are not stored; rt_k/rt_v (nullable) get the values read back.  planes: 2 =
+// K and V, 1 = K only.
 void launch_kv_quant(const dec_config& c, const float* src_k, const float* src_v, int n, const int32_t* dst_rows,
-                     int pos0, int t_first, void* ring_k, void* ring_v, float* rt_k, float* rt_v, cudaStream_t s,
-                     int planes = 2);
-// int8 ring rows of positions h0 .. h0+count-1 -> f32 rows.
-void launch_kv_gather_i8(const dec_config& c, const void* ring_k, const void* ring_v, int h0, int count,
-                         float* lin_k, float* lin_v, cudaStream_t s);
+                     const KvPaging& pg, int seq, int pos0, int t_first, void* ring_k, void* ring_v, float* rt_k,
+                     float* rt_v, cudaStream_t s, int planes = 2);
+// int8 rows of positions h0 .. h0+count-1 of sequence seq -> f32 rows.
+void launch_kv_gather_i8(const dec_config& c, const void* ring_k, const void* ring_v, const KvPaging& pg, int seq,
+                         int h0, int count, float* lin_k, float* lin_v, cudaStream_t s);
+// Paged cache: table[idx[i]] = val[i] for the n entries (at most 256 per launch).
+struct PageSet {
+  int n;
+  int32_t idx[256];
+  int32_t val[256];
+};
+void launch_set_pages(int32_t* table, const PageSet& ps, cudaStream_t s);
 
 // Persistent single-kernel decode step (decode_mk.cu).
 size_t mk_smem_bytes(const dec_config& c, int nsplit);
@@ -279,9 +308,9 @@ cudaError_t update_rows_setup_node(cudaGraphExec_t g, cudaGraphNode_t node, cons
 
 struct RowOut;
 // Batched decode attention (attn_rows.cu): rotated queries Q [B][nq*hd] f32,
-// the layer's ring sets kc/vc (sequence s at s * ring_bytes).
+// the layer's K/V bases kc/vc, rows addressed through pg.
 int attn_rows_splits(const dec_config& c);
-void launch_attn_rows(const dec_config& c, const float* Q, const void* kc, const void* vc, size_t ring_bytes,
+void launch_attn_rows(const dec_config& c, const float* Q, const void* kc, const void* vc, const KvPaging& pg,
                       const int32_t* seq, const int32_t* pos, int B, int nsplit, float* part, RowOut out,
                       cudaStream_t s);
 

@@ -31,7 +31,7 @@ EXPORTED = ["dec_config_validate", "dec_workspace_bytes", "dec_create", "dec_pre
             "dec_check", "dec_timing_enable", "dec_timing_read", "dec_launch_count", "dec_destroy",
             "dec_last_error", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc", "dec_gemm_bf16", "dec_set_graph", "dec_set_fused", "dec_fused_available", "dec_fused_mode", "dec_phase_stamps",
             "dec_prefill_seq", "dec_kv_reset_seq", "dec_length_seq", "dec_decode_batch", "dec_kv_layer_seq",
-            "dec_kv_quantize_int8"]
+            "dec_kv_quantize_int8", "dec_kv_slot", "dec_pages_free"]
 
 KERNEL_CLASSES = {"qkv": 1, "attn": 2, "oproj": 3, "gateup": 4, "down": 5, "lmhead": 6, "router": 7,
                   "pf_gemm": 8, "pf_attn": 9, "step": 10}
@@ -47,7 +47,8 @@ class Config(ctypes.Structure):
         ("rope_high_freq_factor", ctypes.c_float), ("rope_orig_ctx", ctypes.c_int32),
         ("rope_half", ctypes.c_int32), ("rope_dim", ctypes.c_int32), ("n_seqs", ctypes.c_int32),
         ("qk_norm", ctypes.c_int32), ("sandwich_norms", ctypes.c_int32),
-        ("rope_theta_local", ctypes.c_float), ("rope_global_every", ctypes.c_int32)]
+        ("rope_theta_local", ctypes.c_float), ("rope_global_every", ctypes.c_int32),
+        ("page_size", ctypes.c_int32), ("n_pages", ctypes.c_int32)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -98,6 +99,8 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "dec_decode_batch": (I32, [P, I32, ctypes.POINTER(I32), ctypes.POINTER(I32), P, P, P]),
         "dec_kv_layer_seq": (I32, [P, I32, I32, ctypes.POINTER(P), ctypes.POINTER(P)]),
         "dec_kv_quantize_int8": (I32, [P, I32, I32, I32, P, P]),
+        "dec_kv_slot": (I32, [P, I32, I32, I32, ctypes.POINTER(P), ctypes.POINTER(P)]),
+        "dec_pages_free": (I32, [P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -115,7 +118,8 @@ class DecError(RuntimeError):
         self.status = status
 
 
-def make_config(w: dict, kv_dtype: str = "f32", max_tokens: int = 0, n_seqs: int = 0) -> Config:
+def make_config(w: dict, kv_dtype: str = "f32", max_tokens: int = 0, n_seqs: int = 0, page_size: int = 0,
+                n_pages: int = 0) -> Config:
     c = Config()
     for k in ("n_layers", "hidden", "n_heads", "n_kv_heads", "head_dim", "ffn", "vocab",
               "n_experts", "n_experts_used", "max_seq", "sliding_window"):
@@ -141,6 +145,8 @@ def make_config(w: dict, kv_dtype: str = "f32", max_tokens: int = 0, n_seqs: int
     c.sandwich_norms = int(bool(w.get("sandwich_norms", False)))
     c.rope_theta_local = float(w.get("rope_theta_local", 0.0) or 0.0)
     c.rope_global_every = int(w.get("rope_global_every", 0) or 0)
+    c.page_size = int(page_size)
+    c.n_pages = int(n_pages)
     return c
 
 
@@ -296,11 +302,11 @@ class Decoder:
 
     def __init__(self, w: dict, weights: Optional[DeviceWeights] = None, device="cuda", seed: int = 1234,
                  kv_dtype: str = "f32", max_tokens: int = 0, stream: Optional[torch.cuda.Stream] = None,
-                 n_seqs: int = 0):
+                 n_seqs: int = 0, page_size: int = 0, n_pages: int = 0):
         self.w = w
         self.device = torch.device(device)
         self.weights = weights if weights is not None else DeviceWeights(w, device, seed)
-        self.cfg = make_config(w, kv_dtype, max_tokens, n_seqs)
+        self.cfg = make_config(w, kv_dtype, max_tokens, n_seqs, page_size, n_pages)
         st, msg = validate(self.cfg)
         if st != DEC_OK:
             raise DecError(st, msg)
@@ -411,6 +417,30 @@ class Decoder:
                 views.append(self.workspace[off:off + ms * nkv * hd * es].view(self.kv_torch_dtype)
                              .view(ms, nkv, hd))
         return views[0], views[1]
+
+    def kv_slot(self, layer: int, seq: int, slot: int):
+        """(K, V) rows of one slot (either layout): [n_kv_heads, head_dim] views, or uint8 rows of the
+        int8 format for an int8 cache."""
+        k, v = ctypes.c_void_p(), ctypes.c_void_p()
+        st = lib.dec_kv_slot(self.h, int(layer), int(seq), int(slot), ctypes.byref(k), ctypes.byref(v))
+        if st != DEC_OK:
+            raise DecError(st, f"no K/V row for layer {layer}, sequence {seq}, slot {slot}")
+        base = self.workspace.data_ptr()
+        nkv, hd = self.w["n_kv_heads"], self.w["head_dim"]
+        out = []
+        for p in (k.value, v.value):
+            off = p - base
+            if self.kv_dtype == "i8":
+                rb = kv_int8_row_layout(nkv, hd)[0]
+                out.append(self.workspace[off:off + rb].view(1, rb))
+            else:
+                es = 4 if self.kv_torch_dtype == torch.float32 else 2
+                out.append(self.workspace[off:off + nkv * hd * es].view(self.kv_torch_dtype).view(nkv, hd))
+        return out[0], out[1]
+
+    @property
+    def pages_free(self) -> int:
+        return int(lib.dec_pages_free(self.h))
 
     def set_trace(self, ids: Optional[torch.Tensor], logits: Optional[torch.Tensor], capacity: int) -> None:
         self._raise(lib.dec_set_trace(self.h, _ptr(ids), _ptr(logits), int(capacity)))

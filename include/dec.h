@@ -114,6 +114,16 @@ typedef struct dec_config {
                              rope_global_every-th layer, l with (l + 1) % rope_global_every == 0, with
                              rope_theta (0 = no global layer) */
   int32_t rope_global_every;
+  int32_t page_size;      /* 0: each sequence owns contiguous K/V rings of max_seq rows.  Else a paged cache
+                             (rml "The decoder", KV cache): slots are grouped in pages of page_size positions
+                             (a power of two >= 16); pages come from one arena of n_pages pages reserved up
+                             front, each holding its span for every layer (rows ordered page, layer, K/V,
+                             slot), and a sequence takes a page only when a position first lands in it, so
+                             memory follows the sequences' lengths rather than n_seqs * max_seq.  Pages are
+                             returned by dec_kv_reset / dec_kv_reset_seq.  A call that needs more pages than
+                             are free fails with DEC_ENOMEM before anything changes.  Decode of a paged cache
+                             runs the row kernels */
+  int32_t n_pages;        /* pages in the arena (with page_size > 0) */
 } dec_config;
 
 /*
@@ -231,8 +241,17 @@ dec_status dec_decode_batch(dec_handle *h, int32_t batch, const int32_t *seqs, c
  * position p lives in slot p % max_seq under a window, else slot p. */
 dec_status dec_kv_layer(const dec_handle *h, int32_t layer, void **k, void **v);
 
-/* The same for sequence seq in [0, n_seqs) (dec_kv_layer is sequence 0). */
+/* The same for sequence seq in [0, n_seqs) (dec_kv_layer is sequence 0).
+ * DEC_EINVAL for a paged cache (its rows are not contiguous: use dec_kv_slot). */
 dec_status dec_kv_layer_seq(const dec_handle *h, int32_t layer, int32_t seq, void **k, void **v);
+
+/* Device pointers to the K and V rows (n_kv_heads * head_dim elements of kv_dtype, or one
+ * DEC_I8 row) of slot `slot` of sequence seq in layer `layer`, for either layout.
+ * DEC_EINVAL for arguments out of range or a page the sequence does not hold. */
+dec_status dec_kv_slot(const dec_handle *h, int32_t layer, int32_t seq, int32_t slot, void **k, void **v);
+
+/* Paged cache: pages currently free in the arena (-1 for NULL or an unpaged cache). */
+int32_t dec_pages_free(const dec_handle *h);
 
 /* Optional MoE trace for testing: when d_ids/d_logits are non-NULL, every
  * later MoE layer records, for position p, its selected expert ids

@@ -143,3 +143,19 @@ def test_norm_variant_fields_checked(dec):
     assert dec.validate(c)[0] == dec.DEC_EINVAL
     c.qk_norm, c.sandwich_norms = 2, 2
     assert dec.validate(c)[0] == dec.DEC_EINVAL
+
+
+def test_paged_cache_config_and_arena_size(dec):
+    w = synthetic.workload("mistral-7b")
+    c = dec.make_config(w, "f32", n_seqs=64, page_size=16, n_pages=1024)
+    assert dec.validate(c)[0] == dec.DEC_OK
+    rb = w["n_kv_heads"] * w["head_dim"] * 4
+    arena = 1024 * 2 * w["n_layers"] * 16 * rb
+    rings = 64 * 2 * w["n_layers"] * w["max_seq"] * rb
+    # The arena replaces the per-sequence rings: 1024 pages of 16 positions instead of 64 x 4096.
+    flat = dec.workspace_bytes(dec.make_config(w, "f32", n_seqs=64))
+    assert dec.workspace_bytes(c) - (flat - rings) - arena < 64 * 256 * 4 * 2 + 4096
+    for ps, n_pages in ((8, 4), (24, 4), (16, 0)):
+        bad = dec.make_config(w, "f32", page_size=ps, n_pages=n_pages)
+        st, msg = dec.validate(bad)
+        assert st == dec.DEC_EINVAL and ("page" in msg)
