@@ -470,6 +470,9 @@ def run_profile(args):
         w["prompt"] = args.prompt
     if args.layers:
         w["n_layers"] = args.layers
+    if args.profile_batch:
+        run_profile_batched(args, w)
+        return
     d = dec.Decoder(w, kv_dtype=args.kv)
     d.set_graph(False)
     if args.fused != "auto":
@@ -483,6 +486,35 @@ def run_profile(args):
         d.decode_dev(tok, P + i, logits, tok)
     d.check()
     print(f"profile run: {args.workload} prefill {P} + decode {args.profile}, {d.launch_count} kernel launches")
+    d.close()
+
+
+def run_profile_batched(args, w):
+    """Batched decode for per-kernel profilers: args.profile_batch sequences prefilled with their own
+    prompts, two untimed steps, then args.profile steps inside the NVTX range "batched_steps" (a
+    profiler can keep to that range), kernels launched one by one."""
+    from decoder_only_forward_gb300 import dec
+    B, P, V = args.profile_batch, w["prompt"], w["vocab"]
+    ps = args.page_size
+    d = dec.Decoder(w, kv_dtype=args.kv, n_seqs=B, page_size=ps,
+                    n_pages=B * ((w["max_seq"] + ps - 1) // ps) if ps else 0)
+    d.set_graph(False)
+    lg = torch.empty(V, dtype=torch.float32, device="cuda")
+    for sq in range(B):
+        d.prefill(synthetic.prompt_tokens(w, P, seed=100 + sq), 0, lg, seq=sq)
+    seqs = list(range(B))
+    tok = torch.zeros(B, dtype=torch.int32, device="cuda")
+    out = torch.empty((B, V), dtype=torch.float32, device="cuda")
+    for i in range(2):
+        d.decode_batch(seqs, [P + i] * B, tok, out, tok)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("batched_steps")
+    for i in range(args.profile):
+        d.decode_batch(seqs, [P + 2 + i] * B, tok, out, tok)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    d.check()
+    print(f"profile run: {args.workload} batched decode of {B} sequences (prompt {P}), {args.profile} steps")
     d.close()
 
 
@@ -538,6 +570,8 @@ def main():
     ap.add_argument("--profile", type=int, default=0, metavar="D",
                     help="profiling driver: one prefill + D decode steps, kernels launched one by one "
                          "(no graph, no timing passes, no JSON); for per-kernel profilers")
+    ap.add_argument("--profile-batch", type=int, default=0, metavar="B",
+                    help="with --profile D: D batched decode steps of B sequences instead")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
