@@ -117,8 +117,18 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float* __restrict__ 
   __shared__ float red[33];
   const int t = blockIdx.x;
   const float* x = X + (size_t)t * h;
+  // 16-byte loads and 4-wide stores when the rows allow it (few rows: latency-bound).
+  const bool vec = (h & 3) == 0 && ((reinterpret_cast<uintptr_t>(w) & 15) == 0);
   float ss = 0.f;
-  for (int i = threadIdx.x; i < h; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
+  if (vec) {
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    for (int i = threadIdx.x; i < h / 4; i += blockDim.x) {
+      const float4 v = x4[i];
+      ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+    }
+  } else {
+    for (int i = threadIdx.x; i < h; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
+  }
   ss = warp_sum(ss);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) red[warp] = ss;
@@ -130,7 +140,17 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float* __restrict__ 
   }
   __syncthreads();
   const float inv = 1.0f / sqrtf(red[32] / (float)h + eps);
-  for (int i = threadIdx.x; i < h; i += blockDim.x) row_store(out, (size_t)t * h + i, x[i] * inv * w[i]);
+  if (vec) {
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+    for (int i = threadIdx.x; i < h / 4; i += blockDim.x) {
+      const float4 v = x4[i], g = w4[i];
+      row_store4(out, (size_t)t * h + 4 * i,
+                 make_float4(v.x * inv * g.x, v.y * inv * g.y, v.z * inv * g.z, v.w * inv * g.w));
+    }
+  } else {
+    for (int i = threadIdx.x; i < h; i += blockDim.x) row_store(out, (size_t)t * h + i, x[i] * inv * w[i]);
+  }
 }
 
 // ---------------------------------------------------------------------------
