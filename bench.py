@@ -35,6 +35,21 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
+def max_over_ranks(values, device, world: int) -> list:
+    """Each timing taken as the slowest rank's (replicas run in parallel; the job ends with the last)."""
+    if world <= 1:
+        return list(values)
+    t = torch.tensor(list(values), device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def replica_value(n_ranks: int, tokens_per_step: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank processes tokens_per_step per step; the step takes the
+    slowest rank's time."""
+    return n_ranks * tokens_per_step / (ms_per_step / 1e3)
+
+
 def workload_of(args) -> dict:
     """The named workload, with the architecture variant flags applied."""
     kw = {}
@@ -291,12 +306,7 @@ def run_ours(args, rank, world, local_rank):
     pre_ms = [e[0].elapsed_time(e[1]) for e in events]
     dec_ms = [e[1].elapsed_time(e[2]) for e in events]
     tot_ms = sum(p + q for p, q in zip(pre_ms, dec_ms))
-    if world > 1:
-        t = torch.tensor([tot_ms, sum(pre_ms), sum(dec_ms)], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        tot_ms, pre_sum, dec_sum = t.tolist()
-    else:
-        pre_sum, dec_sum = sum(pre_ms), sum(dec_ms)
+    tot_ms, pre_sum, dec_sum = max_over_ranks([tot_ms, sum(pre_ms), sum(dec_ms)], dev, world)
     ms_per_step = tot_ms / args.steps
     pre_s, dec_s = pre_sum / args.steps / 1e3, dec_sum / args.steps / 1e3
 
@@ -364,7 +374,7 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0:
         n, k_steps = world, args.steps
         tokens_per_step = P + D
-        value = n * tokens_per_step / (ms_per_step / 1e3)
+        value = replica_value(n, tokens_per_step, ms_per_step)
         cpu = None
         if not args.no_cpu_baseline:
             npf, ndc = oracle_sample_size(w)
