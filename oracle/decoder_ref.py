@@ -47,6 +47,13 @@ Tradeoffs, optional weight roles):
     the expert sum) is RMS-normalised with its post norm weight before it is
     added to the residual.
 
+Optional 8-bit projection weights (PAN "Llama Forward Pass", weight modes: the
+projection matrices Wq, Wk, Wv, Wo, W_gate, W_up, W_down and an untied W_output
+stay quantised, expanded a block at a time; embeddings and norms stay f32): each
+weight row is stored in groups of 32 input columns by the same rule the pages
+print for the int8 cache, round(w / s) with s = max|w| / 127 in float32, and the
+forward pass uses float32(code * s).  The router stays unquantised (not listed).
+
 Optional int8 K/V cache (RML "The decoder", KV cache): every cached key and
 value row is stored as groups of G channels (G the largest power of two that
 divides head_dim, at most 32, so a group never spans two heads), each group as
@@ -136,6 +143,8 @@ class OracleConfig:
     # Sandwich norms (RML One forward pass step 6): post-attention / post-FFN RMSNorm of
     # each block's output before the residual add (weights post_attn_norm, post_ffn_norm).
     sandwich_norms: bool = False
+    # 8-bit projection weights (PAN weight modes; groups of 32 input columns, see module notes).
+    weight_int8: bool = False
     # Per-layer RoPE base (SIP RoPE, Gemma 3): 0 = one base for every layer; else local
     # layers use rope_theta_local and every rope_global_every-th layer the global base.
     rope_theta_local: float = 0.0
@@ -437,6 +446,70 @@ class Trace:
     hidden: dict = field(default_factory=dict)          # (l, pos) -> [h], after layer l
 
 
+WEIGHT_GROUP = 32   # input columns per scale of an 8-bit weight row
+_PROJECTIONS = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")
+
+
+def weight_int8_roundtrip(mat) -> np.ndarray:
+    """A weight matrix [out, in] as its 8-bit storage gives it back: each row in groups of
+    WEIGHT_GROUP input columns (in must be a multiple of it)."""
+    m = np.asarray(mat, F64)
+    if m.shape[-1] % WEIGHT_GROUP:
+        raise ValueError(f"input width {m.shape[-1]} is not a multiple of {WEIGHT_GROUP}")
+    out = np.empty_like(m)
+    for r in range(m.shape[0]):
+        codes, scales = quantize_int8_groups(m[r], WEIGHT_GROUP)
+        out[r] = dequantize_int8_groups(codes, scales, WEIGHT_GROUP)
+    return out
+
+
+def _is_tied(weights) -> bool:
+    """Whether a weight source's head is its embedding (same array, or the source says so)."""
+    cfg = getattr(weights, "cfg", None)
+    if isinstance(cfg, dict) and "tied" in cfg:
+        return bool(cfg["tied"])
+    return getattr(weights, "_lm_head", None) is None and hasattr(weights, "_embd")
+
+
+class Int8ProjectionWeights:
+    """A weight source whose projection matrices (and untied LM head) read back through
+    8-bit storage; embeddings, norms, biases and the router pass through unchanged."""
+
+    def __init__(self, inner, tied: bool):
+        self.inner = inner
+        self.tied = tied
+        self._memo = {}
+
+    def embed_rows(self, tokens):
+        return self.inner.embed_rows(tokens)
+
+    def out_norm(self):
+        return self.inner.out_norm()
+
+    def lm_head(self):
+        if self.tied:
+            return self.inner.lm_head()
+        if "head" not in self._memo:
+            self._memo["head"] = weight_int8_roundtrip(self.inner.lm_head())
+        return self._memo["head"]
+
+    def layer(self, l: int) -> dict:
+        key = ("layer", l)
+        if key not in self._memo:
+            lw = dict(self.inner.layer(l))
+            for r in _PROJECTIONS:
+                if lw.get(r) is not None:
+                    lw[r] = weight_int8_roundtrip(lw[r])
+            self._memo[key] = lw
+        return self._memo[key]
+
+    def expert(self, l: int, e: int):
+        key = ("expert", l, e)
+        if key not in self._memo:
+            self._memo[key] = tuple(weight_int8_roundtrip(m) for m in self.inner.expert(l, e))
+        return self._memo[key]
+
+
 class Session:
     """One sequence: a per-layer K/V list indexed by absolute position, plus the forward pass.
 
@@ -446,7 +519,8 @@ class Session:
 
     def __init__(self, cfg: OracleConfig, weights, trace: bool = False, trace_hidden: bool = False):
         self.cfg = cfg
-        self.w = weights
+        self.w = Int8ProjectionWeights(weights, getattr(weights, "tied", False) or
+                                       _is_tied(weights)) if cfg.weight_int8 else weights
         self.inv_freq = rope_inv_freq(cfg.head_dim, cfg.rope_theta, cfg.rope_llama3, cfg.rope_dim)
         self.inv_freq_local = (rope_inv_freq(cfg.head_dim, cfg.rope_theta_local, None, cfg.rope_dim)
                                if cfg.rope_theta_local else self.inv_freq)
