@@ -17,6 +17,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -126,7 +127,7 @@ def kv_bytes_per_element(w: dict, kv: str) -> float:
 
 
 def decode_bytes(w: dict, pos: int, kv_es: float) -> float:
-    """Weights + KV read by one decode step at absolute position pos (SURVEY-style roofline bytes)."""
+    """Weights + KV read by one decode step at absolute position pos (the decode roofline's bytes)."""
     b = weight_bytes(w)
     per_layer = b["qkv"] + b["oproj"] + b["gateup"] + b["down"] + b["router"] + 2 * 4 * w["hidden"]
     m = min(pos + 1, w["max_seq"]) if w["sliding_window"] > 0 else pos + 1
@@ -163,7 +164,9 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # nvidia-smi samples of this run; DEC_CLOCKS_DIR keeps them somewhere chosen.
+        out_dir = os.environ.get("DEC_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"clocks_bench_{os.getpid()}.csv")
 
     def __enter__(self):
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
