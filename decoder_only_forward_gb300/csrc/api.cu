@@ -8,6 +8,7 @@
 #include <string>
 #include <vector>
 
+#include "paging.h"
 #include "runtime.h"
 
 using namespace dec;
@@ -18,9 +19,7 @@ struct dec_handle {
   cudaStream_t stream;
   std::vector<int32_t> lens;   // positions held per sequence (host bookkeeping)
   RowsMeta meta;        // rows of the current batched decode step
-  // paged cache: host copy of the page table and the free pages
-  std::vector<int32_t> pages;       // [n_seqs][pages_per_seq], -1 = none
-  std::vector<int32_t> free_pages;  // a stack
+  PageAllocator pages;  // paged cache: host copy of the page table and the free pages
   PageSet pset;
   std::string err;
   // decode graph, captured for one (logits, d_argmax) pair
@@ -339,9 +338,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
   h->stream = (cudaStream_t)cuda_stream;
   h->lens.assign(p.n_seqs, 0);
   if (cfg->page_size > 0) {
-    h->pages.assign((size_t)p.n_seqs * p.pages_per_seq, -1);
-    h->free_pages.resize(cfg->n_pages);
-    for (int i = 0; i < cfg->n_pages; ++i) h->free_pages[i] = cfg->n_pages - 1 - i;   // page 0 on top
+    h->pages.init(p.n_seqs, cfg->max_seq, cfg->page_size, cfg->n_pages, cfg->sliding_window > 0);
   }
   Model& m = h->m;
   m.cfg = *cfg;
@@ -557,34 +554,15 @@ static dec_status check_positions(dec_handle* h, int32_t seq, int32_t n, int32_t
   return DEC_OK;
 }
 
-// Paged cache: the pages that writing positions [p0, p0 + n) of seq needs and
-// does not hold yet, taken from the free stack (all or none: DEC_ENOMEM leaves
-// everything as it was), then written into the device table on the stream.
+// Paged cache: the pages that writing positions [p0, p0 + n) of each sequence
+// needs and does not hold yet, all or none (DEC_ENOMEM leaves everything as it
+// was), then written into the device table on the stream.
 static dec_status reserve_pages(dec_handle* h, const int32_t* seqs, const int32_t* p0s, int count, int32_t n) {
   const dec_config& c = h->m.cfg;
   if (c.page_size <= 0) return DEC_OK;
-  const int pps = h->m.paging.pages_per_seq, P = c.page_size;
   std::vector<std::pair<int, int>> taken;   // (table index, page)
-  for (int i = 0; i < count; ++i) {
-    const int32_t span = n < c.max_seq ? n : c.max_seq;   // under a window the slots of n > max_seq repeat
-    for (int32_t t = 0; t < span; ++t) {
-      const int32_t p = p0s[i] + t;
-      const int32_t slot = c.sliding_window > 0 ? p % c.max_seq : p;
-      const int idx = seqs[i] * pps + slot / P;
-      if (h->pages[idx] >= 0) continue;
-      if (h->free_pages.empty()) {
-        for (auto& tp : taken) {
-          h->free_pages.push_back(tp.second);
-          h->pages[tp.first] = -1;
-        }
-        return fail(h, DEC_ENOMEM, "paged cache: all %d pages are in use", c.n_pages);
-      }
-      const int pg = h->free_pages.back();
-      h->free_pages.pop_back();
-      h->pages[idx] = pg;
-      taken.emplace_back(idx, pg);
-    }
-  }
+  if (!h->pages.reserve(seqs, p0s, count, n, taken))
+    return fail(h, DEC_ENOMEM, "paged cache: all %d pages are in use", c.n_pages);
   PageSet& ps = h->pset;
   for (size_t i = 0; i < taken.size(); i += 256) {
     ps.n = (int)std::min<size_t>(256, taken.size() - i);
@@ -598,13 +576,7 @@ static dec_status reserve_pages(dec_handle* h, const int32_t* seqs, const int32_
 }
 
 static void release_pages(dec_handle* h, int32_t seq) {
-  if (h->m.cfg.page_size <= 0) return;
-  const int pps = h->m.paging.pages_per_seq;
-  for (int i = 0; i < pps; ++i) {
-    int32_t& e = h->pages[(size_t)seq * pps + i];
-    if (e >= 0) h->free_pages.push_back(e);
-    e = -1;
-  }
+  if (h->m.cfg.page_size > 0) h->pages.release(seq);
 }
 
 dec_status dec_prefill_seq(dec_handle* h, int32_t seq, const int32_t* tokens, int32_t n, int32_t start_pos,
@@ -766,7 +738,7 @@ dec_status dec_kv_reset_seq(dec_handle* h, int32_t seq) {
 
 int32_t dec_pages_free(const dec_handle* h) {
   if (!h || h->m.cfg.page_size <= 0) return -1;
-  return (int32_t)h->free_pages.size();
+  return (int32_t)h->pages.free_count();
 }
 
 dec_status dec_kv_slot(const dec_handle* h, int32_t layer, int32_t seq, int32_t slot, void** k, void** v) {
@@ -776,7 +748,7 @@ dec_status dec_kv_slot(const dec_handle* h, int32_t layer, int32_t seq, int32_t 
   const KvPaging& pg = h->m.paging;
   long long row;
   if (h->m.cfg.page_size > 0) {
-    const int32_t page = h->pages[(size_t)seq * pg.pages_per_seq + slot / pg.page];
+    const int32_t page = h->pages.page_of(seq, slot);
     if (page < 0) return DEC_EINVAL;
     row = page * pg.stride_rows + slot % pg.page;
   } else {
@@ -810,8 +782,7 @@ static dec_status run_rows(dec_handle* h, int32_t batch, const int32_t* seqs, co
     meta.pos[i] = p;
     if (c.page_size > 0) {
       const KvPaging& pg = h->m.paging;
-      meta.rows[i] = (int32_t)(h->pages[(size_t)seqs[i] * pg.pages_per_seq + slot / pg.page] * pg.stride_rows +
-                               slot % pg.page);
+      meta.rows[i] = (int32_t)(h->pages.page_of(seqs[i], slot) * pg.stride_rows + slot % pg.page);
     } else {
       meta.rows[i] = seqs[i] * h->m.ring_rows + slot;
     }
