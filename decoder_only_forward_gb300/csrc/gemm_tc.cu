@@ -24,6 +24,7 @@
 
 #include <mutex>
 
+#include "ksplit.h"
 #include "prefill_common.cuh"
 #include "tc.cuh"
 
@@ -319,33 +320,6 @@ static int num_sms() {
   return n > 0 ? n : 1;
 }
 
-// K splits for a GEMM whose tiles alone would leave SMs idle: the count that
-// minimises (waves of units) x (K-blocks per unit) x (time of one weight
-// K-block at an SM's share of HBM), plus the partial sums' round trip for
-// s > 1, within the partial buffer.  rows: the rows the partial buffer holds
-// per split.  A function of the GEMM's shape and the GPU only: for the same
-// weights and tile rows every call takes the same split (and rounding).
-static int pick_ksplit(long long tiles, int kblocks, int BN, long long rows, int N, size_t cap_bytes, int sms) {
-  const double bw = 6.0e12;                                    // bytes/s, a round HBM copy rate
-  const double t_kb = (double)BN * TC_BK * 2.0 / (bw / sms);    // one weight K-block on one SM
-  double best_t = 0.0;
-  int best = 1;
-  for (int s = 1; s <= 16 && s <= kblocks; ++s) {
-    const int kb_per = (kblocks + s - 1) / s;
-    if ((kblocks + kb_per - 1) / kb_per != s) continue;         // a split would be empty
-    const double part_bytes = (double)s * rows * N * 4.0;
-    if (s > 1 && part_bytes > (double)cap_bytes) break;
-    const long long units = tiles * s;
-    double t = (double)((units + sms - 1) / sms) * kb_per * t_kb;
-    if (s > 1) t += 2.0 * part_bytes / bw + 3e-6;               // partials out and back, one more launch
-    if (s == 1 || t < 0.97 * best_t) {
-      best_t = t;
-      best = s;
-    }
-  }
-  return best;
-}
-
 template <int BN, bool SPLIT>
 static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& al, const CUtensorMap& b, int M, int N, int K,
                              const GemmEpi& e, int groups, int max_rows, float* kpart, size_t kpart_bytes,
@@ -359,7 +333,7 @@ static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& al, const 
   const int kblocks = (K + TC_BK - 1) / TC_BK;
   // Grouped GEMMs keep all M rows per split; plain ones a whole number of row tiles.
   const long long rows = groups > 1 ? (long long)M : (long long)m_tiles * TC_BM;
-  const int ksplit = kpart ? pick_ksplit(tiles, kblocks, BN, rows, N, kpart_bytes, sms) : 1;
+  const int ksplit = kpart ? pick_ksplit(tiles, kblocks, BN, TC_BK, rows, N, kpart_bytes, sms) : 1;
   const long long total = tiles * ksplit;
   const int grid = (int)(total < sms ? total : sms);
   kern<<<grid, TC_THREADS, C::SMEM, s>>>(a, al, b, M, N, K, e, groups, m_tiles, ksplit, kpart, st);
