@@ -159,3 +159,16 @@ def test_paged_cache_config_and_arena_size(dec):
         bad = dec.make_config(w, "f32", page_size=ps, n_pages=n_pages)
         st, msg = dec.validate(bad)
         assert st == dec.DEC_EINVAL and ("page" in msg)
+
+
+def test_weight_structs_match_header(dec):
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct dec_layer_weights \{(.*?)\} dec_layer_weights;", text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = re.findall(r"\*\s*([a-z_0-9]+)", body)
+    assert names == [n for n, _ in dec.LayerWeights._fields_]
+    assert ctypes.sizeof(dec.LayerWeights) == 8 * len(names)
+    body = re.search(r"typedef struct dec_weights \{(.*?)\} dec_weights;", text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = re.findall(r"\*\s*([a-z_0-9]+)\s*;", body)
+    assert names == [n for n, _ in dec.Weights._fields_]
