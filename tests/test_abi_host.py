@@ -172,3 +172,16 @@ def test_weight_structs_match_header(dec):
     body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
     names = re.findall(r"\*\s*([a-z_0-9]+)\s*;", body)
     assert names == [n for n, _ in dec.Weights._fields_]
+
+
+def test_header_is_plain_c(tmp_path):
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use.c"
+    src.write_text('#include "dec.h"\nint main(void) { dec_config c = {0}; return (int)dec_workspace_bytes(&c); }\n')
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-I", os.path.join(ROOT, "include"),
+                        str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
