@@ -5,7 +5,11 @@ decode steps, through libdec.so.  ``--impl reference`` times the float64 CPU
 oracle on the host cores instead (the baseline arm).  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload smollm2-135m] [--kv f32|bf16]
+                  [--workload mixtral-8x7b] [--per-workload auto|none|a,b] [--kv f32|bf16|i8]
+
+The main line measures one workload (default Mixtral-8x7B, the largest single-GPU
+configuration); ``per_workload`` repeats the measurement, with fewer steps, for the
+other named workloads in the same run.
 """
 
 from __future__ import annotations
@@ -87,19 +91,16 @@ def weight_bytes(w: dict) -> dict:
     }
 
 
-# DRAM bytes per launch of a roofline kernel, from one ncu capture each (the
-# summaries under profiles/ give the commands).  A figure holds only for the
+# DRAM bytes per launch of a roofline kernel, from one ncu capture each.  A figure holds only for the
 # kernel source it measured: the source file's SHA-256 at capture time must
 # match the current file, else the bench reports traffic as null.
 TRAFFIC = {
     ("smollm2-135m", "down"): {
         "bytes": 1814336, "source": "decoder_only_forward_gb300/csrc/decode.cu",
-        "sha256": "3d7213fecd5001252701110382d8e9dfd57676011ecc1ded9bf6666198c7ae34",
-        "profile": "profiles/gemv_down_smollm2-135m_traffic.md"},
+        "sha256": "3d7213fecd5001252701110382d8e9dfd57676011ecc1ded9bf6666198c7ae34"},
     ("mistral-7b", "step"): {
         "bytes": 15712395008, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
-        "sha256": "4bf7258819f5eaeff409afa95ceaa4deb2af4270224b2c6b5de9309906a0eb17",
-        "profile": "profiles/decode_step_traffic_mistral-7b.md"},
+        "sha256": "4bf7258819f5eaeff409afa95ceaa4deb2af4270224b2c6b5de9309906a0eb17"},
 }
 
 
@@ -212,94 +213,144 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle
-def oracle_sample(w: dict, n_prefill: int, n_decode: int, device: str):
-    """Times the float64 oracle on a bounded sample: batched single-pass prefill of
-    n_prefill tokens + n_decode per-token forwards.  Returns (tok/s, seconds, cores)."""
+class _TimedSource:
+    """Wraps a weight source and adds up the seconds spent drawing weights, so that the
+    oracle's own arithmetic can be timed apart from input generation."""
+
+    def __init__(self, inner):
+        self.inner = inner
+        self.cfg = inner.cfg
+        self.fetch_s = 0.0
+
+    def _t(self, fn, *a):
+        t0 = time.perf_counter()
+        try:
+            return fn(*a)
+        finally:
+            self.fetch_s += time.perf_counter() - t0
+
+    def embed_rows(self, tokens):
+        return self._t(self.inner.embed_rows, tokens)
+
+    def out_norm(self):
+        return self._t(self.inner.out_norm)
+
+    def lm_head(self):
+        return self._t(self.inner.lm_head)
+
+    def layer(self, l):
+        return self._t(self.inner.layer, l)
+
+    def expert(self, l, e):
+        return self._t(self.inner.expert, l, e)
+
+
+def oracle_sample_plan(w: dict) -> dict:
+    """The bounded sample of a workload the float64 oracle is timed on: its first
+    ``layers`` layers, a batched single-pass prefill of ``prefill`` prompt tokens, then
+    ``decode`` per-token forwards; the time is scaled to the whole model by
+    n_layers / layers (the head's share is scaled with it, which overstates the
+    oracle's time by a few percent at most)."""
+    if w["n_experts"]:
+        return dict(layers=1, prefill=128, decode=2)
+    if w["hidden"] >= 2048:
+        return dict(layers=2, prefill=128, decode=2)
+    return dict(layers=w["n_layers"], prefill=64, decode=2)
+
+
+def oracle_sample(w: dict, plan: dict, device: str, src=None):
+    """Times the float64 oracle on the bounded sample ``plan`` of workload ``w``.
+
+    Weights are drawn once (on ``device``) and kept as float64 for the sampled layers;
+    time spent drawing is excluded.  Returns (tok/s scaled to the whole model,
+    seconds of oracle arithmetic, cores, the weight source for reuse)."""
     from oracle import OracleConfig, Session
     cores = len(os.sched_getaffinity(0))
     torch.set_num_threads(cores)
-    src = synthetic.OracleWeightSource(w, device=device, cache=True)
-    sess = Session(OracleConfig.from_dict(w), src)
-    toks = synthetic.prompt_tokens(w, n_prefill + n_decode, seed=0)
-    # Warm the float64 weight copies (drawing them is input generation, not the oracle).
-    for l in range(w["n_layers"]):
-        src.layer(l)
-        if w["n_experts"]:
-            for e in range(w["n_experts"]):
-                src.expert(l, e)
-    src.lm_head()
-    src.out_norm()
+    ws = dict(w, n_layers=plan["layers"])
+    if src is None:
+        src = synthetic.OracleWeightSource(ws, device=device, cache=True)
+    timed = _TimedSource(src)
+    sess = Session(OracleConfig.from_dict(ws), timed)
+    n_pf, n_dc = plan["prefill"], plan["decode"]
+    toks = synthetic.prompt_tokens(w, n_pf + n_dc, seed=0)
     t0 = time.perf_counter()
-    sess.prefill_batched(list(toks[:n_prefill]), 0)
-    for i in range(n_decode):
-        sess.forward(int(toks[n_prefill + i]), n_prefill + i)
-    dt = time.perf_counter() - t0
-    return (n_prefill + n_decode) / dt, dt, cores
+    sess.prefill_batched(list(toks[:n_pf]), 0)
+    for i in range(n_dc):
+        sess.forward(int(toks[n_pf + i]), n_pf + i)
+    dt = time.perf_counter() - t0 - timed.fetch_s
+    scaled = dt * w["n_layers"] / plan["layers"]
+    return (n_pf + n_dc) / scaled, dt, cores, src
 
 
-def oracle_sample_size(w: dict):
-    big = w["hidden"] >= 2048
-    return (8, 1) if big else (48, 2)
+def oracle_sample_text(name: str, w: dict, plan: dict, cores: int) -> str:
+    what = (f"the first {plan['layers']} of {w['n_layers']} layers" if plan["layers"] < w["n_layers"]
+            else f"all {w['n_layers']} layers")
+    experts = f" (each with all {w['n_experts']} experts)" if w["n_experts"] else ""
+    return (f"float64 oracle on {cores} host cores: {what}{experts} of the {name}-shaped model, batched "
+            f"single-pass prefill of {plan['prefill']} prompt tokens + {plan['decode']} per-token forwards; "
+            f"weights drawn beforehand (not timed); time scaled by {w['n_layers']}/{plan['layers']} layers")
 
 
 # ---------------------------------------------------------------- our arm
-def run_ours(args, rank, world, local_rank):
-    from decoder_only_forward_gb300 import build as dec_build
-    if rank == 0:
-        dec_build.build()
-    if world > 1:
-        torch.distributed.barrier()
-    dec_build.build()
-    from decoder_only_forward_gb300 import dec
+PER_WORKLOAD_DEFAULT = ["smollm2-135m", "qwen2.5-0.5b", "mistral-7b", "mixtral-8x7b"]
 
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    w = workload_of(args)
-    P, D = w["prompt"], w["decode"]
+
+def gemm_flops(w: dict, P: int) -> float:
+    """Algorithmic FLOPs of the prefill projection GEMMs (QKV, O, gate/up, down; MoE: the
+    k selected experts per row): 2 * rows * active linear parameters."""
+    h, f, hd = w["hidden"], w["ffn"], w["head_dim"]
+    qd, kd = w["n_heads"] * hd, w["n_kv_heads"] * hd
+    k = w["n_experts_used"] if w["n_experts"] else 1
+    return w["n_layers"] * 2.0 * P * ((qd + 2 * kd) * h + h * qd + k * 3 * f * h)
+
+
+def measure_workload(name, w, dev, args, steps, warmup, weights=None, want_e2e_steps=3,
+                     attribution=True, world=1):
+    """One workload: W untimed steps, then K timed steps of (kv reset, prefill of P tokens,
+    D greedy decode steps), L2 flushed before each; then an end-to-end pass through the
+    API with host buffers, and (optional) attribution passes after the timed region."""
+    from decoder_only_forward_gb300 import dec
+    P, D, V = w["prompt"], w["decode"], w["vocab"]
     kv_es = kv_bytes_per_element(w, args.kv)
-    d = dec.Decoder(w, device=dev, kv_dtype=args.kv)
+    d = dec.Decoder(w, weights=weights, device=dev, kv_dtype=args.kv)
     if args.fused != "auto":
         d.set_fused(args.fused)
     s = d.stream
     prompt_np = synthetic.prompt_tokens(w, P, seed=0)
     prompt_pinned = torch.from_numpy(prompt_np).pin_memory()
-    V = w["vocab"]
     logits = torch.empty(V, dtype=torch.float32, device=dev)
     tok = torch.empty(1, dtype=torch.int32, device=dev)
     flush = torch.empty(max(2 * L2_BYTES, 256 * 2**20) // 4, dtype=torch.float32, device=dev)
 
-    def step():
+    def step(evs=None):
+        if evs is not None:
+            with torch.cuda.stream(s):
+                flush.zero_()
+            evs[0].record(s)
         d.kv_reset()  # each step is a new sequence
         d.prefill(prompt_np, 0, logits, tok)
+        if evs is not None:
+            evs[1].record(s)
         for i in range(D):
             d.decode_dev(tok, P + i, logits, tok)
+        if evs is not None:
+            evs[2].record(s)
 
-    def timed_step(evs):
-        with torch.cuda.stream(s):
-            flush.zero_()
-        evs[0].record(s)
-        d.kv_reset()  # each step is a new sequence
-        d.prefill(prompt_np, 0, logits, tok)
-        evs[1].record(s)
-        for i in range(D):
-            d.decode_dev(tok, P + i, logits, tok)
-        evs[2].record(s)
-
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     d.check()
     torch.cuda.synchronize(dev)
 
-    # ---- timed region (device clocks) ----
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     launches0 = d.launch_count
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(local_rank) as clk:
+    with ClockSampler(dev.index or 0) as clk:
         wall0 = time.perf_counter()
-        for k in range(args.steps):
-            timed_step(events[k])
+        for k in range(steps):
+            step(events[k])
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - wall0
     if world > 1:
@@ -310,114 +361,215 @@ def run_ours(args, rank, world, local_rank):
     dec_ms = [e[1].elapsed_time(e[2]) for e in events]
     tot_ms = sum(p + q for p, q in zip(pre_ms, dec_ms))
     tot_ms, pre_sum, dec_sum = max_over_ranks([tot_ms, sum(pre_ms), sum(dec_ms)], dev, world)
-    ms_per_step = tot_ms / args.steps
-    pre_s, dec_s = pre_sum / args.steps / 1e3, dec_sum / args.steps / 1e3
-
-    hbm, tf, tf_sus, peak_kind = peaks()
-    dbytes = sum(decode_bytes(w, P + i, kv_es) for i in range(D))
-    pflops = prefill_flops(w, P)
+    r = dict(d=d, P=P, D=D, V=V, kv_es=kv_es, steps=steps, warmup=warmup,
+             ms_per_step=tot_ms / steps, pre_s=pre_sum / steps / 1e3, dec_s=dec_sum / steps / 1e3,
+             launches=launches, wall=wall, clocks=clk.summary(), schedule=d.fused_mode(),
+             weights_gb=d.weights.nbytes() / 1e9)
+    r["dbytes"] = sum(decode_bytes(w, P + i, kv_es) for i in range(D))
+    r["pflops"] = prefill_flops(w, P)
 
     # ---- end to end through the public API with host buffers ----
-    tok_host = torch.empty(1, dtype=torch.int32).pin_memory()
-    logits_host = torch.empty(V, dtype=torch.float32).pin_memory()
-    e2e_steps = max(1, min(args.steps, 3))
-    torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        d.kv_reset()
-        d.prefill(prompt_pinned, 0, logits, tok)
-        for i in range(D):
-            d.decode_dev(tok, P + i, logits, tok)
+    if want_e2e_steps:
+        tok_host = torch.empty(1, dtype=torch.int32).pin_memory()
+        logits_host = torch.empty(V, dtype=torch.float32).pin_memory()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(want_e2e_steps):
+            d.kv_reset()
+            d.prefill(prompt_pinned, 0, logits, tok)
+            for i in range(D):
+                d.decode_dev(tok, P + i, logits, tok)
+                with torch.cuda.stream(s):
+                    tok_host.copy_(tok, non_blocking=True)
+                s.synchronize()
             with torch.cuda.stream(s):
-                tok_host.copy_(tok, non_blocking=True)
+                logits_host.copy_(logits, non_blocking=True)
             s.synchronize()
-        with torch.cuda.stream(s):
-            logits_host.copy_(logits, non_blocking=True)
-        s.synchronize()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
+        r["e2e_s"] = (time.perf_counter() - t0) / want_e2e_steps
 
-    # ---- attribution: which kernel class dominates, and its roofline ----
-    classes = ["step", "gateup", "down", "qkv", "oproj", "attn", "lmhead", "router"]
-    per_class = {}
-    for c in classes:
-        d.timing_enable(c, 20000)
-        d.kv_reset()  # each step is a new sequence
-        d.prefill(prompt_np, 0, logits, tok)
-        ms_pf, n_pf = d.timing_read()
-        ms_dc, n_dc = 0.0, 0
-        for i in range(D):
-            d.decode_dev(tok, P + i, logits, tok)
-            a, b = d.timing_read()
-            ms_dc += a
-            n_dc += b
-        per_class[c] = dict(prefill_ms=ms_pf, prefill_launches=n_pf, decode_ms=ms_dc, decode_launches=n_dc)
-    d.timing_enable("gateup", 0)
-    dom = max(classes, key=lambda c: per_class[c]["prefill_ms"] + per_class[c]["decode_ms"])
-    pc = per_class[dom]
-    nl = pc["decode_launches"] + pc["prefill_launches"]
-    wb = weight_bytes(w)
-    if dom == "step":
-        # The whole decode step is one kernel: its bytes are the step's weights + KV.
-        per_launch_bytes = dbytes / D
-    elif dom == "attn":
-        per_launch_bytes = sum(2 * w["n_kv_heads"] * w["head_dim"] * kv_es *
-                               (min(p + 1, w["max_seq"]) if w["sliding_window"] else p + 1)
-                               for p in range(P + D)) / (P + D)
+    if attribution:
+        # Prefill: each tensor-core kernel class timed alone in its own prefill (event pairs
+        # around its launches; the launches are long, so the pairs barely perturb them).
+        pk = {}
+        for c in ("pf_gemm", "pf_attn"):
+            d.timing_enable(c, 100000)
+            d.kv_reset()
+            d.prefill(prompt_np, 0, logits, tok)
+            ms, n = d.timing_read()
+            pk[c] = (ms, n)
+        d.timing_enable("pf_gemm", 0)
+        r["prefill_kernels"] = pk
+        # Decode, persistent step: per-phase GPU timestamps of CTA 0 (one %globaltimer
+        # store per grid barrier; the step is not otherwise changed).
+        if r["schedule"] != "off":
+            ppl_max = 6
+            st = torch.zeros(w["n_layers"] * ppl_max + 2, dtype=torch.int64, device=dev)
+            d.kv_reset()
+            d.prefill(prompt_np, 0, logits, tok)
+            d.phase_stamps(st)
+            rows = []
+            nst = min(D, 16)
+            for i in range(nst):
+                d.decode_dev(tok, P + i, logits, tok)
+                d.synchronize()
+                rows.append(st.cpu().numpy().astype(np.int64).copy())
+            d.phase_stamps(None)
+            d.check()
+            r["phase_rows"] = rows
+    return r
+
+
+def phase_summary(w: dict, rows, merge_phase: bool) -> dict:
+    """Per-phase µs per token (summed over layers) from the persistent step's stamps."""
+    ppl = 6 if merge_phase else 5
+    names = ["qkv", "attn", "merge", "oproj", "gateup", "down"] if ppl == 6 else \
+        ["qkv", "attn", "oproj", "gateup", "down"]
+    n = w["n_layers"] * ppl + 1
+    diffs = np.stack([np.diff(r[: n + 1]) for r in rows[2:]]) if len(rows) > 2 else \
+        np.stack([np.diff(r[: n + 1]) for r in rows])
+    med = np.median(diffs, axis=0)
+    out = {nm: round(float(np.sum(med[:-1].reshape(w["n_layers"], ppl)[:, j])) / 1e3, 1)
+           for j, nm in enumerate(names)}
+    out["lmhead"] = round(float(med[-1]) / 1e3, 1)
+    out["total"] = round(float(np.sum(med)) / 1e3, 1)
+    return out
+
+
+def workload_summary(name, w, r, n, hbm, tf, tf_sus) -> dict:
+    """The prefill/decode figures of one measured workload."""
+    P, D = r["P"], r["D"]
+    out = {
+        "workload": name, "prompt_tokens": P, "decode_tokens": D, "batch": 1, "steps": r["steps"],
+        "warmup": r["warmup"], "decode_schedule": r["schedule"], "weights_gb": round(r["weights_gb"], 3),
+        "step_tok_s": round(n * (P + D) / (r["ms_per_step"] / 1e3), 2), "ms_per_step": round(r["ms_per_step"], 4),
+        "prefill": {"tok_s": round(n * P / r["pre_s"], 1), "ms": round(r["pre_s"] * 1e3, 4), "flops": r["pflops"],
+                    "tensor_frac": round(r["pflops"] / r["pre_s"] / (tf * 1e12), 5),
+                    "tensor_frac_sustained": round(r["pflops"] / r["pre_s"] / (tf_sus * 1e12), 5)},
+        "decode": {"tok_s": round(n * D / r["dec_s"], 1), "ms": round(r["dec_s"] * 1e3, 4),
+                   "bytes_per_token_avg": round(r["dbytes"] / D),
+                   "hbm_frac": round(r["dbytes"] / r["dec_s"] / (hbm * 1e9), 4),
+                   "hbm_frac_nominal_8tbs": round(r["dbytes"] / r["dec_s"] / (NOMINAL_HBM_GBS * 1e9), 4)},
+        "clocks": r["clocks"],
+    }
+    if "e2e_s" in r:
+        out["e2e_tok_s"] = round(n * (P + D) / r["e2e_s"], 2)
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    from decoder_only_forward_gb300 import build as dec_build
+    if rank == 0:
+        dec_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    dec_build.build()
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = workload_of(args)
+    hbm, tf, tf_sus, peak_kind = peaks()
+    r = measure_workload(args.workload, w, dev, args, args.steps, args.warmup,
+                         want_e2e_steps=max(1, min(args.steps, 3)), world=world)
+    d = r["d"]
+    P, D, V = r["P"], r["D"], r["V"]
+    n = world
+
+    # ---- roofline of the dominant kernel: the decode step ----
+    dec_share = r["dec_s"] / (r["ms_per_step"] / 1e3)
+    if r["schedule"] != "off":
+        # One persistent kernel per decode token: its launches are the decode region.
+        per_launch_bytes = r["dbytes"] / D
+        avg_launch_s = r["dec_s"] / D
+        kname = "k_decode_step"
+        traffic = measured_traffic(args.workload, "step")
+        note = ("one launch per token; duration = the timed decode region / D (CUDA events on the "
+                "library's stream), so launch gaps count against the kernel")
     else:
-        per_launch_bytes = wb[dom] + 4 * w["hidden"] * 2
-    avg_launch_s = (pc["prefill_ms"] + pc["decode_ms"]) / max(nl, 1) / 1e3
+        per_launch_bytes = r["dbytes"] / D
+        avg_launch_s = r["dec_s"] / D
+        kname = "decode step (chain of per-layer kernels)"
+        traffic = None
+        note = "per-layer kernels chained by programmatic dependent launch; figure is per token, not per launch"
     achieved = per_launch_bytes / avg_launch_s / 1e9
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": measured_traffic(args.workload, dom),
-                "peak_kind": peak_kind,
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_kind": peak_kind,
                 "bytes_per_launch": int(per_launch_bytes), "avg_launch_us": round(avg_launch_s * 1e6, 3),
-                "launches_per_step": nl}
+                "launches_per_step": D, "share_of_step": round(dec_share, 4), "note": note}
+    pk = r.get("prefill_kernels", {})
+    roofline_prefill = None
+    if pk.get("pf_gemm", (0, 0))[1]:
+        g_ms, g_n = pk["pf_gemm"]
+        gf = gemm_flops(w, P)
+        ach = gf / (g_ms / 1e3) / 1e12
+        roofline_prefill = {
+            "bound": "tensor", "kernel": "k_gemm_tc (prefill projection GEMMs)", "achieved": round(ach, 1),
+            "peak": tf, "unit": "TFLOP/s", "frac": round(ach / tf, 4), "frac_sustained": round(ach / tf_sus, 4),
+            "traffic": None, "peak_kind": peak_kind, "flops_per_launch": round(gf / g_n),
+            "avg_launch_us": round(g_ms * 1e3 / g_n, 3), "launches_per_prefill": g_n,
+            "ms_per_prefill": round(g_ms, 4), "share_of_prefill": round(g_ms / (r["pre_s"] * 1e3), 4),
+            "note": "GEMM launches timed alone in one extra prefill (event pair around each launch)"}
+    prefill_kernels = {c: {"ms": round(ms, 4), "launches": nl} for c, (ms, nl) in pk.items()}
+    phases = None
+    if "phase_rows" in r:
+        # The step stores a start stamp, one per phase and one after the head: the count of
+        # stored stamps gives the phases per layer (5, or 6 with a split-merge phase).
+        nz = int(np.count_nonzero(r["phase_rows"][-1]))
+        phases = phase_summary(w, r["phase_rows"], (nz - 2) // w["n_layers"] == 6)
 
     out = None
     if rank == 0:
-        n, k_steps = world, args.steps
-        tokens_per_step = P + D
-        value = replica_value(n, tokens_per_step, ms_per_step)
+        value = replica_value(n, P + D, r["ms_per_step"])
         cpu = None
         if not args.no_cpu_baseline:
-            npf, ndc = oracle_sample_size(w)
-            cv, secs, cores = oracle_sample(w, npf, ndc, device=str(dev))
-            cpu = {"value": round(cv, 3), "unit": "tok/s", "cores": cores, "kind": "oracle",
-                   "sample": f"float64 oracle: batched single-pass prefill of {npf} prompt tokens + {ndc} "
-                             f"per-token forwards of the same {args.workload}-shaped model "
-                             f"(weights preloaded as float64), {secs:.1f} s"}
+            plan = oracle_sample_plan(w)
+            cv, secs, cores, _ = oracle_sample(w, plan, device=str(dev))
+            cpu = {"value": round(cv, 4), "unit": "tok/s", "cores": cores, "kind": "oracle",
+                   "sample": oracle_sample_text(args.workload, w, plan, cores) + f"; {secs:.1f} s of arithmetic"}
+        s = workload_summary(args.workload, w, r, n, hbm, tf, tf_sus)
         out = {
-            "metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": n, "steps": k_steps,
-            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": n, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"] if w["dtype"] != "f32" else "f32",
             "data": "synthetic (random-init weights N(0,0.02), norms 1+N(0,0.1), uniform random prompt)",
             "config": {"workload": args.workload + (f"+qk_norm_{args.qk_norm}" if args.qk_norm else "")
                        + ("+sandwich" if args.sandwich else ""), "prompt_tokens": P, "decode_tokens": D, "batch": 1,
-                       "decode_schedule": d.fused_mode(),
-                       "kv_dtype": args.kv, "weights_gb": round(d.weights.nbytes() / 1e9, 3),
+                       "decode_schedule": r["schedule"],
+                       "kv_dtype": args.kv, "weights_gb": round(r["weights_gb"], 3),
                        "l2": "flushed before each step (write of a 258 MB buffer); weights also exceed L2",
                        "parallelism": f"replicas x{n}" if n > 1 else "single GPU"},
-            "prefill": {"tok_s": round(n * P / pre_s, 1), "ms": round(pre_s * 1e3, 4),
-                        "flops": pflops, "tensor_frac": round(pflops / pre_s / (tf * 1e12), 5),
-                        "tensor_frac_sustained": round(pflops / pre_s / (tf_sus * 1e12), 5)},
-            "decode": {"tok_s": round(n * D / dec_s, 1), "ms": round(dec_s * 1e3, 4),
-                       "bytes_per_token_avg": round(dbytes / D), "hbm_frac": round(dbytes / dec_s / (hbm * 1e9), 4),
-                       "hbm_frac_nominal_8tbs": round(dbytes / dec_s / (NOMINAL_HBM_GBS * 1e9), 4)},
-            "clocks": clk.summary(),
-            "e2e": {"value": round(n * tokens_per_step / e2e_s, 2), "unit": "tok/s",
+            "prefill": s["prefill"], "decode": s["decode"], "clocks": r["clocks"],
+            "e2e": {"value": round(n * (P + D) / r["e2e_s"], 2), "unit": "tok/s",
                     "h2d_bytes_per_step": 4 * P, "d2h_bytes_per_step": 4 * D + 4 * V,
                     "note": "pinned prompt copied in by dec_prefill; each greedy token read back to the host; "
                             "final logits read back"},
-            "gpu_launches": int(launches / args.steps) * args.steps,
-            "gpu_launches_per_step": int(launches / args.steps),
+            "gpu_launches": int(r["launches"] / args.steps) * args.steps,
+            "gpu_launches_per_step": int(r["launches"] / args.steps),
             "roofline": roofline,
-            "kernel_classes_ms_per_step": {c: round(v["prefill_ms"] + v["decode_ms"], 4) for c, v in per_class.items()},
+            "roofline_prefill": roofline_prefill,
+            "prefill_kernels_ms": prefill_kernels,
+            "decode_phases_us_per_token": phases,
             "cpu_baseline": cpu,
-            "wall_s_timed": round(wall, 3),
+            "wall_s_timed": round(r["wall"], 3),
         }
     if rank == 0 and args.batch > 0:
-        out["batched_decode"] = run_batched(args, w, d.weights, dev, kv_es)
+        out["batched_decode"] = run_batched(args, w, d.weights, dev, r["kv_es"])
     d.close()
+    del d, r
+    if rank == 0 and args.per_workload != "none":
+        names = PER_WORKLOAD_DEFAULT if args.per_workload == "auto" else args.per_workload.split(",")
+        per = {}
+        for nm in names:
+            if nm == args.workload:
+                per[nm] = {"same_as_main_line": True}
+                continue
+            torch.cuda.empty_cache()
+            wn = synthetic.workload(nm)
+            rn = measure_workload(nm, wn, dev, args, args.per_workload_steps, 3, want_e2e_steps=1,
+                                  attribution=False)
+            per[nm] = workload_summary(nm, wn, rn, 1, hbm, tf, tf_sus)
+            rn["d"].close()
+            del rn
+        out["per_workload"] = per
     return out
 
 
@@ -533,24 +685,32 @@ def run_profile_batched(args, w):
 
 # ---------------------------------------------------------------- reference arm (oracle)
 def run_reference(args):
+    """The baseline arm: the float64 oracle as it stands on the host cores, on a bounded
+    sample of the same workload each step (``oracle_sample_plan``), scaled to tok/s of
+    the whole model.  Weights are drawn once (on the GPU when there is one, the same values
+    the library gets) and kept as float64 for the sampled layers."""
     w = workload_of(args)
-    npf, ndc = oracle_sample_size(w)
-    dev = "cpu"
+    plan = oracle_sample_plan(w)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
     rates, secs = [], []
     cores = len(os.sched_getaffinity(0))
+    src = None
     for i in range(args.warmup + args.steps):
-        r, s_, cores = oracle_sample(w, npf, ndc, device=dev)
+        r, s_, cores, src = oracle_sample(w, plan, device=dev, src=src)
         if i >= args.warmup:
             rates.append(r)
             secs.append(s_)
-    value = (npf + ndc) * len(secs) / sum(secs)
-    sample = (f"float64 oracle on {cores} host cores: batched single-pass prefill of {npf} prompt tokens + "
-              f"{ndc} per-token forwards of the {args.workload}-shaped model per step")
+    scale = w["n_layers"] / plan["layers"]
+    tokens = plan["prefill"] + plan["decode"]
+    value = tokens * len(secs) / (sum(secs) * scale)
+    sample = oracle_sample_text(args.workload, w, plan, cores)
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tok/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * sum(secs) / len(secs), 2),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * sum(secs) * scale / len(secs), 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "prompt_tokens": npf, "decode_tokens": ndc, "batch": 1},
+        "config": {"workload": args.workload, "prompt_tokens": w["prompt"], "decode_tokens": w["decode"],
+                   "batch": 1, "sample": {"layers": plan["layers"], "prefill_tokens": plan["prefill"],
+                                          "decode_tokens": plan["decode"], "time_scaled_by": scale}},
         "cpu_baseline": {"value": round(value, 4), "unit": "tok/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -563,7 +723,11 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="smollm2-135m", choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--workload", default="mixtral-8x7b", choices=sorted(synthetic.WORKLOADS),
+                    help="the main line's workload (default: the largest single-GPU configuration)")
+    ap.add_argument("--per-workload", default="auto",
+                    help="also measure these workloads (comma list; auto: every named non-toy workload; none)")
+    ap.add_argument("--per-workload-steps", type=int, default=3)
     ap.add_argument("--kv", default="f32", choices=["f32", "bf16", "i8"])
     ap.add_argument("--prompt", type=int, default=0, help="override the prompt length (profiling only)")
     ap.add_argument("--layers", type=int, default=0,

@@ -4,6 +4,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <new>
 #include <string>
 #include <vector>
@@ -62,6 +63,24 @@ static void drop_graph(dec_handle* h) {
 
 static void timing_start(dec_handle* h) { h->timing.n = 0; }
 static void timing_finish(dec_handle* h) { h->timing.n_done = h->timing.n; }
+
+static std::atomic<int> g_sm_count[64];
+
+int dec::device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 1;
+  }
+  int n = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 1;
+  }
+  g_sm_count[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
 
 static thread_local std::string g_create_error;
 
@@ -361,7 +380,8 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
   // LM head: two CTAs per SM, each warp walking its row pairs with the next
   // pair's loads in flight.
   int lg = (cfg->vocab / 2 + 7) / 8;
-  if (lg > 2 * 152) lg = 2 * 152;
+  const int sms = device_sm_count();
+  if (lg > 2 * sms) lg = 2 * sms;
   m.lm_grid = lg < 1 ? 1 : (lg > LM_GRID_MAX ? LM_GRID_MAX : lg);
   m.tok_embd = w->tok_embd;
   m.out_norm = (const float*)w->out_norm;
@@ -949,13 +969,25 @@ dec_status dec_check(dec_handle* h) {
   if (e != cudaSuccess) return fail(h, DEC_ECUDA, "state read: %s", cudaGetErrorString(e));
   if (words[0]) {
     cudaMemset(&h->m.s.st->err, 0, sizeof words);
-    if (words[0] & ERR_TIMEOUT)
+    if (words[0] & ERR_TIMEOUT) {
+      // A wait that gave up leaves its barrier or last-CTA counter part-way; the
+      // stream is idle now, so every counter starts again from zero.
+      cudaMemset(h->m.s.st->counters, 0, sizeof h->m.s.st->counters);
       return fail(h, DEC_ETIMEOUT, "a bounded device wait timed out (site %u)", words[1]);
+    }
     if (words[0] & ERR_LAYOUT)
       return fail(h, DEC_ECUDA, "a kernel's shared-memory window was not aligned for its tiles (site %u)",
                   words[1]);
     return fail(h, DEC_EINVAL, "a device-side token was outside [0, vocab)");
   }
+  return DEC_OK;
+}
+
+dec_status dec_selftest_wait_timeout(dec_handle* h, int32_t limit_us) {
+  if (!h) return DEC_EINVAL;
+  if (limit_us < 1 || limit_us > 100000) return fail(h, DEC_EINVAL, "limit_us must be in [1, 100000]");
+  cudaError_t e = launch_wait_selftest(h->m, h->stream, (uint64_t)limit_us * 1000u, DEC_SITE_SELFTEST);
+  if (e != cudaSuccess) return fail(h, DEC_ECUDA, "self-test launch: %s", cudaGetErrorString(e));
   return DEC_OK;
 }
 

@@ -20,8 +20,11 @@ bool attend_check(const void* q, const void* k, const void* v, const void* out, 
   if (sliding < 0) return bad("sliding_window must be >= 0");
   if (sliding == 0 && pos >= max_seq) return bad("without a window pos must be < max_seq");
   if (sliding > 0 && max_seq > sliding) return bad("max_seq cannot exceed the window");
+  // A ring shorter than the window cannot hold the window once it wraps: like a
+  // handle's cache, it then holds positions below max_seq only.
+  if (sliding > max_seq && pos >= max_seq) return bad("a ring shorter than the window holds pos < max_seq only");
   int nsplit = (max_seq + 127) / 128;
-  const int cap = (2 * 152) / nkv;
+  const int cap = (2 * device_sm_count()) / nkv;   // about two CTAs per SM
   if (nsplit > cap) nsplit = cap;
   if (nsplit > 64) nsplit = 64;
   if (nsplit < 1) nsplit = 1;

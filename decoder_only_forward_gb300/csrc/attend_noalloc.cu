@@ -19,23 +19,49 @@ constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
 static __device__ __align__(256) unsigned char g_attend_scratch[kNoAllocScratchBytes];
 
 // Device address of g_attend_scratch per device.  In host code the symbol is
-// only a host-side stand-in, never a device address, so it is translated once
-// per device with cudaGetSymbolAddress while that device is current.
+// only a host-side stand-in, never a device address, so it is translated with
+// cudaGetSymbolAddress while that device is current.  The address belongs to the
+// device's current context: after cudaDeviceReset (or a released and re-created
+// primary context) the module is loaded again and the array may move, so each
+// cached address is kept with the context it was resolved in and looked up again
+// when the context changes.
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
+void* g_ctx[kMaxDevices] = {};
+
+using CtxGetCurrentFn = int (*)(void**);   // cuCtxGetCurrent(CUcontext*) -> CUresult
+
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
 
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  CtxGetCurrentFn get = ctx_get_current();
+  if (!get) return cudaErrorDeviceUninitialized;
+  void* ctx = nullptr;   // stays NULL until the runtime has made a context current
+  if (get(&ctx) != 0) return cudaErrorDeviceUninitialized;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_addr[dev]) {
+  if (!ctx || !g_addr[dev] || g_ctx[dev] != ctx) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_attend_scratch);
+    e = cudaGetSymbolAddress(&p, g_attend_scratch);   // makes the device's primary context current
     if (e != cudaSuccess) return e;
+    if (get(&ctx) != 0 || !ctx) return cudaErrorDeviceUninitialized;
     g_addr[dev] = p;
+    g_ctx[dev] = ctx;
   }
   *out = g_addr[dev];
   return cudaSuccess;

@@ -893,7 +893,8 @@ void launch_attend(const float* q, const void* kc, const void* vc, int nq, int n
 
 static inline int gemv_grid(int tasks) {
   int g = (tasks + GEMV_WARPS - 1) / GEMV_WARPS;
-  return g < 1 ? 1 : (g > 152 * 8 ? 152 * 8 : g);
+  const int cap = device_sm_count() * 8;
+  return g < 1 ? 1 : (g > cap ? cap : g);
 }
 
 template <typename F>

@@ -143,7 +143,8 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
 // arrival is an acq_rel atomic after the CTA's bar.sync (so the CTA's writes
 // are released), the last arriver releases the generation, the others acquire
 // it; no full fences.
-__device__ __forceinline__ bool mk_grid_sync(DeviceState* st, unsigned nb, volatile int* abort_flag, unsigned site) {
+__device__ __forceinline__ bool mk_grid_sync(DeviceState* st, unsigned nb, volatile int* abort_flag, unsigned site,
+                                             uint64_t limit_ns = WAIT_LIMIT_NS) {
   compute_sync();
   if (threadIdx.x == 0 && !*abort_flag) {
     unsigned* cnt = &st->counters[CNT_MK_BAR];
@@ -157,7 +158,7 @@ __device__ __forceinline__ bool mk_grid_sync(DeviceState* st, unsigned nb, volat
     } else {
       const uint64_t t0 = globaltimer_ns();
       while (ld_acquire_u32(gen) == g0) {
-        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+        if (globaltimer_ns() - t0 > limit_ns) {
           raise_error(st, ERR_TIMEOUT, site);
           *abort_flag = 1;
           break;
@@ -1727,6 +1728,22 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
 }  // namespace dec
 
 namespace dec {
+
+// ------------------------------------------------------------------ bounded-wait self-test
+// One CTA enters the persistent step's grid barrier expecting two arrivals.  The
+// second never comes, so the wait runs out after limit_ns, records ERR_TIMEOUT with
+// the site and returns: the path a real step takes when a peer CTA never arrives.
+__global__ void __launch_bounds__(MK_COMPUTE, 1) k_wait_selftest(DeviceState* st, uint64_t limit_ns, unsigned site) {
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) abort_flag = 0;
+  __syncthreads();
+  mk_grid_sync(st, 2u, &abort_flag, site, limit_ns);
+}
+
+cudaError_t launch_wait_selftest(const Model& m, cudaStream_t s, uint64_t limit_ns, unsigned site) {
+  k_wait_selftest<<<1, MK_COMPUTE, 0, s>>>(m.s.st, limit_ns, site);
+  return cudaGetLastError();
+}
 
 // ------------------------------------------------------------------ host side
 // Floats of the f32 activation region xs: the phase inputs (on the tensor-core

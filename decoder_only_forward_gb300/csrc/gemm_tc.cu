@@ -308,17 +308,7 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static int num_sms() {
-  static int n = 0;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
-                                                  cudaSuccess)
-      n = 0;
-  });
-  return n > 0 ? n : 1;
-}
+static int num_sms() { return device_sm_count(); }
 
 template <int BN, bool SPLIT>
 static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& al, const CUtensorMap& b, int M, int N, int K,

@@ -88,7 +88,7 @@ void launch_kv_quant(const dec_config& c, const float* src_k, const float* src_v
 void launch_kv_gather_i8(const dec_config& c, const void* ring_k, const void* ring_v, const KvPaging& pg, int seq,
                          int h0, int count, float* lin_k, float* lin_v, cudaStream_t s) {
   const KvRowLayout L = kv_row_layout(c);
-  k_kv_gather_i8<<<152, 256, 0, s>>>((const char*)ring_k, (const char*)ring_v, pg, seq, c.max_seq,
+  k_kv_gather_i8<<<device_sm_count(), 256, 0, s>>>((const char*)ring_k, (const char*)ring_v, pg, seq, c.max_seq,
                                      c.n_kv_heads * c.head_dim, L.group, L.bytes, L.code_off, h0, count, lin_k,
                                      lin_v);
 }

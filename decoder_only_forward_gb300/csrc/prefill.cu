@@ -747,7 +747,7 @@ static void qk_norm_rows(const Model& m, cudaStream_t s, const LayerPtrs& L, int
                                             c.head_dim, c.qk_norm, L.q_norm, L.k_norm, c.rms_eps, rope);
   count_launch(m);
   if (planes) {
-    k_rows_to_planes<<<152, 256, 0, s>>>((const float*)S.A, (size_t)n * qd, S.at.Qb, (size_t)S.at.qcap * qd);
+    k_rows_to_planes<<<device_sm_count(), 256, 0, s>>>((const float*)S.A, (size_t)n * qd, S.at.Qb, (size_t)S.at.qcap * qd);
     count_launch(m);
   }
 }
@@ -804,7 +804,7 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n,
     KV* vdst = direct ? vc : (KV*)S.KVlin_v;
     if (!direct && hist > 0) {
       if (i8) launch_kv_gather_i8(c, L.kc, L.vc, m.paging, seq, h0, hist, (float*)kdst, (float*)vdst, s);
-      else k_kv_gather<KV><<<152, 256, 0, s>>>((const KV*)L.kc, (const KV*)L.vc, m.paging, seq, c.max_seq, kd, h0,
+      else k_kv_gather<KV><<<device_sm_count(), 256, 0, s>>>((const KV*)L.kc, (const KV*)L.vc, m.paging, seq, c.max_seq, kd, h0,
                                                hist, kdst, vdst);
       count_launch(m);
     }
@@ -845,7 +845,7 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n,
     }
     chk(attention<KV>(m, s, kdst, vdst, direct ? 0 : h0, start, n, a_q.out()));
     if (!direct && !i8) {
-      k_kv_commit<KV><<<152, 256, 0, s>>>(kdst, vdst, hist, start, t_first, n, c.max_seq, kd, (KV*)L.kc, (KV*)L.vc,
+      k_kv_commit<KV><<<device_sm_count(), 256, 0, s>>>(kdst, vdst, hist, start, t_first, n, c.max_seq, kd, (KV*)L.kc, (KV*)L.vc,
                                           m.paging, seq);
       count_launch(m);
     }

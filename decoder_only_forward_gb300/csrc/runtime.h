@@ -270,6 +270,10 @@ struct PageSet {
 };
 void launch_set_pages(int32_t* table, const PageSet& ps, cudaStream_t s);
 
+// Streaming multiprocessors of the current device, queried once per device (1 when
+// no device can be queried).  Grid sizes follow it rather than a fixed part.
+int device_sm_count();
+
 // Persistent single-kernel decode step (decode_mk.cu).
 size_t mk_smem_bytes(const dec_config& c, int nsplit);
 size_t mk_maps_bytes(const dec_config& c);
@@ -277,6 +281,9 @@ bool mk_prepare(Model& m, int num_sms);
 // cluster: run on one thread-block cluster of m.mk_cluster CTAs, else over m.mk_nb CTAs (one per SM).
 void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, int32_t token, int32_t pos,
                       float* logits, int32_t* d_argmax, bool cluster);
+// Bounded-wait self-test: one CTA in the persistent step's grid barrier with an
+// arrival that never comes; the wait gives up after limit_ns and records the site.
+cudaError_t launch_wait_selftest(const Model& m, cudaStream_t s, uint64_t limit_ns, unsigned site);
 // Final RMSNorm + LM head (+ argmax) of one residual row x.
 void launch_lmhead(const Model& m, cudaStream_t s, const float* x, float* logits, int32_t* d_argmax);
 

@@ -31,7 +31,8 @@ EXPORTED = ["dec_config_validate", "dec_workspace_bytes", "dec_create", "dec_pre
             "dec_check", "dec_timing_enable", "dec_timing_read", "dec_launch_count", "dec_destroy",
             "dec_last_error", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc", "dec_gemm_bf16", "dec_set_graph", "dec_set_fused", "dec_fused_available", "dec_fused_mode", "dec_phase_stamps",
             "dec_prefill_seq", "dec_kv_reset_seq", "dec_length_seq", "dec_decode_batch", "dec_kv_layer_seq",
-            "dec_kv_quantize_int8", "dec_kv_slot", "dec_pages_free"]
+            "dec_kv_quantize_int8", "dec_kv_slot", "dec_pages_free", "dec_selftest_wait_timeout"]
+DEC_SITE_SELFTEST = 901
 
 KERNEL_CLASSES = {"qkv": 1, "attn": 2, "oproj": 3, "gateup": 4, "down": 5, "lmhead": 6, "router": 7,
                   "pf_gemm": 8, "pf_attn": 9, "step": 10}
@@ -101,6 +102,7 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "dec_kv_quantize_int8": (I32, [P, I32, I32, I32, P, P]),
         "dec_kv_slot": (I32, [P, I32, I32, I32, ctypes.POINTER(P), ctypes.POINTER(P)]),
         "dec_pages_free": (I32, [P]),
+        "dec_selftest_wait_timeout": (I32, [P, I32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -447,6 +449,10 @@ class Decoder:
 
     def check(self) -> None:
         self._raise(lib.dec_check(self.h))
+
+    def selftest_wait_timeout(self, limit_us: int) -> None:
+        """dec_selftest_wait_timeout: enqueue a bounded wait that runs out (see dec.h)."""
+        self._raise(lib.dec_selftest_wait_timeout(self.h, int(limit_us)))
 
     def timing_enable(self, kernel_class: str, max_launches: int) -> None:
         cls = KERNEL_CLASSES.get(kernel_class, 0) if isinstance(kernel_class, str) else int(kernel_class)

@@ -300,10 +300,25 @@ dec_status dec_set_graph(dec_handle *h, int32_t enable);
 int64_t dec_launch_count(const dec_handle *h);
 
 /* Synchronises the handle's stream and reports device-side errors raised since
- * the last check: DEC_ETIMEOUT (a bounded wait gave up), DEC_EINVAL (a device
+ * the last check: DEC_ETIMEOUT (a bounded wait gave up; the handle's barrier and
+ * last-CTA counters are reset so later calls start clean), DEC_EINVAL (a device
  * token out of range), DEC_ECUDA (a CUDA error, or a kernel whose shared-memory
  * window was not aligned for its tile layout and did no work). */
 dec_status dec_check(dec_handle *h);
+
+/* Site number that dec_check names after dec_selftest_wait_timeout's wait ran out. */
+#define DEC_SITE_SELFTEST 901
+
+/* Self-test of the failure path of a bounded device wait (rml "The decoder", One
+ * forward pass: errors come back as a status, the handle stays usable).  Enqueues on
+ * the handle's stream one CTA that enters the persistent decode step's grid barrier
+ * expecting two arrivals; the second never comes, so the wait gives up after
+ * limit_us microseconds (1 .. 100000), records the timeout with site
+ * DEC_SITE_SELFTEST and returns.  The next dec_check returns DEC_ETIMEOUT naming
+ * that site, clears the error and resets the handle's barrier counters, after which
+ * the handle decodes normally.  Errors: DEC_EINVAL (NULL handle, limit out of
+ * range), DEC_ECUDA (launch failure). */
+dec_status dec_selftest_wait_timeout(dec_handle *h, int32_t limit_us);
 
 /* Kernel classes for dec_timing_enable. */
 typedef enum dec_kernel_class {
@@ -335,6 +350,7 @@ dec_status dec_timing_read(dec_handle *h, float *total_ms, int32_t *launches);
  * online softmax; Pantheon "Llama Forward Pass", Grouped Query Attention and
  * Sliding Window).  Query head h reads kv head h*n_kv_heads/n_heads over the
  * readable slots: min(pos+1, max_seq) under a window, else pos+1 (pos < max_seq).
+ * A ring shorter than the window (max_seq < sliding_window) takes pos < max_seq only.
  *   q:   device [n_heads][head_dim] f32, already rotated.
  *   k,v: device rings [max_seq][n_kv_heads][head_dim] of kv_dtype.
  *   out: device [n_heads][head_dim] f32.
@@ -367,8 +383,9 @@ dec_status dec_gemm_bf16(const void *a_hi, const void *a_lo, const void *b, floa
  *   - Sizes whose scratch exceeds 1 MiB (dec_attend_scratch_bytes() > 1 MiB)
  *     are rejected with DEC_EINVAL and a message.
  *   - The first call on a device looks up the array's device address on the
- *     current device (once per device); make that first call before any
- *     stream capture.
+ *     current device (once per device and context: after cudaDeviceReset the
+ *     next call looks it up again); make that first call before any stream
+ *     capture.
  *   - All calls share the one array: calls that overlap on the GPU (other
  *     streams, other threads) race and give undefined results.  The call
  *     resets what must start at zero itself. */

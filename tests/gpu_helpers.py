@@ -48,6 +48,23 @@ def gpu_greedy(dec, prompt, n_decode: int, use_device_argmax: bool = False):
     return np.stack(rows), taus
 
 
+def gpu_teacher_forced(dec, prompt, taus, n_decode: int):
+    """Prefill the prompt, then decode the given tokens (not the handle's own argmax).
+    Returns the logit rows [n_decode + 1, V]: the prefill's last row and each step's."""
+    V = dec.w["vocab"]
+    logits = torch.empty(V, dtype=torch.float32, device=dec.device)
+    P = len(prompt)
+    dec.prefill(prompt, 0, logits)
+    dec.synchronize()
+    rows = [logits.cpu().numpy().copy()]
+    for i in range(n_decode):
+        dec.decode(int(taus[i]), P + i, logits)
+        dec.synchronize()
+        rows.append(logits.cpu().numpy().copy())
+    dec.check()
+    return np.stack(rows)
+
+
 def oracle_session(w: dict, device: str = "cuda", trace: bool = False) -> Session:
     small = w["hidden"] <= 1024
     src = synthetic.OracleWeightSource(w, device=device, cache=small)

@@ -67,3 +67,9 @@ def test_attend_argument_errors(dec_mod):
     with pytest.raises(dec_mod.DecError) as e:
         dec_mod.attend(q, k, k, 3, 0, out, scratch[:16])
     assert e.value.status == dec_mod.DEC_ENOMEM
+    with pytest.raises(dec_mod.DecError) as e:
+        # A 8-slot ring under a 16-position window cannot hold the window once it wraps.
+        dec_mod.attend(q, k, k, 8, 16, out, scratch)
+    assert e.value.status == dec_mod.DEC_EINVAL
+    dec_mod.attend(q, k, k, 7, 16, out, scratch)          # still below max_seq: accepted
+    torch.cuda.synchronize()

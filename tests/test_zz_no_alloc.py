@@ -3,8 +3,9 @@ allocate device memory themselves (a plug-in inside a framework whose pooled
 allocator owns the GPU, or a path where cudaMalloc may not be called).
 
 Called through the C ABI with ctypes, twice in a row (the shared fixed
-scratch keeps the first call's contents), and compared with dec_attend on a
-caller buffer within the attention tolerance of the other tests.  This file
+scratch keeps the first call's contents), and compared with the oracle's
+brute-force attention and with dec_attend on a caller buffer, within the
+attention tolerance of the other tests.  This file
 sorts last so that a run stopping at its first failure has run everything else.
 """
 
@@ -13,6 +14,8 @@ import ctypes
 import numpy as np
 import pytest
 import torch
+
+from oracle import attend_ref
 
 pytestmark = pytest.mark.gpu
 
@@ -45,11 +48,15 @@ def test_noalloc_matches_dec_attend_twice(dec_mod, kv_dtype):
         scratch = torch.empty(dec_mod.attend_scratch_bytes(nq, nkv, hd, max_seq), dtype=torch.uint8,
                               device="cuda")
         dec_mod.attend(q, k, v, pos, sw, ref, scratch, stream)
+        m = min(pos + 1, max_seq) if sw > 0 else pos + 1
+        brute = attend_ref(q.double().cpu().numpy(), k[:m].double().cpu().numpy(),
+                           v[:m].double().cpu().numpy(), nq, nkv)
         for _ in range(2):   # two calls in a row on the shared scratch
             out = torch.full((nq, hd), float("nan"), device="cuda")
             st = _call_noalloc(dec_mod, q, k, v, pos, sw, out, stream)
             assert st == dec_mod.DEC_OK, dec_mod.lib.dec_last_error(None)
             stream.synchronize()
+            np.testing.assert_allclose(out.cpu().numpy(), brute, atol=1e-5, rtol=1e-5)
             np.testing.assert_allclose(out.cpu().numpy(), ref.cpu().numpy(), atol=1e-5, rtol=1e-5)
 
 
