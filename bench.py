@@ -251,11 +251,9 @@ def oracle_sample_plan(w: dict) -> dict:
     ``decode`` per-token forwards; the time is scaled to the whole model by
     n_layers / layers (the head's share is scaled with it, which overstates the
     oracle's time by a few percent at most)."""
-    if w["n_experts"]:
-        return dict(layers=1, prefill=128, decode=2)
     if w["hidden"] >= 2048:
-        return dict(layers=2, prefill=128, decode=2)
-    return dict(layers=w["n_layers"], prefill=64, decode=2)
+        return dict(layers=2, prefill=512, decode=4)
+    return dict(layers=w["n_layers"], prefill=min(512, w["prompt"]), decode=4)
 
 
 def oracle_sample(w: dict, plan: dict, device: str, src=None):

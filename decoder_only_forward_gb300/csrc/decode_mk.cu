@@ -62,8 +62,9 @@ template <> struct MkRing<__nv_bfloat16> {
   static constexpr bool MMA = true;
 };
 constexpr int MK_CHUNK = 8;                         // row blocks reduced together (partials in smem)
-// Tensor maps per layer (bf16 weights): QKV, O, gate/up, down; then the head.
-enum MkMap { MAP_QKV = 0, MAP_O, MAP_GATEUP, MAP_DOWN, MAPS_PER_LAYER };
+// Tensor maps per layer (bf16 weights): QKV, O, gate/up, down, and the K and V
+// rings (3D: head_dim x kv heads x slots, one box = one attention piece); then the head.
+enum MkMap { MAP_QKV = 0, MAP_O, MAP_GATEUP, MAP_DOWN, MAP_K, MAP_V, MAPS_PER_LAYER };
 
 enum MkPhase { PH_QKV = 0, PH_ATTN, PH_MERGE, PH_OPROJ, PH_GATEUP, PH_DOWN, PH_LMHEAD };
 
@@ -99,6 +100,7 @@ struct MkParams {
   int xb_plane;                   // bf16 weights: elements per plane of the (hi, lo) activation copy
   int xs_floats;                  // floats of the f32 activation vector region
   int attn_warp;                  // attention as per-warp tasks fed by the producer rings
+  int attn_ns;                    // warp-task attention: target splits per kv head (<= 32)
 };
 
 // Shared-memory bookkeeping after the weight ring and the union region.
@@ -120,6 +122,8 @@ struct MkMisc {
   int consumed[MK_COMPUTE_WARPS];  // stages each warp consumed (for the abort drain)
   int is_last;
   float mrow[MAX_GROUP], lrow[MAX_GROUP], alpha[MAX_GROUP];
+  float mscale[8 * 32];          // warp-task attention merge: weight of split s for query head h
+  int lastg[MK_COMPUTE_WARPS];   // kv heads whose last split this CTA finished in the current round
   uint64_t cbar;                 // cluster mode: phase barrier, one arrival per CTA of the cluster
   unsigned cgen;                 // cluster mode: barrier instances completed
 };
@@ -139,30 +143,42 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   return v;
 }
 
-// Grid-wide barrier of the compute groups of all CTAs (bounded wait).  The
-// arrival is an acq_rel atomic after the CTA's bar.sync (so the CTA's writes
-// are released), the last arriver releases the generation, the others acquire
-// it; no full fences.
-__device__ __forceinline__ bool mk_grid_sync(DeviceState* st, unsigned nb, volatile int* abort_flag, unsigned site,
-                                             uint64_t limit_ns = WAIT_LIMIT_NS) {
+// Grid-wide barrier of the compute groups of all CTAs (bounded wait), on a
+// 64-bit arrival counter that only grows: barrier instance k of a launch is
+// passed once the counter reaches base + k * nb, base being the counter's value
+// when the launch began (a multiple of nb: every earlier launch added nb per
+// barrier, and a CTA reads it before its own first arrival, when fewer than nb
+// arrivals of this launch can have happened).  Arrival is one release
+// reduction after the CTA's bar.sync (the CTA's writes are released with it),
+// the wait an acquire poll; no read-modify-write round trip and no separate
+// generation word.
+__device__ __forceinline__ unsigned long long* mk_bar_counter(DeviceState* st) {
+  static_assert(offsetof(DeviceState, counters) % 8 == 0 && CNT_MK_GEN == CNT_MK_BAR + 1 && CNT_MK_BAR % 2 == 0,
+                "the barrier counter is one aligned 64-bit word");
+  return reinterpret_cast<unsigned long long*>(&st->counters[CNT_MK_BAR]);
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool mk_grid_sync(DeviceState* st, unsigned long long target, volatile int* abort_flag,
+                                             unsigned site, uint64_t limit_ns = WAIT_LIMIT_NS) {
   compute_sync();
   if (threadIdx.x == 0 && !*abort_flag) {
-    unsigned* cnt = &st->counters[CNT_MK_BAR];
-    unsigned* gen = &st->counters[CNT_MK_GEN];
-    const unsigned g0 = ld_acquire_u32(gen);
-    unsigned prev;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(cnt) : "memory");
-    if (prev == nb - 1) {
-      asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(cnt) : "memory");
-      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(gen) : "memory");
-    } else {
-      const uint64_t t0 = globaltimer_ns();
-      while (ld_acquire_u32(gen) == g0) {
-        if (globaltimer_ns() - t0 > limit_ns) {
-          raise_error(st, ERR_TIMEOUT, site);
-          *abort_flag = 1;
-          break;
-        }
+    unsigned long long* cnt = mk_bar_counter(st);
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(cnt) : "memory");
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_u64(cnt) < target) {
+      if (globaltimer_ns() - t0 > limit_ns) {
+        raise_error(st, ERR_TIMEOUT, site);
+        *abort_flag = 1;
+        break;
       }
     }
   }
@@ -988,11 +1004,28 @@ struct MkAttnGeom {
   static constexpr int RPP = SB / RB;                // keys per piece (stage)
 };
 
-__device__ __forceinline__ void mk_attn_task(const MkParams& P, int t, int m, int& g, int& split, int& s0, int& j1) {
-  g = t / P.nsplit;
-  split = t - g * P.nsplit;
-  s0 = split * P.sps;
-  j1 = min(min(s0 + P.sps, P.max_seq), m);
+// The warp-task attention plan of one step: the m readable slots of each kv head
+// are cut into ns splits of sps keys (a multiple of 8), ns close to
+// P.attn_ns (about one task per CTA) and at most P.nsplit (the partials' stride).
+// It depends on the position only, so producer and consumer agree.
+struct MkAttnPlan {
+  int ns, sps, tasks;
+};
+__device__ __forceinline__ MkAttnPlan mk_attn_plan(const MkParams& P, int m) {
+  MkAttnPlan a;
+  const int target = max(1, min(P.attn_ns, P.nsplit));
+  a.sps = ((m + target - 1) / target + 7) & ~7;
+  a.ns = (m + a.sps - 1) / a.sps;
+  a.tasks = P.nkv * a.ns;
+  return a;
+}
+
+__device__ __forceinline__ void mk_attn_task(const MkAttnPlan& A, int t, int m, int& g, int& split, int& s0,
+                                             int& j1) {
+  g = t / A.ns;
+  split = t - g * A.ns;
+  s0 = split * A.sps;
+  j1 = min(s0 + A.sps, m);
 }
 
 // A CTA's attention tasks t = blockIdx.x + i * nb (i < per = ceil(tasks / nb),
@@ -1000,25 +1033,56 @@ __device__ __forceinline__ void mk_attn_task(const MkParams& P, int t, int m, in
 // largest power of two <= 8 with per * S <= 8 (at least 1): sub-task j = i * S + k
 // runs on warp j % 8 in round j / 8 and takes slice k.  The S softmax states of a
 // task are combined in shared memory at the end of its round.
-__device__ __forceinline__ int mk_attn_ways(const MkParams& P) {
-  const int per = (P.nkv * P.nsplit + P.nb - 1) / P.nb;
+__device__ __forceinline__ int mk_attn_ways(const MkParams& P, const MkAttnPlan& A) {
+  const int per = (A.tasks + P.nb - 1) / P.nb;
   int S = 1;
   while (S < 8 && 2 * S * per <= MK_COMPUTE_WARPS) S *= 2;
   return S;
 }
-__device__ __forceinline__ int mk_attn_subtasks(const MkParams& P, int S) {
-  return (P.nkv * P.nsplit + P.nb - 1) / P.nb * S;
+__device__ __forceinline__ int mk_attn_subtasks(const MkParams& P, const MkAttnPlan& A, int S) {
+  return (A.tasks + P.nb - 1) / P.nb * S;
 }
-__device__ __forceinline__ bool mk_attn_sub(const MkParams& P, int j, int S, int m, int& t, int& g, int& split,
-                                            int& a, int& b) {
+__device__ __forceinline__ bool mk_attn_sub(const MkParams& P, const MkAttnPlan& A, int j, int S, int m, int& t,
+                                            int& g, int& split, int& a, int& b) {
   t = blockIdx.x + (j / S) * P.nb;
-  if (t >= P.nkv * P.nsplit) return false;
+  if (t >= A.tasks) return false;
   int s0, j1;
-  mk_attn_task(P, t, m, g, split, s0, j1);
+  mk_attn_task(A, t, m, g, split, s0, j1);
   const int len = max(0, j1 - s0), k = j % S;
   a = s0 + (len * k) / S;
   b = s0 + (len * (k + 1)) / S;
   return true;
+}
+
+// Merge of kv head g's split partials into the normalised outputs of its G query
+// heads (by the CTA that finished the head's last split; all compute threads).
+// Weight of split s: exp(m_s - M) / sum_s l_s exp(m_s - M) (rml Attend, one-pass
+// softmax state).  Every load of one output is issued before the first use.
+template <int HD>
+__device__ void mk_merge_kv_head(const MkParams& P, int g, int ns, MkMisc* M) {
+  const int G = P.nq / P.nkv, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (warp < G) {
+    const float* base = P.part + (size_t)(g * G + warp) * P.nsplit * (HD + 2);
+    const float ms = lane < ns ? __ldcg(base + (size_t)lane * (HD + 2) + HD) : -INFINITY;
+    const float ls = lane < ns ? __ldcg(base + (size_t)lane * (HD + 2) + HD + 1) : 0.f;
+    const float Mx = warp_max(ms);
+    const float w = ms == -INFINITY ? 0.f : __expf(ms - Mx);
+    const float L = warp_sum(ls * w);
+    M->mscale[warp * 32 + lane] = L > 0.f ? w / L : 0.f;
+  }
+  compute_sync();
+  for (int idx = tid; idx < G * HD; idx += MK_COMPUTE) {
+    const int h = idx / HD, d = idx - h * HD;
+    const float* base = P.part + (size_t)(g * G + h) * P.nsplit * (HD + 2) + d;
+    float v[32];
+#pragma unroll
+    for (int s2 = 0; s2 < 32; ++s2) v[s2] = s2 < ns ? __ldcg(base + (size_t)s2 * (HD + 2)) : 0.f;
+    float o = 0.f;
+#pragma unroll
+    for (int s2 = 0; s2 < 32; ++s2) o = fmaf(M->mscale[h * 32 + s2], v[s2], o);
+    P.attn[(size_t)(g * G + h) * HD + d] = o;
+  }
+  compute_sync();
 }
 
 // 2^x on the special-function unit (subnormal results flushed to zero).
@@ -1087,13 +1151,14 @@ __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8
   uint32_t scl = sc;
   bool ok = true;
   const int own = lane % GP;                                    // this lane's head in the score slots
-  const int S = mk_attn_ways(P), nsub = mk_attn_subtasks(P, S);
+  const MkAttnPlan A = mk_attn_plan(P, m);
+  const int S = mk_attn_ways(P, A), nsub = mk_attn_subtasks(P, A, S);
   float* sst = reinterpret_cast<float*>(ureg);                  // [8 slots][G][HD + 2] softmax states
   (void)tasks;
   for (int j0 = 0; j0 < nsub; j0 += MK_COMPUTE_WARPS) {
    const int j = j0 + warp;
    int t, g, split, s0, j1;
-   if (j < nsub && mk_attn_sub(P, j, S, m, t, g, split, s0, j1)) {
+   if (j < nsub && mk_attn_sub(P, A, j, S, m, t, g, split, s0, j1)) {
     float qv[GP][DPL], acc[GP][DPL];
 #pragma unroll
     for (int h = 0; h < GP; ++h)
@@ -1222,7 +1287,7 @@ __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8
       const int ti = e / (G * HD), h = (e / HD) % G, d = e % HD;
       const int jt = j0 + ti * S;
       int tt, gg, sp, a, b;
-      if (jt >= nsub || !mk_attn_sub(P, jt, S, m, tt, gg, sp, a, b)) continue;
+      if (jt >= nsub || !mk_attn_sub(P, A, jt, S, m, tt, gg, sp, a, b)) continue;
       const float* st0 = sst + (size_t)(ti * S) * G * (HD + 2) + h * (HD + 2);
       float mx = -INFINITY;
       for (int k = 0; k < S; ++k) mx = fmaxf(mx, st0[(size_t)k * G * (HD + 2) + HD]);
@@ -1234,7 +1299,7 @@ __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8
           lsum = fmaf(sk[HD + 1], wk, lsum);
           o = fmaf(sk[d], wk, o);
         }
-      if (P.nsplit == 1) {
+      if (A.ns == 1) {
         P.attn[(size_t)(gg * G + h) * HD + d] = lsum > 0.f ? o / lsum : 0.f;
       } else {
         float* pp = P.part + ((size_t)(gg * G + h) * P.nsplit + sp) * (HD + 2);
@@ -1243,6 +1308,30 @@ __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8
           pp[HD] = mx == -INFINITY ? -INFINITY : mx / LOG2E;
           pp[HD + 1] = lsum;
         }
+      }
+    }
+    if (A.ns > 1) {
+      // This round's partials are out: count them per kv head; the CTA that
+      // writes a head's last split merges the head (no separate merge phase).
+      __threadfence();
+      compute_sync();
+      if (threadIdx.x < tpr) {
+        int last = -1, tt, gg, sp, a, b;
+        const int jt = j0 + threadIdx.x * S;
+        if (jt < nsub && mk_attn_sub(P, A, jt, S, m, tt, gg, sp, a, b)) {
+          unsigned* cnt = &stp->counters[CNT_ATTN + gg];
+          if (atomicAdd(cnt, 1u) == (unsigned)A.ns - 1) {
+            *cnt = 0u;   // every split of this head has arrived: ready for the next layer
+            __threadfence();
+            last = gg;
+          }
+        }
+        M->lastg[threadIdx.x] = last;
+      }
+      compute_sync();
+      for (int i = 0; i < tpr; ++i) {
+        const int lg = M->lastg[i];
+        if (lg >= 0) mk_merge_kv_head<HD>(P, lg, A.ns, M);
       }
     }
     compute_sync();
@@ -1389,12 +1478,27 @@ __device__ void mk_prefetch_attention_kv(const MkParams& P, int l, int HD, int p
   const int kvb = P.kv_bytes;
   const int kd = P.nkv * HD;
   const int m = P.sliding > 0 ? min(P.pos + 1, P.max_seq) : P.pos + 1;
-  const int tasks = P.nkv * P.nsplit;
+  int ns = P.nsplit, sps = P.sps;
+  if (P.attn_warp) {
+    const MkAttnPlan A = mk_attn_plan(P, m);
+    ns = A.ns;
+    sps = A.sps;
+  }
+  const int tasks = P.nkv * ns;
   int idx = part;
+  // With tensor maps (bf16 weights): one prefetch per piece (one ring stage of keys).
+  const int rpp = P.maps ? MkRing<__nv_bfloat16>::BYTES / (HD * kvb) : 0;
   for (int t = blockIdx.x; t < tasks; t += P.nb) {
-    const int g = t / P.nsplit, split = t - g * P.nsplit;
-    const int s0 = split * P.sps, j1 = min(min(s0 + P.sps, P.max_seq), m);
+    const int g = t / ns, split = t - g * ns;
+    const int s0 = split * sps, j1 = min(min(s0 + sps, P.max_seq), m);
     const int n = j1 > s0 ? j1 - s0 : 0;
+    if (rpp) {
+      const int pieces = (n + rpp - 1) / rpp;
+      for (; idx < 2 * pieces; idx += nparts)
+        tma_prefetch_3d(P.maps + l * MAPS_PER_LAYER + ((idx & 1) ? MAP_V : MAP_K), 0, g, s0 + (idx >> 1) * rpp);
+      idx -= 2 * pieces;
+      continue;
+    }
     for (; idx < 2 * n; idx += nparts) {
       const int r = idx >> 1;
       const uint8_t* base = (const uint8_t*)((idx & 1) ? L.vc : L.kc);
@@ -1488,7 +1592,11 @@ __device__ void mk_produce(const MkParams& P, uint8_t* ring, MkMisc* M) {
       for (int i = 0; i < nphase && ok && !*abort_flag; ++i) {
         int ph, l;
         mk_phase_at(P, i, ph, l);
-        if (ph == PH_ATTN) mk_prefetch_attention_kv(P, l, P.hd, w, MK_COMPUTE_WARPS);
+        // The layer's K/V history is final before its QKV phase (only the current
+        // position's row is written there, and the consumer reads that row from
+        // global memory): prefetch it into L2 while the QKV weights stream, so the
+        // attention phase reads it from L2.
+        if (ph == PH_QKV) mk_prefetch_attention_kv(P, l, P.hd, w, MK_COMPUTE_WARPS);
         if constexpr (HD == 64 || HD == 128) {
           if (ph == PH_ATTN && P.attn_warp) {
             // This warp's attention tasks: per RPP keys a K piece, then a V piece,
@@ -1497,22 +1605,30 @@ __device__ void mk_produce(const MkParams& P, uint8_t* ring, MkMisc* M) {
             const MkLayer& L = P.layers[l];
             const int m = P.sliding > 0 ? min(P.pos + 1, P.max_seq) : P.pos + 1;
             const int kd = P.nkv * HD;
-            const int S = mk_attn_ways(P), nsub = mk_attn_subtasks(P, S);
+            const MkAttnPlan A = mk_attn_plan(P, m);
+            const int S = mk_attn_ways(P, A), nsub = mk_attn_subtasks(P, A, S);
             for (int j = w; j < nsub && ok; j += MK_COMPUTE_WARPS) {
               int t, g, split, s0, j1;   // [s0, j1): this sub-task's keys
-              if (!mk_attn_sub(P, j, S, m, t, g, split, s0, j1)) continue;
+              if (!mk_attn_sub(P, A, j, S, m, t, g, split, s0, j1)) continue;
               for (int c0 = s0; c0 < j1 && ok; c0 += AG::RPP) {
                 const int nk = min(AG::RPP, j1 - c0);
                 for (int kv = 0; kv < 2 && ok; ++kv) {
-                  const int st = claim((uint32_t)(nk * AG::RB));
+                  // A tensor map moves the piece (RPP keys of head g) in one copy; the
+                  // box is always whole (slots past the ring read as zeros, unused).
+                  const int st = claim((uint32_t)(P.maps ? AG::RPP * AG::RB : nk * AG::RB));
                   if (st < 0) {
                     ok = false;
                     break;
                   }
-                  const KV* base = (const KV*)(kv ? L.vc : L.kc);
-                  for (int r = 0; r < nk; ++r)
-                    mk_bulk_load(wring + (size_t)st * SB + (size_t)r * AG::RB,
-                                 base + (size_t)(c0 + r) * kd + (size_t)g * HD, (uint32_t)AG::RB, &M->full[w][st]);
+                  if (P.maps) {
+                    tma_load_3d(wring + (size_t)st * SB, P.maps + l * MAPS_PER_LAYER + (kv ? MAP_V : MAP_K),
+                                &M->full[w][st], 0, g, c0);
+                  } else {
+                    const KV* base = (const KV*)(kv ? L.vc : L.kc);
+                    for (int r = 0; r < nk; ++r)
+                      mk_bulk_load(wring + (size_t)st * SB + (size_t)r * AG::RB,
+                                   base + (size_t)(c0 + r) * kd + (size_t)g * HD, (uint32_t)AG::RB, &M->full[w][st]);
+                  }
                 }
               }
             }
@@ -1605,6 +1721,12 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
   uint32_t sc = 0;
   float best = -INFINITY;
   int bidx = 0x7fffffff;
+  // Grid barriers: this launch's base count (thread 0 is the only one that uses it).
+  unsigned long long bar_target = 0;
+  if (tid == 0 && !P.cluster) {
+    const unsigned long long c0 = ld_relaxed_u64(mk_bar_counter(P.st));
+    bar_target = c0 / (unsigned long long)P.nb * (unsigned long long)P.nb;
+  }
   for (int i = 0; i < nphase; ++i) {
     int ph, l;
     mk_phase_at(P, i, ph, l);
@@ -1624,7 +1746,8 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
           mk_merge_heads(P.part, P.nsplit, HD, h0, 1, xs, P.attn, true);
         break;
       case PH_OPROJ:
-        if (P.nsplit > 1 && !P.merge_phase) mk_merge_heads(P.part, P.nsplit, HD, 0, P.nq, xs + qd, xs, false);
+        if (!P.attn_warp && P.nsplit > 1 && !P.merge_phase)
+          mk_merge_heads(P.part, P.nsplit, HD, 0, P.nq, xs + qd, xs, false);
         else mk_copy_to_xs(P.attn, qd, xs);
         if (MMA) mk_to_xb(xs, false, qd, xb, P.xb_plane);
         break;
@@ -1649,8 +1772,9 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
     // alone would leave the others at the next compute barrier).
     if (compute_sync_or(!ok || *abort_flag)) break;
     if (ph != PH_LMHEAD) {
+      bar_target += (unsigned long long)P.nb;
       const bool synced = P.cluster ? mk_cluster_sync(P.st, (unsigned)P.nb, &M->cbar, &M->cgen, abort_flag, 400 + ph)
-                                    : mk_grid_sync(P.st, (unsigned)P.nb, abort_flag, 400 + ph);
+                                    : mk_grid_sync(P.st, bar_target, abort_flag, 400 + ph);
       if (compute_sync_or(!synced)) break;
     }
     if (P.stamps && blockIdx.x == 0 && tid == 0) P.stamps[i + 1] = globaltimer_ns();
@@ -1737,7 +1861,9 @@ __global__ void __launch_bounds__(MK_COMPUTE, 1) k_wait_selftest(DeviceState* st
   __shared__ int abort_flag;
   if (threadIdx.x == 0) abort_flag = 0;
   __syncthreads();
-  mk_grid_sync(st, 2u, &abort_flag, site, limit_ns);
+  // Target: two arrivals beyond the count before this one's; only one comes.
+  const unsigned long long target = ld_relaxed_u64(mk_bar_counter(st)) + 2ull;
+  mk_grid_sync(st, target, &abort_flag, site, limit_ns);
 }
 
 cudaError_t launch_wait_selftest(const Model& m, cudaStream_t s, uint64_t limit_ns, unsigned site) {
@@ -1836,6 +1962,25 @@ static bool mk_build_maps(Model& m) {
     if (!mk_encode(t + MAP_QKV, L.wqkv, qd + 2 * kd, h) || !mk_encode(t + MAP_O, L.wo, h, qd) ||
         !mk_encode(t + MAP_GATEUP, L.w_gateup, E * 2 * f, h) || !mk_encode(t + MAP_DOWN, L.w_down, E * h, f))
       return false;
+  }
+  // K and V rings: [slots][kv heads][head_dim], a box = one attention piece of one head.
+  const bool kvb16 = c.kv_dtype == DEC_BF16;
+  const uint64_t es = kvb16 ? 2 : 4, hd = (uint64_t)c.head_dim;
+  auto encode_ring = [&](CUtensorMap* t, const void* base) {
+    auto fn = mk_encode_fn();
+    if (!fn || !base) return false;
+    const cuuint64_t dims[3] = {hd, (cuuint64_t)c.n_kv_heads, (cuuint64_t)c.max_seq};
+    const cuuint64_t strides[2] = {hd * es, kd * es};
+    const cuuint32_t box[3] = {(cuuint32_t)hd, 1, (cuuint32_t)(MkRing<__nv_bfloat16>::BYTES / (hd * es))};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(t, kvb16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base),
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerPtrs& L = m.layers[l];
+    CUtensorMap* t = &maps[(size_t)l * MAPS_PER_LAYER];
+    if ((hd == 64 || hd == 128) && (!encode_ring(t + MAP_K, L.kc) || !encode_ring(t + MAP_V, L.vc))) return false;
   }
   if (!mk_encode(&maps.back(), m.head, (uint64_t)c.vocab, h)) return false;
   return cudaMemcpy(m.mk_maps, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice) ==
@@ -1937,7 +2082,6 @@ void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, in
   P.sliding = c.sliding_window;
   P.nsplit = m.nsplit;
   P.sps = m.attn_sps;
-  P.merge_phase = (m.nsplit > 1 && (size_t)c.n_heads * m.nsplit * (c.head_dim + 2) * 4 > 64 * 1024) ? 1 : 0;
   P.nb = cluster ? m.mk_cluster : m.mk_nb;
   P.cluster = cluster ? m.mk_cluster : 0;
   P.eps = c.rms_eps;
@@ -1970,6 +2114,12 @@ void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, in
   P.xs_floats = mk_xs_floats(c, m.nsplit);
   P.xb_plane = mk_xb_plane(c);
   P.attn_warp = mk_attn_warp_ok(c) ? 1 : 0;
+  // Warp-task attention merges each kv head's splits inside its own phase; the
+  // CTA-task attention keeps a merge phase for large split sets.
+  P.merge_phase = (!P.attn_warp && m.nsplit > 1 &&
+                   (size_t)c.n_heads * m.nsplit * (c.head_dim + 2) * 4 > 64 * 1024) ? 1 : 0;
+  P.attn_ns = (P.nb + c.n_kv_heads - 1) / c.n_kv_heads;
+  if (P.attn_ns > 32) P.attn_ns = 32;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(P.nb);
   cfg.blockDim = dim3(MK_THREADS);

@@ -39,7 +39,7 @@ struct TcCfg {
   static constexpr int STAGE_BYTES = A_BYTES * (SPLIT ? 2 : 1) + B_BYTES;
   static constexpr int EPI_LD = 33;                          // floats per staged row
   static constexpr int EPI_BYTES = 4 * 32 * EPI_LD * 4;      // one 32 x 32 slice per epilogue warp
-  static constexpr int BAR_BYTES = 256;
+  static constexpr int BAR_BYTES = 256 + 1280;   // barriers and flags, then the grouped tile prefix
   static constexpr int STAGES_FIT = (232448 - 1024 - EPI_BYTES - BAR_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;
@@ -64,24 +64,40 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drained + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* progress = abort_flag + 1;  // [0] K-blocks issued, [1] K-blocks consumed
+  // Grouped GEMM: tile_pref[g] = row tiles of groups before g (the rows of group g
+  // are [offset[g], offset[g+1]), known on the device only).
+  int* tile_pref = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full) + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = (N + BN - 1) / BN;
-  const int per_n = groups * m_tiles;            // tiles sharing one BN block of weight rows
-  const int total = n_tiles * per_n * ksplit;
   const int kblocks = (K + TC_BK - 1) / TC_BK;
   const int kb_per = (kblocks + ksplit - 1) / ksplit;   // every split non-empty (host's choice)
-  // Tile t -> (group, 128-row block, BN-column block); rows of group g are
-  // [offset[g], offset[g+1]) when grouped.  A tile past its group's rows has
-  // no work (the same answer for every role).
+  if (e.group_offset && threadIdx.x == 32) {
+    int acc = 0;
+    for (int g = 0; g < groups; ++g) {
+      tile_pref[g] = acc;
+      const int rg = e.group_offset[g + 1] - e.group_offset[g];
+      acc += min(m_tiles, (max(rg, 0) + TC_BM - 1) / TC_BM);
+    }
+    tile_pref[groups] = acc;
+  }
+  __syncthreads();
+  // Row tiles sharing one BN block of weight rows: only tiles that hold rows are
+  // enumerated, so the persistent CTAs split the real work evenly.
+  const int per_n = e.group_offset ? tile_pref[groups] : m_tiles;
+  const int total = n_tiles * per_n * ksplit;
+  // Unit u -> (K range u % ksplit of) tile (group, 128-row block, BN-column
+  // block), the same answer for every role.
   auto decode_tile = [&](int u, int& row0, int& rows, int& b_row0, int& m0, int& n0) -> bool {
     const int t = u / ksplit;
     const int nb = t / per_n, rem = t % per_n;
-    const int g = rem / m_tiles, mb = rem % m_tiles;
+    int g = 0, mb = rem;
     row0 = 0;
     rows = M;
     b_row0 = 0;
     if (e.group_offset) {
+      while (g + 1 < groups && tile_pref[g + 1] <= rem) ++g;
+      mb = rem - tile_pref[g];
       row0 = e.group_offset[g];
       rows = e.group_offset[g + 1] - row0;
       b_row0 = g * N;

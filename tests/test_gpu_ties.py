@@ -29,7 +29,7 @@ def dec_mod():
 
 
 class _RouterCopies:
-    """Oracle weight source whose router rows 2 and 3 are copies of rows 0 and 1."""
+    """Oracle weight source whose router row e + E/2 is a copy of row e (e < E/2)."""
 
     def __init__(self, inner):
         self.inner = inner
@@ -38,7 +38,8 @@ class _RouterCopies:
     def layer(self, l):
         lw = dict(self.inner.layer(l))
         r = np.array(lw["router"], copy=True)
-        r[2], r[3] = r[0], r[1]
+        half = r.shape[0] // 2
+        r[half:] = r[:half]
         lw["router"] = r
         return lw
 
@@ -64,10 +65,10 @@ class _RouterCopies:
 def test_equal_router_rows_pick_lower_ids(dec_mod, name, kw, mode):
     w = synthetic.workload(name, **kw)
     weights = dec_mod.DeviceWeights(w)
+    half = w["n_experts"] // 2
     for L in weights.layers:
         r = L["router"]
-        r[2].copy_(r[0])
-        r[3].copy_(r[1])
+        r[half:].copy_(r[:half])      # every expert has a twin: logits e and e + E/2 are equal
     d = dec_mod.Decoder(w, weights=weights)
     d.set_fused(mode)
     P, D = 20, 6
@@ -91,10 +92,12 @@ def test_equal_router_rows_pick_lower_ids(dec_mod, name, kw, mode):
     for l in range(w["n_layers"]):
         for p in range(cap):
             # Copied rows give bit-equal logits, so the tie is exact on the device...
-            assert lg[l, p, 2] == lg[l, p, 0] and lg[l, p, 3] == lg[l, p, 1], (l, p)
+            assert np.array_equal(lg[l, p, half:], lg[l, p, :half]), (l, p)
             got = list(ids[l, p])
-            # ...and the lower id of each tied pair is taken first: [0, 2] or [1, 3].
-            assert got in ([0, 2], [1, 3]), (l, p, got)
+            # ...the top two are the best expert of the first half and its twin, and the
+            # lower id is taken first.
+            e = int(np.argmax(lg[l, p, :half]))
+            assert got == [e, e + half], (l, p, got)
             assert got == route_topk(lg[l, p].astype(np.float64), k)[0], (l, p)
             assert got == sess.trace.expert_ids[(l, p)], (l, p)
 
