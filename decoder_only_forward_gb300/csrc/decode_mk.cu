@@ -1129,6 +1129,26 @@ __device__ __forceinline__ void mk_load_dims(const KV* p, float* v, bool global)
   }
 }
 
+// DPL consecutive K/V elements at a shared-memory address, as f32 (explicit
+// ld.shared, so a piece's loads issue back to back without a generic-address check).
+template <typename KV, int DPL>
+__device__ __forceinline__ void mk_lds_dims(uint32_t a, float* v) {
+  if constexpr (sizeof(KV) == 4 && DPL == 4) {
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(a));
+  } else if constexpr (sizeof(KV) == 4 && DPL == 2) {
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v[0]), "=f"(v[1]) : "r"(a));
+  } else if constexpr (sizeof(KV) == 2 && DPL == 4) {
+    uint32_t u0, u1;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(u0), "=r"(u1) : "r"(a));
+    v[0] = bf16_lo(u0); v[1] = bf16_hi(u0); v[2] = bf16_lo(u1); v[3] = bf16_hi(u1);
+  } else {
+    static_assert(sizeof(KV) == 2 && DPL == 2, "K/V row slices of 2 or 4 elements");
+    uint32_t u0;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(u0) : "r"(a));
+    v[0] = bf16_lo(u0); v[1] = bf16_hi(u0);
+  }
+}
+
 template <typename W, typename KV, int HD, int GP>
 __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8_t* ureg, MkMisc* M, uint32_t& sc) {
   using AG = MkAttnGeom<W, KV, HD>;
@@ -1168,6 +1188,18 @@ __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8
         acc[h][d] = 0.f;
       }
     float mown = -INFINITY, lown = 0.f;   // running max / sum of head `own`
+    // The current position's row was written by this step's QKV phase, possibly
+    // after the producer copied the slot: it is read from global memory once.
+    float kcur[DPL], vcur[DPL];
+    const bool has_cur = slot_pos >= s0 && slot_pos < j1;
+    if (has_cur) {
+      mk_load_dims<KV, DPL>(kc + (size_t)slot_pos * kd + (size_t)g * HD + lane * DPL, kcur, true);
+      mk_load_dims<KV, DPL>(vc + (size_t)slot_pos * kd + (size_t)g * HD + lane * DPL, vcur, true);
+    } else {
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) kcur[d] = vcur[d] = 0.f;
+    }
+    const uint32_t lane_off = (uint32_t)(lane * DPL * (int)sizeof(KV));
     for (int c0 = s0; c0 < j1; c0 += RPP) {
       const int nk = min(RPP, j1 - c0);
       // ---- K piece: scores of (key, head) slots, one per lane after the reduction
@@ -1178,6 +1210,8 @@ __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8
         if (mk_mbar_wait(&M->full[warp][st], (scl / NS) & 1u, abort_flag, stp, 203)) tile = wring + (size_t)st * SB;
         else ok = false;
       }
+      // Rows past the piece's keys are read too (stale stage bytes) and masked below.
+      const uint32_t ktile = mk_smem_u32(tile ? tile : wring) + lane_off;
 #pragma unroll
       for (int q = 0; q < NG; ++q) {
         float v[32];
@@ -1186,19 +1220,17 @@ __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8
 #pragma unroll
         for (int kk = 0; kk < KG; ++kk) {
           const int r = q * KG + kk;
-          if (ok && r < nk) {
-            float kv[DPL];
-            const bool cur = c0 + r == slot_pos;
-            mk_load_dims<KV, DPL>(cur ? kc + (size_t)slot_pos * kd + (size_t)g * HD + lane * DPL
-                                      : reinterpret_cast<const KV*>(tile + (size_t)r * RB) + lane * DPL,
-                                  kv, cur);
+          float kv[DPL];
+          mk_lds_dims<KV, DPL>(ktile + (uint32_t)(r * RB), kv);
+          const bool cur = c0 + r == slot_pos;
 #pragma unroll
-            for (int h = 0; h < GP; ++h) {
-              float s = 0.f;
+          for (int d = 0; d < DPL; ++d) kv[d] = cur ? kcur[d] : kv[d];
 #pragma unroll
-              for (int d = 0; d < DPL; ++d) s = fmaf(qv[h][d], kv[d], s);
-              v[kk * GP + h] = s;
-            }
+          for (int h = 0; h < GP; ++h) {
+            float s = 0.f;
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) s = fmaf(qv[h][d], kv[d], s);
+            v[kk * GP + h] = s;
           }
         }
         mk_reduce_scatter32(v);
@@ -1242,20 +1274,20 @@ __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8
         if (mk_mbar_wait(&M->full[warp][st], (scl / NS) & 1u, abort_flag, stp, 204)) tile = wring + (size_t)st * SB;
         else ok = false;
       }
+      const uint32_t vtile = mk_smem_u32(tile ? tile : wring) + lane_off;
 #pragma unroll
       for (int r = 0; r < RPP; ++r) {
-        if (ok && r < nk) {
-          float vv[DPL];
-          const bool cur = c0 + r == slot_pos;
-          mk_load_dims<KV, DPL>(cur ? vc + (size_t)slot_pos * kd + (size_t)g * HD + lane * DPL
-                                    : reinterpret_cast<const KV*>(tile + (size_t)r * RB) + lane * DPL,
-                                vv, cur);
+        float vv[DPL];
+        mk_lds_dims<KV, DPL>(vtile + (uint32_t)(r * RB), vv);
+        const bool cur = c0 + r == slot_pos, live = ok && r < nk;
+        // Rows past the piece's keys may hold any bits: zero them (their weights are 0).
 #pragma unroll
-          for (int h = 0; h < GP; ++h) {
-            const float pw = __shfl_sync(0xffffffffu, pr[r / KG], (r % KG) * GP + h);
+        for (int d = 0; d < DPL; ++d) vv[d] = live ? (cur ? vcur[d] : vv[d]) : 0.f;
 #pragma unroll
-            for (int d = 0; d < DPL; ++d) acc[h][d] = fmaf(pw, vv[d], acc[h][d]);
-          }
+        for (int h = 0; h < GP; ++h) {
+          const float pw = __shfl_sync(0xffffffffu, pr[r / KG], (r % KG) * GP + h);
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) acc[h][d] = fmaf(pw, vv[d], acc[h][d]);
         }
       }
       if (tile) {
