@@ -62,6 +62,8 @@ def workload_of(args) -> dict:
         kw["qk_norm"] = args.qk_norm
     if getattr(args, "sandwich", False):
         kw["sandwich_norms"] = True
+    if getattr(args, "weights", "") == "i8":
+        kw["weight_int8"] = True
     return synthetic.workload(args.workload, **kw)
 
 
@@ -77,16 +79,18 @@ def peaks():
 def weight_bytes(w: dict) -> dict:
     """Bytes of each decode-path matrix (stored dtype), per layer / per launch."""
     es = 4 if w["dtype"] == "f32" else 2
+    # 8-bit projections: one byte per weight plus an f32 scale per 32 columns.
+    ps = 1 + 4 / 32 if w.get("weight_int8") else es
     h, f, hd = w["hidden"], w["ffn"], w["head_dim"]
     qd, kd = w["n_heads"] * hd, w["n_kv_heads"] * hd
     k = w["n_experts_used"] if w["n_experts"] else 1
     return {
-        "qkv": (qd + 2 * kd) * h * es,
-        "oproj": h * qd * es,
-        "gateup": k * 2 * f * h * es,
-        "down": k * h * f * es,
+        "qkv": (qd + 2 * kd) * h * ps,
+        "oproj": h * qd * ps,
+        "gateup": k * 2 * f * h * ps,
+        "down": k * h * f * ps,
         "router": w["n_experts"] * h * es,
-        "lmhead": w["vocab"] * h * es,
+        "lmhead": w["vocab"] * h * (es if w["tied"] else ps),
         "embed_row": h * es,
     }
 
@@ -530,7 +534,8 @@ def run_ours(args, rank, world, local_rank):
             "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"] if w["dtype"] != "f32" else "f32",
             "data": "synthetic (random-init weights N(0,0.02), norms 1+N(0,0.1), uniform random prompt)",
             "config": {"workload": args.workload + (f"+qk_norm_{args.qk_norm}" if args.qk_norm else "")
-                       + ("+sandwich" if args.sandwich else ""), "prompt_tokens": P, "decode_tokens": D, "batch": 1,
+                       + ("+sandwich" if args.sandwich else "") + ("+int8_weights" if args.weights == "i8" else ""),
+                       "prompt_tokens": P, "decode_tokens": D, "batch": 1,
                        "decode_schedule": r["schedule"],
                        "kv_dtype": args.kv, "weights_gb": round(r["weights_gb"], 3),
                        "l2": "flushed before each step (write of a 258 MB buffer); weights also exceed L2",
@@ -727,6 +732,8 @@ def main():
                     help="also measure these workloads (comma list; auto: every named non-toy workload; none)")
     ap.add_argument("--per-workload-steps", type=int, default=3)
     ap.add_argument("--kv", default="f32", choices=["f32", "bf16", "i8"])
+    ap.add_argument("--weights", default="", choices=["", "i8"],
+                    help="i8: 8-bit projection weights (quantised by the library at create)")
     ap.add_argument("--prompt", type=int, default=0, help="override the prompt length (profiling only)")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (with --profile only: small cases for profiler captures)")

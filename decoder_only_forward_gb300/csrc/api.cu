@@ -4,6 +4,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <new>
 #include <string>
@@ -173,6 +174,9 @@ static bool validate(const dec_config* c, std::string& why) {
     return bad("page_size must be 0 or a power of two >= 16");
   if (c->page_size > 0 && c->n_pages < 1) return bad("a paged cache needs n_pages >= 1");
   if (c->n_pages < 0) return bad("n_pages must be >= 0");
+  if (c->weight_quant != 0 && c->weight_quant != 1) return bad("weight_quant must be 0 or 1");
+  if (c->weight_quant && (c->hidden % 32 || c->ffn % 32 || (c->n_heads * c->head_dim) % 32))
+    return bad("8-bit weights need hidden, ffn and n_heads*head_dim multiples of 32 (one scale per 32 columns)");
   if (c->rope_llama3 && !(c->rope_factor > 0.f && c->rope_low_freq_factor > 0.f &&
                           c->rope_high_freq_factor > c->rope_low_freq_factor && c->rope_orig_ctx > 0))
     return bad("llama3 RoPE scaling needs factor > 0, 0 < low < high, orig_ctx > 0");
@@ -282,6 +286,34 @@ WsPlan dec::plan_workspace(const dec_config& c) {
   // kHalf with QK-norm: the norm weights follow the permuted q/k dims.
   const size_t qn = c.qk_norm == 2 ? (size_t)qd : (size_t)hd, kn = c.qk_norm == 2 ? (size_t)kd : (size_t)hd;
   p.qk_perm = take(c.qk_norm && c.rope_half ? 4 * (size_t)c.n_layers * (qn + kn) : 0);
+  // 8-bit weights: codes + scales of every quantised matrix, one expanded matrix
+  // for the row GEMMs, and the two planes' products before their epilogue.
+  {
+    const size_t E1 = c.n_experts ? (size_t)c.n_experts : 1;
+    const size_t mats[5][2] = {{qkv_rows, (size_t)c.hidden}, {(size_t)c.hidden, (size_t)qd},
+                               {E1 * 2 * c.ffn, (size_t)c.hidden}, {E1 * c.hidden, (size_t)c.ffn},
+                               {c.tied_embedding ? 0 : (size_t)c.vocab, (size_t)c.hidden}};
+    size_t q8 = 0, big = 0;
+    for (int i = 0; i < 5; ++i) {
+      const size_t n = mats[i][0] * mats[i][1];
+      q8 += (i < 4 ? (size_t)c.n_layers : 1) * (align_up(n, 256) + align_up(n / 32 * 4, 256));
+      if (n > big) big = n;
+    }
+    const size_t kk = c.n_experts ? (size_t)c.n_experts_used : 1;
+    size_t mn = (size_t)T * qkv_rows;
+    mn = std::max(mn, (size_t)T * c.hidden);
+    mn = std::max(mn, (size_t)T * kk * 2 * c.ffn);
+    mn = std::max(mn, (size_t)T * kk * c.hidden);
+    mn = std::max(mn, (size_t)bmax * c.vocab);   // the head: one row per batched sequence
+    const bool wq = c.weight_quant != 0;
+    p.q8_bytes = wq ? q8 : 0;
+    p.q8 = take(p.q8_bytes);
+    p.deq_bytes = wq ? 4 * big : 0;
+    p.deq = take(p.deq_bytes);
+    // (+ one logits row for the prefill's untied head when only the argmax is asked for)
+    p.q8part_bytes = wq ? 2 * 4 * mn + 4 * (size_t)c.vocab : 0;
+    p.q8part = take(p.q8part_bytes);
+  }
   // KV rings: [layer][K, V][seq][ring_rows][n_kv*hd], ring_rows = max_seq
   // rounded up to 64 rows so every ring starts 256-byte aligned.
   p.n_seqs = c.n_seqs > 0 ? c.n_seqs : 1;
@@ -455,6 +487,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
     d.k_norm = cfg->qk_norm ? (const float*)L.k_norm : nullptr;
     d.post_attn_norm = cfg->sandwich_norms ? (const float*)L.post_attn_norm : nullptr;
     d.post_ffn_norm = cfg->sandwich_norms ? (const float*)L.post_ffn_norm : nullptr;
+    d.q_wqkv = d.q_wo = d.q_gateup = d.q_down = QMat{nullptr, nullptr};
   }
   if (cfg->rope_half) {
     // kHalf pairs (i, i + d/2) become adjacent pairs (2i, 2i+1) on q/k rows
@@ -481,6 +514,48 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
     }
   }
   m.layers = h->layers.data();
+  m.wq8 = cfg->weight_quant != 0;
+  m.q_head = QMat{nullptr, nullptr};
+  S.deq = nullptr;
+  S.deq_bytes = 0;
+  S.q8part = nullptr;
+  S.q8part_bytes = 0;
+  if (m.wq8) {
+    // Quantise every projection (after any kHalf row permutation) into the workspace.
+    char* q = base + p.q8;
+    const bool wb = cfg->weight_dtype == DEC_BF16;
+    cudaError_t qe = cudaSuccess;
+    auto carve = [&](size_t rows, size_t cols, const void* src) {
+      QMat r;
+      r.codes = (const int8_t*)q;
+      q += align_up(rows * cols, 256);
+      r.scales = (const float*)q;
+      q += align_up(rows * cols / 32 * 4, 256);
+      const cudaError_t e = launch_weight_quant(src, wb, rows, (int)cols, (int8_t*)r.codes, (float*)r.scales,
+                                                h->stream);
+      if (qe == cudaSuccess) qe = e;
+      return r;
+    };
+    const size_t hd_ = cfg->hidden, qd_ = (size_t)cfg->n_heads * cfg->head_dim;
+    const size_t kd_ = (size_t)cfg->n_kv_heads * cfg->head_dim, f_ = cfg->ffn;
+    const size_t E1 = cfg->n_experts ? (size_t)cfg->n_experts : 1;
+    for (int l = 0; l < cfg->n_layers; ++l) {
+      LayerPtrs& d = h->layers[l];
+      d.q_wqkv = carve(qd_ + 2 * kd_, hd_, d.wqkv);
+      d.q_wo = carve(hd_, qd_, d.wo);
+      d.q_gateup = carve(E1 * 2 * f_, hd_, d.w_gateup);
+      d.q_down = carve(E1 * hd_, f_, d.w_down);
+    }
+    if (!cfg->tied_embedding) m.q_head = carve((size_t)cfg->vocab, hd_, m.head);
+    if (qe != cudaSuccess) {
+      delete h;
+      return fail(nullptr, DEC_ECUDA, "weight quantisation: %s", cudaGetErrorString(qe));
+    }
+    S.deq = base + p.deq;
+    S.deq_bytes = p.deq_bytes;
+    S.q8part = p.q8part_bytes ? (float*)(base + p.q8part) : nullptr;
+    S.q8part_bytes = p.q8part_bytes;
+  }
   {
     std::vector<MkLayer> tab(cfg->n_layers);
     for (int l = 0; l < cfg->n_layers; ++l) {
@@ -510,6 +585,9 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
     wbytes += (size_t)cfg->n_layers * ((qd + 2 * kd) * cfg->hidden + cfg->hidden * qd + 3 * kslots * cfg->ffn * cfg->hidden);
     wbytes *= cfg->weight_dtype == DEC_BF16 ? 2 : 4;
     h->fused_mode = wbytes >= (size_t)512 << 20 ? DEC_FUSED_GRID : DEC_FUSED_OFF;
+    // 8-bit weights: the per-layer decode kernels read bf16/f32 rows only, so the
+    // persistent step is the fast path whenever it can run.
+    if (m.wq8) h->fused_mode = DEC_FUSED_GRID;
   }
 
   // RoPE frequencies inv_i = theta^(-2i/hd), llama3-scaled when enabled
@@ -664,13 +742,15 @@ static dec_status run_rows(dec_handle* h, int32_t batch, const int32_t* seqs, co
 
 static dec_status run_decode_step(dec_handle* h, const int32_t* d_token, int32_t token, int32_t pos,
                                   float* logits, int32_t* d_argmax) {
-  if (decode_needs_rows(h->m.cfg)) {
-    // int8 caches, QK-norm and sandwich norms run on the row kernels: one row, sequence 0.
+  const bool cluster = h->fused_mode == DEC_FUSED_CLUSTER && h->m.mk_cluster > 0;
+  const bool fused = h->m.mk_ok && (cluster || h->fused_mode == DEC_FUSED_GRID);
+  if (decode_needs_rows(h->m.cfg) || (h->m.wq8 && !fused)) {
+    // int8 caches, QK-norm and sandwich norms run on the row kernels: one row,
+    // sequence 0; so do 8-bit weights when the persistent step is not taken.
     const int32_t seq0 = 0;
     return run_rows(h, 1, &seq0, &pos, d_token, token, logits, d_argmax);
   }
-  const bool cluster = h->fused_mode == DEC_FUSED_CLUSTER && h->m.mk_cluster > 0;
-  if (h->m.mk_ok && (cluster || h->fused_mode == DEC_FUSED_GRID)) {
+  if (fused) {
     timing_start(h);
     launch_decode_mk(h->m, h->stream, d_token, token, pos, logits, d_argmax, cluster);
     timing_finish(h);

@@ -50,7 +50,7 @@ constexpr int MK_KS = 64;                           // keys per attention chunk
 template <typename W> struct MkRing;
 template <> struct MkRing<float> {
   static constexpr int STAGES = 4, BYTES = 4096;
-  static constexpr bool MMA = false;
+  static constexpr bool MMA = false, Q8 = false;
 };
 #ifndef MK_BPS
 #define MK_BPS 2   // 64-column boxes per stage of the tensor-core GEMV
@@ -59,12 +59,34 @@ constexpr int MK_TM = 16, MK_TK = 64;               // one TMA box: rows x colum
 constexpr int MK_KG = MK_TK * MK_BPS;               // columns per stage: each row read in runs of 2^7 * MK_BPS B
 template <> struct MkRing<__nv_bfloat16> {
   static constexpr int STAGES = 8 / MK_BPS, BYTES = 2048 * MK_BPS;
-  static constexpr bool MMA = true;
+  static constexpr bool MMA = true, Q8 = false;
 };
+// 8-bit projections (weight_quant = 1): a stage is 16 rows x MK_QKG int8 codes as
+// two 128-byte swizzled TMA boxes of 128 columns (each row read in 256-byte runs,
+// as on the bf16 path) followed by the rows' f32 scales (16 x 8 groups of 32
+// columns, 512 bytes); three stages per warp.  Embeddings, the router and a tied
+// head stay bf16.
+struct WQ8 {};
+constexpr int MK_QKG = 256;                         // int8 columns per stage
+constexpr int MK_QSC = 4096;                        // offset of a stage's scales
+constexpr int MK_QSTAGE = MK_QSC + 16 * (MK_QKG / 32) * 4;   // bytes a stage receives (4608)
+template <> struct MkRing<WQ8> {
+  // Slots 1024-byte aligned (the swizzled boxes' alignment): 5 KB each.
+  static constexpr int STAGES = 3, BYTES = 5120;
+  static constexpr bool MMA = true, Q8 = true;
+};
+// Element type of the weights that are never quantised (embeddings, router, a tied head).
+template <typename W> struct MkElem { using T = W; };
+template <> struct MkElem<WQ8> { using T = __nv_bfloat16; };
+// Activation planes are zero-padded to whole stages of either path.
+constexpr int MK_PADK = 256;
 constexpr int MK_CHUNK = 8;                         // row blocks reduced together (partials in smem)
 // Tensor maps per layer (bf16 weights): QKV, O, gate/up, down, and the K and V
 // rings (3D: head_dim x kv heads x slots, one box = one attention piece); then the head.
-enum MkMap { MAP_QKV = 0, MAP_O, MAP_GATEUP, MAP_DOWN, MAP_K, MAP_V, MAPS_PER_LAYER };
+enum MkMap { MAP_QKV = 0, MAP_O, MAP_GATEUP, MAP_DOWN, MAP_K, MAP_V,
+             MAP_QKV_S, MAP_O_S, MAP_GATEUP_S, MAP_DOWN_S, MAPS_PER_LAYER };
+constexpr int MAP_SCALE_OFF = MAP_QKV_S - MAP_QKV;   // a projection's scale map, 8-bit weights
+// After the layers: the head, then (8-bit untied head) its scales.
 
 enum MkPhase { PH_QKV = 0, PH_ATTN, PH_MERGE, PH_OPROJ, PH_GATEUP, PH_DOWN, PH_LMHEAD };
 
@@ -101,6 +123,7 @@ struct MkParams {
   int xs_floats;                  // floats of the f32 activation vector region
   int attn_warp;                  // attention as per-warp tasks fed by the producer rings
   int attn_ns;                    // warp-task attention: target splits per kv head (<= 32)
+  int head_q8;                    // 8-bit weights: the LM head is quantised too (untied)
 };
 
 // Shared-memory bookkeeping after the weight ring and the union region.
@@ -312,7 +335,7 @@ __device__ __forceinline__ int mk_share(int n, int nb, int g) { return ((n + nb 
 
 template <typename W>
 __device__ void mk_phase_rows(const MkParams& P, int ph, int l, const int* ids, MkRows& R) {
-  const int es = (int)sizeof(W);
+  const int es = (int)sizeof(typename MkElem<W>::T);
   const int b = blockIdx.x, nb = P.nb;
   const MkLayer& L = P.layers[l < P.n_layers ? l : 0];
   const int qd = P.nq * P.hd, kd = P.nkv * P.hd;
@@ -710,6 +733,59 @@ __device__ __forceinline__ void mk_mma_bf16(float* d, uint32_t a0, uint32_t a1, 
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Four int8 codes (one 32-bit word, bytes = consecutive columns) -> two bf16
+// pairs, exactly: a code c is biased to c + 128, placed as the low byte of the
+// float 2^23 + (c + 128), and 2^23 + 128 is subtracted; a small integer's f32
+// bits are its bf16 bits in the upper half.
+__device__ __forceinline__ void mk_q8_bf16x2(uint32_t u, uint32_t& lo2, uint32_t& hi2) {
+  const uint32_t v = u ^ 0x80808080u;
+  const float f0 = __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7440)) - 8388736.0f;
+  const float f1 = __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7441)) - 8388736.0f;
+  const float f2 = __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7442)) - 8388736.0f;
+  const float f3 = __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7443)) - 8388736.0f;
+  lo2 = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
+  hi2 = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
+}
+
+// One stage of 8-bit weights: 16 rows x MK_QKG codes (two 128-column boxes,
+// 128-byte swizzled) and their scales.  Each 32-column group is reduced with two
+// MMAs into its own accumulator, then scaled by the row's group scale: d[0] / d[2]
+// collect rows grp / grp + 8 (lanes with t4 == 0 hold the activation's columns).
+// Within a 16-column step lane t4 takes 4 consecutive codes as fragment columns
+// (2t4, 2t4+1, 2t4+8, 2t4+9), and the activation's same 4 columns as B: the same
+// permutation of k on both operands leaves the sum unchanged.
+__device__ __forceinline__ void mk_q8_stage(const uint8_t* tile, int kb, int grp, int t4, bool bl,
+                                            const __nv_bfloat16* xbl, float* d) {
+  const uint32_t sbase = mk_smem_u32(tile);
+  const float* sc = reinterpret_cast<const float*>(tile + MK_QSC);
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint32_t base = sbase + 2048u * j;
+    const uint32_t sw0 = ((base >> 7) + (uint32_t)grp) & 7u, sw8 = ((base >> 7) + (uint32_t)grp + 8u) & 7u;
+    const uint32_t r0 = base + (uint32_t)grp * 128u + 4u * (uint32_t)t4, r8 = r0 + 8u * 128u;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      float dg[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t ks = (uint32_t)(2 * g + hh);
+        uint32_t u0, u8;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(u0) : "r"(r0 + ((ks ^ sw0) << 4)));
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(u8) : "r"(r8 + ((ks ^ sw8) << 4)));
+        uint32_t a0, a1, a2, a3;
+        mk_q8_bf16x2(u0, a0, a2);
+        mk_q8_bf16x2(u8, a1, a3);
+        const int k0 = kb * MK_QKG + j * 128 + (int)ks * 16 + 4 * t4;
+        const uint2 bv = bl ? *reinterpret_cast<const uint2*>(xbl + k0) : make_uint2(0u, 0u);
+        mk_mma_bf16(dg, a0, a1, a2, a3, bv.x, bv.y);
+      }
+      const int gi = j * 4 + g;
+      d[0] = fmaf(sc[grp * 8 + gi], dg[0] + dg[1], d[0]);
+      d[2] = fmaf(sc[(grp + 8) * 8 + gi], dg[2] + dg[3], d[2]);
+    }
+  }
+}
+
 // Barrier 1 over the compute threads; returns whether any of them passed
 // `pred`, so that every compute warp takes the same way out of a phase.
 __device__ __forceinline__ bool compute_sync_or(bool pred) {
@@ -729,7 +805,7 @@ __device__ __forceinline__ bool compute_sync_or(bool pred) {
 // groups.  A global source (the FFN activation, K a multiple of 4) is read
 // as float4, four loads in flight per thread.
 __device__ void mk_to_xb(const float* src, bool src_global, int K, __nv_bfloat16* xb, int plane) {
-  const int KP = (K + MK_KG - 1) / MK_KG * MK_KG;
+  const int KP = (K + MK_PADK - 1) / MK_PADK * MK_PADK;
   if (src_global) {
     const int nv = K >> 2, np = KP >> 2;
     for (int i0 = threadIdx.x; i0 < np; i0 += 4 * MK_COMPUTE) {
@@ -893,7 +969,10 @@ __device__ bool mk_gemv_phase(const MkParams& P, int ph, int l, const MkRows& R,
     // ldmatrix; B = the activation's (hi, lo) bf16 planes as columns 0 and 1
     // of the 16 x 8 operand (lanes of groups 0 and 1 carry them, the others
     // zeros); row r's dot product is D[r][0] + D[r][1], f32-accumulated.
-    const int KB = (R.K + MK_KG - 1) / MK_KG;   // column groups (stages) per row block
+    // 8-bit weights: every projection, and the head when it is quantised too.
+    const bool q8 = MkRing<W>::Q8 && (ph != PH_LMHEAD || P.head_q8);
+    const int kgs = q8 ? MK_QKG : MK_KG;
+    const int KB = (R.K + kgs - 1) / kgs;   // column groups (stages) per row block
     const int grp = lane >> 2, t4 = lane & 3;
     __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(xs + P.xs_floats);
     const __nv_bfloat16* xbl = xb + (grp & 1) * P.xb_plane;   // plane of lane groups 0 / 1
@@ -918,6 +997,13 @@ __device__ bool mk_gemv_phase(const MkParams& P, int ph, int l, const MkRows& R,
             if (!tile) {
               ok = false;
               break;
+            }
+            if constexpr (MkRing<W>::Q8) {
+              if (q8) {
+                mk_q8_stage(tile, kb, grp, t4, bl, xbl, d);
+                release_stage();
+                continue;
+              }
             }
 #pragma unroll
             for (int j = 0; j < MK_BPS; ++j) {
@@ -999,7 +1085,7 @@ namespace dec {
 // query heads per kv head; partials have the same layout as the CTA tasks'.
 template <typename W, typename KV, int HD>
 struct MkAttnGeom {
-  static constexpr int SB = MkRing<W>::BYTES;
+  static constexpr int SB = MkRing<W>::BYTES < 4096 ? MkRing<W>::BYTES : 4096;   // bytes of one piece
   static constexpr int RB = HD * (int)sizeof(KV);   // bytes of one head's K or V row
   static constexpr int RPP = SB / RB;                // keys per piece (stage)
 };
@@ -1152,7 +1238,7 @@ __device__ __forceinline__ void mk_lds_dims(uint32_t a, float* v) {
 template <typename W, typename KV, int HD, int GP>
 __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8_t* ureg, MkMisc* M, uint32_t& sc) {
   using AG = MkAttnGeom<W, KV, HD>;
-  constexpr int NS = MkRing<W>::STAGES, SB = AG::SB, RB = AG::RB, RPP = AG::RPP;
+  constexpr int NS = MkRing<W>::STAGES, SB = MkRing<W>::BYTES, RB = AG::RB, RPP = AG::RPP;   // SB: slot stride
   constexpr int DPL = HD / 32;                                  // dims per lane
   constexpr int KG = (32 / GP) < RPP ? (32 / GP) : RPP;         // keys per reduce group
   constexpr int NG = RPP / KG;                                  // groups per piece
@@ -1685,20 +1771,33 @@ __device__ void mk_produce(const MkParams& P, uint8_t* ring, MkMisc* M) {
           const MkSeg S = R.seg[si];   // by value: its fields stay in registers
           if constexpr (MkRing<W>::MMA) {
             // 16 x 64 tiles in the consumer's order: block by block, this
-            // warp's column blocks of each (see mk_first_kb).
+            // warp's column blocks of each (see mk_first_kb).  8-bit weights:
+            // two 128-column code boxes and the rows' scales per stage.
             const CUtensorMap* map = P.maps + S.map;
-            const int KB = (R.K + MK_KG - 1) / MK_KG;
+            const bool q8 = MkRing<W>::Q8 && (ph != PH_LMHEAD || P.head_q8);
+            const CUtensorMap* smap =
+                P.maps + (S.map < P.n_layers * MAPS_PER_LAYER ? S.map + MAP_SCALE_OFF : S.map + 1);
+            const int kgs = q8 ? MK_QKG : MK_KG;
+            const int KB = (R.K + kgs - 1) / kgs;
             const int nblk = (S.rows + MK_TM - 1) / MK_TM;
             for (int blk = 0; blk < nblk && ok; ++blk)
               for (int kb = mk_first_kb(blk % MK_CHUNK, KB, w); kb < KB && ok; kb += MK_COMPUTE_WARPS) {
-                const int st = claim((uint32_t)SB);
+                const int st = claim(q8 ? (uint32_t)MK_QSTAGE : (uint32_t)(2048 * MK_BPS));
                 if (st < 0) {
                   ok = false;
                   break;
                 }
-                for (int j = 0; j < MK_BPS; ++j)
-                  tma_load_2d(wring + (size_t)st * SB + 2048 * j, map, &M->full[w][st], (kb * MK_BPS + j) * MK_TK,
+                if (q8) {
+                  for (int j = 0; j < 2; ++j)
+                    tma_load_2d(wring + (size_t)st * SB + 2048 * j, map, &M->full[w][st], kb * MK_QKG + j * 128,
+                                S.maprow + blk * MK_TM);
+                  tma_load_2d(wring + (size_t)st * SB + MK_QSC, smap, &M->full[w][st], kb * (MK_QKG / 32),
                               S.maprow + blk * MK_TM);
+                } else {
+                  for (int j = 0; j < MK_BPS; ++j)
+                    tma_load_2d(wring + (size_t)st * SB + 2048 * j, map, &M->full[w][st], (kb * MK_BPS + j) * MK_TK,
+                                S.maprow + blk * MK_TM);
+                }
               }
           } else {
             int r0, r1;
@@ -1742,14 +1841,14 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
   // Tensor-core GEMV operand: the activation as bf16 (hi, lo) planes after xs.
   constexpr bool MMA = MkRing<W>::MMA;
   __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(xs + P.xs_floats);
-  const int kpad_h = (P.h + MK_KG - 1) / MK_KG * MK_KG;
+  const int kpad_h = (P.h + MK_PADK - 1) / MK_PADK * MK_PADK;
   // ---------------- compute warps
   if (P.stamps && blockIdx.x == 0 && tid == 0) P.stamps[0] = globaltimer_ns();
   const int token = M->token;
   const int qd = P.nq * P.hd;
   // The residual starts as the token's embedding row (every CTA writes a share).
   for (int i = blockIdx.x * MK_COMPUTE + tid; i < P.h; i += P.nb * MK_COMPUTE)
-    P.x[i] = to_f32(((const W*)P.embed)[(size_t)token * P.h + i]);
+    P.x[i] = to_f32(((const typename MkElem<W>::T*)P.embed)[(size_t)token * P.h + i]);
   uint32_t sc = 0;
   float best = -INFINITY;
   int bidx = 0x7fffffff;
@@ -1766,7 +1865,7 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
     bool ok = true;
     switch (ph) {
       case PH_QKV:
-        mk_norm_to_xs<W>(P.x, l == 0 ? (const W*)P.embed + (size_t)token * P.h : nullptr, L.attn_norm, P.h, P.eps,
+        mk_norm_to_xs<typename MkElem<W>::T>(P.x, l == 0 ? (const typename MkElem<W>::T*)P.embed + (size_t)token * P.h : nullptr, L.attn_norm, P.h, P.eps,
                          xs, M, MMA ? xb : nullptr, P.xb_plane, kpad_h);
         break;
       case PH_ATTN:
@@ -1784,15 +1883,15 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
         if (MMA) mk_to_xb(xs, false, qd, xb, P.xb_plane);
         break;
       case PH_GATEUP:
-        mk_norm_to_xs<W>(P.x, nullptr, L.ffn_norm, P.h, P.eps, xs, M, MMA ? xb : nullptr, P.xb_plane, kpad_h);
-        if (P.E > 0) mk_router<W>(P, l, xs, M);
+        mk_norm_to_xs<typename MkElem<W>::T>(P.x, nullptr, L.ffn_norm, P.h, P.eps, xs, M, MMA ? xb : nullptr, P.xb_plane, kpad_h);
+        if (P.E > 0) mk_router<typename MkElem<W>::T>(P, l, xs, M);
         break;
       case PH_DOWN:
         // (tensor-core path: the activation is converted per segment)
         if (!MMA && P.E == 0) mk_copy_to_xs(P.act, P.f, xs);
         break;
       case PH_LMHEAD:
-        mk_norm_to_xs<W>(P.x, nullptr, P.out_norm, P.h, P.eps, xs, M, MMA ? xb : nullptr, P.xb_plane, kpad_h);
+        mk_norm_to_xs<typename MkElem<W>::T>(P.x, nullptr, P.out_norm, P.h, P.eps, xs, M, MMA ? xb : nullptr, P.xb_plane, kpad_h);
         break;
     }
     if (mk_is_gemv(ph)) {
@@ -1922,7 +2021,7 @@ static int mk_xb_plane(const dec_config& c) {
   size_t k = (size_t)c.hidden;
   if ((size_t)c.n_heads * c.head_dim > k) k = (size_t)c.n_heads * c.head_dim;
   if ((size_t)c.ffn > k) k = c.ffn;
-  return (int)((k + MK_KG - 1) / MK_KG * MK_KG);
+  return (int)((k + MK_PADK - 1) / MK_PADK * MK_PADK);
 }
 
 static size_t mk_u_bytes(const dec_config& c, int nsplit) {
@@ -1950,7 +2049,7 @@ size_t mk_smem_bytes(const dec_config& c, int nsplit) {
 }
 
 size_t mk_maps_bytes(const dec_config& c) {
-  return c.weight_dtype == DEC_BF16 ? sizeof(CUtensorMap) * ((size_t)c.n_layers * MAPS_PER_LAYER + 1) : 0;
+  return c.weight_dtype == DEC_BF16 ? sizeof(CUtensorMap) * ((size_t)c.n_layers * MAPS_PER_LAYER + 2) : 0;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 mk_encode_fn() {
@@ -1987,13 +2086,56 @@ static bool mk_build_maps(Model& m) {
   if (!m.mk_maps) return false;
   const uint64_t h = c.hidden, qd = (uint64_t)c.n_heads * c.head_dim, kd = (uint64_t)c.n_kv_heads * c.head_dim;
   const uint64_t f = c.ffn, E = c.n_experts > 0 ? c.n_experts : 1;
-  std::vector<CUtensorMap> maps((size_t)c.n_layers * MAPS_PER_LAYER + 1);
-  for (int l = 0; l < c.n_layers; ++l) {
-    const LayerPtrs& L = m.layers[l];
-    CUtensorMap* t = &maps[(size_t)l * MAPS_PER_LAYER];
-    if (!mk_encode(t + MAP_QKV, L.wqkv, qd + 2 * kd, h) || !mk_encode(t + MAP_O, L.wo, h, qd) ||
-        !mk_encode(t + MAP_GATEUP, L.w_gateup, E * 2 * f, h) || !mk_encode(t + MAP_DOWN, L.w_down, E * h, f))
+  std::vector<CUtensorMap> maps((size_t)c.n_layers * MAPS_PER_LAYER + 2);
+  const size_t head_map = (size_t)c.n_layers * MAPS_PER_LAYER;
+  if (m.wq8) {
+    // 8-bit weights: codes [rows][K] in boxes of 16 rows x 128 columns (128-byte
+    // swizzle), scales [rows][K / 32] f32 in boxes of 16 rows x 8 groups.
+    auto fn = mk_encode_fn();
+    if (!fn) return false;
+    auto codes = [&](CUtensorMap* t, const QMat& q, uint64_t rows, uint64_t K) {
+      const cuuint64_t dims[2] = {K, rows};
+      const cuuint64_t strides[1] = {K};
+      const cuuint32_t box[2] = {128, (cuuint32_t)MK_TM};
+      const cuuint32_t estr[2] = {1, 1};
+      return q.codes && fn(t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(q.codes), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    auto scales = [&](CUtensorMap* t, const QMat& q, uint64_t rows, uint64_t K) {
+      const cuuint64_t dims[2] = {K / 32, rows};
+      const cuuint64_t strides[1] = {K / 32 * 4};   // rejected unless a multiple of 16 bytes
+      const cuuint32_t box[2] = {(cuuint32_t)(MK_QKG / 32), (cuuint32_t)MK_TM};
+      const cuuint32_t estr[2] = {1, 1};
+      return q.scales && fn(t, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(q.scales), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    for (int l = 0; l < c.n_layers; ++l) {
+      const LayerPtrs& L = m.layers[l];
+      CUtensorMap* t = &maps[(size_t)l * MAPS_PER_LAYER];
+      if (!codes(t + MAP_QKV, L.q_wqkv, qd + 2 * kd, h) || !scales(t + MAP_QKV_S, L.q_wqkv, qd + 2 * kd, h) ||
+          !codes(t + MAP_O, L.q_wo, h, qd) || !scales(t + MAP_O_S, L.q_wo, h, qd) ||
+          !codes(t + MAP_GATEUP, L.q_gateup, E * 2 * f, h) || !scales(t + MAP_GATEUP_S, L.q_gateup, E * 2 * f, h) ||
+          !codes(t + MAP_DOWN, L.q_down, E * h, f) || !scales(t + MAP_DOWN_S, L.q_down, E * h, f))
+        return false;
+    }
+    if (m.q_head.codes) {
+      if (!codes(&maps[head_map], m.q_head, (uint64_t)c.vocab, h) ||
+          !scales(&maps[head_map + 1], m.q_head, (uint64_t)c.vocab, h))
+        return false;
+    } else if (!mk_encode(&maps[head_map], m.head, (uint64_t)c.vocab, h)) {
       return false;
+    }
+  } else {
+    for (int l = 0; l < c.n_layers; ++l) {
+      const LayerPtrs& L = m.layers[l];
+      CUtensorMap* t = &maps[(size_t)l * MAPS_PER_LAYER];
+      if (!mk_encode(t + MAP_QKV, L.wqkv, qd + 2 * kd, h) || !mk_encode(t + MAP_O, L.wo, h, qd) ||
+          !mk_encode(t + MAP_GATEUP, L.w_gateup, E * 2 * f, h) || !mk_encode(t + MAP_DOWN, L.w_down, E * h, f))
+        return false;
+    }
+    if (!mk_encode(&maps[head_map], m.head, (uint64_t)c.vocab, h)) return false;
   }
   // K and V rings: [slots][kv heads][head_dim], a box = one attention piece of one head.
   const bool kvb16 = c.kv_dtype == DEC_BF16;
@@ -2014,7 +2156,6 @@ static bool mk_build_maps(Model& m) {
     CUtensorMap* t = &maps[(size_t)l * MAPS_PER_LAYER];
     if ((hd == 64 || hd == 128) && (!encode_ring(t + MAP_K, L.kc) || !encode_ring(t + MAP_V, L.vc))) return false;
   }
-  if (!mk_encode(&maps.back(), m.head, (uint64_t)c.vocab, h)) return false;
   return cudaMemcpy(m.mk_maps, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice) ==
          cudaSuccess;
 }
@@ -2031,6 +2172,10 @@ static void* mk_pick(int hd) {
 // per-layer kernels), which keeps this file's build time in check.
 static void* mk_func(const dec_config& c) {
   const bool wb = c.weight_dtype == DEC_BF16, kb = c.kv_dtype == DEC_BF16;
+  if (c.weight_quant) {
+    if (!wb) return nullptr;   // 8-bit weights from f32 models decode on the row kernels
+    return kb ? mk_pick<WQ8, __nv_bfloat16>(c.head_dim) : mk_pick<WQ8, float>(c.head_dim);
+  }
   if (!wb) {
     if (c.head_dim != 16) return nullptr;
     return kb ? (void*)k_decode_step<float, __nv_bfloat16, 16> : (void*)k_decode_step<float, float, 16>;
@@ -2146,6 +2291,7 @@ void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, in
   P.xs_floats = mk_xs_floats(c, m.nsplit);
   P.xb_plane = mk_xb_plane(c);
   P.attn_warp = mk_attn_warp_ok(c) ? 1 : 0;
+  P.head_q8 = m.q_head.codes ? 1 : 0;
   // Warp-task attention merges each kv head's splits inside its own phase; the
   // CTA-task attention keeps a merge phase for large split sets.
   P.merge_phase = (!P.attn_warp && m.nsplit > 1 &&

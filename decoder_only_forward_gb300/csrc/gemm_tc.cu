@@ -294,6 +294,18 @@ __global__ void __launch_bounds__(256) k_splitk_epi(const float* __restrict__ pa
   }
 }
 
+// The planes' products summed in order, then the epilogue (8-bit weights: the
+// weight's hi and lo planes were multiplied separately).
+cudaError_t launch_sum_planes_epi(const float* part, int planes, int M, int N, const GemmEpi& e, cudaStream_t s) {
+  const long long pairs = (long long)M * ((N + 1) / 2);
+  long long blocks = (pairs + 255) / 256;
+  const long long cap = 8LL * device_sm_count();
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  k_splitk_epi<<<(int)blocks, 256, 0, s>>>(part, planes, M, N, e);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------------------
 // Host side: tensor maps and launch.
 

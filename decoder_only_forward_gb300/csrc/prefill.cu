@@ -575,10 +575,37 @@ struct Act {
 
 template <typename TW>
 static cudaError_t gemm(const Model& m, cudaStream_t s, const Act& a, const TW* B, int M, int N, int K,
-                        const GemmEpi& e, int groups, int max_rows) {
+                        const GemmEpi& e, int groups, int max_rows, const QMat& q = QMat{nullptr, nullptr}) {
   cudaError_t err = cudaSuccess;
   timer_begin(m, DEC_K_PF_GEMM, s);
-  if (std::is_same<TW, __nv_bfloat16>::value) {
+  if (q.codes) {
+    // 8-bit weights, expanded a matrix at a time (every group's rows): bf16 models
+    // multiply the weight's hi and lo planes separately (each against the
+    // activation's hi and lo planes) and sum the two products before the
+    // epilogue; f32 models expand to f32 for the SIMT GEMM.
+    const size_t rows_b = (size_t)groups * N;
+    if (std::is_same<TW, __nv_bfloat16>::value) {
+      __nv_bfloat16* hi = reinterpret_cast<__nv_bfloat16*>(m.s.deq);
+      __nv_bfloat16* lo = hi + rows_b * K;
+      err = launch_weight_dequant_hilo(q, rows_b, K, hi, lo, s);
+      GemmEpi ep = e;
+      ep.mode = EPI_STORE;
+      ep.n_out = N;
+      for (int pl = 0; pl < 2 && err == cudaSuccess; ++pl) {
+        ep.out_f32 = m.s.q8part + (size_t)pl * M * N;
+        err = launch_gemm_tc(a.base, a.lo(), a.rows, pl ? lo : hi, M, N, K, ep, groups, max_rows, m.s.kpart,
+                             m.s.kpart_bytes, m.s.st, s);
+      }
+      if (err == cudaSuccess) err = launch_sum_planes_epi(m.s.q8part, 2, M, N, e, s);
+      count_launch(m, 4);
+    } else {
+      float* wf = reinterpret_cast<float*>(m.s.deq);
+      err = launch_weight_dequant_f32(q, rows_b, K, wf, s);
+      dim3 grid((max_rows + 63) / 64, (N + 63) / 64, groups);
+      k_gemm_simt<float, float><<<grid, 256, 0, s>>>((const float*)a.base, wf, M, N, K, e);
+      count_launch(m, 1);
+    }
+  } else if (std::is_same<TW, __nv_bfloat16>::value) {
     err = launch_gemm_tc(a.base, a.lo(), a.rows, B, M, N, K, e, groups, max_rows, m.s.kpart, m.s.kpart_bytes, m.s.st,
                          s);
   } else {
@@ -651,13 +678,13 @@ static cudaError_t ffn_rows(const Model& m, cudaStream_t s, const LayerPtrs& L, 
     e1.act = act.base;
     e1.act_bf16 = split;
     e1.act_lo = act.out().lo;
-    chk(gemm<TW>(m, s, a_h, (const TW*)L.w_gateup, n, 2 * f, h, e1, 1, n));
+    chk(gemm<TW>(m, s, a_h, (const TW*)L.w_gateup, n, 2 * f, h, e1, 1, n, L.q_gateup));
     GemmEpi e2{};
     // Sandwich norms: the block output goes to Z and is normalised into x.
     e2.mode = c.sandwich_norms ? EPI_STORE : EPI_RESID;
     e2.n_out = h;
     e2.out_f32 = c.sandwich_norms ? S.Z : S.X;
-    chk(gemm<TW>(m, s, act, (const TW*)L.w_down, n, h, f, e2, 1, n));
+    chk(gemm<TW>(m, s, act, (const TW*)L.w_down, n, h, f, e2, 1, n, L.q_down));
     if (c.sandwich_norms) {
       k_rmsnorm_add_rows<<<n, 256, 0, s>>>(S.X, S.Z, L.post_ffn_norm, c.rms_eps, h);
       count_launch(m);
@@ -695,13 +722,13 @@ static cudaError_t ffn_rows(const Model& m, cudaStream_t s, const LayerPtrs& L, 
   e1.act_bf16 = split;
   e1.act_lo = act_sort.out().lo;
   e1.group_offset = S.pf_offset;
-  chk(gemm<TW>(m, s, a_sort, (const TW*)L.w_gateup, entries, 2 * f, h, e1, E, n));
+  chk(gemm<TW>(m, s, a_sort, (const TW*)L.w_gateup, entries, 2 * f, h, e1, E, n, L.q_gateup));
   GemmEpi e2{};
   e2.mode = EPI_STORE;
   e2.n_out = h;
   e2.out_f32 = S.Y;
   e2.group_offset = S.pf_offset;
-  chk(gemm<TW>(m, s, act_sort, (const TW*)L.w_down, entries, h, f, e2, E, n));
+  chk(gemm<TW>(m, s, act_sort, (const TW*)L.w_down, entries, h, f, e2, E, n, L.q_down));
   if (c.sandwich_norms) {
     cudaMemsetAsync(S.Z, 0, sizeof(float) * (size_t)n * h, s);
     k_moe_combine<<<n, 256, 0, s>>>(S.Y, S.pf_inv, S.pf_wts, k, h, S.Z);
@@ -725,7 +752,7 @@ static cudaError_t oproj_rows(const Model& m, cudaStream_t s, const LayerPtrs& L
   e.mode = c.sandwich_norms ? EPI_STORE : EPI_RESID;
   e.n_out = h;
   e.out_f32 = c.sandwich_norms ? S.Z : S.X;
-  const cudaError_t err = gemm<TW>(m, s, a_q, (const TW*)L.wo, n, h, qd, e, 1, n);
+  const cudaError_t err = gemm<TW>(m, s, a_q, (const TW*)L.wo, n, h, qd, e, 1, n, L.q_wo);
   if (c.sandwich_norms) {
     k_rmsnorm_add_rows<<<n, 256, 0, s>>>(S.X, S.Z, L.post_attn_norm, c.rms_eps, h);
     count_launch(m);
@@ -830,7 +857,7 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n,
       e.v_dst = vdst;
       e.kv_bf16 = std::is_same<KV, __nv_bfloat16>::value;
       e.kv_row0 = direct ? start : hist;
-      chk(gemm<TW>(m, s, a_h, (const TW*)L.wqkv, n, qd + 2 * kd, h, e, 1, n));
+      chk(gemm<TW>(m, s, a_h, (const TW*)L.wqkv, n, qd + 2 * kd, h, e, 1, n, L.q_wqkv));
       if (qkn) qk_norm_rows(m, s, L, n, (float*)kdst, nullptr, e.kv_row0, q_planes, rope);
     }
     const int t_first = n > c.max_seq ? n - c.max_seq : 0;
@@ -852,7 +879,24 @@ static cudaError_t prefill_chunk(const Model& m, cudaStream_t s, int seq, int n,
     chk(oproj_rows<TW>(m, s, L, n, a_q));
     chk(ffn_rows<TW>(m, s, L, l, n, start, seq == 0));
   }
-  if (logits || d_argmax) launch_lmhead(m, s, S.X + (size_t)(n - 1) * h, logits, d_argmax);
+  if ((logits || d_argmax) && m.q_head.codes) {
+    // 8-bit untied head: the last row through the row GEMM, then its argmax.
+    const Act a1{S.A, split, 1, h};
+    k_rmsnorm_rows<<<1, 256, 0, s>>>(S.X + (size_t)(n - 1) * h, m.out_norm, c.rms_eps, h, a1.out());
+    count_launch(m);
+    float* lg = logits ? logits : S.q8part + (S.q8part_bytes / 4 - (size_t)c.vocab);
+    GemmEpi eh{};
+    eh.mode = EPI_STORE;
+    eh.n_out = c.vocab;
+    eh.out_f32 = lg;
+    chk(gemm<TW>(m, s, a1, (const TW*)m.head, 1, c.vocab, h, eh, 1, 1, m.q_head));
+    if (d_argmax) {
+      k_argmax_rows<<<1, 1024, 0, s>>>(lg, c.vocab, d_argmax);
+      count_launch(m);
+    }
+  } else if (logits || d_argmax) {
+    launch_lmhead(m, s, S.X + (size_t)(n - 1) * h, logits, d_argmax);
+  }
   return err;
 }
 
@@ -915,7 +959,7 @@ static cudaError_t decode_rows(const Model& m, cudaStream_t s, int B, float* log
       e.kv_rows = i8 ? nullptr : S.b_rows;
       const float2* rope = e.rope;
       if (c.qk_norm) e.rope = nullptr;
-      chk(gemm<TW>(m, s, a_h, (const TW*)L.wqkv, B, qd + 2 * kd, h, e, 1, B));
+      chk(gemm<TW>(m, s, a_h, (const TW*)L.wqkv, B, qd + 2 * kd, h, e, 1, B, L.q_wqkv));
       if (c.qk_norm) qk_norm_rows(m, s, L, B, (float*)e.k_dst, e.kv_rows, 0, false, rope);
     }
     if (i8) {
@@ -938,7 +982,7 @@ static cudaError_t decode_rows(const Model& m, cudaStream_t s, int B, float* log
     e.mode = EPI_STORE;
     e.n_out = c.vocab;
     e.out_f32 = logits;
-    chk(gemm<TW>(m, s, a_h, (const TW*)m.head, B, c.vocab, h, e, 1, B));
+    chk(gemm<TW>(m, s, a_h, (const TW*)m.head, B, c.vocab, h, e, 1, B, m.q_head));
   }
   if (d_argmax) {
     k_argmax_rows<<<B, 1024, 0, s>>>(logits, c.vocab, d_argmax);

@@ -43,6 +43,13 @@ struct MkLayer {
   void* vc;
 };
 
+// An 8-bit projection matrix (weight_quant = 1): int8 codes [rows][cols] and one
+// f32 scale per 32 columns [rows][cols / 32]; the weight is float32(code * scale).
+struct QMat {
+  const int8_t* codes;   // nullptr: the matrix is used as given
+  const float* scales;
+};
+
 struct LayerPtrs {
   const float* attn_norm;
   const void* wqkv;
@@ -58,6 +65,7 @@ struct LayerPtrs {
   const float* k_norm;
   const float* post_attn_norm;  // sandwich norms (nullable)
   const float* post_ffn_norm;
+  QMat q_wqkv, q_wo, q_gateup, q_down;   // weight_quant = 1: the quantised projections
 };
 
 // bf16 (hi, lo) operand planes of the tensor-core prefill attention; plane
@@ -113,6 +121,12 @@ struct Scratch {
   float* kpart;         // split-K partial sums of the tensor-core GEMMs
   size_t kpart_bytes;
   float* Z;             // [T][h] block output before its post norm (sandwich norms)
+  // weight_quant = 1: one matrix expanded for the row GEMMs (bf16 hi, lo planes, or
+  // f32 for f32 models) and the two planes' products before their shared epilogue.
+  void* deq;
+  size_t deq_bytes;
+  float* q8part;
+  size_t q8part_bytes;
 };
 
 constexpr int LM_GRID_MAX = 1024;
@@ -163,6 +177,8 @@ struct Model {
   int ring_rows;        // rows of one sequence's ring (max_seq rounded up to 64)
   size_t ring_bytes;    // bytes of one sequence's K (or V) ring of one layer
   int num_sms;
+  bool wq8;             // weight_quant = 1
+  QMat q_head;          // the quantised LM head (untied), else no codes
 };
 
 // Workspace plan: byte offsets of every region; total size.
@@ -181,6 +197,8 @@ struct WsPlan {
   size_t page_table;                      // paged cache: [n_seqs][pages_per_seq] int32
   int pages_per_seq;
   size_t qk_perm;                       // kHalf + QK-norm: permuted norm weights
+  size_t q8, q8_bytes;                  // weight_quant: codes and scales of every quantised matrix
+  size_t deq, deq_bytes, q8part, q8part_bytes;
   size_t kv;            // start of the KV rings: [layer][K, V][seq][ring_rows][n_kv*hd]
   size_t kv_layer_bytes; // one layer's K (or V) rings of every sequence
   size_t ring_bytes;    // one sequence's ring
@@ -273,6 +291,18 @@ void launch_set_pages(int32_t* table, const PageSet& ps, cudaStream_t s);
 // Streaming multiprocessors of the current device, queried once per device (1 when
 // no device can be queried).  Grid sizes follow it rather than a fixed part.
 int device_sm_count();
+
+// 8-bit projection weights (weight_int8.cu).
+// Quantises rows [rows][cols] (cols % 32 == 0) of w (f32 or bf16) into codes and scales.
+cudaError_t launch_weight_quant(const void* w, bool w_bf16, size_t rows, int cols, int8_t* codes, float* scales,
+                                cudaStream_t s);
+// Sum of `planes` f32 partial planes [planes][M][N] in order, then the GEMM epilogue e.
+struct GemmEpi;
+cudaError_t launch_sum_planes_epi(const float* part, int planes, int M, int N, const GemmEpi& e, cudaStream_t s);
+// Expands rows [rows][cols] of q into bf16 (hi, lo) planes (hi + lo ~ code * s), or into f32.
+cudaError_t launch_weight_dequant_hilo(const QMat& q, size_t rows, int cols, __nv_bfloat16* hi,
+                                       __nv_bfloat16* lo, cudaStream_t s);
+cudaError_t launch_weight_dequant_f32(const QMat& q, size_t rows, int cols, float* out, cudaStream_t s);
 
 // Persistent single-kernel decode step (decode_mk.cu).
 size_t mk_smem_bytes(const dec_config& c, int nsplit);

@@ -31,7 +31,8 @@ EXPORTED = ["dec_config_validate", "dec_workspace_bytes", "dec_create", "dec_pre
             "dec_check", "dec_timing_enable", "dec_timing_read", "dec_launch_count", "dec_destroy",
             "dec_last_error", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc", "dec_gemm_bf16", "dec_set_graph", "dec_set_fused", "dec_fused_available", "dec_fused_mode", "dec_phase_stamps",
             "dec_prefill_seq", "dec_kv_reset_seq", "dec_length_seq", "dec_decode_batch", "dec_kv_layer_seq",
-            "dec_kv_quantize_int8", "dec_kv_slot", "dec_pages_free", "dec_selftest_wait_timeout"]
+            "dec_kv_quantize_int8", "dec_kv_slot", "dec_pages_free", "dec_selftest_wait_timeout",
+            "dec_weight_quantize_int8"]
 DEC_SITE_SELFTEST = 901
 
 KERNEL_CLASSES = {"qkv": 1, "attn": 2, "oproj": 3, "gateup": 4, "down": 5, "lmhead": 6, "router": 7,
@@ -49,7 +50,7 @@ class Config(ctypes.Structure):
         ("rope_half", ctypes.c_int32), ("rope_dim", ctypes.c_int32), ("n_seqs", ctypes.c_int32),
         ("qk_norm", ctypes.c_int32), ("sandwich_norms", ctypes.c_int32),
         ("rope_theta_local", ctypes.c_float), ("rope_global_every", ctypes.c_int32),
-        ("page_size", ctypes.c_int32), ("n_pages", ctypes.c_int32)]
+        ("page_size", ctypes.c_int32), ("n_pages", ctypes.c_int32), ("weight_quant", ctypes.c_int32)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -103,6 +104,7 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "dec_kv_slot": (I32, [P, I32, I32, I32, ctypes.POINTER(P), ctypes.POINTER(P)]),
         "dec_pages_free": (I32, [P]),
         "dec_selftest_wait_timeout": (I32, [P, I32]),
+        "dec_weight_quantize_int8": (I32, [P, I32, ctypes.c_int64, I32, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -149,6 +151,7 @@ def make_config(w: dict, kv_dtype: str = "f32", max_tokens: int = 0, n_seqs: int
     c.rope_global_every = int(w.get("rope_global_every", 0) or 0)
     c.page_size = int(page_size)
     c.n_pages = int(n_pages)
+    c.weight_quant = 1 if w.get("weight_int8") else 0
     return c
 
 
@@ -229,6 +232,21 @@ def kv_quantize_int8(x: torch.Tensor, n_kv_heads: int, head_dim: int,
     if st != DEC_OK:
         raise DecError(st, lib.dec_last_error(None).decode())
     return out
+
+
+def weight_quantize_int8(w: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> tuple:
+    """dec_weight_quantize_int8 on a device matrix [rows, cols] (f32 or bf16) -> (codes int8 [rows, cols],
+    scales f32 [rows, cols / 32])."""
+    rows, cols = w.shape
+    codes = torch.empty((rows, cols), dtype=torch.int8, device=w.device)
+    scales = torch.empty((rows, cols // 32), dtype=torch.float32, device=w.device)
+    wd = DEC_F32 if w.dtype == torch.float32 else DEC_BF16
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = lib.dec_weight_quantize_int8(w.data_ptr(), wd, rows, cols, codes.data_ptr(), scales.data_ptr(),
+                                      ctypes.c_void_p(s.cuda_stream))
+    if st != DEC_OK:
+        raise DecError(st, lib.dec_last_error(None).decode())
+    return codes, scales
 
 
 def attend_scratch_bytes(nq: int, nkv: int, hd: int, max_seq: int) -> int:
@@ -315,6 +333,9 @@ class Decoder:
         self.ws_bytes = workspace_bytes(self.cfg)
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
         self.stream = stream if stream is not None else torch.cuda.Stream(device=self.device)
+        # dec_create may read the weights on the handle's stream (quantise, permute):
+        # it must see them complete, so it waits for the stream they were drawn on.
+        self.stream.wait_stream(torch.cuda.current_stream(self.device))
         self.kv_dtype = kv_dtype
         self.kv_torch_dtype = {"f32": torch.float32, "bf16": torch.bfloat16, "i8": torch.uint8}[kv_dtype]
         h = ctypes.c_void_p()

@@ -124,6 +124,16 @@ typedef struct dec_config {
                              are free fails with DEC_ENOMEM before anything changes.  Decode of a paged cache
                              runs the row kernels */
   int32_t n_pages;        /* pages in the arena (with page_size > 0) */
+  int32_t weight_quant;   /* 0: projections used as given.  1: 8-bit projection weights (Pantheon "Llama Forward
+                             Pass", weight modes: the projections stay quantised and are expanded a block at a
+                             time): dec_create quantises Wq|Wk|Wv, Wo, gate/up, down (every expert) and an untied
+                             LM head into the workspace, each row in groups of 32 input columns as
+                             round(w / s) with s = max|w| / 127 (the int8 rule the pages give for the cache;
+                             float32 arithmetic, round = halves away from zero, codes in [-127, 127]), and
+                             every later call reads those codes and scales: the forward pass uses
+                             float32(code * s).  Embeddings, norms, biases and the router stay as given.
+                             hidden, ffn and n_heads * head_dim must be multiples of 32.  The projection
+                             pointers are read by dec_create only */
 } dec_config;
 
 /*
@@ -166,8 +176,11 @@ size_t dec_workspace_bytes(const dec_config *cfg);
 /* Creates a handle.  workspace: device, >= dec_workspace_bytes(cfg) bytes,
  * 256-byte aligned, owned by the caller.  cuda_stream: a cudaStream_t (NULL =
  * legacy default stream).  Weights are validated for presence and 16-byte
- * alignment.  Errors: DEC_EINVAL (config, NULL or misaligned pointers),
- * DEC_ENOMEM (workspace too small), DEC_ECUDA. */
+ * alignment.  The weights must be complete when work on cuda_stream starts:
+ * dec_create itself enqueues kernels that read them (8-bit quantisation, the
+ * kHalf row permutation), so a caller that wrote them on another stream makes
+ * cuda_stream wait for it first.  Errors: DEC_EINVAL (config, NULL or
+ * misaligned pointers), DEC_ENOMEM (workspace too small), DEC_ECUDA. */
 dec_status dec_create(const dec_config *cfg, const dec_weights *weights, void *workspace,
                       size_t workspace_bytes, void *cuda_stream, dec_handle **out);
 
@@ -393,6 +406,14 @@ dec_status dec_attend_noalloc(const float *q, const void *k, const void *v, int3
                               int32_t n_kv_heads, int32_t head_dim, int32_t max_seq,
                               int32_t sliding_window, int32_t kv_dtype, int32_t pos, float *out,
                               void *cuda_stream);
+
+/* The 8-bit weight quantiser of weight_quant = 1, callable alone: w (device,
+ * [rows][cols] of weight_dtype DEC_F32 or DEC_BF16, row-major) -> codes (device
+ * int8 [rows][cols]) and scales (device f32 [rows][cols / 32]); cols a multiple
+ * of 32.  Enqueued on cuda_stream.  Errors: DEC_EINVAL, DEC_ECUDA (messages via
+ * dec_last_error(NULL)). */
+dec_status dec_weight_quantize_int8(const void *w, int32_t weight_dtype, int64_t rows, int32_t cols, int8_t *codes,
+                                    float *scales, void *cuda_stream);
 
 /* The int8 K/V quantiser of the cache, callable alone: rows x (device,
  * [n_rows][n_kv_heads * head_dim] f32) -> out (device, n_rows rows of the
