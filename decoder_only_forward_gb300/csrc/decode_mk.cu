@@ -470,7 +470,17 @@ __device__ void mk_fetch(const float* src, int K, float* dst) {
 
 // Element k of the activation as a bf16 (hi, lo) pair: the B operand of the
 // tensor-core GEMV (x = hi + lo to ~16 bits).
-__device__ __forceinline__ void mk_put_xb(__nv_bfloat16* xb, int plane, int k, float v) {
+// With f16 (8-bit weight phases) the pair is two halves instead: hi = f16(v),
+// lo = f16(v - hi), about 22 bits for |v| >= 2^-3 and an absolute error below
+// 2^-25 below that.
+__device__ __forceinline__ void mk_put_xb(__nv_bfloat16* xb, int plane, int k, float v, bool f16 = false) {
+  if (f16) {
+    __half* xh = reinterpret_cast<__half*>(xb);
+    const __half hi = __float2half_rn(v);
+    xh[k] = hi;
+    xh[plane + k] = __float2half_rn(v - __half2float(hi));
+    return;
+  }
   const __nv_bfloat16 hi = __float2bfloat16_rn(v);
   xb[k] = hi;
   xb[plane + k] = __float2bfloat16_rn(v - __bfloat162float(hi));
@@ -481,7 +491,8 @@ __device__ __forceinline__ void mk_put_xb(__nv_bfloat16* xb, int plane, int k, f
 // result also goes to the bf16 (hi, lo) planes, zero-padded to kpad columns.
 template <typename W>
 __device__ void mk_norm_to_xs(const float* x, const W* erow, const float* __restrict__ wn, int K, float eps,
-                              float* xs, MkMisc* M, __nv_bfloat16* xb = nullptr, int plane = 0, int kpad = 0) {
+                              float* xs, MkMisc* M, __nv_bfloat16* xb = nullptr, int plane = 0, int kpad = 0,
+                              bool f16 = false) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (erow) {
     for (int k = tid; k < K; k += MK_COMPUTE) xs[k] = to_f32(erow[k]);
@@ -516,7 +527,7 @@ __device__ void mk_norm_to_xs(const float* x, const W* erow, const float* __rest
       if (k >= kend) break;
       const float v = k < K ? xs[k] * inv * wv[u] : 0.f;
       if (k < K) xs[k] = v;
-      if (xb) mk_put_xb(xb, plane, k, v);
+      if (xb) mk_put_xb(xb, plane, k, v, f16);
     }
   }
   compute_sync();
@@ -733,18 +744,26 @@ __device__ __forceinline__ void mk_mma_bf16(float* d, uint32_t a0, uint32_t a1, 
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Four int8 codes (one 32-bit word, bytes = consecutive columns) -> two bf16
-// pairs, exactly: a code c is biased to c + 128, placed as the low byte of the
-// float 2^23 + (c + 128), and 2^23 + 128 is subtracted; a small integer's f32
-// bits are its bf16 bits in the upper half.
-__device__ __forceinline__ void mk_q8_bf16x2(uint32_t u, uint32_t& lo2, uint32_t& hi2) {
+// Four int8 codes (one 32-bit word, bytes = consecutive columns) -> two f16
+// pairs, exactly: each code is biased by 128 and becomes the low byte of the
+// half 1024 + (c + 128), two halves per byte permute, and one paired
+// subtraction of 1152 leaves c exactly.
+__device__ __forceinline__ void mk_q8_f16x2(uint32_t u, uint32_t& lo2, uint32_t& hi2) {
   const uint32_t v = u ^ 0x80808080u;
-  const float f0 = __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7440)) - 8388736.0f;
-  const float f1 = __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7441)) - 8388736.0f;
-  const float f2 = __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7442)) - 8388736.0f;
-  const float f3 = __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7443)) - 8388736.0f;
-  lo2 = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
-  hi2 = __byte_perm(__float_as_uint(f2), __float_as_uint(f3), 0x7632);
+  const uint32_t bias = 0x64806480u;   // (1152, 1152) as halves
+  const uint32_t p01 = __byte_perm(v, 0x64646464u, 0x4140), p23 = __byte_perm(v, 0x64646464u, 0x4342);
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo2) : "r"(p01), "r"(bias));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi2) : "r"(p23), "r"(bias));
+}
+
+// d (16x8 f32) += a (16x16 f16, row) . b (16x8 f16, col).
+__device__ __forceinline__ void mk_mma_f16(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // One stage of 8-bit weights: 16 rows x MK_QKG codes (two 128-column boxes,
@@ -773,11 +792,11 @@ __device__ __forceinline__ void mk_q8_stage(const uint8_t* tile, int kb, int grp
         asm volatile("ld.shared.u32 %0, [%1];" : "=r"(u0) : "r"(r0 + ((ks ^ sw0) << 4)));
         asm volatile("ld.shared.u32 %0, [%1];" : "=r"(u8) : "r"(r8 + ((ks ^ sw8) << 4)));
         uint32_t a0, a1, a2, a3;
-        mk_q8_bf16x2(u0, a0, a2);
-        mk_q8_bf16x2(u8, a1, a3);
+        mk_q8_f16x2(u0, a0, a2);
+        mk_q8_f16x2(u8, a1, a3);
         const int k0 = kb * MK_QKG + j * 128 + (int)ks * 16 + 4 * t4;
-        const uint2 bv = bl ? *reinterpret_cast<const uint2*>(xbl + k0) : make_uint2(0u, 0u);
-        mk_mma_bf16(dg, a0, a1, a2, a3, bv.x, bv.y);
+        const uint2 bv = bl ? *reinterpret_cast<const uint2*>(xbl + k0) : make_uint2(0u, 0u);   // f16 planes
+        mk_mma_f16(dg, a0, a1, a2, a3, bv.x, bv.y);
       }
       const int gi = j * 4 + g;
       d[0] = fmaf(sc[grp * 8 + gi], dg[0] + dg[1], d[0]);
@@ -804,7 +823,7 @@ __device__ __forceinline__ bool compute_sync_or(bool pred) {
 // The activation vector as bf16 (hi, lo) planes, zero-padded to whole column
 // groups.  A global source (the FFN activation, K a multiple of 4) is read
 // as float4, four loads in flight per thread.
-__device__ void mk_to_xb(const float* src, bool src_global, int K, __nv_bfloat16* xb, int plane) {
+__device__ void mk_to_xb(const float* src, bool src_global, int K, __nv_bfloat16* xb, int plane, bool f16 = false) {
   const int KP = (K + MK_PADK - 1) / MK_PADK * MK_PADK;
   if (src_global) {
     const int nv = K >> 2, np = KP >> 2;
@@ -819,15 +838,15 @@ __device__ void mk_to_xb(const float* src, bool src_global, int K, __nv_bfloat16
       for (int u = 0; u < 4; ++u) {
         const int i = i0 + u * MK_COMPUTE;
         if (i < np) {
-          mk_put_xb(xb, plane, 4 * i, v[u].x);
-          mk_put_xb(xb, plane, 4 * i + 1, v[u].y);
-          mk_put_xb(xb, plane, 4 * i + 2, v[u].z);
-          mk_put_xb(xb, plane, 4 * i + 3, v[u].w);
+          mk_put_xb(xb, plane, 4 * i, v[u].x, f16);
+          mk_put_xb(xb, plane, 4 * i + 1, v[u].y, f16);
+          mk_put_xb(xb, plane, 4 * i + 2, v[u].z, f16);
+          mk_put_xb(xb, plane, 4 * i + 3, v[u].w, f16);
         }
       }
     }
   } else {
-    for (int k = threadIdx.x; k < KP; k += MK_COMPUTE) mk_put_xb(xb, plane, k, k < K ? src[k] : 0.f);
+    for (int k = threadIdx.x; k < KP; k += MK_COMPUTE) mk_put_xb(xb, plane, k, k < K ? src[k] : 0.f, f16);
   }
   compute_sync();
 }
@@ -985,7 +1004,7 @@ __device__ bool mk_gemv_phase(const MkParams& P, int ph, int l, const MkRows& R,
       if (ph == PH_DOWN) {
         // The activation this segment multiplies (MoE: its expert slot's).
         compute_sync();
-        mk_to_xb(P.act + (size_t)(P.E > 0 ? S.slot : 0) * P.f, true, P.f, xb, P.xb_plane);
+        mk_to_xb(P.act + (size_t)(P.E > 0 ? S.slot : 0) * P.f, true, P.f, xb, P.xb_plane, q8);
       }
       const int nblk = (S.rows + MK_TM - 1) / MK_TM;
       for (int c0 = 0; c0 < nblk; c0 += MK_CHUNK) {
@@ -1840,6 +1859,7 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
   float* xs = reinterpret_cast<float*>(ureg);
   // Tensor-core GEMV operand: the activation as bf16 (hi, lo) planes after xs.
   constexpr bool MMA = MkRing<W>::MMA;
+  constexpr bool Q8 = MkRing<W>::Q8;   // 8-bit phases take the activation as f16 (hi, lo) planes
   __nv_bfloat16* xb = reinterpret_cast<__nv_bfloat16*>(xs + P.xs_floats);
   const int kpad_h = (P.h + MK_PADK - 1) / MK_PADK * MK_PADK;
   // ---------------- compute warps
@@ -1866,7 +1886,7 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
     switch (ph) {
       case PH_QKV:
         mk_norm_to_xs<typename MkElem<W>::T>(P.x, l == 0 ? (const typename MkElem<W>::T*)P.embed + (size_t)token * P.h : nullptr, L.attn_norm, P.h, P.eps,
-                         xs, M, MMA ? xb : nullptr, P.xb_plane, kpad_h);
+                         xs, M, MMA ? xb : nullptr, P.xb_plane, kpad_h, Q8);
         break;
       case PH_ATTN:
         if (P.attn_warp) ok = mk_attention_warp_any<W, KV, HD>(P, l, ring, ureg, M, sc);
@@ -1880,10 +1900,11 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
         if (!P.attn_warp && P.nsplit > 1 && !P.merge_phase)
           mk_merge_heads(P.part, P.nsplit, HD, 0, P.nq, xs + qd, xs, false);
         else mk_copy_to_xs(P.attn, qd, xs);
-        if (MMA) mk_to_xb(xs, false, qd, xb, P.xb_plane);
+        if (MMA) mk_to_xb(xs, false, qd, xb, P.xb_plane, Q8);
         break;
       case PH_GATEUP:
-        mk_norm_to_xs<typename MkElem<W>::T>(P.x, nullptr, L.ffn_norm, P.h, P.eps, xs, M, MMA ? xb : nullptr, P.xb_plane, kpad_h);
+        mk_norm_to_xs<typename MkElem<W>::T>(P.x, nullptr, L.ffn_norm, P.h, P.eps, xs, M, MMA ? xb : nullptr, P.xb_plane, kpad_h,
+                                             Q8);
         if (P.E > 0) mk_router<typename MkElem<W>::T>(P, l, xs, M);
         break;
       case PH_DOWN:
@@ -1891,7 +1912,8 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
         if (!MMA && P.E == 0) mk_copy_to_xs(P.act, P.f, xs);
         break;
       case PH_LMHEAD:
-        mk_norm_to_xs<typename MkElem<W>::T>(P.x, nullptr, P.out_norm, P.h, P.eps, xs, M, MMA ? xb : nullptr, P.xb_plane, kpad_h);
+        mk_norm_to_xs<typename MkElem<W>::T>(P.x, nullptr, P.out_norm, P.h, P.eps, xs, M, MMA ? xb : nullptr, P.xb_plane, kpad_h,
+                                             Q8 && P.head_q8);
         break;
     }
     if (mk_is_gemv(ph)) {
