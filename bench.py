@@ -102,6 +102,9 @@ TRAFFIC = {
     ("smollm2-135m", "down"): {
         "bytes": 1814336, "source": "decoder_only_forward_gb300/csrc/decode.cu",
         "sha256": "3d7213fecd5001252701110382d8e9dfd57676011ecc1ded9bf6666198c7ae34"},
+    ("mixtral-8x7b", "step"): {
+        "bytes": 26194874880, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
+        "sha256": "c5a126ed56d888fe8bf125af5601570dd900a0794d82889308d8ccc9b159dd58"},
     ("mistral-7b", "step"): {
         "bytes": 15712395008, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
         "sha256": "4bf7258819f5eaeff409afa95ceaa4deb2af4270224b2c6b5de9309906a0eb17"},
@@ -295,7 +298,17 @@ def oracle_sample_text(name: str, w: dict, plan: dict, cores: int) -> str:
 
 
 # ---------------------------------------------------------------- our arm
-PER_WORKLOAD_DEFAULT = ["smollm2-135m", "qwen2.5-0.5b", "mistral-7b", "mixtral-8x7b"]
+PER_WORKLOAD_DEFAULT = ["smollm2-135m", "qwen2.5-0.5b", "mistral-7b", "mixtral-8x7b",
+                        "mixtral-8x7b+int8_weights"]
+
+
+def named_workload(name: str) -> dict:
+    """A named workload, or one with a variant suffix ("+int8_weights": 8-bit projections)."""
+    base, _, variant = name.partition("+")
+    kw = {"weight_int8": True} if variant == "int8_weights" else {}
+    if variant and not kw:
+        raise ValueError(f"unknown workload variant {variant!r}")
+    return synthetic.workload(base, **kw)
 
 
 def gemm_flops(w: dict, P: int) -> float:
@@ -566,7 +579,7 @@ def run_ours(args, rank, world, local_rank):
                 per[nm] = {"same_as_main_line": True}
                 continue
             torch.cuda.empty_cache()
-            wn = synthetic.workload(nm)
+            wn = named_workload(nm)
             rn = measure_workload(nm, wn, dev, args, args.per_workload_steps, 3, want_e2e_steps=1,
                                   attribution=False)
             per[nm] = workload_summary(nm, wn, rn, 1, hbm, tf, tf_sus)
