@@ -1282,28 +1282,38 @@ __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8
   (void)tasks;
   for (int j0 = 0; j0 < nsub; j0 += MK_COMPUTE_WARPS) {
    const int j = j0 + warp;
-   int t, g, split, s0, j1;
-   if (j < nsub && mk_attn_sub(P, A, j, S, m, t, g, split, s0, j1)) {
-    float qv[GP][DPL], acc[GP][DPL];
+   int t, g = 0, split, s0 = 0, j1 = 0;
+   const bool task = j < nsub && mk_attn_sub(P, A, j, S, m, t, g, split, s0, j1);
+   // The query rows and the current position's K/V row (written by this step's
+   // QKV phase, possibly after the producer copied the slot, so read from global
+   // memory once) are all requested before any of them is used.
+   float qv[GP][DPL], kcur[DPL], vcur[DPL];
+   const bool has_cur = task && slot_pos >= s0 && slot_pos < j1;
+   if (task) {
+#pragma unroll
+    for (int h = 0; h < GP; ++h)
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) qv[h][d] = h < G ? __ldcg(P.q + (size_t)(g * G + h) * HD + lane * DPL + d) : 0.f;
+    const size_t co = (size_t)(has_cur ? slot_pos : 0) * kd + (size_t)g * HD + lane * DPL;
+    mk_load_dims<KV, DPL>(kc + co, kcur, true);
+    mk_load_dims<KV, DPL>(vc + co, vcur, true);
+   }
+   if (task) {
+    // (the scaling below is the first use of the loads above)
+    float acc[GP][DPL];
 #pragma unroll
     for (int h = 0; h < GP; ++h)
 #pragma unroll
       for (int d = 0; d < DPL; ++d) {
-        qv[h][d] = h < G ? __ldcg(P.q + (size_t)(g * G + h) * HD + lane * DPL + d) * qscale : 0.f;
+        qv[h][d] *= qscale;
         acc[h][d] = 0.f;
       }
-    float mown = -INFINITY, lown = 0.f;   // running max / sum of head `own`
-    // The current position's row was written by this step's QKV phase, possibly
-    // after the producer copied the slot: it is read from global memory once.
-    float kcur[DPL], vcur[DPL];
-    const bool has_cur = slot_pos >= s0 && slot_pos < j1;
-    if (has_cur) {
-      mk_load_dims<KV, DPL>(kc + (size_t)slot_pos * kd + (size_t)g * HD + lane * DPL, kcur, true);
-      mk_load_dims<KV, DPL>(vc + (size_t)slot_pos * kd + (size_t)g * HD + lane * DPL, vcur, true);
-    } else {
 #pragma unroll
-      for (int d = 0; d < DPL; ++d) kcur[d] = vcur[d] = 0.f;
+    for (int d = 0; d < DPL; ++d) {
+      kcur[d] = has_cur ? kcur[d] : 0.f;
+      vcur[d] = has_cur ? vcur[d] : 0.f;
     }
+    float mown = -INFINITY, lown = 0.f;   // running max / sum of head `own`
     const uint32_t lane_off = (uint32_t)(lane * DPL * (int)sizeof(KV));
     for (int c0 = s0; c0 < j1; c0 += RPP) {
       const int nk = min(RPP, j1 - c0);
