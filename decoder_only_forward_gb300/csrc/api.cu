@@ -314,6 +314,14 @@ WsPlan dec::plan_workspace(const dec_config& c) {
     p.q8part_bytes = wq ? 2 * 4 * mn + 4 * (size_t)c.vocab : 0;
     p.q8part = take(p.q8part_bytes);
   }
+  // Persistent decode with a fused FFN: every down projection transposed
+  // ([expert][ffn][hidden], bf16) and the per-CTA partial sums of its product.
+  {
+    const bool ft = mk_ffn_fused_layout(c);
+    const size_t E1 = c.n_experts ? (size_t)c.n_experts : 1;
+    p.wdown_t = take(ft ? (size_t)c.n_layers * E1 * c.ffn * c.hidden * 2 : 0);
+    p.fpart = take(ft ? (size_t)MK_MAX_NB * c.hidden * 4 : 0);
+  }
   // KV rings: [layer][K, V][seq][ring_rows][n_kv*hd], ring_rows = max_seq
   // rounded up to 64 rows so every ring starts 256-byte aligned.
   p.n_seqs = c.n_seqs > 0 ? c.n_seqs : 1;
@@ -488,6 +496,25 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
     d.post_attn_norm = cfg->sandwich_norms ? (const float*)L.post_attn_norm : nullptr;
     d.post_ffn_norm = cfg->sandwich_norms ? (const float*)L.post_ffn_norm : nullptr;
     d.q_wqkv = d.q_wo = d.q_gateup = d.q_down = QMat{nullptr, nullptr};
+    d.w_down_t = nullptr;
+  }
+  S.fpart = nullptr;
+  if (mk_ffn_fused_layout(*cfg)) {
+    // The persistent step's fused FFN reads each layer's down projection transposed.
+    const size_t E1 = cfg->n_experts ? (size_t)cfg->n_experts : 1;
+    const size_t lbytes = E1 * cfg->ffn * cfg->hidden * 2;
+    cudaError_t te = cudaSuccess;
+    for (int l = 0; l < cfg->n_layers && te == cudaSuccess; ++l) {
+      LayerPtrs& d = h->layers[l];
+      char* dst = base + p.wdown_t + (size_t)l * lbytes;
+      te = launch_transpose_bf16(d.w_down, cfg->hidden, cfg->ffn, (int)E1, dst, h->stream);
+      d.w_down_t = dst;
+    }
+    if (te != cudaSuccess) {
+      delete h;
+      return fail(nullptr, DEC_ECUDA, "down-projection transpose: %s", cudaGetErrorString(te));
+    }
+    S.fpart = (float*)(base + p.fpart);
   }
   if (cfg->rope_half) {
     // kHalf pairs (i, i + d/2) become adjacent pairs (2i, 2i+1) on q/k rows

@@ -81,10 +81,13 @@ template <> struct MkElem<WQ8> { using T = __nv_bfloat16; };
 // Activation planes are zero-padded to whole stages of either path.
 constexpr int MK_PADK = 256;
 constexpr int MK_CHUNK = 8;                         // row blocks reduced together (partials in smem)
+// Fused FFN: a CTA owns a contiguous range of ffn tasks (slot, ffn index), a
+// multiple of MK_FTS of them and at most MK_FT.
+constexpr int MK_FTS = 16, MK_FT = 256;
 // Tensor maps per layer (bf16 weights): QKV, O, gate/up, down, and the K and V
 // rings (3D: head_dim x kv heads x slots, one box = one attention piece); then the head.
 enum MkMap { MAP_QKV = 0, MAP_O, MAP_GATEUP, MAP_DOWN, MAP_K, MAP_V,
-             MAP_QKV_S, MAP_O_S, MAP_GATEUP_S, MAP_DOWN_S, MAPS_PER_LAYER };
+             MAP_QKV_S, MAP_O_S, MAP_GATEUP_S, MAP_DOWN_S, MAP_DOWN_T, MAPS_PER_LAYER };
 constexpr int MAP_SCALE_OFF = MAP_QKV_S - MAP_QKV;   // a projection's scale map, 8-bit weights
 // After the layers: the head, then (8-bit untied head) its scales.
 
@@ -124,6 +127,8 @@ struct MkParams {
   int attn_warp;                  // attention as per-warp tasks fed by the producer rings
   int attn_ns;                    // warp-task attention: target splits per kv head (<= 32)
   int head_q8;                    // 8-bit weights: the LM head is quantised too (untied)
+  int ffn_fused;                  // FFN as one phase over ffn slices + a partial-sum phase (below)
+  float* fpart;                   // fused FFN: [nb][h] per-CTA partial sums of the down projection
 };
 
 // Shared-memory bookkeeping after the weight ring and the union region.
@@ -147,6 +152,8 @@ struct MkMisc {
   float mrow[MAX_GROUP], lrow[MAX_GROUP], alpha[MAX_GROUP];
   float mscale[8 * 32];          // warp-task attention merge: weight of split s for query head h
   int lastg[MK_COMPUTE_WARPS];   // kv heads whose last split this CTA finished in the current round
+  float fact[MK_FT];             // fused FFN: this CTA's SwiGLU outputs (router-weighted)
+  __nv_bfloat16 fxb[2][MK_FT];   // fused FFN: the same as bf16 (hi, lo) planes
   uint64_t cbar;                 // cluster mode: phase barrier, one arrival per CTA of the cluster
   unsigned cgen;                 // cluster mode: barrier instances completed
 };
@@ -328,7 +335,9 @@ struct MkRows {
   bool paired;
 };
 
-__device__ __forceinline__ bool mk_is_gemv(int ph) { return ph != PH_ATTN && ph != PH_MERGE; }
+__device__ __forceinline__ bool mk_is_gemv(const MkParams& P, int ph) {
+  return ph != PH_ATTN && ph != PH_MERGE && !(ph == PH_DOWN && P.ffn_fused);
+}
 
 // ceil(n / nb) rounded up to a multiple of g.
 __device__ __forceinline__ int mk_share(int n, int nb, int g) { return ((n + nb - 1) / nb + g - 1) / g * g; }
@@ -361,20 +370,24 @@ __device__ void mk_phase_rows(const MkParams& P, int ph, int l, const int* ids, 
     case PH_OPROJ: single(L.wo, P.h, qd, mbase + MAP_O); break;
     case PH_LMHEAD: single(P.head, P.V, P.h, P.n_layers * MAPS_PER_LAYER); break;
     case PH_GATEUP:
-      if (P.E == 0) {
+      if (P.E == 0 && !P.ffn_fused) {
         paired(L.w_gateup, 2 * P.f, P.h, mbase + MAP_GATEUP);
       } else {
         // Tasks = (slot, gate/up row pair), slot-major, split evenly over CTAs.
-        const int T = P.k * P.f, per = mk_share(T, nb, (g + 1) / 2);
+        // Fused FFN: shares of MK_FTS tasks, and out0 = the segment's first task
+        // within the CTA's own range.
+        const int T = P.k * P.f, per = mk_share(T, nb, P.ffn_fused ? MK_FTS : (g + 1) / 2);
         const int t0 = min(T, b * per), t1 = min(T, t0 + per);
         R.K = P.h;
         R.paired = true;
         for (int j = 0; j < P.k; ++j) {
           const int a = max(t0, j * P.f), e = min(t1, (j + 1) * P.f);
           if (e <= a) continue;
-          const uint8_t* base = (const uint8_t*)L.w_gateup + (size_t)ids[j] * 2 * P.f * P.h * es;
+          const int eid = P.E > 0 ? ids[j] : 0;
+          const uint8_t* base = (const uint8_t*)L.w_gateup + (size_t)eid * 2 * P.f * P.h * es;
           const int r0 = 2 * (a - j * P.f);
-          R.seg[R.nseg++] = MkSeg{base, r0, 2 * (e - a), a, j, mbase + MAP_GATEUP, ids[j] * 2 * P.f + r0};
+          R.seg[R.nseg++] =
+              MkSeg{base, r0, 2 * (e - a), P.ffn_fused ? a - t0 : a, j, mbase + MAP_GATEUP, eid * 2 * P.f + r0};
         }
       }
       break;
@@ -675,7 +688,7 @@ __device__ __forceinline__ int mk_first_kb(int b, int KB, int w) {
 // the q / K / V stores, or SwiGLU for gate/up.
 template <typename KV>
 __device__ __forceinline__ void mk_epi_pair(const MkParams& P, int ph, const MkLayer& L, const MkSeg& S,
-                                            const MkMisc* M, int rl, float a0, float a1) {
+                                            MkMisc* M, int rl, float a0, float a1) {
   const int qd = P.nq * P.hd, kd = P.nkv * P.hd;
   if (ph == PH_QKV) {
     const int row = S.row0 + rl;
@@ -702,6 +715,8 @@ __device__ __forceinline__ void mk_epi_pair(const MkParams& P, int ph, const MkL
       dst[o] = from_f32<KV>(v0);
       dst[o + 1] = from_f32<KV>(v1);
     }
+  } else if (P.ffn_fused) {   // PH_GATEUP, fused FFN: the CTA's own task slot, times the router weight
+    M->fact[S.out0 + (rl >> 1)] = (P.E > 0 ? M->wts[S.slot] : 1.f) * (silu_f(a0) * a1);
   } else {  // PH_GATEUP: act[task] = silu(gate) * up
     const int task = P.E > 0 ? S.out0 + (rl >> 1) : (S.row0 + rl) >> 1;
     P.act[task] = silu_f(a0) * a1;
@@ -1090,9 +1105,137 @@ __device__ bool mk_gemv_phase(const MkParams& P, int ph, int l, const MkRows& R,
   return ok;
 }
 
-}  // namespace dec
+// ldmatrix.x4.trans: the four 8x8 b16 matrices whose rows lane l % 8 of lane
+// group l / 8 points to, each delivered transposed.
+__device__ __forceinline__ void mk_ldsm4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
 
-namespace dec {
+// Fused FFN, second half of its phase (Pantheon "Llama Forward Pass", feed
+// forward: down(silu(gate) * up), summed over the selected experts with their
+// router weights).  The CTA's tasks tau (its ffn slice, per expert slot) give
+// a[tau] = w_slot * silu(gate) * up (in M->fact); its share of the down
+// projection is then out[n] = sum_tau Wt[tau][n] a[tau] over the transposed copy
+// Wt of W_down (rows = ffn index, columns = hidden), written to fpart[CTA][n].
+// Warp w owns the MK_KG-column blocks w, w + 8, ...; a stage holds Wt[16 tasks]
+// [MK_KG columns] as MK_BPS 64-column boxes (128-byte swizzled).  A = (columns x
+// tasks) by ldmatrix.trans of that tile, B = a's (hi, lo) bf16 planes as columns
+// 0 and 1; column n's sum is D[n][0] + D[n][1], f32-accumulated over the tasks
+// in their order.
+template <typename W>
+__device__ bool mk_ffn_down_part(const MkParams& P, const MkRows& R, uint8_t* ring, MkMisc* M, uint32_t& sc) {
+  constexpr int NS = MkRing<W>::STAGES, SB = MkRing<W>::BYTES;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  volatile int* abort_flag = &M->abort_flag;
+  uint8_t* wring = ring + (size_t)warp * MK_WARP_RING;
+  DeviceState* const stp = P.st;
+  int ntask = 0;
+  for (int si = 0; si < R.nseg; ++si) ntask += R.seg[si].rows / 2;
+  // The activations as (hi, lo) planes (every task written by the gate/up epilogue).
+  compute_sync();
+  for (int i = tid; i < ntask; i += MK_COMPUTE) {
+    const float v = M->fact[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    M->fxb[0][i] = hi;
+    M->fxb[1][i] = __float2bfloat16_rn(v - __bfloat162float(hi));
+  }
+  compute_sync();
+  if (ntask == 0) return true;   // a CTA past the last task (its partial row is never read)
+  uint32_t scl = sc;
+  bool ok = true;
+  const int grp = lane >> 2, t4 = lane & 3;
+  const bool bl = grp < 2;
+  const __nv_bfloat16* fxbl = M->fxb[grp & 1];
+  // ldmatrix.x4.trans lane roles: matrix q = lane / 8 takes task rows (q >> 1) * 8 + lane % 8
+  // and the 8-column chunk (q & 1) of each 16-column step.
+  const int trow = ((lane >> 4) << 3) + (lane & 7), tch = (lane >> 3) & 1;
+  for (int nbk = warp; nbk < P.h / MK_KG; nbk += MK_COMPUTE_WARPS) {
+    float d[MK_BPS * 4][4];
+#pragma unroll
+    for (int i = 0; i < MK_BPS * 4; ++i) d[i][0] = d[i][1] = d[i][2] = d[i][3] = 0.f;
+    int toff = 0;
+    for (int si = 0; si < R.nseg && ok; ++si) {
+      const int ntb = R.seg[si].rows / (2 * MK_FTS);
+      for (int tb = 0; tb < ntb; ++tb) {
+        const int st = scl % NS;
+        if (!mk_mbar_wait(&M->full[warp][st], (scl / NS) & 1u, abort_flag, stp, 205)) {
+          ok = false;
+          break;
+        }
+        const uint32_t tile = mk_smem_u32(wring + (size_t)st * SB);
+        const int k0 = toff + tb * MK_FTS + 2 * t4;
+        const uint32_t b0 = bl ? *reinterpret_cast<const uint32_t*>(fxbl + k0) : 0u;
+        const uint32_t b1 = bl ? *reinterpret_cast<const uint32_t*>(fxbl + k0 + 8) : 0u;
+#pragma unroll
+        for (int j = 0; j < MK_BPS; ++j) {
+          const uint32_t base = tile + 2048u * j;
+          const uint32_t rsw = ((base >> 7) + (uint32_t)trow) & 7u;   // swizzle phase of this lane's row
+#pragma unroll
+          for (int mt = 0; mt < MK_TK / 16; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            mk_ldsm4_t(base + (uint32_t)trow * 128u + (((uint32_t)(2 * mt + tch) ^ rsw) << 4), a0, a1, a2, a3);
+            mk_mma_bf16(d[j * 4 + mt], a0, a1, a2, a3, b0, b1);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mk_mbar_arrive(&M->empty[warp][st]);
+        ++scl;
+        if (lane == 0) M->consumed[warp] = (int)scl;
+      }
+      toff += R.seg[si].rows / 2;
+    }
+    if (ok && t4 == 0) {
+      float* out = P.fpart + (size_t)blockIdx.x * P.h + (size_t)nbk * MK_KG + grp;
+#pragma unroll
+      for (int i = 0; i < MK_BPS * 4; ++i) {
+        out[16 * i] = d[i][0] + d[i][1];
+        out[16 * i + 8] = d[i][2] + d[i][3];
+      }
+    }
+  }
+  sc = scl;
+  return ok;
+}
+
+// Fused FFN, partial-sum phase: the hidden rows this CTA owns get the down
+// projection's partials of all CTAs that had tasks, summed in CTA order (8
+// interleaved running sums, then those in order), added to the residual.  Each
+// thread requests up to MK_RED_J partials (and its residual row) before adding.
+constexpr int MK_RED_J = 20;
+__device__ void mk_ffn_reduce(const MkParams& P, float* red) {
+  const int tid = threadIdx.x, g8 = tid >> 5, i = tid & 31;
+  const int T = P.k * P.f, per_t = mk_share(T, P.nb, MK_FTS);
+  const int nbusy = (T + per_t - 1) / per_t;
+  const int per = (P.h + P.nb - 1) / P.nb;
+  const int r0 = min(P.h, (int)blockIdx.x * per), r1 = min(P.h, r0 + per);
+  for (int n0 = r0; n0 < r1; n0 += 32) {
+    const int n = n0 + i;
+    const bool live = n < r1;
+    const float xo = (g8 == 0 && live) ? __ldcg(P.x + n) : 0.f;
+    float s = 0.f;
+    for (int c0 = g8; c0 < nbusy; c0 += MK_RED_J * MK_COMPUTE_WARPS) {
+      float v[MK_RED_J];
+#pragma unroll
+      for (int j = 0; j < MK_RED_J; ++j) {
+        const int c = c0 + MK_COMPUTE_WARPS * j;
+        v[j] = (live && c < nbusy) ? __ldcg(P.fpart + (size_t)c * P.h + n) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < MK_RED_J; ++j) s += v[j];
+    }
+    red[g8 * 32 + i] = s;
+    compute_sync();
+    if (tid < 32 && live) {
+      float t = 0.f;
+#pragma unroll
+      for (int g = 0; g < MK_COMPUTE_WARPS; ++g) t += red[g * 32 + tid];
+      P.x[n] = xo + t;
+    }
+    compute_sync();
+  }
+}
 
 // ------------------------------------------------------------------ attention phase, warp tasks
 // Task t = (kv head g, split) belongs to warp (t / nb) % 8 of CTA t % nb.  That
@@ -1782,7 +1925,7 @@ __device__ void mk_produce(const MkParams& P, uint8_t* ring, MkMisc* M) {
             continue;
           }
         }
-        if (!mk_is_gemv(ph)) continue;
+        if (!mk_is_gemv(P, ph)) continue;
         if (P.E > 0 && (ph == PH_GATEUP || ph == PH_DOWN)) {
           // Expert rows are known once this layer's router has run.
           const uint64_t t0 = globaltimer_ns();
@@ -1847,6 +1990,28 @@ __device__ void mk_produce(const MkParams& P, uint8_t* ring, MkMisc* M) {
                 for (int off = 0; off < R.rowbytes && ok; off += SB)
                   ok = issue(base + (size_t)r * R.rowbytes + off, min(SB, R.rowbytes - off));
             }
+          }
+        }
+        if constexpr (MkRing<W>::MMA && !MkRing<W>::Q8) {
+          // Fused FFN: then this warp's stages of the down half (mk_ffn_down_part's
+          // order): per owned column block, each segment's tasks 16 rows at a time
+          // from the transposed copy (its row = the gate/up map row / 2).
+          if (ph == PH_GATEUP && P.ffn_fused) {
+            const CUtensorMap* tmap = P.maps + (l * MAPS_PER_LAYER + MAP_DOWN_T);
+            for (int nbk = w; nbk < P.h / MK_KG && ok; nbk += MK_COMPUTE_WARPS)
+              for (int si = 0; si < R.nseg && ok; ++si) {
+                const int y0 = R.seg[si].maprow / 2, ntb = R.seg[si].rows / (2 * MK_FTS);
+                for (int tb = 0; tb < ntb && ok; ++tb) {
+                  const int st = claim((uint32_t)(2048 * MK_BPS));
+                  if (st < 0) {
+                    ok = false;
+                    break;
+                  }
+                  for (int j = 0; j < MK_BPS; ++j)
+                    tma_load_2d(wring + (size_t)st * SB + 2048 * j, tmap, &M->full[w][st], nbk * MK_KG + j * MK_TK,
+                                y0 + tb * MK_FTS);
+                }
+              }
           }
         }
       }
@@ -1926,10 +2091,15 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
                                              Q8 && P.head_q8);
         break;
     }
-    if (mk_is_gemv(ph)) {
+    if (mk_is_gemv(P, ph)) {
       MkRows R;
       mk_phase_rows<W>(P, ph, l, M->ids, R);
       ok = mk_gemv_phase<W, KV>(P, ph, l, R, ring, M, xs, sc, best, bidx);
+      if constexpr (MMA && !Q8) {
+        if (ph == PH_GATEUP && P.ffn_fused && !compute_sync_or(!ok)) ok = mk_ffn_down_part<W>(P, R, ring, M, sc);
+      }
+    } else if (ph == PH_DOWN && P.ffn_fused) {
+      mk_ffn_reduce(P, xs);
     }
     // Every exit below is agreed by all compute threads (a thread that left
     // alone would leave the others at the next compute barrier).
@@ -2166,6 +2336,7 @@ static bool mk_build_maps(Model& m) {
       if (!mk_encode(t + MAP_QKV, L.wqkv, qd + 2 * kd, h) || !mk_encode(t + MAP_O, L.wo, h, qd) ||
           !mk_encode(t + MAP_GATEUP, L.w_gateup, E * 2 * f, h) || !mk_encode(t + MAP_DOWN, L.w_down, E * h, f))
         return false;
+      if (L.w_down_t && !mk_encode(t + MAP_DOWN_T, L.w_down_t, E * f, h)) return false;
     }
     if (!mk_encode(&maps[head_map], m.head, (uint64_t)c.vocab, h)) return false;
   }
@@ -2190,6 +2361,48 @@ static bool mk_build_maps(Model& m) {
   }
   return cudaMemcpy(m.mk_maps, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice) ==
          cudaSuccess;
+}
+
+bool mk_ffn_fused_layout(const dec_config& c) {
+  return c.weight_dtype == DEC_BF16 && !c.weight_quant && !decode_needs_rows(c) && c.hidden % MK_KG == 0 &&
+         c.ffn % MK_FTS == 0;
+}
+
+// Fused FFN (bf16 weights, transposed down copy present): hidden in whole
+// MK_KG-column blocks, ffn in MK_FTS-task steps (so no task block crosses an
+// expert), at most MK_FT tasks per CTA and MK_MAX_NB partial rows.
+bool mk_ffn_fused_ok(const Model& m, int nb) {
+  const dec_config& c = m.cfg;
+  if (m.wq8 || c.weight_dtype != DEC_BF16 || !m.layers || !m.layers[0].w_down_t || !m.s.fpart) return false;
+  if (c.hidden % MK_KG != 0 || c.ffn % MK_FTS != 0 || nb < 1 || nb > MK_MAX_NB) return false;
+  const int T = (c.n_experts ? c.n_experts_used : 1) * c.ffn;
+  const int per = ((T + nb - 1) / nb + MK_FTS - 1) / MK_FTS * MK_FTS;
+  return per <= MK_FT;
+}
+
+// dst[b][c][r] = src[b][r][c] for bf16 matrices of rows x cols (32 x 32 tiles
+// through shared memory; both sides coalesced).
+__global__ void __launch_bounds__(256) k_transpose_bf16(const __nv_bfloat16* __restrict__ src, int rows, int cols,
+                                                        __nv_bfloat16* __restrict__ dst) {
+  __shared__ __nv_bfloat16 t[32][34];
+  const size_t mat = (size_t)rows * cols * blockIdx.z;
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32, tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int i = ty; i < 32; i += 8) {
+    const int r = r0 + i, c = c0 + tx;
+    if (r < rows && c < cols) t[i][tx] = src[mat + (size_t)r * cols + c];
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int c = c0 + i, r = r0 + tx;
+    if (r < rows && c < cols) dst[mat + (size_t)c * rows + r] = t[tx][i];
+  }
+}
+
+cudaError_t launch_transpose_bf16(const void* src, int rows, int cols, int batch, void* dst, cudaStream_t s) {
+  if (rows <= 0 || cols <= 0 || batch <= 0) return cudaSuccess;
+  const dim3 grid((cols + 31) / 32, (rows + 31) / 32, batch);
+  k_transpose_bf16<<<grid, 256, 0, s>>>((const __nv_bfloat16*)src, rows, cols, (__nv_bfloat16*)dst);
+  return cudaGetLastError();
 }
 
 template <typename W, typename KV>
@@ -2324,6 +2537,8 @@ void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, in
   P.xb_plane = mk_xb_plane(c);
   P.attn_warp = mk_attn_warp_ok(c) ? 1 : 0;
   P.head_q8 = m.q_head.codes ? 1 : 0;
+  P.fpart = S.fpart;
+  P.ffn_fused = mk_ffn_fused_ok(m, P.nb) ? 1 : 0;
   // Warp-task attention merges each kv head's splits inside its own phase; the
   // CTA-task attention keeps a merge phase for large split sets.
   P.merge_phase = (!P.attn_warp && m.nsplit > 1 &&

@@ -66,6 +66,7 @@ struct LayerPtrs {
   const float* post_attn_norm;  // sandwich norms (nullable)
   const float* post_ffn_norm;
   QMat q_wqkv, q_wo, q_gateup, q_down;   // weight_quant = 1: the quantised projections
+  const void* w_down_t;  // persistent decode, fused FFN: w_down transposed, [expert][ffn][hidden] (nullable)
 };
 
 // bf16 (hi, lo) operand planes of the tensor-core prefill attention; plane
@@ -127,6 +128,7 @@ struct Scratch {
   size_t deq_bytes;
   float* q8part;
   size_t q8part_bytes;
+  float* fpart;         // persistent decode, fused FFN: [MK_MAX_NB][h] per-CTA down partials (nullable)
 };
 
 constexpr int LM_GRID_MAX = 1024;
@@ -137,6 +139,7 @@ constexpr int MAX_GROUP = 16;     // query heads per kv head
 constexpr int NUM_COUNTERS = 256;
 constexpr int MAX_BATCH = 256;    // rows of one batched decode step (also <= max_tokens)
 constexpr int AR_MAX_SPLIT = 16;  // key splits per kv head in batched decode attention
+constexpr int MK_MAX_NB = 256;    // CTAs of the persistent decode step with a fused FFN
 
 // Optional CUDA-event pairs recorded around every launch of one kernel class
 // (dec_timing_enable); also captured into the decode graph.
@@ -199,6 +202,7 @@ struct WsPlan {
   size_t qk_perm;                       // kHalf + QK-norm: permuted norm weights
   size_t q8, q8_bytes;                  // weight_quant: codes and scales of every quantised matrix
   size_t deq, deq_bytes, q8part, q8part_bytes;
+  size_t wdown_t, fpart;                // fused decode FFN: transposed down projections, partials
   size_t kv;            // start of the KV rings: [layer][K, V][seq][ring_rows][n_kv*hd]
   size_t kv_layer_bytes; // one layer's K (or V) rings of every sequence
   size_t ring_bytes;    // one sequence's ring
@@ -308,6 +312,12 @@ cudaError_t launch_weight_dequant_f32(const QMat& q, size_t rows, int cols, floa
 size_t mk_smem_bytes(const dec_config& c, int nsplit);
 size_t mk_maps_bytes(const dec_config& c);
 bool mk_prepare(Model& m, int num_sms);
+// Whether the persistent step runs its FFN fused (one phase over ffn slices + partial sums) on nb CTAs.
+bool mk_ffn_fused_ok(const Model& m, int nb);
+// Whether a configuration gets the fused FFN's transposed down copy in its workspace.
+bool mk_ffn_fused_layout(const dec_config& c);
+// dst[b] = src[b]^T for `batch` bf16 matrices of rows x cols.
+cudaError_t launch_transpose_bf16(const void* src, int rows, int cols, int batch, void* dst, cudaStream_t s);
 // cluster: run on one thread-block cluster of m.mk_cluster CTAs, else over m.mk_nb CTAs (one per SM).
 void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, int32_t token, int32_t pos,
                       float* logits, int32_t* d_argmax, bool cluster);

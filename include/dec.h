@@ -170,7 +170,11 @@ typedef struct dec_handle dec_handle;
 dec_status dec_config_validate(const dec_config *cfg, char *msg, size_t msg_len);
 
 /* Bytes of device workspace dec_create needs for cfg (KV cache plus all
- * scratch).  0 if cfg is invalid.  Host only. */
+ * scratch).  0 if cfg is invalid.  Host only.  For bf16 weights without
+ * weight_quant whose hidden size is a multiple of 128 and ffn a multiple of 16,
+ * this includes a transposed copy of every w_down ([expert][ffn][hidden], bf16,
+ * the size of w_down itself) read by the persistent decode step's FFN phase, and
+ * 256 * hidden floats of its partial sums. */
 size_t dec_workspace_bytes(const dec_config *cfg);
 
 /* Creates a handle.  workspace: device, >= dec_workspace_bytes(cfg) bytes,
@@ -178,9 +182,10 @@ size_t dec_workspace_bytes(const dec_config *cfg);
  * legacy default stream).  Weights are validated for presence and 16-byte
  * alignment.  The weights must be complete when work on cuda_stream starts:
  * dec_create itself enqueues kernels that read them (8-bit quantisation, the
- * kHalf row permutation), so a caller that wrote them on another stream makes
- * cuda_stream wait for it first.  Errors: DEC_EINVAL (config, NULL or
- * misaligned pointers), DEC_ENOMEM (workspace too small), DEC_ECUDA. */
+ * kHalf row permutation, the transposed w_down copy), so a caller that wrote
+ * them on another stream makes cuda_stream wait for it first.  Errors:
+ * DEC_EINVAL (config, NULL or misaligned pointers), DEC_ENOMEM (workspace too
+ * small), DEC_ECUDA. */
 dec_status dec_create(const dec_config *cfg, const dec_weights *weights, void *workspace,
                       size_t workspace_bytes, void *cuda_stream, dec_handle **out);
 
@@ -300,7 +305,10 @@ int32_t dec_fused_mode(const dec_handle *h);
  * >= 6*n_layers + 2 entries) is set, every later fused decode step writes the
  * GPU's nanosecond timer at its start ([0]) and after each of its phases
  * (QKV, attention, [merge], output projection, gate/up, down per layer; then
- * the head).  NULL stops it. */
+ * the head).  With the transposed w_down copy (see dec_workspace_bytes) the last
+ * two phases of a layer are the whole FFN over each CTA's ffn slice (gate/up,
+ * then that slice's share of the down projection) and the sum of those shares
+ * into the residual.  NULL stops it. */
 dec_status dec_phase_stamps(dec_handle *h, uint64_t *d_stamps, int32_t capacity);
 
 /* Decode steps run as one captured CUDA graph by default (when the handle's
