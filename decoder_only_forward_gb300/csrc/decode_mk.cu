@@ -146,7 +146,7 @@ struct MkMisc {
   int wbidx[MK_COMPUTE_WARPS];
   int token;
   int abort_flag;
-  int moe_ready;                 // layer index + 1 whose expert ids are in ids[]
+  uint64_t moe_bar;              // completes once per MoE layer when its expert ids are in ids[]
   int consumed[MK_COMPUTE_WARPS];  // stages each warp consumed (for the abort drain)
   int is_last;
   float mrow[MAX_GROUP], lrow[MAX_GROUP], alpha[MAX_GROUP];
@@ -299,6 +299,11 @@ __device__ __forceinline__ bool mk_mbar_wait(uint64_t* bar, uint32_t parity, vol
 // Asks L2 to fetch `bytes` (multiple of 16) from global memory ahead of use.
 __device__ __forceinline__ void mk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// The same for any pointer and size: the whole 16-byte units of a 16-byte aligned range, else nothing.
+__device__ __forceinline__ void mk_prefetch_l2_any(const void* src, uint32_t bytes) {
+  if (src && ((uintptr_t)src & 15u) == 0 && (bytes & ~15u) != 0) mk_prefetch_l2(src, bytes & ~15u);
 }
 
 // Contiguous global -> shared copy of `bytes` (multiple of 16, 16-byte aligned).
@@ -592,52 +597,96 @@ __device__ void mk_router(const MkParams& P, int l, const float* xs, MkMisc* M) 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const W* router = (const W*)P.layers[l].router;
   constexpr int V = Chunk<W>::N;
+  // One warp per expert row; each lane requests up to 16 of its 16-byte chunks
+  // before the first product (same order of products as one chunk at a time).
+  constexpr int RJ = 16;
+  const int nc = P.h / V;
   for (int e = warp; e < P.E; e += MK_COMPUTE_WARPS) {
     const W* row = router + (size_t)e * P.h;
     float a = 0.f;
-    for (int c = lane; c < P.h / V; c += 32) {
-      float wv[V];
-      Chunk<W>::widen(ld_stream16(row + (size_t)c * V), wv);
+    for (int c0 = lane; c0 < nc; c0 += 32 * RJ) {
+      uint4 u[RJ];
 #pragma unroll
-      for (int q = 0; q < V; ++q) a = fmaf(wv[q], xs[c * V + q], a);
+      for (int j = 0; j < RJ; ++j) {
+        const int c = c0 + 32 * j;
+        u[j] = c < nc ? ld_stream16(row + (size_t)c * V) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int j = 0; j < RJ; ++j) {
+        const int c = c0 + 32 * j;
+        if (c < nc) {
+          float wv[V];
+          Chunk<W>::widen(u[j], wv);
+#pragma unroll
+          for (int q = 0; q < V; ++q) a = fmaf(wv[q], xs[c * V + q], a);
+        }
+      }
     }
     a = warp_sum(a);
     if (lane == 0) M->logits[e] = a;
   }
   compute_sync();
-  if (tid == 0) {
-    int sel[MAX_EXPERTS_USED];
-    float mx = -INFINITY;
+  if (warp == 0) {
+    // Top-k by repeated selection, ties to the lower id (rml "The decoder",
+    // Mixture of experts): lane l owns experts l, l + 32, ...; each round takes
+    // the lanes' best untaken expert and the warp's best of those.  Lane j keeps
+    // selection j.
+    constexpr int NONE = 0x7fffffff;
+    unsigned taken = 0u;
+    int my_id = 0;
+    float my_logit = 0.f;
     for (int j = 0; j < P.k; ++j) {
-      int best = -1;
-      for (int e = 0; e < P.E; ++e) {
-        bool taken = false;
-        for (int t = 0; t < j; ++t) taken |= (sel[t] == e);
-        if (taken) continue;
-        if (best < 0 || M->logits[e] > M->logits[best]) best = e;
+      float bv = -INFINITY;
+      int bi = NONE;
+      for (int i = 0, e = lane; e < P.E; ++i, e += 32) {
+        if ((taken >> i) & 1u) continue;
+        const float v = M->logits[e];
+        if (bi == NONE || v > bv) {
+          bv = v;
+          bi = e;
+        }
       }
-      sel[j] = best;
-      mx = fmaxf(mx, M->logits[best]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (oi != NONE && (bi == NONE || ov > bv || (ov == bv && oi < bi))) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == j) {
+        my_id = bi;
+        my_logit = bv;
+      }
     }
-    float pj[MAX_EXPERTS_USED], tot = 0.f;
+    // Softmax over the selected logits (the first selection is their maximum),
+    // summed in selection order.
+    const float mx = __shfl_sync(0xffffffffu, my_logit, 0);
+    const float pj = lane < P.k ? expf(my_logit - mx) : 0.f;
+    float tot = 0.f;
+    for (int j = 0; j < P.k; ++j) tot += __shfl_sync(0xffffffffu, pj, j);
+    const float wj = pj / tot;
     for (int j = 0; j < P.k; ++j) {
-      pj[j] = expf(M->logits[sel[j]] - mx);
-      tot += pj[j];
-    }
-    for (int j = 0; j < P.k; ++j) {
-      M->ids[j] = sel[j];
-      M->wts[j] = pj[j] / tot;
+      const int idj = __shfl_sync(0xffffffffu, my_id, j);
+      const float wtj = __shfl_sync(0xffffffffu, wj, j);
+      if (lane == 0) {
+        M->ids[j] = idj;
+        M->wts[j] = wtj;
+      }
     }
     if (blockIdx.x == 0) {
-      for (int j = 0; j < P.k; ++j) P.ids_out[j] = sel[j];
+      if (lane < P.k) P.ids_out[lane] = my_id;
       if (P.trace_ids) {
         const size_t row = (size_t)l * P.trace_cap + (P.pos % P.trace_cap);
-        for (int j = 0; j < P.k; ++j) P.trace_ids[row * P.k + j] = sel[j];
-        for (int e = 0; e < P.E; ++e) P.trace_logits[row * P.E + e] = M->logits[e];
+        if (lane < P.k) P.trace_ids[row * P.k + lane] = my_id;
+        for (int e = lane; e < P.E; e += 32) P.trace_logits[row * P.E + e] = M->logits[e];
       }
     }
-    __threadfence_block();
-    *(volatile int*)&M->moe_ready = l + 1;   // releases the producer for this layer's experts
+    // Releases this layer's expert rows to the producers (the arrival orders
+    // lane 0's ids / wts writes before their wait returns).
+    if (lane == 0) mk_mbar_arrive(&M->moe_bar);
   }
   compute_sync();
 }
@@ -1635,9 +1684,13 @@ __device__ bool mk_attention_warp_any(const MkParams& P, int l, uint8_t* ring, u
                                       uint32_t& sc) {
   if constexpr (HD == 64 || HD == 128) {
     // Groups of 1-3 query heads per kv head run in the 4-head layout (unused
-    // slots stay empty): two instantiations keep the build short.
+    // slots stay empty).  The 8-head layout only at head_dim 64: at 128 its
+    // 64 query and accumulator registers per lane would spill, and merely
+    // compiling it into the kernel worsens the register allocation of every
+    // other phase (measured 2-4% slower decode steps on Mixtral and Mistral).
     if (P.nq / P.nkv <= 4) return mk_attention_warp<W, KV, HD, 4>(P, l, ring, ureg, M, sc);
-    return mk_attention_warp<W, KV, HD, 8>(P, l, ring, ureg, M, sc);
+    if constexpr (HD == 64) return mk_attention_warp<W, KV, HD, 8>(P, l, ring, ureg, M, sc);
+    return false;
   } else {
     return false;
   }
@@ -1826,7 +1879,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_step(const __grid_cons
         mk_mbar_init(&M->empty[w][s], 1);
       }
     M->abort_flag = 0;
-    M->moe_ready = 0;
+    mk_mbar_init(&M->moe_bar, 1);
     for (int w = 0; w < MK_COMPUTE_WARPS; ++w) M->consumed[w] = 0;
     if (P.cluster) mk_mbar_init(&M->cbar, (uint32_t)P.cluster);
     M->cgen = 0;
@@ -1887,6 +1940,17 @@ __device__ void mk_produce(const MkParams& P, uint8_t* ring, MkMisc* M) {
         // global memory): prefetch it into L2 while the QKV weights stream, so the
         // attention phase reads it from L2.
         if (ph == PH_QKV) mk_prefetch_attention_kv(P, l, P.hd, w, MK_COMPUTE_WARPS);
+        // The next phases' small operands (norm weights, router rows), read by every
+        // CTA right after a barrier: one CTA asks L2 for them a phase ahead.
+        if (blockIdx.x == 0 && w == 0 && l < P.n_layers) {
+          const MkLayer& Lp = P.layers[l];
+          if (ph == PH_OPROJ) {
+            mk_prefetch_l2_any(Lp.ffn_norm, (uint32_t)(P.h * 4));
+            if (P.E > 0) mk_prefetch_l2_any(Lp.router, (uint32_t)(P.E * P.h * (int)sizeof(typename MkElem<W>::T)));
+          } else if (ph == PH_GATEUP) {
+            mk_prefetch_l2_any(l + 1 < P.n_layers ? P.layers[l + 1].attn_norm : P.out_norm, (uint32_t)(P.h * 4));
+          }
+        }
         if constexpr (HD == 64 || HD == 128) {
           if (ph == PH_ATTN && P.attn_warp) {
             // This warp's attention tasks: per RPP keys a K piece, then a V piece,
@@ -1927,15 +1991,11 @@ __device__ void mk_produce(const MkParams& P, uint8_t* ring, MkMisc* M) {
         }
         if (!mk_is_gemv(P, ph)) continue;
         if (P.E > 0 && (ph == PH_GATEUP || ph == PH_DOWN)) {
-          // Expert rows are known once this layer's router has run.
-          const uint64_t t0 = globaltimer_ns();
-          while (*(volatile int*)&M->moe_ready < l + 1 && !*abort_flag) {
-            if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-              raise_error(P.st, ERR_TIMEOUT, 301);
-              *abort_flag = 1;
-            }
-          }
-          if (*abort_flag) break;
+          // Expert rows are known once this layer's router has run: its barrier
+          // completes once per layer, and this producer is never a whole layer
+          // ahead of the router (it needs this layer's rows consumed first), so
+          // completion l is the one with parity l & 1.
+          if (!mk_mbar_wait(&M->moe_bar, (uint32_t)(l & 1), abort_flag, P.st, 301)) break;
         }
         MkRows R;
         mk_phase_rows<W>(P, ph, l, M->ids, R);
@@ -2072,10 +2132,14 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
           mk_merge_heads(P.part, P.nsplit, HD, h0, 1, xs, P.attn, true);
         break;
       case PH_OPROJ:
-        if (!P.attn_warp && P.nsplit > 1 && !P.merge_phase)
+        if (!P.attn_warp && P.nsplit > 1 && !P.merge_phase) {
           mk_merge_heads(P.part, P.nsplit, HD, 0, P.nq, xs + qd, xs, false);
-        else mk_copy_to_xs(P.attn, qd, xs);
-        if (MMA) mk_to_xb(xs, false, qd, xb, P.xb_plane, Q8);
+          if (MMA) mk_to_xb(xs, false, qd, xb, P.xb_plane, Q8);
+        } else if (MMA) {
+          mk_to_xb(P.attn, true, qd, xb, P.xb_plane, Q8);   // the tensor-core GEMV reads only the planes
+        } else {
+          mk_copy_to_xs(P.attn, qd, xs);
+        }
         break;
       case PH_GATEUP:
         mk_norm_to_xs<typename MkElem<W>::T>(P.x, nullptr, L.ffn_norm, P.h, P.eps, xs, M, MMA ? xb : nullptr, P.xb_plane, kpad_h,
@@ -2239,11 +2303,12 @@ static size_t mk_u_bytes(const dec_config& c, int nsplit) {
 }
 
 // Attention as per-warp tasks: head_dim 64/128 (a lane owns head_dim / 32
-// dims), at most 8 query heads per kv head, and a stage holds at least one
-// head's K or V row.
+// dims), at most 8 (head_dim 64) or 4 (head_dim 128) query heads per kv head,
+// and a stage holds at least one head's K or V row; other shapes take the
+// CTA-task attention.
 static bool mk_attn_warp_ok(const dec_config& c) {
   const int G = c.n_heads / c.n_kv_heads;
-  return (c.head_dim == 64 || c.head_dim == 128) && G >= 1 && G <= 8;
+  return (c.head_dim == 64 && G >= 1 && G <= 8) || (c.head_dim == 128 && G >= 1 && G <= 4);
 }
 
 size_t mk_smem_bytes(const dec_config& c, int nsplit) {
