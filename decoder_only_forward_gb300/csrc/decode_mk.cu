@@ -36,6 +36,10 @@ namespace dec {
 constexpr int MK_COMPUTE_WARPS = 8;
 constexpr int MK_COMPUTE = MK_COMPUTE_WARPS * 32;   // 256 compute threads
 constexpr int MK_THREADS = 2 * MK_COMPUTE;          // + one producer warp per compute warp
+constexpr int MK_REGS = 128;                         // registers per thread at launch (65536 / MK_THREADS)
+constexpr int MK_REGS_PRODUCER = 64, MK_REGS_COMPUTE = 192;   // after the split (multiples of 8)
+static_assert(MK_COMPUTE * MK_REGS_PRODUCER + MK_COMPUTE * MK_REGS_COMPUTE == MK_THREADS * MK_REGS,
+              "the split hands out exactly the launch's registers");
 constexpr int MK_WARP_RING = 16 * 1024;            // weight ring of one compute warp
 constexpr int MK_RING_BYTES = MK_COMPUTE_WARPS * MK_WARP_RING;  // 128 KB
 constexpr int MK_MAX_STAGES = 8;
@@ -1906,8 +1910,18 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_step(const __grid_cons
   // arrival, and (at the end) no CTA exits while another may still arrive on
   // its barrier.  barrier.cluster counts every thread of the cluster.
   if (P.cluster) asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-  if ((tid >> 5) >= MK_COMPUTE_WARPS) mk_produce<W, KV, HD>(P, ring, M);
-  else mk_compute<W, KV, HD>(P, ring, ureg, M);
+  // Register split: the producer warpgroups (one active lane per warp) give
+  // registers to the compute warpgroups.  The launch holds MK_THREADS x
+  // MK_REGS registers (the host refuses a build with another count), and the
+  // two shares add up to exactly that, so the increase always completes once
+  // the producers' decrease has run (which waits on nothing).
+  if ((tid >> 5) >= MK_COMPUTE_WARPS) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(MK_REGS_PRODUCER) : "memory");
+    mk_produce<W, KV, HD>(P, ring, M);
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(MK_REGS_COMPUTE) : "memory");
+    mk_compute<W, KV, HD>(P, ring, ureg, M);
+  }
   if (P.cluster) asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
@@ -2514,6 +2528,9 @@ bool mk_prepare(Model& m, int num_sms) {
   void* fn = mk_func(c);
   if (!fn) return false;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return false;
+  // The register split inside the kernel assumes exactly MK_REGS registers per thread at launch.
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess || fa.numRegs != MK_REGS) return false;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, MK_THREADS, smem) != cudaSuccess || per_sm < 1)
     return false;
