@@ -103,8 +103,8 @@ TRAFFIC = {
         "bytes": 1814336, "source": "decoder_only_forward_gb300/csrc/decode.cu",
         "sha256": "3d7213fecd5001252701110382d8e9dfd57676011ecc1ded9bf6666198c7ae34"},
     ("mixtral-8x7b", "step"): {
-        "bytes": 26194874880, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
-        "sha256": "c5a126ed56d888fe8bf125af5601570dd900a0794d82889308d8ccc9b159dd58"},
+        "bytes": 26033930240, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
+        "sha256": "770286cab935e1fa1c7f99e6205c86beaf6fe8180b438a77bbfd96b938d4c993"},
     ("mistral-7b", "step"): {
         "bytes": 15712395008, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
         "sha256": "4bf7258819f5eaeff409afa95ceaa4deb2af4270224b2c6b5de9309906a0eb17"},
@@ -431,14 +431,17 @@ def measure_workload(name, w, dev, args, steps, warmup, weights=None, want_e2e_s
             d.phase_stamps(None)
             d.check()
             r["phase_rows"] = rows
+            r["ffn_fused"] = d.ffn_fused()
     return r
 
 
-def phase_summary(w: dict, rows, merge_phase: bool) -> dict:
-    """Per-phase µs per token (summed over layers) from the persistent step's stamps."""
+def phase_summary(w: dict, rows, merge_phase: bool, ffn_fused: bool = False) -> dict:
+    """Per-phase µs per token (summed over layers) from the persistent step's stamps.  With
+    the fused FFN the last two phases of a layer are the FFN over each CTA's ffn slice
+    ("ffn") and the sum of the CTAs' down-projection partials into the residual ("ffn_sum")."""
     ppl = 6 if merge_phase else 5
-    names = ["qkv", "attn", "merge", "oproj", "gateup", "down"] if ppl == 6 else \
-        ["qkv", "attn", "oproj", "gateup", "down"]
+    ffn = ["ffn", "ffn_sum"] if ffn_fused else ["gateup", "down"]
+    names = (["qkv", "attn", "merge", "oproj"] if ppl == 6 else ["qkv", "attn", "oproj"]) + ffn
     n = w["n_layers"] * ppl + 1
     diffs = np.stack([np.diff(r[: n + 1]) for r in rows[2:]]) if len(rows) > 2 else \
         np.stack([np.diff(r[: n + 1]) for r in rows])
@@ -529,7 +532,7 @@ def run_ours(args, rank, world, local_rank):
         # The step stores a start stamp, one per phase and one after the head: the count of
         # stored stamps gives the phases per layer (5, or 6 with a split-merge phase).
         nz = int(np.count_nonzero(r["phase_rows"][-1]))
-        phases = phase_summary(w, r["phase_rows"], (nz - 2) // w["n_layers"] == 6)
+        phases = phase_summary(w, r["phase_rows"], (nz - 2) // w["n_layers"] == 6, r.get("ffn_fused", False))
 
     out = None
     if rank == 0:

@@ -1028,6 +1028,13 @@ int32_t dec_fused_mode(const dec_handle* h) {
   return DEC_FUSED_OFF;
 }
 
+int32_t dec_ffn_fused(const dec_handle* h) {
+  if (!h) return -1;
+  const int32_t mode = dec_fused_mode(h);
+  if (mode == DEC_FUSED_OFF) return 0;
+  return mk_ffn_fused_ok(h->m, mode == DEC_FUSED_CLUSTER ? h->m.mk_cluster : h->m.mk_nb) ? 1 : 0;
+}
+
 int32_t dec_fused_available(const dec_handle* h, int32_t mode) {
   if (!h) return 0;
   if (mode == DEC_FUSED_OFF) return 1;

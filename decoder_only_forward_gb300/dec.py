@@ -29,7 +29,7 @@ STATUS_NAMES = {0: "DEC_OK", 1: "DEC_EINVAL", 2: "DEC_ERANGE", 3: "DEC_ECUDA", 4
 EXPORTED = ["dec_config_validate", "dec_workspace_bytes", "dec_create", "dec_prefill", "dec_decode",
             "dec_decode_dev", "dec_kv_reset", "dec_length", "dec_kv_layer", "dec_set_trace",
             "dec_check", "dec_timing_enable", "dec_timing_read", "dec_launch_count", "dec_destroy",
-            "dec_last_error", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc", "dec_gemm_bf16", "dec_set_graph", "dec_set_fused", "dec_fused_available", "dec_fused_mode", "dec_phase_stamps",
+            "dec_last_error", "dec_attend_scratch_bytes", "dec_attend", "dec_attend_noalloc", "dec_gemm_bf16", "dec_set_graph", "dec_set_fused", "dec_fused_available", "dec_fused_mode", "dec_ffn_fused", "dec_phase_stamps",
             "dec_prefill_seq", "dec_kv_reset_seq", "dec_length_seq", "dec_decode_batch", "dec_kv_layer_seq",
             "dec_kv_quantize_int8", "dec_kv_slot", "dec_pages_free", "dec_selftest_wait_timeout",
             "dec_weight_quantize_int8"]
@@ -93,6 +93,7 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "dec_set_fused": (I32, [P, I32]),
         "dec_fused_available": (I32, [P, I32]),
         "dec_fused_mode": (I32, [P]),
+        "dec_ffn_fused": (I32, [P]),
         "dec_phase_stamps": (I32, [P, P, I32]),
         "dec_last_error": (ctypes.c_char_p, [P]),
         "dec_prefill_seq": (I32, [P, I32, ctypes.POINTER(I32), I32, I32, P, P]),
@@ -398,6 +399,10 @@ class Decoder:
         """The schedule the next decode step takes: "off", "grid" or "cluster"."""
         m = int(lib.dec_fused_mode(self.h))
         return {v: k for k, v in FUSED_MODES.items()}[m]
+
+    def ffn_fused(self) -> bool:
+        """Whether the next decode step runs the FFN over ffn slices plus a partial-sum phase."""
+        return int(lib.dec_ffn_fused(self.h)) == 1
 
     def fused_available(self, mode) -> int:
         """1 (or the cluster's CTA count) when the schedule can run on this handle, else 0."""

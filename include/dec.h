@@ -301,6 +301,12 @@ int32_t dec_fused_available(const dec_handle *h, int32_t mode);
 /* The schedule the next decode step takes (after any fallback); -1 for NULL. */
 int32_t dec_fused_mode(const dec_handle *h);
 
+/* Whether the next decode step runs its FFN as one phase over ffn slices plus a
+ * partial-sum phase (1: a persistent schedule, bf16 weights without weight_quant,
+ * hidden a multiple of 128, ffn a multiple of 16, at most 256 (slot, ffn) tasks per
+ * CTA) or as a gate/up phase and a down phase (0); -1 for NULL. */
+int32_t dec_ffn_fused(const dec_handle *h);
+
 /* Measurement hook of the persistent decode step: when d_stamps (device,
  * >= 6*n_layers + 2 entries) is set, every later fused decode step writes the
  * GPU's nanosecond timer at its start ([0]) and after each of its phases

@@ -32,10 +32,11 @@ def dec_mod():
     return dec
 
 
-def _run(dec_mod, w, P=24, D=6):
+def _run(dec_mod, w, fused, P=24, D=6):
     d = dec_mod.Decoder(w)
     d.set_fused("grid")
     assert d.fused_mode() == "grid"
+    assert d.ffn_fused() == fused
     prompt = synthetic.prompt_tokens(w, P, seed=3)
     rows, taus = gpu_greedy(d, prompt, D, use_device_argmax=True)
     ref, _ = oracle_teacher_forced(w, prompt, taus, D)
@@ -49,16 +50,24 @@ def _run(dec_mod, w, P=24, D=6):
 def test_dense_ffn_fused_and_two_phase(dec_mod, ffn):
     # 1360 = 85 * 16: one FFN phase over ffn slices; 1352 (8 past a multiple of 16):
     # the gate/up and down phases.
-    _run(dec_mod, synthetic.workload("smollm2-135m", ffn=ffn, **BASE))
+    _run(dec_mod, synthetic.workload("smollm2-135m", ffn=ffn, **BASE), fused=ffn % 16 == 0)
 
 
 def test_moe_ffn_fused_slice_straddles_experts(dec_mod):
     # 2 of 4 experts, ffn 1360: 2720 (slot, ffn) tasks over the CTAs in 32-task
     # shares on a 152-SM GPU, so one CTA's share ends in the second slot's rows.
     w = synthetic.workload("smollm2-135m", ffn=1360, n_experts=4, n_experts_used=2, **BASE)
-    _run(dec_mod, w)
+    _run(dec_mod, w, fused=True)
 
 
 def test_qwen_shape_ffn_fused_with_bias(dec_mod):
     # hidden 896 = seven 128-column blocks (seven of the eight warps own one each).
-    _run(dec_mod, synthetic.workload("qwen2.5-0.5b", n_layers=2, max_seq=64), P=32, D=4)
+    _run(dec_mod, synthetic.workload("qwen2.5-0.5b", n_layers=2, max_seq=64), fused=True, P=32, D=4)
+
+
+def test_per_layer_schedule_reports_no_fused_ffn(dec_mod):
+    w = synthetic.workload("smollm2-135m", ffn=1360, **BASE)
+    d = dec_mod.Decoder(w)
+    d.set_fused("off")
+    assert not d.ffn_fused()
+    d.close()
