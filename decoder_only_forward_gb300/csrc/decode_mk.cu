@@ -135,6 +135,27 @@ struct MkParams {
   float* fpart;                   // fused FFN: [nb][h] per-CTA partial sums of the down projection
 };
 
+// The weight rows one CTA handles in one phase: up to k contiguous segments
+// (one per selected expert).  Producer and consumers both derive it, so they
+// agree stage by stage.  On the tensor-core path every CTA's share is a
+// multiple of 16 rows (the MMA's M), so no CTA reads rows another one owns.
+struct MkSeg {
+  const uint8_t* base;   // row 0 of the segment's matrix
+  int row0, rows;        // rows [row0, row0 + rows)
+  int out0;              // output index of the segment's first row (task space)
+  int slot;              // expert slot (MoE), else 0
+  int map;               // tensor map of the matrix (bf16 weights)
+  int maprow;            // row of the map holding the segment's row row0
+};
+struct MkRows {
+  int nseg;
+  MkSeg seg[MAX_EXPERTS_USED];
+  int K;                 // row length (elements)
+  int rowbytes;
+  int rps;               // rows per stage (CUDA-core path)
+  bool paired;
+};
+
 // Shared-memory bookkeeping after the weight ring and the union region.
 struct MkMisc {
   uint64_t full[MK_COMPUTE_WARPS][MK_MAX_STAGES];
@@ -157,6 +178,11 @@ struct MkMisc {
   float mscale[8 * 32];          // warp-task attention merge: weight of split s for query head h
   int lastg[MK_COMPUTE_WARPS];   // kv heads whose last split this CTA finished in the current round
   float fact[MK_FT];             // fused FFN: this CTA's SwiGLU outputs (router-weighted)
+  // Each warp's row plan of its current phase (compute warps, then producers), in
+  // shared memory: as a local array it lived in local memory that the 28 KB L1 beside
+  // this kernel's shared memory could not keep, so reading a phase's segments cost a
+  // round trip to L2.
+  MkRows rows[2 * MK_COMPUTE_WARPS];
   __nv_bfloat16 fxb[2][MK_FT];   // fused FFN: the same as bf16 (hi, lo) planes
   uint64_t cbar;                 // cluster mode: phase barrier, one arrival per CTA of the cluster
   unsigned cgen;                 // cluster mode: barrier instances completed
@@ -323,26 +349,6 @@ __device__ __forceinline__ void mk_bulk_load(void* dst, const void* src, uint32_
 namespace dec {
 
 // ------------------------------------------------------------------ schedule
-// The weight rows one CTA handles in one phase: up to k contiguous segments
-// (one per selected expert).  Producer and consumers both derive it, so they
-// agree stage by stage.  On the tensor-core path every CTA's share is a
-// multiple of 16 rows (the MMA's M), so no CTA reads rows another one owns.
-struct MkSeg {
-  const uint8_t* base;   // row 0 of the segment's matrix
-  int row0, rows;        // rows [row0, row0 + rows)
-  int out0;              // output index of the segment's first row (task space)
-  int slot;              // expert slot (MoE), else 0
-  int map;               // tensor map of the matrix (bf16 weights)
-  int maprow;            // row of the map holding the segment's row row0
-};
-struct MkRows {
-  int nseg;
-  MkSeg seg[MAX_EXPERTS_USED];
-  int K;                 // row length (elements)
-  int rowbytes;
-  int rps;               // rows per stage (CUDA-core path)
-  bool paired;
-};
 
 __device__ __forceinline__ bool mk_is_gemv(const MkParams& P, int ph) {
   return ph != PH_ATTN && ph != PH_MERGE && !(ph == PH_DOWN && P.ffn_fused);
@@ -2011,7 +2017,7 @@ __device__ void mk_produce(const MkParams& P, uint8_t* ring, MkMisc* M) {
           // completion l is the one with parity l & 1.
           if (!mk_mbar_wait(&M->moe_bar, (uint32_t)(l & 1), abort_flag, P.st, 301)) break;
         }
-        MkRows R;
+        MkRows& R = M->rows[MK_COMPUTE_WARPS + w];   // written and read by this lane only
         mk_phase_rows<W>(P, ph, l, M->ids, R);
         for (int si = 0; si < R.nseg && ok; ++si) {
           const MkSeg S = R.seg[si];   // by value: its fields stay in registers
@@ -2170,8 +2176,9 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
         break;
     }
     if (mk_is_gemv(P, ph)) {
-      MkRows R;
-      mk_phase_rows<W>(P, ph, l, M->ids, R);
+      MkRows& R = M->rows[warp];
+      if ((tid & 31) == 0) mk_phase_rows<W>(P, ph, l, M->ids, R);
+      __syncwarp();
       ok = mk_gemv_phase<W, KV>(P, ph, l, R, ring, M, xs, sc, best, bidx);
       if constexpr (MMA && !Q8) {
         if (ph == PH_GATEUP && P.ffn_fused && !compute_sync_or(!ok)) ok = mk_ffn_down_part<W>(P, R, ring, M, sc);
