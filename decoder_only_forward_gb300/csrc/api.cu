@@ -261,7 +261,6 @@ WsPlan dec::plan_workspace(const dec_config& c) {
   const size_t qkv_rows = (size_t)qd + 2 * kd;
   p.wqkv_perm = take(c.rope_half ? (size_t)c.n_layers * qkv_rows * c.hidden * ws : 0);
   p.bqkv_perm = take(c.rope_half && c.qkv_bias ? (size_t)c.n_layers * qkv_rows * 4 : 0);
-  p.mk_layers = take(sizeof(MkLayer) * (size_t)c.n_layers);
   p.mk_maps = take(mk_maps_bytes(c));
   // Batched decode: per-row metadata and the attention split partials.
   const int bmax = T < MAX_BATCH ? T : MAX_BATCH;
@@ -584,16 +583,9 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
     S.q8part_bytes = p.q8part_bytes;
   }
   {
-    std::vector<MkLayer> tab(cfg->n_layers);
-    for (int l = 0; l < cfg->n_layers; ++l) {
-      const LayerPtrs& d = h->layers[l];
-      tab[l] = MkLayer{d.attn_norm, d.wqkv, d.bqkv, d.wo, d.ffn_norm, d.w_gateup, d.w_down, d.router, d.kc, d.vc};
-    }
-    m.mk_layers = (const MkLayer*)(base + p.mk_layers);
     m.mk_maps = mk_maps_bytes(*cfg) ? (void*)(base + p.mk_maps) : nullptr;
-    cudaError_t e2 = cudaMemcpy((void*)m.mk_layers, tab.data(), sizeof(MkLayer) * tab.size(), cudaMemcpyHostToDevice);
     int dev = 0, sms = 0;
-    if (e2 == cudaSuccess) e2 = cudaGetDevice(&dev);
+    cudaError_t e2 = cudaGetDevice(&dev);
     if (e2 == cudaSuccess) e2 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e2 != cudaSuccess) {
       delete h;

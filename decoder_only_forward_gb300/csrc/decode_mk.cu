@@ -85,6 +85,7 @@ template <> struct MkElem<WQ8> { using T = __nv_bfloat16; };
 // Activation planes are zero-padded to whole stages of either path.
 constexpr int MK_PADK = 256;
 constexpr int MK_CHUNK = 8;                         // row blocks reduced together (partials in smem)
+constexpr int MK_MAX_LAYERS = 128;                  // layers of the persistent step (its parameter block)
 // Fused FFN: a CTA owns a contiguous range of ffn tasks (slot, ffn index), a
 // multiple of MK_FTS of them and at most MK_FT.
 constexpr int MK_FTS = 16, MK_FT = 256;
@@ -100,7 +101,11 @@ enum MkPhase { PH_QKV = 0, PH_ATTN, PH_MERGE, PH_OPROJ, PH_GATEUP, PH_DOWN, PH_L
 struct MkParams {
   int n_layers, h, nq, nkv, hd, f, V, E, k, max_seq, sliding, nsplit, sps, merge_phase, nb;
   float eps;
-  const MkLayer* layers;          // device table
+  // The layer table in the kernel's parameters: read through the constant cache,
+  // so a phase's first use of a layer pointer needs no global load (from a
+  // global-memory table, the attention phase's first K/V row address waited on
+  // one L2 round trip before its own load could start).
+  MkLayer layers[MK_MAX_LAYERS];
   const void* embed;
   const float* out_norm;
   const void* head;
@@ -2524,6 +2529,7 @@ bool mk_prepare(Model& m, int num_sms) {
   m.mk_cluster = 0;
   (void)es;
   if (decode_needs_rows(c)) return false;   // served by the row kernels
+  if (c.n_layers > MK_MAX_LAYERS) return false;   // the layer table travels in the kernel parameters
   // MoE down keeps one row sum per owned row (a CTA owns ceil(hidden / CTAs)
   // rows, in 16-row blocks on the tensor-core path); RoPE table of up to 64 pairs.
   auto rows_per_cta = [&](int nb) { return ((c.hidden + nb - 1) / nb + 15) / 16 * 16; };
@@ -2596,7 +2602,10 @@ void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, in
   P.nb = cluster ? m.mk_cluster : m.mk_nb;
   P.cluster = cluster ? m.mk_cluster : 0;
   P.eps = c.rms_eps;
-  P.layers = m.mk_layers;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const LayerPtrs& d = m.layers[l];
+    P.layers[l] = MkLayer{d.attn_norm, d.wqkv, d.bqkv, d.wo, d.ffn_norm, d.w_gateup, d.w_down, d.router, d.kc, d.vc};
+  }
   P.embed = m.tok_embd;
   P.out_norm = m.out_norm;
   P.head = m.head;

@@ -162,7 +162,6 @@ struct Model {
   Scratch s;
   int nsplit;           // split-K CTAs per kv head in decode attention
   int attn_sps;         // KV slots owned by one split
-  const MkLayer* mk_layers;  // device copy of the layer table (persistent decode kernel)
   size_t mk_smem;       // its dynamic shared memory
   int mk_nb;            // its grid (one CTA per SM)
   bool mk_ok;           // the persistent kernel fits this configuration
@@ -191,7 +190,6 @@ struct WsPlan {
   size_t at_Kb, at_Vt;
   int at_kcap, at_vt_ld;  // 0: no tensor-core prefill attention for this configuration
   size_t wqkv_perm, bqkv_perm;  // kHalf RoPE: q/k rows permuted per head
-  size_t mk_layers;     // layer table of the persistent decode kernel
   size_t mk_maps;       // its weight tensor maps
   size_t b_seq, b_pos, b_rows, b_part;  // batched decode
   size_t kpart, kpart_bytes;            // split-K partials
