@@ -2148,16 +2148,21 @@ __device__ void mk_compute(const MkParams& P, uint8_t* ring, uint8_t* ureg, MkMi
         mk_norm_to_xs<typename MkElem<W>::T>(P.x, l == 0 ? (const typename MkElem<W>::T*)P.embed + (size_t)token * P.h : nullptr, L.attn_norm, P.h, P.eps,
                          xs, M, MMA ? xb : nullptr, P.xb_plane, kpad_h, Q8);
         break;
+      // Head dims 64 / 128 always take the warp-task attention (the host declines
+      // the persistent step for their other shapes): the CTA-task attention and its
+      // merges are compiled only into the other instantiations, which keeps their
+      // code out of the hot kernels.
       case PH_ATTN:
-        if (P.attn_warp) ok = mk_attention_warp_any<W, KV, HD>(P, l, ring, ureg, M, sc);
+        if constexpr (HD == 64 || HD == 128) ok = mk_attention_warp_any<W, KV, HD>(P, l, ring, ureg, M, sc);
         else mk_attention<KV, HD>(P, l, ureg, M);
         break;
       case PH_MERGE:
-        for (int h0 = blockIdx.x; h0 < P.nq; h0 += P.nb)
-          mk_merge_heads(P.part, P.nsplit, HD, h0, 1, xs, P.attn, true);
+        if constexpr (HD != 64 && HD != 128)
+          for (int h0 = blockIdx.x; h0 < P.nq; h0 += P.nb)
+            mk_merge_heads(P.part, P.nsplit, HD, h0, 1, xs, P.attn, true);
         break;
       case PH_OPROJ:
-        if (!P.attn_warp && P.nsplit > 1 && !P.merge_phase) {
+        if (HD != 64 && HD != 128 && P.nsplit > 1 && !P.merge_phase) {
           mk_merge_heads(P.part, P.nsplit, HD, 0, P.nq, xs + qd, xs, false);
           if (MMA) mk_to_xb(xs, false, qd, xb, P.xb_plane, Q8);
         } else if (MMA) {
@@ -2529,6 +2534,8 @@ bool mk_prepare(Model& m, int num_sms) {
   m.mk_cluster = 0;
   (void)es;
   if (decode_needs_rows(c)) return false;   // served by the row kernels
+  // Head dims 64 / 128 run the warp-task attention only.
+  if ((c.head_dim == 64 || c.head_dim == 128) && !mk_attn_warp_ok(c)) return false;
   if (c.n_layers > MK_MAX_LAYERS) return false;   // the layer table travels in the kernel parameters
   // MoE down keeps one row sum per owned row (a CTA owns ceil(hidden / CTAs)
   // rows, in 16-row blocks on the tensor-core path); RoPE table of up to 64 pairs.
