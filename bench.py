@@ -103,8 +103,8 @@ TRAFFIC = {
         "bytes": 1814336, "source": "decoder_only_forward_gb300/csrc/decode.cu",
         "sha256": "3d7213fecd5001252701110382d8e9dfd57676011ecc1ded9bf6666198c7ae34"},
     ("mixtral-8x7b", "step"): {
-        "bytes": 25907966976, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
-        "sha256": "bae86a9f5ee474cdc535b67c19c949168afb6259b88a1e6fe1f87e4bc1c062fd"},
+        "bytes": 25946351872, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
+        "sha256": "73e512ac28b166757929af777b964b298b250d7d1f2bf9c8696f3fd1a4c0f73a"},
     ("mistral-7b", "step"): {
         "bytes": 15712395008, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
         "sha256": "4bf7258819f5eaeff409afa95ceaa4deb2af4270224b2c6b5de9309906a0eb17"},
