@@ -79,6 +79,13 @@ template <> struct MkRing<WQ8> {
   static constexpr int STAGES = 3, BYTES = 5120;
   static constexpr bool MMA = true, Q8 = true;
 };
+// int8 K/V cache (rml "The decoder", KV cache): a ring row is [group scales of
+// every kv head, f32][codes, int8]; a group is 32 channels of one head.
+struct KVI8 {};
+constexpr int MK_I8_RPP = 8;    // keys per attention piece (one TMA box of codes, one of scales; 8 measured faster than 16)
+template <typename KV> constexpr bool kMkKvI8 = false;
+template <> constexpr bool kMkKvI8<KVI8> = true;
+
 // Element type of the weights that are never quantised (embeddings, router, a tied head).
 template <typename W> struct MkElem { using T = W; };
 template <> struct MkElem<WQ8> { using T = __nv_bfloat16; };
@@ -92,7 +99,7 @@ constexpr int MK_FTS = 16, MK_FT = 256;
 // Tensor maps per layer (bf16 weights): QKV, O, gate/up, down, and the K and V
 // rings (3D: head_dim x kv heads x slots, one box = one attention piece); then the head.
 enum MkMap { MAP_QKV = 0, MAP_O, MAP_GATEUP, MAP_DOWN, MAP_K, MAP_V,
-             MAP_QKV_S, MAP_O_S, MAP_GATEUP_S, MAP_DOWN_S, MAP_DOWN_T, MAPS_PER_LAYER };
+             MAP_QKV_S, MAP_O_S, MAP_GATEUP_S, MAP_DOWN_S, MAP_DOWN_T, MAP_KS, MAP_VS, MAPS_PER_LAYER };
 constexpr int MAP_SCALE_OFF = MAP_QKV_S - MAP_QKV;   // a projection's scale map, 8-bit weights
 // After the layers: the head, then (8-bit untied head) its scales.
 
@@ -138,6 +145,9 @@ struct MkParams {
   int head_q8;                    // 8-bit weights: the LM head is quantised too (untied)
   int ffn_fused;                  // FFN as one phase over ffn slices + a partial-sum phase (below)
   float* fpart;                   // fused FFN: [nb][h] per-CTA partial sums of the down projection
+  float* kv_cur;                  // int8 cache: [2][nkv*hd] this position's K and V rows in f32
+  int kv_code_off;                // int8 cache: byte offset of a row's codes (after its scales)
+  int kv_row_bytes;               // int8 cache: bytes of one ring row
 };
 
 // The weight rows one CTA handles in one phase: up to k contiguous segments
@@ -772,6 +782,12 @@ __device__ __forceinline__ void mk_epi_pair(const MkParams& P, int ph, const MkL
     if (row < qd) {
       P.q[row] = v0;
       P.q[row + 1] = v1;
+    } else if constexpr (kMkKvI8<KV>) {
+      // int8 cache: the row is quantised per 32-channel group by the attention task
+      // that holds this position (a group's rows are spread over several CTAs here).
+      P.kv_cur[row - qd] = v0;
+      P.kv_cur[row - qd + 1] = v1;
+      (void)slot;
     } else {
       const bool is_k = row < qd + kd;
       KV* dst = (KV*)(is_k ? L.kc : L.vc);
@@ -1311,9 +1327,15 @@ __device__ void mk_ffn_reduce(const MkParams& P, float* red) {
 // query heads per kv head; partials have the same layout as the CTA tasks'.
 template <typename W, typename KV, int HD>
 struct MkAttnGeom {
+  static constexpr bool I8 = kMkKvI8<KV>;
   static constexpr int SB = MkRing<W>::BYTES < 4096 ? MkRing<W>::BYTES : 4096;   // bytes of one piece
-  static constexpr int RB = HD * (int)sizeof(KV);   // bytes of one head's K or V row
-  static constexpr int RPP = SB / RB;                // keys per piece (stage)
+  static constexpr int RB = I8 ? HD : HD * (int)sizeof(KV);   // bytes of one head's K or V row (codes)
+  // int8: MK_I8_RPP keys per piece, codes then the keys' group scales (HD / 32 floats each).
+  static constexpr int RPP = I8 ? MK_I8_RPP : SB / RB;   // keys per piece (stage)
+  static constexpr int SCB = I8 ? HD / 32 * 4 : 0;   // scale bytes of one head's row
+  static constexpr int SC_OFF = RPP * RB;            // offset of the scales in a stage
+  static constexpr int BYTES = RPP * RB + RPP * SCB; // bytes a piece receives
+  static_assert(BYTES <= SB, "a piece fits a stage");
 };
 
 // The warp-task attention plan of one step: the m readable slots of each kv head
@@ -1461,6 +1483,41 @@ __device__ __forceinline__ void mk_lds_dims(uint32_t a, float* v) {
   }
 }
 
+// Four int8 codes at a shared-memory address and their group scale -> f32
+// (code * scale, one correctly rounded product each, as the cache's reader).
+__device__ __forceinline__ void mk_lds_i8(uint32_t a, uint32_t sa, float* v) {
+  uint32_t u;
+  float sc;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(u) : "r"(a));
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sc) : "r"(sa));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __fmul_rn((float)(int)(signed char)((u >> (8 * i)) & 0xffu), sc);
+}
+
+// int8 cache: this lane's 4 channels of the current position's row (f32) ->
+// the values the cache will hold (per 32-channel group, eight lanes: s = max|x| /
+// 127, codes round(x / s) clamped to +-127, as the cache's quantiser); the lanes of
+// the task that holds the position also write the row's codes and scales for head g.
+__device__ __forceinline__ void mk_quant_i8_row(float* x, bool write, char* row, int code_off, int g, int HD) {
+  const int lane = threadIdx.x & 31;
+  float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float sc = __fdiv_rn(m, 127.0f);
+  uint32_t packed = 0u;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    int code = 0;
+    if (sc > 0.f) code = (int)fminf(fmaxf(roundf(__fdiv_rn(x[i], sc)), -127.0f), 127.0f);
+    x[i] = __fmul_rn((float)code, sc);
+    packed |= ((uint32_t)code & 0xffu) << (8 * i);
+  }
+  if (write) {
+    *reinterpret_cast<uint32_t*>(row + code_off + g * HD + lane * 4) = packed;
+    if ((lane & 7) == 0) reinterpret_cast<float*>(row)[g * (HD / 32) + (lane >> 3)] = sc;
+  }
+}
+
 template <typename W, typename KV, int HD, int GP>
 __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8_t* ureg, MkMisc* M, uint32_t& sc) {
   using AG = MkAttnGeom<W, KV, HD>;
@@ -1501,9 +1558,17 @@ __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8
     for (int h = 0; h < GP; ++h)
 #pragma unroll
       for (int d = 0; d < DPL; ++d) qv[h][d] = h < G ? __ldcg(P.q + (size_t)(g * G + h) * HD + lane * DPL + d) : 0.f;
-    const size_t co = (size_t)(has_cur ? slot_pos : 0) * kd + (size_t)g * HD + lane * DPL;
-    mk_load_dims<KV, DPL>(kc + co, kcur, true);
-    mk_load_dims<KV, DPL>(vc + co, vcur, true);
+    if constexpr (AG::I8) {
+      // int8 cache: this position's rows come in f32 from the QKV phase.
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(P.kv_cur + (size_t)g * HD + lane * DPL));
+      const float4 b = __ldcg(reinterpret_cast<const float4*>(P.kv_cur + kd + (size_t)g * HD + lane * DPL));
+      kcur[0] = a.x; kcur[1] = a.y; kcur[2] = a.z; kcur[3] = a.w;
+      vcur[0] = b.x; vcur[1] = b.y; vcur[2] = b.z; vcur[3] = b.w;
+    } else {
+      const size_t co = (size_t)(has_cur ? slot_pos : 0) * kd + (size_t)g * HD + lane * DPL;
+      mk_load_dims<KV, DPL>(kc + co, kcur, true);
+      mk_load_dims<KV, DPL>(vc + co, vcur, true);
+    }
    }
    if (task) {
     // (the scaling below is the first use of the loads above)
@@ -1515,6 +1580,14 @@ __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8
         qv[h][d] *= qscale;
         acc[h][d] = 0.f;
       }
+    if constexpr (AG::I8) {
+      static_assert(!AG::I8 || DPL == 4, "int8 cache rows: four channels per lane");
+      if (has_cur) {   // (uniform over the warp)
+        const size_t ro = (size_t)slot_pos * P.kv_row_bytes;
+        mk_quant_i8_row(kcur, true, (char*)L.kc + ro, P.kv_code_off, g, HD);
+        mk_quant_i8_row(vcur, true, (char*)L.vc + ro, P.kv_code_off, g, HD);
+      }
+    }
 #pragma unroll
     for (int d = 0; d < DPL; ++d) {
       kcur[d] = has_cur ? kcur[d] : 0.f;
@@ -1543,7 +1616,9 @@ __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8
         for (int kk = 0; kk < KG; ++kk) {
           const int r = q * KG + kk;
           float kv[DPL];
-          mk_lds_dims<KV, DPL>(ktile + (uint32_t)(r * RB), kv);
+          if constexpr (AG::I8)
+            mk_lds_i8(ktile + (uint32_t)(r * RB), ktile - lane_off + AG::SC_OFF + r * AG::SCB + (lane >> 3) * 4, kv);
+          else mk_lds_dims<KV, DPL>(ktile + (uint32_t)(r * RB), kv);
           const bool cur = c0 + r == slot_pos;
 #pragma unroll
           for (int d = 0; d < DPL; ++d) kv[d] = cur ? kcur[d] : kv[d];
@@ -1600,7 +1675,9 @@ __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8
 #pragma unroll
       for (int r = 0; r < RPP; ++r) {
         float vv[DPL];
-        mk_lds_dims<KV, DPL>(vtile + (uint32_t)(r * RB), vv);
+        if constexpr (AG::I8)
+          mk_lds_i8(vtile + (uint32_t)(r * RB), vtile - lane_off + AG::SC_OFF + r * AG::SCB + (lane >> 3) * 4, vv);
+        else mk_lds_dims<KV, DPL>(vtile + (uint32_t)(r * RB), vv);
         const bool cur = c0 + r == slot_pos, live = ok && r < nk;
         // Rows past the piece's keys may hold any bits: zero them (their weights are 0).
 #pragma unroll
@@ -1844,17 +1921,23 @@ __device__ void mk_prefetch_attention_kv(const MkParams& P, int l, int HD, int p
   }
   const int tasks = P.nkv * ns;
   int idx = part;
-  // With tensor maps (bf16 weights): one prefetch per piece (one ring stage of keys).
-  const int rpp = P.maps ? MkRing<__nv_bfloat16>::BYTES / (HD * kvb) : 0;
+  // With tensor maps (bf16 weights): one prefetch per piece (one ring stage of keys)
+  // and map: K and V, and with an int8 cache (MK_I8_RPP keys per piece) their scales too.
+  const bool i8 = P.kv_code_off > 0;
+  const int rpp = P.maps ? (i8 ? MK_I8_RPP : MkRing<__nv_bfloat16>::BYTES / (HD * kvb)) : 0;
+  const int kinds = i8 ? 4 : 2;
   for (int t = blockIdx.x; t < tasks; t += P.nb) {
     const int g = t / ns, split = t - g * ns;
     const int s0 = split * sps, j1 = min(min(s0 + sps, P.max_seq), m);
     const int n = j1 > s0 ? j1 - s0 : 0;
     if (rpp) {
       const int pieces = (n + rpp - 1) / rpp;
-      for (; idx < 2 * pieces; idx += nparts)
-        tma_prefetch_3d(P.maps + l * MAPS_PER_LAYER + ((idx & 1) ? MAP_V : MAP_K), 0, g, s0 + (idx >> 1) * rpp);
-      idx -= 2 * pieces;
+      for (; idx < kinds * pieces; idx += nparts) {
+        const int kind = idx % kinds;
+        const int map = kind == 0 ? MAP_K : kind == 1 ? MAP_V : kind == 2 ? MAP_KS : MAP_VS;
+        tma_prefetch_3d(P.maps + l * MAPS_PER_LAYER + map, 0, g, s0 + (idx / kinds) * rpp);
+      }
+      idx -= kinds * pieces;
       continue;
     }
     for (; idx < 2 * n; idx += nparts) {
@@ -1994,14 +2077,17 @@ __device__ void mk_produce(const MkParams& P, uint8_t* ring, MkMisc* M) {
                 for (int kv = 0; kv < 2 && ok; ++kv) {
                   // A tensor map moves the piece (RPP keys of head g) in one copy; the
                   // box is always whole (slots past the ring read as zeros, unused).
-                  const int st = claim((uint32_t)(P.maps ? AG::RPP * AG::RB : nk * AG::RB));
+                  const int st = claim((uint32_t)(P.maps ? AG::BYTES : nk * AG::RB));
                   if (st < 0) {
                     ok = false;
                     break;
                   }
                   if (P.maps) {
-                    tma_load_3d(wring + (size_t)st * SB, P.maps + l * MAPS_PER_LAYER + (kv ? MAP_V : MAP_K),
-                                &M->full[w][st], 0, g, c0);
+                    const CUtensorMap* lm = P.maps + l * MAPS_PER_LAYER;
+                    tma_load_3d(wring + (size_t)st * SB, lm + (kv ? MAP_V : MAP_K), &M->full[w][st], 0, g, c0);
+                    if constexpr (AG::I8)   // the piece's group scales after its codes
+                      tma_load_3d(wring + (size_t)st * SB + AG::SC_OFF, lm + (kv ? MAP_VS : MAP_KS), &M->full[w][st], 0,
+                                  g, c0);
                   } else {
                     const KV* base = (const KV*)(kv ? L.vc : L.kc);
                     for (int r = 0; r < nk; ++r)
@@ -2437,23 +2523,52 @@ static bool mk_build_maps(Model& m) {
     if (!mk_encode(&maps[head_map], m.head, (uint64_t)c.vocab, h)) return false;
   }
   // K and V rings: [slots][kv heads][head_dim], a box = one attention piece of one head.
-  const bool kvb16 = c.kv_dtype == DEC_BF16;
+  // int8 rings: rows of [scales][codes] (KvRowLayout); the codes map starts at the
+  // codes' offset, the scales map at the row (one head's scales = HD / 32 floats),
+  // both with the row as the slot stride; a box covers the piece's MK_I8_RPP keys.
+  const bool kvb16 = c.kv_dtype == DEC_BF16, kvi8 = c.kv_dtype == DEC_I8;
   const uint64_t es = kvb16 ? 2 : 4, hd = (uint64_t)c.head_dim;
+  const KvRowLayout rl = kv_row_layout(c);
   auto encode_ring = [&](CUtensorMap* t, const void* base) {
     auto fn = mk_encode_fn();
     if (!fn || !base) return false;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (kvi8) {
+      const cuuint64_t dims[3] = {hd, (cuuint64_t)c.n_kv_heads, (cuuint64_t)c.max_seq};
+      const cuuint64_t strides[2] = {hd, (cuuint64_t)rl.bytes};
+      const cuuint32_t box[3] = {(cuuint32_t)hd, 1, (cuuint32_t)MK_I8_RPP};
+      return fn(t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<char*>((const char*)base + rl.code_off), dims,
+                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
     const cuuint64_t dims[3] = {hd, (cuuint64_t)c.n_kv_heads, (cuuint64_t)c.max_seq};
     const cuuint64_t strides[2] = {hd * es, kd * es};
     const cuuint32_t box[3] = {(cuuint32_t)hd, 1, (cuuint32_t)(MkRing<__nv_bfloat16>::BYTES / (hd * es))};
-    const cuuint32_t estr[3] = {1, 1, 1};
     return fn(t, kvb16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base),
               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   };
+  auto encode_scales = [&](CUtensorMap* t, const void* base) {
+    auto fn = mk_encode_fn();
+    if (!fn || !base) return false;
+    const cuuint64_t dims[3] = {hd / 32, (cuuint64_t)c.n_kv_heads, (cuuint64_t)c.max_seq};
+    const cuuint64_t strides[2] = {hd / 32 * 4, (cuuint64_t)rl.bytes};
+    const cuuint32_t box[3] = {(cuuint32_t)(hd / 32), 1, (cuuint32_t)MK_I8_RPP};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(t, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerPtrs& L = m.layers[l];
     CUtensorMap* t = &maps[(size_t)l * MAPS_PER_LAYER];
-    if ((hd == 64 || hd == 128) && (!encode_ring(t + MAP_K, L.kc) || !encode_ring(t + MAP_V, L.vc))) return false;
+    if (kvi8) {
+      if (!decode_kv_i8_persistent(c) || !encode_ring(t + MAP_K, L.kc) || !encode_ring(t + MAP_V, L.vc) ||
+          !encode_scales(t + MAP_KS, L.kc) || !encode_scales(t + MAP_VS, L.vc))
+        return false;
+    } else if ((hd == 64 || hd == 128) && (!encode_ring(t + MAP_K, L.kc) || !encode_ring(t + MAP_V, L.vc))) {
+      return false;
+    }
   }
   return cudaMemcpy(m.mk_maps, maps.data(), sizeof(CUtensorMap) * maps.size(), cudaMemcpyHostToDevice) ==
          cudaSuccess;
@@ -2513,6 +2628,7 @@ static void* mk_pick(int hd) {
 // per-layer kernels), which keeps this file's build time in check.
 static void* mk_func(const dec_config& c) {
   const bool wb = c.weight_dtype == DEC_BF16, kb = c.kv_dtype == DEC_BF16;
+  if (c.kv_dtype == DEC_I8) return decode_kv_i8_persistent(c) ? (void*)k_decode_step<__nv_bfloat16, KVI8, 128> : nullptr;
   if (c.weight_quant) {
     if (!wb) return nullptr;   // 8-bit weights from f32 models decode on the row kernels
     return kb ? mk_pick<WQ8, __nv_bfloat16>(c.head_dim) : mk_pick<WQ8, float>(c.head_dim);
@@ -2636,7 +2752,10 @@ void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, in
   P.trace_cap = m.trace_cap;
   P.u_bytes = (int)mk_u_bytes(c, m.nsplit);
   P.stamps = m.mk_stamps;
-  P.kv_bytes = c.kv_dtype == DEC_BF16 ? 2 : 4;
+  P.kv_bytes = c.kv_dtype == DEC_BF16 ? 2 : c.kv_dtype == DEC_I8 ? 1 : 4;
+  P.kv_cur = S.kv_cur;
+  P.kv_code_off = c.kv_dtype == DEC_I8 ? kv_row_layout(c).code_off : 0;
+  P.kv_row_bytes = kv_row_layout(c).bytes;
   P.maps = reinterpret_cast<const CUtensorMap*>(m.mk_maps);
   P.xs_floats = mk_xs_floats(c, m.nsplit);
   P.xb_plane = mk_xb_plane(c);

@@ -129,6 +129,7 @@ struct Scratch {
   float* q8part;
   size_t q8part_bytes;
   float* fpart;         // persistent decode, fused FFN: [MK_MAX_NB][h] per-CTA down partials (nullable)
+  float* kv_cur;        // persistent decode, int8 cache: [2][n_kv*hd] f32 K and V of the current position
 };
 
 constexpr int LM_GRID_MAX = 1024;
@@ -201,6 +202,7 @@ struct WsPlan {
   size_t q8, q8_bytes;                  // weight_quant: codes and scales of every quantised matrix
   size_t deq, deq_bytes, q8part, q8part_bytes;
   size_t wdown_t, fpart;                // fused decode FFN: transposed down projections, partials
+  size_t kv_cur;                        // persistent decode, int8 cache: the current K/V rows in f32
   size_t kv;            // start of the KV rings: [layer][K, V][seq][ring_rows][n_kv*hd]
   size_t kv_layer_bytes; // one layer's K (or V) rings of every sequence
   size_t ring_bytes;    // one sequence's ring
@@ -249,11 +251,17 @@ struct KvRowLayout {
   int code_off;   // bytes before the codes (the scales' area)
   int group;      // channels per scale
 };
+// int8 caches at head_dim 128 with bf16 weights decode on the persistent step
+// (a head's group scales are one 16-byte block there, a whole TMA stride); the
+// per-layer decode kernels do not read int8 rows.
+inline bool decode_kv_i8_persistent(const dec_config& c) {
+  return c.kv_dtype == DEC_I8 && c.head_dim == 128 && c.weight_dtype == DEC_BF16 && !c.weight_quant;
+}
 // Models whose decode runs the row kernels (one row per step): the persistent
 // step and the per-layer decode kernels implement none of these.
 inline bool decode_needs_rows(const dec_config& c) {
-  return c.kv_dtype == DEC_I8 || c.qk_norm != 0 || c.sandwich_norms != 0 || c.rope_theta_local > 0.f ||
-         c.page_size > 0;
+  return (c.kv_dtype == DEC_I8 && !decode_kv_i8_persistent(c)) || c.qk_norm != 0 || c.sandwich_norms != 0 ||
+         c.rope_theta_local > 0.f || c.page_size > 0;
 }
 // Whether layer l rotates with the global base (every layer without a local base).
 inline bool layer_rope_global(const dec_config& c, int l) {

@@ -144,3 +144,58 @@ def test_qwen_shape_int8_batched(dec_mod):
         ref, sess = _oracle_int8(w, p, taus[s_], 5)
         compare_logits(np.stack(rows[s_]), ref, TOL_BF16_ABS, TOL_BF16_REL)
         _check_ring_codes(d, dec_mod, w, sess, lens[s_] + 5, seq=s_)
+
+
+# The persistent decode step with an int8 cache (head_dim 128, bf16 weights): the
+# warp attention reads each piece's codes and group scales by TMA and multiplies
+# them back in registers; the task holding the current position quantises that row
+# itself (the QKV phase leaves it in f32) with the cache's rule and writes it.
+
+
+def _persistent_int8_case(dec_mod, w, P, D, seed):
+    d = dec_mod.Decoder(w, kv_dtype="i8")
+    d.set_fused("grid")
+    assert d.fused_mode() == "grid"
+    prompt = synthetic.prompt_tokens(w, P, seed=seed)
+    rows, taus = gpu_greedy(d, prompt, D, use_device_argmax=True)
+    ref, sess = _oracle_int8(w, prompt, taus, D)
+    compare_logits(rows, ref, TOL_BF16_ABS, TOL_BF16_REL)
+    check_greedy_tokens(ref, taus, TOL_BF16_ABS)
+    _check_ring_codes(d, dec_mod, w, sess, P + D)
+    return d, prompt, rows, taus
+
+
+def test_mistral_shape_int8_persistent_long_prompt(dec_mod):
+    # 300 keys per kv head: several 16-key pieces per warp and splits merged across CTAs.
+    w = synthetic.workload("mistral-7b", n_layers=2, sliding_window=0, max_seq=320)
+    _persistent_int8_case(dec_mod, w, 300, 8, seed=21)
+
+
+def test_mistral_shape_int8_persistent_window_wraps(dec_mod):
+    w = synthetic.workload("mistral-7b", n_layers=2, sliding_window=40, max_seq=40)
+    _persistent_int8_case(dec_mod, w, 36, 12, seed=22)
+
+
+def test_mixtral_shape_int8_persistent(dec_mod):
+    w = synthetic.workload("mixtral-8x7b", n_layers=2, max_seq=96)
+    _persistent_int8_case(dec_mod, w, 64, 6, seed=23)
+
+
+def test_int8_persistent_step_agrees_with_row_kernels(dec_mod):
+    # The same model and prompt decoded by the persistent step and by the row kernels
+    # (one row per step): the same tokens, logits within rounding.  The two paths
+    # project K/V with different summation orders, so a channel at a code boundary
+    # can land one int8 step apart (a step is 1/127 of its group's largest value):
+    # the bound is looser than for the f32 cache.
+    w = synthetic.workload("mistral-7b", n_layers=2, sliding_window=0, max_seq=96)
+    prompt = synthetic.prompt_tokens(w, 70, seed=24)
+    out = {}
+    weights = None
+    for mode in ("grid", "off"):
+        d = dec_mod.Decoder(w, kv_dtype="i8", weights=weights)
+        weights = d.weights
+        d.set_fused(mode)
+        out[mode] = gpu_greedy(d, prompt, 8)
+        d.close()
+    assert out["grid"][1] == out["off"][1]
+    np.testing.assert_allclose(out["grid"][0], out["off"][0], atol=1e-2, rtol=1e-3)
