@@ -103,8 +103,8 @@ TRAFFIC = {
         "bytes": 1814336, "source": "decoder_only_forward_gb300/csrc/decode.cu",
         "sha256": "3d7213fecd5001252701110382d8e9dfd57676011ecc1ded9bf6666198c7ae34"},
     ("mixtral-8x7b", "step"): {
-        "bytes": 25946351872, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
-        "sha256": "73e512ac28b166757929af777b964b298b250d7d1f2bf9c8696f3fd1a4c0f73a"},
+        "bytes": 25913366528, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
+        "sha256": "581e71aab27f9e21b5df84c7c1422ef19d684902f6909f16ecd9f57d5299f9c6"},
     ("mistral-7b", "step"): {
         "bytes": 15712395008, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
         "sha256": "4bf7258819f5eaeff409afa95ceaa4deb2af4270224b2c6b5de9309906a0eb17"},

@@ -76,10 +76,12 @@ typedef struct dec_config {
   int32_t tied_embedding; /* 1: LM head = token embedding matrix */
   int32_t qkv_bias;       /* 1: bqkv present */
   int32_t weight_dtype;   /* DEC_F32 or DEC_BF16: projection, embedding, router, head matrices */
-  int32_t kv_dtype;       /* DEC_F32, DEC_BF16 or DEC_I8: KV cache storage.  With DEC_I8 (and with
-                             qk_norm or sandwich_norms) every decode step (dec_decode, dec_decode_dev)
-                             runs the batched row kernels with one row; the fused schedules are not
-                             available */
+  int32_t kv_dtype;       /* DEC_F32, DEC_BF16 or DEC_I8: KV cache storage.  With DEC_I8, decode
+                             (dec_decode, dec_decode_dev) runs the persistent schedules when head_dim
+                             is 128 with bf16 weights and no weight_quant (the attention reads the
+                             codes and scales, and quantises the new position's row itself); otherwise,
+                             and under DEC_FUSED_OFF, and with qk_norm or sandwich_norms, it runs the
+                             batched row kernels with one row */
   float rms_eps;
   float rope_theta;
   int32_t rope_llama3;    /* 1: llama3 frequency scaling with the four fields below */
