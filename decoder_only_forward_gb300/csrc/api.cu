@@ -321,7 +321,7 @@ WsPlan dec::plan_workspace(const dec_config& c) {
     p.wdown_t = take(ft ? (size_t)c.n_layers * E1 * c.ffn * c.hidden * 2 : 0);
     p.fpart = take(ft ? (size_t)MK_MAX_NB * c.hidden * 4 : 0);
   }
-  p.kv_cur = take(decode_kv_i8_persistent(c) ? 2 * 4 * (size_t)kd : 0);
+  p.kv_cur = take(decode_kv_i8_persistent(c) || decode_qkn_persistent(c) ? 2 * 4 * (size_t)kd : 0);
   // KV rings: [layer][K, V][seq][ring_rows][n_kv*hd], ring_rows = max_seq
   // rounded up to 64 rows so every ring starts 256-byte aligned.
   p.n_seqs = c.n_seqs > 0 ? c.n_seqs : 1;
@@ -499,7 +499,7 @@ dec_status dec_create(const dec_config* cfg, const dec_weights* w, void* workspa
     d.w_down_t = nullptr;
   }
   S.fpart = nullptr;
-  S.kv_cur = decode_kv_i8_persistent(*cfg) ? (float*)(base + p.kv_cur) : nullptr;
+  S.kv_cur = decode_kv_i8_persistent(*cfg) || decode_qkn_persistent(*cfg) ? (float*)(base + p.kv_cur) : nullptr;
   if (mk_ffn_fused_layout(*cfg)) {
     // The persistent step's fused FFN reads each layer's down projection transposed.
     const size_t E1 = cfg->n_experts ? (size_t)cfg->n_experts : 1;
@@ -765,10 +765,11 @@ static dec_status run_decode_step(dec_handle* h, const int32_t* d_token, int32_t
                                   float* logits, int32_t* d_argmax) {
   const bool cluster = h->fused_mode == DEC_FUSED_CLUSTER && h->m.mk_cluster > 0;
   const bool fused = h->m.mk_ok && (cluster || h->fused_mode == DEC_FUSED_GRID);
-  if (decode_needs_rows(h->m.cfg) || ((h->m.wq8 || h->m.cfg.kv_dtype == DEC_I8) && !fused)) {
-    // QK-norm, sandwich norms and the int8 caches the persistent step does not
-    // read run on the row kernels: one row, sequence 0; so do 8-bit weights and
-    // int8 caches when the persistent step is not taken.
+  if (decode_needs_rows(h->m.cfg) ||
+      ((h->m.wq8 || h->m.cfg.kv_dtype == DEC_I8 || h->m.cfg.qk_norm != 0) && !fused)) {
+    // Sandwich norms, the row-long QK-norm and the int8 caches the persistent step
+    // does not read run on the row kernels: one row, sequence 0; so do 8-bit weights,
+    // int8 caches and QK-norm when the persistent step is not taken.
     const int32_t seq0 = 0;
     return run_rows(h, 1, &seq0, &pos, d_token, token, logits, d_argmax);
   }

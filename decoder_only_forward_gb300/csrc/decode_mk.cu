@@ -148,6 +148,7 @@ struct MkParams {
   float* kv_cur;                  // int8 cache: [2][nkv*hd] this position's K and V rows in f32
   int kv_code_off;                // int8 cache: byte offset of a row's codes (after its scales)
   int kv_row_bytes;               // int8 cache: bytes of one ring row
+  int qkn;                        // per-head QK-norm: q and the current k are normalised and rotated in ATTN
 };
 
 // The weight rows one CTA handles in one phase: up to k contiguous segments
@@ -771,7 +772,7 @@ __device__ __forceinline__ void mk_epi_pair(const MkParams& P, int ph, const MkL
       v0 += L.bqkv[row];
       v1 += L.bqkv[row + 1];
     }
-    if (row < qd + kd) {
+    if (row < qd + kd && !P.qkn) {   // (QK-norm: normalised before the rotation, in ATTN)
       const int d = (row < qd ? row : row - qd) % P.hd;
       const float2 cs = M->cs[d >> 1];
       const float b0 = v0 * cs.x - v1 * cs.y, b1 = v0 * cs.y + v1 * cs.x;
@@ -788,6 +789,9 @@ __device__ __forceinline__ void mk_epi_pair(const MkParams& P, int ph, const MkL
       P.kv_cur[row - qd] = v0;
       P.kv_cur[row - qd + 1] = v1;
       (void)slot;
+    } else if (P.qkn && row < qd + kd) {   // raw k, normalised and stored by ATTN
+      P.kv_cur[row - qd] = v0;
+      P.kv_cur[row - qd + 1] = v1;
     } else {
       const bool is_k = row < qd + kd;
       KV* dst = (KV*)(is_k ? L.kc : L.vc);
@@ -1566,12 +1570,55 @@ __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8
       vcur[0] = b.x; vcur[1] = b.y; vcur[2] = b.z; vcur[3] = b.w;
     } else {
       const size_t co = (size_t)(has_cur ? slot_pos : 0) * kd + (size_t)g * HD + lane * DPL;
-      mk_load_dims<KV, DPL>(kc + co, kcur, true);
+      if (P.qkn) {   // the raw k of this position (f32, from the QKV phase)
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) kcur[d] = __ldcg(P.kv_cur + (size_t)g * HD + lane * DPL + d);
+      } else {
+        mk_load_dims<KV, DPL>(kc + co, kcur, true);
+      }
       mk_load_dims<KV, DPL>(vc + co, vcur, true);
     }
    }
    if (task) {
-    // (the scaling below is the first use of the loads above)
+    if constexpr (!AG::I8) {
+      if (P.qkn) {
+        // Per-head QK-norm, then the rotation (rml "The decoder", One forward pass):
+        // each of the task's query heads and the current key is RMS-normalised over
+        // head_dim with its shared weight, then turned by this position's adjacent-pair
+        // table; the task that holds the position stores the key.
+        const float* wq = L.q_norm;
+        const float* wk = L.k_norm;
+        float w_q[DPL], w_k[DPL];
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) {
+          w_q[d] = wq[lane * DPL + d];
+          w_k[d] = wk[lane * DPL + d];
+        }
+        auto norm_rope = [&](float* x, const float* w) {
+          float ss = 0.f;
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) ss = fmaf(x[d], x[d], ss);
+          const float inv = 1.0f / sqrtf(warp_sum(ss) / (float)HD + P.eps);
+#pragma unroll
+          for (int d = 0; d < DPL; d += 2) {
+            const float a = x[d] * inv * w[d], b = x[d + 1] * inv * w[d + 1];
+            const float2 c = M->cs[(lane * DPL + d) >> 1];
+            x[d] = a * c.x - b * c.y;
+            x[d + 1] = a * c.y + b * c.x;
+          }
+        };
+#pragma unroll
+        for (int h = 0; h < GP; ++h)
+          if (h < G) norm_rope(qv[h], w_q);
+        norm_rope(kcur, w_k);
+        if (has_cur) {
+          KV* dst = (KV*)L.kc + (size_t)slot_pos * kd + (size_t)g * HD + lane * DPL;
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) dst[d] = from_f32<KV>(kcur[d]);
+        }
+      }
+    }
+    // (the scaling below is the first use of the loads above, QK-norm aside)
     float acc[GP][DPL];
 #pragma unroll
     for (int h = 0; h < GP; ++h)
@@ -2727,7 +2774,8 @@ void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, in
   P.eps = c.rms_eps;
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerPtrs& d = m.layers[l];
-    P.layers[l] = MkLayer{d.attn_norm, d.wqkv, d.bqkv, d.wo, d.ffn_norm, d.w_gateup, d.w_down, d.router, d.kc, d.vc};
+    P.layers[l] = MkLayer{d.attn_norm, d.wqkv,  d.bqkv, d.wo, d.ffn_norm, d.w_gateup, d.w_down,
+                          d.router,    d.kc,    d.vc,   d.q_norm, d.k_norm};
   }
   P.embed = m.tok_embd;
   P.out_norm = m.out_norm;
@@ -2756,6 +2804,7 @@ void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, in
   P.kv_cur = S.kv_cur;
   P.kv_code_off = c.kv_dtype == DEC_I8 ? kv_row_layout(c).code_off : 0;
   P.kv_row_bytes = kv_row_layout(c).bytes;
+  P.qkn = decode_qkn_persistent(c) ? 1 : 0;
   P.maps = reinterpret_cast<const CUtensorMap*>(m.mk_maps);
   P.xs_floats = mk_xs_floats(c, m.nsplit);
   P.xb_plane = mk_xb_plane(c);

@@ -41,6 +41,8 @@ struct MkLayer {
   const void* router;
   void* kc;
   void* vc;
+  const float* q_norm;   // per-head QK-norm weights [head_dim] (nullable)
+  const float* k_norm;
 };
 
 // An 8-bit projection matrix (weight_quant = 1): int8 codes [rows][cols] and one
@@ -129,7 +131,7 @@ struct Scratch {
   float* q8part;
   size_t q8part_bytes;
   float* fpart;         // persistent decode, fused FFN: [MK_MAX_NB][h] per-CTA down partials (nullable)
-  float* kv_cur;        // persistent decode, int8 cache: [2][n_kv*hd] f32 K and V of the current position
+  float* kv_cur;        // persistent decode, int8 cache or QK-norm: [2][n_kv*hd] f32 K and V of the current position
 };
 
 constexpr int LM_GRID_MAX = 1024;
@@ -259,9 +261,17 @@ inline bool decode_kv_i8_persistent(const dec_config& c) {
 }
 // Models whose decode runs the row kernels (one row per step): the persistent
 // step and the per-layer decode kernels implement none of these.
+// Per-head QK-norm (one shared head_dim weight) decodes on the persistent step at
+// head_dim 64 / 128 with bf16 weights and an f32 cache: the attention task normalises
+// and rotates its heads' q and the current k itself (the QKV phase leaves them raw).
+// The row-long norm needs a whole row's sum and stays on the row kernels.
+inline bool decode_qkn_persistent(const dec_config& c) {
+  return c.qk_norm == 1 && c.kv_dtype == DEC_F32 && c.weight_dtype == DEC_BF16 && !c.weight_quant &&
+         (c.head_dim == 64 || c.head_dim == 128);
+}
 inline bool decode_needs_rows(const dec_config& c) {
-  return (c.kv_dtype == DEC_I8 && !decode_kv_i8_persistent(c)) || c.qk_norm != 0 || c.sandwich_norms != 0 ||
-         c.rope_theta_local > 0.f || c.page_size > 0;
+  return (c.kv_dtype == DEC_I8 && !decode_kv_i8_persistent(c)) || (c.qk_norm != 0 && !decode_qkn_persistent(c)) ||
+         c.sandwich_norms != 0 || c.rope_theta_local > 0.f || c.page_size > 0;
 }
 // Whether layer l rotates with the global base (every layer without a local base).
 inline bool layer_rope_global(const dec_config& c, int l) {

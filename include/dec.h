@@ -80,7 +80,7 @@ typedef struct dec_config {
                              (dec_decode, dec_decode_dev) runs the persistent schedules when head_dim
                              is 128 with bf16 weights and no weight_quant (the attention reads the
                              codes and scales, and quantises the new position's row itself); otherwise,
-                             and under DEC_FUSED_OFF, and with qk_norm or sandwich_norms, it runs the
+                             and under DEC_FUSED_OFF, and with sandwich_norms or qk_norm 2, it runs the
                              batched row kernels with one row */
   float rms_eps;
   float rope_theta;
@@ -107,7 +107,9 @@ typedef struct dec_config {
                              before RoPE, q and k are RMS-normalised with eps = rms_eps.  0 off; 1 per head
                              with one [head_dim] weight shared by the heads (q_norm, k_norm); 2 over the whole
                              q / k row with [n_heads*head_dim] / [n_kv_heads*head_dim] weights.  Not with a
-                             DEC_BF16 cache (DEC_EINVAL) */
+                             DEC_BF16 cache (DEC_EINVAL).  Decode: mode 1 with bf16 weights, an f32 cache and
+                             head_dim 64 / 128 runs the persistent schedules (the attention normalises and
+                             rotates q and the new k); other cases, and DEC_FUSED_OFF, run the row kernels */
   int32_t sandwich_norms; /* 1: each block's output (attention after wo, FFN after the down projection or
                              the expert sum) is RMS-normalised with post_attn_norm / post_ffn_norm before
                              the residual add (rml "The decoder", One forward pass step 6) */

@@ -141,3 +141,46 @@ def test_qwen_shape_per_layer_base_batched(dec_mod):
     for s_, p in enumerate(prompts):
         ref, _ = oracle_teacher_forced(w, p, taus[s_], 4)
         compare_logits(np.stack(rows[s_]), ref, *tolerances(w))
+
+
+# Per-head QK-norm on the persistent decode step (bf16 weights, f32 cache, head_dim
+# 64 / 128): the QKV phase leaves q and the new k unrotated, and the attention task
+# normalises each head over head_dim, rotates it and stores the key.
+
+
+def _persistent_qkn(dec_mod, w, P, D, seed):
+    d = dec_mod.Decoder(w)
+    d.set_fused("grid")
+    assert d.fused_mode() == "grid"
+    prompt = synthetic.prompt_tokens(w, P, seed=seed)
+    rows, taus = gpu_greedy(d, prompt, D, use_device_argmax=True)
+    ref, _ = oracle_teacher_forced(w, prompt, taus, D)
+    compare_logits(rows, ref, *tolerances(w))
+    check_greedy_tokens(ref, taus, tolerances(w)[0])
+    d.close()
+
+
+def test_mistral_shape_qk_norm_persistent_window_wraps(dec_mod):
+    w = synthetic.workload("mistral-7b", n_layers=2, sliding_window=24, max_seq=24, qk_norm="head")
+    _persistent_qkn(dec_mod, w, 30, 10, seed=41)
+
+
+def test_qwen_shape_qk_norm_persistent_khalf(dec_mod):
+    # head_dim 64, seven query heads per kv head, q/k biases, kHalf-permuted norm weights.
+    w = synthetic.workload("qwen2.5-0.5b", n_layers=2, max_seq=96, qk_norm="head", rope_half=True)
+    _persistent_qkn(dec_mod, w, 60, 8, seed=42)
+
+
+def test_qk_norm_persistent_step_agrees_with_row_kernels(dec_mod):
+    w = synthetic.workload("mistral-7b", n_layers=2, sliding_window=0, max_seq=96, qk_norm="head")
+    prompt = synthetic.prompt_tokens(w, 70, seed=43)
+    out = {}
+    weights = None
+    for mode in ("grid", "off"):
+        d = dec_mod.Decoder(w, weights=weights)
+        weights = d.weights
+        d.set_fused(mode)
+        out[mode] = gpu_greedy(d, prompt, 8)
+        d.close()
+    assert out["grid"][1] == out["off"][1]
+    np.testing.assert_allclose(out["grid"][0], out["off"][0], atol=2e-3, rtol=1e-4)
