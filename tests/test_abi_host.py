@@ -190,20 +190,14 @@ def test_header_is_plain_c(tmp_path):
 def test_workspace_holds_the_transposed_down_copy_when_the_ffn_fuses(dec):
     # bf16 weights, hidden a multiple of 128 and ffn a multiple of 16: the workspace
     # gains a transposed copy of every down projection (2 bytes per element) and
-    # 256 x hidden floats of partial sums; 8-bit weights or ffn off the 16 grid do not.
+    # 256 x hidden floats of partial sums.  With ffn 8 past a multiple of 16 it does not
+    # (its other regions grow by a little for the 8 extra columns).
     base = synthetic.workload("mistral-7b", n_layers=2, max_seq=64)
-    ws = dec.workspace_bytes(dec.make_config(base))
-    ws_q8 = dec.workspace_bytes(dec.make_config(dict(base, weight_int8=True)))
-    copy = 2 * base["n_layers"] * base["ffn"] * base["hidden"]
-    parts = 256 * base["hidden"] * 4
-    assert ws >= copy + parts
-    # the 8-bit workspace holds codes and scales of every projection instead (about half
-    # the bf16 sizes) but no transposed copy
     odd = dict(base, ffn=base["ffn"] + 8)
+    ws = dec.workspace_bytes(dec.make_config(base))
     ws_odd = dec.workspace_bytes(dec.make_config(odd))
-    grow = ws - ws_odd   # 8 fewer ffn columns, but the copy and the partials are gone in `odd`
-    assert copy + parts - 8 * 2 * base["n_layers"] * base["hidden"] * 4 <= grow <= copy + parts + (1 << 24)
-    assert ws_q8 > 0
+    extra = 2 * base["n_layers"] * base["ffn"] * base["hidden"] + 256 * base["hidden"] * 4
+    assert extra - (1 << 20) <= ws - ws_odd <= extra
 
 
 def test_workspace_holds_the_current_kv_rows_for_int8_and_qk_norm_decode(dec):
