@@ -766,10 +766,12 @@ static dec_status run_decode_step(dec_handle* h, const int32_t* d_token, int32_t
   const bool cluster = h->fused_mode == DEC_FUSED_CLUSTER && h->m.mk_cluster > 0;
   const bool fused = h->m.mk_ok && (cluster || h->fused_mode == DEC_FUSED_GRID);
   if (decode_needs_rows(h->m.cfg) ||
-      ((h->m.wq8 || h->m.cfg.kv_dtype == DEC_I8 || h->m.cfg.qk_norm != 0) && !fused)) {
+      ((h->m.wq8 || h->m.cfg.kv_dtype == DEC_I8 || h->m.cfg.qk_norm != 0 || h->m.cfg.rope_theta_local > 0.f) &&
+       !fused)) {
     // Sandwich norms, the row-long QK-norm and the int8 caches the persistent step
     // does not read run on the row kernels: one row, sequence 0; so do 8-bit weights,
-    // int8 caches and QK-norm when the persistent step is not taken.
+    // int8 caches, QK-norm and the per-layer RoPE base when the persistent step is
+    // not taken (the per-layer decode kernels implement none of them).
     const int32_t seq0 = 0;
     return run_rows(h, 1, &seq0, &pos, d_token, token, logits, d_argmax);
   }

@@ -118,6 +118,7 @@ struct MkParams {
   const void* head;
   DeviceState* st;
   const double* inv_freq;
+  const double* inv_freq_local;   // per-layer RoPE base: the local layers' frequencies (nullable)
   float* x;
   float* q;
   float* attn;
@@ -177,7 +178,7 @@ struct MkMisc {
   uint64_t full[MK_COMPUTE_WARPS][MK_MAX_STAGES];
   uint64_t empty[MK_COMPUTE_WARPS][MK_MAX_STAGES];
   float part[MK_CHUNK][MK_COMPUTE_WARPS][MK_TM];  // tensor-core GEMV: per-warp row partials
-  float2 cs[64];                 // (cos, sin) of this position's rotary pairs
+  float2 cs[128];                // (cos, sin) of this position's rotary pairs; [64..]: the local base's
   float red[40];
   float logits[MAX_EXPERTS];
   int ids[MAX_EXPERTS_USED];
@@ -774,7 +775,7 @@ __device__ __forceinline__ void mk_epi_pair(const MkParams& P, int ph, const MkL
     }
     if (row < qd + kd && !P.qkn) {   // (QK-norm: normalised before the rotation, in ATTN)
       const int d = (row < qd ? row : row - qd) % P.hd;
-      const float2 cs = M->cs[d >> 1];
+      const float2 cs = M->cs[(L.rope_local ? 64 : 0) + (d >> 1)];
       const float b0 = v0 * cs.x - v1 * cs.y, b1 = v0 * cs.y + v1 * cs.x;
       v0 = b0;
       v1 = b1;
@@ -1602,7 +1603,7 @@ __device__ bool mk_attention_warp(const MkParams& P, int l, uint8_t* ring, uint8
 #pragma unroll
           for (int d = 0; d < DPL; d += 2) {
             const float a = x[d] * inv * w[d], b = x[d + 1] * inv * w[d + 1];
-            const float2 c = M->cs[(lane * DPL + d) >> 1];
+            const float2 c = M->cs[(L.rope_local ? 64 : 0) + ((lane * DPL + d) >> 1)];
             x[d] = a * c.x - b * c.y;
             x[d + 1] = a * c.y + b * c.x;
           }
@@ -2045,6 +2046,10 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_step(const __grid_cons
     double sn, cn;
     sincos((double)P.pos * P.inv_freq[i], &sn, &cn);
     M->cs[i] = make_float2((float)cn, (float)sn);
+    if (P.inv_freq_local) {   // per-layer RoPE base: the local layers' table
+      sincos((double)P.pos * P.inv_freq_local[i], &sn, &cn);
+      M->cs[64 + i] = make_float2((float)cn, (float)sn);
+    }
   }
   __syncthreads();
   // Cluster mode: every CTA's barrier is initialised before any remote
@@ -2774,14 +2779,15 @@ void launch_decode_mk(const Model& m, cudaStream_t s, const int32_t* d_token, in
   P.eps = c.rms_eps;
   for (int l = 0; l < c.n_layers; ++l) {
     const LayerPtrs& d = m.layers[l];
-    P.layers[l] = MkLayer{d.attn_norm, d.wqkv,  d.bqkv, d.wo, d.ffn_norm, d.w_gateup, d.w_down,
-                          d.router,    d.kc,    d.vc,   d.q_norm, d.k_norm};
+    P.layers[l] = MkLayer{d.attn_norm, d.wqkv,  d.bqkv, d.wo,     d.ffn_norm, d.w_gateup, d.w_down,
+                          d.router,    d.kc,    d.vc,   d.q_norm, d.k_norm,   layer_rope_global(c, l) ? 0 : 1};
   }
   P.embed = m.tok_embd;
   P.out_norm = m.out_norm;
   P.head = m.head;
   P.st = S.st;
   P.inv_freq = S.inv_freq;
+  P.inv_freq_local = S.inv_freq_local;
   P.x = S.x;
   P.q = S.q;
   P.attn = S.attn;

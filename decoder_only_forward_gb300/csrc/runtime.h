@@ -43,6 +43,7 @@ struct MkLayer {
   void* vc;
   const float* q_norm;   // per-head QK-norm weights [head_dim] (nullable)
   const float* k_norm;
+  int rope_local;        // 1: this layer rotates with the local base (per-layer RoPE base)
 };
 
 // An 8-bit projection matrix (weight_quant = 1): int8 codes [rows][cols] and one
@@ -271,7 +272,7 @@ inline bool decode_qkn_persistent(const dec_config& c) {
 }
 inline bool decode_needs_rows(const dec_config& c) {
   return (c.kv_dtype == DEC_I8 && !decode_kv_i8_persistent(c)) || (c.qk_norm != 0 && !decode_qkn_persistent(c)) ||
-         c.sandwich_norms != 0 || c.rope_theta_local > 0.f || c.page_size > 0;
+         c.sandwich_norms != 0 || c.page_size > 0;
 }
 // Whether layer l rotates with the global base (every layer without a local base).
 inline bool layer_rope_global(const dec_config& c, int l) {

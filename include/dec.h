@@ -116,7 +116,9 @@ typedef struct dec_config {
   float rope_theta_local; /* per-layer RoPE base (sipllm "Transformer forward pass", RoPE: Gemma 3): 0 = one
                              base; else local layers rotate with this base (no llama3 scaling) and every
                              rope_global_every-th layer, l with (l + 1) % rope_global_every == 0, with
-                             rope_theta (0 = no global layer) */
+                             rope_theta (0 = no global layer).  Decode takes the persistent schedules
+                             (both tables per step) when the rest of the config allows; DEC_FUSED_OFF runs
+                             the row kernels */
   int32_t rope_global_every;
   int32_t page_size;      /* 0: each sequence owns contiguous K/V rings of max_seq rows.  Else a paged cache
                              (rml "The decoder", KV cache): slots are grouped in pages of page_size positions

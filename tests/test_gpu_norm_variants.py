@@ -184,3 +184,18 @@ def test_qk_norm_persistent_step_agrees_with_row_kernels(dec_mod):
         d.close()
     assert out["grid"][1] == out["off"][1]
     np.testing.assert_allclose(out["grid"][0], out["off"][0], atol=2e-3, rtol=1e-4)
+
+
+def test_qwen_shape_per_layer_base_persistent(dec_mod):
+    # Per-layer RoPE base on the persistent step: the step builds both (cos, sin) tables
+    # and each layer's QKV phase turns q and k with its own.
+    w = synthetic.workload("qwen2.5-0.5b", n_layers=3, max_seq=96, rope_theta_local=10000.0,
+                           rope_global_every=3)
+    _persistent_qkn(dec_mod, w, 50, 8, seed=44)
+
+
+def test_mistral_shape_qk_norm_per_layer_base_persistent(dec_mod):
+    # QK-norm and a per-layer base together: the attention task rotates with the layer's table.
+    w = synthetic.workload("mistral-7b", n_layers=2, max_seq=64, qk_norm="head", rope_theta_local=500.0,
+                           rope_global_every=2)
+    _persistent_qkn(dec_mod, w, 40, 8, seed=45)
