@@ -103,8 +103,8 @@ TRAFFIC = {
         "bytes": 1814336, "source": "decoder_only_forward_gb300/csrc/decode.cu",
         "sha256": "3d7213fecd5001252701110382d8e9dfd57676011ecc1ded9bf6666198c7ae34"},
     ("mixtral-8x7b", "step"): {
-        "bytes": 25926079488, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
-        "sha256": "4886ab89347b0b29c96c7171018d8b11b1b2d07139cc1996e70378f400348252"},
+        "bytes": 25920759040, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
+        "sha256": "089d684fe53ae73b10b7d86dd4ca97ea9697d93c4a182b0a69e84d1ef790b4dd"},
     ("mistral-7b", "step"): {
         "bytes": 15712395008, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
         "sha256": "4bf7258819f5eaeff409afa95ceaa4deb2af4270224b2c6b5de9309906a0eb17"},

@@ -20,6 +20,10 @@
 //   OPROJ  split merge (small sets) -> x += Wo o
 //   GATEUP RMSNorm -> silu(gate) * up (dense), or router -> top-k -> renormalise (MoE)
 //   DOWN   x += Wd act (MoE: selected experts in selection order)
+// or, with the fused FFN (bf16 weights, hidden % 128 == 0, ffn % 16 == 0):
+//   FFN    RMSNorm [-> router] -> each CTA's (slot, ffn) slice: silu(gate) * up, then
+//          that slice's rows of the transposed Wd into a partial sum over hidden
+//   SUM    x += the CTAs' partials, summed in CTA order
 // then LMHEAD: final RMSNorm -> logits + argmax.  Cross-CTA data (x, q,
 // partials, act) is read with ld.global.cg so no stale L1 line is used.
 #include <cudaTypedefs.h>
