@@ -301,7 +301,10 @@ typedef enum dec_schedule {
 dec_status dec_set_fused(dec_handle *h, int32_t mode);
 
 /* Whether a schedule can run on this handle: 1 (DEC_FUSED_OFF, DEC_FUSED_GRID),
- * the cluster's CTA count (DEC_FUSED_CLUSTER), or 0. */
+ * the cluster's CTA count (DEC_FUSED_CLUSTER), or 0.  The persistent schedules need
+ * at most 128 layers (the layer table travels in the kernel's parameters), at most 8
+ * query heads per kv head at head_dim 64 and 4 at head_dim 128, and a shared-memory
+ * plan within the GPU's limit. */
 int32_t dec_fused_available(const dec_handle *h, int32_t mode);
 
 /* The schedule the next decode step takes (after any fallback); -1 for NULL. */
