@@ -105,9 +105,6 @@ TRAFFIC = {
     ("mixtral-8x7b", "step"): {
         "bytes": 25920759040, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
         "sha256": "089d684fe53ae73b10b7d86dd4ca97ea9697d93c4a182b0a69e84d1ef790b4dd"},
-    ("mistral-7b", "step"): {
-        "bytes": 15712395008, "source": "decoder_only_forward_gb300/csrc/decode_mk.cu",
-        "sha256": "4bf7258819f5eaeff409afa95ceaa4deb2af4270224b2c6b5de9309906a0eb17"},
 }
 
 
