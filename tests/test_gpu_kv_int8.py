@@ -199,3 +199,24 @@ def test_int8_persistent_step_agrees_with_row_kernels(dec_mod):
         d.close()
     assert out["grid"][1] == out["off"][1]
     np.testing.assert_allclose(out["grid"][0], out["off"][0], atol=1e-2, rtol=1e-3)
+
+
+def test_int8_persistent_grid_and_cluster_agree(dec_mod):
+    # The one-cluster schedule runs the same int8-cache attention code on 16 (or 8) CTAs.
+    w = synthetic.workload("mistral-7b", n_layers=2, sliding_window=0, max_seq=96)
+    prompt = synthetic.prompt_tokens(w, 50, seed=25)
+    out = {}
+    weights = None
+    for mode in ("grid", "cluster"):
+        d = dec_mod.Decoder(w, kv_dtype="i8", weights=weights)
+        weights = d.weights
+        if not d.fused_available(mode):
+            assert mode == "cluster"
+            d.close()
+            continue
+        d.set_fused(mode)
+        out[mode] = gpu_greedy(d, prompt, 6)
+        d.close()
+    if "cluster" in out:
+        assert out["grid"][1] == out["cluster"][1]
+        np.testing.assert_allclose(out["grid"][0], out["cluster"][0], atol=2e-3, rtol=1e-4)

@@ -199,3 +199,24 @@ def test_mistral_shape_qk_norm_per_layer_base_persistent(dec_mod):
     w = synthetic.workload("mistral-7b", n_layers=2, max_seq=64, qk_norm="head", rope_theta_local=500.0,
                            rope_global_every=2)
     _persistent_qkn(dec_mod, w, 40, 8, seed=45)
+
+
+def test_qk_norm_persistent_grid_and_cluster_agree(dec_mod):
+    w = synthetic.workload("qwen2.5-0.5b", n_layers=2, max_seq=96, qk_norm="head", rope_theta_local=10000.0,
+                           rope_global_every=2)
+    prompt = synthetic.prompt_tokens(w, 40, seed=46)
+    out = {}
+    weights = None
+    for mode in ("grid", "cluster"):
+        d = dec_mod.Decoder(w, weights=weights)
+        weights = d.weights
+        if not d.fused_available(mode):
+            assert mode == "cluster"
+            d.close()
+            continue
+        d.set_fused(mode)
+        out[mode] = gpu_greedy(d, prompt, 6)
+        d.close()
+    if "cluster" in out:
+        assert out["grid"][1] == out["cluster"][1]
+        np.testing.assert_allclose(out["grid"][0], out["cluster"][0], atol=2e-3, rtol=1e-4)
